@@ -1,0 +1,184 @@
+"""CPU oracle of the gradient-compression step -- TEST INFRASTRUCTURE ONLY.
+
+A ctypes binding of ``gcsgd_oracle.c``: a plain, single-threaded C statement
+of Deep Gradient Compression, AdaComp, the sparse decompress-and-average and
+the DCD-PSGD replica update.  Only the tests, the smoke check and the
+benchmark's CPU-baseline leg may import this package; the product path never
+does, and the two share no code.  Inputs come from
+``gradient_compression_sgd_gb300.workloads`` (random draws only).
+
+Parity pins: every function is checked in ``tests/test_oracle_*.py`` against
+brute force, closed forms, library routines and published known answers.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gcsgd_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libgcsgd_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-Wall"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no FMA contraction) into ``libgcsgd_oracle.so``."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = ctypes.CDLL(_LIB_PATH)
+            i64p = ctypes.POINTER(ctypes.c_int64)
+            vp = ctypes.c_void_p
+            L.oracle_dgc_k.restype = ctypes.c_int64
+            L.oracle_dgc_k.argtypes = [ctypes.c_double, ctypes.c_int64]
+            L.oracle_dgc_step.restype = ctypes.c_int
+            L.oracle_dgc_step.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, ctypes.c_double,
+                                          ctypes.c_float, ctypes.c_float, ctypes.c_int, vp, vp,
+                                          ctypes.c_int64, vp, vp]
+            L.oracle_adacomp_step.restype = ctypes.c_int
+            L.oracle_adacomp_step.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp, vp,
+                                              ctypes.c_int64, vp, vp, vp]
+            L.oracle_sparse_average.restype = ctypes.c_int
+            L.oracle_sparse_average.argtypes = [ctypes.c_int, vp, vp, ctypes.c_int64, vp, ctypes.c_int64, vp]
+            L.oracle_philox4x32_10.restype = None
+            L.oracle_philox4x32_10.argtypes = [vp, vp, vp]
+            L.oracle_keep_threshold.restype = ctypes.c_uint64
+            L.oracle_keep_threshold.argtypes = [ctypes.c_double]
+            for f in (L.oracle_dcd_step, L.oracle_dcd_step_replicas):
+                f.restype = ctypes.c_int
+                f.argtypes = [ctypes.c_int, ctypes.c_int64, vp, vp, vp, ctypes.c_float, ctypes.c_double,
+                              ctypes.c_uint64, ctypes.c_uint32]
+            _ = i64p
+            _lib = L
+    return _lib
+
+
+def _p(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _f32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise OracleError(f"{what} returned {rc}")
+
+
+def dgc_k(density: float, n: int) -> int:
+    return int(lib().oracle_dgc_k(float(density), int(n)))
+
+
+def dgc_step(offsets, grad, u, v, density, momentum, clip_thr=0.0, clip_nodes=1, cap=None):
+    """One DGC step of K learners. ``u``/``v`` ([K, N] float32) are updated in place.
+
+    Returns (idx [K, cap] uint32, val [K, cap] float32, counts [K, S] int64,
+    clip_scale [K] float32).
+    """
+    off = np.ascontiguousarray(offsets, dtype=np.int64)
+    S = len(off) - 1
+    grad = _f32(grad)
+    K = grad.shape[0]
+    assert u.dtype == np.float32 and v.dtype == np.float32 and u.flags["C_CONTIGUOUS"] and v.flags["C_CONTIGUOUS"]
+    if cap is None:
+        cap = max(1, sum(dgc_k(density, int(off[s + 1] - off[s])) for s in range(S)))
+    idx = np.zeros((K, cap), dtype=np.uint32)
+    val = np.zeros((K, cap), dtype=np.float32)
+    counts = np.zeros((K, S), dtype=np.int64)
+    cs = np.zeros(K, dtype=np.float32)
+    rc = lib().oracle_dgc_step(K, S, _p(off), _p(grad), _p(u), _p(v), float(density), float(momentum),
+                               float(clip_thr), int(clip_nodes), _p(idx), _p(val), int(cap), _p(counts), _p(cs))
+    _check(rc, "oracle_dgc_step")
+    return idx, val, counts, cs
+
+
+def adacomp_step(offsets, lt, dW, R, cap=None):
+    """One AdaComp step of K learners. ``R`` ([K, N] float32) is updated in place.
+
+    Returns (idx [K, cap], val [K, cap], counts [K, S], scales [K, S], totals [K]).
+    """
+    off = np.ascontiguousarray(offsets, dtype=np.int64)
+    S = len(off) - 1
+    lt = np.ascontiguousarray(lt, dtype=np.int32)
+    dW = _f32(dW)
+    K = dW.shape[0]
+    assert R.dtype == np.float32 and R.flags["C_CONTIGUOUS"]
+    if cap is None:
+        cap = max(1, int(off[-1]))
+    idx = np.zeros((K, cap), dtype=np.uint32)
+    val = np.zeros((K, cap), dtype=np.float32)
+    counts = np.zeros((K, S), dtype=np.int64)
+    scales = np.zeros((K, S), dtype=np.float32)
+    totals = np.zeros(K, dtype=np.int64)
+    rc = lib().oracle_adacomp_step(K, S, _p(off), _p(lt), _p(dW), _p(R), _p(idx), _p(val), int(cap),
+                                   _p(counts), _p(scales), _p(totals))
+    _check(rc, "oracle_adacomp_step")
+    return idx, val, counts, scales, totals
+
+
+def sparse_average(idx, val, counts, n):
+    """Dense [n] float32 average of K sparse lists (idx/val [K, cap], counts [K])."""
+    idx = np.ascontiguousarray(idx, dtype=np.uint32)
+    val = _f32(val)
+    counts = np.ascontiguousarray(counts, dtype=np.int64)
+    K, cap = idx.shape
+    out = np.zeros(int(n), dtype=np.float32)
+    rc = lib().oracle_sparse_average(K, _p(idx), _p(val), int(cap), _p(counts), int(n), _p(out))
+    _check(rc, "oracle_sparse_average")
+    return out
+
+
+def philox4x32_10(ctr, key) -> np.ndarray:
+    c = np.ascontiguousarray(ctr, dtype=np.uint32)
+    k = np.ascontiguousarray(key, dtype=np.uint32)
+    o = np.zeros(4, dtype=np.uint32)
+    lib().oracle_philox4x32_10(_p(c), _p(k), _p(o))
+    return o
+
+
+def keep_threshold(p: float) -> int:
+    return int(lib().oracle_keep_threshold(float(p)))
+
+
+def dcd_step(xhat, g, w, gamma, p, seed, t):
+    """One DCD-PSGD iteration; ``xhat`` ([n, d] float32) is updated in place."""
+    assert xhat.dtype == np.float32 and xhat.flags["C_CONTIGUOUS"]
+    g = _f32(g)
+    w3 = _f32(w)
+    n, d = xhat.shape
+    rc = lib().oracle_dcd_step(n, d, _p(w3), _p(xhat), _p(g), float(gamma), float(p), int(seed), int(t))
+    _check(rc, "oracle_dcd_step")
+    return xhat
+
+
+def dcd_step_replicas(rep, g, w, gamma, p, seed, t):
+    """DCD-PSGD iteration with explicit replicas ``rep`` [n, n, d] (node i's copy of node j)."""
+    assert rep.dtype == np.float32 and rep.flags["C_CONTIGUOUS"]
+    g = _f32(g)
+    w3 = _f32(w)
+    n, _, d = rep.shape
+    rc = lib().oracle_dcd_step_replicas(n, d, _p(w3), _p(rep), _p(g), float(gamma), float(p), int(seed), int(t))
+    _check(rc, "oracle_dcd_step_replicas")
+    return rep

@@ -1,0 +1,179 @@
+"""Pins of the oracle's sparse average and DCD-PSGD step (CPU only)."""
+import numpy as np
+import pytest
+
+import oracle
+from conftest import ulp32
+
+
+# ----------------------------------------------------------- sparse average
+
+def _lists(rng, K, n, cap, fill):
+    idx = np.zeros((K, cap), np.uint32)
+    val = np.zeros((K, cap), np.float32)
+    counts = np.zeros(K, np.int64)
+    for k in range(K):
+        c = int(rng.integers(0, fill + 1))
+        sel = np.sort(rng.choice(n, size=c, replace=False))
+        idx[k, :c] = sel
+        val[k, :c] = rng.standard_normal(c).astype(np.float32)
+        counts[k] = c
+    return idx, val, counts
+
+
+def test_single_list_is_decompression():
+    rng = np.random.default_rng(0)
+    idx, val, counts = _lists(rng, 1, 500, 64, 64)
+    out = oracle.sparse_average(idx, val, counts, 500)
+    want = np.zeros(500, np.float32)
+    want[idx[0, :counts[0]]] = val[0, :counts[0]]
+    np.testing.assert_array_equal(out, want)
+
+
+@pytest.mark.parametrize("K", [2, 3, 4, 8])
+def test_matches_numpy_ordered_scatter_add(K):
+    """numpy's unbuffered ufunc.at adds duplicates in the order given, so the
+    lists concatenated in learner order reproduce the K-ordered fp32 sum."""
+    rng = np.random.default_rng(K)
+    n, cap = 3000, 400
+    idx, val, counts = _lists(rng, K, n, cap, cap)
+    acc = np.zeros(n, np.float32)
+    for k in range(K):
+        np.add.at(acc, idx[k, :counts[k]].astype(np.int64), val[k, :counts[k]])
+    want = acc / np.float32(K)
+    out = oracle.sparse_average(idx, val, counts, n)
+    np.testing.assert_array_equal(out, want)
+    # mass and support
+    assert abs(out.astype(np.float64).sum() * K - sum(val[k, :counts[k]].astype(np.float64).sum() for k in range(K))) < 1e-4
+    support = set()
+    for k in range(K):
+        support |= set(idx[k, :counts[k]].tolist())
+    assert set(np.nonzero(out)[0].tolist()) <= support
+
+
+def test_index_out_of_range_is_rejected():
+    idx = np.array([[5]], np.uint32)
+    val = np.array([[1.0]], np.float32)
+    with pytest.raises(oracle.OracleError):
+        oracle.sparse_average(idx, val, np.array([1]), 5)
+
+
+# -------------------------------------------------------------------- Philox
+
+def test_philox_known_answers(golden):
+    ex = golden("philox4x32_10_kat.txt")
+    with open(__import__("os").path.join(__import__("conftest").GOLDEN, "philox4x32_10_kat.txt")) as f:
+        rows = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    assert len(rows) == 3
+    for r in rows:
+        w = [int(x, 16) for x in r]
+        assert list(oracle.philox4x32_10(w[0:4], w[4:6])) == w[6:10]
+    assert ex is not None
+
+
+def test_keep_threshold():
+    assert oracle.keep_threshold(0.01) == 42_949_673
+    assert oracle.keep_threshold(1.0) == 1 << 32
+    assert oracle.keep_threshold(0.5) == 1 << 31
+
+
+# ---------------------------------------------------------------------- DCD
+
+RING = (1.0 / 3.0, 1.0 / 3.0, 1.0 / 3.0)
+
+
+def _ring_matrix(n, w):
+    W = np.zeros((n, n))
+    for i in range(n):
+        W[i, (i - 1) % n] += w[0]
+        W[i, i] += w[1]
+        W[i, (i + 1) % n] += w[2]
+    return W
+
+
+def test_keep_all_is_dpsgd():
+    """p = 1 (C is the identity): the model becomes x_half = W x - gamma g, which
+    numpy computes in fp64 with the ring's mixing matrix."""
+    rng = np.random.default_rng(4)
+    n, d, gamma = 6, 1001, 0.1
+    w = np.float32(RING).astype(np.float64)
+    x = rng.standard_normal((n, d)).astype(np.float32)
+    g = rng.standard_normal((n, d)).astype(np.float32)
+    x_half = _ring_matrix(n, w) @ x.astype(np.float64) - np.float64(np.float32(gamma)) * g
+    got = oracle.dcd_step(x.copy(), g, RING, gamma, 1.0, 123, 0)
+    scale = np.maximum(np.abs(x_half), np.abs(x)).max()
+    assert np.abs(got - x_half).max() <= 8 * np.spacing(np.float32(scale))
+
+
+def test_single_node_is_sgd():
+    rng = np.random.default_rng(5)
+    d = 777
+    x = rng.standard_normal((1, d)).astype(np.float32)
+    g = rng.standard_normal((1, d)).astype(np.float32)
+    got = oracle.dcd_step(x.copy(), g, (0.0, 1.0, 0.0), 0.05, 1.0, 9, 3)
+    want = x[0].astype(np.float64) - np.float64(np.float32(0.05)) * g[0]
+    # a few fp32 roundings, each at most half an ulp of the largest operand
+    assert np.all(np.abs(got[0] - want) <= 2 * ulp32(np.maximum(np.abs(want), np.abs(x[0]))))
+
+
+def test_random_sparsification_mask_and_scale():
+    """From x = 0 on one node with W = (0, 1, 0), z = -gamma g and the new model
+    is exactly C(z): kept entries are z/p, the others 0.  The kept set is the
+    set of words of Philox(counter (e/4, node, t, 0), key seed) below
+    round(p 2^32); its size is within 5 sigma of the binomial mean, and alpha^2 =
+    ||z - C(z)||^2 / ||z||^2 is near its expectation (1 - p) / p."""
+    rng = np.random.default_rng(6)
+    d, p, t, seed = 200_000, 0.01, 7, 0xDEADBEEF12345678
+    g = rng.standard_normal((1, d)).astype(np.float32)
+    x = np.zeros((1, d), np.float32)
+    cz = oracle.dcd_step(x, g, (0.0, 1.0, 0.0), 0.1, p, seed, t)[0]
+    z = -(np.float32(0.1) * g[0])
+    kept = cz != 0
+    thr = oracle.keep_threshold(p)
+    key = [seed & 0xFFFFFFFF, seed >> 32]
+    for e in rng.choice(d, size=300, replace=False):
+        word = oracle.philox4x32_10([e // 4, 0, t, 0], key)[e % 4]
+        assert bool(word < thr) == bool(kept[e])
+    np.testing.assert_array_equal(cz[kept], z[kept] * np.float32(1.0 / p))
+    mean, sd = d * p, np.sqrt(d * p * (1 - p))
+    assert abs(kept.sum() - mean) < 5 * sd
+    alpha2 = np.sum((z.astype(np.float64) - cz) ** 2) / np.sum(z.astype(np.float64) ** 2)
+    assert abs(alpha2 - (1 - p) / p) < 0.15 * (1 - p) / p
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 5, 8])
+def test_replica_identity(n):
+    """Every node keeps its own copies of its neighbours' models and applies the
+    C(z_j) it receives; starting equal, those copies stay bit-identical to the
+    single shared array xhat (DCD-PSGD step 3)."""
+    rng = np.random.default_rng(n)
+    d, T, gamma, p, seed = 53, 6, 0.1, 0.3, 77
+    x0 = rng.standard_normal(d).astype(np.float32)
+    xhat = np.tile(x0, (n, 1)).copy()
+    rep = np.tile(x0, (n, n, 1)).copy()
+    for t in range(T):
+        g = rng.standard_normal((n, d)).astype(np.float32)
+        oracle.dcd_step(xhat, g, RING, gamma, p, seed, t)
+        oracle.dcd_step_replicas(rep, g, RING, gamma, p, seed, t)
+        for i in range(n):
+            for j in {i, (i - 1) % n, (i + 1) % n}:
+                np.testing.assert_array_equal(rep[i, j], xhat[j])
+
+
+def test_nodes_read_the_previous_iterate():
+    """The step is a function of the old models only: permuting the order in
+    which a reference computes nodes cannot matter, so node i's result equals a
+    one-node evaluation on the old neighbours."""
+    rng = np.random.default_rng(8)
+    n, d = 4, 64
+    x = rng.standard_normal((n, d)).astype(np.float32)
+    g = rng.standard_normal((n, d)).astype(np.float32)
+    full = oracle.dcd_step(x.copy(), g, RING, 0.1, 1.0, 1, 0)
+    for i in range(n):
+        l, r = (i - 1) % n, (i + 1) % n
+        acc = np.float32(RING[0]) * x[l]
+        acc = acc + np.float32(RING[1]) * x[i]
+        acc = acc + np.float32(RING[2]) * x[r]
+        xh = acc - np.float32(0.1) * g[i]
+        want = x[i] + (xh - x[i])
+        np.testing.assert_array_equal(full[i], want)

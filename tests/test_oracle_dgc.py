@@ -1,0 +1,213 @@
+"""Pins of the oracle's Deep Gradient Compression step (CPU only).
+
+Each test checks the oracle against something other than itself: a worked
+example, brute force over all subsets, closed forms of the momentum-corrected
+accumulation in exact rational arithmetic, and numpy's norm routine.
+"""
+import itertools
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from conftest import f32
+
+
+def _step(off, G, u, v, density, m, clip=0.0, nodes=1):
+    return oracle.dgc_step(off, G[None, :] if G.ndim == 1 else G, u, v, density, m, clip, nodes)
+
+
+def test_worked_example(golden):
+    ex = golden("dgc_worked_example.txt")
+    sizes = [int(x) for x in ex["sizes"]]
+    off = np.array([0, sizes[0], sizes[0] + sizes[1]], dtype=np.int64)
+    N = off[-1]
+    u = np.zeros((1, N), np.float32)
+    v = np.zeros((1, N), np.float32)
+    for t in (1, 2):
+        idx, val, counts, cs = oracle.dgc_step(off, f32(ex[f"grad{t}"])[None], u, v,
+                                               float(ex["density"][0]), float(ex["momentum"][0]))
+        tot = counts.sum()
+        assert list(idx[0, :tot]) == [int(x) for x in ex[f"sent{t}_idx"]]
+        np.testing.assert_array_equal(val[0, :tot], f32(ex[f"sent{t}_val"]))
+        np.testing.assert_array_equal(u[0], f32(ex[f"u{t}"]))
+        np.testing.assert_array_equal(v[0], f32(ex[f"v{t}"]))
+        assert cs[0] == 1.0
+
+
+def _brute_force_topk(vals, k):
+    """The unique k-subset S with |v_i| > |v_j|, or equal and i < j, for i in S, j not in S."""
+    n = len(vals)
+    found = []
+    for S in itertools.combinations(range(n), k):
+        Sset = set(S)
+        ok = all(abs(vals[i]) > abs(vals[j]) or (abs(vals[i]) == abs(vals[j]) and i < j)
+                 for i in Sset for j in range(n) if j not in Sset)
+        if ok:
+            found.append(S)
+    assert len(found) == 1, found
+    return list(found[0])
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_topk_matches_brute_force(seed):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(1, 10))
+    pool = np.array([0.0, -0.0, 0.5, -0.5, 1.0, -1.0, 2.0, -3.0, 3.0], np.float32)
+    G = rng.choice(pool, size=n).astype(np.float32)
+    density = float(rng.choice([0.1, 0.25, 0.5, 0.75, 1.0]))
+    k = oracle.dgc_k(density, n)
+    u = np.zeros((1, n), np.float32)
+    v = np.zeros((1, n), np.float32)
+    idx, val, counts, _ = _step(np.array([0, n], np.int64), G, u, v, density, 0.9)
+    assert counts[0, 0] == k
+    want = _brute_force_topk([float(x) for x in G], k)
+    assert list(idx[0, :k]) == want
+    # from a zero state the accumulated velocity equals the gradient
+    np.testing.assert_array_equal(val[0, :k], G[want])
+    # momentum factor masking: zero exactly where sent, untouched elsewhere
+    rest = [i for i in range(n) if i not in want]
+    assert np.all(u[0, want] == 0) and np.all(v[0, want] == 0)
+    np.testing.assert_array_equal(u[0, rest], G[rest])
+    np.testing.assert_array_equal(v[0, rest], G[rest])
+
+
+def test_k_rule():
+    # k = ceil(density * n) in fp64, at least 1, at most n
+    assert oracle.dgc_k(0.001, 1_048_576) == 1049
+    assert oracle.dgc_k(0.001, 1000) == 1
+    assert oracle.dgc_k(0.001, 64) == 1
+    assert oracle.dgc_k(0.001, 2_359_296) == 2360
+    assert oracle.dgc_k(1.0, 7) == 7
+    assert oracle.dgc_k(0.5, 0) == 0
+
+
+def test_momentum_correction_closed_form():
+    """With m = 1/2 and small integer gradients every fp32 operation is exact, so
+    an entry that is never sent must follow the closed form of the corrected
+    accumulation: u_T = sum_j m^(T-j) G_j and v_T = sum_j G_j (1 - m^(T-j+1)) / (1 - m).
+    Entry 0 carries a huge gradient and is sent every step (k = 1), so it must
+    restart from zero each step: sent_t = G_t at entry 0."""
+    rng = np.random.default_rng(7)
+    n, T, m = 16, 6, Fraction(1, 2)
+    Gs = rng.integers(-8, 9, size=(T, n)).astype(np.float32)
+    Gs[:, 0] = 1e6 * np.array([1, -1, 1, -1, 1, -1])[:T]
+    u = np.zeros((1, n), np.float32)
+    v = np.zeros((1, n), np.float32)
+    off = np.array([0, n], np.int64)
+    for t in range(T):
+        idx, val, counts, _ = _step(off, Gs[t], u, v, 1.0 / n, 0.5)
+        assert counts[0, 0] == 1 and idx[0, 0] == 0 and val[0, 0] == Gs[t, 0]
+    for i in range(1, n):
+        uT = sum(m ** (T - 1 - j) * Fraction(float(Gs[j, i])) for j in range(T))
+        vT = sum(Fraction(float(Gs[j, i])) * (1 - m ** (T - j)) / (1 - m) for j in range(T))
+        assert Fraction(float(u[0, i])) == uT
+        assert Fraction(float(v[0, i])) == vT
+
+
+def test_density_one_sends_the_gradient():
+    """Sending everything resets u and v each step, so what is sent is G itself."""
+    rng = np.random.default_rng(3)
+    K, n = 2, 33
+    off = np.array([0, 5, 5, 33], np.int64)  # includes an empty tensor
+    u = np.zeros((K, n), np.float32)
+    v = np.zeros((K, n), np.float32)
+    for t in range(3):
+        G = rng.standard_normal((K, n)).astype(np.float32)
+        idx, val, counts, _ = oracle.dgc_step(off, G, u, v, 1.0, 0.9)
+        assert list(counts[0]) == [5, 0, 28]
+        for k in range(K):
+            assert list(idx[k]) == list(range(n))
+            np.testing.assert_array_equal(val[k], G[k])
+        assert not u.any() and not v.any()
+
+
+def test_zero_momentum_is_plain_residual_accumulation():
+    """m = 0: v accumulates G and sent + residual conserves the total exactly
+    (integer-valued gradients keep fp32 exact)."""
+    rng = np.random.default_rng(11)
+    n, T = 50, 8
+    off = np.array([0, n], np.int64)
+    u = np.zeros((1, n), np.float32)
+    v = np.zeros((1, n), np.float32)
+    total_sent = np.zeros(n, np.float64)
+    total_grad = np.zeros(n, np.float64)
+    for _ in range(T):
+        G = rng.integers(-4, 5, size=n).astype(np.float32)
+        idx, val, counts, _ = _step(off, G, u, v, 0.1, 0.0)
+        total_sent[idx[0, :counts.sum()]] += val[0, :counts.sum()]
+        total_grad += G
+        np.testing.assert_array_equal(u[0][v[0] != 0], G[v[0] != 0])
+    np.testing.assert_array_equal(total_sent + v[0], total_grad)
+
+
+@pytest.mark.parametrize("nodes", [1, 4])
+def test_local_gradient_clipping(nodes):
+    """The scale is thr_k / ||G|| with thr_k = thr / sqrt(N) (Appendix C), from
+    numpy's fp64 norm; it depends on G only (clipping happens before the
+    gradient joins the accumulation), and the clipped gradient's norm is
+    within fp32 rounding of thr_k."""
+    rng = np.random.default_rng(nodes)
+    n = 4096
+    G = (rng.standard_normal(n) * 0.05).astype(np.float32)  # ||G|| ~ 3.2
+    thr = 1.0
+    thr_k = thr / np.sqrt(nodes)
+    norm = np.linalg.norm(G.astype(np.float64))
+    assert norm > thr_k
+    off = np.array([0, n], np.int64)
+    u = np.zeros((1, n), np.float32)
+    v = np.zeros((1, n), np.float32)
+    _, val, _, cs = _step(off, G, u, v, 1.0, 0.0, clip=thr, nodes=nodes)
+    assert cs[0] == np.float32(thr_k / norm)
+    Gc = G * cs[0]
+    np.testing.assert_array_equal(val[0], Gc)  # density 1, zero state: what is sent is c*G
+    assert np.linalg.norm(Gc.astype(np.float64)) <= thr_k * (1 + 1e-6)
+    # with a non-zero state the scale is unchanged: it is a property of G alone
+    u2 = rng.standard_normal((1, n)).astype(np.float32)
+    v2 = rng.standard_normal((1, n)).astype(np.float32)
+    _, val, _, cs2 = _step(off, G, u2, v2, 1.0, 0.9, clip=thr, nodes=nodes)
+    assert cs2[0] == cs[0]
+    # below the threshold nothing is scaled
+    small = G * np.float32(0.01)
+    _, val, _, cs3 = _step(off, small, np.zeros((1, n), np.float32), np.zeros((1, n), np.float32), 1.0, 0.0,
+                           clip=thr, nodes=nodes)
+    assert cs3[0] == 1.0
+    np.testing.assert_array_equal(val[0], small)
+
+
+def test_multi_learner_independence():
+    """Learners share nothing: running K together equals running each alone."""
+    rng = np.random.default_rng(5)
+    off = np.array([0, 100, 130, 400], np.int64)
+    K, n = 3, 400
+    G = rng.standard_normal((K, n)).astype(np.float32)
+    u = rng.standard_normal((K, n)).astype(np.float32)
+    v = rng.standard_normal((K, n)).astype(np.float32)
+    u0, v0 = u.copy(), v.copy()
+    idx, val, counts, _ = oracle.dgc_step(off, G, u, v, 0.05, 0.9, 1.0, 2)
+    for k in range(K):
+        uk, vk = u0[k:k + 1].copy(), v0[k:k + 1].copy()
+        i1, v1, c1, _ = oracle.dgc_step(off, G[k:k + 1], uk, vk, 0.05, 0.9, 1.0, 2)
+        np.testing.assert_array_equal(i1[0], idx[k])
+        np.testing.assert_array_equal(v1[0], val[k])
+        np.testing.assert_array_equal(uk[0], u[k])
+        np.testing.assert_array_equal(vk[0], v[k])
+
+
+def test_sent_plus_residual_is_accumulation():
+    """v_acc = v_new + sent, bit for bit, where v_acc is observed by running
+    the same step with nothing extra sent (density small) on a copy."""
+    rng = np.random.default_rng(9)
+    off = np.array([0, 300, 1000], np.int64)
+    n = 1000
+    G = rng.standard_normal((1, n)).astype(np.float32)
+    u = rng.standard_normal((1, n)).astype(np.float32)
+    v = rng.standard_normal((1, n)).astype(np.float32)
+    # v_acc from density 1 (everything sent, so the sent values are v_acc)
+    _, vacc, _, _ = oracle.dgc_step(off, G, u.copy(), v.copy(), 1.0, 0.9)
+    idx, val, counts, _ = oracle.dgc_step(off, G, u, v, 0.02, 0.9)
+    tot = counts.sum()
+    recon = v[0].copy()
+    recon[idx[0, :tot]] += val[0, :tot]  # v is exactly 0 there
+    np.testing.assert_array_equal(recon, vacc[0])
