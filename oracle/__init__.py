@@ -60,6 +60,9 @@ def lib():
             L.oracle_philox4x32_10.argtypes = [vp, vp, vp]
             L.oracle_keep_threshold.restype = ctypes.c_uint64
             L.oracle_keep_threshold.argtypes = [ctypes.c_double]
+            L.oracle_dcd_step_window.restype = ctypes.c_int
+            L.oracle_dcd_step_window.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, vp, vp, vp,
+                                                 ctypes.c_float, ctypes.c_double, ctypes.c_uint64, ctypes.c_uint32]
             for f in (L.oracle_dcd_step, L.oracle_dcd_step_replicas):
                 f.restype = ctypes.c_int
                 f.argtypes = [ctypes.c_int, ctypes.c_int64, vp, vp, vp, ctypes.c_float, ctypes.c_double,
@@ -170,6 +173,18 @@ def dcd_step(xhat, g, w, gamma, p, seed, t):
     n, d = xhat.shape
     rc = lib().oracle_dcd_step(n, d, _p(w3), _p(xhat), _p(g), float(gamma), float(p), int(seed), int(t))
     _check(rc, "oracle_dcd_step")
+    return xhat
+
+
+def dcd_step_window(xhat, g, w, gamma, p, seed, t, e_base):
+    """DCD-PSGD iteration on the column window [e_base, e_base + d) of a longer model."""
+    assert xhat.dtype == np.float32 and xhat.flags["C_CONTIGUOUS"]
+    g = _f32(g)
+    w3 = _f32(w)
+    n, d = xhat.shape
+    rc = lib().oracle_dcd_step_window(n, d, int(e_base), _p(w3), _p(xhat), _p(g), float(gamma), float(p), int(seed),
+                                      int(t))
+    _check(rc, "oracle_dcd_step_window")
     return xhat
 
 

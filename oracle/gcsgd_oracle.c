@@ -195,8 +195,9 @@ int oracle_dgc_step(int K, int S, const int64_t* seg_off,
  * dW, R : [K][N] fp32 (R updated in place); lt : [S] bin lengths >= 1.
  * out_idx/out_val : [K][cap], learner k's tensors one after another, each in
  * ascending index order.  counts : [K][S].  scales : [K][S].
- * totals : [K] entries of each learner (reported even when they exceed cap,
- * in which case the call returns ORACLE_ECAP after filling cap entries).
+ * totals : [K] entries of each learner, reported even when they exceed cap;
+ * such a learner sends nothing (its residue becomes G) and the call returns
+ * ORACLE_ECAP.
  */
 int oracle_adacomp_step(int K, int S, const int64_t* seg_off, const int32_t* lt,
                         const float* dW, float* R,
@@ -205,18 +206,17 @@ int oracle_adacomp_step(int K, int S, const int64_t* seg_off, const int32_t* lt,
     if (K < 1 || S < 1) return ORACLE_EINVAL;
     for (int s = 0; s < S; ++s) if (lt[s] < 1) return ORACLE_EINVAL;
     const int64_t N = seg_off[S];
-    int64_t max_len = 1;
-    for (int s = 0; s < S; ++s)
-        if (seg_off[s + 1] - seg_off[s] > max_len) max_len = seg_off[s + 1] - seg_off[s];
-    float* G = (float*)malloc(sizeof(float) * (size_t)max_len);
-    float* bmax = (float*)malloc(sizeof(float) * (size_t)max_len);
-    if (!G || !bmax) { free(G); free(bmax); return ORACLE_ENOMEM; }
+    float* G = (float*)malloc(sizeof(float) * (size_t)(N > 0 ? N : 1));
+    float* Q = (float*)malloc(sizeof(float) * (size_t)(N > 0 ? N : 1));
+    unsigned char* sel = (unsigned char*)malloc((size_t)(N > 0 ? N : 1));
+    float* bmax = (float*)malloc(sizeof(float) * (size_t)(N > 0 ? N : 1));
+    if (!G || !Q || !sel || !bmax) { free(G); free(Q); free(sel); free(bmax); return ORACLE_ENOMEM; }
     int rc = ORACLE_OK;
 
     for (int k = 0; k < K; ++k) {
         const float* dWk = dW + (int64_t)k * N;
         float* Rk = R + (int64_t)k * N;
-        int64_t pos = 0;
+        int64_t total = 0;
         for (int s = 0; s < S; ++s) {
             const int64_t off = seg_off[s];
             const int64_t n = seg_off[s + 1] - off;
@@ -229,45 +229,53 @@ int oracle_adacomp_step(int K, int S, const int64_t* seg_off, const int32_t* lt,
                 continue;
             }
             /* 1. G = R + dW */
-            for (int64_t i = 0; i < n; ++i) G[i] = Rk[off + i] + dWk[off + i];
+            for (int64_t i = 0; i < n; ++i) G[off + i] = Rk[off + i] + dWk[off + i];
             /* 2. per-bin maximum of |G|;  4. mean of the maxima */
             csum_t acc = {0.0, 0.0};
             for (int64_t b = 0; b < nb; ++b) {
                 int64_t lo = b * L, hi = lo + L < n ? lo + L : n;
                 float m = 0.0f;
                 for (int64_t i = lo; i < hi; ++i) {
-                    float a = fabsf(G[i]);
+                    float a = fabsf(G[off + i]);
                     if (a > m) m = a;
                 }
                 bmax[b] = m;
                 csum_add(&acc, (double)m);
             }
             const float scale = (float)(csum_value(&acc) / (double)nb);
-            /* 3. select |G + dW| >= bin max;  5. quantise and keep the residue */
+            /* 3. select |G + dW| >= bin max;  5. the value sent */
             for (int64_t i = 0; i < n; ++i) {
                 const float m = bmax[i / L];
-                const float h = G[i] + dWk[off + i];
-                const int sel = (fabsf(h) >= m) && (m > 0.0f) && (G[i] != 0.0f);
-                if (sel) {
-                    const float q = G[i] > 0.0f ? scale : -scale;
-                    if (pos < cap) {
-                        out_idx[(int64_t)k * cap + pos] = (uint32_t)(off + i);
-                        out_val[(int64_t)k * cap + pos] = q;
-                    }
-                    ++pos;
-                    ++sent;
-                    Rk[off + i] = G[i] - q;
-                } else {
-                    Rk[off + i] = G[i];
-                }
+                const float h = G[off + i] + dWk[off + i];
+                sel[off + i] = (fabsf(h) >= m) && (m > 0.0f) && (G[off + i] != 0.0f);
+                Q[off + i] = G[off + i] > 0.0f ? scale : -scale;
+                sent += sel[off + i];
             }
             counts[(int64_t)k * S + s] = sent;
             scales[(int64_t)k * S + s] = scale;
+            total += sent;
         }
-        totals[k] = pos;
-        if (pos > cap) rc = ORACLE_ECAP;
+        totals[k] = total;
+        /* Reading (capacity is not on the page): a learner whose message does
+         * not fit in cap entries sends nothing this step; its residue keeps
+         * all of G, so no gradient mass is lost. */
+        const int fits = total <= cap;
+        if (!fits) rc = ORACLE_ECAP;
+        int64_t pos = 0;
+        for (int64_t i = 0; i < N; ++i) {
+            if (fits && sel[i]) {
+                out_idx[(int64_t)k * cap + pos] = (uint32_t)i;
+                out_val[(int64_t)k * cap + pos] = Q[i];
+                ++pos;
+                Rk[i] = G[i] - Q[i];
+            } else {
+                Rk[i] = G[i];
+            }
+        }
     }
     free(G);
+    free(Q);
+    free(sel);
     free(bmax);
     return rc;
 }
@@ -369,10 +377,15 @@ static float dcd_compress(float z, uint32_t word, uint64_t thr, float inv_p) {
  * iteration t.  C is random sparsification ("... any other operators", the
  * paragraph that defines alpha): keep an entry with probability p, scaled by
  * 1/p; the keep draw is Philox4x32-10 word (seed, node, t, e).
+ *
+ * oracle_dcd_step_window computes the columns [e_base, e_base + d) of a
+ * longer model (the same arithmetic; e_base only enters the counter), so a
+ * sampled window of a full-size run can be checked; xhat and g are then the
+ * [n][d] window.
  */
-int oracle_dcd_step(int n, int64_t d, const float w[3], float* xhat, const float* g,
-                    float gamma, double p, uint64_t seed, uint32_t t) {
-    if (n < 1 || d < 0 || !(p > 0.0 && p <= 1.0)) return ORACLE_EINVAL;
+int oracle_dcd_step_window(int n, int64_t d, int64_t e_base, const float w[3], float* xhat, const float* g,
+                           float gamma, double p, uint64_t seed, uint32_t t) {
+    if (n < 1 || d < 0 || e_base < 0 || !(p > 0.0 && p <= 1.0)) return ORACLE_EINVAL;
     float* xn = (float*)malloc(sizeof(float) * (size_t)(n * d > 0 ? n * d : 1));
     if (!xn) return ORACLE_ENOMEM;
     const uint64_t thr = oracle_keep_threshold(p);
@@ -389,13 +402,19 @@ int oracle_dcd_step(int n, int64_t d, const float w[3], float* xhat, const float
             acc = acc + w[2] * xr[e];
             const float xh = acc - gamma * gi[e];
             const float z = xh - xi[e];
-            const float cz = dcd_compress(z, dcd_word(seed, (uint32_t)i, t, (uint64_t)e), thr, inv_p);
+            const uint32_t word = dcd_word(seed, (uint32_t)i, t, (uint64_t)(e_base + e));
+            const float cz = dcd_compress(z, word, thr, inv_p);
             xn[(int64_t)i * d + e] = xi[e] + cz;
         }
     }
     memcpy(xhat, xn, sizeof(float) * (size_t)(n * d));
     free(xn);
     return ORACLE_OK;
+}
+
+int oracle_dcd_step(int n, int64_t d, const float w[3], float* xhat, const float* g,
+                    float gamma, double p, uint64_t seed, uint32_t t) {
+    return oracle_dcd_step_window(n, d, 0, w, xhat, g, gamma, p, seed, t);
 }
 
 /*

@@ -177,3 +177,15 @@ def test_nodes_read_the_previous_iterate():
         xh = acc - np.float32(0.1) * g[i]
         want = x[i] + (xh - x[i])
         np.testing.assert_array_equal(full[i], want)
+
+
+def test_window_matches_full_step():
+    """A column window computed on its own equals the same columns of the full step."""
+    rng = np.random.default_rng(12)
+    n, d = 5, 2000
+    x = rng.standard_normal((n, d)).astype(np.float32)
+    g = rng.standard_normal((n, d)).astype(np.float32)
+    full = oracle.dcd_step(x.copy(), g, RING, 0.1, 0.2, 99, 4)
+    for e0, e1 in [(0, 7), (13, 500), (1999, 2000), (1024, 2000)]:
+        win = oracle.dcd_step_window(np.ascontiguousarray(x[:, e0:e1]), g[:, e0:e1], RING, 0.1, 0.2, 99, 4, e0)
+        np.testing.assert_array_equal(win, full[:, e0:e1])
