@@ -1,0 +1,372 @@
+#!/usr/bin/env python
+"""Gradient GB/s through one compress + average step on GB300.
+
+Workload (default): the ResNet-50 parameter layout (161 tensors, 25,557,032
+fp32 values) for K = 4 simulated learners; one step is Deep Gradient
+Compression of all four learners' gradients (density 0.001 per tensor,
+momentum 0.9, exact top-k, masking) followed by the sparse average of their
+four messages into a dense gradient.  Inputs are seeded synthetic gradients
+already resident in HBM; three distinct gradient sets rotate, 409 MB each,
+so every step streams inputs far larger than the 129 MB L2.
+
+One JSON line on rank 0: whole-job gradient GB/s (value), the same metric end
+to end with host buffers (e2e), the roofline of the dominant kernel, the CPU
+oracle's figure on a bounded sample (cpu_baseline), clocks and launches.
+``--impl reference`` times the CPU oracle itself (the only other
+implementation of this path) on the same workload.
+
+Multi-GPU (torchrun): every rank runs its own K learners (independent
+problems, no collective in the data path); value = all ranks' gradient bytes
+over the slowest rank's time (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "gradient GB/s through compress+average step; % of GB300 HBM roofline"
+FALLBACK_HBM_GBS = 6800.0
+DGC_BYTES_PER_ELEM = 20  # read g, u, v; write u, v
+N_SETS = 3
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gcsgd", choices=["gcsgd", "reference"])
+    ap.add_argument("--config", type=int, default=2, choices=[2, 4],
+                    help="2: ResNet-50 layout K=4 (the metric's workload); 4: GRU layout K=8")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        for r in rows:
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                                 r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# --------------------------------------------------------- CPU oracle sample
+
+def oracle_sample(w, learner_grad: np.ndarray, target_s: float, min_steps: int = 1):
+    """Time the oracle's DGC step + average on every 4th tensor of learner 0.
+
+    Returns (gradient bytes processed, seconds, description)."""
+    import oracle
+    sizes = np.asarray(w.sizes)
+    pick = np.arange(0, len(sizes), 4)
+    off = w.offsets
+    g = np.concatenate([learner_grad[off[s]:off[s + 1]] for s in pick])[None, :]
+    sub = np.concatenate([[0], np.cumsum(sizes[pick])]).astype(np.int64)
+    n = int(sub[-1])
+    u = np.zeros((1, n), np.float32)
+    v = np.zeros((1, n), np.float32)
+    oracle.lib()
+    t0 = time.perf_counter()
+    steps = 0
+    while steps < min_steps or time.perf_counter() - t0 < target_s:
+        idx, val, counts, _ = oracle.dgc_step(sub, g, u, v, w.density, w.momentum)
+        oracle.sparse_average(idx, val, counts.sum(axis=1), n)
+        steps += 1
+    dt = time.perf_counter() - t0
+    desc = (f"oracle DGC step + sparse average of learner 0 on every 4th tensor of the layout "
+            f"({len(pick)} tensors, {n} values), {steps} step(s), single thread")
+    return 4.0 * n * steps, dt, desc
+
+
+# ------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import torch  # noqa: F401  (seeded generator)
+    from gradient_compression_sgd_gb300 import workloads as wl
+    w = wl.workload(args.config)
+    grad0 = wl.gradient(w, 0, 0).numpy()
+    for _ in range(args.warmup):
+        oracle_sample(w, grad0, 0.0)
+    times, nbytes = [], 0.0
+    desc = ""
+    for _ in range(args.steps):
+        b, dt, desc = oracle_sample(w, grad0, 0.0)
+        times.append(dt)
+        nbytes = b
+    total = sum(times)
+    value = nbytes * len(times) / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0, sigma^2) per tensor, sigma log-uniform in [1e-5, 1e-2])",
+        "config": config_dict(w, sample=desc),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def config_dict(w, **extra):
+    d = {"workload": w.name, "learners": w.learners, "elements_per_learner": w.n, "segments": len(w.sizes),
+         "density": w.density, "momentum": w.momentum, "step": "dgc_compress(K learners) + sparse_average",
+         "l2": "inputs larger than L2: 3 rotating gradient sets of K*N*4 bytes each"}
+    d.update(extra)
+    return d
+
+
+def kernel_source_sha() -> str:
+    with open(os.path.join(ROOT, "gradient_compression_sgd_gb300", "csrc", "dgc.cu"), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per dgc_update launch from the committed ncu summary, if it
+    was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"dgc_update_{workload}.md")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and line.startswith("- "):
+                    k, v = line[2:].split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha") != kernel_source_sha():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# -------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import gradient_compression_sgd_gb300 as gc
+    from gradient_compression_sgd_gb300 import build as gbuild
+    from gradient_compression_sgd_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0 or world == 1:
+        gbuild.build()
+    if world > 1:
+        dist.barrier()
+    gc.lib()
+
+    w = wl.workload(args.config)
+    K, N = w.learners, w.n
+    dev = torch.device("cuda", local)
+    grads = [wl.gradients(w, t, device=dev) for t in range(N_SETS)]
+    dgc = gc.DGC(w.offsets, K, w.density, w.momentum, device=dev)
+    u = torch.zeros((K, N), device=dev)
+    v = torch.zeros((K, N), device=dev)
+    avg = torch.empty(N, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        out, totals = dgc(grads[i % N_SETS], u, v)
+        gc.sparse_average(out, totals, N, avg)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+
+    clocks = ClockSampler(local)
+    gc.launch_count_reset()
+    gc.trace_enable(True)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    gc.trace_enable(False)
+    launches = gc.launch_count()
+    trace = gc.trace_read()
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    grad_bytes = 4.0 * K * N
+    value = world * grad_bytes / (ms * 1e-3) / 1e9
+
+    # end to end through the public API: pinned host gradient in, dense average out
+    host = [g.cpu().pin_memory() for g in grads[:2]]
+    gdev = torch.empty((K, N), device=dev)
+    avg_host = torch.empty(N, pin_memory=True)
+    u2 = torch.zeros((K, N), device=dev)
+    v2 = torch.zeros((K, N), device=dev)
+
+    def e2e_step(i):
+        gdev.copy_(host[i % 2], non_blocking=True)
+        out, totals = dgc(gdev, u2, v2)
+        gc.sparse_average(out, totals, N, avg)
+        avg_host.copy_(avg, non_blocking=True)
+
+    for i in range(max(1, args.warmup)):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(args.steps, 20))
+    f0.record(stream)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = f0.elapsed_time(f1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    e2e = world * grad_bytes / (ms_e2e * 1e-3) / 1e9
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+
+    hbm, peak_kind = peaks()
+    n_up, ms_up = trace.get("dgc_update", (0, 0.0))
+    upd_ms = ms_up / max(n_up, 1)
+    upd_bytes = float(DGC_BYTES_PER_ELEM) * K * N
+    achieved = upd_bytes / (upd_ms * 1e-3) / 1e9 if upd_ms > 0 else None
+    traffic = profiled_traffic(w.name)
+    sent = int(dgc.totals.sum().item())
+    step_bytes = DGC_BYTES_PER_ELEM * K * N + 8.0 * sent + 4.0 * N + 8.0 * sent
+    kernels = {name: {"launches": c, "ms_per_launch": t / max(c, 1), "share": t / max(sum(x[1] for x in trace.values()), 1e-9)}
+               for name, (c, t) in trace.items()}
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        b, dt, desc = oracle_sample(w, grads[0][0].cpu().numpy(), args.cpu_seconds)
+        cpu = {"value": b / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0, sigma^2) per tensor, sigma log-uniform in [1e-5, 1e-2])",
+        "config": config_dict(w),
+        "elements_per_s": world * K * N / (ms * 1e-3),
+        "step_roofline_frac": step_bytes / (ms * 1e-3) / 1e9 / hbm,
+        "roofline": {"bound": "hbm", "kernel": "dgc_update", "achieved": achieved, "peak": hbm,
+                     "peak_kind": f"{peak_kind} (copy)", "unit": "GB/s",
+                     "frac": (achieved / hbm) if achieved else None,
+                     "algorithmic_bytes_per_launch": upd_bytes, "traffic": traffic,
+                     "frac_of_nominal_8tbs": (achieved / 8000.0) if achieved else None},
+        "kernels": kernels,
+        "e2e": {"value": e2e, "unit": "GB/s", "ms_per_step": ms_e2e, "h2d_bytes_per_step": int(grad_bytes),
+                "d2h_bytes_per_step": int(4 * N)},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

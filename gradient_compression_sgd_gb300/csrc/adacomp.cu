@@ -1,0 +1,580 @@
+// adacomp.cu -- AdaComp for K learners.
+//
+// "AdaComp : Adaptive Residual Gradient Compression for Data-Parallel
+// Distributed Training", Proposed method: G = R + dW per layer; the layer is
+// cut into bins of L_T values and each bin's max |G| is found; entries with
+// |G + dW| >= the bin max are selected (O(N), no global sort); one scale per
+// layer, the mean of the bin maxima; a selected entry is sent as
+// sign(G) * scale and the residue keeps what was not sent.
+//
+// Launch sequence (caller's stream, no host sync):
+//   ada_plan     one CTA: per-segment plan (bins, tiles), zeroes counters
+//   [ada_bigmax] only for segments with L_T > 4096: bin maxima via atomics
+//   ada_bins     the bandwidth-bound pass: 128-bit loads of R and dW, G = R+dW,
+//                bin maxima in shared memory (warp-aggregated atomicMax on the
+//                |G| bit patterns), selection, R <- G stored once, ordered
+//                compaction of the selected (index, G) into the learner's
+//                pool, and a compensated fp64 sum of the tile's bin maxima
+//   ada_scan     one CTA per (learner, segment): prefix of the tile counts in
+//                index order, the segment's count and its scale
+//   ada_emit     one warp per tile: writes (index, sign(G)*scale) at its
+//                ordered slot and fixes the residue R = G - sign(G)*scale.
+// Tiles hold whole bins (bins of L_T <= 4096 never straddle tiles), so a
+// bin's maximum is final inside one CTA and the first pass is single-read.
+#include <math.h>
+
+#include "common.cuh"
+
+namespace gcsgd {
+namespace ada {
+
+constexpr int NT = 256;
+constexpr uint32_t kTileMax = 4096;
+
+enum : uint32_t { kModeEmpty = 0, kModeSmall = 1, kModeBig = 2 };
+
+struct SegPlan {
+    uint32_t off, n, L, mode;
+    uint32_t nbins;     // ceil(n / L)
+    uint32_t tile_len;  // elements per tile (whole bins in small mode)
+    uint32_t bpt;       // bins per tile (small mode)
+    uint32_t ntiles;
+    uint32_t tile_off;  // first tile within a learner
+    uint32_t big_off;   // first big-bin slot within a learner (big mode)
+    float invL;         // fp32 1/L: bin = floor((e + 0.5) * invL) is exact for e < 4096
+    uint32_t pad;
+};
+
+template <int MAXS>
+struct SegTable {
+    uint32_t off[MAXS + 1];
+    uint32_t L[MAXS];
+};
+
+__host__ __device__ inline uint32_t gcd4(uint32_t L) { return (L & 3) == 0 ? 4 : ((L & 1) == 0 ? 2 : 1); }
+
+__host__ __device__ inline void seg_fields(uint32_t n, uint32_t L, SegPlan* p) {
+    p->n = n;
+    p->L = L;
+    p->nbins = n ? (uint32_t)(((uint64_t)n + L - 1) / L) : 0;
+    p->bpt = 0;
+    p->invL = 1.0f / (float)L;
+    p->pad = 0;
+    if (n == 0) {
+        p->mode = kModeEmpty;
+        p->tile_len = 0;
+        p->ntiles = 0;
+    } else if (L <= kTileMax) {
+        p->mode = kModeSmall;
+        uint32_t bpt = kTileMax / L;
+        const uint32_t g = 4 / gcd4(L);  // keep tiles 16-byte aligned where possible
+        if (bpt >= g) bpt -= bpt % g;
+        p->bpt = bpt;
+        p->tile_len = bpt * L;
+        p->ntiles = (p->nbins + bpt - 1) / bpt;
+    } else {
+        p->mode = kModeBig;
+        p->tile_len = kTileMax;
+        p->ntiles = (n + kTileMax - 1) / kTileMax;
+    }
+}
+
+struct HostPlan {
+    uint64_t tiles_per_learner;
+    uint64_t big_per_learner;
+};
+
+void host_plan(const int64_t* off, const int32_t* lt, int S, HostPlan* hp) {
+    hp->tiles_per_learner = 0;
+    hp->big_per_learner = 0;
+    for (int s = 0; s < S; ++s) {
+        SegPlan p;
+        seg_fields((uint32_t)(off[s + 1] - off[s]), (uint32_t)lt[s], &p);
+        hp->tiles_per_learner += p.ntiles;
+        if (p.mode == kModeBig) hp->big_per_learner += p.nbins;
+    }
+}
+
+struct Workspace {
+    SegPlan* plan;
+    uint32_t* pool_cnt;
+    uint2* tile_tab;     // (pool slot, count)
+    double2* tile_sum;   // compensated sum of the tile's bin maxima
+    uint32_t* tile_rel;  // first output slot of the tile within its segment
+    uint32_t* big;       // bin maxima (|G| bits) of big-mode segments
+    uint2* pool;         // (index within the learner, G bits)
+};
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+size_t layout(int S, int K, int64_t cap, const HostPlan& hp, void* base, Workspace* w) {
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align256(o + bytes);
+        return at;
+    };
+    const uint64_t T = (uint64_t)K * hp.tiles_per_learner;
+    const size_t o_plan = take(sizeof(SegPlan) * (size_t)S);
+    const size_t o_cnt = take(sizeof(uint32_t) * (size_t)K);
+    const size_t o_tt = take(sizeof(uint2) * T);
+    const size_t o_ts = take(sizeof(double2) * T);
+    const size_t o_tr = take(sizeof(uint32_t) * T);
+    const size_t o_big = take(sizeof(uint32_t) * (size_t)K * hp.big_per_learner);
+    const size_t o_pool = take(sizeof(uint2) * (size_t)K * (size_t)cap);
+    if (w) {
+        char* b = (char*)base;
+        w->plan = (SegPlan*)(b + o_plan);
+        w->pool_cnt = (uint32_t*)(b + o_cnt);
+        w->tile_tab = (uint2*)(b + o_tt);
+        w->tile_sum = (double2*)(b + o_ts);
+        w->tile_rel = (uint32_t*)(b + o_tr);
+        w->big = (uint32_t*)(b + o_big);
+        w->pool = (uint2*)(b + o_pool);
+    }
+    return o;
+}
+
+// Neumaier step: (s, c) += x.
+__device__ __forceinline__ void csum_add(double& s, double& c, double x) {
+    const double t = __dadd_rn(s, x);
+    c = __dadd_rn(c, fabs(s) >= fabs(x) ? __dadd_rn(__dsub_rn(s, t), x) : __dadd_rn(__dsub_rn(x, t), s));
+    s = t;
+}
+
+template <int MAXS>
+__global__ void __launch_bounds__(1024) ada_plan(SegTable<MAXS> st, int S, int K, uint64_t big_per_learner,
+                                                 SegPlan* __restrict__ plan, uint32_t* __restrict__ pool_cnt,
+                                                 uint32_t* __restrict__ big) {
+    __shared__ uint64_t scan[1024 / 32 + 1];
+    __shared__ uint64_t carry[2];
+    if (threadIdx.x < 2) carry[threadIdx.x] = 0;
+    __syncthreads();
+    for (int base = 0; base < S; base += 1024) {
+        const int s = base + (int)threadIdx.x;
+        const bool live = s < S;
+        SegPlan p;
+        seg_fields(live ? st.off[s + 1] - st.off[s] : 0u, live ? st.L[s] : 1u, &p);
+        p.off = live ? st.off[s] : 0u;
+        uint64_t tot;
+        const uint64_t ex_t = block_exclusive_scan<1024>(live ? p.ntiles : 0, scan, &tot);
+        const uint64_t c0 = carry[0];
+        __syncthreads();
+        if (threadIdx.x == 0) carry[0] = c0 + tot;
+        const uint64_t ex_b = block_exclusive_scan<1024>(live && p.mode == kModeBig ? p.nbins : 0, scan, &tot);
+        const uint64_t c1 = carry[1];
+        __syncthreads();
+        if (threadIdx.x == 0) carry[1] = c1 + tot;
+        if (live) {
+            p.tile_off = (uint32_t)(c0 + ex_t);
+            p.big_off = (uint32_t)(c1 + ex_b);
+            plan[s] = p;
+        }
+        __syncthreads();
+    }
+    for (int k = threadIdx.x; k < K; k += 1024) pool_cnt[k] = 0;
+    for (uint64_t i = threadIdx.x; i < (uint64_t)K * big_per_learner; i += 1024) big[i] = 0;
+}
+
+__device__ __forceinline__ int find_segment_by_tile(const SegPlan* plan, int S, uint32_t lt) {
+    int lo = 0, hi = S;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(&plan[mid].tile_off) <= lt) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+// Bin maxima of segments whose bins are longer than a tile.
+__global__ void __launch_bounds__(NT) ada_bigmax(const SegPlan* __restrict__ plan, int S, uint64_t N,
+                                                 uint32_t tiles_per_learner, uint64_t total_tiles,
+                                                 const float* __restrict__ dW, const float* __restrict__ R,
+                                                 uint32_t* __restrict__ big, uint64_t big_per_learner) {
+    const int lane = threadIdx.x & 31;
+    for (uint64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+        const uint32_t k = (uint32_t)(t / tiles_per_learner);
+        const uint32_t lt = (uint32_t)(t - (uint64_t)k * tiles_per_learner);
+        const int s = find_segment_by_tile(plan, S, lt);
+        const SegPlan p = plan[s];
+        if (p.mode != kModeBig) continue;
+        const uint32_t start = (lt - p.tile_off) * kTileMax;
+        const uint32_t len = p.n - start < kTileMax ? p.n - start : kTileMax;
+        const uint64_t base = (uint64_t)k * N + p.off + start;
+        uint32_t* bm = big + (uint64_t)k * big_per_learner + p.big_off;
+        for (uint32_t e0 = 0; e0 < len; e0 += NT) {
+            const uint32_t e = e0 + threadIdx.x;
+            const bool in = e < len;
+            const float g = in ? __fadd_rn(R[base + e], __ldg(dW + base + e)) : 0.0f;
+            const uint32_t bin = in ? (start + e) / p.L : 0xffffffffu;
+            const unsigned am = __ballot_sync(kFull, in);
+            if (in) {
+                const unsigned grp = __match_any_sync(am, bin);
+                const uint32_t mx = __reduce_max_sync(grp, mag_key(g));
+                if (lane == __ffs(grp) - 1) atomicMax(&bm[bin], mx);
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(NT, 2) ada_bins(const SegPlan* __restrict__ plan, int S, uint64_t N,
+                                                  uint32_t tiles_per_learner, uint64_t total_tiles,
+                                                  const float* __restrict__ dW, float* __restrict__ R,
+                                                  const uint32_t* __restrict__ big, uint64_t big_per_learner,
+                                                  uint32_t* __restrict__ pool_cnt, uint2* __restrict__ tile_tab,
+                                                  double2* __restrict__ tile_sum, uint2* __restrict__ pool,
+                                                  uint64_t pool_cap) {
+    __shared__ uint32_t bmax[kTileMax];
+    __shared__ uint64_t scan[NT / 32 + 1];
+    __shared__ uint32_t s_base;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (uint64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+        const uint32_t k = (uint32_t)(t / tiles_per_learner);
+        const uint32_t lt = (uint32_t)(t - (uint64_t)k * tiles_per_learner);
+        const int s = find_segment_by_tile(plan, S, lt);
+        const SegPlan p = plan[s];
+        const uint32_t tj = lt - p.tile_off;
+        const uint32_t start = tj * p.tile_len;
+        const uint32_t len = p.n - start < p.tile_len ? p.n - start : p.tile_len;
+        const uint64_t base = (uint64_t)k * N + p.off + start;
+        const bool small = p.mode == kModeSmall;
+        const uint32_t nbt = small ? (p.nbins - tj * p.bpt < p.bpt ? p.nbins - tj * p.bpt : p.bpt) : 0;
+        const bool aligned = (base & 3) == 0;
+        const uint32_t* bigm = big + (uint64_t)k * big_per_learner + p.big_off;
+
+        if (small)
+            for (uint32_t b = threadIdx.x; b < nbt; b += NT) bmax[b] = 0u;
+
+        float4 Gv[4], Dv[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const uint32_t e = 4u * (r * NT + threadIdx.x);
+            if (aligned && e + 4 <= len) {
+                Dv[r] = __ldg(reinterpret_cast<const float4*>(dW + base + e));
+                Gv[r] = *reinterpret_cast<const float4*>(R + base + e);
+            } else {
+                float* d4 = &Dv[r].x;
+                float* g4 = &Gv[r].x;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const bool in = e + j < len;
+                    d4[j] = in ? __ldg(dW + base + e + j) : 0.0f;
+                    g4[j] = in ? R[base + e + j] : 0.0f;
+                }
+            }
+        }
+        __syncthreads();  // bmax zeroed
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const uint32_t e = 4u * (r * NT + threadIdx.x);
+            float* g4 = &Gv[r].x;
+            const float* d4 = &Dv[r].x;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) g4[j] = __fadd_rn(g4[j], d4[j]);  // G = R + dW
+            if (small) {
+                if (p.L >= 4) {
+                    // the four entries span at most two bins: b0 and b0 + 1
+                    const uint32_t b0 = e < len ? (uint32_t)__float2int_rd(((float)e + 0.5f) * p.invL) : 0xffffffffu;
+                    uint32_t mA = 0, mB = 0;
+                    bool hasB = false;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (e + j >= len) break;
+                        const uint32_t bj = (uint32_t)__float2int_rd(((float)(e + j) + 0.5f) * p.invL);
+                        const uint32_t key = mag_key(g4[j]);
+                        if (bj == b0) mA = max(mA, key);
+                        else { mB = max(mB, key); hasB = true; }
+                    }
+                    const bool inA = b0 != 0xffffffffu;
+                    unsigned am = __ballot_sync(kFull, inA);
+                    if (inA) {
+                        const unsigned grp = __match_any_sync(am, b0);
+                        const uint32_t mx = __reduce_max_sync(grp, mA);
+                        if (lane == __ffs(grp) - 1) atomicMax(&bmax[b0], mx);
+                    }
+                    am = __ballot_sync(kFull, hasB);
+                    if (hasB) {
+                        const unsigned grp = __match_any_sync(am, b0 + 1);
+                        const uint32_t mx = __reduce_max_sync(grp, mB);
+                        if (lane == __ffs(grp) - 1) atomicMax(&bmax[b0 + 1], mx);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (e + j < len) {
+                            const uint32_t bj = (uint32_t)__float2int_rd(((float)(e + j) + 0.5f) * p.invL);
+                            atomicMax(&bmax[bj], mag_key(g4[j]));
+                        }
+                }
+            }
+        }
+        __syncthreads();  // bin maxima final
+        // compensated sum of this tile's bin maxima, in bin order (warp 0)
+        if (small && warp == 0) {
+            const uint32_t per = (nbt + 31) / 32;
+            double sm = 0.0, cm = 0.0;
+            for (uint32_t b = lane * per; b < nbt && b < (lane + 1) * per; ++b)
+                csum_add(sm, cm, (double)__uint_as_float(bmax[b]));
+            double S0 = 0.0, C0 = 0.0;
+            for (int l = 0; l < 32; ++l) {
+                const double ls = __shfl_sync(kFull, sm, l);
+                const double lc = __shfl_sync(kFull, cm, l);
+                csum_add(S0, C0, ls);
+                C0 = __dadd_rn(C0, lc);
+            }
+            if (lane == 0) tile_sum[t] = make_double2(S0, C0);
+        }
+        // selection, residue store, candidate flags
+        uint64_t packed = 0;
+        uint32_t flags = 0;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const uint32_t e = 4u * (r * NT + threadIdx.x);
+            float* g4 = &Gv[r].x;
+            const float* d4 = &Dv[r].x;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                bool sel = false;
+                if (e + j < len) {
+                    uint32_t gm;
+                    if (small) gm = bmax[(uint32_t)__float2int_rd(((float)(e + j) + 0.5f) * p.invL)];
+                    else gm = __ldg(&bigm[(start + e + j) / p.L]);
+                    const uint32_t hk = mag_key(__fadd_rn(g4[j], d4[j]));  // |G + dW|
+                    sel = hk >= gm && gm > 0u && mag_key(g4[j]) != 0u;
+                }
+                flags |= (uint32_t)sel << (4 * r + j);
+            }
+            packed |= (uint64_t)__popc((flags >> (4 * r)) & 0xFu) << (16 * r);
+            if (aligned && e + 4 <= len) {
+                *reinterpret_cast<float4*>(R + base + e) = Gv[r];
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (e + j < len) R[base + e + j] = g4[j];
+            }
+        }
+        if (!__syncthreads_or(flags != 0)) {
+            if (threadIdx.x == 0) tile_tab[t] = make_uint2(0u, 0u);
+            continue;
+        }
+        uint64_t total;
+        const uint64_t ex = block_exclusive_scan<NT>(packed, scan, &total);
+        uint32_t cnt_total = 0, round_base[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            round_base[r] = cnt_total;
+            cnt_total += (uint32_t)(total >> (16 * r)) & 0xFFFFu;
+        }
+        if (threadIdx.x == 0) {
+            const uint32_t b = atomicAdd(&pool_cnt[k], cnt_total);
+            s_base = b;
+            tile_tab[t] = make_uint2(b, cnt_total);
+        }
+        __syncthreads();
+        const uint32_t pb = s_base;
+        if ((uint64_t)pb + cnt_total <= pool_cap) {
+            uint2* dst = pool + (uint64_t)k * pool_cap + pb;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                uint32_t pos = round_base[r] + ((uint32_t)(ex >> (16 * r)) & 0xFFFFu);
+                const uint32_t e = 4u * (r * NT + threadIdx.x);
+                const float* g4 = &Gv[r].x;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if ((flags >> (4 * r + j)) & 1u) dst[pos++] = make_uint2(p.off + start + e + j, __float_as_uint(g4[j]));
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// One CTA per (learner, segment): output slots of the tiles in index order,
+// the segment's count, and its scale = mean of the bin maxima.
+__global__ void __launch_bounds__(NT) ada_scan(const SegPlan* __restrict__ plan, int S,
+                                               uint32_t tiles_per_learner, const uint2* __restrict__ tile_tab,
+                                               const double2* __restrict__ tile_sum, const uint32_t* __restrict__ big,
+                                               uint64_t big_per_learner, uint32_t* __restrict__ tile_rel,
+                                               int64_t* __restrict__ counts, float* __restrict__ scales) {
+    __shared__ uint64_t scan[NT / 32 + 1];
+    const int unit = blockIdx.x;
+    const int k = unit / S, s = unit - k * S;
+    const SegPlan p = plan[s];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint64_t t0 = (uint64_t)k * tiles_per_learner + p.tile_off;
+    uint64_t run = 0;
+    for (uint32_t jb = 0; jb < p.ntiles; jb += NT) {
+        const uint32_t j = jb + threadIdx.x;
+        const uint32_t c = j < p.ntiles ? tile_tab[t0 + j].y : 0u;
+        uint64_t tot;
+        const uint64_t ex = block_exclusive_scan<NT>(c, scan, &tot);
+        if (j < p.ntiles) tile_rel[t0 + j] = (uint32_t)(run + ex);
+        run += tot;
+    }
+    if (warp == 0) {
+        // compensated sum of the bin maxima in bin order, 32 contiguous runs
+        double sm = 0.0, cm = 0.0;
+        if (p.mode == kModeSmall) {
+            const uint32_t per = (p.ntiles + 31) / 32;
+            for (uint32_t j = lane * per; j < p.ntiles && j < (lane + 1) * per; ++j) {
+                const double2 ts = tile_sum[t0 + j];
+                csum_add(sm, cm, ts.x);
+                cm = __dadd_rn(cm, ts.y);
+            }
+        } else if (p.mode == kModeBig) {
+            const uint32_t* bm = big + (uint64_t)k * big_per_learner + p.big_off;
+            const uint32_t per = (p.nbins + 31) / 32;
+            for (uint32_t b = lane * per; b < p.nbins && b < (lane + 1) * per; ++b)
+                csum_add(sm, cm, (double)__uint_as_float(bm[b]));
+        }
+        double S0 = 0.0, C0 = 0.0;
+        for (int l = 0; l < 32; ++l) {
+            const double ls = __shfl_sync(kFull, sm, l);
+            const double lc = __shfl_sync(kFull, cm, l);
+            csum_add(S0, C0, ls);
+            C0 = __dadd_rn(C0, lc);
+        }
+        if (lane == 0) {
+            counts[unit] = (int64_t)run;
+            scales[unit] = p.nbins ? (float)(__dadd_rn(S0, C0) / (double)p.nbins) : 0.0f;
+        }
+    }
+}
+
+// One warp per run of tiles: emit (index, sign(G)*scale) at the ordered slot
+// and fix the residue.  A learner whose total exceeds cap sends nothing; its
+// residue keeps G = R + dW (already stored by ada_bins).
+__global__ void __launch_bounds__(NT) ada_emit(const SegPlan* __restrict__ plan, int S, uint64_t N,
+                                               uint32_t tiles_per_learner, uint64_t total_tiles,
+                                               uint64_t tiles_per_warp, const uint2* __restrict__ tile_tab,
+                                               const uint32_t* __restrict__ tile_rel, const uint2* __restrict__ pool,
+                                               uint64_t pool_cap, const int64_t* __restrict__ counts,
+                                               const float* __restrict__ scales, float* __restrict__ R,
+                                               gcsgd_pair* __restrict__ out, uint64_t cap, int K,
+                                               int64_t* __restrict__ totals) {
+    const int lane = threadIdx.x & 31;
+    const uint64_t gw = ((uint64_t)blockIdx.x * NT + threadIdx.x) >> 5;
+    if (blockIdx.x == 0 && threadIdx.x < 32) {
+        for (int k = 0; k < K; ++k) {
+            int64_t sum = 0;
+            for (int s = lane; s < S; s += 32) sum += counts[(uint64_t)k * S + s];
+            for (int d = 16; d > 0; d >>= 1) sum += __shfl_down_sync(kFull, sum, d);
+            if (lane == 0) totals[k] = sum;
+        }
+    }
+    const uint64_t t0 = gw * tiles_per_warp;
+    uint64_t t1 = t0 + tiles_per_warp;
+    if (t1 > total_tiles) t1 = total_tiles;
+    int cur_k = -1, cur_s = -1;
+    int64_t unit_off = 0, learner_total = 0;
+    float scale = 0.0f;
+    for (uint64_t t = t0; t < t1; ++t) {
+        const uint2 ent = tile_tab[t];
+        if (ent.y == 0) continue;
+        const uint32_t k = (uint32_t)(t / tiles_per_learner);
+        const uint32_t lt = (uint32_t)(t - (uint64_t)k * tiles_per_learner);
+        const int s = find_segment_by_tile(plan, S, lt);
+        if ((int)k != cur_k || s != cur_s) {
+            int64_t before = 0, all = 0;
+            for (int q = lane; q < S; q += 32) {
+                const int64_t c = counts[(uint64_t)k * S + q];
+                all += c;
+                if (q < s) before += c;
+            }
+            for (int d = 16; d > 0; d >>= 1) {
+                before += __shfl_down_sync(kFull, before, d);
+                all += __shfl_down_sync(kFull, all, d);
+            }
+            unit_off = __shfl_sync(kFull, before, 0);
+            learner_total = __shfl_sync(kFull, all, 0);
+            scale = scales[(uint64_t)k * S + s];
+            cur_k = (int)k;
+            cur_s = s;
+        }
+        if ((uint64_t)learner_total > cap) continue;  // nothing sent: residue keeps G
+        const uint2* src = pool + (uint64_t)k * pool_cap + ent.x;
+        const uint64_t slot0 = (uint64_t)unit_off + tile_rel[t];
+        for (uint32_t j = lane; j < ent.y; j += 32) {
+            const uint2 it = src[j];
+            const float g = __uint_as_float(it.y);
+            const float q = g > 0.0f ? scale : -scale;
+            R[(uint64_t)k * N + it.x] = __fsub_rn(g, q);
+            gcsgd_pair pr;
+            pr.idx = it.x;
+            pr.val = q;
+            out[(uint64_t)k * cap + slot0 + j] = pr;
+        }
+    }
+}
+
+}  // namespace ada
+
+size_t adacomp_workspace_bytes(const int64_t* off, const int32_t* lt, int S, int K, int64_t cap) {
+    ada::HostPlan hp;
+    ada::host_plan(off, lt, S, &hp);
+    return ada::layout(S, K, cap, hp, nullptr, nullptr);
+}
+
+int adacomp_launch(const int64_t* off, int S, const int32_t* lt, int K, const float* dW, float* R, gcsgd_pair* out,
+                   int64_t cap, int64_t* counts, float* scales, int64_t* totals, void* ws, size_t ws_bytes,
+                   cudaStream_t stream) {
+    using namespace ada;
+    HostPlan hp;
+    host_plan(off, lt, S, &hp);
+    Workspace w;
+    const size_t need = layout(S, K, cap, hp, ws, &w);
+    if (ws_bytes < need)
+        return set_error(GCSGD_ERR_WORKSPACE, "adacomp_compress: workspace of %zu bytes, %zu needed", ws_bytes, need);
+    const uint64_t N = (uint64_t)off[S];
+    const uint64_t T = (uint64_t)K * hp.tiles_per_learner;
+    int rc;
+    {
+        LaunchScope ls("ada_plan", stream);
+        if (S <= 256) {
+            SegTable<256> st;
+            for (int s = 0; s <= S; ++s) st.off[s] = (uint32_t)off[s];
+            for (int s = 0; s < S; ++s) st.L[s] = (uint32_t)lt[s];
+            ada_plan<256><<<1, 1024, 0, stream>>>(st, S, K, hp.big_per_learner, w.plan, w.pool_cnt, w.big);
+        } else {
+            SegTable<GCSGD_MAX_SEGMENTS> st;
+            for (int s = 0; s <= S; ++s) st.off[s] = (uint32_t)off[s];
+            for (int s = 0; s < S; ++s) st.L[s] = (uint32_t)lt[s];
+            ada_plan<GCSGD_MAX_SEGMENTS><<<1, 1024, 0, stream>>>(st, S, K, hp.big_per_learner, w.plan, w.pool_cnt,
+                                                                w.big);
+        }
+        if ((rc = check_launch("ada_plan"))) return rc;
+    }
+    const uint64_t grid_cap = (uint64_t)sm_count() * 2;
+    if (hp.big_per_learner > 0 && T > 0) {
+        LaunchScope ls("ada_bigmax", stream);
+        ada_bigmax<<<(unsigned)(T < grid_cap ? T : grid_cap), NT, 0, stream>>>(
+            w.plan, S, N, (uint32_t)hp.tiles_per_learner, T, dW, R, w.big, hp.big_per_learner);
+        if ((rc = check_launch("ada_bigmax"))) return rc;
+    }
+    if (T > 0) {
+        LaunchScope ls("ada_bins", stream);
+        ada_bins<<<(unsigned)(T < grid_cap ? T : grid_cap), NT, 0, stream>>>(
+            w.plan, S, N, (uint32_t)hp.tiles_per_learner, T, dW, R, w.big, hp.big_per_learner, w.pool_cnt,
+            w.tile_tab, w.tile_sum, w.pool, (uint64_t)cap);
+        if ((rc = check_launch("ada_bins"))) return rc;
+    }
+    {
+        LaunchScope ls("ada_scan", stream);
+        ada_scan<<<(unsigned)(K * S), NT, 0, stream>>>(w.plan, S, (uint32_t)hp.tiles_per_learner, w.tile_tab,
+                                                        w.tile_sum, w.big, hp.big_per_learner, w.tile_rel, counts,
+                                                        scales);
+        if ((rc = check_launch("ada_scan"))) return rc;
+    }
+    {
+        LaunchScope ls("ada_emit", stream);
+        const uint64_t warps = (uint64_t)sm_count() * 8 * (NT / 32);
+        const uint64_t per = T ? (T + warps - 1) / warps : 1;
+        const uint64_t nw = T ? (T + per - 1) / per : 1;
+        const unsigned grid = (unsigned)((nw + NT / 32 - 1) / (NT / 32));
+        ada_emit<<<grid, NT, 0, stream>>>(w.plan, S, N, (uint32_t)hp.tiles_per_learner, T, per, w.tile_tab,
+                                          w.tile_rel, w.pool, (uint64_t)cap, counts, scales, R, out, (uint64_t)cap, K,
+                                          totals);
+        if ((rc = check_launch("ada_emit"))) return rc;
+    }
+    return GCSGD_OK;
+}
+
+}  // namespace gcsgd

@@ -1,0 +1,272 @@
+// api.cu -- the C ABI of libgcsgd: argument checks, error text, launch
+// counting and per-kernel event tracing.  All compute lives in dgc.cu,
+// adacomp.cu, spavg.cu and dcd.cu.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "dgc.cuh"
+
+namespace gcsgd {
+
+size_t adacomp_workspace_bytes(const int64_t* off, const int32_t* lt, int S, int K, int64_t cap);
+int adacomp_launch(const int64_t* off, int S, const int32_t* lt, int K, const float* dW, float* R, gcsgd_pair* out,
+                   int64_t cap, int64_t* counts, float* scales, int64_t* totals, void* ws, size_t ws_bytes,
+                   cudaStream_t stream);
+int spavg_launch(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int K, int64_t n, float* out,
+                 cudaStream_t stream);
+int dcd_launch(int n, int64_t d, const float* w, float* xhat, const float* grad, float gamma, double p, uint64_t seed,
+               uint32_t t, cudaStream_t stream);
+
+// ------------------------------------------------------------------ errors
+
+static thread_local char g_err[512] = "";
+
+int set_error(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int check_launch(const char* name) {
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(GCSGD_ERR_CUDA, "%s: launch failed: %s", name, cudaGetErrorString(e));
+    return GCSGD_OK;
+}
+
+int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+    int n = 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    return n;
+}
+
+// ------------------------------------------------------- launches, tracing
+
+static std::atomic<int64_t> g_launches{0};
+static std::atomic<bool> g_trace{false};
+static std::mutex g_trace_mu;
+struct PendingEvent {
+    std::string name;
+    cudaEvent_t a, b;
+};
+static std::vector<PendingEvent> g_pending;
+static std::vector<cudaEvent_t> g_free_events;
+
+static cudaEvent_t take_event() {
+    if (!g_free_events.empty()) {
+        cudaEvent_t e = g_free_events.back();
+        g_free_events.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+LaunchScope::LaunchScope(const char* n, cudaStream_t s) : name(n), stream(s), slot(-1) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (!g_trace.load(std::memory_order_relaxed)) return;
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    cudaEvent_t a = take_event(), b = take_event();
+    if (!a || !b) return;
+    cudaEventRecord(a, s);
+    g_pending.push_back({std::string(n), a, b});
+    slot = (int)g_pending.size() - 1;
+}
+
+LaunchScope::~LaunchScope() {
+    if (slot < 0) return;
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (slot < (int)g_pending.size()) cudaEventRecord(g_pending[slot].b, stream);
+}
+
+// ------------------------------------------------------------ validation
+
+static int check_layout(const char* fn, const int64_t* off, int32_t S) {
+    if (!off) return set_error(GCSGD_ERR_INVALID_ARG, "%s: seg_offsets is NULL", fn);
+    if (S < 1 || S > GCSGD_MAX_SEGMENTS)
+        return set_error(GCSGD_ERR_INVALID_ARG, "%s: n_seg = %d outside [1, %d]", fn, S, GCSGD_MAX_SEGMENTS);
+    if (off[0] != 0) return set_error(GCSGD_ERR_INVALID_ARG, "%s: seg_offsets[0] must be 0", fn);
+    for (int s = 0; s < S; ++s)
+        if (off[s + 1] < off[s])
+            return set_error(GCSGD_ERR_INVALID_ARG, "%s: seg_offsets decreases at segment %d", fn, s);
+    if (off[S] >= (int64_t)1 << 32)
+        return set_error(GCSGD_ERR_INVALID_ARG, "%s: N = %lld does not fit uint32 indices", fn, (long long)off[S]);
+    return GCSGD_OK;
+}
+
+static int check_ws(const char* fn, const void* ws, size_t bytes, size_t need) {
+    if (bytes < need)
+        return set_error(GCSGD_ERR_WORKSPACE, "%s: workspace of %zu bytes, %zu needed", fn, bytes, need);
+    if (need > 0 && (!ws || ((uintptr_t)ws & 255)))
+        return set_error(GCSGD_ERR_INVALID_ARG, "%s: workspace must be non-NULL and 256-byte aligned", fn);
+    return GCSGD_OK;
+}
+
+static size_t dgc_ws_bytes(const int64_t* off, int32_t S, int32_t K, double density) {
+    dgc::HostPlan hp;
+    dgc::host_plan(off, S, density, &hp);
+    return dgc_workspace_layout(S, K, hp, nullptr, nullptr);
+}
+
+}  // namespace gcsgd
+
+using namespace gcsgd;
+
+extern "C" {
+
+const char* gcsgd_last_error(void) { return g_err; }
+
+int32_t gcsgd_version(void) { return 100; }
+
+int64_t gcsgd_launch_count(void) { return g_launches.load(); }
+
+void gcsgd_launch_count_reset(void) { g_launches.store(0); }
+
+int gcsgd_trace_enable(int32_t on) {
+    g_trace.store(on != 0);
+    return GCSGD_OK;
+}
+
+int gcsgd_trace_read(gcsgd_trace_entry* entries, int32_t max, int32_t* n_out) {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    std::map<std::string, std::pair<int64_t, double>> agg;
+    std::vector<std::string> order;
+    int rc = GCSGD_OK;
+    for (auto& p : g_pending) {
+        float ms = 0.0f;
+        if (cudaEventSynchronize(p.b) != cudaSuccess || cudaEventElapsedTime(&ms, p.a, p.b) != cudaSuccess)
+            rc = set_error(GCSGD_ERR_CUDA, "gcsgd_trace_read: event timing failed");
+        if (!agg.count(p.name)) order.push_back(p.name);
+        agg[p.name].first += 1;
+        agg[p.name].second += ms;
+        g_free_events.push_back(p.a);
+        g_free_events.push_back(p.b);
+    }
+    g_pending.clear();
+    int32_t n = 0;
+    for (auto& name : order) {
+        if (entries && n < max) {
+            memset(&entries[n], 0, sizeof(gcsgd_trace_entry));
+            strncpy(entries[n].name, name.c_str(), sizeof(entries[n].name) - 1);
+            entries[n].launches = agg[name].first;
+            entries[n].total_ms = agg[name].second;
+        }
+        ++n;
+    }
+    if (n_out) *n_out = n;
+    return rc;
+}
+
+int64_t gcsgd_dgc_k(double density, int64_t n) {
+    if (n <= 0) return 0;
+    return (int64_t)dgc_k_of(density, (uint64_t)n);
+}
+
+int gcsgd_dgc_workspace_size(const int64_t* seg_offsets, int32_t n_seg, int32_t K, double density, size_t* bytes) {
+    int rc;
+    if ((rc = check_layout("gcsgd_dgc_workspace_size", seg_offsets, n_seg))) return rc;
+    if (K < 1 || !bytes) return set_error(GCSGD_ERR_INVALID_ARG, "gcsgd_dgc_workspace_size: K < 1 or bytes NULL");
+    if (!(density > 0.0 && density <= 1.0))
+        return set_error(GCSGD_ERR_INVALID_ARG, "gcsgd_dgc_workspace_size: density %g outside (0, 1]", density);
+    *bytes = dgc_ws_bytes(seg_offsets, n_seg, K, density);
+    return GCSGD_OK;
+}
+
+int dgc_compress(const int64_t* seg_offsets, int32_t n_seg, int32_t K, const float* grad, float* u, float* v,
+                 double density, float momentum, float clip_thr, int32_t clip_nodes, gcsgd_pair* out, int64_t cap,
+                 int64_t* counts, int64_t* totals, void* workspace, size_t workspace_bytes, void* stream) {
+    const char* fn = "dgc_compress";
+    int rc;
+    if ((rc = check_layout(fn, seg_offsets, n_seg))) return rc;
+    if (K < 1) return set_error(GCSGD_ERR_INVALID_ARG, "%s: K = %d < 1", fn, K);
+    if (!(density > 0.0 && density <= 1.0))
+        return set_error(GCSGD_ERR_INVALID_ARG, "%s: density %g outside (0, 1]", fn, density);
+    if (!isfinite(momentum) || !isfinite(clip_thr))
+        return set_error(GCSGD_ERR_INVALID_ARG, "%s: momentum and clip_thr must be finite", fn);
+    if (clip_nodes < 1) return set_error(GCSGD_ERR_INVALID_ARG, "%s: clip_nodes = %d < 1", fn, clip_nodes);
+    if (cap < 0) return set_error(GCSGD_ERR_INVALID_ARG, "%s: cap < 0", fn);
+    if (seg_offsets[n_seg] > 0 && (!grad || !u || !v))
+        return set_error(GCSGD_ERR_INVALID_ARG, "%s: grad, u and v must be non-NULL", fn);
+    if (!counts) return set_error(GCSGD_ERR_INVALID_ARG, "%s: counts is NULL", fn);
+    if (cap > 0 && !out) return set_error(GCSGD_ERR_INVALID_ARG, "%s: out is NULL", fn);
+    if ((rc = check_ws(fn, workspace, workspace_bytes, dgc_ws_bytes(seg_offsets, n_seg, K, density)))) return rc;
+    return dgc_launch(seg_offsets, n_seg, K, grad, u, v, density, momentum, clip_thr, clip_nodes, out, cap, counts,
+                      totals, workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+int gcsgd_adacomp_workspace_size(const int64_t* seg_offsets, int32_t n_seg, const int32_t* lt, int32_t K,
+                                 int64_t cap, size_t* bytes) {
+    const char* fn = "gcsgd_adacomp_workspace_size";
+    int rc;
+    if ((rc = check_layout(fn, seg_offsets, n_seg))) return rc;
+    if (!lt || K < 1 || cap < 0 || !bytes) return set_error(GCSGD_ERR_INVALID_ARG, "%s: bad argument", fn);
+    for (int s = 0; s < n_seg; ++s)
+        if (lt[s] < 1) return set_error(GCSGD_ERR_INVALID_ARG, "%s: lt[%d] = %d < 1", fn, s, lt[s]);
+    *bytes = adacomp_workspace_bytes(seg_offsets, lt, n_seg, K, cap);
+    return GCSGD_OK;
+}
+
+int adacomp_compress(const int64_t* seg_offsets, int32_t n_seg, const int32_t* lt, int32_t K, const float* dW,
+                     float* residue, gcsgd_pair* out, int64_t cap, int64_t* counts, float* scales, int64_t* totals,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+    const char* fn = "adacomp_compress";
+    int rc;
+    if ((rc = check_layout(fn, seg_offsets, n_seg))) return rc;
+    if (!lt) return set_error(GCSGD_ERR_INVALID_ARG, "%s: lt is NULL", fn);
+    for (int s = 0; s < n_seg; ++s)
+        if (lt[s] < 1) return set_error(GCSGD_ERR_INVALID_ARG, "%s: lt[%d] = %d < 1", fn, s, lt[s]);
+    if (K < 1) return set_error(GCSGD_ERR_INVALID_ARG, "%s: K = %d < 1", fn, K);
+    if (cap < 0 || cap >= (int64_t)1 << 32) return set_error(GCSGD_ERR_INVALID_ARG, "%s: cap outside [0, 2^32)", fn);
+    if (seg_offsets[n_seg] > 0 && (!dW || !residue))
+        return set_error(GCSGD_ERR_INVALID_ARG, "%s: dW and residue must be non-NULL", fn);
+    if (!counts || !scales || !totals)
+        return set_error(GCSGD_ERR_INVALID_ARG, "%s: counts, scales and totals must be non-NULL", fn);
+    if (cap > 0 && !out) return set_error(GCSGD_ERR_INVALID_ARG, "%s: out is NULL", fn);
+    if ((rc = check_ws(fn, workspace, workspace_bytes, adacomp_workspace_bytes(seg_offsets, lt, n_seg, K, cap))))
+        return rc;
+    return adacomp_launch(seg_offsets, n_seg, lt, K, dW, residue, out, cap, counts, scales, totals, workspace,
+                          workspace_bytes, (cudaStream_t)stream);
+}
+
+int sparse_average(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int32_t K, int64_t n, float* out,
+                   void* stream) {
+    const char* fn = "sparse_average";
+    if (K < 1 || K > 4096) return set_error(GCSGD_ERR_INVALID_ARG, "%s: K = %d outside [1, 4096]", fn, K);
+    if (n < 0 || n > ((int64_t)1 << 32)) return set_error(GCSGD_ERR_INVALID_ARG, "%s: n outside [0, 2^32]", fn);
+    if (cap < 0) return set_error(GCSGD_ERR_INVALID_ARG, "%s: cap < 0", fn);
+    if (!counts || (n > 0 && !out) || (cap > 0 && !lists))
+        return set_error(GCSGD_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+    return spavg_launch(lists, cap, counts, K, n, out, (cudaStream_t)stream);
+}
+
+int dcd_step(int32_t n_nodes, int64_t d, const float* w_ring, float* xhat, const float* grad, float gamma,
+             double keep_p, uint64_t seed, uint32_t t, void* stream) {
+    const char* fn = "dcd_step";
+    if (n_nodes < 1) return set_error(GCSGD_ERR_INVALID_ARG, "%s: n_nodes < 1", fn);
+    if (d < 0 || d >= ((int64_t)1 << 36)) return set_error(GCSGD_ERR_INVALID_ARG, "%s: d outside [0, 2^36)", fn);
+    if (!w_ring) return set_error(GCSGD_ERR_INVALID_ARG, "%s: w_ring is NULL", fn);
+    if (d > 0 && (!xhat || !grad)) return set_error(GCSGD_ERR_INVALID_ARG, "%s: xhat and grad must be non-NULL", fn);
+    if (!(keep_p > 0.0 && keep_p <= 1.0))
+        return set_error(GCSGD_ERR_INVALID_ARG, "%s: keep_p %g outside (0, 1]", fn, keep_p);
+    if (!isfinite(gamma) || !isfinite(w_ring[0]) || !isfinite(w_ring[1]) || !isfinite(w_ring[2]))
+        return set_error(GCSGD_ERR_INVALID_ARG, "%s: gamma and weights must be finite", fn);
+    return dcd_launch(n_nodes, d, w_ring, xhat, grad, gamma, keep_p, seed, t, (cudaStream_t)stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,171 @@
+// dcd.cu -- one DCD-PSGD iteration of n ring nodes in one pass.
+//
+// "Communication Compression for Decentralized Training", DCD-PSGD steps
+// 1-3: mix the neighbours' replicas with W and take the SGD step
+// (x_half), compress the difference z = x_half - x, and add C(z) to the model
+// and to every replica of it.  Every holder of a replica of node i applies
+// the same C(z_i), so one array xhat[n][d] stands for all models and
+// replicas.  C is random sparsification: keep z_e with probability p and
+// scale it by 1/p, the keep draw taken from Philox4x32-10 (Salmon et al.,
+// SC'11) at counter (e/4, node, t, e/2^34) under key (seed).
+//
+// Each thread owns four consecutive elements of every node: it loads the
+// n models' and gradients' float4s, computes all n new values from the old
+// ones held in registers, and stores them, so the update is in place with no
+// second buffer and every element is read and written exactly once.  One
+// Philox call yields the keep words of the thread's four elements of a node.
+#include "common.cuh"
+
+namespace gcsgd {
+namespace dcd {
+
+constexpr int NT = 256;
+
+struct Params {
+    float w0, w1, w2, gamma, inv_p;
+    uint64_t thr;  // keep when word < thr (2^32 keeps everything)
+    uint32_t key0, key1, t;
+};
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+    constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u, W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += W0;
+            k1 += W1;
+        }
+        const uint32_t hi0 = __umulhi(M0, c.x), lo0 = M0 * c.x;
+        const uint32_t hi1 = __umulhi(M1, c.z), lo1 = M1 * c.z;
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    }
+    return c;
+}
+
+__device__ __forceinline__ float mix_step(const Params& P, float xl, float xi, float xr, float g, uint32_t word) {
+    float acc = __fmul_rn(P.w0, xl);
+    acc = __fadd_rn(acc, __fmul_rn(P.w1, xi));
+    acc = __fadd_rn(acc, __fmul_rn(P.w2, xr));
+    const float xh = __fsub_rn(acc, __fmul_rn(P.gamma, g));
+    const float z = __fsub_rn(xh, xi);
+    const float cz = ((uint64_t)word < P.thr) ? __fmul_rn(z, P.inv_p) : 0.0f;
+    return __fadd_rn(xi, cz);
+}
+
+__device__ __forceinline__ float4 node_update(const Params& P, const float4& L, const float4& X, const float4& Rr,
+                                              const float4& G, uint64_t q, uint32_t node) {
+    const uint4 w = philox4x32_10(make_uint4((uint32_t)q, node, P.t, (uint32_t)(q >> 32)), P.key0, P.key1);
+    float4 o;
+    o.x = mix_step(P, L.x, X.x, Rr.x, G.x, w.x);
+    o.y = mix_step(P, L.y, X.y, Rr.y, G.y, w.y);
+    o.z = mix_step(P, L.z, X.z, Rr.z, G.z, w.z);
+    o.w = mix_step(P, L.w, X.w, Rr.w, G.w, w.w);
+    return o;
+}
+
+__device__ __forceinline__ float4 ld4(const float* p, uint64_t e, uint64_t d, bool vec) {
+    if (vec) return *reinterpret_cast<const float4*>(p + e);
+    float4 r;
+    r.x = e < d ? p[e] : 0.f;
+    r.y = e + 1 < d ? p[e + 1] : 0.f;
+    r.z = e + 2 < d ? p[e + 2] : 0.f;
+    r.w = e + 3 < d ? p[e + 3] : 0.f;
+    return r;
+}
+
+__device__ __forceinline__ void st4(float* p, uint64_t e, uint64_t d, bool vec, const float4& v) {
+    if (vec) {
+        *reinterpret_cast<float4*>(p + e) = v;
+        return;
+    }
+    if (e < d) p[e] = v.x;
+    if (e + 1 < d) p[e + 1] = v.y;
+    if (e + 2 < d) p[e + 2] = v.z;
+    if (e + 3 < d) p[e + 3] = v.w;
+}
+
+// NN > 0: node count known at compile time, every load issued up front.
+template <int NN>
+__global__ void __launch_bounds__(NT, 2) dcd_fixed(Params P, uint64_t d, float* __restrict__ xhat,
+                                                const float* __restrict__ grad, bool rows_aligned) {
+    const uint64_t nq = (d + 3) / 4;
+    for (uint64_t q = (uint64_t)blockIdx.x * NT + threadIdx.x; q < nq; q += (uint64_t)gridDim.x * NT) {
+        const uint64_t e = 4 * q;
+        const bool vec = rows_aligned && e + 4 <= d;
+        float4 X[NN], G[NN];
+#pragma unroll
+        for (int i = 0; i < NN; ++i) {
+            X[i] = ld4(xhat + (uint64_t)i * d, e, d, vec);
+            G[i] = ld4(grad + (uint64_t)i * d, e, d, vec);
+        }
+#pragma unroll
+        for (int i = 0; i < NN; ++i) {
+            const int l = (i + NN - 1) % NN, r = (i + 1) % NN;
+            const float4 o = node_update(P, X[l], X[i], X[r], G[i], q, (uint32_t)i);
+            st4(xhat + (uint64_t)i * d, e, d, vec, o);
+        }
+    }
+}
+
+// Any node count: a rolling window keeps the old left neighbour and node 0.
+__global__ void __launch_bounds__(NT) dcd_rolling(Params P, int n, uint64_t d, float* __restrict__ xhat,
+                                                  const float* __restrict__ grad, bool rows_aligned) {
+    const uint64_t nq = (d + 3) / 4;
+    for (uint64_t q = (uint64_t)blockIdx.x * NT + threadIdx.x; q < nq; q += (uint64_t)gridDim.x * NT) {
+        const uint64_t e = 4 * q;
+        const bool vec = rows_aligned && e + 4 <= d;
+        const float4 x0 = ld4(xhat, e, d, vec);
+        float4 left = ld4(xhat + (uint64_t)(n - 1) * d, e, d, vec);
+        float4 cur = x0;
+        for (int i = 0; i < n; ++i) {
+            const float4 right = (i == n - 1) ? x0 : ld4(xhat + (uint64_t)(i + 1) * d, e, d, vec);
+            const float4 g = ld4(grad + (uint64_t)i * d, e, d, vec);
+            const float4 o = node_update(P, left, cur, right, g, q, (uint32_t)i);
+            st4(xhat + (uint64_t)i * d, e, d, vec, o);
+            left = cur;
+            cur = right;
+        }
+    }
+}
+
+}  // namespace dcd
+
+int dcd_launch(int n, int64_t d, const float* w, float* xhat, const float* grad, float gamma, double p,
+               uint64_t seed, uint32_t t, cudaStream_t stream) {
+    using namespace dcd;
+    if (d == 0) return GCSGD_OK;
+    Params P;
+    P.w0 = w[0];
+    P.w1 = w[1];
+    P.w2 = w[2];
+    P.gamma = gamma;
+    P.inv_p = (float)(1.0 / p);
+    P.thr = p >= 1.0 ? (1ull << 32) : (uint64_t)llround(p * 4294967296.0);
+    P.key0 = (uint32_t)seed;
+    P.key1 = (uint32_t)(seed >> 32);
+    P.t = t;
+    const bool rows_aligned = ((d & 3) == 0) && (((uintptr_t)xhat & 15) == 0) && (((uintptr_t)grad & 15) == 0);
+    const uint64_t nq = ((uint64_t)d + 3) / 4;
+    uint64_t grid = (uint64_t)sm_count() * (n <= 4 ? 8 : 4);
+    const uint64_t need = (nq + NT - 1) / NT;
+    if (grid > need) grid = need;
+    LaunchScope ls("dcd_step", stream);
+    switch (n) {
+#define DCD_CASE(NNV) \
+    case NNV: dcd_fixed<NNV><<<(unsigned)grid, NT, 0, stream>>>(P, (uint64_t)d, xhat, grad, rows_aligned); break;
+        DCD_CASE(1)
+        DCD_CASE(2)
+        DCD_CASE(3)
+        DCD_CASE(4)
+        DCD_CASE(5)
+        DCD_CASE(6)
+        DCD_CASE(7)
+        DCD_CASE(8)
+#undef DCD_CASE
+        default:
+            dcd_rolling<<<(unsigned)grid, NT, 0, stream>>>(P, n, (uint64_t)d, xhat, grad, rows_aligned);
+    }
+    return check_launch("dcd_step");
+}
+
+}  // namespace gcsgd

@@ -1,0 +1,211 @@
+/*
+ * gcsgd.h -- C ABI of the GB300 gradient-compression library (libgcsgd.so).
+ *
+ * The per-worker hot path of communication-efficient data-parallel SGD:
+ * Deep Gradient Compression, AdaComp, the decompress-and-average of K
+ * learners' sparse messages, and the DCD-PSGD replica update.  K learners
+ * (or n ring nodes) are batched in one call on one GPU.
+ *
+ * Conventions for every entry point
+ *  - Pointers are device pointers unless the comment says "host".  The
+ *    caller owns every buffer; the library allocates no memory in these
+ *    calls and never synchronises the stream.  Work is enqueued on `stream`
+ *    (a cudaStream_t; NULL is the legacy default stream) and runs
+ *    asynchronously.
+ *  - Tensors are flat, contiguous, row-major fp32.  A "layout" is a host
+ *    array seg_offsets[n_seg + 1] of int64 with seg_offsets[0] = 0 and
+ *    non-decreasing entries: segment (tensor) s is the element range
+ *    [seg_offsets[s], seg_offsets[s+1]) of each learner's N =
+ *    seg_offsets[n_seg] elements.  Empty segments are allowed.  N must be
+ *    below 2^32 (indices are uint32), n_seg at most GCSGD_MAX_SEGMENTS.
+ *  - A learner's sparse message is a list of gcsgd_pair with global
+ *    (within the learner) indices: segments one after another, each in
+ *    ascending index order, so the whole list is ascending.  Lists of K
+ *    learners sit at out + k*cap.
+ *  - Inputs must be finite; NaN/Inf give unspecified (but memory-safe)
+ *    results.
+ *  - Return value: GCSGD_OK, or a negative GCSGD_ERR_*; nothing was enqueued
+ *    when an argument check fails.  gcsgd_last_error() describes the last
+ *    failure of the calling thread.
+ */
+#ifndef GCSGD_H
+#define GCSGD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GCSGD_OK 0
+#define GCSGD_ERR_INVALID_ARG (-1)  /* null pointer, bad size, bad layout, bad scalar */
+#define GCSGD_ERR_CAPACITY (-2)     /* output capacity too small for a known count   */
+#define GCSGD_ERR_WORKSPACE (-3)    /* workspace smaller than *_workspace_size says  */
+#define GCSGD_ERR_CUDA (-4)         /* a CUDA runtime call failed (launch, device)   */
+
+#define GCSGD_MAX_SEGMENTS 2048
+
+/* One entry of a sparse message: 8 bytes, index then fp32 value. */
+typedef struct {
+    uint32_t idx;
+    float val;
+} gcsgd_pair;
+
+/* ------------------------------------------------------------------ DGC */
+
+/* Entries DGC sends from a segment of n values: max(1, ceil(density*n))
+ * computed in fp64, capped at n; 0 for an empty segment.  ("Deep Gradient
+ * Compression", section 3.1: only the largest-magnitude fraction of the
+ * accumulated gradient is sent.)  Host function. */
+int64_t gcsgd_dgc_k(double density, int64_t n);
+
+/* Bytes of device workspace dgc_compress needs for this layout, K and
+ * density (written to *bytes).  Host function. */
+int gcsgd_dgc_workspace_size(const int64_t* seg_offsets, int32_t n_seg, int32_t K,
+                             double density, size_t* bytes);
+
+/*
+ * One Deep Gradient Compression step for K learners ("Deep Gradient
+ * Compression: Reducing the Communication Bandwidth for Distributed
+ * Training", Appendix D with vanilla momentum; sections 3.1-3.3 and
+ * Appendix C):
+ *   1. local gradient clipping, when clip_thr > 0: if the L2 norm s of a
+ *      learner's gradient exceeds thr_k = clip_thr / sqrt(clip_nodes), the
+ *      gradient is scaled by c = (float)(thr_k / s) before accumulation;
+ *   2. momentum correction: u <- m*u + c*G, then v <- v + u (fp32, one
+ *      rounding per operation, no FMA);
+ *   3. exact per-segment top-k of |v| with k_s = gcsgd_dgc_k(density, n_s);
+ *      ties go to the lower index;
+ *   4. the selected (index, v) are written out and momentum factor masking
+ *      zeroes u and v at those indices.
+ *
+ * seg_offsets   host [n_seg+1] layout (see above).
+ * grad          [K][N] fp32 gradients, read only.
+ * u, v          [K][N] fp32 momentum and accumulated velocity, updated in
+ *               place (caller-owned state; zero them before the first step).
+ * density       in (0, 1];  momentum any finite value;  clip_thr <= 0 turns
+ *               clipping off;  clip_nodes >= 1 (the N of thr*N^-1/2).
+ * out           [K][cap] pairs; learner k's list at out + k*cap holds
+ *               sum_s k_s entries; cap must be at least that sum
+ *               (GCSGD_ERR_CAPACITY otherwise).
+ * counts        [K][n_seg] int64, entries per segment (always k_s).
+ * totals        [K] int64 entries per learner, or NULL.
+ * workspace     device scratch of at least gcsgd_dgc_workspace_size bytes,
+ *               256-byte aligned; its contents need not be initialised and
+ *               are not kept between calls.  Calls that share a workspace
+ *               must be ordered on the GPU.
+ */
+int dgc_compress(const int64_t* seg_offsets, int32_t n_seg, int32_t K,
+                 const float* grad, float* u, float* v,
+                 double density, float momentum, float clip_thr, int32_t clip_nodes,
+                 gcsgd_pair* out, int64_t cap, int64_t* counts, int64_t* totals,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* -------------------------------------------------------------- AdaComp */
+
+/* Bytes of device workspace adacomp_compress needs.  lt: host [n_seg] bin
+ * lengths L_T >= 1. Host function. */
+int gcsgd_adacomp_workspace_size(const int64_t* seg_offsets, int32_t n_seg, const int32_t* lt,
+                                 int32_t K, int64_t cap, size_t* bytes);
+
+/*
+ * One AdaComp step for K learners ("AdaComp : Adaptive Residual Gradient
+ * Compression for Data-Parallel Distributed Training", Proposed method):
+ *   G = R + dW; per bin of L_T values (a last partial bin is a bin of its
+ *   own) gmax = max |G|; an entry is selected when |G + dW| >= gmax of its
+ *   bin, gmax > 0 and G != 0; scale_s = mean of gmax over every bin of the
+ *   segment (fp64 sum, rounded to fp32 once); a selected entry is sent as
+ *   sign(G)*scale_s and the residue keeps R = G - sign(G)*scale_s; an
+ *   unselected entry keeps R = G.
+ *
+ * seg_offsets host layout;  lt host [n_seg] L_T per segment (>= 1).
+ * dW          [K][N] new gradients, read only.
+ * residue     [K][N] R, updated in place (zero it before the first step).
+ * out         [K][cap] pairs, lists as described above.
+ * counts      [K][n_seg] int64 entries per segment.
+ * scales      [K][n_seg] fp32 scale of each segment.
+ * totals      [K] int64 entries per learner (required).  The number of
+ *             selected entries is only known on the GPU: when totals[k] >
+ *             cap the list and residue of learner k are unspecified and the
+ *             caller must retry with a larger cap.
+ * workspace   at least gcsgd_adacomp_workspace_size bytes, 256-byte aligned.
+ */
+int adacomp_compress(const int64_t* seg_offsets, int32_t n_seg, const int32_t* lt, int32_t K,
+                     const float* dW, float* residue,
+                     gcsgd_pair* out, int64_t cap, int64_t* counts, float* scales, int64_t* totals,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------- sparse average */
+
+/*
+ * Decompress and average K learners' sparse messages ("AdaComp ...",
+ * Proposed method: learners exchange compressed gradients and average them
+ * before the weight update; "Deep Gradient Compression", Appendix A: the
+ * nodes' gradients are summed):
+ *   out[j] = (sum over the lists k = 0..K-1 that contain j, added in that
+ *             order in fp32 starting from +0) / K   (one fp32 divide),
+ *   out[j] = 0 where no list contains j.
+ * lists   [K][cap] pairs; list k is lists[k*cap .. k*cap + counts[k]),
+ *         strictly ascending indices below n.  Entries that break this are
+ *         skipped or misplaced but never cause an out-of-range access.
+ * counts  [K] int64 device array (0 <= counts[k] <= cap).
+ * out     [n] fp32, fully overwritten.
+ */
+int sparse_average(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int32_t K,
+                   int64_t n, float* out, void* stream);
+
+/* ------------------------------------------------------------- DCD-PSGD */
+
+/*
+ * One DCD-PSGD iteration of n_nodes nodes on a ring ("Communication
+ * Compression for Decentralized Training", DCD-PSGD steps 1-3), every node
+ * and every replica held once in xhat (each holder of a replica of node i
+ * applies the same C(z_i), so all replicas of x_i equal x_i):
+ *   x_half_i = w[0]*xhat_{i-1} + w[1]*xhat_i + w[2]*xhat_{i+1} - gamma*g_i
+ *              (indices mod n_nodes, products and sums in that order, fp32);
+ *   z_i      = x_half_i - xhat_i;
+ *   C(z)_e   = z_e * (float)(1/keep_p) if word < round(keep_p * 2^32), else 0,
+ *              word = Philox4x32-10(counter (e/4, i, t, e/2^34),
+ *                                   key (seed low, seed high))[e mod 4];
+ *   xhat_i  <- xhat_i + C(z_i).
+ * All nodes read the models of iteration t.
+ * w_ring  host [3] weights of the left neighbour, self and right neighbour.
+ * xhat    [n_nodes][d] fp32 models, updated in place.
+ * grad    [n_nodes][d] fp32 stochastic gradients, read only.
+ * keep_p  in (0, 1];  t the iteration number (part of the counter).
+ */
+int dcd_step(int32_t n_nodes, int64_t d, const float* w_ring, float* xhat, const float* grad,
+             float gamma, double keep_p, uint64_t seed, uint32_t t, void* stream);
+
+/* ----------------------------------------------------- errors, tracing */
+
+/* Message of the calling thread's last failure ("" if none).  Host. */
+const char* gcsgd_last_error(void);
+
+/* Library version: major*10000 + minor*100 + patch.  Host. */
+int32_t gcsgd_version(void);
+
+/* Number of kernels this process has launched through the library since
+ * load or the last gcsgd_launch_count_reset().  Host. */
+int64_t gcsgd_launch_count(void);
+void gcsgd_launch_count_reset(void);
+
+/* Per-kernel timing.  While enabled, every kernel launch is bracketed by
+ * two CUDA events recorded on its own stream (a small extra cost).
+ * gcsgd_trace_read waits for the recorded events, then writes up to `max`
+ * entries (kernel name, launches, summed milliseconds) and the entry count
+ * to *n_out; it clears the record.  Host functions. */
+typedef struct {
+    char name[48];
+    int64_t launches;
+    double total_ms;
+} gcsgd_trace_entry;
+int gcsgd_trace_enable(int32_t on);
+int gcsgd_trace_read(gcsgd_trace_entry* entries, int32_t max, int32_t* n_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GCSGD_H */

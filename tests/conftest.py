@@ -40,3 +40,27 @@ def f32(vals) -> np.ndarray:
 def ulp32(x) -> np.ndarray:
     x = np.abs(np.asarray(x, dtype=np.float32))
     return np.spacing(np.maximum(x, np.float32(np.finfo(np.float32).tiny)))
+
+
+@pytest.fixture(scope="session")
+def cuda_lib():
+    """The CUDA library, built in-tree and loaded; GPU tests need a CUDA device."""
+    import torch
+
+    from gradient_compression_sgd_gb300 import build
+
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    build.build()
+    import gradient_compression_sgd_gb300 as gc
+
+    gc.lib()
+    return gc
+
+
+def rel_err(a, b) -> float:
+    """max |a - b| / max(|b|, tiny) elementwise."""
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    if a.size == 0:
+        return 0.0
+    return float(np.max(np.abs(a - b) / np.maximum(np.abs(b), np.finfo(np.float32).tiny)))

@@ -1,0 +1,226 @@
+"""AdaComp, sparse-average and DCD parity: CUDA library against the CPU oracle.
+
+Indices, counts and masks are compared bit for bit; fp32 values within 1e-6
+relative (1e-5 for the K-way averages, where the contract allows a different
+summation order; the kernel keeps learner order, so they are expected exact).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from conftest import rel_err
+from gradient_compression_sgd_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+VAL_RTOL = 1e-6
+AVG_RTOL = 1e-5
+
+
+# ------------------------------------------------------------------ AdaComp
+
+def run_adacomp(gc, offsets, lt, dWs, cap=None, R0=None):
+    import torch
+    offsets = np.asarray(offsets, np.int64)
+    K, N = dWs[0].shape
+    cap = cap if cap is not None else max(1, N)
+    R_o = np.zeros((K, N), np.float32) if R0 is None else R0.copy()
+    R_g = torch.from_numpy(R_o.copy()).cuda()
+    a = gc.AdaComp(offsets, lt, K, cap)
+    results = []
+    for t, dW in enumerate(dWs):
+        G = R_o + dW  # fp32, the value the residue is measured against
+        try:
+            idx_o, val_o, counts_o, scales_o, totals_o = oracle.adacomp_step(offsets, lt, dW, R_o, cap=cap)
+            over = False
+        except oracle.OracleError:
+            over = True
+        out, totals = a(torch.from_numpy(np.ascontiguousarray(dW)).cuda(), R_g)
+        torch.cuda.synchronize()
+        tot_g = totals.cpu().numpy()
+        if over:
+            results.append(("overflow", tot_g))
+            assert np.any(tot_g > cap)
+            assert rel_err(R_g.cpu().numpy(), R_o) <= VAL_RTOL
+            continue
+        np.testing.assert_array_equal(a.counts.cpu().numpy(), counts_o, err_msg=f"counts t={t}")
+        np.testing.assert_array_equal(tot_g, totals_o)
+        assert rel_err(a.scales.cpu().numpy(), scales_o) <= VAL_RTOL, f"scales t={t}"
+        idx_g = gc.pair_indices(out).cpu().numpy()
+        val_g = gc.pair_values(out).cpu().numpy()
+        for k in range(K):
+            n = int(totals_o[k])
+            np.testing.assert_array_equal(idx_g[k, :n], idx_o[k, :n].astype(np.int64), err_msg=f"idx k={k} t={t}")
+            assert rel_err(val_g[k, :n], val_o[k, :n]) <= VAL_RTOL
+        # residue: relative to |G| (cancellation near G ~ scale makes |R| a poor yardstick)
+        Rg = R_g.cpu().numpy()
+        denom = np.maximum(np.abs(G), np.abs(R_o))
+        err = np.abs(Rg.astype(np.float64) - R_o) / np.maximum(denom, np.finfo(np.float32).tiny)
+        assert float(err.max(initial=0.0)) <= VAL_RTOL, f"residue t={t}"
+        results.append(("ok", tot_g))
+    return a, results
+
+
+def test_config1_adacomp_lt50(cuda_lib):
+    """The config-1 tensor (1,048,576 values N(0, 1e-3)) with L_T = 50
+    (20,972 bins, the last one of 26 values), 3 steps with the residue carried."""
+    w = wl.workload(1)
+    dWs = [wl.gradients(w, t).numpy() for t in range(w.steps)]
+    run_adacomp(cuda_lib, w.offsets, [w.also_adacomp_lt], dWs)
+
+
+def test_config3_small(cuda_lib):
+    """LSTM (hidden 150, vocab 1000; L_T = 500) + VGG-16 convs at 1/8 width
+    (L_T = 50), Laplace gradients, K = 8, 5 steps."""
+    w = wl.workload(3, small=True)
+    dWs = [wl.gradients(w, t).numpy() for t in range(w.steps)]
+    run_adacomp(cuda_lib, w.offsets, w.lt, dWs)
+
+
+@pytest.mark.parametrize("L", [1, 3, 4, 50, 64, 500, 4096, 5000, 123457])
+def test_bin_lengths(cuda_lib, L):
+    """Bin lengths below 4, odd, a whole tile, longer than a tile (bins that
+    straddle tiles), and one bin for the whole segment."""
+    rng = np.random.default_rng(L)
+    sizes = [123457, 0, 4099, 77]
+    off = wl.layout_offsets(sizes)
+    K = 2
+    dWs = [rng.laplace(0, 1e-3, size=(K, off[-1])).astype(np.float32) for _ in range(3)]
+    run_adacomp(cuda_lib, off, [L] * len(sizes), dWs)
+
+
+def test_mixed_bins_and_ragged_offsets(cuda_lib):
+    rng = np.random.default_rng(5)
+    sizes = [7, 50001, 13, 4096, 4097, 99999]
+    lt = [2, 50, 5, 500, 4096, 7000]
+    off = wl.layout_offsets(sizes)
+    dWs = [rng.laplace(0, 1e-2, size=(3, off[-1])).astype(np.float32) for _ in range(3)]
+    dWs[1][:, 100:400] = 0.0  # all-zero bins select nothing
+    run_adacomp(cuda_lib, off, lt, dWs)
+
+
+def test_capacity_overflow_sends_nothing_and_keeps_the_residue(cuda_lib):
+    rng = np.random.default_rng(6)
+    off = wl.layout_offsets([20000])
+    dWs = [rng.laplace(0, 1.0, size=(2, 20000)).astype(np.float32) for _ in range(2)]
+    dWs[0][1] *= 0  # learner 1 sends nothing at step 0: fits
+    _, res = run_adacomp(cuda_lib, off, [1], dWs, cap=5000)
+    assert res[0][0] == "overflow"
+
+
+# ------------------------------------------------------------ sparse average
+
+def run_average(gc, idx, val, counts, n):
+    import torch
+    K, cap = idx.shape
+    pairs = torch.zeros((K, cap, 2), dtype=torch.int32)
+    pairs[..., 0] = torch.from_numpy(idx.astype(np.int64)).to(torch.int32)
+    pairs[..., 1] = torch.from_numpy(val.view(np.int32))
+    pairs = pairs.cuda()
+    out = torch.full((max(n, 1),), float("nan"), device="cuda")
+    gc.sparse_average(pairs, torch.from_numpy(counts.astype(np.int64)).cuda(), n, out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()[:n]
+    want = oracle.sparse_average(idx, val, counts, n)
+    assert rel_err(got, want) <= AVG_RTOL
+    np.testing.assert_array_equal(np.nonzero(got)[0], np.nonzero(want)[0])
+    return got, want
+
+
+@pytest.mark.parametrize("K", [1, 2, 4, 8, 33])
+@pytest.mark.parametrize("n", [1, 4095, 4096, 100003])
+def test_sparse_average_random_lists(cuda_lib, K, n):
+    rng = np.random.default_rng(K * 7 + n)
+    cap = max(1, min(n, 3000))
+    idx = np.zeros((K, cap), np.uint32)
+    val = np.zeros((K, cap), np.float32)
+    counts = np.zeros(K, np.int64)
+    for k in range(K):
+        c = int(rng.integers(0, cap + 1))
+        idx[k, :c] = np.sort(rng.choice(n, size=c, replace=False))
+        val[k, :c] = rng.standard_normal(c).astype(np.float32)
+        counts[k] = c
+    got, want = run_average(cuda_lib, idx, val, counts, n)
+    np.testing.assert_array_equal(got, want)  # learner order kept: exact
+
+
+def test_sparse_average_of_dgc_messages(cuda_lib):
+    """The K = 4 messages of the small ResNet-50 layout after DGC step 1."""
+    import torch
+    gc = cuda_lib
+    w = wl.workload(2, small=True)
+    G = wl.gradients(w, 0)
+    d = gc.DGC(w.offsets, w.learners, w.density, w.momentum)
+    u = torch.zeros((w.learners, w.n), device="cuda")
+    v = torch.zeros((w.learners, w.n), device="cuda")
+    out, totals = d(G.cuda(), u, v)
+    torch.cuda.synchronize()
+    idx = gc.pair_indices(out).cpu().numpy().astype(np.uint32)
+    val = gc.pair_values(out).cpu().numpy()
+    run_average(gc, idx, val, totals.cpu().numpy(), w.n)
+
+
+def test_sparse_average_dense_lists(cuda_lib):
+    """Every index in every list (density 1): each output is a K-term sum."""
+    rng = np.random.default_rng(1)
+    K, n = 5, 9000
+    idx = np.tile(np.arange(n, dtype=np.uint32), (K, 1))
+    val = rng.standard_normal((K, n)).astype(np.float32)
+    got, want = run_average(cuda_lib, idx, val, np.full(K, n, np.int64), n)
+    np.testing.assert_array_equal(got, want)
+
+
+# ---------------------------------------------------------------------- DCD
+
+def run_dcd(gc, n, d, T, p, w=(1 / 3, 1 / 3, 1 / 3), gamma=0.1, seed=0x5EED):
+    import torch
+    rng = np.random.default_rng(n * 1000 + d)
+    x0 = (rng.standard_normal(d) * 1e-2).astype(np.float32)
+    x_o = np.tile(x0, (n, 1)).copy()
+    x_g = torch.from_numpy(x_o.copy()).cuda()
+    for t in range(T):
+        g = (rng.standard_normal((n, d)) * 1e-3).astype(np.float32)
+        oracle.dcd_step(x_o, g, w, gamma, p, seed, t)
+        gc.dcd_step(x_g, torch.from_numpy(g).cuda(), w, gamma, p, seed, t)
+    torch.cuda.synchronize()
+    got = x_g.cpu().numpy()
+    np.testing.assert_array_equal(got == x0[None, :], x_o == x0[None, :])  # identical keep masks
+    assert rel_err(got, x_o) <= VAL_RTOL
+
+
+def test_config5_small(cuda_lib):
+    """Ring of 8 nodes, d = 262,144, W = 1/3, gamma = 0.1, keep 1% scaled x100, 10 iterations."""
+    w = wl.workload(5, small=True)
+    run_dcd(cuda_lib, w.learners, w.n, w.steps, w.keep_p, w.ring_w, w.gamma, wl.dcd_seed(w))
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 5, 8, 9, 13])
+@pytest.mark.parametrize("d", [1, 7, 4096, 10001])
+def test_dcd_nodes_and_sizes(cuda_lib, n, d):
+    run_dcd(cuda_lib, n, d, 3, 0.3)
+
+
+def test_dcd_keep_all_and_weights(cuda_lib):
+    run_dcd(cuda_lib, 4, 5000, 2, 1.0, w=(0.25, 0.5, 0.25))
+    run_dcd(cuda_lib, 1, 5000, 2, 1.0, w=(0.0, 1.0, 0.0))
+
+
+def test_philox_matches_curand(cuda_lib):
+    """The library's and the oracle's keep draws are Philox4x32-10; cuRAND's
+    host generator (a library routine) gives the stream of counter i under
+    key seed as output words 4i..4i+3 -- when that holds, the oracle's
+    generator must reproduce it."""
+    import ctypes
+    cr = ctypes.CDLL("libcurand.so")
+    gen = ctypes.c_void_p()
+    assert cr.curandCreateGeneratorHost(ctypes.byref(gen), 106) == 0  # CURAND_RNG_PSEUDO_PHILOX4_32_10
+    seed = 0x123456789ABCDEF0
+    assert cr.curandSetPseudoRandomGeneratorSeed(gen, ctypes.c_ulonglong(seed)) == 0
+    buf = np.zeros(64, np.uint32)
+    assert cr.curandGenerate(gen, buf.ctypes.data_as(ctypes.c_void_p), ctypes.c_size_t(64)) == 0
+    cr.curandDestroyGenerator(gen)
+    key = [seed & 0xFFFFFFFF, seed >> 32]
+    mine = np.concatenate([oracle.philox4x32_10([i, 0, 0, 0], key) for i in range(16)])
+    if not np.array_equal(mine, buf):
+        pytest.skip("cuRAND's host stream uses another counter layout; the known-answer pins stand")
+    np.testing.assert_array_equal(mine, buf)

@@ -1,0 +1,193 @@
+"""DGC parity: the CUDA library against the CPU oracle, element by element.
+
+Indices, counts and the masked state are compared bit for bit; values within
+the 1e-6 relative tolerance of the contract (the kernels use the same
+per-operation fp32 rounding, so they are expected to be exact).
+"""
+import zlib
+
+import numpy as np
+import pytest
+
+import oracle
+from conftest import rel_err
+from gradient_compression_sgd_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+VAL_RTOL = 1e-6
+
+
+def run_dgc(gc, offsets, grads, density, momentum, clip_thr=0.0, clip_nodes=1, u0=None, v0=None):
+    """Step both sides through the gradient list and compare after every step."""
+    import torch
+    offsets = np.asarray(offsets, np.int64)
+    K, N = grads[0].shape
+    u_o = np.zeros((K, N), np.float32) if u0 is None else u0.copy()
+    v_o = np.zeros((K, N), np.float32) if v0 is None else v0.copy()
+    u_g = torch.from_numpy(u_o.copy()).cuda()
+    v_g = torch.from_numpy(v_o.copy()).cuda()
+    d = gc.DGC(offsets, K, density, momentum, clip_thr, clip_nodes)
+    for t, G in enumerate(grads):
+        idx_o, val_o, counts_o, _ = oracle.dgc_step(offsets, G, u_o, v_o, density, momentum, clip_thr, clip_nodes,
+                                                    cap=d.cap)
+        out, totals = d(torch.from_numpy(np.ascontiguousarray(G)).cuda(), u_g, v_g)
+        torch.cuda.synchronize()
+        counts_g = d.counts.cpu().numpy()
+        np.testing.assert_array_equal(counts_g, counts_o, err_msg=f"counts, step {t}")
+        assert list(totals.cpu().numpy()) == [int(counts_o[k].sum()) for k in range(K)]
+        idx_g = gc.pair_indices(out).cpu().numpy()
+        val_g = gc.pair_values(out).cpu().numpy()
+        for k in range(K):
+            n = int(counts_o[k].sum())
+            np.testing.assert_array_equal(idx_g[k, :n], idx_o[k, :n].astype(np.int64), err_msg=f"idx k={k} t={t}")
+            assert rel_err(val_g[k, :n], val_o[k, :n]) <= VAL_RTOL, f"values k={k} t={t}"
+        assert rel_err(u_g.cpu().numpy(), u_o) <= VAL_RTOL, f"u, step {t}"
+        assert rel_err(v_g.cpu().numpy(), v_o) <= VAL_RTOL, f"v, step {t}"
+        # masking: zero exactly at the sent indices
+        vg = v_g.cpu().numpy()
+        for k in range(K):
+            n = int(counts_o[k].sum())
+            assert not np.any(vg[k, idx_o[k, :n]])
+    return d
+
+
+def test_config1_dgc_single_tensor_with_clipping(cuda_lib):
+    """1,048,576 values N(0, 1e-3), density 0.001 (k = 1049), clip thr 1.0
+    (the norm is ~1.02, so clipping fires), momentum 0.9, 3 steps."""
+    w = wl.workload(1)
+    grads = [wl.gradients(w, t).numpy() for t in range(w.steps)]
+    d = run_dgc(cuda_lib, w.offsets, grads, w.density, w.momentum, w.clip_thr, w.clip_nodes)
+    assert d.cap == 1049
+
+
+@pytest.mark.parametrize("config", [2, 4])
+def test_small_configs(cuda_lib, config):
+    """The ResNet-50 layout at 1/8 width (161 tensors, K = 4, 5 steps) and the
+    GRU layout shrunk to 256x768 (K = 8, 10 steps)."""
+    w = wl.workload(config, small=True)
+    grads = [wl.gradients(w, t).numpy() for t in range(w.steps)]
+    run_dgc(cuda_lib, w.offsets, grads, w.density, w.momentum)
+
+
+EDGE_LAYOUTS = {
+    "single_1": [1],
+    "tiny": [3, 1, 2],
+    "empty_segments": [0, 5, 0, 0, 17, 0],
+    "tile_plus_one": [4097],
+    "misaligned": [7, 33, 65537, 12, 50001, 3],
+    "pool_segment": [40000],
+    "two_pool_segments_ragged": [100003, 70001],
+}
+
+
+@pytest.mark.parametrize("name", list(EDGE_LAYOUTS))
+@pytest.mark.parametrize("density", [0.001, 0.05, 1.0])
+def test_edge_layouts(cuda_lib, name, density):
+    sizes = EDGE_LAYOUTS[name]
+    off = wl.layout_offsets(sizes)
+    rng = np.random.default_rng(zlib.crc32(f"{name}/{density}".encode()))
+    K = 3
+    grads = [(rng.standard_normal((K, off[-1])) * rng.uniform(1e-4, 1e-1)).astype(np.float32) for _ in range(3)]
+    run_dgc(cuda_lib, off, grads, density, 0.9)
+
+
+@pytest.mark.parametrize("levels", [1, 3, 7])
+def test_ties_and_zeros(cuda_lib, levels):
+    """Few distinct magnitudes (and all-zero gradients for levels = 1): the
+    threshold value is shared by many entries and the lower indices must win."""
+    rng = np.random.default_rng(levels)
+    off = wl.layout_offsets([50000, 1000, 70000])
+    K = 2
+    grads = []
+    for t in range(3):
+        q = rng.integers(-(levels // 2), levels // 2 + 1, size=(K, off[-1])).astype(np.float32) * 0.25
+        grads.append(q)
+    run_dgc(cuda_lib, off, grads, 0.01, 0.0)
+    run_dgc(cuda_lib, off, grads, 0.003, 0.5)
+
+
+def test_hint_above_the_kth_value_falls_back(cuda_lib):
+    """Distinct large values only in the blocks the threshold sample reads, tiny
+    ones elsewhere: only the sampled rank-a values clear the candidate
+    threshold, fewer than k, so the select must fall back to the full
+    segment and still be exact.  (The sample layout mirrors the kernel's
+    plan: R = max(3k, 512), m = min(32 n / R, 8192) rounded down to 32,
+    blocks of 32 at stride n / (m / 32).)"""
+    n, density = 40000, 0.003
+    k = oracle.dgc_k(density, n)
+    R = max(3 * k, 512)
+    m = min(32 * n // R, 8192) & ~31
+    nblk, stride = m // 32, n // (m // 32)
+    G = np.full((1, n), 1e-6, np.float32)
+    pos = np.concatenate([np.arange(b * stride, b * stride + 32) for b in range(nblk)])
+    G[0, pos] = 1.0 + np.arange(len(pos), dtype=np.float32) / len(pos)
+    G[0, 30001:30050] = 0.5  # below the sampled values, above the rest
+    run_dgc(cuda_lib, [0, n], [G], density, 0.9)
+
+
+def test_nonzero_initial_state_and_momentum_zero(cuda_lib):
+    rng = np.random.default_rng(11)
+    off = wl.layout_offsets([1000, 200000, 36864])
+    K, N = 2, off[-1]
+    u0 = rng.standard_normal((K, N)).astype(np.float32) * 0.1
+    v0 = rng.standard_normal((K, N)).astype(np.float32)
+    grads = [rng.standard_normal((K, N)).astype(np.float32) for _ in range(2)]
+    run_dgc(cuda_lib, off, grads, 0.002, 0.9, u0=u0, v0=v0)
+    run_dgc(cuda_lib, off, grads, 0.002, 0.0, u0=u0, v0=v0)
+
+
+@pytest.mark.parametrize("nodes", [1, 4])
+def test_clipping_multi_learner(cuda_lib, nodes):
+    rng = np.random.default_rng(nodes)
+    off = wl.layout_offsets([300000, 5000])
+    K, N = 3, off[-1]
+    scale = np.array([1e-4, 1e-3, 1e-2], np.float32)[:, None]  # some learners clip, some do not
+    grads = [(rng.standard_normal((K, N)) * scale).astype(np.float32) for _ in range(3)]
+    run_dgc(cuda_lib, off, grads, 0.001, 0.9, clip_thr=1.0, clip_nodes=nodes)
+
+
+def test_checkpoint_resume_is_bit_identical(cuda_lib):
+    """The state is the caller's u and v: 3 steps straight equal 1 step, a
+    save/restore of (u, v) through host memory, then 2 more steps."""
+    import torch
+    gc = cuda_lib
+    w = wl.workload(2, small=True)
+    off = w.offsets
+    K, N = w.learners, w.n
+    grads = [wl.gradients(w, t).cuda() for t in range(3)]
+    d = gc.DGC(off, K, w.density, w.momentum)
+    u = torch.zeros((K, N), device="cuda")
+    v = torch.zeros((K, N), device="cuda")
+    outs = []
+    for t in range(3):
+        o, _ = d(grads[t], u, v)
+        outs.append(o.clone())
+    u2 = torch.zeros((K, N), device="cuda")
+    v2 = torch.zeros((K, N), device="cuda")
+    d2 = gc.DGC(off, K, w.density, w.momentum)
+    o0, _ = d2(grads[0], u2, v2)
+    saved = (u2.cpu().clone(), v2.cpu().clone())
+    u3, v3 = saved[0].cuda(), saved[1].cuda()
+    for t in (1, 2):
+        o, _ = d2(grads[t], u3, v3)
+        assert torch.equal(o, outs[t])
+    assert torch.equal(u3, u) and torch.equal(v3, v)
+
+
+def test_async_on_side_stream(cuda_lib):
+    """Calls enqueue on the given stream and never synchronise."""
+    import torch
+    gc = cuda_lib
+    off = wl.layout_offsets([100000, 3000])
+    K, N = 2, off[-1]
+    g = torch.randn((K, N), device="cuda") * 1e-3
+    u = torch.zeros((K, N), device="cuda")
+    v = torch.zeros((K, N), device="cuda")
+    d = gc.DGC(off, K, 0.01, 0.9)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        out, totals = d(g, u, v, stream=s)
+    s.synchronize()
+    assert int(totals[0]) == sum(gc.dgc_k(0.01, int(off[i + 1] - off[i])) for i in range(2))
