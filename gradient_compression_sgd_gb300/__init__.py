@@ -74,6 +74,7 @@ def lib():
         L.gcsgd_dgc_k.argtypes = [f64, i64]
         L.gcsgd_dgc_workspace_size.argtypes = [vp, i32, i32, f64, vp]
         L.dgc_compress.argtypes = [vp, i32, i32, vp, vp, vp, f64, f32, f32, i32, vp, i64, vp, vp, vp, sz, vp]
+        L.dgc_compress_noalloc.argtypes = [vp, i32, i32, vp, vp, vp, f64, f32, f32, i32, vp, i64, vp, vp, vp]
         L.gcsgd_adacomp_workspace_size.argtypes = [vp, i32, vp, i32, i64, vp]
         L.adacomp_compress.argtypes = [vp, i32, vp, i32, vp, vp, vp, i64, vp, vp, vp, vp, sz, vp]
         L.sparse_average.argtypes = [vp, i64, vp, i32, i64, vp, vp]
@@ -173,6 +174,26 @@ def dgc_compress(offsets, grad, u, v, out, counts, workspace, density, momentum,
         _dev(out, "out", torch.int32), int(cap), _dev(counts, "counts", torch.int64),
         _dev(totals, "totals", torch.int64), _dev(workspace, "workspace", torch.uint8), int(workspace.numel()),
         _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def dgc_compress_noalloc(offsets, grad, u, v, out, counts, density, momentum, clip_thr=0.0, clip_nodes=1,
+                         totals=None, stream=None):
+    """dgc_compress with the library's fixed scratch instead of a workspace, for
+    callers that may not allocate device memory (see dgc_compress_noalloc in
+    include/gcsgd.h: at most NOALLOC_SCRATCH_BYTES of scratch; overlapping
+    calls race on the shared scratch)."""
+    import torch
+    off = _offsets(offsets)
+    K = grad.shape[0]
+    cap = out.shape[1]
+    _check("dgc_compress_noalloc", lib().dgc_compress_noalloc(
+        _ptr(off), len(off) - 1, int(K), _dev(grad, "grad", torch.float32), _dev(u, "u", torch.float32),
+        _dev(v, "v", torch.float32), float(density), float(momentum), float(clip_thr), int(clip_nodes),
+        _dev(out, "out", torch.int32), int(cap), _dev(counts, "counts", torch.int64),
+        _dev(totals, "totals", torch.int64), _stream(stream)))
 
 
 class DGC:

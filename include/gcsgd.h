@@ -102,6 +102,33 @@ int dgc_compress(const int64_t* seg_offsets, int32_t n_seg, int32_t K,
                  gcsgd_pair* out, int64_t cap, int64_t* counts, int64_t* totals,
                  void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * dgc_compress without a workspace argument, for callers that cannot
+ * allocate device memory (for example a plugin whose host framework's caching
+ * allocator owns the device-memory budget, or a loop that must not enter the
+ * driver's allocator, which can block or synchronise, in the middle of a
+ * step).  The pages have no counterpart: this is a deployment variant of the
+ * same DGC step, with the same arguments and results as dgc_compress.
+ *
+ * Its scratch is a fixed array of GCSGD_NOALLOC_SCRATCH_BYTES built into the
+ * library; every GPU that loads the library holds it until the process
+ * exits.  A layout and K that need more scratch than that
+ * (gcsgd_dgc_workspace_size) are rejected with GCSGD_ERR_WORKSPACE before any
+ * GPU work.  The first call on a device looks up the array's device address
+ * (once per device, with that device current); make that first call before
+ * any stream capture.  The call allocates nothing (no cudaMalloc, no
+ * cudaFree).  All calls share the one array and leave their contents in it;
+ * nothing in it needs clearing between calls, but calls that overlap on the
+ * GPU (unordered streams, several host threads) race on it and must not be
+ * made.
+ */
+#define GCSGD_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int dgc_compress_noalloc(const int64_t* seg_offsets, int32_t n_seg, int32_t K,
+                         const float* grad, float* u, float* v,
+                         double density, float momentum, float clip_thr, int32_t clip_nodes,
+                         gcsgd_pair* out, int64_t cap, int64_t* counts, int64_t* totals,
+                         void* stream);
+
 /* -------------------------------------------------------------- AdaComp */
 
 /* Bytes of device workspace adacomp_compress needs.  lt: host [n_seg] bin
