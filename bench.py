@@ -51,7 +51,9 @@ def parse():
     ap.add_argument("--impl", default="gcsgd", choices=["gcsgd", "reference"])
     ap.add_argument("--config", type=int, default=2, choices=[2, 4],
                     help="2: ResNet-50 layout K=4 (the metric's workload); 4: GRU layout K=8")
+    ap.add_argument("--learners", type=int, default=0, help="override K (smaller cases for ncu captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement (ncu captures)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
     return ap.parse_args()
 
@@ -233,6 +235,9 @@ def run_gpu(args):
     gc.lib()
 
     w = wl.workload(args.config)
+    if args.learners:
+        w.learners = args.learners
+        w.name = f"{w.name.rsplit('_k', 1)[0]}_k{args.learners}"
     K, N = w.learners, w.n
     dev = torch.device("cuda", local)
     grads = [wl.gradients(w, t, device=dev) for t in range(N_SETS)]
@@ -280,37 +285,40 @@ def run_gpu(args):
     value = world * grad_bytes / (ms * 1e-3) / 1e9
 
     # end to end through the public API: pinned host gradient in, dense average out
-    host = [g.cpu().pin_memory() for g in grads[:2]]
-    gdev = torch.empty((K, N), device=dev)
-    avg_host = torch.empty(N, pin_memory=True)
-    u2 = torch.zeros((K, N), device=dev)
-    v2 = torch.zeros((K, N), device=dev)
+    e2e, ms_e2e = None, None
+    if not args.no_e2e:
+        host = [g.cpu().pin_memory() for g in grads[:2]]
+        gdev = torch.empty((K, N), device=dev)
+        avg_host = torch.empty(N, pin_memory=True)
+        u2 = torch.zeros((K, N), device=dev)
+        v2 = torch.zeros((K, N), device=dev)
 
-    def e2e_step(i):
-        gdev.copy_(host[i % 2], non_blocking=True)
-        out, totals = dgc(gdev, u2, v2)
-        gc.sparse_average(out, totals, N, avg)
-        avg_host.copy_(avg, non_blocking=True)
+        def e2e_step(i):
+            gdev.copy_(host[i % 2], non_blocking=True)
+            out, totals = dgc(gdev, u2, v2)
+            gc.sparse_average(out, totals, N, avg)
+            avg_host.copy_(avg, non_blocking=True)
 
-    for i in range(max(1, args.warmup)):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    f0 = torch.cuda.Event(enable_timing=True)
-    f1 = torch.cuda.Event(enable_timing=True)
-    e2e_steps = max(3, min(args.steps, 20))
-    f0.record(stream)
-    for i in range(e2e_steps):
-        e2e_step(i)
-    f1.record(stream)
-    torch.cuda.synchronize()
-    ms_e2e = f0.elapsed_time(f1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
-    e2e = world * grad_bytes / (ms_e2e * 1e-3) / 1e9
+        for i in range(max(1, args.warmup)):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        e2e_steps = max(3, min(args.steps, 20))
+        f0.record(stream)
+        for i in range(e2e_steps):
+            e2e_step(i)
+        f1.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = f0.elapsed_time(f1) / e2e_steps
+        if world > 1:
+            t = torch.tensor([ms_e2e], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        e2e = world * grad_bytes / (ms_e2e * 1e-3) / 1e9
+
 
     if rank != 0:
         if world > 1:
@@ -325,6 +333,7 @@ def run_gpu(args):
     achieved = upd_bytes / (upd_ms * 1e-3) / 1e9 if upd_ms > 0 else None
     traffic = profiled_traffic(w.name)
     sent = int(dgc.totals.sum().item())
+    select_paths = dgc.stats()
     step_bytes = DGC_BYTES_PER_ELEM * K * N + 8.0 * sent + 4.0 * N + 8.0 * sent
     kernels = {name: {"launches": c, "ms_per_launch": t / max(c, 1), "share": t / max(sum(x[1] for x in trace.values()), 1e-9)}
                for name, (c, t) in trace.items()}
@@ -348,8 +357,9 @@ def run_gpu(args):
                      "algorithmic_bytes_per_launch": upd_bytes, "traffic": traffic,
                      "frac_of_nominal_8tbs": (achieved / 8000.0) if achieved else None},
         "kernels": kernels,
-        "e2e": {"value": e2e, "unit": "GB/s", "ms_per_step": ms_e2e, "h2d_bytes_per_step": int(grad_bytes),
-                "d2h_bytes_per_step": int(4 * N)},
+        "select_paths": select_paths,
+        "e2e": None if e2e is None else {"value": e2e, "unit": "GB/s", "ms_per_step": ms_e2e,
+                                         "h2d_bytes_per_step": int(grad_bytes), "d2h_bytes_per_step": int(4 * N)},
         "gpu_launches": launches,
         "clocks": clk,
         "cpu_baseline": cpu,

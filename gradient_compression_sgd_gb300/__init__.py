@@ -39,6 +39,11 @@ class GcsgdError(RuntimeError):
         self.code = code
 
 
+class DgcStats(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int64) for name in
+                ("units", "empty", "raw", "pool", "pool_global", "raw_global", "hint_failed")]
+
+
 class TraceEntry(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int64), ("total_ms", ctypes.c_double)]
 
@@ -75,6 +80,7 @@ def lib():
         L.gcsgd_dgc_workspace_size.argtypes = [vp, i32, i32, f64, vp]
         L.dgc_compress.argtypes = [vp, i32, i32, vp, vp, vp, f64, f32, f32, i32, vp, i64, vp, vp, vp, sz, vp]
         L.dgc_compress_noalloc.argtypes = [vp, i32, i32, vp, vp, vp, f64, f32, f32, i32, vp, i64, vp, vp, vp]
+        L.gcsgd_dgc_stats.argtypes = [vp, i32, i32, f64, vp, vp, vp]
         L.gcsgd_adacomp_workspace_size.argtypes = [vp, i32, vp, i32, i64, vp]
         L.adacomp_compress.argtypes = [vp, i32, vp, i32, vp, vp, vp, i64, vp, vp, vp, vp, sz, vp]
         L.sparse_average.argtypes = [vp, i64, vp, i32, i64, vp, vp]
@@ -211,6 +217,14 @@ class DGC:
         self.out = pairs_buffer(K, self.cap, device)
         self.counts = torch.zeros((K, self.S), dtype=torch.int64, device=device)
         self.totals = torch.zeros(K, dtype=torch.int64, device=device)
+
+    def stats(self, stream=None) -> dict:
+        """How the last call selected each (learner, segment) (gcsgd_dgc_stats; synchronises)."""
+        st = DgcStats()
+        _check("gcsgd_dgc_stats", lib().gcsgd_dgc_stats(
+            _ptr(self.offsets), self.S, self.K, self.density, ctypes.c_void_p(self.workspace.data_ptr()),
+            _stream(stream), ctypes.byref(st)))
+        return {name: int(getattr(st, name)) for name, _ in DgcStats._fields_}
 
     def __call__(self, grad, u, v, stream=None):
         dgc_compress(self.offsets, grad, u, v, self.out, self.counts, self.workspace, self.density,

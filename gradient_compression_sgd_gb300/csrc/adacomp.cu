@@ -191,9 +191,9 @@ __global__ void __launch_bounds__(NT) ada_bigmax(const SegPlan* __restrict__ pla
                                                  const float* __restrict__ dW, const float* __restrict__ R,
                                                  uint32_t* __restrict__ big, uint64_t big_per_learner) {
     const int lane = threadIdx.x & 31;
-    for (uint64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-        const uint32_t k = (uint32_t)(t / tiles_per_learner);
-        const uint32_t lt = (uint32_t)(t - (uint64_t)k * tiles_per_learner);
+    for (uint32_t t = blockIdx.x; t < (uint32_t)total_tiles; t += gridDim.x) {
+        const uint32_t k = t / tiles_per_learner;
+        const uint32_t lt = t - k * tiles_per_learner;
         const int s = find_segment_by_tile(plan, S, lt);
         const SegPlan p = plan[s];
         if (p.mode != kModeBig) continue;
@@ -227,9 +227,9 @@ __global__ void __launch_bounds__(NT, 2) ada_bins(const SegPlan* __restrict__ pl
     __shared__ uint64_t scan[NT / 32 + 1];
     __shared__ uint32_t s_base;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (uint64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-        const uint32_t k = (uint32_t)(t / tiles_per_learner);
-        const uint32_t lt = (uint32_t)(t - (uint64_t)k * tiles_per_learner);
+    for (uint32_t t = blockIdx.x; t < (uint32_t)total_tiles; t += gridDim.x) {
+        const uint32_t k = t / tiles_per_learner;
+        const uint32_t lt = t - k * tiles_per_learner;
         const int s = find_segment_by_tile(plan, S, lt);
         const SegPlan p = plan[s];
         const uint32_t tj = lt - p.tile_off;
@@ -469,8 +469,8 @@ __global__ void __launch_bounds__(NT) ada_emit(const SegPlan* __restrict__ plan,
     for (uint64_t t = t0; t < t1; ++t) {
         const uint2 ent = tile_tab[t];
         if (ent.y == 0) continue;
-        const uint32_t k = (uint32_t)(t / tiles_per_learner);
-        const uint32_t lt = (uint32_t)(t - (uint64_t)k * tiles_per_learner);
+        const uint32_t k = (uint32_t)t / tiles_per_learner;
+        const uint32_t lt = (uint32_t)t - k * tiles_per_learner;
         const int s = find_segment_by_tile(plan, S, lt);
         if ((int)k != cur_k || s != cur_s) {
             int64_t before = 0, all = 0;
@@ -525,6 +525,8 @@ int adacomp_launch(const int64_t* off, int S, const int32_t* lt, int K, const fl
         return set_error(GCSGD_ERR_WORKSPACE, "adacomp_compress: workspace of %zu bytes, %zu needed", ws_bytes, need);
     const uint64_t N = (uint64_t)off[S];
     const uint64_t T = (uint64_t)K * hp.tiles_per_learner;
+    if (T >= ((uint64_t)1 << 32))
+        return set_error(GCSGD_ERR_INVALID_ARG, "adacomp_compress: K * tiles = %llu exceeds 2^32", (unsigned long long)T);
     int rc;
     {
         LaunchScope ls("ada_plan", stream);

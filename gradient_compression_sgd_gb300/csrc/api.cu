@@ -210,6 +210,15 @@ int dgc_compress(const int64_t* seg_offsets, int32_t n_seg, int32_t K, const flo
                       totals, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
+int gcsgd_dgc_stats(const int64_t* seg_offsets, int32_t n_seg, int32_t K, double density, const void* workspace,
+                    void* stream, gcsgd_dgc_stats_t* out) {
+    int rc;
+    if ((rc = check_layout("gcsgd_dgc_stats", seg_offsets, n_seg))) return rc;
+    if (K < 1 || !workspace || !out || !(density > 0.0 && density <= 1.0))
+        return set_error(GCSGD_ERR_INVALID_ARG, "gcsgd_dgc_stats: bad argument");
+    return dgc_collect_stats(seg_offsets, n_seg, K, density, workspace, (cudaStream_t)stream, out);
+}
+
 int gcsgd_adacomp_workspace_size(const int64_t* seg_offsets, int32_t n_seg, const int32_t* lt, int32_t K,
                                  int64_t cap, size_t* bytes) {
     const char* fn = "gcsgd_adacomp_workspace_size";

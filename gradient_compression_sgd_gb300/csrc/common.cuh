@@ -81,7 +81,6 @@ struct SelectResult {
 template <int NT, class Load>
 __device__ SelectResult radix_select_desc(Load load, uint64_t count, uint32_t rank,
                                           uint32_t* hist, uint64_t* scan, uint32_t* sel) {
-    const int lane = threadIdx.x & 31;
     uint32_t prefix = 0, pmask = 0, need = rank, greater = 0;
 #pragma unroll 1
     for (int pass = 0; pass < 3; ++pass) {
@@ -90,17 +89,18 @@ __device__ SelectResult radix_select_desc(Load load, uint64_t count, uint32_t ra
         for (int b = threadIdx.x; b < nb; b += NT) hist[b] = 0;
         if (threadIdx.x == 0) { sel[0] = 0; sel[1] = 0; }
         __syncthreads();
-        for (uint64_t base = 0; base < count; base += NT) {
-            const uint64_t i = base + threadIdx.x;
-            uint32_t key = 0;
-            bool p = (i < count) && load(i, &key);
-            p = p && ((key & pmask) == prefix);
-            const uint32_t bkt = (key >> shift) & (uint32_t)(nb - 1);
-            const unsigned am = __ballot_sync(kFull, p);
-            if (p) {
-                const unsigned grp = __match_any_sync(am, bkt);
-                if (lane == __ffs(grp) - 1) atomicAdd(&hist[bkt], (uint32_t)__popc(grp));
+        for (uint64_t base = 0; base < count; base += 4 * (uint64_t)NT) {
+            uint32_t key[4];
+            bool ok[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {  // four independent loads in flight
+                const uint64_t i = base + (uint64_t)j * NT + threadIdx.x;
+                key[j] = 0;
+                ok[j] = (i < count) && load(i, &key[j]);
             }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (ok[j] && ((key[j] & pmask) == prefix)) atomicAdd(&hist[(key[j] >> shift) & (uint32_t)(nb - 1)], 1u);
         }
         __syncthreads();
         // thread t owns buckets [hi - w, hi) counted from the top

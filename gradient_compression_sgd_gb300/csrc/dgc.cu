@@ -8,23 +8,27 @@
 //
 // Launch sequence of one call (all on the caller's stream, no host sync):
 //   [dgc_sumsq]   per-learner sum of squares, only when clipping is on
-//   dgc_plan      one CTA: per-segment plan (k_s, tiles, pool sizes, offsets)
-//                 and, when clipping is on, the clip scale of each learner
-//   dgc_hint      one CTA per (learner, segment): a strided sample of the
-//                 updated |v| gives a threshold hint safely below the k-th
-//                 largest value
+//   dgc_prepare   one CTA per (learner, segment) plus one: the extra CTA
+//                 writes the per-segment plan (k_s, tiles, pool sizes and
+//                 offsets) and each learner's clip scale; the others read a
+//                 strided sample of the updated |v| of their segment and take
+//                 a threshold hint safely below the k-th largest value
 //   dgc_update    the bandwidth-bound pass: reads g, u, v once (128-bit
 //                 loads), writes u', v' once, and appends every |v'| >= hint
 //                 to a small per-(learner, segment) candidate pool, keeping
 //                 index order inside each 4096-element tile
-//   dgc_select    one CTA per (learner, segment): exact radix select of the
-//                 k-th largest |v'| among the candidates (or, if the hint
-//                 failed, among all of the segment's v'), then the ordered
-//                 emission of (index, v') with ties to the lower index, and
-//                 the masking u = v = 0 at the sent indices.
+//   dgc_select    one CTA per (learner, segment): stages the candidates (in
+//                 index order, through the tile table) or, for small segments
+//                 and when the hint failed, the segment's v' in shared memory,
+//                 finds the k-th largest |v'| exactly by radix select, then
+//                 emits (index, v') in index order with ties to the lower
+//                 index and masks u = v = 0 at the sent indices.
 // The answer never depends on the hint: a pool is used only when it provably
 // contains every entry of the top k (at least k candidates, no overflow).
 #include <math.h>
+#include <string.h>
+
+#include <vector>
 
 #include "common.cuh"
 #include "dgc.cuh"
@@ -32,15 +36,23 @@
 namespace gcsgd {
 namespace dgc {
 
-constexpr int NT = 256;                 // threads per CTA in every DGC kernel
-constexpr int kTile = 4096;             // elements per dgc_update tile (NT x 4 float4)
-constexpr uint32_t kRawMax = 32768;     // segments up to this size select from v' directly
-constexpr uint32_t kSampleMax = 8192;   // largest hint sample (keys held in shared memory)
-constexpr uint32_t kSampleAbove = 32;   // sampled entries expected above the hint
-constexpr uint32_t kPoolFloor = 512;    // smallest expected candidate count
-constexpr int kSumsqBlocks = 128;       // CTAs per learner in dgc_sumsq
+constexpr int NT = 256;                  // threads per CTA of dgc_update and dgc_sumsq
+constexpr int NTS = 512;                 // threads per CTA of dgc_select
+constexpr int NTP = 256;                 // threads per CTA of dgc_prepare
+constexpr int kHintBits = 12;            // hint histogram: top 12 bits of |v| (1/16 of a binade)
+constexpr uint32_t kSmallK = 32;         // raw segments with k <= 32 ...
+constexpr uint32_t kSmallN = 8192;       // ... and at most 8192 values use the register top-k
+constexpr int kTile = 4096;              // elements per dgc_update tile (NT x 4 float4)
+constexpr uint32_t kRawMax = 16384;      // segments up to this size select from v' directly
+constexpr uint32_t kSampleMax = 16384;   // largest hint sample (keys held in shared memory)
+constexpr uint32_t kSampleAbove = 48;    // sampled entries expected above the hint
+constexpr uint32_t kPoolFloor = 512;     // smallest expected candidate count
+constexpr uint32_t kStageItems = 8192;   // candidates dgc_select stages in shared memory
+constexpr size_t kStageBytes = kStageItems * sizeof(uint2);  // also holds kRawMax floats
+static_assert(kStageBytes >= kRawMax * sizeof(float), "the stage must hold a raw segment");
+constexpr int kSumsqBlocks = 128;        // CTAs per learner in dgc_sumsq
 
-__host__ __device__ inline void seg_fields(uint32_t n, double density, SegPlan* p) {
+__host__ __device__ __forceinline__ void seg_fields(uint32_t n, double density, SegPlan* p) {
     p->n = n;
     p->k = dgc_k_of(density, n);
     p->ntiles = (n + kTile - 1) / kTile;
@@ -49,11 +61,11 @@ __host__ __device__ inline void seg_fields(uint32_t n, double density, SegPlan* 
     p->a = 0;
     if (n == 0) {
         p->kind = kKindEmpty;
-    } else if (n <= kRawMax || 3ull * p->k > n / 2) {
+    } else if (n <= kRawMax || 5ull * p->k / 2 > n / 2) {
         p->kind = kKindRaw;
     } else {
         p->kind = kKindPool;
-        const uint64_t R = 3ull * p->k > kPoolFloor ? 3ull * p->k : kPoolFloor;  // expected candidates
+        const uint64_t R = 5ull * p->k / 2 > kPoolFloor ? 5ull * p->k / 2 : kPoolFloor;  // expected candidates
         const uint64_t cap = 4 * R + 256;
         p->cap = (uint32_t)(cap < n ? cap : n);
         uint64_t m = (uint64_t)kSampleAbove * n / R;
@@ -109,64 +121,22 @@ __global__ void __launch_bounds__(NT) dgc_sumsq(const float* __restrict__ grad, 
     }
 }
 
-// One CTA: the per-segment plan (prefix sums of pool sizes, tiles and
-// message lengths) and each learner's clip scale.
-template <int MAXS>
-__global__ void __launch_bounds__(1024) dgc_plan(SegOffsets<MAXS> so, int S, int K, double density,
-                                                 float clip_thr, int clip_nodes, int nparts,
-                                                 const double* __restrict__ part, SegPlan* __restrict__ plan,
-                                                 float* __restrict__ clip_c) {
-    __shared__ uint64_t scan[1024 / 32 + 1];
-    __shared__ uint64_t carry[3];
-    if (threadIdx.x < 3) carry[threadIdx.x] = 0;
-    __syncthreads();
-    for (int base = 0; base < S; base += 1024) {
-        const int s = base + (int)threadIdx.x;
-        SegPlan p;
-        const bool live = s < S;
-        seg_fields(live ? so.off[s + 1] - so.off[s] : 0u, density, &p);
-        p.off = live ? so.off[s] : 0u;
-        uint64_t tot;
-        const uint64_t ex_pool = block_exclusive_scan<1024>(live ? p.cap : 0, scan, &tot);
-        const uint64_t c0 = carry[0];
-        __syncthreads();
-        if (threadIdx.x == 0) carry[0] = c0 + tot;
-        const uint64_t ex_tile = block_exclusive_scan<1024>(live ? p.ntiles : 0, scan, &tot);
-        const uint64_t c1 = carry[1];
-        __syncthreads();
-        if (threadIdx.x == 0) carry[1] = c1 + tot;
-        const uint64_t ex_out = block_exclusive_scan<1024>(live ? p.k : 0, scan, &tot);
-        const uint64_t c2 = carry[2];
-        __syncthreads();
-        if (threadIdx.x == 0) carry[2] = c2 + tot;
-        if (live) {
-            p.pool_off = (uint32_t)(c0 + ex_pool);
-            p.tile_off = (uint32_t)(c1 + ex_tile);
-            p.out_off = (uint32_t)(c2 + ex_out);
-            p.pad = 0;
-            plan[s] = p;
-        }
-        __syncthreads();
+// Local gradient clipping scale (Appendix C): thr_k = thr / sqrt(N_nodes),
+// c = thr_k / ||G|| when ||G|| > thr_k.  The per-CTA partial sums of squares
+// are combined in a fixed order with compensated summation, so every CTA that
+// evaluates this gets the same c.
+__device__ float clip_scale(const double* __restrict__ part, int k, float clip_thr, int clip_nodes) {
+    if (!(clip_thr > 0.0f)) return 1.0f;
+    double s = 0.0, comp = 0.0;
+    for (int i = 0; i < kSumsqBlocks; ++i) {
+        const double x = part[(uint64_t)k * kSumsqBlocks + i];
+        const double t = s + x;
+        comp += fabs(s) >= fabs(x) ? (s - t) + x : (x - t) + s;
+        s = t;
     }
-    // local gradient clipping scale (Appendix C): thr_k = thr / sqrt(N_nodes);
-    // c = thr_k / ||G|| when ||G|| > thr_k.  Partial sums are combined in a
-    // fixed order with compensated summation.
-    for (int k = threadIdx.x; k < K; k += 1024) {
-        float c = 1.0f;
-        if (clip_thr > 0.0f) {
-            double s = 0.0, comp = 0.0;
-            for (int i = 0; i < nparts; ++i) {
-                const double x = part[(uint64_t)k * nparts + i];
-                const double t = s + x;
-                comp += fabs(s) >= fabs(x) ? (s - t) + x : (x - t) + s;
-                s = t;
-            }
-            const double norm = sqrt(s + comp);
-            const double thr_k = (double)clip_thr / sqrt((double)clip_nodes);
-            if (norm > thr_k) c = (float)(thr_k / norm);
-        }
-        clip_c[k] = c;
-    }
+    const double norm = sqrt(s + comp);
+    const double thr_k = (double)clip_thr / sqrt((double)clip_nodes);
+    return norm > thr_k ? (float)(thr_k / norm) : 1.0f;
 }
 
 // The update of one element: u' = m*u + c*g, v' = v + u'.
@@ -175,41 +145,175 @@ __device__ __forceinline__ void dgc_elem(float g, float& u, float& v, float m, f
     v = __fadd_rn(v, u);
 }
 
-// One CTA per (learner, segment).  Samples kSampleAbove/R of the segment in
-// 32-element blocks, computes the updated |v| there exactly as dgc_update
-// will, and takes the a-th largest sampled key as the candidate threshold.
-__global__ void __launch_bounds__(NT) dgc_hint(const SegPlan* __restrict__ plan, int S, uint64_t N,
-                                               const float* __restrict__ grad, const float* __restrict__ u,
-                                               const float* __restrict__ v, float momentum,
-                                               const float* __restrict__ clip_c, uint32_t* __restrict__ hint,
-                                               uint32_t* __restrict__ pool_cnt) {
-    __shared__ uint32_t keys[kSampleMax];
-    __shared__ uint32_t hist[2048];
-    __shared__ uint64_t scan[NT / 32 + 1];
-    __shared__ uint32_t sel[4];
-    const int unit = blockIdx.x;
-    const int k = unit / S, s = unit - k * S;
-    const SegPlan p = plan[s];
-    if (threadIdx.x == 0) pool_cnt[unit] = 0;
-    if (p.kind != kKindPool) {
-        if (threadIdx.x == 0) hint[unit] = 0xffffffffu;  // no candidates
-        return;
-    }
-    const float c = clip_c[k];
-    const uint32_t nblk = p.m / 32;
-    const uint32_t stride = p.n / nblk;  // >= 512 since m <= n / 16
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint64_t base = (uint64_t)k * N + p.off;
-    for (uint32_t b = warp; b < nblk; b += NT / 32) {
-        const uint64_t i = base + (uint64_t)b * stride + lane;
-        float uu = __ldg(u + i), vv = __ldg(v + i);
-        dgc_elem(__ldg(grad + i), uu, vv, momentum, c);
-        keys[b * 32 + lane] = mag_key(vv);
+// Lower edge of the histogram bucket that holds the rank-th largest counted
+// key (buckets from the top); *above receives the count in higher buckets.
+// hist has NB buckets; every thread of the CTA must call it.
+template <int NT, int NB>
+__device__ uint32_t crossing_bucket(const uint32_t* hist, uint32_t rank, uint64_t* scan, uint32_t* s_out,
+                                    uint32_t* above_out) {
+    constexpr int W = NB / NT;
+    const int hi = NB - (int)threadIdx.x * W;
+    uint32_t mine = 0;
+    for (int b = hi - 1; b >= hi - W; --b) mine += hist[b];
+    uint64_t tot;
+    uint32_t above = (uint32_t)block_exclusive_scan<NT>(mine, scan, &tot);
+    if (threadIdx.x == 0) {
+        s_out[0] = 0;
+        s_out[1] = 0;
     }
     __syncthreads();
-    const SelectResult r = radix_select_desc<NT>(
-        [&](uint64_t i, uint32_t* key) { *key = keys[i]; return true; }, p.m, p.a, hist, scan, sel);
-    if (threadIdx.x == 0) hint[unit] = r.thresh > 1u ? r.thresh : 1u;
+    for (int b = hi - 1; b >= hi - W; --b) {
+        const uint32_t h = hist[b];
+        if (above < rank && rank <= above + h) {
+            s_out[0] = (uint32_t)b;
+            s_out[1] = above;
+        }
+        above += h;
+    }
+    __syncthreads();
+    const uint32_t r = s_out[0];
+    *above_out = s_out[1];
+    __syncthreads();
+    return r;
+}
+
+// CTA 0 first writes the per-segment plan, the clip scales and the order in
+// which dgc_select takes the segments (largest first).  Then the CTAs walk
+// the (learner, segment) units with a grid stride: a segment with a
+// candidate pool samples m of its values in 32-element blocks spread evenly
+// over it and computes the updated |v| there exactly as dgc_update will.  The
+// hint is the a-th largest sampled key (a = R m / n for R = max(2.5k, 512)
+// expected candidates), located by a 12-bit histogram of the keys and a
+// second 12-bit histogram inside the bucket that holds it, and rounded down
+// to that second bucket's edge (within 2^-16 of the sample).  Being a rank
+// estimate, it keeps the candidate count near R whatever the distribution of
+// |v| -- including the pile-up of entries just below the send threshold that
+// accumulation builds.  The hint only steers speed: dgc_select checks that
+// the pool holds the top k.
+template <int MAXS>
+__global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, int S, int K, double density,
+                                                     float clip_thr, int clip_nodes, const double* __restrict__ part,
+                                                     SegPlan* __restrict__ plan, float* __restrict__ clip_c,
+                                                     uint16_t* __restrict__ order, uint64_t N,
+                                                     const float* __restrict__ grad, const float* __restrict__ u,
+                                                     const float* __restrict__ v, float momentum,
+                                                     uint32_t* __restrict__ hint, uint32_t* __restrict__ pool_cnt) {
+    constexpr int NB = 1 << kHintBits;
+    extern __shared__ __align__(16) uint32_t keys[];  // kSampleMax
+    __shared__ uint32_t hist[NB];
+    __shared__ uint64_t scan[NTP / 32 + 1];
+    __shared__ uint64_t carry[3];
+    __shared__ SegPlan s_p;
+    __shared__ float s_c;
+    __shared__ uint32_t s_sel[2];
+    if (blockIdx.x == 0) {
+        if (threadIdx.x < 3) carry[threadIdx.x] = 0;
+        __syncthreads();
+        for (int base = 0; base < S; base += NTP) {
+            const int s = base + (int)threadIdx.x;
+            SegPlan p;
+            const bool live = s < S;
+            seg_fields(live ? so.off[s + 1] - so.off[s] : 0u, density, &p);
+            p.off = live ? so.off[s] : 0u;
+            uint64_t tot;
+            const uint64_t ex_pool = block_exclusive_scan<NTP>(live ? p.cap : 0, scan, &tot);
+            const uint64_t c0 = carry[0];
+            __syncthreads();
+            if (threadIdx.x == 0) carry[0] = c0 + tot;
+            const uint64_t ex_tile = block_exclusive_scan<NTP>(live ? p.ntiles : 0, scan, &tot);
+            const uint64_t c1 = carry[1];
+            __syncthreads();
+            if (threadIdx.x == 0) carry[1] = c1 + tot;
+            const uint64_t ex_out = block_exclusive_scan<NTP>(live ? p.k : 0, scan, &tot);
+            const uint64_t c2 = carry[2];
+            __syncthreads();
+            if (threadIdx.x == 0) carry[2] = c2 + tot;
+            if (live) {
+                p.pool_off = (uint32_t)(c0 + ex_pool);
+                p.tile_off = (uint32_t)(c1 + ex_tile);
+                p.out_off = (uint32_t)(c2 + ex_out);
+                p.pad = 0;
+                plan[s] = p;
+                // rank by size, largest first (ties: lower index first)
+                const uint32_t ns = so.off[s + 1] - so.off[s];
+                uint32_t rank = 0;
+                for (int q = 0; q < S; ++q) {
+                    const uint32_t nq = so.off[q + 1] - so.off[q];
+                    rank += nq > ns || (nq == ns && q < s);
+                }
+                order[rank] = (uint16_t)s;
+            }
+            __syncthreads();
+        }
+        for (int k = threadIdx.x; k < K; k += NTP) clip_c[k] = clip_scale(part, k, clip_thr, clip_nodes);
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int unit = blockIdx.x; unit < K * S; unit += gridDim.x) {
+        const int k = unit / S, s = unit - k * S;
+        if (threadIdx.x == 0) {  // one thread evaluates the plan (fp64 and 64-bit integer math)
+            seg_fields(so.off[s + 1] - so.off[s], density, &s_p);
+            s_p.off = so.off[s];
+            s_c = s_p.kind == kKindPool ? clip_scale(part, k, clip_thr, clip_nodes) : 1.0f;
+            pool_cnt[unit] = 0;
+            if (s_p.kind != kKindPool) hint[unit] = 0xffffffffu;  // no candidates
+        }
+        for (int b = threadIdx.x; b < NB; b += NTP) hist[b] = 0;
+        __syncthreads();
+        const SegPlan p = s_p;
+        if (p.kind != kKindPool) {
+            __syncthreads();
+            continue;
+        }
+        const float c = s_c;
+        const uint32_t nblk = p.m / 32;
+        const uint32_t stride = p.n / nblk;  // >= 512 since m <= n / 16
+        const uint64_t base = (uint64_t)k * N + p.off;
+        const float* gs = grad + base;
+        const float* us = u + base;
+        const float* vs = v + base;
+        // sample element 32 b + lane sits at b * stride + lane; a warp issues
+        // the loads of 12 blocks before using any of them
+        constexpr int kB = 12;
+        for (uint32_t b0 = warp; b0 < nblk; b0 += kB * (NTP / 32)) {
+            float gg[kB], uu[kB], vv[kB];
+#pragma unroll
+            for (int j = 0; j < kB; ++j) {
+                const uint32_t b = b0 + j * (NTP / 32);
+                gg[j] = uu[j] = vv[j] = 0.0f;
+                if (b < nblk) {
+                    const uint32_t i = b * stride + lane;
+                    gg[j] = __ldg(gs + i);
+                    uu[j] = __ldg(us + i);
+                    vv[j] = __ldg(vs + i);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kB; ++j) {
+                const uint32_t b = b0 + j * (NTP / 32);
+                if (b < nblk) {
+                    dgc_elem(gg[j], uu[j], vv[j], momentum, c);
+                    const uint32_t key = mag_key(vv[j]);
+                    keys[b * 32 + lane] = key;
+                    atomicAdd(&hist[key >> (31 - kHintBits)], 1u);
+                }
+            }
+        }
+        __syncthreads();
+        uint32_t above;
+        const uint32_t b1 = crossing_bucket<NTP, NB>(hist, p.a, scan, s_sel, &above);
+        const uint32_t need = p.a - above;
+        for (int b = threadIdx.x; b < NB; b += NTP) hist[b] = 0;
+        __syncthreads();
+        for (uint32_t i = threadIdx.x; i < p.m; i += NTP) {
+            const uint32_t key = keys[i];
+            if ((key >> (31 - kHintBits)) == b1) atomicAdd(&hist[(key >> (31 - 2 * kHintBits)) & (NB - 1)], 1u);
+        }
+        __syncthreads();
+        const uint32_t b2 = crossing_bucket<NTP, NB>(hist, need, scan, s_sel, &above);
+        const uint32_t h = (b1 << (31 - kHintBits)) | (b2 << (31 - 2 * kHintBits));
+        if (threadIdx.x == 0) hint[unit] = h > 1u ? h : 1u;
+        __syncthreads();
+    }
 }
 
 __device__ __forceinline__ int find_segment_by_tile(const SegPlan* plan, int S, uint32_t lt) {
@@ -236,9 +340,9 @@ __global__ void __launch_bounds__(NT, 3) dgc_update(const SegPlan* __restrict__ 
                                                     uint2* __restrict__ pool, uint64_t pool_per_learner) {
     __shared__ uint64_t scan[NT / 32 + 1];
     __shared__ uint32_t s_base;
-    for (uint64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-        const uint32_t k = (uint32_t)(t / tiles_per_learner);
-        const uint32_t lt = (uint32_t)(t - (uint64_t)k * tiles_per_learner);
+    for (uint32_t t = blockIdx.x; t < (uint32_t)total_tiles; t += gridDim.x) {
+        const uint32_t k = t / tiles_per_learner;
+        const uint32_t lt = t - k * tiles_per_learner;
         const int s = find_segment_by_tile(plan, S, lt);
         const SegPlan p = plan[s];
         const uint32_t start = (lt - p.tile_off) * (uint32_t)kTile;
@@ -332,21 +436,193 @@ __global__ void __launch_bounds__(NT, 3) dgc_update(const SegPlan* __restrict__ 
     }
 }
 
+// Ordered emission over `count` items given in ascending index order, four
+// consecutive items per thread per round: an item is sent if its key > T, or
+// == T and fewer than `ties` equal keys precede it; its slot is (#greater
+// before it) + min(#equal before it, ties).  Sent items are written to dst and
+// u = v = 0 at their indices (momentum factor masking).
+template <class Get>
+__device__ void emit_in_order(Get get, uint32_t count, uint32_t T, uint32_t greater, uint32_t ties,
+                              const SegPlan& p, gcsgd_pair* __restrict__ dst, float* __restrict__ u,
+                              float* __restrict__ v, uint64_t ebase, uint64_t* scan) {
+    uint32_t run_gt = 0, run_eq = 0;
+    for (uint32_t cb = 0; cb < count; cb += 4 * NTS) {
+        const uint32_t i0 = cb + 4 * threadIdx.x;
+        uint32_t loc[4], bits[4];
+        uint32_t ngt = 0, neq = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            loc[j] = 0xffffffffu;
+            bits[j] = 0;
+            if (i0 + j < count) get(i0 + j, &loc[j], &bits[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (i0 + j < count) {
+                const uint32_t key = bits[j] & 0x7fffffffu;
+                ngt += key > T;
+                neq += key == T;
+            }
+        }
+        uint64_t tot;
+        const uint64_t ex = block_exclusive_scan<NTS>((uint64_t)ngt | ((uint64_t)neq << 32), scan, &tot);
+        uint32_t gb = run_gt + (uint32_t)ex, eb = run_eq + (uint32_t)(ex >> 32);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (i0 + j >= count) break;
+            const uint32_t key = bits[j] & 0x7fffffffu;
+            const bool gt = key > T, eq = key == T;
+            const uint32_t slot = gb + (eb < ties ? eb : ties);
+            if ((gt || (eq && eb < ties)) && slot < p.k && loc[j] < p.n) {
+                gcsgd_pair pr;
+                pr.idx = p.off + loc[j];
+                pr.val = __uint_as_float(bits[j]);
+                dst[slot] = pr;
+                u[ebase + loc[j]] = 0.0f;
+                v[ebase + loc[j]] = 0.0f;
+            }
+            gb += gt;
+            eb += eq;
+        }
+        run_gt += (uint32_t)tot;
+        run_eq += (uint32_t)(tot >> 32);
+        if (run_gt >= greater && run_eq >= ties) break;  // all k sent
+    }
+}
+
+// Largest 64-bit value across a warp.
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t x) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+        const uint64_t y = __shfl_xor_sync(kFull, x, d);
+        x = y > x ? y : x;
+    }
+    return x;
+}
+
+// Exact top-k for a segment of n <= kSmallN values and k <= kSmallK, held in
+// registers (thread t owns elements t + j NTS).  The order key packs
+// (|v| bits, ~index) into 64 bits, so the largest key is the largest
+// magnitude with ties to the lower index and all keys are distinct.  Each
+// warp takes its own top k by k rounds of warp max (only the winning thread
+// rescans its elements); warp 0 merges the 16 warps' candidates the same
+// way; the k winners go out in index order and u = v = 0 there.
+__device__ void small_topk(const SegPlan& p, const float* __restrict__ vseg, float* __restrict__ u,
+                           float* __restrict__ v, uint64_t ebase, gcsgd_pair* __restrict__ dst, uint64_t* cand,
+                           uint64_t* win) {
+    constexpr int J = kSmallN / NTS;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t jn = (p.n + NTS - 1) / NTS;  // elements per thread in use (uniform)
+    uint32_t mag[J];
+    uint32_t live = 0;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        mag[j] = 0;
+        const uint32_t i = threadIdx.x + j * NTS;
+        if ((uint32_t)j < jn && i < p.n) {
+            mag[j] = mag_key(vseg[i]);
+            live |= 1u << j;
+        }
+    }
+    auto best_of = [&]() {
+        uint64_t b = 0;
+#pragma unroll
+        for (int j = 0; j < J; ++j)
+            if ((live >> j) & 1u) {
+                const uint64_t key = ((uint64_t)mag[j] << 32) | (uint32_t)~(threadIdx.x + j * NTS);
+                b = key > b ? key : b;
+            }
+        return b;
+    };
+    uint64_t tb = best_of();
+    uint32_t r = 0;
+    for (; r < p.k; ++r) {
+        const uint64_t wb = warp_max_u64(tb);
+        if (wb == 0) break;  // this warp has no elements left
+        if (tb == wb) {      // the owner drops its winner and rescans
+            const uint32_t idx = ~(uint32_t)wb;
+            live &= ~(1u << ((idx - threadIdx.x) / NTS));
+            tb = best_of();
+        }
+        if (lane == 0) cand[warp * kSmallK + r] = wb;
+    }
+    for (uint32_t q = r + lane; q < kSmallK; q += 32) cand[warp * kSmallK + q] = 0;
+    __syncthreads();
+    if (warp == 0) {
+        constexpr int C = (NTS / 32) * kSmallK / 32;  // candidates per lane
+        uint64_t c[C];
+        uint32_t cl = 0;
+#pragma unroll
+        for (int i = 0; i < C; ++i) {
+            c[i] = cand[lane + 32 * i];
+            if (c[i]) cl |= 1u << i;
+        }
+        auto best_c = [&]() {
+            uint64_t b = 0;
+#pragma unroll
+            for (int i = 0; i < C; ++i)
+                if ((cl >> i) & 1u) b = c[i] > b ? c[i] : b;
+            return b;
+        };
+        uint64_t cb = best_c();
+        for (uint32_t q = 0; q < p.k; ++q) {
+            const uint64_t wb = warp_max_u64(cb);
+            if (cb == wb && wb != 0) {
+#pragma unroll
+                for (int i = 0; i < C; ++i)
+                    if (c[i] == wb) cl &= ~(1u << i);
+                cb = best_c();
+            }
+            if (lane == 0) win[q] = wb;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < p.k) {
+        const uint32_t idx = ~(uint32_t)win[threadIdx.x];
+        uint32_t rank = 0;
+        for (uint32_t q = 0; q < p.k; ++q) rank += ~(uint32_t)win[q] < idx;
+        if (idx < p.n) {
+            gcsgd_pair pr;
+            pr.idx = p.off + idx;
+            pr.val = vseg[idx];
+            dst[rank] = pr;
+            u[ebase + idx] = 0.0f;
+            v[ebase + idx] = 0.0f;
+        }
+    }
+}
+
 // One CTA per (learner, segment): exact top-k and ordered emission.
-__global__ void __launch_bounds__(NT) dgc_select(const SegPlan* __restrict__ plan, int S, uint64_t N,
-                                                 uint32_t tiles_per_learner, float* __restrict__ u,
-                                                 float* __restrict__ v, const uint32_t* __restrict__ pool_cnt,
-                                                 const uint2* __restrict__ tile_tab, const uint2* __restrict__ pool,
-                                                 uint64_t pool_per_learner, gcsgd_pair* __restrict__ out, uint64_t cap,
-                                                 int64_t* __restrict__ counts, int64_t* __restrict__ totals,
-                                                 uint32_t out_per_learner) {
+// Sources, fastest first:
+//   pool, staged  -- the candidates (k <= count <= pool capacity, so they hold
+//                    the whole top k), copied tile by tile in index order into
+//                    shared memory when they fit (kStageItems);
+//   raw, small k  -- segments of at most kSmallN values with k <= 32: top k
+//                    kept in registers (small_topk);
+//   raw, staged   -- other segments of at most kRawMax values: v' copied to
+//                    shared memory;
+//   global        -- anything else (a failed hint, or more candidates than
+//                    fit): the same selection read from global memory.
+__global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__ plan, int S, uint64_t N,
+                                                  uint32_t tiles_per_learner, float* __restrict__ u,
+                                                  float* __restrict__ v, const uint32_t* __restrict__ pool_cnt,
+                                                  const uint2* __restrict__ tile_tab, const uint2* __restrict__ pool,
+                                                  uint64_t pool_per_learner, gcsgd_pair* __restrict__ out,
+                                                  uint64_t cap, int64_t* __restrict__ counts,
+                                                  int64_t* __restrict__ totals, uint32_t out_per_learner,
+                                                  const uint16_t* __restrict__ order, int K) {
+    extern __shared__ __align__(16) unsigned char stage_raw[];  // kStageBytes
+    uint2* stage = reinterpret_cast<uint2*>(stage_raw);
+    float* stagef = reinterpret_cast<float*>(stage_raw);
     __shared__ uint32_t hist[2048];
-    __shared__ uint64_t scan[NT / 32 + 1];
+    __shared__ uint64_t scan[NTS / 32 + 1];
     __shared__ uint32_t sel[4];
-    __shared__ uint32_t toff[NT + 1];
-    __shared__ uint32_t tbase[NT];
-    const int unit = blockIdx.x;
-    const int k = unit / S, s = unit - k * S;
+    __shared__ uint32_t toff[NTS + 1];
+    __shared__ uint32_t tbase[NTS];
+    // largest segments first, every learner's copy of a segment together
+    const int k = (int)blockIdx.x % K;
+    const int s = order[(int)blockIdx.x / K];
+    const int unit = k * S + s;
     const SegPlan p = plan[s];
     if (threadIdx.x == 0) {
         counts[unit] = p.k;
@@ -355,119 +631,183 @@ __global__ void __launch_bounds__(NT) dgc_select(const SegPlan* __restrict__ pla
     if (p.k == 0) return;
     const uint64_t ebase = (uint64_t)k * N + p.off;
     const uint32_t pc = p.kind == kKindPool ? pool_cnt[unit] : 0;
-    const bool use_pool = p.kind == kKindPool && pc >= p.k && pc <= p.cap;
+    const bool pool_ok = p.kind == kKindPool && pc >= p.k && pc <= p.cap;
     const uint2* items = pool + (uint64_t)k * pool_per_learner + p.pool_off;
+    const uint2* tt = tile_tab + (uint64_t)k * tiles_per_learner + p.tile_off;
     const float* vseg = v + ebase;
-
-    SelectResult r;
-    if (use_pool) {
-        r = radix_select_desc<NT>(
-            [&](uint64_t i, uint32_t* key) { *key = __ldg(&items[i].y) & 0x7fffffffu; return true; }, pc, p.k, hist,
-            scan, sel);
-    } else {
-        r = radix_select_desc<NT>([&](uint64_t i, uint32_t* key) { *key = mag_key(vseg[i]); return true; }, p.n, p.k,
-                                  hist, scan, sel);
-    }
-    const uint32_t T = r.thresh, ties = r.ties, greater = r.greater;
     gcsgd_pair* dst = out + (uint64_t)k * cap + p.out_off;
 
-    // Ordered emission: an element is sent if its key > T, or == T and fewer
-    // than `ties` equal keys precede it.  Its slot is (#greater before it) +
-    // min(#equal before it, ties).
-    uint32_t run_gt = 0, run_eq = 0;
-
-    if (!use_pool) {
-        const bool aligned = (ebase & 3) == 0;
-        for (uint32_t cb = 0; cb < p.n; cb += 4 * NT) {
-            const uint32_t e = cb + 4 * threadIdx.x;
-            float x[4];
-            if (aligned && e + 4 <= p.n) {
-                const float4 q = *reinterpret_cast<const float4*>(vseg + e);
-                x[0] = q.x; x[1] = q.y; x[2] = q.z; x[3] = q.w;
-            } else {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) x[j] = e + j < p.n ? vseg[e + j] : 0.0f;
-            }
-            uint32_t ngt = 0, neq = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (e + j < p.n) {
-                    const uint32_t key = mag_key(x[j]);
-                    ngt += key > T;
-                    neq += key == T;
-                }
-            }
+    if (pool_ok && pc <= kStageItems) {
+        // stage the candidates in index order: tiles in order, items of a tile in order
+        uint32_t run = 0;
+        for (uint32_t tb = 0; tb < p.ntiles; tb += NTS) {
+            const uint32_t j = tb + threadIdx.x;
+            const uint2 ent = j < p.ntiles ? tt[j] : make_uint2(0u, 0u);
             uint64_t tot;
-            const uint64_t ex = block_exclusive_scan<NT>((uint64_t)ngt | ((uint64_t)neq << 32), scan, &tot);
-            uint32_t gb = run_gt + (uint32_t)ex, eb = run_eq + (uint32_t)(ex >> 32);
+            toff[threadIdx.x] = (uint32_t)block_exclusive_scan<NTS>(ent.y, scan, &tot);
+            tbase[threadIdx.x] = ent.x;
+            __syncthreads();
+            const uint32_t total = (uint32_t)tot;
+            for (uint32_t q0 = 0; q0 < total; q0 += 4 * NTS) {
+                uint2 it[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (e + j >= p.n) break;
-                const uint32_t key = mag_key(x[j]);
-                const bool gt = key > T, eq = key == T;
-                const uint32_t slot = gb + (eb < ties ? eb : ties);
-                if ((gt || (eq && eb < ties)) && slot < p.k) {
-                    dst[slot].idx = p.off + e + j;
-                    dst[slot].val = x[j];
-                    u[ebase + e + j] = 0.0f;
-                    v[ebase + e + j] = 0.0f;
+                for (int jj = 0; jj < 4; ++jj) {
+                    const uint32_t q = q0 + jj * NTS + threadIdx.x;
+                    if (q < total) {
+                        int lo = 0, hi = NTS;  // last tile with toff <= q
+                        while (hi - lo > 1) {
+                            const int mid = (lo + hi) >> 1;
+                            if (toff[mid] <= q) lo = mid; else hi = mid;
+                        }
+                        it[jj] = items[tbase[lo] + (q - toff[lo])];
+                    }
                 }
-                gb += gt;
-                eb += eq;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const uint32_t q = q0 + jj * NTS + threadIdx.x;
+                    if (q < total && run + q < kStageItems) stage[run + q] = it[jj];
+                }
+            }
+            run += total;
+            __syncthreads();
+        }
+        const SelectResult r = radix_select_desc<NTS>(
+            [&](uint64_t i, uint32_t* key) { *key = stage[i].y & 0x7fffffffu; return true; }, pc, p.k, hist, scan,
+            sel);
+        emit_in_order(
+            [&](uint32_t i, uint32_t* loc, uint32_t* bits) {
+                const uint2 it = stage[i];
+                *loc = it.x;
+                *bits = it.y;
+            },
+            pc, r.thresh, r.greater, r.ties, p, dst, u, v, ebase, scan);
+        return;
+    }
+    if (!pool_ok && p.n <= kSmallN && p.k <= kSmallK) {
+        small_topk(p, vseg, u, v, ebase, dst, reinterpret_cast<uint64_t*>(stage_raw),
+                   reinterpret_cast<uint64_t*>(stage_raw) + (NTS / 32) * kSmallK);
+        return;
+    }
+    if (!pool_ok && p.n <= kRawMax) {
+        // kRawMax = 8 float4 per thread: issue every load before the first store
+        const bool aligned = (ebase & 3) == 0;
+        float4 q[kRawMax / (4 * NTS)];
+#pragma unroll
+        for (int r = 0; r < (int)(kRawMax / (4 * NTS)); ++r) {
+            const uint32_t e0 = 4 * (r * NTS + threadIdx.x);
+            if (aligned && e0 + 4 <= p.n) {
+                q[r] = *reinterpret_cast<const float4*>(vseg + e0);
+            } else {
+                q[r].x = e0 < p.n ? vseg[e0] : 0.f;
+                q[r].y = e0 + 1 < p.n ? vseg[e0 + 1] : 0.f;
+                q[r].z = e0 + 2 < p.n ? vseg[e0 + 2] : 0.f;
+                q[r].w = e0 + 3 < p.n ? vseg[e0 + 3] : 0.f;
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < (int)(kRawMax / (4 * NTS)); ++r) {
+            const uint32_t e0 = 4 * (r * NTS + threadIdx.x);
+            if (e0 + 4 <= p.n) {
+                *reinterpret_cast<float4*>(stagef + e0) = q[r];
+            } else {
+                if (e0 < p.n) stagef[e0] = q[r].x;
+                if (e0 + 1 < p.n) stagef[e0 + 1] = q[r].y;
+                if (e0 + 2 < p.n) stagef[e0 + 2] = q[r].z;
+            }
+        }
+        __syncthreads();
+        const SelectResult r = radix_select_desc<NTS>(
+            [&](uint64_t i, uint32_t* key) { *key = mag_key(stagef[i]); return true; }, p.n, p.k, hist, scan, sel);
+        emit_in_order(
+            [&](uint32_t i, uint32_t* loc, uint32_t* bits) {
+                *loc = i;
+                *bits = __float_as_uint(stagef[i]);
+            },
+            p.n, r.thresh, r.greater, r.ties, p, dst, u, v, ebase, scan);
+        return;
+    }
+    if (!pool_ok) {
+        // the hint failed: select among all of the segment's v' in global memory
+        const SelectResult r = radix_select_desc<NTS>(
+            [&](uint64_t i, uint32_t* key) { *key = mag_key(vseg[i]); return true; }, p.n, p.k, hist, scan, sel);
+        emit_in_order(
+            [&](uint32_t i, uint32_t* loc, uint32_t* bits) {
+                *loc = i;
+                *bits = __float_as_uint(vseg[i]);
+            },
+            p.n, r.thresh, r.greater, r.ties, p, dst, u, v, ebase, scan);
+        return;
+    }
+    // a valid pool too large to stage: select from global memory, emit through the tile table
+    const SelectResult r = radix_select_desc<NTS>(
+        [&](uint64_t i, uint32_t* key) { *key = __ldg(&items[i].y) & 0x7fffffffu; return true; }, pc, p.k, hist,
+        scan, sel);
+    const uint32_t T = r.thresh, ties = r.ties;
+    uint32_t run_gt = 0, run_eq = 0;
+    for (uint32_t tb = 0; tb < p.ntiles; tb += NTS) {
+        const uint32_t j = tb + threadIdx.x;
+        const uint2 ent = j < p.ntiles ? tt[j] : make_uint2(0u, 0u);
+        uint64_t tot;
+        toff[threadIdx.x] = (uint32_t)block_exclusive_scan<NTS>(ent.y, scan, &tot);
+        tbase[threadIdx.x] = ent.x;
+        __syncthreads();
+        const uint32_t chunk_items = (uint32_t)tot;
+        for (uint32_t ib = 0; ib < chunk_items; ib += NTS) {
+            const uint32_t q = ib + threadIdx.x;
+            uint32_t local = 0xffffffffu, bits = 0;
+            const bool live = q < chunk_items;
+            if (live) {
+                int lo = 0, hi = NTS;
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (toff[mid] <= q) lo = mid; else hi = mid;
+                }
+                const uint2 it = items[tbase[lo] + (q - toff[lo])];
+                local = it.x;
+                bits = it.y;
+            }
+            const uint32_t key = bits & 0x7fffffffu;
+            const bool gt = live && key > T, eq = live && key == T;
+            const uint64_t ex2 = block_exclusive_scan<NTS>((uint64_t)gt | ((uint64_t)eq << 32), scan, &tot);
+            const uint32_t gb = run_gt + (uint32_t)ex2, eb = run_eq + (uint32_t)(ex2 >> 32);
+            const uint32_t slot = gb + (eb < ties ? eb : ties);
+            if ((gt || (eq && eb < ties)) && slot < p.k && local < p.n) {
+                gcsgd_pair pr;
+                pr.idx = p.off + local;
+                pr.val = __uint_as_float(bits);
+                dst[slot] = pr;
+                u[ebase + local] = 0.0f;
+                v[ebase + local] = 0.0f;
             }
             run_gt += (uint32_t)tot;
             run_eq += (uint32_t)(tot >> 32);
-            if (run_gt >= greater && run_eq >= ties) break;  // everything sent
         }
-    } else {
-        const uint2* tt = tile_tab + (uint64_t)k * tiles_per_learner + p.tile_off;
-        for (uint32_t tb = 0; tb < p.ntiles; tb += NT) {
-            const uint32_t j = tb + threadIdx.x;
-            uint2 ent = make_uint2(0u, 0u);
-            if (j < p.ntiles) ent = tt[j];
-            uint64_t tot;
-            const uint32_t ex = (uint32_t)block_exclusive_scan<NT>(ent.y, scan, &tot);
-            toff[threadIdx.x] = ex;
-            tbase[threadIdx.x] = ent.x;
-            if (threadIdx.x == 0) toff[NT] = (uint32_t)tot;
-            __syncthreads();
-            const uint32_t chunk_items = (uint32_t)tot;
-            for (uint32_t ib = 0; ib < chunk_items; ib += NT) {
-                const uint32_t q = ib + threadIdx.x;
-                uint32_t local = 0, bits = 0;
-                bool live = q < chunk_items;
-                if (live) {
-                    int lo = 0, hi = NT;  // last tile with toff <= q
-                    while (hi - lo > 1) {
-                        const int mid = (lo + hi) >> 1;
-                        if (toff[mid] <= q) lo = mid; else hi = mid;
-                    }
-                    const uint2 it = items[tbase[lo] + (q - toff[lo])];
-                    local = it.x;
-                    bits = it.y;
-                }
-                const uint32_t key = bits & 0x7fffffffu;
-                const bool gt = live && key > T, eq = live && key == T;
-                const uint64_t ex2 = block_exclusive_scan<NT>((uint64_t)gt | ((uint64_t)eq << 32), scan, &tot);
-                const uint32_t gb = run_gt + (uint32_t)ex2, eb = run_eq + (uint32_t)(ex2 >> 32);
-                const uint32_t slot = gb + (eb < ties ? eb : ties);
-                if ((gt || (eq && eb < ties)) && slot < p.k && local < p.n) {
-                    dst[slot].idx = p.off + local;
-                    dst[slot].val = __uint_as_float(bits);
-                    u[ebase + local] = 0.0f;
-                    v[ebase + local] = 0.0f;
-                }
-                run_gt += (uint32_t)tot;
-                run_eq += (uint32_t)(tot >> 32);
-            }
-            __syncthreads();  // toff/tbase reused by the next chunk
-        }
+        __syncthreads();  // toff/tbase reused by the next chunk
     }
 }
 
 }  // namespace dgc
 
 // ------------------------------------------------------------- host launch
+
+// Opt in to more than 48 KB of dynamic shared memory, once per device.
+static int dgc_set_smem_limits() {
+    using namespace dgc;
+    static bool done[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return set_error(GCSGD_ERR_CUDA, "dgc_compress: no current device");
+    if (done[dev]) return GCSGD_OK;
+    if (cudaFuncSetAttribute(dgc_prepare<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(kSampleMax * sizeof(uint32_t))) != cudaSuccess ||
+        cudaFuncSetAttribute(dgc_prepare<GCSGD_MAX_SEGMENTS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(kSampleMax * sizeof(uint32_t))) != cudaSuccess ||
+        cudaFuncSetAttribute(dgc_select, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStageBytes) !=
+            cudaSuccess)
+        return set_error(GCSGD_ERR_CUDA, "dgc_compress: cannot raise the shared-memory limit");
+    done[dev] = true;
+    return GCSGD_OK;
+}
 
 int dgc_launch(const int64_t* off, int S, int K, const float* grad, float* u, float* v, double density,
                float momentum, float clip_thr, int clip_nodes, gcsgd_pair* out, int64_t cap, int64_t* counts,
@@ -490,28 +830,31 @@ int dgc_launch(const int64_t* off, int S, int K, const float* grad, float* u, fl
         dgc_sumsq<<<dim3(kSumsqBlocks, K), NT, 0, stream>>>(grad, N, w.clip_part);
         if ((rc = check_launch("dgc_sumsq"))) return rc;
     }
+    const unsigned units = (unsigned)K * (unsigned)S;
+    if ((rc = dgc_set_smem_limits())) return rc;
     {
-        LaunchScope ls("dgc_plan", stream);
+        LaunchScope ls("dgc_prepare", stream);
+        const size_t smem = kSampleMax * sizeof(uint32_t);
+        const unsigned prep_grid = units < (unsigned)sm_count() * 2 ? units : (unsigned)sm_count() * 2;
         if (S <= 256) {
             SegOffsets<256> so;
             for (int s = 0; s <= S; ++s) so.off[s] = (uint32_t)off[s];
-            dgc_plan<256><<<1, 1024, 0, stream>>>(so, S, K, density, clip_thr, clip_nodes, kSumsqBlocks,
-                                                  w.clip_part, w.plan, w.clip_c);
+            dgc_prepare<256><<<prep_grid, NTP, smem, stream>>>(so, S, K, density, clip_thr, clip_nodes, w.clip_part,
+                                                               w.plan, w.clip_c, w.order, N, grad, u, v, momentum,
+                                                               w.hint, w.pool_cnt);
         } else {
             SegOffsets<GCSGD_MAX_SEGMENTS> so;
             for (int s = 0; s <= S; ++s) so.off[s] = (uint32_t)off[s];
-            dgc_plan<GCSGD_MAX_SEGMENTS><<<1, 1024, 0, stream>>>(so, S, K, density, clip_thr, clip_nodes,
-                                                                 kSumsqBlocks, w.clip_part, w.plan, w.clip_c);
+            dgc_prepare<GCSGD_MAX_SEGMENTS><<<prep_grid, NTP, smem, stream>>>(
+                so, S, K, density, clip_thr, clip_nodes, w.clip_part, w.plan, w.clip_c, w.order, N, grad, u, v,
+                momentum, w.hint, w.pool_cnt);
         }
-        if ((rc = check_launch("dgc_plan"))) return rc;
-    }
-    const unsigned units = (unsigned)K * (unsigned)S;
-    {
-        LaunchScope ls("dgc_hint", stream);
-        dgc_hint<<<units, NT, 0, stream>>>(w.plan, S, N, grad, u, v, momentum, w.clip_c, w.hint, w.pool_cnt);
-        if ((rc = check_launch("dgc_hint"))) return rc;
+        if ((rc = check_launch("dgc_prepare"))) return rc;
     }
     const uint64_t total_tiles = (uint64_t)K * hp.tiles_per_learner;
+    if (total_tiles >= ((uint64_t)1 << 32))
+        return set_error(GCSGD_ERR_INVALID_ARG, "dgc_compress: K * tiles = %llu exceeds 2^32",
+                         (unsigned long long)total_tiles);
     if (total_tiles > 0) {
         LaunchScope ls("dgc_update", stream);
         uint64_t grid = (uint64_t)sm_count() * 3;
@@ -523,15 +866,42 @@ int dgc_launch(const int64_t* off, int S, int K, const float* grad, float* u, fl
     }
     {
         LaunchScope ls("dgc_select", stream);
-        dgc_select<<<units, NT, 0, stream>>>(w.plan, S, N, (uint32_t)hp.tiles_per_learner, u, v, w.pool_cnt,
+        dgc_select<<<units, NTS, kStageBytes, stream>>>(w.plan, S, N, (uint32_t)hp.tiles_per_learner, u, v, w.pool_cnt,
                                              w.tile_tab, w.pool, hp.pool_per_learner, out, (uint64_t)cap, counts,
-                                             totals, (uint32_t)hp.out_per_learner);
+                                             totals, (uint32_t)hp.out_per_learner, w.order, K);
         if ((rc = check_launch("dgc_select"))) return rc;
     }
     return GCSGD_OK;
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+int dgc_collect_stats(const int64_t* off, int S, int K, double density, const void* ws, cudaStream_t stream,
+                      gcsgd_dgc_stats_t* st) {
+    using namespace dgc;
+    HostPlan hp;
+    host_plan(off, S, density, &hp);
+    DgcWorkspace w;
+    dgc_workspace_layout(S, K, hp, const_cast<void*>(ws), &w);
+    std::vector<uint32_t> cnt((size_t)K * S);
+    cudaError_t e = cudaMemcpyAsync(cnt.data(), w.pool_cnt, sizeof(uint32_t) * cnt.size(), cudaMemcpyDeviceToHost,
+                                    stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return set_error(GCSGD_ERR_CUDA, "gcsgd_dgc_stats: %s", cudaGetErrorString(e));
+    memset(st, 0, sizeof(*st));
+    st->units = (int64_t)K * S;
+    for (int k = 0; k < K; ++k)
+        for (int s = 0; s < S; ++s) {
+            SegPlan p;
+            seg_fields((uint32_t)(off[s + 1] - off[s]), density, &p);
+            const uint32_t c = cnt[(size_t)k * S + s];
+            if (p.kind == kKindEmpty) ++st->empty;
+            else if (p.kind == kKindRaw) (p.n <= kRawMax ? st->raw : st->raw_global)++;
+            else if (c < p.k || c > p.cap) ++st->hint_failed;
+            else (c <= kStageItems ? st->pool : st->pool_global)++;
+        }
+    return GCSGD_OK;
+}
 
 size_t dgc_workspace_layout(int S, int K, const dgc::HostPlan& hp, void* base, dgc::DgcWorkspace* w) {
     using namespace dgc;
@@ -544,6 +914,7 @@ size_t dgc_workspace_layout(int S, int K, const dgc::HostPlan& hp, void* base, d
     const size_t o_plan = take(sizeof(SegPlan) * (size_t)S);
     const size_t o_cc = take(sizeof(float) * (size_t)K);
     const size_t o_part = take(sizeof(double) * (size_t)K * kSumsqBlocks);
+    const size_t o_order = take(sizeof(uint16_t) * (size_t)S);
     const size_t o_hint = take(sizeof(uint32_t) * (size_t)K * S);
     const size_t o_cnt = take(sizeof(uint32_t) * (size_t)K * S);
     const size_t o_tt = take(sizeof(uint2) * (size_t)K * hp.tiles_per_learner);
@@ -553,6 +924,7 @@ size_t dgc_workspace_layout(int S, int K, const dgc::HostPlan& hp, void* base, d
         w->plan = (SegPlan*)(b + o_plan);
         w->clip_c = (float*)(b + o_cc);
         w->clip_part = (double*)(b + o_part);
+        w->order = (uint16_t*)(b + o_order);
         w->hint = (uint32_t*)(b + o_hint);
         w->pool_cnt = (uint32_t*)(b + o_cnt);
         w->tile_tab = (uint2*)(b + o_tt);

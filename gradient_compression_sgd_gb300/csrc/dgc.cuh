@@ -43,6 +43,7 @@ struct DgcWorkspace {
     SegPlan* plan;
     float* clip_c;
     double* clip_part;
+    uint16_t* order;  // segments by size, largest first
     uint32_t* hint;
     uint32_t* pool_cnt;
     uint2* tile_tab;
@@ -54,6 +55,9 @@ int host_plan(const int64_t* off, int S, double density, HostPlan* hp);
 }  // namespace dgc
 
 size_t dgc_workspace_layout(int S, int K, const dgc::HostPlan& hp, void* base, dgc::DgcWorkspace* w);
+
+int dgc_collect_stats(const int64_t* off, int S, int K, double density, const void* ws, cudaStream_t stream,
+                      gcsgd_dgc_stats_t* st);
 
 int dgc_launch(const int64_t* off, int S, int K, const float* grad, float* u, float* v, double density,
                float momentum, float clip_thr, int clip_nodes, gcsgd_pair* out, int64_t cap, int64_t* counts,

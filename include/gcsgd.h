@@ -102,6 +102,22 @@ int dgc_compress(const int64_t* seg_offsets, int32_t n_seg, int32_t K,
                  gcsgd_pair* out, int64_t cap, int64_t* counts, int64_t* totals,
                  void* workspace, size_t workspace_bytes, void* stream);
 
+/* Diagnostics of the last dgc_compress call made with `workspace`: how each
+ * (learner, segment) found its top k.  The answer is exact on every path;
+ * only the speed differs.  Host function; it copies a few counters from
+ * the workspace and synchronises `stream`. */
+typedef struct {
+    int64_t units;        /* K * n_seg */
+    int64_t empty;        /* empty segments */
+    int64_t raw;          /* small segment: its v' staged in shared memory */
+    int64_t pool;         /* candidate pool held the top k and was staged in shared memory */
+    int64_t pool_global;  /* candidate pool held the top k but was read from global memory */
+    int64_t raw_global;   /* large segment at high density: the whole v' read from global memory */
+    int64_t hint_failed;  /* candidate pool missed (too few or overflow): the whole v' read */
+} gcsgd_dgc_stats_t;
+int gcsgd_dgc_stats(const int64_t* seg_offsets, int32_t n_seg, int32_t K, double density,
+                    const void* workspace, void* stream, gcsgd_dgc_stats_t* out);
+
 /*
  * dgc_compress without a workspace argument, for callers that cannot
  * allocate device memory (for example a plugin whose host framework's caching

@@ -205,22 +205,33 @@ def test_dcd_keep_all_and_weights(cuda_lib):
     run_dcd(cuda_lib, 1, 5000, 2, 1.0, w=(0.0, 1.0, 0.0))
 
 
-def test_philox_matches_curand(cuda_lib):
-    """The library's and the oracle's keep draws are Philox4x32-10; cuRAND's
-    host generator (a library routine) gives the stream of counter i under
-    key seed as output words 4i..4i+3 -- when that holds, the oracle's
-    generator must reproduce it."""
+def test_philox_matches_curand_device_api(cuda_lib, tmp_path):
+    """The oracle's Philox4x32-10 word block at counter (q, node, t, q >> 32)
+    under key (seed) equals cuRAND's curand4 after curand_init(seed,
+    subsequence = t, offset = 4 (q + node 2^32)) -- a library routine."""
     import ctypes
-    cr = ctypes.CDLL("libcurand.so")
-    gen = ctypes.c_void_p()
-    assert cr.curandCreateGeneratorHost(ctypes.byref(gen), 106) == 0  # CURAND_RNG_PSEUDO_PHILOX4_32_10
-    seed = 0x123456789ABCDEF0
-    assert cr.curandSetPseudoRandomGeneratorSeed(gen, ctypes.c_ulonglong(seed)) == 0
-    buf = np.zeros(64, np.uint32)
-    assert cr.curandGenerate(gen, buf.ctypes.data_as(ctypes.c_void_p), ctypes.c_size_t(64)) == 0
-    cr.curandDestroyGenerator(gen)
+    import subprocess
+
+    import torch
+    from gradient_compression_sgd_gb300 import build as gbuild
+    src = __import__("os").path.join(__import__("os").path.dirname(__file__), "curand_philox.cu")
+    so = str(tmp_path / "curand_philox.so")
+    subprocess.check_call([gbuild.nvcc(), *gbuild.ARCH, "-O2", "-shared", "-Xcompiler", "-fPIC", "-cudart", "shared",
+                           src, "-o", so])
+    L = ctypes.CDLL(so)
+    rng = np.random.default_rng(3)
+    seed = 0x5EED000000000005
+    qs = np.concatenate([[0, 1, 2, 3, 6_399_999], rng.integers(0, 1 << 31, size=59)]).astype(np.uint64)
+    nodes = rng.integers(0, 8, size=len(qs)).astype(np.uint64)
+    ts = rng.integers(0, 10, size=len(qs)).astype(np.uint64)
+    sub = torch.from_numpy(ts.astype(np.int64)).cuda()
+    off = torch.from_numpy((4 * (qs + (nodes << np.uint64(32)))).astype(np.int64)).cuda()
+    out = torch.zeros((len(qs), 4), dtype=torch.int32, device="cuda")
+    assert L.curand_philox_blocks(ctypes.c_ulonglong(seed), ctypes.c_void_p(sub.data_ptr()),
+                                  ctypes.c_void_p(off.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                                  ctypes.c_int(len(qs))) == 0
+    got = out.cpu().numpy().view(np.uint32)
     key = [seed & 0xFFFFFFFF, seed >> 32]
-    mine = np.concatenate([oracle.philox4x32_10([i, 0, 0, 0], key) for i in range(16)])
-    if not np.array_equal(mine, buf):
-        pytest.skip("cuRAND's host stream uses another counter layout; the known-answer pins stand")
-    np.testing.assert_array_equal(mine, buf)
+    for i in range(len(qs)):
+        want = oracle.philox4x32_10([int(qs[i]) & 0xFFFFFFFF, int(nodes[i]), int(ts[i]), int(qs[i]) >> 32], key)
+        np.testing.assert_array_equal(got[i], want)

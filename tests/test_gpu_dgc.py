@@ -67,7 +67,9 @@ def test_small_configs(cuda_lib, config):
     GRU layout shrunk to 256x768 (K = 8, 10 steps)."""
     w = wl.workload(config, small=True)
     grads = [wl.gradients(w, t).numpy() for t in range(w.steps)]
-    run_dgc(cuda_lib, w.offsets, grads, w.density, w.momentum)
+    d = run_dgc(cuda_lib, w.offsets, grads, w.density, w.momentum)
+    st = d.stats()
+    assert st["units"] == w.learners * len(w.sizes) and st["hint_failed"] == 0
 
 
 EDGE_LAYOUTS = {
@@ -108,22 +110,27 @@ def test_ties_and_zeros(cuda_lib, levels):
 
 
 def test_hint_above_the_kth_value_falls_back(cuda_lib):
-    """Distinct large values only in the blocks the threshold sample reads, tiny
-    ones elsewhere: only the sampled rank-a values clear the candidate
-    threshold, fewer than k, so the select must fall back to the full
-    segment and still be exact.  (The sample layout mirrors the kernel's
-    plan: R = max(3k, 512), m = min(32 n / R, 8192) rounded down to 32,
-    blocks of 32 at stride n / (m / 32).)"""
+    """Values planted where the threshold sample reads push the candidate
+    threshold above the k-th value: exactly a sampled values are 3.0 (so the
+    hint is 3.0 and only a < k entries qualify), the other sampled values 1.0
+    (ties), some unsampled ones 0.5, the rest tiny.  The select must fall
+    back to the whole segment and still be exact.  (The sample layout mirrors
+    the kernel's plan: R = max(3k, 512), m = min(48 n / R, 16384) rounded
+    down to 32, blocks of 32 at stride n / (m / 32), a = round(R m / n).)"""
     n, density = 40000, 0.003
     k = oracle.dgc_k(density, n)
     R = max(3 * k, 512)
-    m = min(32 * n // R, 8192) & ~31
+    m = min(48 * n // R, 16384) & ~31
     nblk, stride = m // 32, n // (m // 32)
+    a = (R * m + n // 2) // n
+    assert a < k
     G = np.full((1, n), 1e-6, np.float32)
     pos = np.concatenate([np.arange(b * stride, b * stride + 32) for b in range(nblk)])
-    G[0, pos] = 1.0 + np.arange(len(pos), dtype=np.float32) / len(pos)
-    G[0, 30001:30050] = 0.5  # below the sampled values, above the rest
-    run_dgc(cuda_lib, [0, n], [G], density, 0.9)
+    G[0, pos] = 1.0
+    G[0, pos[np.linspace(0, len(pos) - 1, a).astype(int)]] = 3.0
+    G[0, 30001:30050] = 0.5
+    d = run_dgc(cuda_lib, [0, n], [G], density, 0.9)
+    assert d.stats()["hint_failed"] == 1
 
 
 def test_nonzero_initial_state_and_momentum_zero(cuda_lib):

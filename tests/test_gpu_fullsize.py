@@ -61,6 +61,8 @@ def test_dgc_full_size(cuda_lib, config):
         u_prev, v_prev = u.clone(), v.clone()
         out, totals = d(G, u, v)
         torch.cuda.synchronize()
+        st = d.stats()
+        assert st["hint_failed"] == 0 and st["raw_global"] == 0, st  # the fast paths served every segment
         # learner 0 against the oracle
         idx_o, val_o, counts_o, _ = oracle.dgc_step(off, G[0:1].cpu().numpy(), u0, v0, w.density, w.momentum,
                                                     cap=d.cap)
