@@ -49,8 +49,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gcsgd", choices=["gcsgd", "reference"])
-    ap.add_argument("--config", type=int, default=2, choices=[2, 4],
-                    help="2: ResNet-50 layout K=4 (the metric's workload); 4: GRU layout K=8")
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5],
+                    help="2 (default): ResNet-50 layout, DGC K=4 + average -- the metric's workload; "
+                         "1: one 1M tensor, DGC with clipping; 3: LSTM+VGG AdaComp K=8 + average; "
+                         "4: GRU layout DGC K=8 + average; 5: DCD ring of 8 nodes")
     ap.add_argument("--learners", type=int, default=0, help="override K (smaller cases for ncu captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement (ncu captures)")
@@ -184,22 +186,32 @@ def run_reference(args):
 
 
 def config_dict(w, **extra):
+    steps = {"dgc": "dgc_compress(K learners) + sparse_average", "adacomp": "adacomp_compress(K learners) + sparse_average",
+             "dcd": "dcd_step(n ring nodes)"}
     d = {"workload": w.name, "learners": w.learners, "elements_per_learner": w.n, "segments": len(w.sizes),
-         "density": w.density, "momentum": w.momentum, "step": "dgc_compress(K learners) + sparse_average",
-         "l2": "inputs larger than L2: 3 rotating gradient sets of K*N*4 bytes each"}
+         "step": steps[w.method], "l2": "inputs larger than L2: 3 rotating gradient sets of K*N*4 bytes each"}
+    if w.method == "dgc":
+        d.update(density=w.density, momentum=w.momentum, clip_thr=w.clip_thr)
+    elif w.method == "adacomp":
+        d.update(bin_lengths=sorted(set(w.lt)))
+    else:
+        d.update(gamma=w.gamma, keep_p=w.keep_p)
     d.update(extra)
     return d
 
 
-def kernel_source_sha() -> str:
-    with open(os.path.join(ROOT, "gradient_compression_sgd_gb300", "csrc", "dgc.cu"), "rb") as f:
+def kernel_source_sha(name: str = "dgc.cu") -> str:
+    with open(os.path.join(ROOT, "gradient_compression_sgd_gb300", "csrc", name), "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per dgc_update launch from the committed ncu summary, if it
+KERNEL_SOURCE = {"dgc_update": "dgc.cu", "ada_bins": "adacomp.cu", "dcd_step": "dcd.cu", "spavg": "spavg.cu"}
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
     was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"dgc_update_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
         kv = {}
         with open(path) as f:
@@ -207,7 +219,7 @@ def profiled_traffic(workload: str):
                 if ":" in line and line.startswith("- "):
                     k, v = line[2:].split(":", 1)
                     kv[k.strip()] = v.strip()
-        if kv.get("kernel_source_sha") != kernel_source_sha():
+        if kv.get("kernel_source_sha") != kernel_source_sha(KERNEL_SOURCE[kernel]):
             return None
         return float(kv["dram_bytes_per_launch"])
     except Exception:
@@ -215,6 +227,82 @@ def profiled_traffic(workload: str):
 
 
 # -------------------------------------------------------------- GPU arm
+
+class DgcPath:
+    """DGC of K learners + sparse average of their messages (configs 1, 2, 4)."""
+    dominant, bytes_per_elem = "dgc_update", DGC_BYTES_PER_ELEM
+
+    def __init__(self, gc, w, dev):
+        import torch
+        self.gc, self.w, self.K, self.N = gc, w, w.learners, w.n
+        self.obj = gc.DGC(w.offsets, self.K, w.density, w.momentum, w.clip_thr, w.clip_nodes, device=dev)
+        self.state = [torch.zeros((self.K, self.N), device=dev) for _ in range(2)]
+        self.avg = torch.empty(self.N, device=dev)
+
+    def fresh_state(self):
+        import torch
+        return [torch.zeros_like(x) for x in self.state]
+
+    def step(self, g, state=None, t=0):
+        u, v = state or self.state
+        out, totals = self.obj(g, u, v)
+        self.gc.sparse_average(out, totals, self.N, self.avg)
+        return self.avg
+
+    def sent(self):
+        return int(self.obj.totals.sum().item())
+
+    def extra(self):
+        return {"select_paths": self.obj.stats()}
+
+
+class AdaCompPath(DgcPath):
+    """AdaComp of K learners + sparse average of their messages (config 3)."""
+    dominant, bytes_per_elem = "ada_bins", 12
+
+    def __init__(self, gc, w, dev):
+        import torch
+        self.gc, self.w, self.K, self.N = gc, w, w.learners, w.n
+        self.obj = gc.AdaComp(w.offsets, w.lt, self.K, self.N // 8, device=dev)
+        self.state = [torch.zeros((self.K, self.N), device=dev)]
+        self.avg = torch.empty(self.N, device=dev)
+
+    def step(self, g, state=None, t=0):
+        (R,) = state or self.state
+        out, totals = self.obj(g, R)
+        self.gc.sparse_average(out, totals, self.N, self.avg)
+        return self.avg
+
+    def extra(self):
+        tot = self.obj.totals.cpu()
+        return {"sent_fraction": float(tot.sum()) / (self.K * self.N), "cap_per_learner": self.obj.cap,
+                "learners_over_cap": int((tot > self.obj.cap).sum())}
+
+
+class DcdPath:
+    """One DCD-PSGD ring iteration of n nodes (config 5)."""
+    dominant, bytes_per_elem = "dcd_step", 12
+
+    def __init__(self, gc, w, dev):
+        from gradient_compression_sgd_gb300 import workloads as wl
+        self.gc, self.w, self.K, self.N = gc, w, w.learners, w.n
+        self.state = [wl.dcd_initial_model(w, device=dev)]
+        self.seed = wl.dcd_seed(w)
+
+    def fresh_state(self):
+        return [self.state[0].clone()]
+
+    def step(self, g, state=None, t=0):
+        (x,) = state or self.state
+        self.gc.dcd_step(x, g, self.w.ring_w, self.w.gamma, self.w.keep_p, self.seed, t)
+        return x[0]
+
+    def sent(self):
+        return 0
+
+    def extra(self):
+        return {}
+
 
 def run_gpu(args):
     import torch
@@ -241,18 +329,11 @@ def run_gpu(args):
     K, N = w.learners, w.n
     dev = torch.device("cuda", local)
     grads = [wl.gradients(w, t, device=dev) for t in range(N_SETS)]
-    dgc = gc.DGC(w.offsets, K, w.density, w.momentum, device=dev)
-    u = torch.zeros((K, N), device=dev)
-    v = torch.zeros((K, N), device=dev)
-    avg = torch.empty(N, device=dev)
+    path = {"dgc": DgcPath, "adacomp": AdaCompPath, "dcd": DcdPath}[w.method](gc, w, dev)
     stream = torch.cuda.current_stream()
 
-    def step(i):
-        out, totals = dgc(grads[i % N_SETS], u, v)
-        gc.sparse_average(out, totals, N, avg)
-
     for i in range(args.warmup):
-        step(i)
+        path.step(grads[i % N_SETS], t=i)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -267,7 +348,7 @@ def run_gpu(args):
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
-        step(i)
+        path.step(grads[i % N_SETS], t=args.warmup + i)
     e1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -284,24 +365,26 @@ def run_gpu(args):
     grad_bytes = 4.0 * K * N
     value = world * grad_bytes / (ms * 1e-3) / 1e9
 
-    # end to end through the public API: pinned host gradient in, dense average out
-    e2e, ms_e2e = None, None
+    # end to end through the public API: pinned host gradient in, the step's dense result out
+    e2e, ms_e2e, d2h = None, None, 0
     if not args.no_e2e:
         host = [g.cpu().pin_memory() for g in grads[:2]]
         gdev = torch.empty((K, N), device=dev)
-        avg_host = torch.empty(N, pin_memory=True)
-        u2 = torch.zeros((K, N), device=dev)
-        v2 = torch.zeros((K, N), device=dev)
+        state2 = path.fresh_state()
+        res_host = None
 
         def e2e_step(i):
+            nonlocal res_host
             gdev.copy_(host[i % 2], non_blocking=True)
-            out, totals = dgc(gdev, u2, v2)
-            gc.sparse_average(out, totals, N, avg)
-            avg_host.copy_(avg, non_blocking=True)
+            res = path.step(gdev, state2, t=i)
+            if res_host is None:
+                res_host = torch.empty(res.shape, dtype=res.dtype, pin_memory=True)
+            res_host.copy_(res, non_blocking=True)
 
         for i in range(max(1, args.warmup)):
             e2e_step(i)
         torch.cuda.synchronize()
+        d2h = int(res_host.numel() * res_host.element_size())
         if world > 1:
             dist.barrier()
         f0 = torch.cuda.Event(enable_timing=True)
@@ -319,7 +402,6 @@ def run_gpu(args):
             ms_e2e = float(t.item())
         e2e = world * grad_bytes / (ms_e2e * 1e-3) / 1e9
 
-
     if rank != 0:
         if world > 1:
             dist.barrier()
@@ -327,19 +409,19 @@ def run_gpu(args):
         return 0
 
     hbm, peak_kind = peaks()
-    n_up, ms_up = trace.get("dgc_update", (0, 0.0))
-    upd_ms = ms_up / max(n_up, 1)
-    upd_bytes = float(DGC_BYTES_PER_ELEM) * K * N
-    achieved = upd_bytes / (upd_ms * 1e-3) / 1e9 if upd_ms > 0 else None
-    traffic = profiled_traffic(w.name)
-    sent = int(dgc.totals.sum().item())
-    select_paths = dgc.stats()
-    step_bytes = DGC_BYTES_PER_ELEM * K * N + 8.0 * sent + 4.0 * N + 8.0 * sent
-    kernels = {name: {"launches": c, "ms_per_launch": t / max(c, 1), "share": t / max(sum(x[1] for x in trace.values()), 1e-9)}
+    n_dom, ms_dom = trace.get(path.dominant, (0, 0.0))
+    dom_ms = ms_dom / max(n_dom, 1)
+    dom_bytes = float(path.bytes_per_elem) * K * N
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9 if dom_ms > 0 else None
+    traffic = profiled_traffic(path.dominant, w.name)
+    sent = path.sent()
+    step_bytes = path.bytes_per_elem * K * N + 16.0 * sent + (4.0 * N if w.method != "dcd" else 0.0)
+    total_ms = max(sum(x[1] for x in trace.values()), 1e-9)
+    kernels = {name: {"launches": c, "ms_per_launch": t / max(c, 1), "share": t / total_ms}
                for name, (c, t) in trace.items()}
 
     cpu = None
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and w.method == "dgc":
         b, dt, desc = oracle_sample(w, grads[0][0].cpu().numpy(), args.cpu_seconds)
         cpu = {"value": b / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc}
 
@@ -347,19 +429,20 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded N(0, sigma^2) per tensor, sigma log-uniform in [1e-5, 1e-2])",
+        "data": "synthetic (seeded N(0, sigma^2) per tensor, sigma log-uniform in [1e-5, 1e-2])"
+                if w.config == 2 else f"synthetic (seeded, config {w.config} recipe)",
         "config": config_dict(w),
         "elements_per_s": world * K * N / (ms * 1e-3),
         "step_roofline_frac": step_bytes / (ms * 1e-3) / 1e9 / hbm,
-        "roofline": {"bound": "hbm", "kernel": "dgc_update", "achieved": achieved, "peak": hbm,
+        "roofline": {"bound": "hbm", "kernel": path.dominant, "achieved": achieved, "peak": hbm,
                      "peak_kind": f"{peak_kind} (copy)", "unit": "GB/s",
                      "frac": (achieved / hbm) if achieved else None,
-                     "algorithmic_bytes_per_launch": upd_bytes, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": dom_bytes, "traffic": traffic,
                      "frac_of_nominal_8tbs": (achieved / 8000.0) if achieved else None},
         "kernels": kernels,
-        "select_paths": select_paths,
+        **path.extra(),
         "e2e": None if e2e is None else {"value": e2e, "unit": "GB/s", "ms_per_step": ms_e2e,
-                                         "h2d_bytes_per_step": int(grad_bytes), "d2h_bytes_per_step": int(4 * N)},
+                                         "h2d_bytes_per_step": int(grad_bytes), "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clk,
         "cpu_baseline": cpu,

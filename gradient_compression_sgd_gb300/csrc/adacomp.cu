@@ -216,14 +216,63 @@ __global__ void __launch_bounds__(NT) ada_bigmax(const SegPlan* __restrict__ pla
     }
 }
 
-__global__ void __launch_bounds__(NT, 2) ada_bins(const SegPlan* __restrict__ plan, int S, uint64_t N,
+// Bin of tile element e (small mode): floor((e + 0.5) / L), exact for e < 4096.
+__device__ __forceinline__ uint32_t bin_of(uint32_t e, float invL) {
+    return (uint32_t)__float2int_rd(((float)e + 0.5f) * invL);
+}
+
+// Selection of one tile's entries: sent iff |G + dW| >= the bin's max |G|,
+// the max > 0 and G != 0.  MODE 0: bins of L >= 4 inside the tile (a float4
+// spans at most two bins, split at `cut`); MODE 1: bins of L < 4; MODE 2:
+// bins longer than a tile, maxima precomputed in global memory.  Bit 4r+j of
+// `flags` marks element j of round r; `packed` holds the per-round counts.
+template <int MODE>
+__device__ __forceinline__ void select_tile(const float4 (&Gv)[4], const float4 (&Dv)[4], uint32_t len, uint32_t L,
+                                            float invL, uint32_t nbt, const uint32_t* bmax, const uint32_t* bigm,
+                                            uint32_t start, uint32_t& flags, uint64_t& packed) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const uint32_t e = 4u * (r * NT + threadIdx.x);
+        if (e >= len) continue;
+        const float* g4 = &Gv[r].x;
+        const float* d4 = &Dv[r].x;
+        uint32_t gm[4];
+        if (MODE == 0) {
+            const uint32_t b0 = bin_of(e, invL);
+            const uint32_t cut = (b0 + 1) * L - e;
+            const uint32_t m0 = bmax[b0];
+            const uint32_t m1 = cut < 4 && b0 + 1 < nbt ? bmax[b0 + 1] : m0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) gm[j] = (uint32_t)j < cut ? m0 : m1;
+        } else if (MODE == 1) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) gm[j] = e + j < len ? bmax[bin_of(e + j, invL)] : 0u;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) gm[j] = e + j < len ? __ldg(&bigm[(start + e + j) / L]) : 0u;
+        }
+        uint32_t f = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t hk = mag_key(__fadd_rn(g4[j], d4[j]));  // |G + dW|
+            const bool sel = hk >= gm[j] && gm[j] > 0u && mag_key(g4[j]) != 0u;
+            f |= (uint32_t)sel << j;
+        }
+        if (e + 4 > len) f &= (1u << (len - e)) - 1u;  // a partial float4 at the tile end
+        flags |= f << (4 * r);
+        packed |= (uint64_t)__popc(f) << (16 * r);
+    }
+}
+
+__global__ void __launch_bounds__(NT, 3) ada_bins(const SegPlan* __restrict__ plan, int S, uint64_t N,
                                                   uint32_t tiles_per_learner, uint64_t total_tiles,
                                                   const float* __restrict__ dW, float* __restrict__ R,
                                                   const uint32_t* __restrict__ big, uint64_t big_per_learner,
                                                   uint32_t* __restrict__ pool_cnt, uint2* __restrict__ tile_tab,
                                                   double2* __restrict__ tile_sum, uint2* __restrict__ pool,
                                                   uint64_t pool_cap) {
-    __shared__ uint32_t bmax[kTileMax];
+    __shared__ __align__(16) uint32_t gk[kTileMax];  // |G| bit patterns of the tile
+    __shared__ uint32_t bmax[kTileMax];               // bin maxima (|G| bits)
     __shared__ uint64_t scan[NT / 32 + 1];
     __shared__ uint32_t s_base;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -237,119 +286,93 @@ __global__ void __launch_bounds__(NT, 2) ada_bins(const SegPlan* __restrict__ pl
         const uint32_t len = p.n - start < p.tile_len ? p.n - start : p.tile_len;
         const uint64_t base = (uint64_t)k * N + p.off + start;
         const bool small = p.mode == kModeSmall;
+        const uint32_t L = p.L;
         const uint32_t nbt = small ? (p.nbins - tj * p.bpt < p.bpt ? p.nbins - tj * p.bpt : p.bpt) : 0;
         const bool aligned = (base & 3) == 0;
         const uint32_t* bigm = big + (uint64_t)k * big_per_learner + p.big_off;
+        const float* dWt = dW + base;
+        float* Rt = R + base;
 
-        if (small)
-            for (uint32_t b = threadIdx.x; b < nbt; b += NT) bmax[b] = 0u;
-
+        // 1. G = R + dW (registers) and |G| keys to shared memory
         float4 Gv[4], Dv[4];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const uint32_t e = 4u * (r * NT + threadIdx.x);
             if (aligned && e + 4 <= len) {
-                Dv[r] = __ldg(reinterpret_cast<const float4*>(dW + base + e));
-                Gv[r] = *reinterpret_cast<const float4*>(R + base + e);
+                Dv[r] = __ldg(reinterpret_cast<const float4*>(dWt + e));
+                Gv[r] = *reinterpret_cast<const float4*>(Rt + e);
             } else {
                 float* d4 = &Dv[r].x;
                 float* g4 = &Gv[r].x;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const bool in = e + j < len;
-                    d4[j] = in ? __ldg(dW + base + e + j) : 0.0f;
-                    g4[j] = in ? R[base + e + j] : 0.0f;
+                    d4[j] = in ? __ldg(dWt + e + j) : 0.0f;
+                    g4[j] = in ? Rt[e + j] : 0.0f;
                 }
             }
         }
-        __syncthreads();  // bmax zeroed
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const uint32_t e = 4u * (r * NT + threadIdx.x);
-            float* g4 = &Gv[r].x;
-            const float* d4 = &Dv[r].x;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) g4[j] = __fadd_rn(g4[j], d4[j]);  // G = R + dW
-            if (small) {
-                if (p.L >= 4) {
-                    // the four entries span at most two bins: b0 and b0 + 1
-                    const uint32_t b0 = e < len ? (uint32_t)__float2int_rd(((float)e + 0.5f) * p.invL) : 0xffffffffu;
-                    uint32_t mA = 0, mB = 0;
-                    bool hasB = false;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        if (e + j >= len) break;
-                        const uint32_t bj = (uint32_t)__float2int_rd(((float)(e + j) + 0.5f) * p.invL);
-                        const uint32_t key = mag_key(g4[j]);
-                        if (bj == b0) mA = max(mA, key);
-                        else { mB = max(mB, key); hasB = true; }
-                    }
-                    const bool inA = b0 != 0xffffffffu;
-                    unsigned am = __ballot_sync(kFull, inA);
-                    if (inA) {
-                        const unsigned grp = __match_any_sync(am, b0);
-                        const uint32_t mx = __reduce_max_sync(grp, mA);
-                        if (lane == __ffs(grp) - 1) atomicMax(&bmax[b0], mx);
-                    }
-                    am = __ballot_sync(kFull, hasB);
-                    if (hasB) {
-                        const unsigned grp = __match_any_sync(am, b0 + 1);
-                        const uint32_t mx = __reduce_max_sync(grp, mB);
-                        if (lane == __ffs(grp) - 1) atomicMax(&bmax[b0 + 1], mx);
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        if (e + j < len) {
-                            const uint32_t bj = (uint32_t)__float2int_rd(((float)(e + j) + 0.5f) * p.invL);
-                            atomicMax(&bmax[bj], mag_key(g4[j]));
-                        }
+            Gv[r].x = __fadd_rn(Gv[r].x, Dv[r].x);
+            Gv[r].y = __fadd_rn(Gv[r].y, Dv[r].y);
+            Gv[r].z = __fadd_rn(Gv[r].z, Dv[r].z);
+            Gv[r].w = __fadd_rn(Gv[r].w, Dv[r].w);
+            if (small && e < kTileMax)
+                *reinterpret_cast<uint4*>(gk + e) =
+                    make_uint4(mag_key(Gv[r].x), mag_key(Gv[r].y), mag_key(Gv[r].z), mag_key(Gv[r].w));
+        }
+        __syncthreads();
+        // 2. bin maxima: a warp per bin for L >= 32, a thread per bin below
+        if (small) {
+            if (L >= 32) {
+                for (uint32_t b = warp; b < nbt; b += NT / 32) {
+                    const uint32_t lo = b * L, hi = lo + L < len ? lo + L : len;
+                    uint32_t m = 0;
+                    for (uint32_t i = lo + lane; i < hi; i += 32) m = max(m, gk[i]);
+                    m = __reduce_max_sync(kFull, m);
+                    if (lane == 0) bmax[b] = m;
+                }
+            } else {
+                for (uint32_t b = threadIdx.x; b < nbt; b += NT) {
+                    const uint32_t lo = b * L, hi = lo + L < len ? lo + L : len;
+                    uint32_t m = 0;
+                    for (uint32_t i = lo; i < hi; ++i) m = max(m, gk[i]);
+                    bmax[b] = m;
                 }
             }
         }
-        __syncthreads();  // bin maxima final
-        // compensated sum of this tile's bin maxima, in bin order (warp 0)
+        __syncthreads();
+        // sum of this tile's bin maxima (warp 0): each lane adds a run of
+        // bins in fp64, then a fixed shuffle tree; at most 133 fp64 adds
+        // per lane, so the relative error stays below 2^-45 (GB300's fp64
+        // rate is a few operations per cycle per SM, so it is kept short)
         if (small && warp == 0) {
             const uint32_t per = (nbt + 31) / 32;
-            double sm = 0.0, cm = 0.0;
+            double sm = 0.0;
             for (uint32_t b = lane * per; b < nbt && b < (lane + 1) * per; ++b)
-                csum_add(sm, cm, (double)__uint_as_float(bmax[b]));
-            double S0 = 0.0, C0 = 0.0;
-            for (int l = 0; l < 32; ++l) {
-                const double ls = __shfl_sync(kFull, sm, l);
-                const double lc = __shfl_sync(kFull, cm, l);
-                csum_add(S0, C0, ls);
-                C0 = __dadd_rn(C0, lc);
-            }
-            if (lane == 0) tile_sum[t] = make_double2(S0, C0);
+                sm = __dadd_rn(sm, (double)__uint_as_float(bmax[b]));
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) sm = __dadd_rn(sm, __shfl_down_sync(kFull, sm, d));
+            if (lane == 0) tile_sum[t] = make_double2(sm, 0.0);
         }
-        // selection, residue store, candidate flags
+        // 3. selection, residue store, candidate flags (the mode is uniform per tile)
         uint64_t packed = 0;
         uint32_t flags = 0;
+        if (small && L >= 4) select_tile<0>(Gv, Dv, len, L, p.invL, nbt, bmax, bigm, start, flags, packed);
+        else if (small) select_tile<1>(Gv, Dv, len, L, p.invL, nbt, bmax, bigm, start, flags, packed);
+        else select_tile<2>(Gv, Dv, len, L, p.invL, nbt, bmax, bigm, start, flags, packed);
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const uint32_t e = 4u * (r * NT + threadIdx.x);
-            float* g4 = &Gv[r].x;
-            const float* d4 = &Dv[r].x;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                bool sel = false;
-                if (e + j < len) {
-                    uint32_t gm;
-                    if (small) gm = bmax[(uint32_t)__float2int_rd(((float)(e + j) + 0.5f) * p.invL)];
-                    else gm = __ldg(&bigm[(start + e + j) / p.L]);
-                    const uint32_t hk = mag_key(__fadd_rn(g4[j], d4[j]));  // |G + dW|
-                    sel = hk >= gm && gm > 0u && mag_key(g4[j]) != 0u;
-                }
-                flags |= (uint32_t)sel << (4 * r + j);
-            }
-            packed |= (uint64_t)__popc((flags >> (4 * r)) & 0xFu) << (16 * r);
             if (aligned && e + 4 <= len) {
-                *reinterpret_cast<float4*>(R + base + e) = Gv[r];
+                *reinterpret_cast<float4*>(Rt + e) = Gv[r];
             } else {
+                const float* g4 = &Gv[r].x;
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    if (e + j < len) R[base + e + j] = g4[j];
+                    if (e + j < len) Rt[e + j] = g4[j];
             }
         }
         if (!__syncthreads_or(flags != 0)) {
@@ -439,68 +462,76 @@ __global__ void __launch_bounds__(NT) ada_scan(const SegPlan* __restrict__ plan,
     }
 }
 
-// One warp per run of tiles: emit (index, sign(G)*scale) at the ordered slot
-// and fix the residue.  A learner whose total exceeds cap sends nothing; its
-// residue keeps G = R + dW (already stored by ada_bins).
+// Last segment whose first element is <= idx.
+__device__ __forceinline__ int find_segment_by_index(const SegPlan* plan, int S, uint32_t idx) {
+    int lo = 0, hi = S;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(&plan[mid].off) <= idx) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+// One thread per pool entry: the entry's index gives its segment and tile,
+// and its distance from the tile's pool base gives its rank inside the tile,
+// so its output slot is (entries of the learner's earlier segments) + (the
+// tile's first slot in its segment) + rank.  It writes (index,
+// sign(G)*scale) there and fixes the residue R = G - sign(G)*scale.  A
+// learner whose total exceeds cap sends nothing; its residue keeps G = R + dW
+// (already stored by ada_bins).  seg_out: K*S words of shared memory.
 __global__ void __launch_bounds__(NT) ada_emit(const SegPlan* __restrict__ plan, int S, uint64_t N,
-                                               uint32_t tiles_per_learner, uint64_t total_tiles,
-                                               uint64_t tiles_per_warp, const uint2* __restrict__ tile_tab,
+                                               uint32_t tiles_per_learner, const uint2* __restrict__ tile_tab,
                                                const uint32_t* __restrict__ tile_rel, const uint2* __restrict__ pool,
-                                               uint64_t pool_cap, const int64_t* __restrict__ counts,
-                                               const float* __restrict__ scales, float* __restrict__ R,
-                                               gcsgd_pair* __restrict__ out, uint64_t cap, int K,
-                                               int64_t* __restrict__ totals) {
-    const int lane = threadIdx.x & 31;
-    const uint64_t gw = ((uint64_t)blockIdx.x * NT + threadIdx.x) >> 5;
-    if (blockIdx.x == 0 && threadIdx.x < 32) {
-        for (int k = 0; k < K; ++k) {
-            int64_t sum = 0;
-            for (int s = lane; s < S; s += 32) sum += counts[(uint64_t)k * S + s];
-            for (int d = 16; d > 0; d >>= 1) sum += __shfl_down_sync(kFull, sum, d);
-            if (lane == 0) totals[k] = sum;
+                                               const uint32_t* __restrict__ pool_cnt, uint64_t pool_cap,
+                                               const int64_t* __restrict__ counts, const float* __restrict__ scales,
+                                               float* __restrict__ R, gcsgd_pair* __restrict__ out, uint64_t cap,
+                                               int K, int64_t* __restrict__ totals) {
+    extern __shared__ __align__(8) unsigned char emit_smem[];
+    uint64_t* s_total = reinterpret_cast<uint64_t*>(emit_smem);            // [K] entries of each learner
+    uint32_t* seg_out = reinterpret_cast<uint32_t*>(emit_smem + 8 * K);  // [K][S] first slot of each segment
+    __shared__ uint64_t scan[NT / 32 + 1];
+    for (int k = 0; k < K; ++k) {
+        uint64_t run = 0;
+        for (int sb = 0; sb < S; sb += NT) {
+            const int s = sb + (int)threadIdx.x;
+            const uint64_t c = s < S ? (uint64_t)counts[(uint64_t)k * S + s] : 0;
+            uint64_t tot;
+            const uint64_t ex = block_exclusive_scan<NT>(c, scan, &tot);
+            if (s < S) seg_out[k * S + s] = (uint32_t)(run + ex);
+            run += tot;
+        }
+        if (threadIdx.x == 0) {
+            s_total[k] = run;
+            if (blockIdx.x == 0) totals[k] = (int64_t)run;
         }
     }
-    const uint64_t t0 = gw * tiles_per_warp;
-    uint64_t t1 = t0 + tiles_per_warp;
-    if (t1 > total_tiles) t1 = total_tiles;
-    int cur_k = -1, cur_s = -1;
-    int64_t unit_off = 0, learner_total = 0;
-    float scale = 0.0f;
-    for (uint64_t t = t0; t < t1; ++t) {
-        const uint2 ent = tile_tab[t];
-        if (ent.y == 0) continue;
-        const uint32_t k = (uint32_t)t / tiles_per_learner;
-        const uint32_t lt = (uint32_t)t - k * tiles_per_learner;
-        const int s = find_segment_by_tile(plan, S, lt);
-        if ((int)k != cur_k || s != cur_s) {
-            int64_t before = 0, all = 0;
-            for (int q = lane; q < S; q += 32) {
-                const int64_t c = counts[(uint64_t)k * S + q];
-                all += c;
-                if (q < s) before += c;
-            }
-            for (int d = 16; d > 0; d >>= 1) {
-                before += __shfl_down_sync(kFull, before, d);
-                all += __shfl_down_sync(kFull, all, d);
-            }
-            unit_off = __shfl_sync(kFull, before, 0);
-            learner_total = __shfl_sync(kFull, all, 0);
-            scale = scales[(uint64_t)k * S + s];
-            cur_k = (int)k;
-            cur_s = s;
-        }
-        if ((uint64_t)learner_total > cap) continue;  // nothing sent: residue keeps G
-        const uint2* src = pool + (uint64_t)k * pool_cap + ent.x;
-        const uint64_t slot0 = (uint64_t)unit_off + tile_rel[t];
-        for (uint32_t j = lane; j < ent.y; j += 32) {
-            const uint2 it = src[j];
+    __syncthreads();
+    const uint64_t stride = (uint64_t)gridDim.x * NT;
+    for (int k = 0; k < K; ++k) {
+        if (s_total[k] > cap) continue;  // nothing sent
+        const uint32_t pc = pool_cnt[k];
+        const uint2* src = pool + (uint64_t)k * pool_cap;
+        const uint2* tt = tile_tab + (uint64_t)k * tiles_per_learner;
+        const uint32_t* tr = tile_rel + (uint64_t)k * tiles_per_learner;
+        float* Rk = R + (uint64_t)k * N;
+        gcsgd_pair* ok = out + (uint64_t)k * cap;
+        for (uint64_t q = (uint64_t)blockIdx.x * NT + threadIdx.x; q < pc; q += stride) {
+            const uint2 it = src[q];
+            const int s = find_segment_by_index(plan, S, it.x);
+            const SegPlan p = plan[s];
+            const uint32_t t = p.tile_off + (it.x - p.off) / p.tile_len;
+            const uint2 ent = tt[t];
+            const uint64_t slot = (uint64_t)seg_out[k * S + s] + tr[t] + ((uint32_t)q - ent.x);
             const float g = __uint_as_float(it.y);
-            const float q = g > 0.0f ? scale : -scale;
-            R[(uint64_t)k * N + it.x] = __fsub_rn(g, q);
-            gcsgd_pair pr;
-            pr.idx = it.x;
-            pr.val = q;
-            out[(uint64_t)k * cap + slot0 + j] = pr;
+            const float scale = scales[(uint64_t)k * S + s];
+            const float val = g > 0.0f ? scale : -scale;
+            Rk[it.x] = __fsub_rn(g, val);
+            if (slot < cap) {
+                gcsgd_pair pr;
+                pr.idx = it.x;
+                pr.val = val;
+                ok[slot] = pr;
+            }
         }
     }
 }
@@ -544,7 +575,7 @@ int adacomp_launch(const int64_t* off, int S, const int32_t* lt, int K, const fl
         }
         if ((rc = check_launch("ada_plan"))) return rc;
     }
-    const uint64_t grid_cap = (uint64_t)sm_count() * 2;
+    const uint64_t grid_cap = (uint64_t)sm_count() * 3;
     if (hp.big_per_learner > 0 && T > 0) {
         LaunchScope ls("ada_bigmax", stream);
         ada_bigmax<<<(unsigned)(T < grid_cap ? T : grid_cap), NT, 0, stream>>>(
@@ -567,13 +598,25 @@ int adacomp_launch(const int64_t* off, int S, const int32_t* lt, int K, const fl
     }
     {
         LaunchScope ls("ada_emit", stream);
-        const uint64_t warps = (uint64_t)sm_count() * 8 * (NT / 32);
-        const uint64_t per = T ? (T + warps - 1) / warps : 1;
-        const uint64_t nw = T ? (T + per - 1) / per : 1;
-        const unsigned grid = (unsigned)((nw + NT / 32 - 1) / (NT / 32));
-        ada_emit<<<grid, NT, 0, stream>>>(w.plan, S, N, (uint32_t)hp.tiles_per_learner, T, per, w.tile_tab,
-                                          w.tile_rel, w.pool, (uint64_t)cap, counts, scales, R, out, (uint64_t)cap, K,
-                                          totals);
+        const size_t smem = sizeof(uint32_t) * (size_t)K * S + sizeof(uint64_t) * (size_t)K;
+        if (smem > 200 * 1024)
+            return set_error(GCSGD_ERR_INVALID_ARG, "adacomp_compress: K * n_seg = %d too large (at most ~51000)",
+                             K * S);
+        if (smem > 48 * 1024) {
+            static bool done[64] = {};
+            int dev = 0;
+            cudaGetDevice(&dev);
+            if (dev < 64 && !done[dev]) {
+                if (cudaFuncSetAttribute(ada_emit, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
+                    cudaSuccess)
+                    return set_error(GCSGD_ERR_CUDA, "adacomp_compress: cannot raise the shared-memory limit");
+                done[dev] = true;
+            }
+        }
+        ada_emit<<<(unsigned)sm_count() * 4, NT, smem, stream>>>(w.plan, S, N, (uint32_t)hp.tiles_per_learner,
+                                                                 w.tile_tab, w.tile_rel, w.pool, w.pool_cnt,
+                                                                 (uint64_t)cap, counts, scales, R, out,
+                                                                 (uint64_t)cap, K, totals);
         if ((rc = check_launch("ada_emit"))) return rc;
     }
     return GCSGD_OK;

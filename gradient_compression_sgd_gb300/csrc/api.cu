@@ -256,7 +256,7 @@ int adacomp_compress(const int64_t* seg_offsets, int32_t n_seg, const int32_t* l
 int sparse_average(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int32_t K, int64_t n, float* out,
                    void* stream) {
     const char* fn = "sparse_average";
-    if (K < 1 || K > 4096) return set_error(GCSGD_ERR_INVALID_ARG, "%s: K = %d outside [1, 4096]", fn, K);
+    if (K < 1 || K > 512) return set_error(GCSGD_ERR_INVALID_ARG, "%s: K = %d outside [1, 512]", fn, K);
     if (n < 0 || n > ((int64_t)1 << 32)) return set_error(GCSGD_ERR_INVALID_ARG, "%s: n outside [0, 2^32]", fn);
     if (cap < 0) return set_error(GCSGD_ERR_INVALID_ARG, "%s: cap < 0", fn);
     if (!counts || (n > 0 && !out) || (cap > 0 && !lists))

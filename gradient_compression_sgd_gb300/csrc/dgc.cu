@@ -38,8 +38,7 @@ namespace dgc {
 
 constexpr int NT = 256;                  // threads per CTA of dgc_update and dgc_sumsq
 constexpr int NTS = 512;                 // threads per CTA of dgc_select
-constexpr int NTP = 256;                 // threads per CTA of dgc_prepare
-constexpr int kHintBits = 12;            // hint histogram: top 12 bits of |v| (1/16 of a binade)
+constexpr int NTP = 512;                 // threads per CTA of dgc_prepare
 constexpr uint32_t kSmallK = 32;         // raw segments with k <= 32 ...
 constexpr uint32_t kSmallN = 8192;       // ... and at most 8192 values use the register top-k
 constexpr int kTile = 4096;              // elements per dgc_update tile (NT x 4 float4)
@@ -83,12 +82,14 @@ int host_plan(const int64_t* off, int S, double density, HostPlan* hp) {
     hp->tiles_per_learner = 0;
     hp->pool_per_learner = 0;
     hp->out_per_learner = 0;
+    hp->pool_segments = 0;
     for (int s = 0; s < S; ++s) {
         SegPlan p;
         seg_fields((uint32_t)(off[s + 1] - off[s]), density, &p);
         hp->tiles_per_learner += p.ntiles;
         hp->pool_per_learner += p.cap;
         hp->out_per_learner += p.k;
+        hp->pool_segments += p.kind == kKindPool;
     }
     return 0;
 }
@@ -145,68 +146,36 @@ __device__ __forceinline__ void dgc_elem(float g, float& u, float& v, float m, f
     v = __fadd_rn(v, u);
 }
 
-// Lower edge of the histogram bucket that holds the rank-th largest counted
-// key (buckets from the top); *above receives the count in higher buckets.
-// hist has NB buckets; every thread of the CTA must call it.
-template <int NT, int NB>
-__device__ uint32_t crossing_bucket(const uint32_t* hist, uint32_t rank, uint64_t* scan, uint32_t* s_out,
-                                    uint32_t* above_out) {
-    constexpr int W = NB / NT;
-    const int hi = NB - (int)threadIdx.x * W;
-    uint32_t mine = 0;
-    for (int b = hi - 1; b >= hi - W; --b) mine += hist[b];
-    uint64_t tot;
-    uint32_t above = (uint32_t)block_exclusive_scan<NT>(mine, scan, &tot);
-    if (threadIdx.x == 0) {
-        s_out[0] = 0;
-        s_out[1] = 0;
-    }
-    __syncthreads();
-    for (int b = hi - 1; b >= hi - W; --b) {
-        const uint32_t h = hist[b];
-        if (above < rank && rank <= above + h) {
-            s_out[0] = (uint32_t)b;
-            s_out[1] = above;
-        }
-        above += h;
-    }
-    __syncthreads();
-    const uint32_t r = s_out[0];
-    *above_out = s_out[1];
-    __syncthreads();
-    return r;
-}
-
-// CTA 0 first writes the per-segment plan, the clip scales and the order in
-// which dgc_select takes the segments (largest first).  Then the CTAs walk
-// the (learner, segment) units with a grid stride: a segment with a
-// candidate pool samples m of its values in 32-element blocks spread evenly
-// over it and computes the updated |v| there exactly as dgc_update will.  The
-// hint is the a-th largest sampled key (a = R m / n for R = max(2.5k, 512)
-// expected candidates), located by a 12-bit histogram of the keys and a
-// second 12-bit histogram inside the bucket that holds it, and rounded down
-// to that second bucket's edge (within 2^-16 of the sample).  Being a rank
-// estimate, it keeps the candidate count near R whatever the distribution of
+// The last CTA writes the per-segment plan, the clip scales and the order in
+// which dgc_select takes the segments (largest first).  The other CTAs walk
+// the (learner, segment) units that have a candidate pool, one per CTA when
+// there are enough CTAs: each samples m of the segment's values in
+// 32-element blocks spread evenly over it and computes the updated |v|
+// there exactly as dgc_update will.  The
+// hint is the a-th largest sampled key (a = R m / n <= 48 for R =
+// max(2.5k, 512) expected candidates), found exactly by radix select over the
+// sampled keys held in shared memory.
+// Being a rank estimate, it keeps the candidate count near R whatever the
+// distribution of
 // |v| -- including the pile-up of entries just below the send threshold that
 // accumulation builds.  The hint only steers speed: dgc_select checks that
 // the pool holds the top k.
 template <int MAXS>
-__global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, int S, int K, double density,
+__global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, PoolList<MAXS> pl, int S, int K,
+                                                     double density,
                                                      float clip_thr, int clip_nodes, const double* __restrict__ part,
                                                      SegPlan* __restrict__ plan, float* __restrict__ clip_c,
                                                      uint16_t* __restrict__ order, uint64_t N,
                                                      const float* __restrict__ grad, const float* __restrict__ u,
                                                      const float* __restrict__ v, float momentum,
                                                      uint32_t* __restrict__ hint, uint32_t* __restrict__ pool_cnt) {
-    constexpr int NB = 1 << kHintBits;
     extern __shared__ __align__(16) uint32_t keys[];  // kSampleMax
-    __shared__ uint32_t hist[NB];
+    __shared__ uint32_t hist[2048];
     __shared__ uint64_t scan[NTP / 32 + 1];
     __shared__ uint64_t carry[3];
-    __shared__ SegPlan s_p;
     __shared__ float s_c;
-    __shared__ uint32_t s_sel[2];
-    if (blockIdx.x == 0) {
+    __shared__ uint32_t s_sel[4];
+    if (blockIdx.x == gridDim.x - 1) {  // the extra CTA: plan, order, clip scales
         if (threadIdx.x < 3) carry[threadIdx.x] = 0;
         __syncthreads();
         for (int base = 0; base < S; base += NTP) {
@@ -246,24 +215,25 @@ __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, int S
             __syncthreads();
         }
         for (int k = threadIdx.x; k < K; k += NTP) clip_c[k] = clip_scale(part, k, clip_thr, clip_nodes);
+        return;
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int unit = blockIdx.x; unit < K * S; unit += gridDim.x) {
-        const int k = unit / S, s = unit - k * S;
-        if (threadIdx.x == 0) {  // one thread evaluates the plan (fp64 and 64-bit integer math)
-            seg_fields(so.off[s + 1] - so.off[s], density, &s_p);
-            s_p.off = so.off[s];
-            s_c = s_p.kind == kKindPool ? clip_scale(part, k, clip_thr, clip_nodes) : 1.0f;
+    const int P = (int)pl.n_pool;
+    const int samplers = (int)gridDim.x - 1;
+    for (int pj = blockIdx.x; pj < K * P; pj += samplers) {  // only segments with a candidate pool
+        const int k = pj / P, q = pj - k * P;
+        const int s = pl.seg[q];
+        const int unit = k * S + s;
+        if (threadIdx.x == 0) {
+            s_c = clip_scale(part, k, clip_thr, clip_nodes);
             pool_cnt[unit] = 0;
-            if (s_p.kind != kKindPool) hint[unit] = 0xffffffffu;  // no candidates
         }
-        for (int b = threadIdx.x; b < NB; b += NTP) hist[b] = 0;
         __syncthreads();
-        const SegPlan p = s_p;
-        if (p.kind != kKindPool) {
-            __syncthreads();
-            continue;
-        }
+        SegPlan p;
+        p.off = so.off[s];
+        p.n = so.off[s + 1] - so.off[s];
+        p.m = pl.m[q];
+        p.a = pl.a[q];
         const float c = s_c;
         const uint32_t nblk = p.m / 32;
         const uint32_t stride = p.n / nblk;  // >= 512 since m <= n / 16
@@ -272,8 +242,8 @@ __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, int S
         const float* us = u + base;
         const float* vs = v + base;
         // sample element 32 b + lane sits at b * stride + lane; a warp issues
-        // the loads of 12 blocks before using any of them
-        constexpr int kB = 12;
+        // the loads of 8 blocks before using any of them
+        constexpr int kB = 8;
         for (uint32_t b0 = warp; b0 < nblk; b0 += kB * (NTP / 32)) {
             float gg[kB], uu[kB], vv[kB];
 #pragma unroll
@@ -292,25 +262,14 @@ __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, int S
                 const uint32_t b = b0 + j * (NTP / 32);
                 if (b < nblk) {
                     dgc_elem(gg[j], uu[j], vv[j], momentum, c);
-                    const uint32_t key = mag_key(vv[j]);
-                    keys[b * 32 + lane] = key;
-                    atomicAdd(&hist[key >> (31 - kHintBits)], 1u);
+                    keys[b * 32 + lane] = mag_key(vv[j]);
                 }
             }
         }
         __syncthreads();
-        uint32_t above;
-        const uint32_t b1 = crossing_bucket<NTP, NB>(hist, p.a, scan, s_sel, &above);
-        const uint32_t need = p.a - above;
-        for (int b = threadIdx.x; b < NB; b += NTP) hist[b] = 0;
-        __syncthreads();
-        for (uint32_t i = threadIdx.x; i < p.m; i += NTP) {
-            const uint32_t key = keys[i];
-            if ((key >> (31 - kHintBits)) == b1) atomicAdd(&hist[(key >> (31 - 2 * kHintBits)) & (NB - 1)], 1u);
-        }
-        __syncthreads();
-        const uint32_t b2 = crossing_bucket<NTP, NB>(hist, need, scan, s_sel, &above);
-        const uint32_t h = (b1 << (31 - kHintBits)) | (b2 << (31 - 2 * kHintBits));
+        const SelectResult sr = radix_select_desc<NTP>(
+            [&](uint64_t i, uint32_t* key) { *key = keys[i]; return true; }, p.m, p.a, hist, scan, s_sel);
+        const uint32_t h = sr.thresh;
         if (threadIdx.x == 0) hint[unit] = h > 1u ? h : 1u;
         __syncthreads();
     }
@@ -349,7 +308,7 @@ __global__ void __launch_bounds__(NT, 3) dgc_update(const SegPlan* __restrict__ 
         const uint32_t len = p.n - start < (uint32_t)kTile ? p.n - start : (uint32_t)kTile;
         const uint64_t base = (uint64_t)k * N + p.off + start;
         const uint32_t unit = k * S + s;
-        const uint32_t h = __ldg(&hint[unit]);
+        const uint32_t h = p.kind == kKindPool ? __ldg(&hint[unit]) : 0xffffffffu;  // no candidates
         const float c = __ldg(&clip_c[k]);
         const bool aligned = (base & 3) == 0;
 
@@ -835,18 +794,35 @@ int dgc_launch(const int64_t* off, int S, int K, const float* grad, float* u, fl
     {
         LaunchScope ls("dgc_prepare", stream);
         const size_t smem = kSampleMax * sizeof(uint32_t);
-        const unsigned prep_grid = units < (unsigned)sm_count() * 2 ? units : (unsigned)sm_count() * 2;
+        auto fill = [&](auto& so, auto& pl) {
+            pl.n_pool = 0;
+            for (int s = 0; s <= S; ++s) so.off[s] = (uint32_t)off[s];
+            for (int s = 0; s < S; ++s) {
+                SegPlan sp;
+                seg_fields((uint32_t)(off[s + 1] - off[s]), density, &sp);
+                if (sp.kind != kKindPool) continue;
+                pl.seg[pl.n_pool] = (uint16_t)s;
+                pl.m[pl.n_pool] = sp.m;
+                pl.a[pl.n_pool] = sp.a;
+                ++pl.n_pool;
+            }
+        };
+        const unsigned pool_units = (unsigned)K * (unsigned)hp.pool_segments;
+        const unsigned slots = (unsigned)sm_count() * 2 - 1;  // two CTAs of NTP threads per SM
+        const unsigned prep_grid = (pool_units < slots ? pool_units : slots) + 1;  // + the plan CTA
         if (S <= 256) {
             SegOffsets<256> so;
-            for (int s = 0; s <= S; ++s) so.off[s] = (uint32_t)off[s];
-            dgc_prepare<256><<<prep_grid, NTP, smem, stream>>>(so, S, K, density, clip_thr, clip_nodes, w.clip_part,
-                                                               w.plan, w.clip_c, w.order, N, grad, u, v, momentum,
-                                                               w.hint, w.pool_cnt);
+            PoolList<256> pl;
+            fill(so, pl);
+            dgc_prepare<256><<<prep_grid, NTP, smem, stream>>>(so, pl, S, K, density, clip_thr, clip_nodes,
+                                                               w.clip_part, w.plan, w.clip_c, w.order, N, grad, u, v,
+                                                               momentum, w.hint, w.pool_cnt);
         } else {
             SegOffsets<GCSGD_MAX_SEGMENTS> so;
-            for (int s = 0; s <= S; ++s) so.off[s] = (uint32_t)off[s];
+            PoolList<GCSGD_MAX_SEGMENTS> pl;
+            fill(so, pl);
             dgc_prepare<GCSGD_MAX_SEGMENTS><<<prep_grid, NTP, smem, stream>>>(
-                so, S, K, density, clip_thr, clip_nodes, w.clip_part, w.plan, w.clip_c, w.order, N, grad, u, v,
+                so, pl, S, K, density, clip_thr, clip_nodes, w.clip_part, w.plan, w.clip_c, w.order, N, grad, u, v,
                 momentum, w.hint, w.pool_cnt);
         }
         if ((rc = check_launch("dgc_prepare"))) return rc;

@@ -33,10 +33,21 @@ struct SegOffsets {
     uint32_t off[MAXS + 1];
 };
 
+// Segments with a candidate pool and their sample sizes, from the host plan
+// (passed by value so the sampling CTAs need no fp64 or 64-bit division).
+template <int MAXS>
+struct PoolList {
+    uint32_t n_pool;
+    uint16_t seg[MAXS];
+    uint32_t m[MAXS];  // sample size (multiple of 32)
+    uint32_t a[MAXS];  // rank of the hint within the sample
+};
+
 struct HostPlan {
     uint64_t tiles_per_learner;
     uint64_t pool_per_learner;
     uint64_t out_per_learner;
+    uint64_t pool_segments;
 };
 
 struct DgcWorkspace {

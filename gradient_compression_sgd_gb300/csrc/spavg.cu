@@ -9,12 +9,15 @@
 // in it are added in list order k = 0..K-1 (entries inside one list have
 // distinct indices, so the adds of one k never collide; a barrier between
 // lists keeps the fp32 sum in k order, bit-identical to the definition),
-// then the tile is divided by K and written to HBM with 128-bit stores.  A
-// CTA first finds, for every list, the run of entries inside its whole index
-// range (both ends searched in parallel, 32 probes per round trip) and copies
-// those entries to shared memory in one round of loads, so its tiles need no
-// further global reads.  The dense output is written exactly once and each
-// entry is read once, which is the minimum traffic.
+// then the tile is divided by K and written to HBM with 128-bit stores.  Each
+// list keeps a window of its next entries staged in shared memory, refilled
+// (one round of loads) only when it no longer reaches past the current tile,
+// so most tiles need no global reads.  Each warp owns 512 output indices of
+// the tile and adds, for its indices, list 0, then list 1, ..., so the
+// learner order holds with warp-level synchronisation only.  The dense output
+// is written exactly once and each entry is read once (a list denser than its
+// window in some tile is read in place for that tile), which is the minimum
+// traffic.
 #include "common.cuh"
 
 namespace gcsgd {
@@ -23,7 +26,7 @@ namespace spavg {
 constexpr int NT = 256;
 constexpr int NW = NT / 32;
 constexpr uint32_t kTile = 4096;   // output elements per shared-memory tile
-constexpr uint32_t kStage = 2048;  // list entries a CTA stages for its whole index range
+constexpr uint32_t kStage = 4096;  // list entries a CTA keeps staged (split evenly among the K lists)
 
 // First position p in [0, cnt] with list[p].idx >= target, for a list sorted
 // ascending; 32 probes per round trip.  Called by a whole warp.
@@ -56,14 +59,18 @@ __device__ __forceinline__ float div_k(float x, float fk, float inv_k, bool pow2
     return pow2 ? __fmul_rn(x, inv_k) : __fdiv_rn(x, fk);
 }
 
-__device__ __forceinline__ void store_tile(const float* acc, float* out, uint64_t r0, uint64_t r1, float fk) {
+// Writes acc / K for the output range [r0, r1) and leaves acc zeroed for the
+// next tile.
+__device__ __forceinline__ void store_tile(float* acc, float* out, uint64_t r0, uint64_t r1, float fk) {
     const uint64_t len = r1 - r0;
     const int K = (int)fk;
     const bool pow2 = (K & (K - 1)) == 0;
     const float inv_k = 1.0f / fk;
     const bool out_aligned = ((uintptr_t)(out + r0) & 15) == 0;
-    for (uint32_t j = threadIdx.x * 4; j < len; j += NT * 4) {
+    for (uint32_t j = threadIdx.x * 4; j < kTile; j += NT * 4) {
         float4 q = *reinterpret_cast<const float4*>(acc + j);
+        *reinterpret_cast<float4*>(acc + j) = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j >= len) continue;
         if ((__float_as_uint(q.x) | __float_as_uint(q.y) | __float_as_uint(q.z) | __float_as_uint(q.w)) != 0u) {
             q.x = div_k(q.x, fk, inv_k, pow2);
             q.y = div_k(q.y, fk, inv_k, pow2);
@@ -79,18 +86,42 @@ __device__ __forceinline__ void store_tile(const float* acc, float* out, uint64_
     }
 }
 
-// Shared memory: acc[kTile] | stage[kStage] pairs | lo[K] hi[K] cnt[K] (u64) | soff[K+1] sptr[K] (u32)
+// First position in [a, b) of a sorted run whose index is >= target.
+__device__ __forceinline__ uint32_t lower_in(const gcsgd_pair* st, uint32_t a, uint32_t b, uint64_t target) {
+    while (a < b) {
+        const uint32_t m = (a + b) >> 1;
+        if ((uint64_t)st[m].idx < target) a = m + 1; else b = m;
+    }
+    return a;
+}
+
+// First position in [a, b) of a sorted list in global memory whose index is >= target.
+__device__ __forceinline__ uint64_t lower_global(const gcsgd_pair* L, uint64_t a, uint64_t b, uint64_t target) {
+    while (a < b) {
+        const uint64_t m = (a + b) >> 1;
+        if ((uint64_t)__ldg(&L[m].idx) < target) a = m + 1; else b = m;
+    }
+    return a;
+}
+
+// Shared memory: acc[kTile] | stage[kStage] pairs | per list (u64): cnt, ptr, wbeg |
+// (u32): wlen, flag, soff[K+1] | bnd[K][NW+1] (u32)
 __global__ void __launch_bounds__(NT) spavg_kernel(const gcsgd_pair* __restrict__ lists, uint64_t cap,
                                                    const int64_t* __restrict__ counts, int K, uint64_t n,
-                                                   float* __restrict__ out, uint64_t tiles, uint64_t tiles_per_cta) {
+                                                   float* __restrict__ out, uint64_t tiles, uint64_t tiles_per_cta,
+                                                   uint32_t C) {
     extern __shared__ __align__(16) unsigned char smem[];
     float* acc = reinterpret_cast<float*>(smem);
     gcsgd_pair* stage = reinterpret_cast<gcsgd_pair*>(smem + kTile * sizeof(float));
-    uint64_t* lo = reinterpret_cast<uint64_t*>(smem + kTile * sizeof(float) + kStage * sizeof(gcsgd_pair));
-    uint64_t* hi = lo + K;
-    uint64_t* cnt = hi + K;
-    uint32_t* soff = reinterpret_cast<uint32_t*>(cnt + K);  // list k staged at [soff[k], soff[k+1])
-    uint32_t* sptr = soff + K + 1;                           // first staged entry not yet added
+    const size_t stage_items = (size_t)K * C > kStage ? (size_t)K * C : kStage;  // as sized by the host
+    uint64_t* cnt = reinterpret_cast<uint64_t*>(smem + kTile * sizeof(float) + stage_items * sizeof(gcsgd_pair));
+    uint64_t* ptr = cnt + K;   // first entry of list k not yet added (global position)
+    uint64_t* wbeg = ptr + K;  // global position of the first staged entry of list k
+    uint32_t* wlen = reinterpret_cast<uint32_t*>(wbeg + K);  // staged entries of list k
+    uint32_t* flag = wlen + K;                               // window k refills / list k is dense in this tile
+    uint32_t* soff = flag + K;                               // range staging: list k at [soff[k], soff[k+1])
+    uint32_t* bnd = soff + K + 1;                            // [K][NW+1] slice bounds within the windows
+    __shared__ int s_any;
     __shared__ uint32_t s_total;
     const uint64_t t0 = (uint64_t)blockIdx.x * tiles_per_cta;
     if (t0 >= tiles) return;
@@ -98,36 +129,42 @@ __global__ void __launch_bounds__(NT) spavg_kernel(const gcsgd_pair* __restrict_
     const uint64_t R0 = t0 * kTile, R1 = t1 * kTile < n ? t1 * kTile : n;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float fk = (float)K;
+    constexpr uint32_t kSpan = kTile / NW;  // output indices owned by one warp within a tile
 
     for (int k = threadIdx.x; k < K; k += NT) {
         const int64_t c = counts[k];
         cnt[k] = c < 0 ? 0 : ((uint64_t)c > cap ? cap : (uint64_t)c);
+        wlen[k] = 0;
     }
     __syncthreads();
     // each list's run inside this CTA's index range [R0, R1): both ends searched in parallel
     for (int q = warp; q < 2 * K; q += NW) {
         const int k = q < K ? q : q - K;
         const uint64_t p = warp_lower_bound(lists + (uint64_t)k * cap, cnt[k], q < K ? R0 : R1);
-        if (lane == 0) (q < K ? lo : hi)[k] = p;
+        if (lane == 0) {
+            if (q < K) ptr[k] = p;
+            else wbeg[k] = p;  // temporarily: the run's end
+        }
+        __syncwarp();
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        uint32_t run = 0;
-        bool fits = true;
+        uint64_t run = 0;
         for (int k = 0; k < K; ++k) {
-            soff[k] = run;
-            const uint64_t c = hi[k] > lo[k] ? hi[k] - lo[k] : 0;
-            if (run + c > kStage) fits = false;
-            run = fits ? run + (uint32_t)c : run;
+            soff[k] = (uint32_t)(run < kStage ? run : kStage);
+            run += wbeg[k] > ptr[k] ? wbeg[k] - ptr[k] : 0;
         }
-        soff[K] = run;
-        s_total = fits ? run : 0xffffffffu;
+        soff[K] = (uint32_t)(run < kStage ? run : kStage);
+        s_total = run <= kStage ? (uint32_t)run : 0xffffffffu;
     }
+    for (uint32_t j = threadIdx.x * 4; j < kTile; j += NT * 4)
+        *reinterpret_cast<float4*>(acc + j) = make_float4(0.f, 0.f, 0.f, 0.f);
     __syncthreads();
     const uint32_t total = s_total;
 
     if (total != 0xffffffffu) {
-        // stage every entry of the range once (four loads in flight per thread)
+        // The whole range's entries fit: stage them once (four loads in
+        // flight per thread); warp 0 adds them tile by tile in learner order.
         for (uint32_t q0 = 0; q0 < total; q0 += 4 * NT) {
             gcsgd_pair it[4];
             int kk[4];
@@ -142,26 +179,21 @@ __global__ void __launch_bounds__(NT) spavg_kernel(const gcsgd_pair* __restrict_
                         if (soff[m] <= q) k = m; else kh = m;
                     }
                     kk[j] = k;
-                    it[j] = lists[(uint64_t)k * cap + lo[k] + (q - soff[k])];
+                    it[j] = lists[(uint64_t)k * cap + ptr[k] + (q - soff[k])];
                 }
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 if (kk[j] >= 0) stage[q0 + j * NT + threadIdx.x] = it[j];
         }
-        for (int k = threadIdx.x; k < K; k += NT) sptr[k] = soff[k];
+        for (int k = threadIdx.x; k < K; k += NT) wlen[k] = soff[k];  // reuse: next staged entry of list k
         __syncthreads();
         for (uint64_t t = t0; t < t1; ++t) {
             const uint64_t r0 = t * kTile;
             const uint64_t r1 = r0 + kTile < n ? r0 + kTile : n;
-            for (uint32_t j = threadIdx.x * 4; j < kTile; j += NT * 4)
-                *reinterpret_cast<float4*>(acc + j) = make_float4(0.f, 0.f, 0.f, 0.f);
-            __syncthreads();
             if (warp == 0) {
-                // warp 0 adds the lists in learner order; within a list the
-                // indices are distinct, so its lanes never collide
                 for (int k = 0; k < K; ++k) {
-                    uint32_t a = sptr[k];
+                    uint32_t a = wlen[k];
                     const uint32_t e = soff[k + 1];
                     for (;;) {
                         const uint32_t i = a + lane;
@@ -179,52 +211,105 @@ __global__ void __launch_bounds__(NT) spavg_kernel(const gcsgd_pair* __restrict_
                         if (c < 32) break;
                     }
                     __syncwarp();  // list k's adds land before list k+1's
-                    if (lane == 0) sptr[k] = a;
+                    if (lane == 0) wlen[k] = a;
                 }
             }
             __syncthreads();
-            store_tile(acc, out, r0, r1, fk);
+            store_tile(acc, out, r0, r1, fk);  // also re-zeroes acc
             __syncthreads();
         }
         return;
     }
 
-    // More entries than fit the stage (dense lists): walk each tile's entries in global memory.
-    uint64_t* ptr = lo;
-    uint64_t* end = hi;
+    // Too many entries for one staging: each list keeps a window of C of its
+    // next entries, refilled when it no longer reaches past the tile; each
+    // warp owns kSpan output indices of the tile and adds the lists in order.
+    for (int k = threadIdx.x; k < K; k += NT) wbeg[k] = ptr[k];
+    __syncthreads();
     for (uint64_t t = t0; t < t1; ++t) {
         const uint64_t r0 = t * kTile;
         const uint64_t r1 = r0 + kTile < n ? r0 + kTile : n;
-        for (uint32_t j = threadIdx.x * 4; j < kTile; j += NT * 4)
-            *reinterpret_cast<float4*>(acc + j) = make_float4(0.f, 0.f, 0.f, 0.f);
-        __syncthreads();  // everyone has read hi[] before it is reused as end[]
-        for (int k = warp; k < K; k += NW) {
-            const gcsgd_pair* L = lists + (uint64_t)k * cap;
-            uint64_t e = ptr[k];
-            for (;;) {
-                const uint64_t q = e + lane;
-                const bool in = q < cnt[k] && (uint64_t)__ldg(&L[q].idx) < r1;
-                const unsigned b = __ballot_sync(kFull, in);
-                const int c = __popc(b);
-                e += c;
-                if (c < 32) break;
+        if (threadIdx.x == 0) s_any = 0;
+        __syncthreads();
+        for (int k = threadIdx.x; k < K; k += NT) {
+            const gcsgd_pair* st = stage + (size_t)k * C;
+            const bool covers = wbeg[k] + wlen[k] == cnt[k] || (wlen[k] > 0 && (uint64_t)st[wlen[k] - 1].idx >= r1);
+            flag[k] = 0;
+            if (!covers) {
+                wbeg[k] = ptr[k];
+                const uint64_t left = cnt[k] - ptr[k];
+                wlen[k] = (uint32_t)(left < C ? left : C);
+                flag[k] = 1;
+                s_any = 1;
             }
-            if (lane == 0) end[k] = e;
         }
         __syncthreads();
-        for (int k = 0; k < K; ++k) {
-            const gcsgd_pair* L = lists + (uint64_t)k * cap;
-            for (uint64_t p = ptr[k] + threadIdx.x; p < end[k]; p += NT) {
-                const gcsgd_pair it = L[p];
-                if ((uint64_t)it.idx >= r0 && (uint64_t)it.idx < r1) {
-                    float* a = acc + (it.idx - r0);
-                    *a = __fadd_rn(*a, it.val);
+        if (s_any) {
+            for (int k = 0; k < K; ++k) {  // refill windows (four loads in flight per thread)
+                if (!flag[k] || wlen[k] == 0) continue;
+                const gcsgd_pair* L = lists + (uint64_t)k * cap + wbeg[k];
+                gcsgd_pair* st = stage + (size_t)k * C;
+                const uint32_t wl = wlen[k];
+                for (uint32_t q0 = 0; q0 < wl; q0 += 4 * NT) {
+                    gcsgd_pair it[4];
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const uint32_t q = q0 + jj * NT + threadIdx.x;
+                        if (q < wl) it[jj] = L[q];
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const uint32_t q = q0 + jj * NT + threadIdx.x;
+                        if (q < wl) st[q] = it[jj];
+                    }
                 }
             }
             __syncthreads();
         }
+        // slice bounds: one thread per (list, warp slice edge), all searched at once
+        for (int q = threadIdx.x; q < K * (NW + 1); q += NT) {
+            const int k = q / (NW + 1), w = q - k * (NW + 1);
+            const gcsgd_pair* st = stage + (size_t)k * C;
+            const bool covers = wbeg[k] + wlen[k] == cnt[k] || (wlen[k] > 0 && (uint64_t)st[wlen[k] - 1].idx >= r1);
+            if (w == 0) flag[k] = !covers;  // dense in this tile: read in place
+            const uint64_t edge = r0 + (uint64_t)w * kSpan < r1 ? r0 + (uint64_t)w * kSpan : r1;
+            bnd[q] = covers ? lower_in(st, (uint32_t)(ptr[k] - wbeg[k]), wlen[k], edge) : 0u;
+        }
+        __syncthreads();
+        const uint64_t s0 = r0 + (uint64_t)warp * kSpan;
+        const uint64_t s1 = s0 + kSpan < r1 ? s0 + kSpan : r1;
+        if (s0 < r1) {
+            for (int k = 0; k < K; ++k) {
+                if (!flag[k]) {
+                    const gcsgd_pair* st = stage + (size_t)k * C;
+                    const uint32_t a = bnd[k * (NW + 1) + warp], b = bnd[k * (NW + 1) + warp + 1];
+                    for (uint32_t i = a + lane; i < b; i += 32) {
+                        const gcsgd_pair it = st[i];
+                        if ((uint64_t)it.idx >= s0 && (uint64_t)it.idx < s1) {  // always, for sorted lists
+                            float* acc_j = acc + (it.idx - r0);
+                            *acc_j = __fadd_rn(*acc_j, it.val);
+                        }
+                    }
+                } else {
+                    const gcsgd_pair* L = lists + (uint64_t)k * cap;
+                    const uint64_t a = lower_global(L, ptr[k], cnt[k], s0);
+                    const uint64_t b = lower_global(L, a, cnt[k], s1);
+                    for (uint64_t i = a + lane; i < b; i += 32) {
+                        const gcsgd_pair it = L[i];
+                        if ((uint64_t)it.idx >= s0 && (uint64_t)it.idx < s1) {
+                            float* acc_j = acc + (it.idx - r0);
+                            *acc_j = __fadd_rn(*acc_j, it.val);
+                        }
+                    }
+                }
+                __syncwarp();  // list k's adds land before list k+1's
+            }
+        }
+        __syncthreads();
+        for (int k = threadIdx.x; k < K; k += NT)
+            ptr[k] = flag[k] ? lower_global(lists + (uint64_t)k * cap, ptr[k], cnt[k], r1)
+                             : wbeg[k] + bnd[k * (NW + 1) + NW];
         store_tile(acc, out, r0, r1, fk);
-        for (int k = threadIdx.x; k < K; k += NT) ptr[k] = end[k];
         __syncthreads();
     }
 }
@@ -236,12 +321,16 @@ int spavg_launch(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, in
     using namespace spavg;
     if (n == 0) return GCSGD_OK;
     const uint64_t tiles = ((uint64_t)n + kTile - 1) / kTile;
-    uint64_t grid = (uint64_t)sm_count() * 6;
+    uint64_t grid = (uint64_t)sm_count() * 4;
     if (grid > tiles) grid = tiles;
     const uint64_t per = (tiles + grid - 1) / grid;
     grid = (tiles + per - 1) / per;
-    const size_t smem = kTile * sizeof(float) + kStage * sizeof(gcsgd_pair) + 3 * sizeof(uint64_t) * (size_t)K +
-                        sizeof(uint32_t) * (2 * (size_t)K + 1);
+    uint32_t C = kStage / (uint32_t)K;  // window per list when the range does not fit the stage
+    if (C < 32) C = 32;
+    const size_t stage_items = (size_t)K * C > kStage ? (size_t)K * C : kStage;
+    const size_t smem = kTile * sizeof(float) + stage_items * sizeof(gcsgd_pair) + 3 * sizeof(uint64_t) * (size_t)K +
+                        sizeof(uint32_t) * (3 * (size_t)K + 1 + (size_t)K * (NW + 1));
+    if (smem > 200 * 1024) return set_error(GCSGD_ERR_INVALID_ARG, "sparse_average: K = %d too large", K);
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -251,7 +340,8 @@ int spavg_launch(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, in
         attr_set[dev] = true;
     }
     LaunchScope ls("spavg", stream);
-    spavg_kernel<<<(unsigned)grid, NT, smem, stream>>>(lists, (uint64_t)cap, counts, K, (uint64_t)n, out, tiles, per);
+    spavg_kernel<<<(unsigned)grid, NT, smem, stream>>>(lists, (uint64_t)cap, counts, K, (uint64_t)n, out, tiles, per,
+                                                       C);
     return check_launch("spavg");
 }
 

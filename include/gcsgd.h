@@ -189,7 +189,7 @@ int adacomp_compress(const int64_t* seg_offsets, int32_t n_seg, const int32_t* l
  *   out[j] = (sum over the lists k = 0..K-1 that contain j, added in that
  *             order in fp32 starting from +0) / K   (one fp32 divide),
  *   out[j] = 0 where no list contains j.
- * lists   [K][cap] pairs; list k is lists[k*cap .. k*cap + counts[k]),
+ * lists   [K][cap] pairs (K at most 512); list k is lists[k*cap .. k*cap + counts[k]),
  *         strictly ascending indices below n.  Entries that break this are
  *         skipped or misplaced but never cause an out-of-range access.
  * counts  [K] int64 device array (0 <= counts[k] <= cap).
