@@ -64,6 +64,23 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest `x` over all ranks of the default process group (x itself
+    when there is none): the job's time is its slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(world: int, bytes_per_rank: float, ms: float) -> float:
+    """Whole-job GB/s: every rank's bytes over the slowest rank's time."""
+    return world * bytes_per_rank / (ms * 1e-3) / 1e9
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -126,30 +143,66 @@ class ClockSampler:
 
 # --------------------------------------------------------- CPU oracle sample
 
-def oracle_sample(w, learner_grad: np.ndarray, target_s: float, min_steps: int = 1):
-    """Time the oracle's DGC step + average on every 4th tensor of learner 0.
-
-    Returns (gradient bytes processed, seconds, description)."""
-    import oracle
+def oracle_inputs(w):
+    """Learner 0's (or, for DCD, every node's) seeded step-0 input on the host,
+    cut to the bounded sample the oracle is timed on."""
+    from gradient_compression_sgd_gb300 import workloads as wl
+    if w.method == "dcd":
+        win = min(w.n, 1 << 20)
+        g = np.stack([wl.gradient(w, k, 0)[:win].numpy() for k in range(w.learners)])
+        x = np.ascontiguousarray(wl.dcd_initial_model(w)[:, :win].numpy())
+        return {"g": g, "x": x, "win": win}
+    grad = wl.gradient(w, 0, 0).numpy()
     sizes = np.asarray(w.sizes)
     pick = np.arange(0, len(sizes), 4)
     off = w.offsets
-    g = np.concatenate([learner_grad[off[s]:off[s + 1]] for s in pick])[None, :]
+    g = np.concatenate([grad[off[s]:off[s + 1]] for s in pick])[None, :]
     sub = np.concatenate([[0], np.cumsum(sizes[pick])]).astype(np.int64)
-    n = int(sub[-1])
-    u = np.zeros((1, n), np.float32)
-    v = np.zeros((1, n), np.float32)
+    lt = [w.lt[s] for s in pick] if w.method == "adacomp" else None
+    return {"g": g, "sub": sub, "pick": pick, "lt": lt}
+
+
+def oracle_sample(w, inputs, target_s: float, min_steps: int = 1):
+    """Time the oracle on a bounded sample of the workload: the DGC or AdaComp
+    step + sparse average of learner 0 on every 4th tensor of the layout, or
+    one DCD ring iteration of all nodes on the first 2^20 columns.
+
+    Returns (gradient bytes processed, seconds, description)."""
+    import oracle
+    from gradient_compression_sgd_gb300 import workloads as wl
     oracle.lib()
+    g = inputs["g"]
+    if w.method == "dcd":
+        x = inputs["x"].copy()
+        seed = wl.dcd_seed(w)
+        def one(t):
+            oracle.dcd_step_window(x, g, w.ring_w, w.gamma, w.keep_p, seed, t, 0)
+        n = g.size
+        what = (f"oracle DCD ring iteration of all {w.learners} nodes on columns [0, {inputs['win']}) "
+                f"({n} values)")
+    else:
+        sub = inputs["sub"]
+        n = int(sub[-1])
+        state = np.zeros((1, n), np.float32)
+        if w.method == "dgc":
+            v = np.zeros((1, n), np.float32)
+            def one(t):
+                idx, val, counts, _ = oracle.dgc_step(sub, g, state, v, w.density, w.momentum,
+                                                      w.clip_thr, w.clip_nodes)
+                oracle.sparse_average(idx, val, counts.sum(axis=1), n)
+        else:
+            def one(t):
+                idx, val, counts, _, _ = oracle.adacomp_step(sub, inputs["lt"], g, state)
+                oracle.sparse_average(idx, val, counts.sum(axis=1), n)
+        what = (f"oracle {w.method.upper()} step + sparse average of learner 0 on every 4th tensor of the "
+                f"layout ({len(inputs['pick'])} tensors, {n} values)")
     t0 = time.perf_counter()
     steps = 0
     while steps < min_steps or time.perf_counter() - t0 < target_s:
-        idx, val, counts, _ = oracle.dgc_step(sub, g, u, v, w.density, w.momentum)
-        oracle.sparse_average(idx, val, counts.sum(axis=1), n)
+        one(steps)
         steps += 1
     dt = time.perf_counter() - t0
-    desc = (f"oracle DGC step + sparse average of learner 0 on every 4th tensor of the layout "
-            f"({len(pick)} tensors, {n} values), {steps} step(s), single thread")
-    return 4.0 * n * steps, dt, desc
+    return 4.0 * n * steps, dt, f"{what}, {steps} step(s), single thread"
 
 
 # ------------------------------------------------------------ reference arm
@@ -161,13 +214,13 @@ def run_reference(args):
     import torch  # noqa: F401  (seeded generator)
     from gradient_compression_sgd_gb300 import workloads as wl
     w = wl.workload(args.config)
-    grad0 = wl.gradient(w, 0, 0).numpy()
+    inputs = oracle_inputs(w)
     for _ in range(args.warmup):
-        oracle_sample(w, grad0, 0.0)
+        oracle_sample(w, inputs, 0.0)
     times, nbytes = [], 0.0
     desc = ""
     for _ in range(args.steps):
-        b, dt, desc = oracle_sample(w, grad0, 0.0)
+        b, dt, desc = oracle_sample(w, inputs, 0.0)
         times.append(dt)
         nbytes = b
     total = sum(times)
@@ -357,13 +410,9 @@ def run_gpu(args):
     gc.trace_enable(False)
     launches = gc.launch_count()
     trace = gc.trace_read()
-    ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
     grad_bytes = 4.0 * K * N
-    value = world * grad_bytes / (ms * 1e-3) / 1e9
+    value = job_gbs(world, grad_bytes, ms)
 
     # end to end through the public API: pinned host gradient in, the step's dense result out
     e2e, ms_e2e, d2h = None, None, 0
@@ -395,12 +444,8 @@ def run_gpu(args):
             e2e_step(i)
         f1.record(stream)
         torch.cuda.synchronize()
-        ms_e2e = f0.elapsed_time(f1) / e2e_steps
-        if world > 1:
-            t = torch.tensor([ms_e2e], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_e2e = float(t.item())
-        e2e = world * grad_bytes / (ms_e2e * 1e-3) / 1e9
+        ms_e2e = max_over_ranks(f0.elapsed_time(f1) / e2e_steps, dev)
+        e2e = job_gbs(world, grad_bytes, ms_e2e)
 
     if rank != 0:
         if world > 1:
@@ -421,8 +466,8 @@ def run_gpu(args):
                for name, (c, t) in trace.items()}
 
     cpu = None
-    if world == 1 and not args.no_cpu_baseline and w.method == "dgc":
-        b, dt, desc = oracle_sample(w, grads[0][0].cpu().numpy(), args.cpu_seconds)
+    if world == 1 and not args.no_cpu_baseline:
+        b, dt, desc = oracle_sample(w, oracle_inputs(w), args.cpu_seconds)
         cpu = {"value": b / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc}
 
     line = {

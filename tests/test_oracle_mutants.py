@@ -1,0 +1,89 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case plants one mistake in a copy of the oracle's C source (a wrong
+order of the momentum updates, the tie rule reversed, a missing mask, > for
+>=, a wrong neighbour on the ring, a swapped Philox key word, ...), rebuilds
+the copy and runs the oracle's pin tests against it: at least one pin must
+fail.  Nothing here touches the CUDA path; the mistakes live only in a
+temporary copy of the oracle.
+"""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC_PATH = os.path.join(ROOT, "oracle", "gcsgd_oracle.c")
+PIN_FILES = ["test_oracle_dgc.py", "test_oracle_adacomp.py", "test_oracle_average_dcd.py"]
+
+# name -> (text in the oracle, planted replacement)
+MUTANTS = {
+    # DGC (momentum correction, selection, masking, clipping, k)
+    "v_before_u": ("uk[i] = mu + g;\n            vk[i] = vk[i] + uk[i];",
+                   "vk[i] = vk[i] + uk[i];\n            uk[i] = mu + g;"),
+    "no_momentum": ("float mu = momentum * uk[i];", "float mu = 0.0f * uk[i];"),
+    "ties_to_higher_index": ("return x->idx < y->idx ? -1 : 1;", "return x->idx > y->idx ? -1 : 1;"),
+    "u_not_masked": ("uk[off + i] = 0.0f;\n            }", "}"),
+    "v_not_masked": ("vk[off + i] = 0.0f;\n                uk", "uk"),
+    "clip_ignores_nodes": ("/ sqrt((double)clip_nodes)", "/ 1.0"),
+    "clip_scale_inverted": ("if (norm > thr_k) { c = (float)(thr_k / norm)", "if (norm > thr_k) { c = (float)(norm / thr_k)"),
+    "k_floor": ("double kd = ceil(density * (double)n);", "double kd = floor(density * (double)n);"),
+    # AdaComp
+    "ada_strict_gt": ("(fabsf(h) >= m)", "(fabsf(h) > m)"),
+    "ada_h_without_dw": ("const float h = G[off + i] + dWk[off + i];", "const float h = G[off + i];"),
+    "ada_sign_from_h": ("Q[off + i] = G[off + i] > 0.0f ? scale : -scale;", "Q[off + i] = h > 0.0f ? scale : -scale;"),
+    "ada_residue_not_reduced": ("Rk[i] = G[i] - Q[i];", "Rk[i] = G[i];"),
+    "ada_mean_over_nb_minus_1": ("/ (double)nb);", "/ (double)(nb > 1 ? nb - 1 : 1));"),
+    "ada_partial_bin_dropped": ("const int64_t nb = (n + L - 1) / L;", "const int64_t nb = n / L > 0 ? n / L : 1;"),
+    # sparse average
+    "average_not_divided": ("out[j] = out[j] / fk;", "out[j] = out[j];"),
+    # Philox and DCD-PSGD
+    "philox_key_word_swapped": ("uint32_t n0 = hi1 ^ c1 ^ k0;", "uint32_t n0 = hi1 ^ c1 ^ k1;"),
+    "dcd_wrong_neighbour": ("const int l = (i + n - 1) % n, r = (i + 1) % n;\n        const float* xl",
+                            "const int l = (i + n - 1) % n, r = (i + 2) % n;\n        const float* xl"),
+    "dcd_gradient_sign": ("const float xh = acc - gamma * gi[e];", "const float xh = acc + gamma * gi[e];"),
+    "dcd_no_unbiasing_scale": ("return ((uint64_t)word < thr) ? z * inv_p : 0.0f;",
+                               "return ((uint64_t)word < thr) ? z : 0.0f;"),
+    "dcd_counter_words_swapped": ("uint32_t ctr[4] = {(uint32_t)(e >> 2), node, t, (uint32_t)(e >> 34)};",
+                                  "uint32_t ctr[4] = {(uint32_t)(e >> 2), t, node, (uint32_t)(e >> 34)};"),
+}
+
+
+def _copy_tree(dst):
+    os.makedirs(os.path.join(dst, "tests"))
+    for f in ["conftest.py", *PIN_FILES]:
+        shutil.copy(os.path.join(ROOT, "tests", f), os.path.join(dst, "tests", f))
+    shutil.copytree(os.path.join(ROOT, "tests", "golden"), os.path.join(dst, "tests", "golden"))
+    os.makedirs(os.path.join(dst, "oracle"))
+    for f in ["__init__.py", "gcsgd_oracle.c"]:
+        shutil.copy(os.path.join(ROOT, "oracle", f), os.path.join(dst, "oracle", f))
+    pkg = "gradient_compression_sgd_gb300"
+    os.makedirs(os.path.join(dst, pkg))
+    for f in ["__init__.py", "workloads.py", "build.py"]:
+        shutil.copy(os.path.join(ROOT, pkg, f), os.path.join(dst, pkg, f))
+    shutil.copy(os.path.join(ROOT, "pytest.ini"), dst)
+
+
+def test_unmutated_copy_passes(tmp_path):
+    _copy_tree(str(tmp_path))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        *[os.path.join("tests", f) for f in PIN_FILES]],
+                       cwd=tmp_path, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_fails_a_pin(name, tmp_path):
+    src = open(SRC_PATH).read()
+    a, b = MUTANTS[name]
+    assert src.count(a) >= 1, f"mutation site for {name} no longer in the oracle"
+    _copy_tree(str(tmp_path))
+    with open(tmp_path / "oracle" / "gcsgd_oracle.c", "w") as f:
+        f.write(src.replace(a, b, 1))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        *[os.path.join("tests", f) for f in PIN_FILES]],
+                       cwd=tmp_path, capture_output=True, text=True, timeout=600)
+    last = (r.stdout.strip().splitlines() or [""])[-1]
+    assert r.returncode == 1 and "failed" in last, f"{name} not caught: {last}\n{r.stdout[-1500:]}"
