@@ -65,67 +65,142 @@ __device__ __forceinline__ uint64_t block_exclusive_scan(uint64_t x, uint64_t* s
     return res;
 }
 
-// Result of an exact descending selection on 31-bit magnitude keys.
+// Result of a descending selection on 31-bit magnitude keys.
 struct SelectResult {
     uint32_t thresh;   // key of the rank-th largest item
     uint32_t greater;  // items with key > thresh
     uint32_t ties;     // items with key == thresh to take (1 .. count(== thresh))
 };
 
-// Exact rank-th largest of `count` keys (1 <= rank <= count), by three
-// radix passes over bits [30:20], [19:9] and [8:0] of the keys with a
-// shared-memory histogram; only keys that share the digits chosen so far take
-// part in the next pass.  `load(i, &key)` returns false for items to skip.
-// hist: 2048 words of shared memory; scan: NT/32 + 1 words of 64-bit shared
-// memory; sel: 4 words of shared memory.  Every thread must call it.
+// Keys the selection keeps after its first digit (the first digit's bucket
+// usually holds a small fraction of the items).
+constexpr int kCandMax = 2048;
+
+// Shared-memory scratch of radix_select_desc.
+struct RadixSmem {
+    uint32_t hist[2048];
+    uint32_t cand[kCandMax];
+    uint64_t scan[33];
+    uint32_t sel[4];
+};
+
+// First digit of a key: bits [30:20] (exponent and three mantissa bits).
+__device__ __forceinline__ void radix_hist_add(RadixSmem& rs, uint32_t key) { atomicAdd(&rs.hist[key >> 20], 1u); }
+
+template <int NT>
+__device__ __forceinline__ void radix_hist_clear(RadixSmem& rs) {
+    for (int b = threadIdx.x; b < 2048; b += NT) rs.hist[b] = 0;
+}
+
+// Histogram of digit (key >> shift) & (nb - 1) over the keys whose bits under
+// pmask equal prefix.  Ends synchronised.
 template <int NT, class Load>
-__device__ SelectResult radix_select_desc(Load load, uint64_t count, uint32_t rank,
-                                          uint32_t* hist, uint64_t* scan, uint32_t* sel) {
-    uint32_t prefix = 0, pmask = 0, need = rank, greater = 0;
-#pragma unroll 1
-    for (int pass = 0; pass < 3; ++pass) {
-        const int shift = pass == 0 ? 20 : (pass == 1 ? 9 : 0);
-        const int nb = pass == 2 ? 512 : 2048;
-        for (int b = threadIdx.x; b < nb; b += NT) hist[b] = 0;
-        if (threadIdx.x == 0) { sel[0] = 0; sel[1] = 0; }
+__device__ void radix_count(RadixSmem& rs, Load load, uint64_t count, uint32_t pmask, uint32_t prefix, int shift,
+                            int nb) {
+    for (int b = threadIdx.x; b < nb; b += NT) rs.hist[b] = 0;
+    __syncthreads();
+    for (uint64_t base = 0; base < count; base += 4 * (uint64_t)NT) {
+        uint32_t key[4];
+        bool ok[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {  // four independent loads in flight
+            const uint64_t i = base + (uint64_t)j * NT + threadIdx.x;
+            key[j] = 0;
+            ok[j] = (i < count) && load(i, &key[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (ok[j] && ((key[j] & pmask) == prefix)) atomicAdd(&rs.hist[(key[j] >> shift) & (uint32_t)(nb - 1)], 1u);
+    }
+    __syncthreads();
+}
+
+// The bucket holding the need-th largest item of the histogram rs.hist[0, nb)
+// (counted from the top): *bucket, *above = items in higher buckets, *cnt =
+// items in the bucket.  Every thread must call it; ends synchronised, with
+// rs.hist intact.
+template <int NT>
+__device__ void radix_pick(RadixSmem& rs, int nb, uint32_t need, uint32_t* bucket, uint32_t* above, uint32_t* cnt) {
+    static_assert(NT >= 32 && NT <= 512 && NT % 32 == 0, "2048 / NT buckets per thread, at least one");
+    const int w = nb / NT;  // thread t owns buckets [hi - w, hi) counted from the top
+    const int hi = nb - (int)threadIdx.x * w;
+    uint32_t mine = 0;
+    for (int b = hi - 1; b >= hi - w; --b) mine += rs.hist[b];
+    uint64_t tot;
+    uint32_t ab = (uint32_t)block_exclusive_scan<NT>(mine, rs.scan, &tot);
+    for (int b = hi - 1; b >= hi - w; --b) {
+        const uint32_t h = rs.hist[b];
+        if (ab < need && need <= ab + h) {
+            rs.sel[0] = (uint32_t)b;
+            rs.sel[1] = ab;
+            rs.sel[2] = h;
+        }
+        ab += h;
+    }
+    __syncthreads();
+    *bucket = rs.sel[0];
+    *above = rs.sel[1];
+    *cnt = rs.sel[2];
+    __syncthreads();
+}
+
+// The rank-th largest of `count` 31-bit keys (1 <= rank <= count), by radix
+// digits [30:20], [19:9] and [8:0] with shared-memory histograms.  After the
+// first digit the keys of the chosen bucket are copied to rs.cand when they
+// fit, so the later digits look at those few keys only.  `load(i, &key)`
+// returns false for items to skip.  With hist_ready the caller has already
+// added every key's first digit into rs.hist (radix_hist_clear, then
+// radix_hist_add per key, then a barrier).  PASSES = 3 is exact; PASSES = 2
+// returns the rank-th largest key with its low 9 bits cleared (greater and
+// ties then refer to the truncated keys).  Every thread must call it.
+template <int NT, int PASSES, class Load>
+__device__ SelectResult radix_select_desc(Load load, uint64_t count, uint32_t rank, RadixSmem& rs, bool hist_ready) {
+    static_assert(PASSES == 2 || PASSES == 3, "two or three digits");
+    const int lane = threadIdx.x & 31;
+    if (!hist_ready) radix_count<NT>(rs, load, count, 0u, 0u, 20, 2048);
+    uint32_t b, ab, c1;
+    radix_pick<NT>(rs, 2048, rank, &b, &ab, &c1);
+    uint32_t prefix = b << 20, pmask = 0x7ffu << 20, need = rank - ab, greater = ab;
+    const bool compact = c1 <= (uint32_t)kCandMax;
+    if (compact) {
+        if (threadIdx.x == 0) rs.sel[3] = 0;
         __syncthreads();
         for (uint64_t base = 0; base < count; base += 4 * (uint64_t)NT) {
             uint32_t key[4];
             bool ok[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {  // four independent loads in flight
+            for (int j = 0; j < 4; ++j) {
                 const uint64_t i = base + (uint64_t)j * NT + threadIdx.x;
                 key[j] = 0;
                 ok[j] = (i < count) && load(i, &key[j]);
             }
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (ok[j] && ((key[j] & pmask) == prefix)) atomicAdd(&hist[(key[j] >> shift) & (uint32_t)(nb - 1)], 1u);
-        }
-        __syncthreads();
-        // thread t owns buckets [hi - w, hi) counted from the top
-        const int w = nb / NT;
-        const int t = threadIdx.x;
-        const int hi = nb - t * w;
-        uint32_t mine = 0;
-        for (int b = hi - 1; b >= hi - w; --b) mine += hist[b];
-        uint64_t tot;
-        uint32_t above = (uint32_t)block_exclusive_scan<NT>(mine, scan, &tot);
-        for (int b = hi - 1; b >= hi - w; --b) {
-            const uint32_t h = hist[b];
-            if (above < need && need <= above + h) {
-                sel[0] = (uint32_t)b;
-                sel[1] = above;
+            for (int j = 0; j < 4; ++j) {
+                const bool hit = ok[j] && (key[j] & pmask) == prefix;
+                const unsigned m = __ballot_sync(kFull, hit);
+                if (m) {
+                    uint32_t at = 0;
+                    if (lane == 0) at = atomicAdd(&rs.sel[3], (uint32_t)__popc(m));
+                    at = __shfl_sync(kFull, at, 0);
+                    if (hit) rs.cand[at + __popc(m & ((1u << lane) - 1u))] = key[j];
+                }
             }
-            above += h;
         }
         __syncthreads();
-        const uint32_t b = sel[0], ab = sel[1];
+    }
+    auto cand = [&](uint64_t i, uint32_t* key) { *key = rs.cand[i]; return true; };
+#pragma unroll 1
+    for (int pass = 1; pass < PASSES; ++pass) {
+        const int shift = pass == 1 ? 9 : 0;
+        const int nb = pass == 1 ? 2048 : 512;
+        if (compact) radix_count<NT>(rs, cand, c1, pmask, prefix, shift, nb);
+        else radix_count<NT>(rs, load, count, pmask, prefix, shift, nb);
+        uint32_t cb;
+        radix_pick<NT>(rs, nb, need, &b, &ab, &cb);
         prefix |= b << shift;
         pmask |= (uint32_t)(nb - 1) << shift;
         greater += ab;
         need -= ab;
-        __syncthreads();
     }
     SelectResult r;
     r.thresh = prefix;

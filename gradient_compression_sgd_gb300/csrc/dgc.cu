@@ -45,8 +45,10 @@ constexpr int kTile = 4096;              // elements per dgc_update tile (NT x 4
 constexpr uint32_t kRawMax = 16384;      // segments up to this size select from v' directly
 constexpr uint32_t kSampleMax = 16384;   // largest hint sample (keys held in shared memory)
 constexpr uint32_t kSampleAbove = 48;    // sampled entries expected above the hint
+constexpr uint32_t kSampleBlock = 64;    // consecutive values per sample block
 constexpr uint32_t kPoolFloor = 512;     // smallest expected candidate count
 constexpr uint32_t kStageItems = 8192;   // candidates dgc_select stages in shared memory
+constexpr int kChunkTiles = 4 * NTS;     // tile-table entries dgc_select scans per round
 constexpr size_t kStageBytes = kStageItems * sizeof(uint2);  // also holds kRawMax floats
 static_assert(kStageBytes >= kRawMax * sizeof(float), "the stage must hold a raw segment");
 constexpr int kSumsqBlocks = 128;        // CTAs per learner in dgc_sumsq
@@ -69,8 +71,8 @@ __host__ __device__ __forceinline__ void seg_fields(uint32_t n, double density, 
         p->cap = (uint32_t)(cap < n ? cap : n);
         uint64_t m = (uint64_t)kSampleAbove * n / R;
         if (m > kSampleMax) m = kSampleMax;
-        m &= ~(uint64_t)31;
-        if (m < 32) m = 32;
+        m &= ~(uint64_t)(kSampleBlock - 1);
+        if (m < kSampleBlock) m = kSampleBlock;
         p->m = (uint32_t)m;
         uint64_t a = (R * m + n / 2) / n;
         p->a = (uint32_t)(a < 1 ? 1 : (a > m ? m : a));
@@ -170,11 +172,9 @@ __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, PoolL
                                                      const float* __restrict__ v, float momentum,
                                                      uint32_t* __restrict__ hint, uint32_t* __restrict__ pool_cnt) {
     extern __shared__ __align__(16) uint32_t keys[];  // kSampleMax
-    __shared__ uint32_t hist[2048];
-    __shared__ uint64_t scan[NTP / 32 + 1];
+    __shared__ RadixSmem rs;
     __shared__ uint64_t carry[3];
     __shared__ float s_c;
-    __shared__ uint32_t s_sel[4];
     if (blockIdx.x == gridDim.x - 1) {  // the extra CTA: plan, order, clip scales
         if (threadIdx.x < 3) carry[threadIdx.x] = 0;
         __syncthreads();
@@ -185,15 +185,15 @@ __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, PoolL
             seg_fields(live ? so.off[s + 1] - so.off[s] : 0u, density, &p);
             p.off = live ? so.off[s] : 0u;
             uint64_t tot;
-            const uint64_t ex_pool = block_exclusive_scan<NTP>(live ? p.cap : 0, scan, &tot);
+            const uint64_t ex_pool = block_exclusive_scan<NTP>(live ? p.cap : 0, rs.scan, &tot);
             const uint64_t c0 = carry[0];
             __syncthreads();
             if (threadIdx.x == 0) carry[0] = c0 + tot;
-            const uint64_t ex_tile = block_exclusive_scan<NTP>(live ? p.ntiles : 0, scan, &tot);
+            const uint64_t ex_tile = block_exclusive_scan<NTP>(live ? p.ntiles : 0, rs.scan, &tot);
             const uint64_t c1 = carry[1];
             __syncthreads();
             if (threadIdx.x == 0) carry[1] = c1 + tot;
-            const uint64_t ex_out = block_exclusive_scan<NTP>(live ? p.k : 0, scan, &tot);
+            const uint64_t ex_out = block_exclusive_scan<NTP>(live ? p.k : 0, rs.scan, &tot);
             const uint64_t c2 = carry[2];
             __syncthreads();
             if (threadIdx.x == 0) carry[2] = c2 + tot;
@@ -235,40 +235,52 @@ __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, PoolL
         p.m = pl.m[q];
         p.a = pl.a[q];
         const float c = s_c;
-        const uint32_t nblk = p.m / 32;
-        const uint32_t stride = p.n / nblk;  // >= 512 since m <= n / 16
+        const uint32_t nblk = p.m / kSampleBlock;
+        const uint32_t stride = p.n / nblk;  // >= 64 * 512 / 48 (m <= 48 n / 512): blocks never overlap
         const uint64_t base = (uint64_t)k * N + p.off;
         const float* gs = grad + base;
         const float* us = u + base;
         const float* vs = v + base;
-        // sample element 32 b + lane sits at b * stride + lane; a warp issues
-        // the loads of 8 blocks before using any of them
-        constexpr int kB = 8;
+        radix_hist_clear<NTP>(rs);
+        __syncthreads();
+        // sample element j of block b sits at b * stride + j; a warp issues
+        // the loads of kB blocks (two values per lane each) before using any
+        constexpr int kB = 4, kH = kSampleBlock / 32;
         for (uint32_t b0 = warp; b0 < nblk; b0 += kB * (NTP / 32)) {
-            float gg[kB], uu[kB], vv[kB];
+            float gg[kB][kH], uu[kB][kH], vv[kB][kH];
 #pragma unroll
             for (int j = 0; j < kB; ++j) {
                 const uint32_t b = b0 + j * (NTP / 32);
-                gg[j] = uu[j] = vv[j] = 0.0f;
-                if (b < nblk) {
-                    const uint32_t i = b * stride + lane;
-                    gg[j] = __ldg(gs + i);
-                    uu[j] = __ldg(us + i);
-                    vv[j] = __ldg(vs + i);
+#pragma unroll
+                for (int h = 0; h < kH; ++h) {
+                    gg[j][h] = uu[j][h] = vv[j][h] = 0.0f;
+                    if (b < nblk) {
+                        const uint32_t i = b * stride + 32 * h + lane;
+                        gg[j][h] = __ldg(gs + i);
+                        uu[j][h] = __ldg(us + i);
+                        vv[j][h] = __ldg(vs + i);
+                    }
                 }
             }
 #pragma unroll
             for (int j = 0; j < kB; ++j) {
                 const uint32_t b = b0 + j * (NTP / 32);
                 if (b < nblk) {
-                    dgc_elem(gg[j], uu[j], vv[j], momentum, c);
-                    keys[b * 32 + lane] = mag_key(vv[j]);
+#pragma unroll
+                    for (int h = 0; h < kH; ++h) {
+                        dgc_elem(gg[j][h], uu[j][h], vv[j][h], momentum, c);
+                        const uint32_t key = mag_key(vv[j][h]);
+                        keys[b * kSampleBlock + 32 * h + lane] = key;
+                        radix_hist_add(rs, key);
+                    }
                 }
             }
         }
         __syncthreads();
-        const SelectResult sr = radix_select_desc<NTP>(
-            [&](uint64_t i, uint32_t* key) { *key = keys[i]; return true; }, p.m, p.a, hist, scan, s_sel);
+        // two digits suffice: the hint only needs to sit at or below the
+        // a-th largest sampled key
+        const SelectResult sr = radix_select_desc<NTP, 2>(
+            [&](uint64_t i, uint32_t* key) { *key = keys[i]; return true; }, p.m, p.a, rs, true);
         const uint32_t h = sr.thresh;
         if (threadIdx.x == 0) hint[unit] = h > 1u ? h : 1u;
         __syncthreads();
@@ -395,58 +407,64 @@ __global__ void __launch_bounds__(NT, 3) dgc_update(const SegPlan* __restrict__ 
     }
 }
 
-// Ordered emission over `count` items given in ascending index order, four
-// consecutive items per thread per round: an item is sent if its key > T, or
-// == T and fewer than `ties` equal keys precede it; its slot is (#greater
-// before it) + min(#equal before it, ties).  Sent items are written to dst and
-// u = v = 0 at their indices (momentum factor masking).
+// Ordered emission over `count` items given in ascending index order: an
+// item is sent if its key > T, or == T and fewer than `ties` equal keys
+// precede it; its slot is (#greater before it) + min(#equal before it, ties).
+// Sent items are written to dst and u = v = 0 at their indices (momentum
+// factor masking).  Warp w owns one contiguous run of the items: a first
+// sweep counts its greater and equal keys (warp ballots), one barrier shares
+// the 16 warp counts, and a second sweep writes, ranking each item by ballots
+// inside its warp.  wsum: NTS / 32 words of shared memory.
 template <class Get>
-__device__ void emit_in_order(Get get, uint32_t count, uint32_t T, uint32_t greater, uint32_t ties,
-                              const SegPlan& p, gcsgd_pair* __restrict__ dst, float* __restrict__ u,
-                              float* __restrict__ v, uint64_t ebase, uint64_t* scan) {
-    uint32_t run_gt = 0, run_eq = 0;
-    for (uint32_t cb = 0; cb < count; cb += 4 * NTS) {
-        const uint32_t i0 = cb + 4 * threadIdx.x;
-        uint32_t loc[4], bits[4];
-        uint32_t ngt = 0, neq = 0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            loc[j] = 0xffffffffu;
-            bits[j] = 0;
-            if (i0 + j < count) get(i0 + j, &loc[j], &bits[j]);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if (i0 + j < count) {
-                const uint32_t key = bits[j] & 0x7fffffffu;
-                ngt += key > T;
-                neq += key == T;
-            }
-        }
-        uint64_t tot;
-        const uint64_t ex = block_exclusive_scan<NTS>((uint64_t)ngt | ((uint64_t)neq << 32), scan, &tot);
-        uint32_t gb = run_gt + (uint32_t)ex, eb = run_eq + (uint32_t)(ex >> 32);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if (i0 + j >= count) break;
-            const uint32_t key = bits[j] & 0x7fffffffu;
-            const bool gt = key > T, eq = key == T;
-            const uint32_t slot = gb + (eb < ties ? eb : ties);
-            if ((gt || (eq && eb < ties)) && slot < p.k && loc[j] < p.n) {
-                gcsgd_pair pr;
-                pr.idx = p.off + loc[j];
-                pr.val = __uint_as_float(bits[j]);
-                dst[slot] = pr;
-                u[ebase + loc[j]] = 0.0f;
-                v[ebase + loc[j]] = 0.0f;
-            }
-            gb += gt;
-            eb += eq;
-        }
-        run_gt += (uint32_t)tot;
-        run_eq += (uint32_t)(tot >> 32);
-        if (run_gt >= greater && run_eq >= ties) break;  // all k sent
+__device__ void emit_in_order(Get get, uint32_t count, uint32_t T, uint32_t ties, const SegPlan& p,
+                              gcsgd_pair* __restrict__ dst, float* __restrict__ u, float* __restrict__ v,
+                              uint64_t ebase, uint2* wsum) {
+    constexpr uint32_t NW = NTS / 32;
+    const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t per = (count + NW * 32 - 1) / (NW * 32) * 32;  // items per warp, a multiple of 32
+    const uint32_t lo = warp * per < count ? warp * per : count;
+    const uint32_t hi = lo + per < count ? lo + per : count;
+    const unsigned below = (1u << lane) - 1u;
+    uint32_t ngt = 0, neq = 0;
+    for (uint32_t b = lo; b < hi; b += 32) {
+        const uint32_t i = b + lane;
+        uint32_t loc = 0, bits = 0;
+        if (i < hi) get(i, &loc, &bits);
+        const uint32_t key = bits & 0x7fffffffu;
+        ngt += __popc(__ballot_sync(kFull, i < hi && key > T));
+        neq += __popc(__ballot_sync(kFull, i < hi && key == T));
     }
+    if (lane == 0) wsum[warp] = make_uint2(ngt, neq);
+    __syncthreads();
+    uint32_t gb = 0, eb = 0;
+    for (uint32_t w = 0; w < warp; ++w) {
+        const uint2 c = wsum[w];
+        gb += c.x;
+        eb += c.y;
+    }
+    if (ngt > 0 || (neq > 0 && eb < ties)) {
+        for (uint32_t b = lo; b < hi; b += 32) {
+            const uint32_t i = b + lane;
+            uint32_t loc = 0, bits = 0;
+            if (i < hi) get(i, &loc, &bits);
+            const uint32_t key = bits & 0x7fffffffu;
+            const bool gt = i < hi && key > T, eq = i < hi && key == T;
+            const unsigned mg = __ballot_sync(kFull, gt), me = __ballot_sync(kFull, eq);
+            const uint32_t g_before = gb + __popc(mg & below), e_before = eb + __popc(me & below);
+            const uint32_t slot = g_before + (e_before < ties ? e_before : ties);
+            if ((gt || (eq && e_before < ties)) && slot < p.k && loc < p.n) {
+                gcsgd_pair pr;
+                pr.idx = p.off + loc;
+                pr.val = __uint_as_float(bits);
+                dst[slot] = pr;
+                u[ebase + loc] = 0.0f;
+                v[ebase + loc] = 0.0f;
+            }
+            gb += __popc(mg);
+            eb += __popc(me);
+        }
+    }
+    __syncthreads();  // wsum is reused
 }
 
 // Largest 64-bit value across a warp.
@@ -573,11 +591,10 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
     extern __shared__ __align__(16) unsigned char stage_raw[];  // kStageBytes
     uint2* stage = reinterpret_cast<uint2*>(stage_raw);
     float* stagef = reinterpret_cast<float*>(stage_raw);
-    __shared__ uint32_t hist[2048];
-    __shared__ uint64_t scan[NTS / 32 + 1];
-    __shared__ uint32_t sel[4];
-    __shared__ uint32_t toff[NTS + 1];
-    __shared__ uint32_t tbase[NTS];
+    __shared__ RadixSmem rs;
+    __shared__ uint32_t toff[kChunkTiles];
+    __shared__ uint32_t tbase[kChunkTiles];
+    __shared__ uint2 wsum[NTS / 32];
     // largest segments first, every learner's copy of a segment together
     const int k = (int)blockIdx.x % K;
     const int s = order[(int)blockIdx.x / K];
@@ -597,14 +614,28 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
     gcsgd_pair* dst = out + (uint64_t)k * cap + p.out_off;
 
     if (pool_ok && pc <= kStageItems) {
-        // stage the candidates in index order: tiles in order, items of a tile in order
+        // stage the candidates in index order (tiles in order, items of a tile
+        // in order) and count their first radix digit on the way
+        radix_hist_clear<NTS>(rs);
         uint32_t run = 0;
-        for (uint32_t tb = 0; tb < p.ntiles; tb += NTS) {
-            const uint32_t j = tb + threadIdx.x;
-            const uint2 ent = j < p.ntiles ? tt[j] : make_uint2(0u, 0u);
+        for (uint32_t tb = 0; tb < p.ntiles; tb += kChunkTiles) {
+            constexpr int TPT = kChunkTiles / NTS;  // tiles per thread
+            uint2 ent[TPT];
+            uint32_t c = 0;
+#pragma unroll
+            for (int j = 0; j < TPT; ++j) {
+                const uint32_t jt = tb + TPT * threadIdx.x + j;
+                ent[j] = jt < p.ntiles ? tt[jt] : make_uint2(0u, 0u);
+                c += ent[j].y;
+            }
             uint64_t tot;
-            toff[threadIdx.x] = (uint32_t)block_exclusive_scan<NTS>(ent.y, scan, &tot);
-            tbase[threadIdx.x] = ent.x;
+            uint32_t ex = (uint32_t)block_exclusive_scan<NTS>(c, rs.scan, &tot);
+#pragma unroll
+            for (int j = 0; j < TPT; ++j) {
+                toff[TPT * threadIdx.x + j] = ex;
+                tbase[TPT * threadIdx.x + j] = ent[j].x;
+                ex += ent[j].y;
+            }
             __syncthreads();
             const uint32_t total = (uint32_t)tot;
             for (uint32_t q0 = 0; q0 < total; q0 += 4 * NTS) {
@@ -613,7 +644,7 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
                 for (int jj = 0; jj < 4; ++jj) {
                     const uint32_t q = q0 + jj * NTS + threadIdx.x;
                     if (q < total) {
-                        int lo = 0, hi = NTS;  // last tile with toff <= q
+                        int lo = 0, hi = kChunkTiles;  // last tile with toff <= q
                         while (hi - lo > 1) {
                             const int mid = (lo + hi) >> 1;
                             if (toff[mid] <= q) lo = mid; else hi = mid;
@@ -624,22 +655,24 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
                     const uint32_t q = q0 + jj * NTS + threadIdx.x;
-                    if (q < total && run + q < kStageItems) stage[run + q] = it[jj];
+                    if (q < total && run + q < kStageItems) {
+                        stage[run + q] = it[jj];
+                        radix_hist_add(rs, it[jj].y & 0x7fffffffu);
+                    }
                 }
             }
             run += total;
             __syncthreads();
         }
-        const SelectResult r = radix_select_desc<NTS>(
-            [&](uint64_t i, uint32_t* key) { *key = stage[i].y & 0x7fffffffu; return true; }, pc, p.k, hist, scan,
-            sel);
+        const SelectResult r = radix_select_desc<NTS, 3>(
+            [&](uint64_t i, uint32_t* key) { *key = stage[i].y & 0x7fffffffu; return true; }, pc, p.k, rs, true);
         emit_in_order(
             [&](uint32_t i, uint32_t* loc, uint32_t* bits) {
                 const uint2 it = stage[i];
                 *loc = it.x;
                 *bits = it.y;
             },
-            pc, r.thresh, r.greater, r.ties, p, dst, u, v, ebase, scan);
+            pc, r.thresh, r.ties, p, dst, u, v, ebase, wsum);
         return;
     }
     if (!pool_ok && p.n <= kSmallN && p.k <= kSmallK) {
@@ -649,6 +682,7 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
     }
     if (!pool_ok && p.n <= kRawMax) {
         // kRawMax = 8 float4 per thread: issue every load before the first store
+        radix_hist_clear<NTS>(rs);
         const bool aligned = (ebase & 3) == 0;
         float4 q[kRawMax / (4 * NTS)];
 #pragma unroll
@@ -674,40 +708,49 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
                 if (e0 + 2 < p.n) stagef[e0 + 2] = q[r].z;
             }
         }
+        __syncthreads();  // the histogram is clear everywhere before any count
+#pragma unroll
+        for (int r = 0; r < (int)(kRawMax / (4 * NTS)); ++r) {
+            const uint32_t e0 = 4 * (r * NTS + threadIdx.x);
+            if (e0 < p.n) radix_hist_add(rs, mag_key(q[r].x));
+            if (e0 + 1 < p.n) radix_hist_add(rs, mag_key(q[r].y));
+            if (e0 + 2 < p.n) radix_hist_add(rs, mag_key(q[r].z));
+            if (e0 + 3 < p.n) radix_hist_add(rs, mag_key(q[r].w));
+        }
         __syncthreads();
-        const SelectResult r = radix_select_desc<NTS>(
-            [&](uint64_t i, uint32_t* key) { *key = mag_key(stagef[i]); return true; }, p.n, p.k, hist, scan, sel);
+        const SelectResult r = radix_select_desc<NTS, 3>(
+            [&](uint64_t i, uint32_t* key) { *key = mag_key(stagef[i]); return true; }, p.n, p.k, rs, true);
         emit_in_order(
             [&](uint32_t i, uint32_t* loc, uint32_t* bits) {
                 *loc = i;
                 *bits = __float_as_uint(stagef[i]);
             },
-            p.n, r.thresh, r.greater, r.ties, p, dst, u, v, ebase, scan);
+            p.n, r.thresh, r.ties, p, dst, u, v, ebase, wsum);
         return;
     }
     if (!pool_ok) {
         // the hint failed: select among all of the segment's v' in global memory
-        const SelectResult r = radix_select_desc<NTS>(
-            [&](uint64_t i, uint32_t* key) { *key = mag_key(vseg[i]); return true; }, p.n, p.k, hist, scan, sel);
+        const SelectResult r = radix_select_desc<NTS, 3>(
+            [&](uint64_t i, uint32_t* key) { *key = mag_key(vseg[i]); return true; }, p.n, p.k, rs, false);
         emit_in_order(
             [&](uint32_t i, uint32_t* loc, uint32_t* bits) {
                 *loc = i;
                 *bits = __float_as_uint(vseg[i]);
             },
-            p.n, r.thresh, r.greater, r.ties, p, dst, u, v, ebase, scan);
+            p.n, r.thresh, r.ties, p, dst, u, v, ebase, wsum);
         return;
     }
     // a valid pool too large to stage: select from global memory, emit through the tile table
-    const SelectResult r = radix_select_desc<NTS>(
-        [&](uint64_t i, uint32_t* key) { *key = __ldg(&items[i].y) & 0x7fffffffu; return true; }, pc, p.k, hist,
-        scan, sel);
+    const SelectResult r = radix_select_desc<NTS, 3>(
+        [&](uint64_t i, uint32_t* key) { *key = __ldg(&items[i].y) & 0x7fffffffu; return true; }, pc, p.k, rs,
+        false);
     const uint32_t T = r.thresh, ties = r.ties;
     uint32_t run_gt = 0, run_eq = 0;
     for (uint32_t tb = 0; tb < p.ntiles; tb += NTS) {
         const uint32_t j = tb + threadIdx.x;
         const uint2 ent = j < p.ntiles ? tt[j] : make_uint2(0u, 0u);
         uint64_t tot;
-        toff[threadIdx.x] = (uint32_t)block_exclusive_scan<NTS>(ent.y, scan, &tot);
+        toff[threadIdx.x] = (uint32_t)block_exclusive_scan<NTS>(ent.y, rs.scan, &tot);
         tbase[threadIdx.x] = ent.x;
         __syncthreads();
         const uint32_t chunk_items = (uint32_t)tot;
@@ -727,7 +770,7 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
             }
             const uint32_t key = bits & 0x7fffffffu;
             const bool gt = live && key > T, eq = live && key == T;
-            const uint64_t ex2 = block_exclusive_scan<NTS>((uint64_t)gt | ((uint64_t)eq << 32), scan, &tot);
+            const uint64_t ex2 = block_exclusive_scan<NTS>((uint64_t)gt | ((uint64_t)eq << 32), rs.scan, &tot);
             const uint32_t gb = run_gt + (uint32_t)ex2, eb = run_eq + (uint32_t)(ex2 >> 32);
             const uint32_t slot = gb + (eb < ties ? eb : ties);
             if ((gt || (eq && eb < ties)) && slot < p.k && local < p.n) {

@@ -110,17 +110,21 @@ def test_capacity_overflow_sends_nothing_and_keeps_the_residue(cuda_lib):
 
 # ------------------------------------------------------------ sparse average
 
-def run_average(gc, idx, val, counts, n):
+def run_average(gc, idx, val, counts, n, out_offset=0):
     import torch
     K, cap = idx.shape
     pairs = torch.zeros((K, cap, 2), dtype=torch.int32)
     pairs[..., 0] = torch.from_numpy(idx.astype(np.int64)).to(torch.int32)
     pairs[..., 1] = torch.from_numpy(val.view(np.int32))
     pairs = pairs.cuda()
-    out = torch.full((max(n, 1),), float("nan"), device="cuda")
+    # NaN everywhere, so an output the kernel fails to write shows
+    buf = torch.full((max(n, 1) + out_offset + 5,), float("nan"), device="cuda")
+    out = buf[out_offset:out_offset + max(n, 1)]
     gc.sparse_average(pairs, torch.from_numpy(counts.astype(np.int64)).cuda(), n, out)
     torch.cuda.synchronize()
     got = out.cpu().numpy()[:n]
+    rest = buf.cpu().numpy()
+    assert np.isnan(rest[:out_offset]).all() and np.isnan(rest[out_offset + n:]).all()  # nothing outside out
     want = oracle.sparse_average(idx, val, counts, n)
     assert rel_err(got, want) <= AVG_RTOL
     np.testing.assert_array_equal(np.nonzero(got)[0], np.nonzero(want)[0])
@@ -142,6 +146,25 @@ def test_sparse_average_random_lists(cuda_lib, K, n):
         counts[k] = c
     got, want = run_average(cuda_lib, idx, val, counts, n)
     np.testing.assert_array_equal(got, want)  # learner order kept: exact
+
+
+@pytest.mark.parametrize("offset", [1, 2, 3])
+@pytest.mark.parametrize("K", [3, 4])
+def test_sparse_average_unaligned_output(cuda_lib, offset, K):
+    """The output vector need not start on a 16-byte boundary."""
+    rng = np.random.default_rng(offset * 10 + K)
+    n, cap = 50001, 400
+    idx = np.zeros((K, cap), np.uint32)
+    val = np.zeros((K, cap), np.float32)
+    counts = np.zeros(K, np.int64)
+    for k in range(K):
+        c = int(rng.integers(1, cap + 1))
+        pick = np.concatenate([[0, n - 1], rng.choice(np.arange(1, n - 1), size=c - 2, replace=False)])[:c]
+        idx[k, :c] = np.sort(pick)
+        val[k, :c] = rng.standard_normal(c).astype(np.float32)
+        counts[k] = c
+    got, want = run_average(cuda_lib, idx, val, counts, n, out_offset=offset)
+    np.testing.assert_array_equal(got, want)
 
 
 def test_sparse_average_of_dgc_messages(cuda_lib):

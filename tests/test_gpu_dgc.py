@@ -115,17 +115,17 @@ def test_hint_above_the_kth_value_falls_back(cuda_lib):
     hint is 3.0 and only a < k entries qualify), the other sampled values 1.0
     (ties), some unsampled ones 0.5, the rest tiny.  The select must fall
     back to the whole segment and still be exact.  (The sample layout mirrors
-    the kernel's plan: R = max(3k, 512), m = min(48 n / R, 16384) rounded
-    down to 32, blocks of 32 at stride n / (m / 32), a = round(R m / n).)"""
+    the kernel's plan: R = max(2.5 k, 512), m = min(48 n / R, 16384) rounded
+    down to 64, blocks of 64 at stride n / (m / 64), a = round(R m / n).)"""
     n, density = 40000, 0.003
     k = oracle.dgc_k(density, n)
-    R = max(3 * k, 512)
-    m = min(48 * n // R, 16384) & ~31
-    nblk, stride = m // 32, n // (m // 32)
+    R = max(5 * k // 2, 512)
+    m = min(48 * n // R, 16384) & ~63
+    nblk, stride = m // 64, n // (m // 64)
     a = (R * m + n // 2) // n
     assert a < k
     G = np.full((1, n), 1e-6, np.float32)
-    pos = np.concatenate([np.arange(b * stride, b * stride + 32) for b in range(nblk)])
+    pos = np.concatenate([np.arange(b * stride, b * stride + 64) for b in range(nblk)])
     G[0, pos] = 1.0
     G[0, pos[np.linspace(0, len(pos) - 1, a).astype(int)]] = 3.0
     G[0, 30001:30050] = 0.5
