@@ -292,15 +292,18 @@ class DgcPath:
         self.state = [torch.zeros((self.K, self.N), device=dev) for _ in range(2)]
         self.avg = torch.empty(self.N, device=dev)
 
+    result_in_state = False  # the step's result is a separate buffer (double-buffered end to end)
+
     def fresh_state(self):
         import torch
         return [torch.zeros_like(x) for x in self.state]
 
-    def step(self, g, state=None, t=0):
+    def step(self, g, state=None, t=0, res=None):
         u, v = state or self.state
         out, totals = self.obj(g, u, v)
-        self.gc.sparse_average(out, totals, self.N, self.avg)
-        return self.avg
+        res = self.avg if res is None else res
+        self.gc.sparse_average(out, totals, self.N, res)
+        return res
 
     def sent(self):
         return int(self.obj.totals.sum().item())
@@ -320,11 +323,12 @@ class AdaCompPath(DgcPath):
         self.state = [torch.zeros((self.K, self.N), device=dev)]
         self.avg = torch.empty(self.N, device=dev)
 
-    def step(self, g, state=None, t=0):
+    def step(self, g, state=None, t=0, res=None):
         (R,) = state or self.state
         out, totals = self.obj(g, R)
-        self.gc.sparse_average(out, totals, self.N, self.avg)
-        return self.avg
+        res = self.avg if res is None else res
+        self.gc.sparse_average(out, totals, self.N, res)
+        return res
 
     def extra(self):
         tot = self.obj.totals.cpu()
@@ -345,7 +349,9 @@ class DcdPath:
     def fresh_state(self):
         return [self.state[0].clone()]
 
-    def step(self, g, state=None, t=0):
+    result_in_state = True  # the result (node 0's model) is the state itself
+
+    def step(self, g, state=None, t=0, res=None):
         (x,) = state or self.state
         self.gc.dcd_step(x, g, self.w.ring_w, self.w.gamma, self.w.keep_p, self.seed, t)
         return x[0]
@@ -414,34 +420,57 @@ def run_gpu(args):
     grad_bytes = 4.0 * K * N
     value = job_gbs(world, grad_bytes, ms)
 
-    # end to end through the public API: pinned host gradient in, the step's dense result out
+    # end to end through the public API: every step copies its gradients in
+    # from pinned host memory and its dense result out to pinned host memory.
+    # Double-buffered on three streams, so step i+1's upload overlaps step i's
+    # compute and download (the link is full duplex; the upload bounds it).
     e2e, ms_e2e, d2h = None, None, 0
     if not args.no_e2e:
         host = [g.cpu().pin_memory() for g in grads[:2]]
-        gdev = torch.empty((K, N), device=dev)
+        gdev = [torch.empty((K, N), device=dev) for _ in range(2)]
+        res_dev = [torch.empty(N, device=dev) for _ in range(2)]
+        res_host = [None, None]
         state2 = path.fresh_state()
-        res_host = None
+        copy_s = torch.cuda.Stream(device=dev)
+        d2h_s = torch.cuda.Stream(device=dev)
+        ev = {name: [torch.cuda.Event() for _ in range(2)] for name in ("copied", "free", "done", "read")}
 
         def e2e_step(i):
-            nonlocal res_host
-            gdev.copy_(host[i % 2], non_blocking=True)
-            res = path.step(gdev, state2, t=i)
-            if res_host is None:
-                res_host = torch.empty(res.shape, dtype=res.dtype, pin_memory=True)
-            res_host.copy_(res, non_blocking=True)
+            b = i % 2
+            copy_s.wait_event(ev["free"][b])  # the step two back has consumed gdev[b]
+            with torch.cuda.stream(copy_s):
+                gdev[b].copy_(host[i % 2], non_blocking=True)
+            ev["copied"][b].record(copy_s)
+            stream.wait_event(ev["copied"][b])
+            stream.wait_event(ev["read"][b])  # res_dev[b] is no longer being downloaded
+            res = path.step(gdev[b], state2, t=i, res=res_dev[b])
+            ev["free"][b].record(stream)
+            if res_host[b] is None:
+                res_host[b] = torch.empty(res.shape, dtype=res.dtype, pin_memory=True)
+            if path.result_in_state:  # download before the next step updates it
+                res_host[b].copy_(res, non_blocking=True)
+            else:
+                ev["done"][b].record(stream)
+                d2h_s.wait_event(ev["done"][b])
+                with torch.cuda.stream(d2h_s):
+                    res_host[b].copy_(res, non_blocking=True)
+                ev["read"][b].record(d2h_s)
 
         for i in range(max(1, args.warmup)):
             e2e_step(i)
         torch.cuda.synchronize()
-        d2h = int(res_host.numel() * res_host.element_size())
+        d2h = int(res_host[0].numel() * res_host[0].element_size())
         if world > 1:
             dist.barrier()
         f0 = torch.cuda.Event(enable_timing=True)
         f1 = torch.cuda.Event(enable_timing=True)
         e2e_steps = max(3, min(args.steps, 20))
         f0.record(stream)
+        copy_s.wait_event(f0)
         for i in range(e2e_steps):
             e2e_step(i)
+        stream.wait_stream(copy_s)
+        stream.wait_stream(d2h_s)
         f1.record(stream)
         torch.cuda.synchronize()
         ms_e2e = max_over_ranks(f0.elapsed_time(f1) / e2e_steps, dev)
