@@ -185,6 +185,10 @@ __device__ __forceinline__ int find_segment_by_tile(const SegPlan* plan, int S, 
     return lo;
 }
 
+// Bits of |x| with NaN read as 0: maxima of these bit patterns are the float
+// maxima of |x| over the numbers (NaN never wins, as in a `>` scan).
+__device__ __forceinline__ uint32_t nan0_key(float x) { return __float_as_uint(fmaxf(fabsf(x), 0.0f)); }
+
 // Bin maxima of segments whose bins are longer than a tile.
 __global__ void __launch_bounds__(NT) ada_bigmax(const SegPlan* __restrict__ plan, int S, uint64_t N,
                                                  uint32_t tiles_per_learner, uint64_t total_tiles,
@@ -209,7 +213,7 @@ __global__ void __launch_bounds__(NT) ada_bigmax(const SegPlan* __restrict__ pla
             const unsigned am = __ballot_sync(kFull, in);
             if (in) {
                 const unsigned grp = __match_any_sync(am, bin);
-                const uint32_t mx = __reduce_max_sync(grp, mag_key(g));
+                const uint32_t mx = __reduce_max_sync(grp, nan0_key(g));
                 if (lane == __ffs(grp) - 1) atomicMax(&bm[bin], mx);
             }
         }
@@ -221,8 +225,10 @@ __device__ __forceinline__ uint32_t bin_of(uint32_t e, float invL) {
     return (uint32_t)__float2int_rd(((float)e + 0.5f) * invL);
 }
 
+
 // Selection of one tile's entries: sent iff |G + dW| >= the bin's max |G|,
-// the max > 0 and G != 0.  MODE 0: bins of L >= 4 inside the tile (a float4
+// the max > 0 and G != 0 (float compares, as the definition is written: a
+// NaN is never sent).  MODE 0: bins of L >= 4 inside the tile (a float4
 // spans at most two bins, split at `cut`); MODE 1: bins of L < 4; MODE 2:
 // bins longer than a tile, maxima precomputed in global memory.  Bit 4r+j of
 // `flags` marks element j of round r; `packed` holds the per-round counts.
@@ -236,26 +242,25 @@ __device__ __forceinline__ void select_tile(const float4 (&Gv)[4], const float4 
         if (e >= len) continue;
         const float* g4 = &Gv[r].x;
         const float* d4 = &Dv[r].x;
-        uint32_t gm[4];
+        float gm[4];
         if (MODE == 0) {
             const uint32_t b0 = bin_of(e, invL);
             const uint32_t cut = (b0 + 1) * L - e;
-            const uint32_t m0 = bmax[b0];
-            const uint32_t m1 = cut < 4 && b0 + 1 < nbt ? bmax[b0 + 1] : m0;
+            const float m0 = __uint_as_float(bmax[b0]);
+            const float m1 = cut < 4 && b0 + 1 < nbt ? __uint_as_float(bmax[b0 + 1]) : m0;
 #pragma unroll
             for (int j = 0; j < 4; ++j) gm[j] = (uint32_t)j < cut ? m0 : m1;
         } else if (MODE == 1) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) gm[j] = e + j < len ? bmax[bin_of(e + j, invL)] : 0u;
+            for (int j = 0; j < 4; ++j) gm[j] = e + j < len ? __uint_as_float(bmax[bin_of(e + j, invL)]) : 0.0f;
         } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) gm[j] = e + j < len ? __ldg(&bigm[(start + e + j) / L]) : 0u;
+            for (int j = 0; j < 4; ++j) gm[j] = e + j < len ? __uint_as_float(__ldg(&bigm[(start + e + j) / L])) : 0.0f;
         }
         uint32_t f = 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const uint32_t hk = mag_key(__fadd_rn(g4[j], d4[j]));  // |G + dW|
-            const bool sel = hk >= gm[j] && gm[j] > 0u && mag_key(g4[j]) != 0u;
+            const bool sel = fabsf(__fadd_rn(g4[j], d4[j])) >= gm[j] && gm[j] > 0.0f && g4[j] != 0.0f;
             f |= (uint32_t)sel << j;
         }
         if (e + 4 > len) f &= (1u << (len - e)) - 1u;  // a partial float4 at the tile end
@@ -319,9 +324,9 @@ __global__ void __launch_bounds__(NT, 3) ada_bins(const SegPlan* __restrict__ pl
             Gv[r].y = __fadd_rn(Gv[r].y, Dv[r].y);
             Gv[r].z = __fadd_rn(Gv[r].z, Dv[r].z);
             Gv[r].w = __fadd_rn(Gv[r].w, Dv[r].w);
-            if (small && e < kTileMax)
-                *reinterpret_cast<uint4*>(gk + e) =
-                    make_uint4(mag_key(Gv[r].x), mag_key(Gv[r].y), mag_key(Gv[r].z), mag_key(Gv[r].w));
+            if (small && e < kTileMax)  // |G| bits; NaN counts as 0 (it never wins a maximum)
+                *reinterpret_cast<uint4*>(gk + e) = make_uint4(nan0_key(Gv[r].x), nan0_key(Gv[r].y),
+                                                               nan0_key(Gv[r].z), nan0_key(Gv[r].w));
         }
         __syncthreads();
         // 2. bin maxima: a warp per bin for L >= 32, a thread per bin below
@@ -394,16 +399,18 @@ __global__ void __launch_bounds__(NT, 3) ada_bins(const SegPlan* __restrict__ pl
         }
         __syncthreads();
         const uint32_t pb = s_base;
-        if ((uint64_t)pb + cnt_total <= pool_cap) {
+        if ((uint64_t)pb + cnt_total <= pool_cap && flags) {
             uint2* dst = pool + (uint64_t)k * pool_cap + pb;
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
+                const uint32_t fr = (flags >> (4 * r)) & 0xFu;
+                if (!fr) continue;
                 uint32_t pos = round_base[r] + ((uint32_t)(ex >> (16 * r)) & 0xFFFFu);
                 const uint32_t e = 4u * (r * NT + threadIdx.x);
                 const float* g4 = &Gv[r].x;
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    if ((flags >> (4 * r + j)) & 1u) dst[pos++] = make_uint2(p.off + start + e + j, __float_as_uint(g4[j]));
+                    if ((fr >> j) & 1u) dst[pos++] = make_uint2(p.off + start + e + j, __float_as_uint(g4[j]));
             }
         }
         __syncthreads();

@@ -89,6 +89,38 @@ def test_bin_lengths(cuda_lib, L):
     run_adacomp(cuda_lib, off, [L] * len(sizes), dWs)
 
 
+def test_nan_entries_are_never_sent(cuda_lib):
+    """A NaN in G never wins a bin maximum and is never sent (every comparison
+    with NaN is false); its residue stays NaN; the rest is unaffected."""
+    import torch
+    gc = cuda_lib
+    rng = np.random.default_rng(17)
+    sizes, lt = [5000, 30000, 9000], [50, 500, 7000]
+    off = wl.layout_offsets(sizes)
+    K, N = 2, off[-1]
+    dW = rng.laplace(0, 1e-3, size=(K, N)).astype(np.float32)
+    dW[0, [3, 77, 5123, 30001, 36000]] = np.nan
+    dW[1, [0, 4999, 35000]] = np.nan
+    R_o = np.zeros((K, N), np.float32)
+    idx_o, val_o, counts_o, scales_o, totals_o = oracle.adacomp_step(off, lt, dW, R_o, cap=N)
+    R_g = torch.zeros((K, N), device="cuda")
+    a = gc.AdaComp(off, lt, K, N)
+    out, totals = a(torch.from_numpy(dW).cuda(), R_g)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(a.counts.cpu().numpy(), counts_o)
+    np.testing.assert_array_equal(totals.cpu().numpy(), totals_o)
+    assert rel_err(a.scales.cpu().numpy(), scales_o) <= VAL_RTOL
+    idx_g, val_g = gc.pair_indices(out).cpu().numpy(), gc.pair_values(out).cpu().numpy()
+    for k in range(K):
+        n = int(totals_o[k])
+        np.testing.assert_array_equal(idx_g[k, :n], idx_o[k, :n].astype(np.int64))
+        assert not np.isnan(val_g[k, :n]).any() and rel_err(val_g[k, :n], val_o[k, :n]) <= VAL_RTOL
+    Rg = R_g.cpu().numpy()
+    np.testing.assert_array_equal(np.isnan(Rg), np.isnan(R_o))
+    fin = ~np.isnan(R_o)
+    assert rel_err(Rg[fin], R_o[fin]) <= VAL_RTOL
+
+
 def test_mixed_bins_and_ragged_offsets(cuda_lib):
     rng = np.random.default_rng(5)
     sizes = [7, 50001, 13, 4096, 4097, 99999]
