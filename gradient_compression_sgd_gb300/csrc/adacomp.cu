@@ -293,10 +293,10 @@ __global__ void __launch_bounds__(NT, 3) ada_bins(const SegPlan* __restrict__ pl
         const bool small = p.mode == kModeSmall;
         const uint32_t L = p.L;
         const uint32_t nbt = small ? (p.nbins - tj * p.bpt < p.bpt ? p.nbins - tj * p.bpt : p.bpt) : 0;
-        const bool aligned = (base & 3) == 0;
         const uint32_t* bigm = big + (uint64_t)k * big_per_learner + p.big_off;
         const float* dWt = dW + base;
         float* Rt = R + base;
+        const bool aligned = (((uintptr_t)dWt | (uintptr_t)Rt) & 15) == 0;  // 128-bit accesses
 
         // 1. G = R + dW (registers) and |G| keys to shared memory
         float4 Gv[4], Dv[4];

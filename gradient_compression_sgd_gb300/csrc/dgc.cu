@@ -322,7 +322,8 @@ __global__ void __launch_bounds__(NT, 3) dgc_update(const SegPlan* __restrict__ 
         const uint32_t unit = k * S + s;
         const uint32_t h = p.kind == kKindPool ? __ldg(&hint[unit]) : 0xffffffffu;  // no candidates
         const float c = __ldg(&clip_c[k]);
-        const bool aligned = (base & 3) == 0;
+        const bool aligned =  // 128-bit accesses need 16-byte addresses
+            (((uintptr_t)(grad + base) | (uintptr_t)(u + base) | (uintptr_t)(v + base)) & 15) == 0;
 
         float4 G[4], U[4], V[4];
 #pragma unroll
@@ -683,7 +684,7 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
     if (!pool_ok && p.n <= kRawMax) {
         // kRawMax = 8 float4 per thread: issue every load before the first store
         radix_hist_clear<NTS>(rs);
-        const bool aligned = (ebase & 3) == 0;
+        const bool aligned = ((uintptr_t)vseg & 15) == 0;
         float4 q[kRawMax / (4 * NTS)];
 #pragma unroll
         for (int r = 0; r < (int)(kRawMax / (4 * NTS)); ++r) {

@@ -19,13 +19,22 @@ AVG_RTOL = 1e-5
 
 # ------------------------------------------------------------------ AdaComp
 
-def run_adacomp(gc, offsets, lt, dWs, cap=None, R0=None):
+def shifted(a, offset):
+    """A CUDA copy of `a` starting `offset` floats past an allocation's start."""
+    import torch
+    flat = torch.zeros(a.size + offset, dtype=torch.float32, device="cuda")
+    view = flat[offset:].view(a.shape)
+    view.copy_(torch.from_numpy(np.ascontiguousarray(a)))
+    return view
+
+
+def run_adacomp(gc, offsets, lt, dWs, cap=None, R0=None, offset=0):
     import torch
     offsets = np.asarray(offsets, np.int64)
     K, N = dWs[0].shape
     cap = cap if cap is not None else max(1, N)
     R_o = np.zeros((K, N), np.float32) if R0 is None else R0.copy()
-    R_g = torch.from_numpy(R_o.copy()).cuda()
+    R_g = shifted(R_o, offset)
     a = gc.AdaComp(offsets, lt, K, cap)
     results = []
     for t, dW in enumerate(dWs):
@@ -35,7 +44,7 @@ def run_adacomp(gc, offsets, lt, dWs, cap=None, R0=None):
             over = False
         except oracle.OracleError:
             over = True
-        out, totals = a(torch.from_numpy(np.ascontiguousarray(dW)).cuda(), R_g)
+        out, totals = a(shifted(dW, offset), R_g)
         torch.cuda.synchronize()
         tot_g = totals.cpu().numpy()
         if over:
@@ -87,6 +96,16 @@ def test_bin_lengths(cuda_lib, L):
     K = 2
     dWs = [rng.laplace(0, 1e-3, size=(K, off[-1])).astype(np.float32) for _ in range(3)]
     run_adacomp(cuda_lib, off, [L] * len(sizes), dWs)
+
+
+@pytest.mark.parametrize("offset", [1, 2, 3])
+def test_buffers_not_16_byte_aligned(cuda_lib, offset):
+    """dW and R starting 4, 8 or 12 bytes past a 16-byte boundary."""
+    rng = np.random.default_rng(offset + 40)
+    sizes, lt = [50001, 8000, 4096], [50, 500, 64]
+    off = wl.layout_offsets(sizes)
+    dWs = [rng.laplace(0, 1e-3, size=(2, off[-1])).astype(np.float32) for _ in range(2)]
+    run_adacomp(cuda_lib, off, lt, dWs, offset=offset)
 
 
 def test_nan_entries_are_never_sent(cuda_lib):

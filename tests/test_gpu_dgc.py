@@ -18,20 +18,30 @@ pytestmark = pytest.mark.gpu
 VAL_RTOL = 1e-6
 
 
-def run_dgc(gc, offsets, grads, density, momentum, clip_thr=0.0, clip_nodes=1, u0=None, v0=None):
+def shifted(a, offset):
+    """A CUDA copy of `a` that starts `offset` floats past an allocation's start
+    (offset 1..3: not 16-byte aligned)."""
+    import torch
+    flat = torch.zeros(a.size + offset, dtype=torch.float32, device="cuda")
+    view = flat[offset:].view(a.shape)
+    view.copy_(torch.from_numpy(np.ascontiguousarray(a)))
+    return view
+
+
+def run_dgc(gc, offsets, grads, density, momentum, clip_thr=0.0, clip_nodes=1, u0=None, v0=None, offset=0):
     """Step both sides through the gradient list and compare after every step."""
     import torch
     offsets = np.asarray(offsets, np.int64)
     K, N = grads[0].shape
     u_o = np.zeros((K, N), np.float32) if u0 is None else u0.copy()
     v_o = np.zeros((K, N), np.float32) if v0 is None else v0.copy()
-    u_g = torch.from_numpy(u_o.copy()).cuda()
-    v_g = torch.from_numpy(v_o.copy()).cuda()
+    u_g = shifted(u_o, offset)
+    v_g = shifted(v_o, offset)
     d = gc.DGC(offsets, K, density, momentum, clip_thr, clip_nodes)
     for t, G in enumerate(grads):
         idx_o, val_o, counts_o, _ = oracle.dgc_step(offsets, G, u_o, v_o, density, momentum, clip_thr, clip_nodes,
                                                     cap=d.cap)
-        out, totals = d(torch.from_numpy(np.ascontiguousarray(G)).cuda(), u_g, v_g)
+        out, totals = d(shifted(G, offset), u_g, v_g)
         torch.cuda.synchronize()
         counts_g = d.counts.cpu().numpy()
         np.testing.assert_array_equal(counts_g, counts_o, err_msg=f"counts, step {t}")
@@ -131,6 +141,15 @@ def test_hint_above_the_kth_value_falls_back(cuda_lib):
     G[0, 30001:30050] = 0.5
     d = run_dgc(cuda_lib, [0, n], [G], density, 0.9)
     assert d.stats()["hint_failed"] == 1
+
+
+@pytest.mark.parametrize("offset", [1, 2, 3])
+def test_buffers_not_16_byte_aligned(cuda_lib, offset):
+    """g, u and v starting 4, 8 or 12 bytes past a 16-byte boundary."""
+    rng = np.random.default_rng(offset)
+    off = wl.layout_offsets([5000, 70001, 4096, 20000])
+    grads = [rng.standard_normal((2, off[-1])).astype(np.float32) for _ in range(2)]
+    run_dgc(cuda_lib, off, grads, 0.01, 0.9, offset=offset)
 
 
 def test_nonzero_initial_state_and_momentum_zero(cuda_lib):
