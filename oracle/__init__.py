@@ -56,6 +56,9 @@ def lib():
                                               ctypes.c_int64, vp, vp, vp]
             L.oracle_sparse_average.restype = ctypes.c_int
             L.oracle_sparse_average.argtypes = [ctypes.c_int, vp, vp, ctypes.c_int64, vp, ctypes.c_int64, vp]
+            L.oracle_sparse_average_update.restype = ctypes.c_int
+            L.oracle_sparse_average_update.argtypes = [ctypes.c_int, vp, vp, ctypes.c_int64, vp, ctypes.c_int64,
+                                                       ctypes.c_float, vp]
             L.oracle_philox4x32_10.restype = None
             L.oracle_philox4x32_10.argtypes = [vp, vp, vp]
             L.oracle_keep_threshold.restype = ctypes.c_uint64
@@ -151,6 +154,18 @@ def sparse_average(idx, val, counts, n):
     rc = lib().oracle_sparse_average(K, _p(idx), _p(val), int(cap), _p(counts), int(n), _p(out))
     _check(rc, "oracle_sparse_average")
     return out
+
+
+def sparse_average_update(idx, val, counts, n, lr, w):
+    """w[j] -= lr * avg[j] at every index some list carries; ``w`` ([n] float32) is updated in place."""
+    idx = np.ascontiguousarray(idx, dtype=np.uint32)
+    val = _f32(val)
+    counts = np.ascontiguousarray(counts, dtype=np.int64)
+    assert w.dtype == np.float32 and w.flags["C_CONTIGUOUS"] and w.size >= n
+    K, cap = idx.shape
+    rc = lib().oracle_sparse_average_update(K, _p(idx), _p(val), int(cap), _p(counts), int(n), float(lr), _p(w))
+    _check(rc, "oracle_sparse_average_update")
+    return w
 
 
 def philox4x32_10(ctr, key) -> np.ndarray:

@@ -309,6 +309,40 @@ int oracle_sparse_average(int K, const uint32_t* idx, const float* val, int64_t 
     return ORACLE_OK;
 }
 
+/*
+ * Averaged sparse update of the weights: the learners' messages are averaged
+ * as above and the weights step against the average, w[j] <- w[j] - lr * avg[j]
+ * ("AdaComp ...", Proposed method: learners exchange compressed gradients and
+ * average them to update the weights; "Deep Gradient Compression", Appendix A:
+ * the summed gradients optimise the model).  Reading: only the indices that
+ * some message carries are updated (every other weight keeps its exact bits);
+ * lr * avg and the subtraction are one fp32 rounding each.
+ */
+int oracle_sparse_average_update(int K, const uint32_t* idx, const float* val, int64_t cap,
+                                 const int64_t* counts, int64_t n, float lr, float* w) {
+    if (K < 1 || n < 0) return ORACLE_EINVAL;
+    float* avg = (float*)malloc(sizeof(float) * (size_t)(n > 0 ? n : 1));
+    unsigned char* carried = (unsigned char*)calloc((size_t)(n > 0 ? n : 1), 1);
+    if (!avg || !carried) {
+        free(avg);
+        free(carried);
+        return ORACLE_ENOMEM;
+    }
+    int rc = oracle_sparse_average(K, idx, val, cap, counts, n, avg);
+    if (rc == ORACLE_OK) {
+        for (int k = 0; k < K; ++k)
+            for (int64_t p = 0; p < counts[k]; ++p) carried[idx[(int64_t)k * cap + p]] = 1;
+        for (int64_t j = 0; j < n; ++j)
+            if (carried[j]) {
+                const float step = lr * avg[j];
+                w[j] = w[j] - step;
+            }
+    }
+    free(avg);
+    free(carried);
+    return rc;
+}
+
 /* ------------------------------------------------------- Philox4x32-10 */
 
 /*

@@ -58,6 +58,44 @@ def test_index_out_of_range_is_rejected():
         oracle.sparse_average(idx, val, np.array([1]), 5)
 
 
+# ------------------------------------------- averaged sparse weight update
+
+@pytest.mark.parametrize("K", [1, 2, 4, 7])
+def test_update_matches_numpy(K):
+    """w[j] -= lr * avg[j] on the support, with avg from numpy's ordered
+    ufunc.at and one float32 rounding per operation; every other weight keeps
+    its bits (including -0.0 and a NaN payload)."""
+    rng = np.random.default_rng(100 + K)
+    n, cap = 4000, 300
+    idx, val, counts = _lists(rng, K, n, cap, cap)
+    w0 = rng.standard_normal(n).astype(np.float32)
+    support = np.zeros(n, bool)
+    for k in range(K):
+        support[idx[k, :counts[k]]] = True
+    off = np.nonzero(~support)[0]
+    w0[off[0]] = -0.0
+    w0[off[1]] = np.frombuffer(np.uint32(0x7FC00123).tobytes(), np.float32)[0]
+    acc = np.zeros(n, np.float32)
+    for k in range(K):
+        np.add.at(acc, idx[k, :counts[k]].astype(np.int64), val[k, :counts[k]])
+    avg = acc / np.float32(K)
+    lr = np.float32(0.0375)
+    want = w0.copy()
+    want[support] = want[support] - lr * avg[support]
+    got = oracle.sparse_average_update(idx, val, counts, n, lr, w0.copy())
+    np.testing.assert_array_equal(got.view(np.uint32)[~support], w0.view(np.uint32)[~support])
+    np.testing.assert_array_equal(got[support], want[support])
+
+
+def test_update_single_list_dyadic_is_exact():
+    """K = 1, lr = 1/2 and dyadic values: every step is exact, w - v/2."""
+    idx = np.array([[1, 4, 7]], np.uint32)
+    val = np.array([[2.0, -0.5, 3.0]], np.float32)
+    w = np.array([1, 1, 1, 1, 1, 1, 1, 1], np.float32)
+    oracle.sparse_average_update(idx, val, np.array([3]), 8, 0.5, w)
+    np.testing.assert_array_equal(w, np.array([1, 0, 1, 1, 1.25, 1, 1, -0.5], np.float32))
+
+
 # -------------------------------------------------------------------- Philox
 
 def test_philox_known_answers(golden):

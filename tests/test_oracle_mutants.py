@@ -39,6 +39,9 @@ MUTANTS = {
     "ada_partial_bin_dropped": ("const int64_t nb = (n + L - 1) / L;", "const int64_t nb = n / L > 0 ? n / L : 1;"),
     # sparse average
     "average_not_divided": ("out[j] = out[j] / fk;", "out[j] = out[j];"),
+    "update_adds_the_step": ("w[j] = w[j] - step;", "w[j] = w[j] + step;"),
+    "update_skips_last_list": ("for (int k = 0; k < K; ++k)\n            for (int64_t p = 0; p < counts[k]; ++p) carried",
+                               "for (int k = 0; k < K - 1; ++k)\n            for (int64_t p = 0; p < counts[k]; ++p) carried"),
     # Philox and DCD-PSGD
     "philox_key_word_swapped": ("uint32_t n0 = hi1 ^ c1 ^ k0;", "uint32_t n0 = hi1 ^ c1 ^ k1;"),
     "dcd_wrong_neighbour": ("const int l = (i + n - 1) % n, r = (i + 1) % n;\n        const float* xl",
