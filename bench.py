@@ -308,6 +308,12 @@ class DgcPath:
     def sent(self):
         return int(self.obj.totals.sum().item())
 
+    def step_update(self, g, w, lr, state=None):
+        """Compress, then the fused average-and-update of the weights (no dense average)."""
+        u, v = state or self.state
+        out, totals = self.obj(g, u, v)
+        self.gc.sparse_average_update(out, totals, self.N, lr, w)
+
     def extra(self):
         return {"select_paths": self.obj.stats()}
 
@@ -329,6 +335,11 @@ class AdaCompPath(DgcPath):
         res = self.avg if res is None else res
         self.gc.sparse_average(out, totals, self.N, res)
         return res
+
+    def step_update(self, g, w, lr, state=None):
+        (R,) = state or self.state
+        out, totals = self.obj(g, R)
+        self.gc.sparse_average_update(out, totals, self.N, lr, w)
 
     def extra(self):
         tot = self.obj.totals.cpu()
@@ -419,6 +430,31 @@ def run_gpu(args):
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
     grad_bytes = 4.0 * K * N
     value = job_gbs(world, grad_bytes, ms)
+
+    # the fused variant: compress + averaged weight update on the carried
+    # indices only (no dense average written)
+    fused = None
+    if hasattr(path, "step_update"):
+        weights = torch.zeros(N, device=dev)
+        state_u = path.fresh_state()
+        for i in range(args.warmup):
+            path.step_update(grads[i % N_SETS], weights, 0.01, state_u)
+        torch.cuda.synchronize()
+        gc.trace_enable(True)
+        h0 = torch.cuda.Event(enable_timing=True)
+        h1 = torch.cuda.Event(enable_timing=True)
+        h0.record(stream)
+        for i in range(args.steps):
+            path.step_update(grads[i % N_SETS], weights, 0.01, state_u)
+        h1.record(stream)
+        torch.cuda.synchronize()
+        gc.trace_enable(False)
+        tr_u = gc.trace_read()
+        ms_u = max_over_ranks(h0.elapsed_time(h1) / args.steps, dev)
+        nu, tu = tr_u.get("spavg_update", (0, 0.0))
+        fused = {"step": "compress + sparse_average_update (weights stepped on the carried indices)",
+                 "value": job_gbs(world, 4.0 * K * N, ms_u), "unit": "GB/s", "ms_per_step": ms_u,
+                 "update_ms_per_launch": tu / max(nu, 1)}
 
     # end to end through the public API: every step copies its gradients in
     # from pinned host memory and its dense result out to pinned host memory.
@@ -517,6 +553,7 @@ def run_gpu(args):
         **path.extra(),
         "e2e": None if e2e is None else {"value": e2e, "unit": "GB/s", "ms_per_step": ms_e2e,
                                          "h2d_bytes_per_step": int(grad_bytes), "d2h_bytes_per_step": d2h},
+        "fused_update": fused,
         "gpu_launches": launches,
         "clocks": clk,
         "cpu_baseline": cpu,

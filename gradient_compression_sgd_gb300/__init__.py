@@ -84,6 +84,7 @@ def lib():
         L.gcsgd_adacomp_workspace_size.argtypes = [vp, i32, vp, i32, i64, vp]
         L.adacomp_compress.argtypes = [vp, i32, vp, i32, vp, vp, vp, i64, vp, vp, vp, vp, sz, vp]
         L.sparse_average.argtypes = [vp, i64, vp, i32, i64, vp, vp]
+        L.sparse_average_update.argtypes = [vp, i64, vp, i32, i64, f32, vp, vp]
         L.dcd_step.argtypes = [i32, i64, vp, vp, vp, f32, f64, u64, u32, vp]
         _lib = L
         return L
@@ -291,6 +292,17 @@ def sparse_average(lists, counts, n: int, out, stream=None):
     _check("sparse_average", lib().sparse_average(
         _dev(lists, "lists", torch.int32), int(cap), _dev(counts, "counts", torch.int64), int(K), int(n),
         _dev(out, "out", torch.float32), _stream(stream)))
+
+
+def sparse_average_update(lists, counts, n: int, lr: float, w, stream=None):
+    """w[j] -= lr * (K-way average)[j] at every carried index (see sparse_average_update in include/gcsgd.h)."""
+    import torch
+    K, cap = lists.shape[0], lists.shape[1]
+    if counts.numel() != K:
+        raise ValueError("counts must have K entries")
+    _check("sparse_average_update", lib().sparse_average_update(
+        _dev(lists, "lists", torch.int32), int(cap), _dev(counts, "counts", torch.int64), int(K), int(n),
+        float(lr), _dev(w, "w", torch.float32), _stream(stream)))
 
 
 # -------------------------------------------------------------------- DCD

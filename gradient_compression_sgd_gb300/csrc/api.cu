@@ -22,7 +22,7 @@ int adacomp_launch(const int64_t* off, int S, const int32_t* lt, int K, const fl
                    int64_t cap, int64_t* counts, float* scales, int64_t* totals, void* ws, size_t ws_bytes,
                    cudaStream_t stream);
 int spavg_launch(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int K, int64_t n, float* out,
-                 cudaStream_t stream);
+                 cudaStream_t stream, bool update, float lr);
 int dcd_launch(int n, int64_t d, const float* w, float* xhat, const float* grad, float gamma, double p, uint64_t seed,
                uint32_t t, cudaStream_t stream);
 
@@ -253,15 +253,29 @@ int adacomp_compress(const int64_t* seg_offsets, int32_t n_seg, const int32_t* l
                           workspace_bytes, (cudaStream_t)stream);
 }
 
-int sparse_average(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int32_t K, int64_t n, float* out,
-                   void* stream) {
-    const char* fn = "sparse_average";
+static int check_average(const char* fn, const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int32_t K,
+                         int64_t n, const float* out) {
     if (K < 1 || K > 512) return set_error(GCSGD_ERR_INVALID_ARG, "%s: K = %d outside [1, 512]", fn, K);
     if (n < 0 || n > ((int64_t)1 << 32)) return set_error(GCSGD_ERR_INVALID_ARG, "%s: n outside [0, 2^32]", fn);
     if (cap < 0) return set_error(GCSGD_ERR_INVALID_ARG, "%s: cap < 0", fn);
     if (!counts || (n > 0 && !out) || (cap > 0 && !lists))
         return set_error(GCSGD_ERR_INVALID_ARG, "%s: NULL pointer", fn);
-    return spavg_launch(lists, cap, counts, K, n, out, (cudaStream_t)stream);
+    return GCSGD_OK;
+}
+
+int sparse_average(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int32_t K, int64_t n, float* out,
+                   void* stream) {
+    int rc = check_average("sparse_average", lists, cap, counts, K, n, out);
+    if (rc) return rc;
+    return spavg_launch(lists, cap, counts, K, n, out, (cudaStream_t)stream, false, 0.0f);
+}
+
+int sparse_average_update(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int32_t K, int64_t n,
+                          float lr, float* w, void* stream) {
+    int rc = check_average("sparse_average_update", lists, cap, counts, K, n, w);
+    if (rc) return rc;
+    if (!isfinite(lr)) return set_error(GCSGD_ERR_INVALID_ARG, "sparse_average_update: lr is not finite");
+    return spavg_launch(lists, cap, counts, K, n, w, (cudaStream_t)stream, true, lr);
 }
 
 int dcd_step(int32_t n_nodes, int64_t d, const float* w_ring, float* xhat, const float* grad, float gamma,

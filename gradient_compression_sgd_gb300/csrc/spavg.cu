@@ -18,6 +18,14 @@
 // is written exactly once and each entry is read once (a list denser than its
 // window in some tile is read in place for that tile), which is the minimum
 // traffic.
+//
+// Update mode (sparse_average_update): the same sums, but instead of a dense
+// average the weights are stepped, w[j] -= lr * avg[j], at the carried
+// indices only.  When a CTA's entries fit its stage and K <= 32, each warp
+// merges the staged runs and updates 32 weights at a time (merge_update: the
+// work follows the entries, no dense pass); otherwise the tile path marks the
+// carried positions in a bitmap and read-modify-writes only those
+// (update_tile).
 #include "common.cuh"
 
 namespace gcsgd {
@@ -86,6 +94,49 @@ __device__ __forceinline__ void store_tile(float* acc, float* out, uint64_t r0, 
     }
 }
 
+// Update mode: w[j] <- w[j] - lr * (acc[j] / K) at the positions of the tile
+// that some list carries (`touched` bits), with 128-bit read-modify-writes
+// where aligned; leaves acc zeroed.  Also clears `next_touched`, the bitmap
+// of the tile after this one (its last readers finished before this tile
+// began).
+__device__ __forceinline__ void update_tile(float* acc, const uint32_t* touched, uint32_t* next_touched, float* w,
+                                            uint64_t r0, uint64_t r1, float fk, float lr) {
+    constexpr int kRounds = kTile / (4 * NT);
+    const uint64_t len = r1 - r0;
+    const int K = (int)fk;
+    const bool pow2 = (K & (K - 1)) == 0;
+    const float inv_k = 1.0f / fk;
+    const bool w_aligned = ((uintptr_t)(w + r0) & 15) == 0;
+    float4 q[kRounds], x[kRounds];
+    uint32_t bits[kRounds];
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {  // every weight load in flight before the first use
+        const uint32_t j = 4 * (r * NT + threadIdx.x);
+        q[r] = *reinterpret_cast<const float4*>(acc + j);
+        *reinterpret_cast<float4*>(acc + j) = make_float4(0.f, 0.f, 0.f, 0.f);
+        bits[r] = j < len ? (touched[j >> 5] >> (j & 31)) & 0xFu : 0u;
+        if (bits[r] && w_aligned && j + 4 <= len) x[r] = *reinterpret_cast<const float4*>(w + r0 + j);
+    }
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+        if (!bits[r]) continue;
+        const uint32_t j = 4 * (r * NT + threadIdx.x);
+        const float* qq = &q[r].x;
+        float* wj = w + r0 + j;
+        if (w_aligned && j + 4 <= len) {
+            float* xx = &x[r].x;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                if ((bits[r] >> c) & 1u) xx[c] = __fsub_rn(xx[c], __fmul_rn(lr, div_k(qq[c], fk, inv_k, pow2)));
+            *reinterpret_cast<float4*>(wj) = x[r];
+        } else {
+            for (int c = 0; c < 4 && j + c < len; ++c)
+                if ((bits[r] >> c) & 1u) wj[c] = __fsub_rn(wj[c], __fmul_rn(lr, div_k(qq[c], fk, inv_k, pow2)));
+        }
+    }
+    for (uint32_t t = threadIdx.x; t < kTile / 32; t += NT) next_touched[t] = 0u;
+}
+
 // First position in [a, b) of a sorted run whose index is >= target.
 __device__ __forceinline__ uint32_t lower_in(const gcsgd_pair* st, uint32_t a, uint32_t b, uint64_t target) {
     while (a < b) {
@@ -104,12 +155,73 @@ __device__ __forceinline__ uint64_t lower_global(const gcsgd_pair* L, uint64_t a
     return a;
 }
 
+// Update mode over a staged range with K <= 32 lists: warp w merges the K
+// sorted runs over its part of [R0, R1), lane k holding list k's next entry.
+// At the smallest head index the heads there are summed in learner order
+// from +0 (the definition's fp32 sum, bit for bit); lane b of the warp keeps
+// the b-th such (index, sum), and every 32 of them the lanes update their
+// weights together (independent loads, one latency per 32 updates).  No
+// dense pass: the work follows the entries.
+__device__ void merge_update(const gcsgd_pair* stage, const uint32_t* soff, int K, uint64_t R0, uint64_t R1, float fk,
+                             float lr, float* w) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint64_t per_w = (R1 - R0 + NW - 1) / NW;
+    const uint64_t P0 = R0 + (uint64_t)warp * per_w < R1 ? R0 + (uint64_t)warp * per_w : R1;
+    const uint64_t P1 = P0 + per_w < R1 ? P0 + per_w : R1;
+    const bool pow2 = (K & (K - 1)) == 0;
+    const float inv_k = 1.0f / fk;
+    uint32_t c = 0, e = 0, hidx = 0xffffffffu;  // head of list `lane` (valid when `has`)
+    float hval = 0.0f;
+    bool has = false;
+    auto load_head = [&]() {
+        has = false;
+        if (c < e) {
+            const gcsgd_pair it = stage[c];
+            if ((uint64_t)it.idx < P1) {
+                hidx = it.idx;
+                hval = it.val;
+                has = true;
+            }
+        }
+    };
+    if (lane < K) {
+        e = soff[lane + 1];
+        c = lower_in(stage, soff[lane], e, P0);
+        load_head();
+    }
+    uint32_t my_idx = 0, nb = 0;
+    float my_sum = 0.0f;
+    auto flush = [&]() {
+        if ((uint32_t)lane < nb) w[my_idx] = __fsub_rn(w[my_idx], __fmul_rn(lr, div_k(my_sum, fk, inv_k, pow2)));
+        nb = 0;
+    };
+    for (;;) {  // every round advances at least one lane: at most `total` rounds
+        if (!__any_sync(kFull, has)) break;
+        const uint32_t m = __reduce_min_sync(kFull, has ? hidx : 0xffffffffu);
+        const unsigned at = __ballot_sync(kFull, has && hidx == m);
+        float sum = 0.0f;
+        for (unsigned mm = at; mm; mm &= mm - 1u) sum = __fadd_rn(sum, __shfl_sync(kFull, hval, __ffs(mm) - 1));
+        if ((uint64_t)m >= P0 && (uint32_t)lane == nb) {  // (m < P0 only for unsorted input)
+            my_idx = m;
+            my_sum = sum;
+        }
+        nb += (uint64_t)m >= P0 ? 1u : 0u;
+        if (has && hidx == m) {
+            ++c;
+            load_head();
+        }
+        if (nb == 32) flush();
+    }
+    flush();
+}
+
 // Shared memory: acc[kTile] | stage[kStage] pairs | per list (u64): cnt, ptr, wbeg |
 // (u32): wlen, flag, soff[K+1] | bnd[K][NW+1] (u32)
+template <bool UPDATE>
 __global__ void __launch_bounds__(NT) spavg_kernel(const gcsgd_pair* __restrict__ lists, uint64_t cap,
                                                    const int64_t* __restrict__ counts, int K, uint64_t n,
                                                    float* __restrict__ out, uint64_t tiles, uint64_t tiles_per_cta,
-                                                   uint32_t C) {
+                                                   uint32_t C, float lr) {
     extern __shared__ __align__(16) unsigned char smem[];
     float* acc = reinterpret_cast<float*>(smem);
     gcsgd_pair* stage = reinterpret_cast<gcsgd_pair*>(smem + kTile * sizeof(float));
@@ -123,6 +235,9 @@ __global__ void __launch_bounds__(NT) spavg_kernel(const gcsgd_pair* __restrict_
     uint32_t* bnd = soff + K + 1;                            // [K][NW+1] slice bounds within the windows
     __shared__ int s_any;
     __shared__ uint32_t s_total;
+    __shared__ uint32_t touched2[2][kTile / 32];  // update mode: positions some list carries, by tile parity
+    if (UPDATE)
+        for (uint32_t q = threadIdx.x; q < 2 * (kTile / 32); q += NT) (&touched2[0][0])[q] = 0u;
     const uint64_t t0 = (uint64_t)blockIdx.x * tiles_per_cta;
     if (t0 >= tiles) return;
     const uint64_t t1 = t0 + tiles_per_cta < tiles ? t0 + tiles_per_cta : tiles;
@@ -188,6 +303,10 @@ __global__ void __launch_bounds__(NT) spavg_kernel(const gcsgd_pair* __restrict_
         }
         for (int k = threadIdx.x; k < K; k += NT) wlen[k] = soff[k];  // reuse: next staged entry of list k
         __syncthreads();
+        if (UPDATE && K <= 32) {
+            merge_update(stage, soff, K, R0, R1, fk, lr, out);
+            return;
+        }
         for (uint64_t t = t0; t < t1; ++t) {
             const uint64_t r0 = t * kTile;
             const uint64_t r1 = r0 + kTile < n ? r0 + kTile : n;
@@ -203,8 +322,9 @@ __global__ void __launch_bounds__(NT) spavg_kernel(const gcsgd_pair* __restrict_
                         if (i < e) it = stage[i];
                         const bool in = i < e && (uint64_t)it.idx < r1;
                         if (in && (uint64_t)it.idx >= r0) {
-                            float* acc_j = acc + (it.idx - r0);
-                            *acc_j = __fadd_rn(*acc_j, it.val);
+                            const uint32_t pos = (uint32_t)(it.idx - r0);
+                            acc[pos] = __fadd_rn(acc[pos], it.val);
+                            if (UPDATE) atomicOr(&touched2[t & 1][pos >> 5], 1u << (pos & 31));
                         }
                         const int c = __popc(__ballot_sync(kFull, in));
                         a += c;
@@ -215,7 +335,8 @@ __global__ void __launch_bounds__(NT) spavg_kernel(const gcsgd_pair* __restrict_
                 }
             }
             __syncthreads();
-            store_tile(acc, out, r0, r1, fk);  // also re-zeroes acc
+            if (UPDATE) update_tile(acc, touched2[t & 1], touched2[(t + 1) & 1], out, r0, r1, fk, lr);
+            else store_tile(acc, out, r0, r1, fk);  // also re-zeroes acc
             __syncthreads();
         }
         return;
@@ -286,8 +407,9 @@ __global__ void __launch_bounds__(NT) spavg_kernel(const gcsgd_pair* __restrict_
                     for (uint32_t i = a + lane; i < b; i += 32) {
                         const gcsgd_pair it = st[i];
                         if ((uint64_t)it.idx >= s0 && (uint64_t)it.idx < s1) {  // always, for sorted lists
-                            float* acc_j = acc + (it.idx - r0);
-                            *acc_j = __fadd_rn(*acc_j, it.val);
+                            const uint32_t pos = (uint32_t)(it.idx - r0);
+                            acc[pos] = __fadd_rn(acc[pos], it.val);
+                            if (UPDATE) atomicOr(&touched2[t & 1][pos >> 5], 1u << (pos & 31));
                         }
                     }
                 } else {
@@ -297,8 +419,9 @@ __global__ void __launch_bounds__(NT) spavg_kernel(const gcsgd_pair* __restrict_
                     for (uint64_t i = a + lane; i < b; i += 32) {
                         const gcsgd_pair it = L[i];
                         if ((uint64_t)it.idx >= s0 && (uint64_t)it.idx < s1) {
-                            float* acc_j = acc + (it.idx - r0);
-                            *acc_j = __fadd_rn(*acc_j, it.val);
+                            const uint32_t pos = (uint32_t)(it.idx - r0);
+                            acc[pos] = __fadd_rn(acc[pos], it.val);
+                            if (UPDATE) atomicOr(&touched2[t & 1][pos >> 5], 1u << (pos & 31));
                         }
                     }
                 }
@@ -309,7 +432,8 @@ __global__ void __launch_bounds__(NT) spavg_kernel(const gcsgd_pair* __restrict_
         for (int k = threadIdx.x; k < K; k += NT)
             ptr[k] = flag[k] ? lower_global(lists + (uint64_t)k * cap, ptr[k], cnt[k], r1)
                              : wbeg[k] + bnd[k * (NW + 1) + NW];
-        store_tile(acc, out, r0, r1, fk);
+        if (UPDATE) update_tile(acc, touched2[t & 1], touched2[(t + 1) & 1], out, r0, r1, fk, lr);
+        else store_tile(acc, out, r0, r1, fk);
         __syncthreads();
     }
 }
@@ -317,7 +441,7 @@ __global__ void __launch_bounds__(NT) spavg_kernel(const gcsgd_pair* __restrict_
 }  // namespace spavg
 
 int spavg_launch(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int K, int64_t n, float* out,
-                 cudaStream_t stream) {
+                 cudaStream_t stream, bool update, float lr) {
     using namespace spavg;
     if (n == 0) return GCSGD_OK;
     const uint64_t tiles = ((uint64_t)n + kTile - 1) / kTile;
@@ -335,14 +459,21 @@ int spavg_launch(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, in
     int dev = 0;
     cudaGetDevice(&dev);
     if (smem > 48 * 1024 && dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(spavg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) != cudaSuccess)
+        if (cudaFuncSetAttribute(spavg_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(spavg_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
+                cudaSuccess)
             return set_error(GCSGD_ERR_CUDA, "sparse_average: cannot raise the shared-memory limit");
         attr_set[dev] = true;
     }
-    LaunchScope ls("spavg", stream);
-    spavg_kernel<<<(unsigned)grid, NT, smem, stream>>>(lists, (uint64_t)cap, counts, K, (uint64_t)n, out, tiles, per,
-                                                       C);
-    return check_launch("spavg");
+    LaunchScope ls(update ? "spavg_update" : "spavg", stream);
+    if (update)
+        spavg_kernel<true><<<(unsigned)grid, NT, smem, stream>>>(lists, (uint64_t)cap, counts, K, (uint64_t)n, out,
+                                                                 tiles, per, C, lr);
+    else
+        spavg_kernel<false><<<(unsigned)grid, NT, smem, stream>>>(lists, (uint64_t)cap, counts, K, (uint64_t)n, out,
+                                                                  tiles, per, C, 0.0f);
+    return check_launch(update ? "spavg_update" : "spavg");
 }
 
 }  // namespace gcsgd

@@ -198,6 +198,24 @@ int adacomp_compress(const int64_t* seg_offsets, int32_t n_seg, const int32_t* l
 int sparse_average(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int32_t K,
                    int64_t n, float* out, void* stream);
 
+/*
+ * The averaged sparse weight update: the K messages are averaged exactly as
+ * sparse_average does (learner order, one fp32 divide by K) and the weights
+ * step against the average, w[j] <- w[j] - lr * avg_j (one fp32 rounding for
+ * the product and one for the difference), at every index j that at least
+ * one message carries; every other weight keeps its bits.  Learners
+ * exchange compressed gradients and average them to update the weights
+ * ("AdaComp ...", Proposed method; "Deep Gradient Compression", Appendix A:
+ * the summed gradients optimise the model).  Unlike sparse_average, no dense
+ * average is written: only the carried weights are read and rewritten.
+ * lists, cap, counts, K, n: as for sparse_average.
+ * lr      learning rate (finite; the caller folds any 1/K or sum convention in).
+ * w       [n] fp32 weights, updated in place; any alignment.
+ * Errors: as for sparse_average.
+ */
+int sparse_average_update(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int32_t K,
+                          int64_t n, float lr, float* w, void* stream);
+
 /* ------------------------------------------------------------- DCD-PSGD */
 
 /*

@@ -95,6 +95,10 @@ def test_other_entry_points_reject_bad_arguments(L):
     assert rc == -1 and "lt" in msg
     rc, msg = _call(L, "sparse_average", x, 10, x, 0, 100, x, None)
     assert rc == -1
+    rc, msg = _call(L, "sparse_average_update", x, 10, x, 4, 100, ctypes.c_float(float("nan")), x, None)
+    assert rc == -1 and "lr" in msg
+    rc, msg = _call(L, "sparse_average_update", x, 10, x, 513, 100, ctypes.c_float(0.1), x, None)
+    assert rc == -1 and "K" in msg
     w = np.array([1, 1, 1], np.float32)
     rc, msg = _call(L, "dcd_step", 8, 100, w.ctypes.data_as(ctypes.c_void_p), x, x, ctypes.c_float(0.1), 0.0,
                     ctypes.c_uint64(1), ctypes.c_uint32(0), None)

@@ -244,6 +244,78 @@ def test_sparse_average_dense_lists(cuda_lib):
     np.testing.assert_array_equal(got, want)
 
 
+# --------------------------------------------- averaged sparse weight update
+
+def run_update(gc, idx, val, counts, n, lr, seed=0, w_offset=0):
+    """Weights after the fused average-update, CUDA vs oracle, bit for bit
+    (untouched weights included: -0.0 and a NaN payload among them)."""
+    import torch
+    K, cap = idx.shape
+    rng = np.random.default_rng(seed)
+    w0 = rng.standard_normal(max(n, 1)).astype(np.float32)
+    if n > 2:
+        w0[n // 2] = -0.0
+        w0[n - 1] = np.frombuffer(np.uint32(0x7FC00321).tobytes(), np.float32)[0]
+    pairs = torch.zeros((K, cap, 2), dtype=torch.int32)
+    pairs[..., 0] = torch.from_numpy(idx.astype(np.int64)).to(torch.int32)
+    pairs[..., 1] = torch.from_numpy(val.view(np.int32))
+    w_g = shifted(w0, w_offset)
+    gc.sparse_average_update(pairs.cuda(), torch.from_numpy(counts.astype(np.int64)).cuda(), n, lr, w_g)
+    torch.cuda.synchronize()
+    want = oracle.sparse_average_update(idx, val, counts, n, lr, w0.copy())
+    got = w_g.cpu().numpy()[:n]
+    # bit for bit, except that a NaN weight that gets updated is NaN on both
+    # sides with whatever payload the hardware's subtraction returns
+    both_nan = np.isnan(got) & np.isnan(want[:n])
+    carried = np.zeros(n, bool)
+    for k in range(K):
+        carried[idx[k, :counts[k]]] = True
+    np.testing.assert_array_equal(got.view(np.uint32)[~both_nan | ~carried], want[:n].view(np.uint32)[~both_nan | ~carried])
+    np.testing.assert_array_equal(np.isnan(got), np.isnan(want[:n]))
+
+
+@pytest.mark.parametrize("K", [1, 2, 4, 8, 33])
+@pytest.mark.parametrize("n", [1, 4095, 4096, 100003])
+def test_update_random_lists(cuda_lib, K, n):
+    rng = np.random.default_rng(K * 11 + n)
+    cap = max(1, min(n, 3000))
+    idx = np.zeros((K, cap), np.uint32)
+    val = np.zeros((K, cap), np.float32)
+    counts = np.zeros(K, np.int64)
+    for k in range(K):
+        c = int(rng.integers(0, cap + 1))
+        idx[k, :c] = np.sort(rng.choice(n, size=c, replace=False))
+        val[k, :c] = rng.standard_normal(c).astype(np.float32)
+        counts[k] = c
+    run_update(cuda_lib, idx, val, counts, n, 0.05, seed=K + n)
+
+
+@pytest.mark.parametrize("offset", [1, 3])
+def test_update_unaligned_weights_and_dense_lists(cuda_lib, offset):
+    """Every index in every list (the dense, windowed path) and weights off a 16-byte boundary."""
+    rng = np.random.default_rng(offset)
+    K, n = 5, 9000
+    idx = np.tile(np.arange(n, dtype=np.uint32), (K, 1))
+    val = rng.standard_normal((K, n)).astype(np.float32)
+    run_update(cuda_lib, idx, val, np.full(K, n, np.int64), n, -0.01, seed=offset, w_offset=offset)
+
+
+def test_update_of_dgc_messages(cuda_lib):
+    """The K = 4 messages of the small ResNet-50 layout after DGC step 1."""
+    import torch
+    gc = cuda_lib
+    w = wl.workload(2, small=True)
+    G = wl.gradients(w, 0)
+    d = gc.DGC(w.offsets, w.learners, w.density, w.momentum)
+    u = torch.zeros((w.learners, w.n), device="cuda")
+    v = torch.zeros((w.learners, w.n), device="cuda")
+    out, totals = d(G.cuda(), u, v)
+    torch.cuda.synchronize()
+    idx = gc.pair_indices(out).cpu().numpy().astype(np.uint32)
+    val = gc.pair_values(out).cpu().numpy()
+    run_update(gc, idx, val, totals.cpu().numpy(), w.n, 0.1, seed=3, w_offset=2)
+
+
 # ---------------------------------------------------------------------- DCD
 
 def run_dcd(gc, n, d, T, p, w=(1 / 3, 1 / 3, 1 / 3), gamma=0.1, seed=0x5EED):
