@@ -51,6 +51,10 @@ def lib():
             L.oracle_dgc_step.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, ctypes.c_double,
                                           ctypes.c_float, ctypes.c_float, ctypes.c_int, vp, vp,
                                           ctypes.c_int64, vp, vp]
+            L.oracle_dgc_step_sampled.restype = ctypes.c_int
+            L.oracle_dgc_step_sampled.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, ctypes.c_double,
+                                                  ctypes.c_double, ctypes.c_float, ctypes.c_float, ctypes.c_int, vp,
+                                                  vp, ctypes.c_int64, vp, vp]
             L.oracle_adacomp_step.restype = ctypes.c_int
             L.oracle_adacomp_step.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp, vp,
                                               ctypes.c_int64, vp, vp, vp]
@@ -117,6 +121,28 @@ def dgc_step(offsets, grad, u, v, density, momentum, clip_thr=0.0, clip_nodes=1,
     rc = lib().oracle_dgc_step(K, S, _p(off), _p(grad), _p(u), _p(v), float(density), float(momentum),
                                float(clip_thr), int(clip_nodes), _p(idx), _p(val), int(cap), _p(counts), _p(cs))
     _check(rc, "oracle_dgc_step")
+    return idx, val, counts, cs
+
+
+def dgc_step_sampled(offsets, grad, u, v, density, sample_frac, momentum, clip_thr=0.0, clip_nodes=1, cap=None):
+    """The DGC step with the sampled threshold (tensors above 16384 values).
+
+    Same returns as ``dgc_step``; learner k's list has ``counts[k].sum()`` entries."""
+    off = np.ascontiguousarray(offsets, dtype=np.int64)
+    S = len(off) - 1
+    grad = _f32(grad)
+    K = grad.shape[0]
+    assert u.dtype == np.float32 and v.dtype == np.float32 and u.flags["C_CONTIGUOUS"] and v.flags["C_CONTIGUOUS"]
+    if cap is None:
+        cap = max(1, sum(dgc_k(density, int(off[s + 1] - off[s])) for s in range(S)))
+    idx = np.zeros((K, cap), dtype=np.uint32)
+    val = np.zeros((K, cap), dtype=np.float32)
+    counts = np.zeros((K, S), dtype=np.int64)
+    cs = np.zeros(K, dtype=np.float32)
+    rc = lib().oracle_dgc_step_sampled(K, S, _p(off), _p(grad), _p(u), _p(v), float(density), float(sample_frac),
+                                       float(momentum), float(clip_thr), int(clip_nodes), _p(idx), _p(val), int(cap),
+                                       _p(counts), _p(cs))
+    _check(rc, "oracle_dgc_step_sampled")
     return idx, val, counts, cs
 
 

@@ -99,12 +99,39 @@ static int keyed_cmp(const void* a, const void* b) {
  * counts : [K][S] entries sent per tensor.  clip_scale : [K] the c applied
  *     (1 when not clipped), may be NULL.
  */
-int oracle_dgc_step(int K, int S, const int64_t* seg_off,
-                    const float* grad, float* u, float* v,
-                    double density, float momentum, float clip_thr, int clip_nodes,
-                    uint32_t* out_idx, float* out_val, int64_t cap,
-                    int64_t* counts, float* clip_scale) {
+/*
+ * The sampled threshold ("Deep Gradient Compression", section 5, system
+ * analysis: a 0.1 % to 1 % sample of the gradients estimates the population
+ * threshold; section 6: hierarchical threshold selection).  The pages give
+ * the idea, not the procedure; reading, per tensor of n values with k_s to
+ * send, when n > 16384 and k_s <= n / 5 (smaller tensors are selected
+ * exactly, their sample would be most of the tensor):
+ *   - the sample is m = floor(sample_frac * n) rounded down to a multiple of
+ *     64 (at least 64, at most 16384) values of the updated |v|, taken as
+ *     m / 64 blocks of 64 consecutive values starting at b * (n / (m / 64));
+ *   - the threshold tau is the a-th largest sampled |v| (bit pattern order),
+ *     a = round(k_s * m / n) clamped to [1, m];
+ *   - every entry with |v| >= tau is selected; when that is more than k_s
+ *     (the hierarchical second step) the k_s largest of them are kept, which
+ *     is the exact top-k, otherwise all of them are sent (fewer than k_s).
+ * Learner k's list holds its tensors' selections one after another, so its
+ * length is the sum of the per-tensor counts.
+ */
+#define ORACLE_SAMPLED_MIN_N 16384
+#define ORACLE_SAMPLE_BLOCK 64
+#define ORACLE_SAMPLE_MAX 16384
+
+static int dgc_sampled(int64_t n, int64_t ks, double sample_frac) {
+    return sample_frac > 0.0 && n > ORACLE_SAMPLED_MIN_N && 5 * ks <= n;
+}
+
+static int dgc_step_impl(int K, int S, const int64_t* seg_off,
+                         const float* grad, float* u, float* v,
+                         double density, double sample_frac, float momentum, float clip_thr, int clip_nodes,
+                         uint32_t* out_idx, float* out_val, int64_t cap,
+                         int64_t* counts, float* clip_scale) {
     if (K < 1 || S < 1 || !(density > 0.0 && density <= 1.0) || clip_nodes < 1) return ORACLE_EINVAL;
+    if (!(sample_frac >= 0.0 && sample_frac <= 1.0)) return ORACLE_EINVAL;
     const int64_t N = seg_off[S];
     int64_t total = 0;
     for (int s = 0; s < S; ++s) total += oracle_dgc_k(density, seg_off[s + 1] - seg_off[s]);
@@ -153,8 +180,33 @@ int oracle_dgc_step(int K, int S, const int64_t* seg_off,
                 order[i].idx = (uint32_t)i;
                 sent[i] = 0;
             }
+            int64_t take = ks;
+            if (dgc_sampled(n, ks, sample_frac)) {
+                /* the sample and its a-th largest |v| */
+                int64_t m = (int64_t)(sample_frac * (double)n);
+                m -= m % ORACLE_SAMPLE_BLOCK;
+                if (m < ORACLE_SAMPLE_BLOCK) m = ORACLE_SAMPLE_BLOCK;
+                if (m > ORACLE_SAMPLE_MAX) m = ORACLE_SAMPLE_MAX;
+                const int64_t nblk = m / ORACLE_SAMPLE_BLOCK, stride = n / nblk;
+                keyed_t* smp = (keyed_t*)malloc(sizeof(keyed_t) * (size_t)m);
+                if (!smp) { free(order); free(sent); return ORACLE_ENOMEM; }
+                for (int64_t b = 0; b < nblk; ++b)
+                    for (int64_t j = 0; j < ORACLE_SAMPLE_BLOCK; ++j) {
+                        smp[b * ORACLE_SAMPLE_BLOCK + j].key = mag_key(vk[off + b * stride + j]);
+                        smp[b * ORACLE_SAMPLE_BLOCK + j].idx = 0;
+                    }
+                qsort(smp, (size_t)m, sizeof(keyed_t), keyed_cmp);
+                int64_t a = (ks * m + n / 2) / n;
+                if (a < 1) a = 1;
+                if (a > m) a = m;
+                const uint32_t tau = smp[a - 1].key;
+                free(smp);
+                int64_t c = 0;
+                for (int64_t i = 0; i < n; ++i) c += order[i].key >= tau;
+                if (c < ks) take = c;  /* all of |v| >= tau; else the k_s largest of them */
+            }
             if (n > 1) qsort(order, (size_t)n, sizeof(keyed_t), keyed_cmp);
-            for (int64_t j = 0; j < ks; ++j) sent[order[j].idx] = 1;
+            for (int64_t j = 0; j < take; ++j) sent[order[j].idx] = 1;
             for (int64_t i = 0; i < n; ++i) {
                 if (!sent[i]) continue;
                 out_idx[pos] = (uint32_t)(off + i);
@@ -163,12 +215,32 @@ int oracle_dgc_step(int K, int S, const int64_t* seg_off,
                 vk[off + i] = 0.0f;
                 uk[off + i] = 0.0f;
             }
-            counts[(int64_t)k * S + s] = ks;
+            counts[(int64_t)k * S + s] = take;
         }
     }
     free(order);
     free(sent);
     return ORACLE_OK;
+}
+
+int oracle_dgc_step(int K, int S, const int64_t* seg_off,
+                    const float* grad, float* u, float* v,
+                    double density, float momentum, float clip_thr, int clip_nodes,
+                    uint32_t* out_idx, float* out_val, int64_t cap,
+                    int64_t* counts, float* clip_scale) {
+    return dgc_step_impl(K, S, seg_off, grad, u, v, density, 0.0, momentum, clip_thr, clip_nodes, out_idx, out_val,
+                         cap, counts, clip_scale);
+}
+
+/* The DGC step with the sampled threshold (see dgc_sampled above). */
+int oracle_dgc_step_sampled(int K, int S, const int64_t* seg_off,
+                            const float* grad, float* u, float* v,
+                            double density, double sample_frac, float momentum, float clip_thr, int clip_nodes,
+                            uint32_t* out_idx, float* out_val, int64_t cap,
+                            int64_t* counts, float* clip_scale) {
+    if (!(sample_frac > 0.0)) return ORACLE_EINVAL;
+    return dgc_step_impl(K, S, seg_off, grad, u, v, density, sample_frac, momentum, clip_thr, clip_nodes, out_idx,
+                         out_val, cap, counts, clip_scale);
 }
 
 /* --------------------------------------------------------- AdaComp (step) */

@@ -211,3 +211,88 @@ def test_sent_plus_residual_is_accumulation():
     recon = v[0].copy()
     recon[idx[0, :tot]] += val[0, :tot]  # v is exactly 0 there
     np.testing.assert_array_equal(recon, vacc[0])
+
+
+# ------------------------------------------------------- sampled threshold
+
+def test_sampled_hand_example():
+    """n = 20480, density 0.001 (k = 21), a 1 % sample: m = 192 values in 3
+    blocks of 64 at stride 6826 ([0, 64), [6826, 6890), [13652, 13716));
+    a = round(21 * 192 / 20480) = 0 -> 1, so tau is the largest sampled |v|
+    (5.0, planted at 6830).  |v| >= 5.0 holds at 100 (6.0), 200 (7.0), 6830
+    and 20000 (5.0, a tie with tau): 4 < 21 entries, all of them sent."""
+    n = 20480
+    G = np.full((1, n), 1e-3, np.float32)
+    G[0, 6830] = 5.0
+    G[0, 100] = 6.0
+    G[0, 200] = -7.0
+    G[0, 20000] = 5.0
+    G[0, 300] = 4.9
+    u = np.zeros((1, n), np.float32)
+    v = np.zeros((1, n), np.float32)
+    idx, val, counts, _ = oracle.dgc_step_sampled([0, n], G, u, v, 0.001, 0.01, 0.9)
+    assert counts.tolist() == [[4]]
+    assert idx[0, :4].tolist() == [100, 200, 6830, 20000]
+    assert val[0, :4].tolist() == [6.0, -7.0, 5.0, 5.0]
+    assert not v[0, [100, 200, 6830, 20000]].any() and not u[0, [100, 200, 6830, 20000]].any()
+    assert v[0, 300] == np.float32(4.9) and u[0, 300] == np.float32(4.9)
+
+
+@pytest.mark.parametrize("frac", [0.001, 0.003, 0.01])
+def test_sampled_is_a_top_set_and_exact_when_full(frac):
+    """Whatever the sample, the sent set is the top of |v| (everything sent is
+    at least as large as everything kept); when it reaches k it is exactly
+    the exact step's top-k; tensors of at most 16384 values are exact."""
+    rng = np.random.default_rng(int(frac * 1e4))
+    sizes = [16384, 50000, 200000, 33333]
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    K, N = 2, int(off[-1])
+    for step in range(3):
+        G = (rng.standard_normal((K, N)) * rng.choice([1e-4, 1e-2], size=(K, 1))).astype(np.float32)
+        u0 = rng.standard_normal((K, N)).astype(np.float32) * 1e-3
+        v0 = rng.standard_normal((K, N)).astype(np.float32) * 1e-3
+        us, vs = u0.copy(), v0.copy()
+        ue, ve = u0.copy(), v0.copy()
+        idx_s, val_s, cnt_s, _ = oracle.dgc_step_sampled(off, G, us, vs, 0.002, frac, 0.9)
+        idx_e, val_e, cnt_e, _ = oracle.dgc_step(off, G, ue, ve, 0.002, 0.9)
+        vacc = ve.copy()  # the accumulated v before masking: reconstruct from the exact run
+        for k in range(K):
+            vacc[k, idx_e[k, :cnt_e[k].sum()]] = val_e[k, :cnt_e[k].sum()]
+        for k in range(K):
+            ps, pe = 0, 0
+            for s in range(len(sizes)):
+                cs, ce = int(cnt_s[k, s]), int(cnt_e[k, s])
+                assert cs <= ce
+                sent = idx_s[k, ps:ps + cs].astype(np.int64)
+                if s == 0 or cs == ce:
+                    np.testing.assert_array_equal(sent, idx_e[k, pe:pe + ce])
+                mag = np.abs(vacc[k, off[s]:off[s + 1]])
+                mask = np.zeros(sizes[s], bool)
+                mask[sent - off[s]] = True
+                if cs and (~mask).any():
+                    assert mag[mask].min() >= mag[~mask].max()
+                np.testing.assert_array_equal(val_s[k, ps:ps + cs], vacc[k, sent])
+                ps, pe = ps + cs, pe + ce
+        G_sent = vs.copy()
+        assert not any(G_sent[k, idx_s[k, :cnt_s[k].sum()]].any() for k in range(K))
+
+
+def test_sampled_hand_example_rank_above_one():
+    """n = 20480, k = 21, a 50 % sample: m = 10240 values in 160 blocks of 64
+    at stride 128 (positions 128 b .. 128 b + 63); a = round(21 * 10240 /
+    20480) = 11.  Twelve sampled values 100..111 (at 128 b, b = 0..11) put tau
+    at the 11th largest, 101; unsampled 150 (at 64) is above it, unsampled
+    100.5 (at 65) below: 11 + 1 = 12 < 21 entries sent."""
+    n = 20480
+    G = np.full((1, n), 1e-3, np.float32)
+    for b in range(12):
+        G[0, 128 * b] = 100.0 + b
+    G[0, 64] = 150.0
+    G[0, 65] = 100.5
+    u = np.zeros((1, n), np.float32)
+    v = np.zeros((1, n), np.float32)
+    idx, val, counts, _ = oracle.dgc_step_sampled([0, n], G, u, v, 0.001, 0.5, 0.9)
+    want = sorted([128 * b for b in range(1, 12)] + [64])
+    assert counts.tolist() == [[12]]
+    assert idx[0, :12].tolist() == want
+    assert v[0, 65] == np.float32(100.5) and v[0, 0] == np.float32(100.0)

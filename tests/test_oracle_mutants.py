@@ -30,6 +30,11 @@ MUTANTS = {
     "clip_ignores_nodes": ("/ sqrt((double)clip_nodes)", "/ 1.0"),
     "clip_scale_inverted": ("if (norm > thr_k) { c = (float)(thr_k / norm)", "if (norm > thr_k) { c = (float)(norm / thr_k)"),
     "k_floor": ("double kd = ceil(density * (double)n);", "double kd = floor(density * (double)n);"),
+    # DGC with the sampled threshold
+    "sampled_strict_gt": ("c += order[i].key >= tau;", "c += order[i].key > tau;"),
+    "sampled_rank_floor": ("int64_t a = (ks * m + n / 2) / n;", "int64_t a = (ks * m) / n;"),
+    "sampled_stride": ("const int64_t nblk = m / ORACLE_SAMPLE_BLOCK, stride = n / nblk;",
+                       "const int64_t nblk = m / ORACLE_SAMPLE_BLOCK, stride = n / (nblk + 1);"),
     # AdaComp
     "ada_strict_gt": ("(fabsf(h) >= m)", "(fabsf(h) > m)"),
     "ada_h_without_dw": ("const float h = G[off + i] + dWk[off + i];", "const float h = G[off + i];"),
