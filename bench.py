@@ -456,6 +456,36 @@ def run_gpu(args):
                  "value": job_gbs(world, 4.0 * K * N, ms_u), "unit": "GB/s", "ms_per_step": ms_u,
                  "update_ms_per_launch": tu / max(nu, 1)}
 
+    # the sampled threshold (1 % samples, at most 16384 values per tensor):
+    # the same step with the selection threshold taken from the sample
+    sampled = None
+    if w.method == "dgc":
+        d_s = gc.DGC(w.offsets, K, w.density, w.momentum, w.clip_thr, w.clip_nodes, device=dev, sample_frac=0.01)
+        u_s, v_s = torch.zeros((K, N), device=dev), torch.zeros((K, N), device=dev)
+        avg_s = torch.empty(N, device=dev)
+
+        def sampled_step(i):
+            out_s, tot_s = d_s(grads[i % N_SETS], u_s, v_s)
+            gc.sparse_average(out_s, tot_s, N, avg_s)
+
+        for i in range(args.warmup):
+            sampled_step(i)
+        torch.cuda.synchronize()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for i in range(args.steps):
+            sampled_step(i)
+        g1.record(stream)
+        torch.cuda.synchronize()
+        ms_s = max_over_ranks(g0.elapsed_time(g1) / args.steps, dev)
+        k_s = np.array([gc.dgc_k(w.density, n) for n in w.sizes], np.int64)
+        cnt = d_s.counts.cpu().numpy()
+        sampled = {"step": "dgc_compress_sampled (1 % sample per tensor, at most 16384) + sparse_average",
+                   "value": job_gbs(world, 4.0 * K * N, ms_s), "unit": "GB/s", "ms_per_step": ms_s,
+                   "sent_vs_exact_k": float(cnt.sum()) / float(K * k_s.sum()),
+                   "tensors_short_of_k": float((cnt < k_s[None, :]).mean())}
+
     # end to end through the public API: every step copies its gradients in
     # from pinned host memory and its dense result out to pinned host memory.
     # Double-buffered on three streams, so step i+1's upload overlaps step i's
@@ -554,6 +584,7 @@ def run_gpu(args):
         "e2e": None if e2e is None else {"value": e2e, "unit": "GB/s", "ms_per_step": ms_e2e,
                                          "h2d_bytes_per_step": int(grad_bytes), "d2h_bytes_per_step": d2h},
         "fused_update": fused,
+        "sampled_threshold": sampled,
         "gpu_launches": launches,
         "clocks": clk,
         "cpu_baseline": cpu,

@@ -80,6 +80,9 @@ def lib():
         L.gcsgd_dgc_workspace_size.argtypes = [vp, i32, i32, f64, vp]
         L.dgc_compress.argtypes = [vp, i32, i32, vp, vp, vp, f64, f32, f32, i32, vp, i64, vp, vp, vp, sz, vp]
         L.dgc_compress_noalloc.argtypes = [vp, i32, i32, vp, vp, vp, f64, f32, f32, i32, vp, i64, vp, vp, vp]
+        L.gcsgd_dgc_sampled_workspace_size.argtypes = [vp, i32, i32, f64, f64, vp]
+        L.dgc_compress_sampled.argtypes = [vp, i32, i32, vp, vp, vp, f64, f64, f32, f32, i32, vp, i64, vp, vp, vp,
+                                           sz, vp]
         L.gcsgd_dgc_stats.argtypes = [vp, i32, i32, f64, vp, vp, vp]
         L.gcsgd_adacomp_workspace_size.argtypes = [vp, i32, vp, i32, i64, vp]
         L.adacomp_compress.argtypes = [vp, i32, vp, i32, vp, vp, vp, i64, vp, vp, vp, vp, sz, vp]
@@ -186,6 +189,30 @@ def dgc_compress(offsets, grad, u, v, out, counts, workspace, density, momentum,
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
+def dgc_sampled_workspace_size(offsets, K: int, density: float, sample_frac: float) -> int:
+    off = _offsets(offsets)
+    out = ctypes.c_size_t(0)
+    _check("gcsgd_dgc_sampled_workspace_size",
+           lib().gcsgd_dgc_sampled_workspace_size(_ptr(off), len(off) - 1, int(K), float(density), float(sample_frac),
+                                                  ctypes.byref(out)))
+    return int(out.value)
+
+
+def dgc_compress_sampled(offsets, grad, u, v, out, counts, workspace, density, sample_frac, momentum, clip_thr=0.0,
+                         clip_nodes=1, totals=None, stream=None):
+    """The DGC step with the sampled threshold (see dgc_compress_sampled in include/gcsgd.h)."""
+    import torch
+    off = _offsets(offsets)
+    K = grad.shape[0]
+    cap = out.shape[1]
+    _check("dgc_compress_sampled", lib().dgc_compress_sampled(
+        _ptr(off), len(off) - 1, int(K), _dev(grad, "grad", torch.float32), _dev(u, "u", torch.float32),
+        _dev(v, "v", torch.float32), float(density), float(sample_frac), float(momentum), float(clip_thr),
+        int(clip_nodes), _dev(out, "out", torch.int32), int(cap), _dev(counts, "counts", torch.int64),
+        _dev(totals, "totals", torch.int64), _dev(workspace, "workspace", torch.uint8), int(workspace.numel()),
+        _stream(stream)))
+
+
 def dgc_compress_noalloc(offsets, grad, u, v, out, counts, density, momentum, clip_thr=0.0, clip_nodes=1,
                          totals=None, stream=None):
     """dgc_compress with the library's fixed scratch instead of a workspace, for
@@ -207,14 +234,17 @@ class DGC:
     """Buffers of DGC on one layout: workspace, [K, cap] messages and counters."""
 
     def __init__(self, offsets, K: int, density: float, momentum: float, clip_thr: float = 0.0,
-                 clip_nodes: int = 1, device="cuda"):
+                 clip_nodes: int = 1, device="cuda", sample_frac: float = 0.0):
         import torch
         self.offsets = _offsets(offsets)
         self.S = len(self.offsets) - 1
         self.K, self.density, self.momentum = int(K), float(density), float(momentum)
         self.clip_thr, self.clip_nodes = float(clip_thr), int(clip_nodes)
+        self.sample_frac = float(sample_frac)  # > 0: the sampled threshold (dgc_compress_sampled)
         self.cap = sum(dgc_k(density, int(self.offsets[s + 1] - self.offsets[s])) for s in range(self.S))
-        self.workspace = torch.empty(dgc_workspace_size(self.offsets, K, density), dtype=torch.uint8, device=device)
+        ws = (dgc_sampled_workspace_size(self.offsets, K, density, self.sample_frac) if self.sample_frac > 0
+              else dgc_workspace_size(self.offsets, K, density))
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=device)
         self.out = pairs_buffer(K, self.cap, device)
         self.counts = torch.zeros((K, self.S), dtype=torch.int64, device=device)
         self.totals = torch.zeros(K, dtype=torch.int64, device=device)
@@ -228,8 +258,13 @@ class DGC:
         return {name: int(getattr(st, name)) for name, _ in DgcStats._fields_}
 
     def __call__(self, grad, u, v, stream=None):
-        dgc_compress(self.offsets, grad, u, v, self.out, self.counts, self.workspace, self.density,
-                     self.momentum, self.clip_thr, self.clip_nodes, totals=self.totals, stream=stream)
+        if self.sample_frac > 0:
+            dgc_compress_sampled(self.offsets, grad, u, v, self.out, self.counts, self.workspace, self.density,
+                                 self.sample_frac, self.momentum, self.clip_thr, self.clip_nodes, totals=self.totals,
+                                 stream=stream)
+        else:
+            dgc_compress(self.offsets, grad, u, v, self.out, self.counts, self.workspace, self.density,
+                         self.momentum, self.clip_thr, self.clip_nodes, totals=self.totals, stream=stream)
         return self.out, self.totals
 
 

@@ -118,10 +118,10 @@ static int check_ws(const char* fn, const void* ws, size_t bytes, size_t need) {
     return GCSGD_OK;
 }
 
-static size_t dgc_ws_bytes(const int64_t* off, int32_t S, int32_t K, double density) {
+static size_t dgc_ws_bytes(const int64_t* off, int32_t S, int32_t K, double density, double sample_frac) {
     dgc::HostPlan hp;
-    dgc::host_plan(off, S, density, &hp);
-    return dgc_workspace_layout(S, K, hp, nullptr, nullptr);
+    dgc::host_plan(off, S, density, sample_frac, &hp);
+    return dgc_workspace_layout(S, K, hp, sample_frac > 0.0, nullptr, nullptr);
 }
 
 }  // namespace gcsgd
@@ -184,14 +184,28 @@ int gcsgd_dgc_workspace_size(const int64_t* seg_offsets, int32_t n_seg, int32_t 
     if (K < 1 || !bytes) return set_error(GCSGD_ERR_INVALID_ARG, "gcsgd_dgc_workspace_size: K < 1 or bytes NULL");
     if (!(density > 0.0 && density <= 1.0))
         return set_error(GCSGD_ERR_INVALID_ARG, "gcsgd_dgc_workspace_size: density %g outside (0, 1]", density);
-    *bytes = dgc_ws_bytes(seg_offsets, n_seg, K, density);
+    *bytes = dgc_ws_bytes(seg_offsets, n_seg, K, density, 0.0);
     return GCSGD_OK;
 }
 
-int dgc_compress(const int64_t* seg_offsets, int32_t n_seg, int32_t K, const float* grad, float* u, float* v,
-                 double density, float momentum, float clip_thr, int32_t clip_nodes, gcsgd_pair* out, int64_t cap,
-                 int64_t* counts, int64_t* totals, void* workspace, size_t workspace_bytes, void* stream) {
-    const char* fn = "dgc_compress";
+int gcsgd_dgc_sampled_workspace_size(const int64_t* seg_offsets, int32_t n_seg, int32_t K, double density,
+                                     double sample_frac, size_t* bytes) {
+    const char* fn = "gcsgd_dgc_sampled_workspace_size";
+    int rc;
+    if ((rc = check_layout(fn, seg_offsets, n_seg))) return rc;
+    if (K < 1 || !bytes) return set_error(GCSGD_ERR_INVALID_ARG, "%s: K < 1 or bytes NULL", fn);
+    if (!(density > 0.0 && density <= 1.0))
+        return set_error(GCSGD_ERR_INVALID_ARG, "%s: density %g outside (0, 1]", fn, density);
+    if (!(sample_frac > 0.0 && sample_frac <= 1.0))
+        return set_error(GCSGD_ERR_INVALID_ARG, "%s: sample_frac %g outside (0, 1]", fn, sample_frac);
+    *bytes = dgc_ws_bytes(seg_offsets, n_seg, K, density, sample_frac);
+    return GCSGD_OK;
+}
+
+static int dgc_common(const char* fn, const int64_t* seg_offsets, int32_t n_seg, int32_t K, const float* grad,
+                      float* u, float* v, double density, double sample_frac, float momentum, float clip_thr,
+                      int32_t clip_nodes, gcsgd_pair* out, int64_t cap, int64_t* counts, int64_t* totals,
+                      void* workspace, size_t workspace_bytes, void* stream) {
     int rc;
     if ((rc = check_layout(fn, seg_offsets, n_seg))) return rc;
     if (K < 1) return set_error(GCSGD_ERR_INVALID_ARG, "%s: K = %d < 1", fn, K);
@@ -205,9 +219,27 @@ int dgc_compress(const int64_t* seg_offsets, int32_t n_seg, int32_t K, const flo
         return set_error(GCSGD_ERR_INVALID_ARG, "%s: grad, u and v must be non-NULL", fn);
     if (!counts) return set_error(GCSGD_ERR_INVALID_ARG, "%s: counts is NULL", fn);
     if (cap > 0 && !out) return set_error(GCSGD_ERR_INVALID_ARG, "%s: out is NULL", fn);
-    if ((rc = check_ws(fn, workspace, workspace_bytes, dgc_ws_bytes(seg_offsets, n_seg, K, density)))) return rc;
-    return dgc_launch(seg_offsets, n_seg, K, grad, u, v, density, momentum, clip_thr, clip_nodes, out, cap, counts,
-                      totals, workspace, workspace_bytes, (cudaStream_t)stream);
+    if ((rc = check_ws(fn, workspace, workspace_bytes, dgc_ws_bytes(seg_offsets, n_seg, K, density, sample_frac))))
+        return rc;
+    return dgc_launch(seg_offsets, n_seg, K, grad, u, v, density, sample_frac, momentum, clip_thr, clip_nodes, out,
+                      cap, counts, totals, workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+int dgc_compress(const int64_t* seg_offsets, int32_t n_seg, int32_t K, const float* grad, float* u, float* v,
+                 double density, float momentum, float clip_thr, int32_t clip_nodes, gcsgd_pair* out, int64_t cap,
+                 int64_t* counts, int64_t* totals, void* workspace, size_t workspace_bytes, void* stream) {
+    return dgc_common("dgc_compress", seg_offsets, n_seg, K, grad, u, v, density, 0.0, momentum, clip_thr, clip_nodes,
+                      out, cap, counts, totals, workspace, workspace_bytes, stream);
+}
+
+int dgc_compress_sampled(const int64_t* seg_offsets, int32_t n_seg, int32_t K, const float* grad, float* u, float* v,
+                         double density, double sample_frac, float momentum, float clip_thr, int32_t clip_nodes,
+                         gcsgd_pair* out, int64_t cap, int64_t* counts, int64_t* totals, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+    if (!(sample_frac > 0.0 && sample_frac <= 1.0))
+        return set_error(GCSGD_ERR_INVALID_ARG, "dgc_compress_sampled: sample_frac %g outside (0, 1]", sample_frac);
+    return dgc_common("dgc_compress_sampled", seg_offsets, n_seg, K, grad, u, v, density, sample_frac, momentum,
+                      clip_thr, clip_nodes, out, cap, counts, totals, workspace, workspace_bytes, stream);
 }
 
 int gcsgd_dgc_stats(const int64_t* seg_offsets, int32_t n_seg, int32_t K, double density, const void* workspace,

@@ -53,17 +53,36 @@ constexpr size_t kStageBytes = kStageItems * sizeof(uint2);  // also holds kRawM
 static_assert(kStageBytes >= kRawMax * sizeof(float), "the stage must hold a raw segment");
 constexpr int kSumsqBlocks = 128;        // CTAs per learner in dgc_sumsq
 
-__host__ __device__ __forceinline__ void seg_fields(uint32_t n, double density, SegPlan* p) {
+// Plan of one segment.  sample_frac = 0: the exact step (the hint only
+// steers the candidate pool).  sample_frac > 0: the sampled threshold (the
+// system-analysis reading: m = floor(sample_frac n) rounded down to 64-value
+// blocks, at most kSampleMax, and the hint is the round(k m / n)-th largest
+// sampled |v|, which is then the selection threshold itself).
+__host__ __device__ __forceinline__ void seg_fields(uint32_t n, double density, double sample_frac, SegPlan* p) {
     p->n = n;
     p->k = dgc_k_of(density, n);
     p->ntiles = (n + kTile - 1) / kTile;
     p->cap = 0;
     p->m = 0;
     p->a = 0;
+    p->sampled = 0;
     if (n == 0) {
         p->kind = kKindEmpty;
-    } else if (n <= kRawMax || 5ull * p->k / 2 > n / 2) {
+    } else if (n <= kRawMax || 5ull * p->k > n) {
         p->kind = kKindRaw;
+    } else if (sample_frac > 0.0) {
+        p->kind = kKindPool;
+        p->sampled = 1;
+        const uint64_t R = p->k > kPoolFloor ? p->k : kPoolFloor;  // expected candidates ~ k
+        const uint64_t cap = 4 * R + 256;
+        p->cap = (uint32_t)(cap < n ? cap : n);
+        uint64_t m = (uint64_t)(sample_frac * (double)n);
+        m -= m % kSampleBlock;
+        if (m < kSampleBlock) m = kSampleBlock;
+        if (m > kSampleMax) m = kSampleMax;
+        p->m = (uint32_t)m;
+        uint64_t a = ((uint64_t)p->k * m + n / 2) / n;
+        p->a = (uint32_t)(a < 1 ? 1 : (a > m ? m : a));
     } else {
         p->kind = kKindPool;
         const uint64_t R = 5ull * p->k / 2 > kPoolFloor ? 5ull * p->k / 2 : kPoolFloor;  // expected candidates
@@ -79,15 +98,15 @@ __host__ __device__ __forceinline__ void seg_fields(uint32_t n, double density, 
     }
 }
 
-// Host mirror of dgc_plan's totals (workspace sizing and argument checks).
-int host_plan(const int64_t* off, int S, double density, HostPlan* hp) {
+// Host mirror of the plan's totals (workspace sizing and argument checks).
+int host_plan(const int64_t* off, int S, double density, double sample_frac, HostPlan* hp) {
     hp->tiles_per_learner = 0;
     hp->pool_per_learner = 0;
     hp->out_per_learner = 0;
     hp->pool_segments = 0;
     for (int s = 0; s < S; ++s) {
         SegPlan p;
-        seg_fields((uint32_t)(off[s + 1] - off[s]), density, &p);
+        seg_fields((uint32_t)(off[s + 1] - off[s]), density, sample_frac, &p);
         hp->tiles_per_learner += p.ntiles;
         hp->pool_per_learner += p.cap;
         hp->out_per_learner += p.k;
@@ -164,7 +183,7 @@ __device__ __forceinline__ void dgc_elem(float g, float& u, float& v, float m, f
 // the pool holds the top k.
 template <int MAXS>
 __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, PoolList<MAXS> pl, int S, int K,
-                                                     double density,
+                                                     double density, double sample_frac,
                                                      float clip_thr, int clip_nodes, const double* __restrict__ part,
                                                      SegPlan* __restrict__ plan, float* __restrict__ clip_c,
                                                      uint16_t* __restrict__ order, uint64_t N,
@@ -182,7 +201,7 @@ __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, PoolL
             const int s = base + (int)threadIdx.x;
             SegPlan p;
             const bool live = s < S;
-            seg_fields(live ? so.off[s + 1] - so.off[s] : 0u, density, &p);
+            seg_fields(live ? so.off[s + 1] - so.off[s] : 0u, density, sample_frac, &p);
             p.off = live ? so.off[s] : 0u;
             uint64_t tot;
             const uint64_t ex_pool = block_exclusive_scan<NTP>(live ? p.cap : 0, rs.scan, &tot);
@@ -201,7 +220,6 @@ __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, PoolL
                 p.pool_off = (uint32_t)(c0 + ex_pool);
                 p.tile_off = (uint32_t)(c1 + ex_tile);
                 p.out_off = (uint32_t)(c2 + ex_out);
-                p.pad = 0;
                 plan[s] = p;
                 // rank by size, largest first (ties: lower index first)
                 const uint32_t ns = so.off[s + 1] - so.off[s];
@@ -277,12 +295,19 @@ __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, PoolL
             }
         }
         __syncthreads();
-        // two digits suffice: the hint only needs to sit at or below the
-        // a-th largest sampled key
-        const SelectResult sr = radix_select_desc<NTP, 2>(
-            [&](uint64_t i, uint32_t* key) { *key = keys[i]; return true; }, p.m, p.a, rs, true);
-        const uint32_t h = sr.thresh;
-        if (threadIdx.x == 0) hint[unit] = h > 1u ? h : 1u;
+        if (sample_frac > 0.0) {
+            // the sampled threshold: the a-th largest sampled key, exactly
+            const SelectResult sr = radix_select_desc<NTP, 3>(
+                [&](uint64_t i, uint32_t* key) { *key = keys[i]; return true; }, p.m, p.a, rs, true);
+            if (threadIdx.x == 0) hint[unit] = sr.thresh;
+        } else {
+            // two digits suffice: the hint only needs to sit at or below the
+            // a-th largest sampled key
+            const SelectResult sr = radix_select_desc<NTP, 2>(
+                [&](uint64_t i, uint32_t* key) { *key = keys[i]; return true; }, p.m, p.a, rs, true);
+            const uint32_t h = sr.thresh;
+            if (threadIdx.x == 0) hint[unit] = h > 1u ? h : 1u;
+        }
         __syncthreads();
     }
 }
@@ -588,7 +613,7 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
                                                   uint64_t pool_per_learner, gcsgd_pair* __restrict__ out,
                                                   uint64_t cap, int64_t* __restrict__ counts,
                                                   int64_t* __restrict__ totals, uint32_t out_per_learner,
-                                                  const uint16_t* __restrict__ order, int K) {
+                                                  const uint16_t* __restrict__ order, int K, int sampled) {
     extern __shared__ __align__(16) unsigned char stage_raw[];  // kStageBytes
     uint2* stage = reinterpret_cast<uint2*>(stage_raw);
     float* stagef = reinterpret_cast<float*>(stage_raw);
@@ -601,14 +626,16 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
     const int s = order[(int)blockIdx.x / K];
     const int unit = k * S + s;
     const SegPlan p = plan[s];
+    const uint32_t pc = p.kind == kKindPool ? pool_cnt[unit] : 0;
+    // sampled threshold, fewer than k above it: every candidate is sent
+    const bool take_all = p.kind == kKindPool && p.sampled && pc < p.k;
     if (threadIdx.x == 0) {
-        counts[unit] = p.k;
-        if (s == 0 && totals) totals[k] = out_per_learner;
+        counts[unit] = take_all ? pc : p.k;
+        if (s == 0 && totals && !sampled) totals[k] = out_per_learner;
     }
     if (p.k == 0) return;
     const uint64_t ebase = (uint64_t)k * N + p.off;
-    const uint32_t pc = p.kind == kKindPool ? pool_cnt[unit] : 0;
-    const bool pool_ok = p.kind == kKindPool && pc >= p.k && pc <= p.cap;
+    const bool pool_ok = p.kind == kKindPool && (pc >= p.k || take_all) && pc <= p.cap;
     const uint2* items = pool + (uint64_t)k * pool_per_learner + p.pool_off;
     const uint2* tt = tile_tab + (uint64_t)k * tiles_per_learner + p.tile_off;
     const float* vseg = v + ebase;
@@ -665,15 +692,20 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
             run += total;
             __syncthreads();
         }
-        const SelectResult r = radix_select_desc<NTS, 3>(
-            [&](uint64_t i, uint32_t* key) { *key = stage[i].y & 0x7fffffffu; return true; }, pc, p.k, rs, true);
+        uint32_t T = 0, ties = pc;  // take_all: every key >= 0 goes, in index order
+        if (!take_all) {
+            const SelectResult r = radix_select_desc<NTS, 3>(
+                [&](uint64_t i, uint32_t* key) { *key = stage[i].y & 0x7fffffffu; return true; }, pc, p.k, rs, true);
+            T = r.thresh;
+            ties = r.ties;
+        }
         emit_in_order(
             [&](uint32_t i, uint32_t* loc, uint32_t* bits) {
                 const uint2 it = stage[i];
                 *loc = it.x;
                 *bits = it.y;
             },
-            pc, r.thresh, r.ties, p, dst, u, v, ebase, wsum);
+            pc, T, ties, p, dst, u, v, ebase, wsum);
         return;
     }
     if (!pool_ok && p.n <= kSmallN && p.k <= kSmallK) {
@@ -742,10 +774,14 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
         return;
     }
     // a valid pool too large to stage: select from global memory, emit through the tile table
-    const SelectResult r = radix_select_desc<NTS, 3>(
-        [&](uint64_t i, uint32_t* key) { *key = __ldg(&items[i].y) & 0x7fffffffu; return true; }, pc, p.k, rs,
-        false);
-    const uint32_t T = r.thresh, ties = r.ties;
+    uint32_t T = 0, ties = pc;  // take_all: every candidate goes
+    if (!take_all) {
+        const SelectResult r = radix_select_desc<NTS, 3>(
+            [&](uint64_t i, uint32_t* key) { *key = __ldg(&items[i].y) & 0x7fffffffu; return true; }, pc, p.k, rs,
+            false);
+        T = r.thresh;
+        ties = r.ties;
+    }
     uint32_t run_gt = 0, run_eq = 0;
     for (uint32_t tb = 0; tb < p.ntiles; tb += NTS) {
         const uint32_t j = tb + threadIdx.x;
@@ -789,6 +825,44 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
     }
 }
 
+// Sampled threshold: the selection wrote tensor s's entries at its k_s-slot
+// region of the scratch list; each learner's list is packed to be contiguous
+// (tensors in order, a warp per tensor) and its total written.
+__global__ void __launch_bounds__(NTS) dgc_pack(const SegPlan* __restrict__ plan, int S,
+                                               const int64_t* __restrict__ counts, const gcsgd_pair* __restrict__ msg,
+                                               uint32_t out_per_learner, gcsgd_pair* __restrict__ out, uint64_t cap,
+                                               int64_t* __restrict__ totals) {
+    constexpr int NW = NTS / 32;
+    __shared__ uint64_t scan[NW + 1];
+    __shared__ uint64_t pre[NTS];
+    __shared__ uint32_t cnt[NTS];
+    __shared__ uint64_t s_carry;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int k = blockIdx.x;
+    const gcsgd_pair* src = msg + (uint64_t)k * out_per_learner;
+    gcsgd_pair* dst = out + (uint64_t)k * cap;
+    if (threadIdx.x == 0) s_carry = 0;
+    __syncthreads();
+    for (int base = 0; base < S; base += NTS) {
+        const int s = base + (int)threadIdx.x;
+        const uint32_t c = s < S ? (uint32_t)counts[(int64_t)k * S + s] : 0u;
+        uint64_t tot;
+        const uint64_t ex = block_exclusive_scan<NTS>(c, scan, &tot);
+        pre[threadIdx.x] = s_carry + ex;
+        cnt[threadIdx.x] = c;
+        __syncthreads();
+        for (int q = warp; q < NTS && base + q < S; q += NW) {
+            const uint64_t at = pre[q];
+            const uint32_t from = __ldg(&plan[base + q].out_off);
+            for (uint32_t i = lane; i < cnt[q]; i += 32) dst[at + i] = src[from + i];
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) s_carry += tot;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0 && totals) totals[k] = (int64_t)s_carry;
+}
+
 }  // namespace dgc
 
 // ------------------------------------------------------------- host launch
@@ -813,14 +887,15 @@ static int dgc_set_smem_limits() {
 }
 
 int dgc_launch(const int64_t* off, int S, int K, const float* grad, float* u, float* v, double density,
-               float momentum, float clip_thr, int clip_nodes, gcsgd_pair* out, int64_t cap, int64_t* counts,
-               int64_t* totals, void* ws, size_t ws_bytes, cudaStream_t stream) {
+               double sample_frac, float momentum, float clip_thr, int clip_nodes, gcsgd_pair* out, int64_t cap,
+               int64_t* counts, int64_t* totals, void* ws, size_t ws_bytes, cudaStream_t stream) {
     using namespace dgc;
     HostPlan hp;
-    host_plan(off, S, density, &hp);
+    host_plan(off, S, density, sample_frac, &hp);
     const uint64_t N = (uint64_t)off[S];
+    const bool sampled = sample_frac > 0.0;
     DgcWorkspace w;
-    const size_t need = dgc_workspace_layout(S, K, hp, ws, &w);
+    const size_t need = dgc_workspace_layout(S, K, hp, sampled, ws, &w);
     if (ws_bytes < need)
         return set_error(GCSGD_ERR_WORKSPACE, "dgc_compress: workspace of %zu bytes, %zu needed", ws_bytes, need);
     if ((uint64_t)cap < hp.out_per_learner)
@@ -843,7 +918,7 @@ int dgc_launch(const int64_t* off, int S, int K, const float* grad, float* u, fl
             for (int s = 0; s <= S; ++s) so.off[s] = (uint32_t)off[s];
             for (int s = 0; s < S; ++s) {
                 SegPlan sp;
-                seg_fields((uint32_t)(off[s + 1] - off[s]), density, &sp);
+                seg_fields((uint32_t)(off[s + 1] - off[s]), density, sample_frac, &sp);
                 if (sp.kind != kKindPool) continue;
                 pl.seg[pl.n_pool] = (uint16_t)s;
                 pl.m[pl.n_pool] = sp.m;
@@ -858,7 +933,7 @@ int dgc_launch(const int64_t* off, int S, int K, const float* grad, float* u, fl
             SegOffsets<256> so;
             PoolList<256> pl;
             fill(so, pl);
-            dgc_prepare<256><<<prep_grid, NTP, smem, stream>>>(so, pl, S, K, density, clip_thr, clip_nodes,
+            dgc_prepare<256><<<prep_grid, NTP, smem, stream>>>(so, pl, S, K, density, sample_frac, clip_thr, clip_nodes,
                                                                w.clip_part, w.plan, w.clip_c, w.order, N, grad, u, v,
                                                                momentum, w.hint, w.pool_cnt);
         } else {
@@ -866,7 +941,8 @@ int dgc_launch(const int64_t* off, int S, int K, const float* grad, float* u, fl
             PoolList<GCSGD_MAX_SEGMENTS> pl;
             fill(so, pl);
             dgc_prepare<GCSGD_MAX_SEGMENTS><<<prep_grid, NTP, smem, stream>>>(
-                so, pl, S, K, density, clip_thr, clip_nodes, w.clip_part, w.plan, w.clip_c, w.order, N, grad, u, v,
+                so, pl, S, K, density, sample_frac, clip_thr, clip_nodes, w.clip_part, w.plan, w.clip_c, w.order, N,
+                grad, u, v,
                 momentum, w.hint, w.pool_cnt);
         }
         if ((rc = check_launch("dgc_prepare"))) return rc;
@@ -886,10 +962,19 @@ int dgc_launch(const int64_t* off, int S, int K, const float* grad, float* u, fl
     }
     {
         LaunchScope ls("dgc_select", stream);
+        // the sampled threshold writes each tensor's entries into its k_s-slot region of the scratch list
+        gcsgd_pair* dst = sampled ? w.msg : out;
+        const uint64_t dst_stride = sampled ? hp.out_per_learner : (uint64_t)cap;
         dgc_select<<<units, NTS, kStageBytes, stream>>>(w.plan, S, N, (uint32_t)hp.tiles_per_learner, u, v, w.pool_cnt,
-                                             w.tile_tab, w.pool, hp.pool_per_learner, out, (uint64_t)cap, counts,
-                                             totals, (uint32_t)hp.out_per_learner, w.order, K);
+                                             w.tile_tab, w.pool, hp.pool_per_learner, dst, dst_stride, counts,
+                                             totals, (uint32_t)hp.out_per_learner, w.order, K, sampled ? 1 : 0);
         if ((rc = check_launch("dgc_select"))) return rc;
+    }
+    if (sampled) {
+        LaunchScope ls("dgc_pack", stream);
+        dgc_pack<<<(unsigned)K, NTS, 0, stream>>>(w.plan, S, counts, w.msg, (uint32_t)hp.out_per_learner, out,
+                                                 (uint64_t)cap, totals);
+        if ((rc = check_launch("dgc_pack"))) return rc;
     }
     return GCSGD_OK;
 }
@@ -900,9 +985,9 @@ int dgc_collect_stats(const int64_t* off, int S, int K, double density, const vo
                       gcsgd_dgc_stats_t* st) {
     using namespace dgc;
     HostPlan hp;
-    host_plan(off, S, density, &hp);
+    host_plan(off, S, density, 0.0, &hp);
     DgcWorkspace w;
-    dgc_workspace_layout(S, K, hp, const_cast<void*>(ws), &w);
+    dgc_workspace_layout(S, K, hp, false, const_cast<void*>(ws), &w);
     std::vector<uint32_t> cnt((size_t)K * S);
     cudaError_t e = cudaMemcpyAsync(cnt.data(), w.pool_cnt, sizeof(uint32_t) * cnt.size(), cudaMemcpyDeviceToHost,
                                     stream);
@@ -913,7 +998,7 @@ int dgc_collect_stats(const int64_t* off, int S, int K, double density, const vo
     for (int k = 0; k < K; ++k)
         for (int s = 0; s < S; ++s) {
             SegPlan p;
-            seg_fields((uint32_t)(off[s + 1] - off[s]), density, &p);
+            seg_fields((uint32_t)(off[s + 1] - off[s]), density, 0.0, &p);
             const uint32_t c = cnt[(size_t)k * S + s];
             if (p.kind == kKindEmpty) ++st->empty;
             else if (p.kind == kKindRaw) (p.n <= kRawMax ? st->raw : st->raw_global)++;
@@ -923,7 +1008,8 @@ int dgc_collect_stats(const int64_t* off, int S, int K, double density, const vo
     return GCSGD_OK;
 }
 
-size_t dgc_workspace_layout(int S, int K, const dgc::HostPlan& hp, void* base, dgc::DgcWorkspace* w) {
+size_t dgc_workspace_layout(int S, int K, const dgc::HostPlan& hp, bool sampled, void* base,
+                            dgc::DgcWorkspace* w) {
     using namespace dgc;
     size_t o = 0;
     auto take = [&](size_t bytes) {
@@ -939,6 +1025,7 @@ size_t dgc_workspace_layout(int S, int K, const dgc::HostPlan& hp, void* base, d
     const size_t o_cnt = take(sizeof(uint32_t) * (size_t)K * S);
     const size_t o_tt = take(sizeof(uint2) * (size_t)K * hp.tiles_per_learner);
     const size_t o_pool = take(sizeof(uint2) * (size_t)K * hp.pool_per_learner);
+    const size_t o_msg = take(sampled ? sizeof(gcsgd_pair) * (size_t)K * hp.out_per_learner : 0);
     if (w) {
         char* b = (char*)base;
         w->plan = (SegPlan*)(b + o_plan);
@@ -949,6 +1036,7 @@ size_t dgc_workspace_layout(int S, int K, const dgc::HostPlan& hp, void* base, d
         w->pool_cnt = (uint32_t*)(b + o_cnt);
         w->tile_tab = (uint2*)(b + o_tt);
         w->pool = (uint2*)(b + o_pool);
+        w->msg = sampled ? (gcsgd_pair*)(b + o_msg) : nullptr;
     }
     return o;
 }

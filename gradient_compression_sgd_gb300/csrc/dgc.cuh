@@ -24,7 +24,7 @@ struct SegPlan {
     uint32_t tile_off;  // first tile within a learner's tiles
     uint32_t ntiles;    // tiles of 4096 elements
     uint32_t out_off;   // first message slot within a learner's list
-    uint32_t pad;
+    uint32_t sampled;   // 1: sampled threshold (the hint is the selection threshold)
 };
 
 // Segment offsets passed by value to dgc_plan (no host-to-device copy).
@@ -59,19 +59,20 @@ struct DgcWorkspace {
     uint32_t* pool_cnt;
     uint2* tile_tab;
     uint2* pool;
+    gcsgd_pair* msg;  // sampled threshold: per-tensor regions before packing
 };
 
-int host_plan(const int64_t* off, int S, double density, HostPlan* hp);
+int host_plan(const int64_t* off, int S, double density, double sample_frac, HostPlan* hp);
 
 }  // namespace dgc
 
-size_t dgc_workspace_layout(int S, int K, const dgc::HostPlan& hp, void* base, dgc::DgcWorkspace* w);
+size_t dgc_workspace_layout(int S, int K, const dgc::HostPlan& hp, bool sampled, void* base, dgc::DgcWorkspace* w);
 
 int dgc_collect_stats(const int64_t* off, int S, int K, double density, const void* ws, cudaStream_t stream,
                       gcsgd_dgc_stats_t* st);
 
 int dgc_launch(const int64_t* off, int S, int K, const float* grad, float* u, float* v, double density,
-               float momentum, float clip_thr, int clip_nodes, gcsgd_pair* out, int64_t cap, int64_t* counts,
-               int64_t* totals, void* ws, size_t ws_bytes, cudaStream_t stream);
+               double sample_frac, float momentum, float clip_thr, int clip_nodes, gcsgd_pair* out, int64_t cap,
+               int64_t* counts, int64_t* totals, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 }  // namespace gcsgd

@@ -102,6 +102,36 @@ int dgc_compress(const int64_t* seg_offsets, int32_t n_seg, int32_t K,
                  gcsgd_pair* out, int64_t cap, int64_t* counts, int64_t* totals,
                  void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * The DGC step with the sampled threshold ("Deep Gradient Compression",
+ * section 5: a 0.1 % to 1 % sample of the gradients estimates the population
+ * threshold; section 6: hierarchical threshold selection).  Steps 1, 2 and 4
+ * as dgc_compress; step 3, for every tensor of n > 16384 values with
+ * 5 k_s <= n (smaller ones are selected exactly):
+ *   m   = floor(sample_frac * n) rounded down to a multiple of 64, clamped to
+ *         [64, 16384]; the sample is m / 64 blocks of 64 consecutive updated
+ *         |v| starting at b * floor(n / (m / 64));
+ *   tau = the a-th largest sampled |v| (bit-pattern order),
+ *         a = round(k_s * m / n) clamped to [1, m];
+ *   every entry with |v| >= tau is selected; past k_s the k_s largest of
+ *   them are kept (ties to the lower index: the exact top-k), otherwise all
+ *   of them are sent, fewer than k_s.
+ * counts[k][s] is the number sent for tensor s (at most k_s) and learner k's
+ * list in out holds the tensors' entries back to back, totals[k] of them.
+ * sample_frac in (0, 1]; the workspace comes from
+ * gcsgd_dgc_sampled_workspace_size.  Other arguments and errors: as
+ * dgc_compress.
+ */
+int dgc_compress_sampled(const int64_t* seg_offsets, int32_t n_seg, int32_t K,
+                         const float* grad, float* u, float* v,
+                         double density, double sample_frac, float momentum, float clip_thr, int32_t clip_nodes,
+                         gcsgd_pair* out, int64_t cap, int64_t* counts, int64_t* totals,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes of dgc_compress_sampled for this layout, K and sample_frac.  Host. */
+int gcsgd_dgc_sampled_workspace_size(const int64_t* seg_offsets, int32_t n_seg, int32_t K, double density,
+                                     double sample_frac, size_t* bytes);
+
 /* Diagnostics of the last dgc_compress call made with `workspace`: how each
  * (learner, segment) found its top k.  The answer is exact on every path;
  * only the speed differs.  Host function; it copies a few counters from

@@ -217,3 +217,65 @@ def test_async_on_side_stream(cuda_lib):
         out, totals = d(g, u, v, stream=s)
     s.synchronize()
     assert int(totals[0]) == sum(gc.dgc_k(0.01, int(off[i + 1] - off[i])) for i in range(2))
+
+
+# ------------------------------------------------------- sampled threshold
+
+def run_dgc_sampled(gc, offsets, grads, density, frac, momentum, offset=0):
+    """The sampled-threshold step, CUDA against the oracle after every step:
+    per-tensor counts, the packed lists, u and v."""
+    offsets = np.asarray(offsets, np.int64)
+    K, N = grads[0].shape
+    u_o = np.zeros((K, N), np.float32)
+    v_o = np.zeros((K, N), np.float32)
+    u_g = shifted(u_o, offset)
+    v_g = shifted(v_o, offset)
+    d = gc.DGC(offsets, K, density, momentum, sample_frac=frac)
+    short = 0
+    for t, G in enumerate(grads):
+        idx_o, val_o, counts_o, _ = oracle.dgc_step_sampled(offsets, G, u_o, v_o, density, frac, momentum, cap=d.cap)
+        out, totals = d(shifted(G, offset), u_g, v_g)
+        import torch
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(d.counts.cpu().numpy(), counts_o, err_msg=f"counts, step {t}")
+        tot = totals.cpu().numpy()
+        assert tot.tolist() == counts_o.sum(axis=1).tolist()
+        idx_g = gc.pair_indices(out).cpu().numpy()
+        val_g = gc.pair_values(out).cpu().numpy()
+        for k in range(K):
+            n = int(tot[k])
+            np.testing.assert_array_equal(idx_g[k, :n], idx_o[k, :n].astype(np.int64), err_msg=f"idx k={k} t={t}")
+            assert rel_err(val_g[k, :n], val_o[k, :n]) <= VAL_RTOL
+        assert rel_err(u_g.cpu().numpy(), u_o) <= VAL_RTOL and rel_err(v_g.cpu().numpy(), v_o) <= VAL_RTOL
+        short += int((counts_o < np.array([[oracle.dgc_k(density, int(offsets[s + 1] - offsets[s]))
+                                             for s in range(len(offsets) - 1)]])).sum())
+    return short
+
+
+@pytest.mark.parametrize("frac", [0.001, 0.003, 0.01, 0.2])
+def test_sampled_threshold(cuda_lib, frac):
+    rng = np.random.default_rng(int(frac * 1000) + 7)
+    off = wl.layout_offsets([16384, 50000, 200000, 33333, 0, 700000])
+    grads = [(rng.standard_normal((2, off[-1])) * 1e-3).astype(np.float32) for _ in range(3)]
+    run_dgc_sampled(cuda_lib, off, grads, 0.002, frac, 0.9)
+
+
+def test_sampled_threshold_resnet50_small_layout(cuda_lib):
+    """The 1/8-width ResNet-50 layout, K = 4, 1 % samples, 5 steps; some
+    tensors send fewer than k (the approximation the sample makes)."""
+    w = wl.workload(2, small=True)
+    grads = [wl.gradients(w, t).numpy() for t in range(5)]
+    short = run_dgc_sampled(cuda_lib, w.offsets, grads, w.density, 0.01, w.momentum, offset=1)
+    assert short > 0
+
+
+def test_sampled_hand_examples_on_the_gpu(cuda_lib):
+    n = 20480
+    G = np.full((1, n), 1e-3, np.float32)
+    G[0, 6830], G[0, 100], G[0, 200], G[0, 20000], G[0, 300] = 5.0, 6.0, -7.0, 5.0, 4.9
+    run_dgc_sampled(cuda_lib, [0, n], [G], 0.001, 0.01, 0.9)
+    G = np.full((1, n), 1e-3, np.float32)
+    for b in range(12):
+        G[0, 128 * b] = 100.0 + b
+    G[0, 64], G[0, 65] = 150.0, 100.5
+    run_dgc_sampled(cuda_lib, [0, n], [G], 0.001, 0.5, 0.9)
