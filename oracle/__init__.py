@@ -67,6 +67,9 @@ def lib():
             L.oracle_philox4x32_10.argtypes = [vp, vp, vp]
             L.oracle_keep_threshold.restype = ctypes.c_uint64
             L.oracle_keep_threshold.argtypes = [ctypes.c_double]
+            L.oracle_ecd_step.restype = ctypes.c_int
+            L.oracle_ecd_step.argtypes = [ctypes.c_int, ctypes.c_int64, vp, vp, vp, vp, vp, ctypes.c_float,
+                                          ctypes.c_double, ctypes.c_uint64, ctypes.c_uint32]
             L.oracle_dcd_step_window.restype = ctypes.c_int
             L.oracle_dcd_step_window.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, vp, vp, vp,
                                                  ctypes.c_float, ctypes.c_double, ctypes.c_uint64, ctypes.c_uint32]
@@ -238,3 +241,16 @@ def dcd_step_replicas(rep, g, w, gamma, p, seed, t):
     rc = lib().oracle_dcd_step_replicas(n, d, _p(w3), _p(rep), _p(g), float(gamma), float(p), int(seed), int(t))
     _check(rc, "oracle_dcd_step_replicas")
     return rep
+
+
+def ecd_step(x, x_prev, xt, g, w, gamma, p, seed, t):
+    """One ECD-PSGD iteration t >= 1: ``xt`` updated in place, ``x_prev`` receives x_{t+1}."""
+    for a in (x, x_prev, xt):
+        assert a.dtype == np.float32 and a.flags["C_CONTIGUOUS"]
+    g = _f32(g)
+    w3 = _f32(w)
+    n, d = x.shape
+    rc = lib().oracle_ecd_step(n, d, _p(w3), _p(x), _p(x_prev), _p(xt), _p(g), float(gamma), float(p), int(seed),
+                               int(t))
+    _check(rc, "oracle_ecd_step")
+    return x_prev, xt

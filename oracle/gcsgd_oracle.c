@@ -563,3 +563,51 @@ int oracle_dcd_step_replicas(int n, int64_t d, const float w[3], float* rep, con
     free(cz);
     return ORACLE_OK;
 }
+
+/* ------------------------------------------------------------- ECD-PSGD */
+
+/*
+ * One ECD-PSGD iteration t >= 1 of n nodes on a ring ("Communication
+ * Compression for Decentralized Training", ECD-PSGD, equations (3) and (4)):
+ * each node j extrapolates
+ *     z_j = (1 - t/2) x_{t-1}^(j) + (t/2) x_t^(j)                     (3)
+ * and its neighbours update their estimate of its model from C(z_j)
+ *     xt_j <- (1 - 2/t) xt_j + (2/t) C(z_j).                          (4)
+ * Reading (the equivalent update form is not printed): ECD-PSGD keeps the
+ * D-PSGD step with the neighbours' models replaced by these estimates,
+ *     x_{t+1}^(i) = w[0] xt_{i-1} + w[1] x_t^(i) + w[2] xt_{i+1} - gamma g_i,
+ * a node using its own model exactly.  Every holder of an estimate of x^(j)
+ * applies the same C(z_j), so one array xt[n][d] stands for all of them.  C is
+ * the random sparsification of the DCD-PSGD step (Philox4x32-10, keep with
+ * probability p, scale 1/p).  The coefficients are rounded to fp32 once from
+ * fp64: a = 1 - t/2, b = t/2, c = 1 - 2/t, e2 = 2/t.
+ * x [n][d] holds x_t (read), x_prev [n][d] holds x_{t-1} and receives x_{t+1},
+ * xt [n][d] the estimates (updated in place), g [n][d] the gradients.
+ */
+int oracle_ecd_step(int n, int64_t d, const float w[3], const float* x, float* x_prev, float* xt, const float* g,
+                    float gamma, double p, uint64_t seed, uint32_t t) {
+    if (n < 1 || d < 0 || !(p > 0.0 && p <= 1.0) || t < 1) return ORACLE_EINVAL;
+    const uint64_t thr = oracle_keep_threshold(p);
+    const float inv_p = (float)(1.0 / p);
+    const float a = (float)(1.0 - 0.5 * (double)t), b = (float)(0.5 * (double)t);
+    const float c = (float)(1.0 - 2.0 / (double)t), e2 = (float)(2.0 / (double)t);
+    /* (3), (4): the new estimates of every node */
+    for (int j = 0; j < n; ++j)
+        for (int64_t e = 0; e < d; ++e) {
+            const int64_t q = (int64_t)j * d + e;
+            const float z = a * x_prev[q] + b * x[q];
+            const float cz = dcd_compress(z, dcd_word(seed, (uint32_t)j, t, (uint64_t)e), thr, inv_p);
+            xt[q] = c * xt[q] + e2 * cz;
+        }
+    /* the D-PSGD step on the estimates */
+    for (int i = 0; i < n; ++i) {
+        const int l = (i + n - 1) % n, r = (i + 1) % n;
+        for (int64_t e = 0; e < d; ++e) {
+            float acc = w[0] * xt[(int64_t)l * d + e];
+            acc = acc + w[1] * x[(int64_t)i * d + e];
+            acc = acc + w[2] * xt[(int64_t)r * d + e];
+            x_prev[(int64_t)i * d + e] = acc - gamma * g[(int64_t)i * d + e];
+        }
+    }
+    return ORACLE_OK;
+}

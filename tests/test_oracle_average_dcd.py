@@ -227,3 +227,67 @@ def test_window_matches_full_step():
     for e0, e1 in [(0, 7), (13, 500), (1999, 2000), (1024, 2000)]:
         win = oracle.dcd_step_window(np.ascontiguousarray(x[:, e0:e1]), g[:, e0:e1], RING, 0.1, 0.2, 99, 4, e0)
         np.testing.assert_array_equal(win, full[:, e0:e1])
+
+
+# ------------------------------------------------------------------ ECD-PSGD
+
+def _ecd_state(rng, n, d):
+    x_prev = (rng.standard_normal((n, d)) * 1e-2).astype(np.float32)
+    x = (x_prev + rng.standard_normal((n, d)) * 1e-3).astype(np.float32)
+    g = (rng.standard_normal((n, d)) * 1e-3).astype(np.float32)
+    return x, x_prev, g
+
+
+def test_ecd_t2_identity_compression_is_d_psgd():
+    """At t = 2 the extrapolation weights are (0, 1) and the estimate weights
+    (0, 1), so with C the identity the estimate is x_t itself and the step is
+    D-PSGD: W x_t - gamma g, added left, self, right in fp32."""
+    rng = np.random.default_rng(0)
+    n, d = 5, 777
+    x, x_prev, g = _ecd_state(rng, n, d)
+    xt = rng.standard_normal((n, d)).astype(np.float32)  # the old estimate is weighted by 0
+    w = np.array([0.25, 0.5, 0.25], np.float32)
+    new, est = oracle.ecd_step(x, x_prev.copy(), xt, g, w, np.float32(0.1), 1.0, 5, 2)
+    np.testing.assert_array_equal(est, x)
+    want = (w[0] * np.roll(x, 1, axis=0) + w[1] * x) + w[2] * np.roll(x, -1, axis=0)
+    want = want - np.float32(0.1) * g
+    np.testing.assert_array_equal(new, want.astype(np.float32))
+
+
+@pytest.mark.parametrize("t", [1, 3, 7, 40])
+def test_ecd_estimate_tracks_the_model_without_compression(t):
+    """With C the identity and a consistent estimate (xt = x_{t-1}),
+    equations (3) and (4) give xt_t = x_t up to fp32 rounding."""
+    rng = np.random.default_rng(t)
+    n, d = 3, 4000
+    x, x_prev, g = _ecd_state(rng, n, d)
+    xt = x_prev.copy()
+    _, est = oracle.ecd_step(x, x_prev.copy(), xt, g, np.array([1 / 3] * 3, np.float32), np.float32(0.1), 1.0, 9, t)
+    # the terms are O(t |x|), so the rounding error scales with t
+    assert np.max(np.abs(est - x)) <= 4 * t * np.finfo(np.float32).eps * np.max(np.abs(x))
+
+
+def test_ecd_self_weight_one_is_sgd():
+    rng = np.random.default_rng(3)
+    x, x_prev, g = _ecd_state(rng, 4, 1000)
+    new, _ = oracle.ecd_step(x, x_prev.copy(), x_prev.copy(), g, np.array([0, 1, 0], np.float32),
+                             np.float32(0.05), 0.01, 11, 6)
+    np.testing.assert_array_equal(new, x - np.float32(0.05) * g)
+
+
+def test_ecd_t2_keep_mask_from_philox():
+    """At t = 2, xt = C(x_t): x_t / p where Philox keeps it, 0 elsewhere; the
+    counter is (e / 4, node, t, e / 2^34), the word e mod 4, key = the seed."""
+    rng = np.random.default_rng(4)
+    n, d, p, seed = 2, 2048, 0.25, 0x1234_5678_9ABC_DEF0
+    x, x_prev, g = _ecd_state(rng, n, d)
+    _, est = oracle.ecd_step(x, x_prev.copy(), np.zeros((n, d), np.float32), g, np.array([1 / 3] * 3, np.float32),
+                             np.float32(0.1), p, seed, 2)
+    thr = oracle.keep_threshold(p)
+    key = (seed & 0xFFFFFFFF, seed >> 32)
+    for i in range(n):
+        for e in range(0, d, 4):
+            words = oracle.philox4x32_10((e // 4, i, 2, 0), key)
+            for q in range(4):
+                want = np.float32(x[i, e + q] * np.float32(1 / p)) if words[q] < thr else np.float32(0)
+                assert est[i, e + q] == want

@@ -54,6 +54,9 @@ MUTANTS = {
     "dcd_gradient_sign": ("const float xh = acc - gamma * gi[e];", "const float xh = acc + gamma * gi[e];"),
     "dcd_no_unbiasing_scale": ("return ((uint64_t)word < thr) ? z * inv_p : 0.0f;",
                                "return ((uint64_t)word < thr) ? z : 0.0f;"),
+    "ecd_extrapolation_swapped": ("const float z = a * x_prev[q] + b * x[q];", "const float z = b * x_prev[q] + a * x[q];"),
+    "ecd_estimate_weight": ("const float c = (float)(1.0 - 2.0 / (double)t)", "const float c = (float)(1.0 - 1.0 / (double)t)"),
+    "ecd_self_from_estimate": ("acc = acc + w[1] * x[(int64_t)i * d + e];", "acc = acc + w[1] * xt[(int64_t)i * d + e];"),
     "dcd_counter_words_swapped": ("uint32_t ctr[4] = {(uint32_t)(e >> 2), node, t, (uint32_t)(e >> 34)};",
                                   "uint32_t ctr[4] = {(uint32_t)(e >> 2), t, node, (uint32_t)(e >> 34)};"),
 }
