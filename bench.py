@@ -486,6 +486,38 @@ def run_gpu(args):
                    "sent_vs_exact_k": float(cnt.sum()) / float(K * k_s.sum()),
                    "tensors_short_of_k": float((cnt < k_s[None, :]).mean())}
 
+    # the ECD-PSGD iteration on the same ring (extrapolated estimates,
+    # equations (3)-(4)): 24 algorithmic bytes per node-element (read x_t,
+    # x_{t-1}, the estimate and g; write x_{t+1} and the estimate)
+    ecd = None
+    if w.method == "dcd":
+        from gradient_compression_sgd_gb300 import workloads as wl2
+        x_a = wl2.dcd_initial_model(w, device=dev)
+        x_b, x_t = x_a.clone(), x_a.clone()
+        seed = wl2.dcd_seed(w)
+        for i in range(args.warmup):
+            gc.ecd_step(x_a, x_b, x_t, grads[i % N_SETS], w.ring_w, w.gamma, w.keep_p, seed, i + 1)
+            x_a, x_b = x_b, x_a
+        torch.cuda.synchronize()
+        gc.trace_enable(True)
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for i in range(args.steps):
+            gc.ecd_step(x_a, x_b, x_t, grads[i % N_SETS], w.ring_w, w.gamma, w.keep_p, seed, args.warmup + i + 1)
+            x_a, x_b = x_b, x_a
+        c1.record(stream)
+        torch.cuda.synchronize()
+        gc.trace_enable(False)
+        tr_e = gc.trace_read()
+        ms_e = max_over_ranks(c0.elapsed_time(c1) / args.steps, dev)
+        ne, te = tr_e.get("ecd_step", (0, 0.0))
+        kms = te / max(ne, 1)
+        hbm_e, _ = peaks()
+        ach = 24.0 * K * N / (kms * 1e-3) / 1e9 if kms > 0 else None
+        ecd = {"step": "ecd_step (ring of the same nodes)", "value": job_gbs(world, 4.0 * K * N, ms_e), "unit": "GB/s",
+               "ms_per_step": ms_e, "kernel_achieved_gbs": ach, "frac_of_measured_copy": (ach / hbm_e) if ach else None}
+
     # end to end through the public API: every step copies its gradients in
     # from pinned host memory and its dense result out to pinned host memory.
     # Double-buffered on three streams, so step i+1's upload overlaps step i's
@@ -585,6 +617,7 @@ def run_gpu(args):
                                          "h2d_bytes_per_step": int(grad_bytes), "d2h_bytes_per_step": d2h},
         "fused_update": fused,
         "sampled_threshold": sampled,
+        "ecd_variant": ecd,
         "gpu_launches": launches,
         "clocks": clk,
         "cpu_baseline": cpu,

@@ -89,6 +89,7 @@ def lib():
         L.sparse_average.argtypes = [vp, i64, vp, i32, i64, vp, vp]
         L.sparse_average_update.argtypes = [vp, i64, vp, i32, i64, f32, vp, vp]
         L.dcd_step.argtypes = [i32, i64, vp, vp, vp, f32, f64, u64, u32, vp]
+        L.ecd_step.argtypes = [i32, i64, vp, vp, vp, vp, vp, f32, f64, u64, u32, vp]
         _lib = L
         return L
 
@@ -137,6 +138,20 @@ def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def ecd_step(x, x_prev, xtilde, grad, w_ring, gamma: float, keep_p: float, seed: int, t: int, stream=None):
+    """One ECD-PSGD ring iteration t >= 1 (see ecd_step in include/gcsgd.h): x_prev receives x_{t+1},
+    xtilde is updated in place."""
+    import torch
+    n, d = x.shape
+    w = np.ascontiguousarray(np.asarray(w_ring, dtype=np.float32))
+    if w.shape != (3,):
+        raise ValueError("w_ring must hold 3 weights (left, self, right)")
+    _check("ecd_step", lib().ecd_step(int(n), int(d), _ptr(w), _dev(x, "x", torch.float32),
+                                      _dev(x_prev, "x_prev", torch.float32), _dev(xtilde, "xtilde", torch.float32),
+                                      _dev(grad, "grad", torch.float32), float(gamma), float(keep_p),
+                                      int(seed) & 0xFFFFFFFFFFFFFFFF, int(t) & 0xFFFFFFFF, _stream(stream)))
 
 
 def pairs_buffer(K: int, cap: int, device="cuda"):

@@ -25,6 +25,8 @@ int spavg_launch(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, in
                  cudaStream_t stream, bool update, float lr);
 int dcd_launch(int n, int64_t d, const float* w, float* xhat, const float* grad, float gamma, double p, uint64_t seed,
                uint32_t t, cudaStream_t stream);
+int ecd_launch(int n, int64_t d, const float* w, const float* x, float* x_prev, float* xt, const float* grad,
+               float gamma, double p, uint64_t seed, uint32_t t, cudaStream_t stream);
 
 // ------------------------------------------------------------------ errors
 
@@ -322,6 +324,21 @@ int dcd_step(int32_t n_nodes, int64_t d, const float* w_ring, float* xhat, const
     if (!isfinite(gamma) || !isfinite(w_ring[0]) || !isfinite(w_ring[1]) || !isfinite(w_ring[2]))
         return set_error(GCSGD_ERR_INVALID_ARG, "%s: gamma and weights must be finite", fn);
     return dcd_launch(n_nodes, d, w_ring, xhat, grad, gamma, keep_p, seed, t, (cudaStream_t)stream);
+}
+
+int ecd_step(int32_t n_nodes, int64_t d, const float* w_ring, const float* x, float* x_prev, float* xtilde,
+             const float* grad, float gamma, double keep_p, uint64_t seed, uint32_t t, void* stream) {
+    const char* fn = "ecd_step";
+    if (n_nodes < 1) return set_error(GCSGD_ERR_INVALID_ARG, "%s: n_nodes < 1", fn);
+    if (d < 0 || d >= ((int64_t)1 << 36)) return set_error(GCSGD_ERR_INVALID_ARG, "%s: d outside [0, 2^36)", fn);
+    if (t < 1) return set_error(GCSGD_ERR_INVALID_ARG, "%s: t = 0 (iterations count from 1)", fn);
+    if (!w_ring) return set_error(GCSGD_ERR_INVALID_ARG, "%s: w_ring is NULL", fn);
+    if (d > 0 && (!x || !x_prev || !xtilde || !grad))
+        return set_error(GCSGD_ERR_INVALID_ARG, "%s: x, x_prev, xtilde and grad must be non-NULL", fn);
+    if (!(keep_p > 0.0 && keep_p <= 1.0))
+        return set_error(GCSGD_ERR_INVALID_ARG, "%s: keep_p %g outside (0, 1]", fn, keep_p);
+    if (!isfinite(gamma)) return set_error(GCSGD_ERR_INVALID_ARG, "%s: gamma is not finite", fn);
+    return ecd_launch(n_nodes, d, w_ring, x, x_prev, xtilde, grad, gamma, keep_p, seed, t, (cudaStream_t)stream);
 }
 
 }  // extern "C"

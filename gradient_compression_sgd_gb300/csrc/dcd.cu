@@ -128,6 +128,117 @@ __global__ void __launch_bounds__(NT) dcd_rolling(Params P, int n, uint64_t d, f
     }
 }
 
+// ---------------------------------------------------------------- ECD-PSGD
+//
+// "Communication Compression for Decentralized Training", ECD-PSGD,
+// equations (3) and (4): node j extrapolates z_j = (1 - t/2) x_{t-1} +
+// (t/2) x_t, its neighbours' estimate of it becomes xt_j <- (1 - 2/t) xt_j +
+// (2/t) C(z_j), and the D-PSGD step runs on the estimates (a node uses its own
+// model): x_{t+1}^(i) = w0 xt_{i-1} + w1 x_t^(i) + w2 xt_{i+1} - gamma g_i.
+// One estimate array stands for every holder (they all apply the same
+// C(z_j)).  Per thread: four consecutive elements of every node; the new
+// estimates are computed first, then each node's step; x_{t+1} goes into the
+// x_{t-1} buffer once that node's x_{t-1} has been read.
+
+struct EcdParams {
+    float w0, w1, w2, gamma, inv_p;
+    float a, b, c, e2;  // 1 - t/2, t/2, 1 - 2/t, 2/t (rounded once to fp32)
+    uint64_t thr;
+    uint32_t key0, key1, t;
+};
+
+__device__ __forceinline__ float4 ecd_estimate(const EcdParams& P, const float4& X, const float4& XP,
+                                               const float4& XT, uint64_t q, uint32_t node) {
+    const uint4 w = philox4x32_10(make_uint4((uint32_t)q, node, P.t, (uint32_t)(q >> 32)), P.key0, P.key1);
+    const float* x = &X.x;
+    const float* xp = &XP.x;
+    const float* xt = &XT.x;
+    const uint32_t* wd = &w.x;
+    float4 o;
+    float* oo = &o.x;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float z = __fadd_rn(__fmul_rn(P.a, xp[j]), __fmul_rn(P.b, x[j]));
+        const float cz = ((uint64_t)wd[j] < P.thr) ? __fmul_rn(z, P.inv_p) : 0.0f;
+        oo[j] = __fadd_rn(__fmul_rn(P.c, xt[j]), __fmul_rn(P.e2, cz));
+    }
+    return o;
+}
+
+__device__ __forceinline__ float4 ecd_mix(const EcdParams& P, const float4& L, const float4& X, const float4& R,
+                                          const float4& G) {
+    const float* l = &L.x;
+    const float* x = &X.x;
+    const float* r = &R.x;
+    const float* g = &G.x;
+    float4 o;
+    float* oo = &o.x;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float acc = __fmul_rn(P.w0, l[j]);
+        acc = __fadd_rn(acc, __fmul_rn(P.w1, x[j]));
+        acc = __fadd_rn(acc, __fmul_rn(P.w2, r[j]));
+        oo[j] = __fsub_rn(acc, __fmul_rn(P.gamma, g[j]));
+    }
+    return o;
+}
+
+// NN <= 4: every node's float4s in registers (larger rings take the rolling
+// window, which keeps the register count low enough for two CTAs per SM).
+template <int NN>
+__global__ void __launch_bounds__(NT, 2) ecd_fixed(EcdParams P, uint64_t d, const float* __restrict__ x,
+                                                float* __restrict__ x_prev, float* __restrict__ xt,
+                                                const float* __restrict__ grad, bool rows_aligned) {
+    const uint64_t nq = (d + 3) / 4;
+    for (uint64_t q = (uint64_t)blockIdx.x * NT + threadIdx.x; q < nq; q += (uint64_t)gridDim.x * NT) {
+        const uint64_t e = 4 * q;
+        const bool vec = rows_aligned && e + 4 <= d;
+        float4 X[NN], T[NN];
+#pragma unroll
+        for (int i = 0; i < NN; ++i) {
+            X[i] = ld4(x + (uint64_t)i * d, e, d, vec);
+            const float4 xp = ld4(x_prev + (uint64_t)i * d, e, d, vec);
+            const float4 xo = ld4(xt + (uint64_t)i * d, e, d, vec);
+            T[i] = ecd_estimate(P, X[i], xp, xo, q, (uint32_t)i);
+        }
+#pragma unroll
+        for (int i = 0; i < NN; ++i) {
+            const int l = (i + NN - 1) % NN, r = (i + 1) % NN;
+            const float4 g = ld4(grad + (uint64_t)i * d, e, d, vec);
+            st4(x_prev + (uint64_t)i * d, e, d, vec, ecd_mix(P, T[l], X[i], T[r], g));
+            st4(xt + (uint64_t)i * d, e, d, vec, T[i]);
+        }
+    }
+}
+
+// Any node count: estimates computed along a rolling window (node 0's and
+// node n-1's are kept for the wrap-around).
+__global__ void __launch_bounds__(NT) ecd_rolling(EcdParams P, int n, uint64_t d, const float* __restrict__ x,
+                                                  float* __restrict__ x_prev, float* __restrict__ xt,
+                                                  const float* __restrict__ grad, bool rows_aligned) {
+    const uint64_t nq = (d + 3) / 4;
+    for (uint64_t q = (uint64_t)blockIdx.x * NT + threadIdx.x; q < nq; q += (uint64_t)gridDim.x * NT) {
+        const uint64_t e = 4 * q;
+        const bool vec = rows_aligned && e + 4 <= d;
+        auto est = [&](int i) {
+            return ecd_estimate(P, ld4(x + (uint64_t)i * d, e, d, vec), ld4(x_prev + (uint64_t)i * d, e, d, vec),
+                                ld4(xt + (uint64_t)i * d, e, d, vec), q, (uint32_t)i);
+        };
+        const float4 t0 = est(0);
+        float4 left = est(n - 1);
+        float4 cur = t0;
+        for (int i = 0; i < n; ++i) {
+            const float4 right = (i == n - 1) ? t0 : est(i + 1);
+            const float4 xi = ld4(x + (uint64_t)i * d, e, d, vec);
+            const float4 g = ld4(grad + (uint64_t)i * d, e, d, vec);
+            st4(x_prev + (uint64_t)i * d, e, d, vec, ecd_mix(P, left, xi, right, g));
+            st4(xt + (uint64_t)i * d, e, d, vec, cur);
+            left = cur;
+            cur = right;
+        }
+    }
+}
+
 }  // namespace dcd
 
 int dcd_launch(int n, int64_t d, const float* w, float* xhat, const float* grad, float gamma, double p,
@@ -166,6 +277,47 @@ int dcd_launch(int n, int64_t d, const float* w, float* xhat, const float* grad,
             dcd_rolling<<<(unsigned)grid, NT, 0, stream>>>(P, n, (uint64_t)d, xhat, grad, rows_aligned);
     }
     return check_launch("dcd_step");
+}
+
+int ecd_launch(int n, int64_t d, const float* w, const float* x, float* x_prev, float* xt, const float* grad,
+               float gamma, double p, uint64_t seed, uint32_t t, cudaStream_t stream) {
+    using namespace dcd;
+    if (d == 0) return GCSGD_OK;
+    EcdParams P;
+    P.w0 = w[0];
+    P.w1 = w[1];
+    P.w2 = w[2];
+    P.gamma = gamma;
+    P.inv_p = (float)(1.0 / p);
+    P.a = (float)(1.0 - 0.5 * (double)t);
+    P.b = (float)(0.5 * (double)t);
+    P.c = (float)(1.0 - 2.0 / (double)t);
+    P.e2 = (float)(2.0 / (double)t);
+    P.thr = p >= 1.0 ? (1ull << 32) : (uint64_t)llround(p * 4294967296.0);
+    P.key0 = (uint32_t)seed;
+    P.key1 = (uint32_t)(seed >> 32);
+    P.t = t;
+    const bool rows_aligned = ((d & 3) == 0) && ((((uintptr_t)x | (uintptr_t)x_prev | (uintptr_t)xt |
+                                                   (uintptr_t)grad) & 15) == 0);
+    const uint64_t nq = ((uint64_t)d + 3) / 4;
+    uint64_t grid = (uint64_t)sm_count() * (n <= 4 ? 8 : 4);
+    const uint64_t need = (nq + NT - 1) / NT;
+    if (grid > need) grid = need;
+    LaunchScope ls("ecd_step", stream);
+    switch (n) {
+#define ECD_CASE(NNV)                                                                                        \
+    case NNV:                                                                                                \
+        ecd_fixed<NNV><<<(unsigned)grid, NT, 0, stream>>>(P, (uint64_t)d, x, x_prev, xt, grad, rows_aligned); \
+        break;
+        ECD_CASE(1)
+        ECD_CASE(2)
+        ECD_CASE(3)
+        ECD_CASE(4)
+#undef ECD_CASE
+        default:
+            ecd_rolling<<<(unsigned)grid, NT, 0, stream>>>(P, n, (uint64_t)d, x, x_prev, xt, grad, rows_aligned);
+    }
+    return check_launch("ecd_step");
 }
 
 }  // namespace gcsgd

@@ -269,6 +269,26 @@ int sparse_average_update(const gcsgd_pair* lists, int64_t cap, const int64_t* c
 int dcd_step(int32_t n_nodes, int64_t d, const float* w_ring, float* xhat, const float* grad,
              float gamma, double keep_p, uint64_t seed, uint32_t t, void* stream);
 
+/*
+ * One ECD-PSGD iteration t >= 1 of n_nodes nodes on a ring ("Communication
+ * Compression for Decentralized Training", ECD-PSGD, equations (3)-(4)):
+ *   z_j   = (1 - t/2) x_{t-1}^(j) + (t/2) x_t^(j)          (extrapolation)
+ *   xt_j <- (1 - 2/t) xt_j + (2/t) C(z_j)                   (neighbours' estimate)
+ *   x_{t+1}^(i) = w[0] xt_{i-1} + w[1] x_t^(i) + w[2] xt_{i+1} - gamma g_i
+ * (reading: the D-PSGD step on the estimates, a node using its own model;
+ * every holder of an estimate applies the same C(z_j), so xtilde holds one
+ * estimate per node).  The coefficients are rounded once to fp32; products
+ * and sums in the order written, fp32.  C is dcd_step's random
+ * sparsification (same Philox counter, node and t).
+ * x       [n_nodes][d] x_t, read only.
+ * x_prev  [n_nodes][d] x_{t-1} on entry, x_{t+1} on return (the caller swaps
+ *         x and x_prev for the next iteration).
+ * xtilde  [n_nodes][d] the estimates, updated in place (start: the initial model).
+ * t >= 1; other arguments as dcd_step.
+ */
+int ecd_step(int32_t n_nodes, int64_t d, const float* w_ring, const float* x, float* x_prev, float* xtilde,
+             const float* grad, float gamma, double keep_p, uint64_t seed, uint32_t t, void* stream);
+
 /* ----------------------------------------------------- errors, tracing */
 
 /* Message of the calling thread's last failure ("" if none).  Host. */

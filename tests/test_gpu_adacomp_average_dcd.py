@@ -381,3 +381,36 @@ def test_philox_matches_curand_device_api(cuda_lib, tmp_path):
     for i in range(len(qs)):
         want = oracle.philox4x32_10([int(qs[i]) & 0xFFFFFFFF, int(nodes[i]), int(ts[i]), int(qs[i]) >> 32], key)
         np.testing.assert_array_equal(got[i], want)
+
+
+# ----------------------------------------------------------------- ECD-PSGD
+
+def run_ecd(gc, n, d, T, p, w=(1 / 3, 1 / 3, 1 / 3), gamma=0.1, seed=0xEC0, offset=0):
+    """T iterations (t = 1..T) on both sides, the caller swapping x and
+    x_prev after each; models and estimates compared after every step."""
+    rng = np.random.default_rng(n * 1000 + d + offset)
+    x0 = (rng.standard_normal(d) * 1e-2).astype(np.float32)
+    xo, xpo, xto = (np.tile(x0, (n, 1)).copy() for _ in range(3))
+    xg, xpg, xtg = (shifted(np.tile(x0, (n, 1)), offset) for _ in range(3))
+    for t in range(1, T + 1):
+        g = (rng.standard_normal((n, d)) * 1e-3).astype(np.float32)
+        oracle.ecd_step(xo, xpo, xto, g, w, gamma, p, seed, t)
+        gc.ecd_step(xg, xpg, xtg, shifted(g, offset), w, gamma, p, seed, t)
+        xo, xpo = xpo, xo
+        xg, xpg = xpg, xg
+        import torch
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(xg.cpu().numpy().view(np.uint32), xo.view(np.uint32), err_msg=f"model t={t}")
+        np.testing.assert_array_equal(xtg.cpu().numpy().view(np.uint32), xto.view(np.uint32), err_msg=f"est t={t}")
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 5, 8, 9, 13])
+@pytest.mark.parametrize("d", [1, 7, 4096, 10001])
+def test_ecd_nodes_and_sizes(cuda_lib, n, d):
+    run_ecd(cuda_lib, n, d, 4, 0.3)
+
+
+@pytest.mark.parametrize("offset", [1, 3])
+def test_ecd_ring8_sparsified_unaligned(cuda_lib, offset):
+    """The config-5 ring (8 nodes, keep 1 % scaled x100) at d = 262,144, 6 iterations, buffers off 16 bytes."""
+    run_ecd(cuda_lib, 8, 262144, 6, 0.01, offset=offset)
