@@ -70,6 +70,14 @@ def lib():
             L.oracle_ecd_step.restype = ctypes.c_int
             L.oracle_ecd_step.argtypes = [ctypes.c_int, ctypes.c_int64, vp, vp, vp, vp, vp, ctypes.c_float,
                                           ctypes.c_double, ctypes.c_uint64, ctypes.c_uint32]
+            L.oracle_dgc_encode.restype = ctypes.c_int64
+            L.oracle_dgc_encode.argtypes = [vp, vp, ctypes.c_int64, vp, ctypes.c_int64]
+            L.oracle_dgc_decode.restype = ctypes.c_int
+            L.oracle_dgc_decode.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, vp]
+            L.oracle_adacomp_encode.restype = ctypes.c_int64
+            L.oracle_adacomp_encode.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, vp, ctypes.c_int64]
+            L.oracle_adacomp_decode.restype = ctypes.c_int
+            L.oracle_adacomp_decode.argtypes = [vp, ctypes.c_int64, vp, ctypes.c_int, vp]
             L.oracle_dcd_step_window.restype = ctypes.c_int
             L.oracle_dcd_step_window.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, vp, vp, vp,
                                                  ctypes.c_float, ctypes.c_double, ctypes.c_uint64, ctypes.c_uint32]
@@ -254,3 +262,44 @@ def ecd_step(x, x_prev, xt, g, w, gamma, p, seed, t):
                                int(t))
     _check(rc, "oracle_ecd_step")
     return x_prev, xt
+
+
+def dgc_encode(idx, val) -> bytes:
+    """DGC's byte stream of one learner's ascending (idx, val) list."""
+    idx = np.ascontiguousarray(idx, dtype=np.uint32)
+    val = _f32(val)
+    cap = 6 * (len(idx) + int(idx.max(initial=0)) // 65536 + 2)
+    buf = np.zeros(max(cap, 6), np.uint8)
+    nb = lib().oracle_dgc_encode(_p(idx), _p(val), len(idx), _p(buf), len(buf))
+    if nb < 0:
+        raise OracleError("oracle_dgc_encode: indices do not ascend or the buffer is short")
+    return buf[:nb].tobytes()
+
+
+def dgc_decode(stream: bytes, n: int) -> np.ndarray:
+    buf = np.frombuffer(stream, np.uint8).copy() if stream else np.zeros(1, np.uint8)
+    out = np.zeros(max(int(n), 1), np.float32)
+    _check(lib().oracle_dgc_decode(_p(buf), len(stream), int(n), _p(out)), "oracle_dgc_decode")
+    return out[:n]
+
+
+def adacomp_encode(offsets, idx, val, counts, scales) -> bytes:
+    off = np.ascontiguousarray(offsets, dtype=np.int64)
+    S = len(off) - 1
+    idx = np.ascontiguousarray(idx, dtype=np.uint32)
+    val = _f32(val)
+    counts = np.ascontiguousarray(counts, dtype=np.int64)
+    scales = _f32(scales)
+    buf = np.zeros(8 * S + 4 * int(counts.sum()) + 1, np.uint8)
+    nb = lib().oracle_adacomp_encode(_p(off), S, _p(idx), _p(val), _p(counts), _p(scales), _p(buf), len(buf))
+    if nb < 0:
+        raise OracleError("oracle_adacomp_encode: buffer too short")
+    return buf[:nb].tobytes()
+
+
+def adacomp_decode(stream: bytes, offsets) -> np.ndarray:
+    off = np.ascontiguousarray(offsets, dtype=np.int64)
+    buf = np.frombuffer(stream, np.uint8).copy() if stream else np.zeros(1, np.uint8)
+    out = np.zeros(max(int(off[-1]), 1), np.float32)
+    _check(lib().oracle_adacomp_decode(_p(buf), len(stream), _p(off), len(off) - 1, _p(out)), "oracle_adacomp_decode")
+    return out[:int(off[-1])]

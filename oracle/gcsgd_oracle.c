@@ -611,3 +611,109 @@ int oracle_ecd_step(int n, int64_t d, const float w[3], const float* x, float* x
     }
     return ORACLE_OK;
 }
+
+/* -------------------------------------------------------- wire encodings */
+
+static void put_u16(unsigned char* b, uint16_t x) { b[0] = (unsigned char)(x & 0xff); b[1] = (unsigned char)(x >> 8); }
+static void put_u32(unsigned char* b, uint32_t x) {
+    for (int i = 0; i < 4; ++i) b[i] = (unsigned char)((x >> (8 * i)) & 0xff);
+}
+static uint16_t get_u16(const unsigned char* b) { return (uint16_t)(b[0] | (b[1] << 8)); }
+static uint32_t get_u32(const unsigned char* b) {
+    return (uint32_t)b[0] | ((uint32_t)b[1] << 8) | ((uint32_t)b[2] << 16) | ((uint32_t)b[3] << 24);
+}
+
+/*
+ * DGC's message as a byte stream ("Deep Gradient Compression", section 3.1:
+ * the encoder packs 32-bit non-zero gradient values and 16-bit zero run
+ * lengths).  Reading: one 6-byte record per sent entry, little-endian
+ * [uint16 number of unsent positions since the previous entry (or the
+ * start)][fp32 value]; a gap of 65536 or more is split by escape records
+ * (65535, +0.0f), each standing for 65535 zeros and one explicit zero.
+ * idx ascending.  Writes at most 6 * (count + escapes) bytes; returns the
+ * byte count, or -1 if out_cap is too small or the indices do not ascend.
+ */
+int64_t oracle_dgc_encode(const uint32_t* idx, const float* val, int64_t count, unsigned char* out, int64_t out_cap) {
+    int64_t at = 0, next = 0; /* next: first position not yet covered */
+    for (int64_t j = 0; j < count; ++j) {
+        if ((int64_t)idx[j] < next) return -1;
+        int64_t gap = (int64_t)idx[j] - next;
+        while (gap >= 65536) {
+            if (at + 6 > out_cap) return -1;
+            put_u16(out + at, 65535);
+            put_u32(out + at + 2, 0u);
+            at += 6;
+            gap -= 65536;
+        }
+        if (at + 6 > out_cap) return -1;
+        put_u16(out + at, (uint16_t)gap);
+        put_u32(out + at + 2, bits_of(val[j]));
+        at += 6;
+        next = (int64_t)idx[j] + 1;
+    }
+    return at;
+}
+
+/* Decodes a DGC byte stream into dense[n] (zeros elsewhere); -1 if it runs past n. */
+int oracle_dgc_decode(const unsigned char* in, int64_t nbytes, int64_t n, float* dense) {
+    for (int64_t j = 0; j < n; ++j) dense[j] = 0.0f;
+    int64_t pos = 0;
+    for (int64_t at = 0; at + 6 <= nbytes; at += 6) {
+        pos += get_u16(in + at);
+        if (pos >= n) return -1;
+        uint32_t b = get_u32(in + at + 2);
+        memcpy(&dense[pos], &b, 4);
+        ++pos;
+    }
+    return 0;
+}
+
+/*
+ * AdaComp's message as a byte stream ("AdaComp ...", Proposed method: one
+ * scale per layer, the mean of |g_max|, with each sent entry as sign +
+ * scale).  Reading: per layer, in order, a header [uint32 count][fp32 scale]
+ * and then count uint32 words (local index << 1 | sign bit, sign = 1 for a
+ * negative value), little-endian.  idx/val: the learner's list (layers one
+ * after another, ascending); counts/scales: [S].  Returns the byte count or
+ * -1 if out_cap is too small.
+ */
+int64_t oracle_adacomp_encode(const int64_t* seg_off, int S, const uint32_t* idx, const float* val,
+                              const int64_t* counts, const float* scales, unsigned char* out, int64_t out_cap) {
+    int64_t at = 0, j = 0;
+    for (int s = 0; s < S; ++s) {
+        if (at + 8 + 4 * counts[s] > out_cap) return -1;
+        put_u32(out + at, (uint32_t)counts[s]);
+        put_u32(out + at + 4, bits_of(scales[s]));
+        at += 8;
+        for (int64_t q = 0; q < counts[s]; ++q, ++j) {
+            const uint32_t local = (uint32_t)((int64_t)idx[j] - seg_off[s]);
+            const uint32_t sign = val[j] < 0.0f ? 1u : 0u;
+            put_u32(out + at, (local << 1) | sign);
+            at += 4;
+        }
+    }
+    return at;
+}
+
+/* Decodes an AdaComp byte stream into dense[n]: +-scale at the sent entries. */
+int oracle_adacomp_decode(const unsigned char* in, int64_t nbytes, const int64_t* seg_off, int S, float* dense) {
+    const int64_t n = seg_off[S];
+    for (int64_t j = 0; j < n; ++j) dense[j] = 0.0f;
+    int64_t at = 0;
+    for (int s = 0; s < S; ++s) {
+        if (at + 8 > nbytes) return -1;
+        const uint32_t c = get_u32(in + at);
+        const uint32_t sb = get_u32(in + at + 4);
+        float scale;
+        memcpy(&scale, &sb, 4);
+        at += 8;
+        for (uint32_t q = 0; q < c; ++q, at += 4) {
+            if (at + 4 > nbytes) return -1;
+            const uint32_t w = get_u32(in + at);
+            const int64_t local = (int64_t)(w >> 1);
+            if (seg_off[s] + local >= seg_off[s + 1]) return -1;
+            dense[seg_off[s] + local] = (w & 1u) ? -scale : scale;
+        }
+    }
+    return 0;
+}

@@ -16,7 +16,7 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC_PATH = os.path.join(ROOT, "oracle", "gcsgd_oracle.c")
-PIN_FILES = ["test_oracle_dgc.py", "test_oracle_adacomp.py", "test_oracle_average_dcd.py"]
+PIN_FILES = ["test_oracle_dgc.py", "test_oracle_adacomp.py", "test_oracle_average_dcd.py", "test_oracle_wire.py"]
 
 # name -> (text in the oracle, planted replacement)
 MUTANTS = {
@@ -47,6 +47,9 @@ MUTANTS = {
     "update_adds_the_step": ("w[j] = w[j] - step;", "w[j] = w[j] + step;"),
     "update_skips_last_list": ("for (int k = 0; k < K; ++k)\n            for (int64_t p = 0; p < counts[k]; ++p) carried",
                                "for (int k = 0; k < K - 1; ++k)\n            for (int64_t p = 0; p < counts[k]; ++p) carried"),
+    # wire encodings
+    "wire_escape_width": ("            gap -= 65536;", "            gap -= 65535;"),
+    "wire_sign_bit": ("const uint32_t sign = val[j] < 0.0f ? 1u : 0u;", "const uint32_t sign = val[j] > 0.0f ? 1u : 0u;"),
     # Philox and DCD-PSGD
     "philox_key_word_swapped": ("uint32_t n0 = hi1 ^ c1 ^ k0;", "uint32_t n0 = hi1 ^ c1 ^ k1;"),
     "dcd_wrong_neighbour": ("const int l = (i + n - 1) % n, r = (i + 1) % n;\n        const float* xl",
