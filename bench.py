@@ -431,6 +431,40 @@ def run_gpu(args):
     grad_bytes = 4.0 * K * N
     value = job_gbs(world, grad_bytes, ms)
 
+    # the messages as byte streams (DGC: 16-bit zero runs + 32-bit values;
+    # AdaComp: per-layer count and scale, then index|sign words), from the
+    # last timed step's messages: size, compression ratio, encode time
+    wire = None
+    if w.method in ("dgc", "adacomp"):
+        obj = path.obj
+        tot_max = int(obj.totals.max().item())
+        cap_b = 6 * (tot_max + N // 65536 + 2) if w.method == "dgc" else 8 * len(w.sizes) + 4 * tot_max
+        cap_b += (-cap_b) % 16
+        streams = torch.zeros((K, cap_b), dtype=torch.uint8, device=dev)
+        nbytes = torch.zeros(K, dtype=torch.int64, device=dev)
+
+        def encode():
+            if w.method == "dgc":
+                gc.dgc_encode(obj.out, obj.totals, streams, nbytes)
+            else:
+                gc.adacomp_encode(w.offsets, obj.out, obj.counts, obj.scales, streams, nbytes)
+
+        encode()
+        torch.cuda.synchronize()
+        q0 = torch.cuda.Event(enable_timing=True)
+        q1 = torch.cuda.Event(enable_timing=True)
+        q0.record(stream)
+        for _ in range(10):
+            encode()
+        q1.record(stream)
+        torch.cuda.synchronize()
+        nb = nbytes.cpu().numpy().astype(np.float64)
+        wire = {"format": "16-bit zero runs + fp32 values" if w.method == "dgc"
+                else "per layer [count, scale] + (index << 1 | sign) words",
+                "bytes_per_learner": float(nb.mean()), "dense_bytes_per_learner": 4.0 * N,
+                "compression_ratio": float(4.0 * N / nb.mean()) if nb.mean() > 0 else None,
+                "encode_ms": q0.elapsed_time(q1) / 10}
+
     # the fused variant: compress + averaged weight update on the carried
     # indices only (no dense average written)
     fused = None
@@ -615,6 +649,7 @@ def run_gpu(args):
         **path.extra(),
         "e2e": None if e2e is None else {"value": e2e, "unit": "GB/s", "ms_per_step": ms_e2e,
                                          "h2d_bytes_per_step": int(grad_bytes), "d2h_bytes_per_step": d2h},
+        "wire": wire,
         "fused_update": fused,
         "sampled_threshold": sampled,
         "ecd_variant": ecd,

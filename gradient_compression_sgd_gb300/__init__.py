@@ -90,6 +90,10 @@ def lib():
         L.sparse_average_update.argtypes = [vp, i64, vp, i32, i64, f32, vp, vp]
         L.dcd_step.argtypes = [i32, i64, vp, vp, vp, f32, f64, u64, u32, vp]
         L.ecd_step.argtypes = [i32, i64, vp, vp, vp, vp, vp, f32, f64, u64, u32, vp]
+        L.dgc_encode.argtypes = [vp, i64, vp, i32, vp, i64, vp, vp]
+        L.dgc_decode.argtypes = [vp, i64, vp, i32, vp, i64, vp, vp]
+        L.adacomp_encode.argtypes = [vp, i32, vp, i64, vp, vp, i32, vp, i64, vp, vp]
+        L.adacomp_decode.argtypes = [vp, i32, vp, i64, vp, i32, vp, i64, vp, vp]
         _lib = L
         return L
 
@@ -152,6 +156,43 @@ def ecd_step(x, x_prev, xtilde, grad, w_ring, gamma: float, keep_p: float, seed:
                                       _dev(x_prev, "x_prev", torch.float32), _dev(xtilde, "xtilde", torch.float32),
                                       _dev(grad, "grad", torch.float32), float(gamma), float(keep_p),
                                       int(seed) & 0xFFFFFFFFFFFFFFFF, int(t) & 0xFFFFFFFF, _stream(stream)))
+
+
+def dgc_encode(lists, totals, streams, nbytes, stream=None):
+    """DGC messages [K, cap] -> byte streams [K, stream_cap] (uint8); nbytes [K] (see dgc_encode in include/gcsgd.h)."""
+    import torch
+    K, cap = lists.shape[0], lists.shape[1]
+    _check("dgc_encode", lib().dgc_encode(_dev(lists, "lists", torch.int32), int(cap), _dev(totals, "totals", torch.int64),
+                                          int(K), _dev(streams, "streams", torch.uint8), int(streams.shape[1]),
+                                          _dev(nbytes, "nbytes", torch.int64), _stream(stream)))
+
+
+def dgc_decode(streams, nbytes, lists, totals, stream=None):
+    import torch
+    K = streams.shape[0]
+    _check("dgc_decode", lib().dgc_decode(_dev(streams, "streams", torch.uint8), int(streams.shape[1]),
+                                          _dev(nbytes, "nbytes", torch.int64), int(K), _dev(lists, "lists", torch.int32),
+                                          int(lists.shape[1]), _dev(totals, "totals", torch.int64), _stream(stream)))
+
+
+def adacomp_encode(offsets, lists, counts, scales, streams, nbytes, stream=None):
+    import torch
+    off = _offsets(offsets)
+    K, cap = lists.shape[0], lists.shape[1]
+    _check("adacomp_encode", lib().adacomp_encode(
+        _ptr(off), len(off) - 1, _dev(lists, "lists", torch.int32), int(cap), _dev(counts, "counts", torch.int64),
+        _dev(scales, "scales", torch.float32), int(K), _dev(streams, "streams", torch.uint8), int(streams.shape[1]),
+        _dev(nbytes, "nbytes", torch.int64), _stream(stream)))
+
+
+def adacomp_decode(offsets, streams, nbytes, lists, totals, stream=None):
+    import torch
+    off = _offsets(offsets)
+    K = streams.shape[0]
+    _check("adacomp_decode", lib().adacomp_decode(
+        _ptr(off), len(off) - 1, _dev(streams, "streams", torch.uint8), int(streams.shape[1]),
+        _dev(nbytes, "nbytes", torch.int64), int(K), _dev(lists, "lists", torch.int32), int(lists.shape[1]),
+        _dev(totals, "totals", torch.int64), _stream(stream)))
 
 
 def pairs_buffer(K: int, cap: int, device="cuda"):

@@ -27,6 +27,15 @@ int dcd_launch(int n, int64_t d, const float* w, float* xhat, const float* grad,
                uint32_t t, cudaStream_t stream);
 int ecd_launch(int n, int64_t d, const float* w, const float* x, float* x_prev, float* xt, const float* grad,
                float gamma, double p, uint64_t seed, uint32_t t, cudaStream_t stream);
+int wire_dgc_encode(const gcsgd_pair* lists, int64_t cap, const int64_t* totals, int K, uint8_t* streams,
+                    int64_t stream_cap, int64_t* nbytes, cudaStream_t stream);
+int wire_dgc_decode(const uint8_t* streams, int64_t stream_cap, const int64_t* nbytes, int K, gcsgd_pair* lists,
+                    int64_t cap, int64_t* totals, cudaStream_t stream);
+int wire_ada_encode(const int64_t* off, int S, const gcsgd_pair* lists, int64_t cap, const int64_t* counts,
+                    const float* scales, int K, uint8_t* streams, int64_t stream_cap, int64_t* nbytes,
+                    cudaStream_t stream);
+int wire_ada_decode(const int64_t* off, int S, const uint8_t* streams, int64_t stream_cap, const int64_t* nbytes,
+                    int K, gcsgd_pair* lists, int64_t cap, int64_t* totals, cudaStream_t stream);
 
 // ------------------------------------------------------------------ errors
 
@@ -339,6 +348,55 @@ int ecd_step(int32_t n_nodes, int64_t d, const float* w_ring, const float* x, fl
         return set_error(GCSGD_ERR_INVALID_ARG, "%s: keep_p %g outside (0, 1]", fn, keep_p);
     if (!isfinite(gamma)) return set_error(GCSGD_ERR_INVALID_ARG, "%s: gamma is not finite", fn);
     return ecd_launch(n_nodes, d, w_ring, x, x_prev, xtilde, grad, gamma, keep_p, seed, t, (cudaStream_t)stream);
+}
+
+static int check_streams(const char* fn, int32_t K, const void* streams, int64_t stream_cap, const void* a,
+                         const void* b) {
+    if (K < 1) return set_error(GCSGD_ERR_INVALID_ARG, "%s: K = %d < 1", fn, K);
+    if (stream_cap < 0 || (stream_cap & 15))
+        return set_error(GCSGD_ERR_INVALID_ARG, "%s: stream_cap must be a non-negative multiple of 16", fn);
+    if (!streams || ((uintptr_t)streams & 15))
+        return set_error(GCSGD_ERR_INVALID_ARG, "%s: streams must be non-NULL and 16-byte aligned", fn);
+    if (!a || !b) return set_error(GCSGD_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+    return GCSGD_OK;
+}
+
+int dgc_encode(const gcsgd_pair* lists, int64_t cap, const int64_t* totals, int32_t K, uint8_t* streams,
+               int64_t stream_cap, int64_t* nbytes, void* stream) {
+    int rc = check_streams("dgc_encode", K, streams, stream_cap, totals, nbytes);
+    if (rc) return rc;
+    if (cap < 0 || (cap > 0 && !lists)) return set_error(GCSGD_ERR_INVALID_ARG, "dgc_encode: bad lists or cap");
+    return wire_dgc_encode(lists, cap, totals, K, streams, stream_cap, nbytes, (cudaStream_t)stream);
+}
+
+int dgc_decode(const uint8_t* streams, int64_t stream_cap, const int64_t* nbytes, int32_t K, gcsgd_pair* lists,
+               int64_t cap, int64_t* totals, void* stream) {
+    int rc = check_streams("dgc_decode", K, streams, stream_cap, nbytes, totals);
+    if (rc) return rc;
+    if (cap < 0 || (cap > 0 && !lists)) return set_error(GCSGD_ERR_INVALID_ARG, "dgc_decode: bad lists or cap");
+    return wire_dgc_decode(streams, stream_cap, nbytes, K, lists, cap, totals, (cudaStream_t)stream);
+}
+
+int adacomp_encode(const int64_t* seg_offsets, int32_t n_seg, const gcsgd_pair* lists, int64_t cap,
+                   const int64_t* counts, const float* scales, int32_t K, uint8_t* streams, int64_t stream_cap,
+                   int64_t* nbytes, void* stream) {
+    int rc;
+    if ((rc = check_layout("adacomp_encode", seg_offsets, n_seg))) return rc;
+    if ((rc = check_streams("adacomp_encode", K, streams, stream_cap, counts, nbytes))) return rc;
+    if (!scales || cap < 0 || (cap > 0 && !lists))
+        return set_error(GCSGD_ERR_INVALID_ARG, "adacomp_encode: bad lists, cap or scales");
+    return wire_ada_encode(seg_offsets, n_seg, lists, cap, counts, scales, K, streams, stream_cap, nbytes,
+                           (cudaStream_t)stream);
+}
+
+int adacomp_decode(const int64_t* seg_offsets, int32_t n_seg, const uint8_t* streams, int64_t stream_cap,
+                   const int64_t* nbytes, int32_t K, gcsgd_pair* lists, int64_t cap, int64_t* totals, void* stream) {
+    int rc;
+    if ((rc = check_layout("adacomp_decode", seg_offsets, n_seg))) return rc;
+    if ((rc = check_streams("adacomp_decode", K, streams, stream_cap, nbytes, totals))) return rc;
+    if (cap < 0 || (cap > 0 && !lists)) return set_error(GCSGD_ERR_INVALID_ARG, "adacomp_decode: bad lists or cap");
+    return wire_ada_decode(seg_offsets, n_seg, streams, stream_cap, nbytes, K, lists, cap, totals,
+                           (cudaStream_t)stream);
 }
 
 }  // extern "C"

@@ -289,6 +289,47 @@ int dcd_step(int32_t n_nodes, int64_t d, const float* w_ring, float* xhat, const
 int ecd_step(int32_t n_nodes, int64_t d, const float* w_ring, const float* x, float* x_prev, float* xtilde,
              const float* grad, float gamma, double keep_p, uint64_t seed, uint32_t t, void* stream);
 
+/* -------------------------------------------------------- wire formats */
+
+/*
+ * DGC's messages as byte streams ("Deep Gradient Compression", section 3.1:
+ * the encoder packs 32-bit non-zero gradient values and 16-bit zero run
+ * lengths).  Learner k's list (lists[k*cap ..], totals[k] entries, indices
+ * strictly ascending) becomes streams[k*stream_cap ..]: one 6-byte record
+ * per entry, little-endian [uint16 unsent positions since the previous
+ * entry (or index 0)][fp32 value]; a gap of 65536 or more is split by escape
+ * records (65535, +0.0f), each standing for 65535 zeros and one zero.
+ * nbytes[k] = the stream's length, or -1 if it would exceed stream_cap or the
+ * indices do not ascend (then nothing is written).  streams: 16-byte
+ * aligned, stream_cap a multiple of 16.  Device arrays; one CTA per learner.
+ */
+int dgc_encode(const gcsgd_pair* lists, int64_t cap, const int64_t* totals, int32_t K, uint8_t* streams,
+               int64_t stream_cap, int64_t* nbytes, void* stream);
+
+/* The inverse: records back to (index, value) pairs, escapes dropped;
+ * totals[k] = entries, or -1 if more than cap. */
+int dgc_decode(const uint8_t* streams, int64_t stream_cap, const int64_t* nbytes, int32_t K, gcsgd_pair* lists,
+               int64_t cap, int64_t* totals, void* stream);
+
+/*
+ * AdaComp's messages as byte streams ("AdaComp ...", Proposed method: one
+ * scale per layer, the mean |g_max|, and each sent entry as sign + scale).
+ * Per layer s, in order: [uint32 counts[k][s]][fp32 scales[k][s]], then one
+ * uint32 (local index << 1 | sign bit, 1 = negative) per entry; the list
+ * holds the layers one after another (as adacomp_compress writes it).
+ * nbytes[k] = the length, or -1 if over stream_cap or if the counts add up
+ * to more than cap (a learner that overflowed sends nothing).  Same
+ * alignment rules.
+ */
+int adacomp_encode(const int64_t* seg_offsets, int32_t n_seg, const gcsgd_pair* lists, int64_t cap,
+                   const int64_t* counts, const float* scales, int32_t K, uint8_t* streams, int64_t stream_cap,
+                   int64_t* nbytes, void* stream);
+
+/* The inverse: (global index, +-scale) pairs; totals[k] = entries, or -1 if
+ * the stream is malformed or holds more than cap. */
+int adacomp_decode(const int64_t* seg_offsets, int32_t n_seg, const uint8_t* streams, int64_t stream_cap,
+                   const int64_t* nbytes, int32_t K, gcsgd_pair* lists, int64_t cap, int64_t* totals, void* stream);
+
 /* ----------------------------------------------------- errors, tracing */
 
 /* Message of the calling thread's last failure ("" if none).  Host. */
