@@ -258,7 +258,7 @@ def kernel_source_sha(name: str = "dgc.cu") -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-KERNEL_SOURCE = {"dgc_update": "dgc.cu", "ada_bins": "adacomp.cu", "dcd_step": "dcd.cu", "spavg": "spavg.cu"}
+KERNEL_SOURCE = {"dgc_update": "dgc.cu", "ada_bins": "adacomp.cu", "ada_bins_warp": "adacomp.cu", "dcd_step": "dcd.cu", "spavg": "spavg.cu"}
 
 
 def profiled_traffic(kernel: str, workload: str):
@@ -320,7 +320,7 @@ class DgcPath:
 
 class AdaCompPath(DgcPath):
     """AdaComp of K learners + sparse average of their messages (config 3)."""
-    dominant, bytes_per_elem = "ada_bins", 12
+    dominant, bytes_per_elem = "ada_bins_warp", 12  # every L_T of this workload is <= 512
 
     def __init__(self, gc, w, dev):
         import torch

@@ -30,6 +30,7 @@ namespace ada {
 
 constexpr int NT = 256;
 constexpr uint32_t kTileMax = 4096;
+constexpr uint32_t kWarpChunk = 512;  // values per warp chunk (4 float4 per lane)
 
 enum : uint32_t { kModeEmpty = 0, kModeSmall = 1, kModeBig = 2 };
 
@@ -42,7 +43,7 @@ struct SegPlan {
     uint32_t tile_off;  // first tile within a learner
     uint32_t big_off;   // first big-bin slot within a learner (big mode)
     float invL;         // fp32 1/L: bin = floor((e + 0.5) * invL) is exact for e < 4096
-    uint32_t pad;
+    uint32_t bpw;       // warp chunks: bins per warp (4 <= L <= 512; a tile is 8 chunks), else 0
 };
 
 template <int MAXS>
@@ -59,16 +60,24 @@ __host__ __device__ inline void seg_fields(uint32_t n, uint32_t L, SegPlan* p) {
     p->nbins = n ? (uint32_t)(((uint64_t)n + L - 1) / L) : 0;
     p->bpt = 0;
     p->invL = 1.0f / (float)L;
-    p->pad = 0;
+    p->bpw = 0;
     if (n == 0) {
         p->mode = kModeEmpty;
         p->tile_len = 0;
         p->ntiles = 0;
     } else if (L <= kTileMax) {
         p->mode = kModeSmall;
-        uint32_t bpt = kTileMax / L;
         const uint32_t g = 4 / gcd4(L);  // keep tiles 16-byte aligned where possible
-        if (bpt >= g) bpt -= bpt % g;
+        uint32_t bpt;
+        if (L >= 4 && L <= kWarpChunk) {  // warp chunks of whole bins, eight per tile
+            uint32_t bpw = kWarpChunk / L;
+            if (bpw >= g) bpw -= bpw % g;
+            p->bpw = bpw;
+            bpt = (NT / 32) * bpw;
+        } else {
+            bpt = kTileMax / L;
+            if (bpt >= g) bpt -= bpt % g;
+        }
         p->bpt = bpt;
         p->tile_len = bpt * L;
         p->ntiles = (p->nbins + bpt - 1) / bpt;
@@ -91,7 +100,7 @@ void host_plan(const int64_t* off, const int32_t* lt, int S, HostPlan* hp) {
         SegPlan p;
         seg_fields((uint32_t)(off[s + 1] - off[s]), (uint32_t)lt[s], &p);
         hp->tiles_per_learner += p.ntiles;
-        if (p.mode == kModeBig) hp->big_per_learner += p.nbins;
+        if (p.mode == kModeBig || p.bpw) hp->big_per_learner += p.nbins;
     }
 }
 
@@ -148,7 +157,9 @@ __global__ void __launch_bounds__(1024) ada_plan(SegTable<MAXS> st, int S, int K
                                                  uint32_t* __restrict__ big) {
     __shared__ uint64_t scan[1024 / 32 + 1];
     __shared__ uint64_t carry[2];
+    __shared__ int s_nbig, s_big[64];  // the big-bin segments (all of them are scanned if more)
     if (threadIdx.x < 2) carry[threadIdx.x] = 0;
+    if (threadIdx.x == 0) s_nbig = 0;
     __syncthreads();
     for (int base = 0; base < S; base += 1024) {
         const int s = base + (int)threadIdx.x;
@@ -161,7 +172,8 @@ __global__ void __launch_bounds__(1024) ada_plan(SegTable<MAXS> st, int S, int K
         const uint64_t c0 = carry[0];
         __syncthreads();
         if (threadIdx.x == 0) carry[0] = c0 + tot;
-        const uint64_t ex_b = block_exclusive_scan<1024>(live && p.mode == kModeBig ? p.nbins : 0, scan, &tot);
+        const uint64_t ex_b =
+            block_exclusive_scan<1024>(live && (p.mode == kModeBig || p.bpw) ? p.nbins : 0, scan, &tot);
         const uint64_t c1 = carry[1];
         __syncthreads();
         if (threadIdx.x == 0) carry[1] = c1 + tot;
@@ -169,11 +181,24 @@ __global__ void __launch_bounds__(1024) ada_plan(SegTable<MAXS> st, int S, int K
             p.tile_off = (uint32_t)(c0 + ex_t);
             p.big_off = (uint32_t)(c1 + ex_b);
             plan[s] = p;
+            if (p.mode == kModeBig) {
+                const int q = atomicAdd(&s_nbig, 1);
+                if (q < 64) s_big[q] = s;
+            }
         }
         __syncthreads();
     }
     for (int k = threadIdx.x; k < K; k += 1024) pool_cnt[k] = 0;
-    for (uint64_t i = threadIdx.x; i < (uint64_t)K * big_per_learner; i += 1024) big[i] = 0;
+    // big-bin maxima are accumulated by atomicMax and start at 0 (warp-chunk
+    // bins are written once by ada_bins_warp)
+    __syncthreads();
+    const int nbig = s_nbig < 64 ? s_nbig : 64;
+    for (int q = 0; q < (s_nbig <= 64 ? nbig : S); ++q) {
+        const SegPlan p = plan[s_nbig <= 64 ? s_big[q] : q];
+        if (p.mode != kModeBig) continue;
+        for (int k = 0; k < K; ++k)
+            for (uint32_t b = threadIdx.x; b < p.nbins; b += 1024) big[(uint64_t)k * big_per_learner + p.big_off + b] = 0;
+    }
 }
 
 __device__ __forceinline__ int find_segment_by_tile(const SegPlan* plan, int S, uint32_t lt) {
@@ -269,6 +294,187 @@ __device__ __forceinline__ void select_tile(const float4 (&Gv)[4], const float4 
     }
 }
 
+// Warp-chunk tiles (4 <= L_T <= 512): warp w of a tile owns bins
+// [w bpw, (w + 1) bpw), at most 512 values, four float4 per lane.  It finds
+// their maxima from its registers (one bin: a warp reduction; several:
+// shared-memory atomicMax per float4 part), writes them to the bins array
+// (ada_scan averages them in fp64, so this pass needs no fp64), selects,
+// stores R <- G and ranks its candidates with warp scans; two block
+// barriers per tile give the warps their pool offsets.  Lean enough for four
+// CTAs per SM, so more loads stay in flight.
+__global__ void __launch_bounds__(NT, 4) ada_bins_warp(const SegPlan* __restrict__ plan, int S, uint64_t N,
+                                                       uint32_t tiles_per_learner, uint64_t total_tiles,
+                                                       const float* __restrict__ dW, float* __restrict__ R,
+                                                       uint32_t* __restrict__ bins, uint64_t bins_per_learner,
+                                                       uint32_t* __restrict__ pool_cnt, uint2* __restrict__ tile_tab,
+                                                       uint2* __restrict__ pool, uint64_t pool_cap) {
+    __shared__ uint32_t wbins[NT / 32][kWarpChunk / 4];
+    __shared__ uint32_t s_base, s_total;
+    __shared__ uint32_t wcnt[NT / 32], wbase[NT / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (uint32_t t = blockIdx.x; t < (uint32_t)total_tiles; t += gridDim.x) {
+        const uint32_t k = t / tiles_per_learner;
+        const uint32_t lt = t - k * tiles_per_learner;
+        const int s = find_segment_by_tile(plan, S, lt);
+        const SegPlan p = plan[s];
+        if (p.mode != kModeSmall || !p.bpw) continue;  // other tiles: ada_bins
+        const uint32_t tj = lt - p.tile_off;
+        const uint32_t start = tj * p.tile_len;
+        const uint32_t len = p.n - start < p.tile_len ? p.n - start : p.tile_len;
+        const uint64_t base = (uint64_t)k * N + p.off + start;
+        const uint32_t L = p.L;
+        const float* dWt = dW + base;
+        float* Rt = R + base;
+        const uint32_t bpw = p.bpw, cl = bpw * L, c0 = (uint32_t)warp * cl;
+        const uint32_t clen = c0 < len ? (len - c0 < cl ? len - c0 : cl) : 0u;
+        uint32_t* wb = wbins[warp];  // this warp's bin maxima (bpw <= 128)
+        const float* dWc = dWt + c0;
+        float* Rc = Rt + c0;
+        const bool cal = (((uintptr_t)dWc | (uintptr_t)Rc) & 15) == 0;
+        float4 Gv[4], Dv[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const uint32_t e = 4u * (lane + 32 * r);
+            if (cal && e + 4 <= clen) {
+                Dv[r] = __ldg(reinterpret_cast<const float4*>(dWc + e));
+                Gv[r] = *reinterpret_cast<const float4*>(Rc + e);
+            } else {
+                float* d4 = &Dv[r].x;
+                float* g4 = &Gv[r].x;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const bool in = e + j < clen;
+                    d4[j] = in ? __ldg(dWc + e + j) : 0.0f;
+                    g4[j] = in ? Rc[e + j] : 0.0f;
+                }
+            }
+            Gv[r].x = __fadd_rn(Gv[r].x, Dv[r].x);
+            Gv[r].y = __fadd_rn(Gv[r].y, Dv[r].y);
+            Gv[r].z = __fadd_rn(Gv[r].z, Dv[r].z);
+            Gv[r].w = __fadd_rn(Gv[r].w, Dv[r].w);
+        }
+        // bin maxima (|G|, NaN read as 0): one bin per chunk -> a warp
+        // reduction; several -> shared-memory atomicMax per float4 part
+        float m_one = 0.0f;
+        if (bpw == 1) {
+            float m = 0.0f;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const uint32_t e = 4u * (lane + 32 * r);
+                const float* g4 = &Gv[r].x;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (e + j < clen) m = fmaxf(m, fabsf(g4[j]));
+            }
+            m_one = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(m)));
+        } else {
+            for (uint32_t b = lane; b < bpw; b += 32) wb[b] = 0u;
+            __syncwarp();
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const uint32_t e = 4u * (lane + 32 * r);
+                if (e >= clen) continue;
+                const uint32_t b0 = bin_of(e, p.invL), cut = (b0 + 1) * L - e;
+                const float* g4 = &Gv[r].x;
+                float m0 = 0.0f, m1 = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float a = e + j < clen ? fabsf(g4[j]) : 0.0f;
+                    if ((uint32_t)j < cut) m0 = fmaxf(m0, a); else m1 = fmaxf(m1, a);
+                }
+                if (m0 > 0.0f) atomicMax(&wb[b0], __float_as_uint(m0));
+                if (cut < 4 && m1 > 0.0f) atomicMax(&wb[b0 + 1], __float_as_uint(m1));
+            }
+            __syncwarp();
+        }
+        // this chunk's bin maxima to the bins array (ada_scan averages them)
+        const uint32_t nbw = clen ? (clen + L - 1) / L : 0u;
+        uint32_t* gb = bins + (uint64_t)k * bins_per_learner + p.big_off + tj * p.bpt + (uint32_t)warp * bpw;
+        if (bpw == 1) {
+            if (lane == 0 && nbw) gb[0] = __float_as_uint(m_one);
+        } else {
+            for (uint32_t b = lane; b < nbw; b += 32) gb[b] = wb[b];
+        }
+        // selection (float compares, as the definition), R <- G, candidate counts per round
+        uint32_t flags = 0, packed = 0;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const uint32_t e = 4u * (lane + 32 * r);
+            const float* g4 = &Gv[r].x;
+            const float* d4 = &Dv[r].x;
+            if (e < clen) {
+                float gm0 = m_one, gm1 = m_one;
+                uint32_t cut = 4;
+                if (bpw != 1) {
+                    const uint32_t b0 = bin_of(e, p.invL);
+                    cut = (b0 + 1) * L - e;
+                    gm0 = __uint_as_float(wb[b0]);
+                    gm1 = cut < 4 && b0 + 1 < bpw ? __uint_as_float(wb[b0 + 1]) : gm0;
+                }
+                uint32_t f = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float gm = (uint32_t)j < cut ? gm0 : gm1;
+                    const bool sel = e + j < clen && fabsf(__fadd_rn(g4[j], d4[j])) >= gm && gm > 0.0f &&
+                                     g4[j] != 0.0f;
+                    f |= (uint32_t)sel << j;
+                }
+                flags |= f << (4 * r);
+                packed |= (uint32_t)__popc(f) << (8 * r);
+            }
+            if (cal && e + 4 <= clen) {
+                *reinterpret_cast<float4*>(Rc + e) = Gv[r];
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (e + j < clen) Rc[e + j] = g4[j];
+            }
+        }
+        // rank inside the warp: rounds in order, lanes in order (8 bits per round)
+        uint32_t incl = packed;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, incl, d);
+            if (lane >= d) incl += y;
+        }
+        const uint32_t wtot = __shfl_sync(kFull, incl, 31), excl = incl - packed;
+        const uint32_t W = (wtot & 0xFFu) + ((wtot >> 8) & 0xFFu) + ((wtot >> 16) & 0xFFu) + (wtot >> 24);
+        if (lane == 0) wcnt[warp] = W;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            uint32_t tot = 0;
+            for (int q = 0; q < NT / 32; ++q) {
+                wbase[q] = tot;
+                tot += wcnt[q];
+            }
+            uint32_t b = 0;
+            if (tot) b = atomicAdd(&pool_cnt[k], tot);
+            s_base = b;
+            s_total = tot;
+            tile_tab[t] = make_uint2(tot ? b : 0u, tot);
+        }
+        __syncthreads();
+        const uint32_t pb = s_base;
+        if (flags && (uint64_t)pb + s_total <= pool_cap) {
+            uint2* dst = pool + (uint64_t)k * pool_cap + pb + wbase[warp];
+            uint32_t rb = 0;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const uint32_t fr = (flags >> (4 * r)) & 0xFu;
+                uint32_t pos = rb + ((excl >> (8 * r)) & 0xFFu);
+                rb += (wtot >> (8 * r)) & 0xFFu;
+                if (!fr) continue;
+                const uint32_t e = 4u * (lane + 32 * r);
+                const float* g4 = &Gv[r].x;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if ((fr >> j) & 1u) dst[pos++] = make_uint2(p.off + start + c0 + e + j, __float_as_uint(g4[j]));
+            }
+        }
+
+    }
+}
+
 __global__ void __launch_bounds__(NT, 3) ada_bins(const SegPlan* __restrict__ plan, int S, uint64_t N,
                                                   uint32_t tiles_per_learner, uint64_t total_tiles,
                                                   const float* __restrict__ dW, float* __restrict__ R,
@@ -297,6 +503,8 @@ __global__ void __launch_bounds__(NT, 3) ada_bins(const SegPlan* __restrict__ pl
         const float* dWt = dW + base;
         float* Rt = R + base;
         const bool aligned = (((uintptr_t)dWt | (uintptr_t)Rt) & 15) == 0;  // 128-bit accesses
+
+        if (small && p.bpw) continue;  // warp-chunk tiles: ada_bins_warp
 
         // 1. G = R + dW (registers) and |G| keys to shared memory
         float4 Gv[4], Dv[4];
@@ -439,21 +647,34 @@ __global__ void __launch_bounds__(NT) ada_scan(const SegPlan* __restrict__ plan,
         if (j < p.ntiles) tile_rel[t0 + j] = (uint32_t)(run + ex);
         run += tot;
     }
+    // bins kept in the bins array (big bins, warp chunks): every thread adds
+    // a strided share in fp64 (plain adds: at most nbins / 256 per thread),
+    // then a fixed tree; the error stays far below the fp32 scale's rounding
+    __shared__ double s_wsum[NT / 32];
+    double bins_sum = 0.0;
+    const bool in_bins = p.mode == kModeBig || p.bpw;
+    if (in_bins) {
+        const uint32_t* bm = big + (uint64_t)k * big_per_learner + p.big_off;
+        double su = 0.0;
+        for (uint32_t b = threadIdx.x; b < p.nbins; b += NT) su = __dadd_rn(su, (double)__uint_as_float(bm[b]));
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) su = __dadd_rn(su, __shfl_down_sync(kFull, su, d));
+        if (lane == 0) s_wsum[warp] = su;
+        __syncthreads();
+        for (int q = 0; q < NT / 32; ++q) bins_sum = __dadd_rn(bins_sum, s_wsum[q]);
+    }
     if (warp == 0) {
-        // compensated sum of the bin maxima in bin order, 32 contiguous runs
+        // compensated sum of the tiles' sums of bin maxima in bin order, 32 contiguous runs
         double sm = 0.0, cm = 0.0;
-        if (p.mode == kModeSmall) {
+        if (p.mode == kModeSmall && !p.bpw) {
             const uint32_t per = (p.ntiles + 31) / 32;
             for (uint32_t j = lane * per; j < p.ntiles && j < (lane + 1) * per; ++j) {
                 const double2 ts = tile_sum[t0 + j];
                 csum_add(sm, cm, ts.x);
                 cm = __dadd_rn(cm, ts.y);
             }
-        } else if (p.mode == kModeBig) {
-            const uint32_t* bm = big + (uint64_t)k * big_per_learner + p.big_off;
-            const uint32_t per = (p.nbins + 31) / 32;
-            for (uint32_t b = lane * per; b < p.nbins && b < (lane + 1) * per; ++b)
-                csum_add(sm, cm, (double)__uint_as_float(bm[b]));
+        } else if (in_bins && lane == 0) {
+            sm = bins_sum;
         }
         double S0 = 0.0, C0 = 0.0;
         for (int l = 0; l < 32; ++l) {
@@ -583,13 +804,29 @@ int adacomp_launch(const int64_t* off, int S, const int32_t* lt, int K, const fl
         if ((rc = check_launch("ada_plan"))) return rc;
     }
     const uint64_t grid_cap = (uint64_t)sm_count() * 3;
-    if (hp.big_per_learner > 0 && T > 0) {
+    bool any_warp = false, any_other = false, any_big = false;
+    for (int s = 0; s < S; ++s) {
+        SegPlan sp;
+        seg_fields((uint32_t)(off[s + 1] - off[s]), (uint32_t)lt[s], &sp);
+        if (sp.mode == kModeEmpty) continue;
+        (sp.mode == kModeSmall && sp.bpw ? any_warp : any_other) = true;
+        any_big |= sp.mode == kModeBig;
+    }
+    if (any_big && T > 0) {
         LaunchScope ls("ada_bigmax", stream);
         ada_bigmax<<<(unsigned)(T < grid_cap ? T : grid_cap), NT, 0, stream>>>(
             w.plan, S, N, (uint32_t)hp.tiles_per_learner, T, dW, R, w.big, hp.big_per_learner);
         if ((rc = check_launch("ada_bigmax"))) return rc;
     }
-    if (T > 0) {
+    if (T > 0 && any_warp) {
+        LaunchScope ls("ada_bins_warp", stream);
+        const uint64_t wgrid = (uint64_t)sm_count() * 4;
+        ada_bins_warp<<<(unsigned)(T < wgrid ? T : wgrid), NT, 0, stream>>>(
+            w.plan, S, N, (uint32_t)hp.tiles_per_learner, T, dW, R, w.big, hp.big_per_learner, w.pool_cnt,
+            w.tile_tab, w.pool, (uint64_t)cap);
+        if ((rc = check_launch("ada_bins_warp"))) return rc;
+    }
+    if (T > 0 && any_other) {
         LaunchScope ls("ada_bins", stream);
         ada_bins<<<(unsigned)(T < grid_cap ? T : grid_cap), NT, 0, stream>>>(
             w.plan, S, N, (uint32_t)hp.tiles_per_learner, T, dW, R, w.big, hp.big_per_learner, w.pool_cnt,
