@@ -8,19 +8,24 @@
 // sign(G) * scale and the residue keeps what was not sent.
 //
 // Launch sequence (caller's stream, no host sync):
-//   ada_plan     one CTA: per-segment plan (bins, tiles), zeroes counters
-//   [ada_bigmax] only for segments with L_T > 4096: bin maxima via atomics
-//   ada_bins     the bandwidth-bound pass: 128-bit loads of R and dW, G = R+dW,
-//                bin maxima in shared memory (warp-aggregated atomicMax on the
-//                |G| bit patterns), selection, R <- G stored once, ordered
-//                compaction of the selected (index, G) into the learner's
-//                pool, and a compensated fp64 sum of the tile's bin maxima
-//   ada_scan     one CTA per (learner, segment): prefix of the tile counts in
-//                index order, the segment's count and its scale
-//   ada_emit     one warp per tile: writes (index, sign(G)*scale) at its
-//                ordered slot and fixes the residue R = G - sign(G)*scale.
+//   ada_plan      one CTA: per-segment plan (bins, tiles, emit groups), zeroes
+//                 the big-bin maxima
+//   [ada_bigmax]  only for segments with L_T > 4096: bin maxima via atomics
+//   ada_bins_warp the bandwidth-bound pass for 4 <= L_T <= 512: a tile is one
+//                 warp's chunk of whole bins (<= 512 values) in registers;
+//                 G = R + dW, bin maxima, selection, R <- G stored once, the
+//                 selected (index, G) written in index order into the pool
+//                 slots of the chunk's own index range
+//   [ada_bins]    the same pass for other bin lengths, one 4096-value tile per
+//                 CTA (bin maxima in shared memory; fp64 tile sums)
+//   ada_scan      one CTA per (learner, segment): output slots of the emit
+//                 groups, the segment's count and its scale
+//   ada_emit      one warp per group of 8 tiles: writes (index, sign(G)*scale)
+//                 at its ordered slot and fixes the residue R = G - sign(G)*scale.
 // Tiles hold whole bins (bins of L_T <= 4096 never straddle tiles), so a
-// bin's maximum is final inside one CTA and the first pass is single-read.
+// bin's maximum is final inside one warp or CTA and the first pass is
+// single-read.  Every tile owns the pool slots of its index range, so no
+// counter is shared between CTAs and the result is deterministic.
 #include <math.h>
 
 #include "common.cuh"
@@ -43,8 +48,11 @@ struct SegPlan {
     uint32_t tile_off;  // first tile within a learner
     uint32_t big_off;   // first big-bin slot within a learner (big mode)
     float invL;         // fp32 1/L: bin = floor((e + 0.5) * invL) is exact for e < 4096
-    uint32_t bpw;       // warp chunks: bins per warp (4 <= L <= 512; a tile is 8 chunks), else 0
+    uint32_t bpw;       // warp chunks: bins per chunk (4 <= L <= 512; a tile is one chunk), else 0
+    uint32_t grp_off;   // first emit group (kGroup consecutive tiles) within a learner
 };
+
+constexpr uint32_t kGroup = 8;  // tiles per ada_emit work item
 
 template <int MAXS>
 struct SegTable {
@@ -73,7 +81,7 @@ __host__ __device__ inline void seg_fields(uint32_t n, uint32_t L, SegPlan* p) {
             uint32_t bpw = kWarpChunk / L;
             if (bpw >= g) bpw -= bpw % g;
             p->bpw = bpw;
-            bpt = (NT / 32) * bpw;
+            bpt = bpw;
         } else {
             bpt = kTileMax / L;
             if (bpt >= g) bpt -= bpt % g;
@@ -91,32 +99,34 @@ __host__ __device__ inline void seg_fields(uint32_t n, uint32_t L, SegPlan* p) {
 struct HostPlan {
     uint64_t tiles_per_learner;
     uint64_t big_per_learner;
+    uint64_t groups_per_learner;
 };
 
 void host_plan(const int64_t* off, const int32_t* lt, int S, HostPlan* hp) {
     hp->tiles_per_learner = 0;
     hp->big_per_learner = 0;
+    hp->groups_per_learner = 0;
     for (int s = 0; s < S; ++s) {
         SegPlan p;
         seg_fields((uint32_t)(off[s + 1] - off[s]), (uint32_t)lt[s], &p);
         hp->tiles_per_learner += p.ntiles;
+        hp->groups_per_learner += (p.ntiles + kGroup - 1) / kGroup;
         if (p.mode == kModeBig || p.bpw) hp->big_per_learner += p.nbins;
     }
 }
 
 struct Workspace {
     SegPlan* plan;
-    uint32_t* pool_cnt;
-    uint2* tile_tab;     // (pool slot, count)
+    uint2* tile_tab;     // (pool slot = the tile's first index, count)
     double2* tile_sum;   // compensated sum of the tile's bin maxima
-    uint32_t* tile_rel;  // first output slot of the tile within its segment
+    uint32_t* grp_rel;   // first output slot of the emit group within its segment
     uint32_t* big;       // bin maxima (|G| bits) of big-mode segments
-    uint2* pool;         // (index within the learner, G bits)
+    uint2* pool;         // (index within the learner, G bits); a tile's entries sit at its own index range
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-size_t layout(int S, int K, int64_t cap, const HostPlan& hp, void* base, Workspace* w) {
+size_t layout(int S, int K, int64_t off_total, const HostPlan& hp, void* base, Workspace* w) {
     size_t o = 0;
     auto take = [&](size_t bytes) {
         const size_t at = o;
@@ -124,20 +134,19 @@ size_t layout(int S, int K, int64_t cap, const HostPlan& hp, void* base, Workspa
         return at;
     };
     const uint64_t T = (uint64_t)K * hp.tiles_per_learner;
+    const uint64_t N = (uint64_t)off_total;
     const size_t o_plan = take(sizeof(SegPlan) * (size_t)S);
-    const size_t o_cnt = take(sizeof(uint32_t) * (size_t)K);
     const size_t o_tt = take(sizeof(uint2) * T);
     const size_t o_ts = take(sizeof(double2) * T);
-    const size_t o_tr = take(sizeof(uint32_t) * T);
+    const size_t o_tr = take(sizeof(uint32_t) * (size_t)K * hp.groups_per_learner);
     const size_t o_big = take(sizeof(uint32_t) * (size_t)K * hp.big_per_learner);
-    const size_t o_pool = take(sizeof(uint2) * (size_t)K * (size_t)cap);
+    const size_t o_pool = take(sizeof(uint2) * (size_t)K * (size_t)N);  // one slot per element: no shared counter
     if (w) {
         char* b = (char*)base;
         w->plan = (SegPlan*)(b + o_plan);
-        w->pool_cnt = (uint32_t*)(b + o_cnt);
         w->tile_tab = (uint2*)(b + o_tt);
         w->tile_sum = (double2*)(b + o_ts);
-        w->tile_rel = (uint32_t*)(b + o_tr);
+        w->grp_rel = (uint32_t*)(b + o_tr);
         w->big = (uint32_t*)(b + o_big);
         w->pool = (uint2*)(b + o_pool);
     }
@@ -153,12 +162,11 @@ __device__ __forceinline__ void csum_add(double& s, double& c, double x) {
 
 template <int MAXS>
 __global__ void __launch_bounds__(1024) ada_plan(SegTable<MAXS> st, int S, int K, uint64_t big_per_learner,
-                                                 SegPlan* __restrict__ plan, uint32_t* __restrict__ pool_cnt,
-                                                 uint32_t* __restrict__ big) {
+                                                 SegPlan* __restrict__ plan, uint32_t* __restrict__ big) {
     __shared__ uint64_t scan[1024 / 32 + 1];
-    __shared__ uint64_t carry[2];
+    __shared__ uint64_t carry[3];
     __shared__ int s_nbig, s_big[64];  // the big-bin segments (all of them are scanned if more)
-    if (threadIdx.x < 2) carry[threadIdx.x] = 0;
+    if (threadIdx.x < 3) carry[threadIdx.x] = 0;
     if (threadIdx.x == 0) s_nbig = 0;
     __syncthreads();
     for (int base = 0; base < S; base += 1024) {
@@ -177,9 +185,14 @@ __global__ void __launch_bounds__(1024) ada_plan(SegTable<MAXS> st, int S, int K
         const uint64_t c1 = carry[1];
         __syncthreads();
         if (threadIdx.x == 0) carry[1] = c1 + tot;
+        const uint64_t ex_g = block_exclusive_scan<1024>(live ? (p.ntiles + kGroup - 1) / kGroup : 0, scan, &tot);
+        const uint64_t c2 = carry[2];
+        __syncthreads();
+        if (threadIdx.x == 0) carry[2] = c2 + tot;
         if (live) {
             p.tile_off = (uint32_t)(c0 + ex_t);
             p.big_off = (uint32_t)(c1 + ex_b);
+            p.grp_off = (uint32_t)(c2 + ex_g);
             plan[s] = p;
             if (p.mode == kModeBig) {
                 const int q = atomicAdd(&s_nbig, 1);
@@ -188,7 +201,6 @@ __global__ void __launch_bounds__(1024) ada_plan(SegTable<MAXS> st, int S, int K
         }
         __syncthreads();
     }
-    for (int k = threadIdx.x; k < K; k += 1024) pool_cnt[k] = 0;
     // big-bin maxima are accumulated by atomicMax and start at 0 (warp-chunk
     // bins are written once by ada_bins_warp)
     __syncthreads();
@@ -294,118 +306,119 @@ __device__ __forceinline__ void select_tile(const float4 (&Gv)[4], const float4 
     }
 }
 
-// Warp-chunk tiles (4 <= L_T <= 512): warp w of a tile owns bins
-// [w bpw, (w + 1) bpw), at most 512 values, four float4 per lane.  It finds
-// their maxima from its registers (one bin: a warp reduction; several:
+// Warp-chunk tiles (4 <= L_T <= 512): a tile is one warp's chunk of bpw
+// whole bins, at most 512 values, four float4 per lane.  Warps run
+// independently, with no block barrier and no shared counter: a warp finds
+// its bins' maxima from its registers (one bin: a warp reduction; several:
 // shared-memory atomicMax per float4 part), writes them to the bins array
-// (ada_scan averages them in fp64, so this pass needs no fp64), selects,
-// stores R <- G and ranks its candidates with warp scans; two block
-// barriers per tile give the warps their pool offsets.  Lean enough for four
-// CTAs per SM, so more loads stay in flight.
+// (ada_scan averages them in fp64), selects, stores R <- G and writes its
+// candidates in index order into the pool slots of its own index range.
+// Lanes past the chunk's end hold 0: G = 0 never raises a maximum and is
+// never sent, so only the loads and stores test bounds.  A warp walks the
+// tiles with a stride of all warps, keeping its segment's plan in registers.
 __global__ void __launch_bounds__(NT, 4) ada_bins_warp(const SegPlan* __restrict__ plan, int S, uint64_t N,
                                                        uint32_t tiles_per_learner, uint64_t total_tiles,
                                                        const float* __restrict__ dW, float* __restrict__ R,
                                                        uint32_t* __restrict__ bins, uint64_t bins_per_learner,
-                                                       uint32_t* __restrict__ pool_cnt, uint2* __restrict__ tile_tab,
-                                                       uint2* __restrict__ pool, uint64_t pool_cap) {
+                                                       uint2* __restrict__ tile_tab, uint2* __restrict__ pool) {
     __shared__ uint32_t wbins[NT / 32][kWarpChunk / 4];
-    __shared__ uint32_t s_base, s_total;
-    __shared__ uint32_t wcnt[NT / 32], wbase[NT / 32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (uint32_t t = blockIdx.x; t < (uint32_t)total_tiles; t += gridDim.x) {
-        const uint32_t k = t / tiles_per_learner;
-        const uint32_t lt = t - k * tiles_per_learner;
-        const int s = find_segment_by_tile(plan, S, lt);
-        const SegPlan p = plan[s];
-        if (p.mode != kModeSmall || !p.bpw) continue;  // other tiles: ada_bins
-        const uint32_t tj = lt - p.tile_off;
-        const uint32_t start = tj * p.tile_len;
-        const uint32_t len = p.n - start < p.tile_len ? p.n - start : p.tile_len;
-        const uint64_t base = (uint64_t)k * N + p.off + start;
-        const uint32_t L = p.L;
-        const float* dWt = dW + base;
-        float* Rt = R + base;
-        const uint32_t bpw = p.bpw, cl = bpw * L, c0 = (uint32_t)warp * cl;
-        const uint32_t clen = c0 < len ? (len - c0 < cl ? len - c0 : cl) : 0u;
-        uint32_t* wb = wbins[warp];  // this warp's bin maxima (bpw <= 128)
-        const float* dWc = dWt + c0;
-        float* Rc = Rt + c0;
-        const bool cal = (((uintptr_t)dWc | (uintptr_t)Rc) & 15) == 0;
-        float4 Gv[4], Dv[4];
+    const uint32_t nw = gridDim.x * (NT / 32), T = (uint32_t)total_tiles;  // T < 2^32 (checked by the host)
+    uint32_t t = blockIdx.x * (NT / 32) + warp;
+    if (t >= T) return;
+    uint32_t k = t / tiles_per_learner, lt = t - k * tiles_per_learner;
+    // the fields of the current segment that a chunk needs (bpw = 0: not a warp-chunk segment)
+    struct {
+        uint32_t off, n, L, bpw, tile_len, tile_off, big_off, next_off;
+        float invL;
+    } p;
+    auto load_seg = [&](uint32_t at) {
+        const int s = find_segment_by_tile(plan, S, at);
+        const SegPlan q = plan[s];
+        p.off = q.off, p.n = q.n, p.L = q.L, p.bpw = q.mode == kModeSmall ? q.bpw : 0u;
+        p.tile_len = q.tile_len, p.tile_off = q.tile_off, p.big_off = q.big_off, p.invL = q.invL;
+        p.next_off = s + 1 < S ? __ldg(&plan[s + 1].tile_off) : tiles_per_learner;
+    };
+    load_seg(lt);
+    uint32_t* wb = wbins[warp];  // this warp's bin maxima (bpw <= 128)
+    for (;;) {
+        if (p.bpw) {  // other tiles: ada_bins
+            const uint32_t tj = lt - p.tile_off;
+            const uint32_t start = tj * p.tile_len;
+            const uint32_t clen = p.n - start < p.tile_len ? p.n - start : p.tile_len;
+            const uint32_t rel = p.off + start;  // the chunk's first index within the learner
+            const uint64_t base = (uint64_t)k * N + rel;
+            const float* dWc = dW + base;
+            float* Rc = R + base;
+            const bool cal = (((uintptr_t)dWc | (uintptr_t)Rc) & 15) == 0;
+            float4 Gv[4], Dv[4];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const uint32_t e = 4u * (lane + 32 * r);
-            if (cal && e + 4 <= clen) {
-                Dv[r] = __ldg(reinterpret_cast<const float4*>(dWc + e));
-                Gv[r] = *reinterpret_cast<const float4*>(Rc + e);
+            for (int r = 0; r < 4; ++r) {
+                const uint32_t e = 4u * (lane + 32 * r);
+                if (cal && e + 4 <= clen) {
+                    Dv[r] = __ldg(reinterpret_cast<const float4*>(dWc + e));
+                    Gv[r] = *reinterpret_cast<const float4*>(Rc + e);
+                } else {
+                    float* d4 = &Dv[r].x;
+                    float* g4 = &Gv[r].x;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const bool in = e + j < clen;
+                        d4[j] = in ? __ldg(dWc + e + j) : 0.0f;
+                        g4[j] = in ? Rc[e + j] : 0.0f;
+                    }
+                }
+                Gv[r].x = __fadd_rn(Gv[r].x, Dv[r].x);
+                Gv[r].y = __fadd_rn(Gv[r].y, Dv[r].y);
+                Gv[r].z = __fadd_rn(Gv[r].z, Dv[r].z);
+                Gv[r].w = __fadd_rn(Gv[r].w, Dv[r].w);
+            }
+            // bin maxima of |G| (fmaxf skips a NaN, so NaN reads as 0)
+            const uint32_t bpw = p.bpw, L = p.L;
+            uint32_t* gb = bins + (uint64_t)k * bins_per_learner + p.big_off + tj * bpw;
+            float m_one = 0.0f;
+            if (bpw == 1) {
+                float m = 0.0f;
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    m = fmaxf(m, fmaxf(fmaxf(fabsf(Gv[r].x), fabsf(Gv[r].y)), fmaxf(fabsf(Gv[r].z), fabsf(Gv[r].w))));
+                }
+                m_one = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(m)));
+                if (lane == 0) gb[0] = __float_as_uint(m_one);
             } else {
-                float* d4 = &Dv[r].x;
-                float* g4 = &Gv[r].x;
+                for (uint32_t b = lane; b < bpw; b += 32) wb[b] = 0u;
+                __syncwarp();
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const bool in = e + j < clen;
-                    d4[j] = in ? __ldg(dWc + e + j) : 0.0f;
-                    g4[j] = in ? Rc[e + j] : 0.0f;
+                for (int r = 0; r < 4; ++r) {
+                    const uint32_t e = 4u * (lane + 32 * r);
+                    if (e >= clen) continue;
+                    const uint32_t b0 = bin_of(e, p.invL), cut = (b0 + 1) * L - e;
+                    const float* g4 = &Gv[r].x;
+                    float m0 = 0.0f, m1 = 0.0f;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float a = fabsf(g4[j]);
+                        if ((uint32_t)j < cut) m0 = fmaxf(m0, a); else m1 = fmaxf(m1, a);
+                    }
+                    if (m0 > 0.0f) atomicMax(&wb[b0], __float_as_uint(m0));
+                    if (m1 > 0.0f) atomicMax(&wb[b0 + 1], __float_as_uint(m1));  // only past a bin edge
                 }
+                __syncwarp();
+                const uint32_t nbw = bin_of(clen - 1, p.invL) + 1;
+                for (uint32_t b = lane; b < nbw; b += 32) gb[b] = wb[b];
             }
-            Gv[r].x = __fadd_rn(Gv[r].x, Dv[r].x);
-            Gv[r].y = __fadd_rn(Gv[r].y, Dv[r].y);
-            Gv[r].z = __fadd_rn(Gv[r].z, Dv[r].z);
-            Gv[r].w = __fadd_rn(Gv[r].w, Dv[r].w);
-        }
-        // bin maxima (|G|, NaN read as 0): one bin per chunk -> a warp
-        // reduction; several -> shared-memory atomicMax per float4 part
-        float m_one = 0.0f;
-        if (bpw == 1) {
-            float m = 0.0f;
+            // selection (float compares, as the definition: |G + dW| >= bin max
+            // and G != 0; a bin max of 0 leaves only G = 0 or NaN, never
+            // sent), R <- G, candidate counts per round
+            uint32_t flags = 0, packed = 0;
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const uint32_t e = 4u * (lane + 32 * r);
                 const float* g4 = &Gv[r].x;
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (e + j < clen) m = fmaxf(m, fabsf(g4[j]));
-            }
-            m_one = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(m)));
-        } else {
-            for (uint32_t b = lane; b < bpw; b += 32) wb[b] = 0u;
-            __syncwarp();
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const uint32_t e = 4u * (lane + 32 * r);
-                if (e >= clen) continue;
-                const uint32_t b0 = bin_of(e, p.invL), cut = (b0 + 1) * L - e;
-                const float* g4 = &Gv[r].x;
-                float m0 = 0.0f, m1 = 0.0f;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float a = e + j < clen ? fabsf(g4[j]) : 0.0f;
-                    if ((uint32_t)j < cut) m0 = fmaxf(m0, a); else m1 = fmaxf(m1, a);
-                }
-                if (m0 > 0.0f) atomicMax(&wb[b0], __float_as_uint(m0));
-                if (cut < 4 && m1 > 0.0f) atomicMax(&wb[b0 + 1], __float_as_uint(m1));
-            }
-            __syncwarp();
-        }
-        // this chunk's bin maxima to the bins array (ada_scan averages them)
-        const uint32_t nbw = clen ? (clen + L - 1) / L : 0u;
-        uint32_t* gb = bins + (uint64_t)k * bins_per_learner + p.big_off + tj * p.bpt + (uint32_t)warp * bpw;
-        if (bpw == 1) {
-            if (lane == 0 && nbw) gb[0] = __float_as_uint(m_one);
-        } else {
-            for (uint32_t b = lane; b < nbw; b += 32) gb[b] = wb[b];
-        }
-        // selection (float compares, as the definition), R <- G, candidate counts per round
-        uint32_t flags = 0, packed = 0;
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const uint32_t e = 4u * (lane + 32 * r);
-            const float* g4 = &Gv[r].x;
-            const float* d4 = &Dv[r].x;
-            if (e < clen) {
+                const float* d4 = &Dv[r].x;
                 float gm0 = m_one, gm1 = m_one;
                 uint32_t cut = 4;
-                if (bpw != 1) {
+                if (bpw != 1 && e < clen) {
                     const uint32_t b0 = bin_of(e, p.invL);
                     cut = (b0 + 1) * L - e;
                     gm0 = __uint_as_float(wb[b0]);
@@ -415,63 +428,57 @@ __global__ void __launch_bounds__(NT, 4) ada_bins_warp(const SegPlan* __restrict
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const float gm = (uint32_t)j < cut ? gm0 : gm1;
-                    const bool sel = e + j < clen && fabsf(__fadd_rn(g4[j], d4[j])) >= gm && gm > 0.0f &&
-                                     g4[j] != 0.0f;
+                    const bool sel = fabsf(__fadd_rn(g4[j], d4[j])) >= gm && g4[j] != 0.0f;
                     f |= (uint32_t)sel << j;
                 }
                 flags |= f << (4 * r);
                 packed |= (uint32_t)__popc(f) << (8 * r);
-            }
-            if (cal && e + 4 <= clen) {
-                *reinterpret_cast<float4*>(Rc + e) = Gv[r];
-            } else {
+                if (cal && e + 4 <= clen) {
+                    *reinterpret_cast<float4*>(Rc + e) = Gv[r];
+                } else {
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (e + j < clen) Rc[e + j] = g4[j];
+                    for (int j = 0; j < 4; ++j)
+                        if (e + j < clen) Rc[e + j] = g4[j];
+                }
             }
-        }
-        // rank inside the warp: rounds in order, lanes in order (8 bits per round)
-        uint32_t incl = packed;
+            // rank inside the chunk: rounds in order, lanes in order (8 bits per round)
+            uint32_t incl = packed;
 #pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const uint32_t y = __shfl_up_sync(kFull, incl, d);
-            if (lane >= d) incl += y;
-        }
-        const uint32_t wtot = __shfl_sync(kFull, incl, 31), excl = incl - packed;
-        const uint32_t W = (wtot & 0xFFu) + ((wtot >> 8) & 0xFFu) + ((wtot >> 16) & 0xFFu) + (wtot >> 24);
-        if (lane == 0) wcnt[warp] = W;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            uint32_t tot = 0;
-            for (int q = 0; q < NT / 32; ++q) {
-                wbase[q] = tot;
-                tot += wcnt[q];
+            for (int d = 1; d < 32; d <<= 1) {
+                const uint32_t y = __shfl_up_sync(kFull, incl, d);
+                if (lane >= d) incl += y;
             }
-            uint32_t b = 0;
-            if (tot) b = atomicAdd(&pool_cnt[k], tot);
-            s_base = b;
-            s_total = tot;
-            tile_tab[t] = make_uint2(tot ? b : 0u, tot);
-        }
-        __syncthreads();
-        const uint32_t pb = s_base;
-        if (flags && (uint64_t)pb + s_total <= pool_cap) {
-            uint2* dst = pool + (uint64_t)k * pool_cap + pb + wbase[warp];
-            uint32_t rb = 0;
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const uint32_t fr = (flags >> (4 * r)) & 0xFu;
-                uint32_t pos = rb + ((excl >> (8 * r)) & 0xFFu);
-                rb += (wtot >> (8 * r)) & 0xFFu;
-                if (!fr) continue;
-                const uint32_t e = 4u * (lane + 32 * r);
-                const float* g4 = &Gv[r].x;
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if ((fr >> j) & 1u) dst[pos++] = make_uint2(p.off + start + c0 + e + j, __float_as_uint(g4[j]));
+            const uint32_t wtot = __shfl_sync(kFull, incl, 31), excl = incl - packed;
+            if (lane == 0) {
+                const uint32_t W = (wtot & 0xFFu) + ((wtot >> 8) & 0xFFu) + ((wtot >> 16) & 0xFFu) + (wtot >> 24);
+                tile_tab[(uint64_t)k * tiles_per_learner + lt] = make_uint2(rel, W);
             }
+            if (flags) {
+                uint2* dst = pool + base;
+                uint32_t rb = 0;
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const uint32_t fr = (flags >> (4 * r)) & 0xFu;
+                    uint32_t pos = rb + ((excl >> (8 * r)) & 0xFFu);
+                    rb += (wtot >> (8 * r)) & 0xFFu;
+                    if (!fr) continue;
+                    const uint32_t e = 4u * (lane + 32 * r);
+                    const float* g4 = &Gv[r].x;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if ((fr >> j) & 1u) dst[pos++] = make_uint2(rel + e + j, __float_as_uint(g4[j]));
+                }
+            }
+            __syncwarp();  // wb is rewritten by the next chunk
         }
-
+        if (T - t <= nw) break;
+        t += nw;
+        lt += nw;
+        while (lt >= tiles_per_learner) {
+            lt -= tiles_per_learner;
+            ++k;
+        }
+        if (lt < p.tile_off || lt >= p.next_off) load_seg(lt);
     }
 }
 
@@ -479,13 +486,11 @@ __global__ void __launch_bounds__(NT, 3) ada_bins(const SegPlan* __restrict__ pl
                                                   uint32_t tiles_per_learner, uint64_t total_tiles,
                                                   const float* __restrict__ dW, float* __restrict__ R,
                                                   const uint32_t* __restrict__ big, uint64_t big_per_learner,
-                                                  uint32_t* __restrict__ pool_cnt, uint2* __restrict__ tile_tab,
-                                                  double2* __restrict__ tile_sum, uint2* __restrict__ pool,
-                                                  uint64_t pool_cap) {
+                                                  uint2* __restrict__ tile_tab, double2* __restrict__ tile_sum,
+                                                  uint2* __restrict__ pool) {
     __shared__ __align__(16) uint32_t gk[kTileMax];  // |G| bit patterns of the tile
     __shared__ uint32_t bmax[kTileMax];               // bin maxima (|G| bits)
     __shared__ uint64_t scan[NT / 32 + 1];
-    __shared__ uint32_t s_base;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (uint32_t t = blockIdx.x; t < (uint32_t)total_tiles; t += gridDim.x) {
         const uint32_t k = t / tiles_per_learner;
@@ -589,7 +594,7 @@ __global__ void __launch_bounds__(NT, 3) ada_bins(const SegPlan* __restrict__ pl
             }
         }
         if (!__syncthreads_or(flags != 0)) {
-            if (threadIdx.x == 0) tile_tab[t] = make_uint2(0u, 0u);
+            if (threadIdx.x == 0) tile_tab[t] = make_uint2(p.off + start, 0u);
             continue;
         }
         uint64_t total;
@@ -600,15 +605,10 @@ __global__ void __launch_bounds__(NT, 3) ada_bins(const SegPlan* __restrict__ pl
             round_base[r] = cnt_total;
             cnt_total += (uint32_t)(total >> (16 * r)) & 0xFFFFu;
         }
-        if (threadIdx.x == 0) {
-            const uint32_t b = atomicAdd(&pool_cnt[k], cnt_total);
-            s_base = b;
-            tile_tab[t] = make_uint2(b, cnt_total);
-        }
-        __syncthreads();
-        const uint32_t pb = s_base;
-        if ((uint64_t)pb + cnt_total <= pool_cap && flags) {
-            uint2* dst = pool + (uint64_t)k * pool_cap + pb;
+        // the tile's entries go to the pool slots of its own index range
+        if (threadIdx.x == 0) tile_tab[t] = make_uint2(p.off + start, cnt_total);
+        if (flags) {
+            uint2* dst = pool + base;
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const uint32_t fr = (flags >> (4 * r)) & 0xFu;
@@ -625,12 +625,13 @@ __global__ void __launch_bounds__(NT, 3) ada_bins(const SegPlan* __restrict__ pl
     }
 }
 
-// One CTA per (learner, segment): output slots of the tiles in index order,
-// the segment's count, and its scale = mean of the bin maxima.
+// One CTA per (learner, segment): output slots of the emit groups in index
+// order, the segment's count, and its scale = mean of the bin maxima.
 __global__ void __launch_bounds__(NT) ada_scan(const SegPlan* __restrict__ plan, int S,
                                                uint32_t tiles_per_learner, const uint2* __restrict__ tile_tab,
                                                const double2* __restrict__ tile_sum, const uint32_t* __restrict__ big,
-                                               uint64_t big_per_learner, uint32_t* __restrict__ tile_rel,
+                                               uint64_t big_per_learner, uint32_t groups_per_learner,
+                                               uint32_t* __restrict__ grp_rel,
                                                int64_t* __restrict__ counts, float* __restrict__ scales) {
     __shared__ uint64_t scan[NT / 32 + 1];
     const int unit = blockIdx.x;
@@ -638,13 +639,26 @@ __global__ void __launch_bounds__(NT) ada_scan(const SegPlan* __restrict__ plan,
     const SegPlan p = plan[s];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint64_t t0 = (uint64_t)k * tiles_per_learner + p.tile_off;
+    // output slots of the emit groups (kGroup consecutive tiles; ada_emit
+    // ranks the tiles inside a group), two groups per thread per round
     uint64_t run = 0;
-    for (uint32_t jb = 0; jb < p.ntiles; jb += NT) {
-        const uint32_t j = jb + threadIdx.x;
-        const uint32_t c = j < p.ntiles ? tile_tab[t0 + j].y : 0u;
+    const uint32_t ng = (p.ntiles + kGroup - 1) / kGroup;
+    uint32_t* gr = grp_rel + (uint64_t)k * groups_per_learner + p.grp_off;
+    for (uint32_t gb = 0; gb < ng; gb += 2 * NT) {
+        const uint32_t g0 = gb + 2 * threadIdx.x;
+        uint32_t c[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            c[q] = 0;
+            if (g0 + q < ng) {
+                const uint32_t j0 = (g0 + q) * kGroup, j1 = j0 + kGroup < p.ntiles ? j0 + kGroup : p.ntiles;
+                for (uint32_t j = j0; j < j1; ++j) c[q] += tile_tab[t0 + j].y;
+            }
+        }
         uint64_t tot;
-        const uint64_t ex = block_exclusive_scan<NT>(c, scan, &tot);
-        if (j < p.ntiles) tile_rel[t0 + j] = (uint32_t)(run + ex);
+        const uint64_t at = run + block_exclusive_scan<NT>(c[0] + c[1], scan, &tot);
+        if (g0 < ng) gr[g0] = (uint32_t)at;
+        if (g0 + 1 < ng) gr[g0 + 1] = (uint32_t)(at + c[0]);
         run += tot;
     }
     // bins kept in the bins array (big bins, warp chunks): every thread adds
@@ -690,30 +704,31 @@ __global__ void __launch_bounds__(NT) ada_scan(const SegPlan* __restrict__ plan,
     }
 }
 
-// Last segment whose first element is <= idx.
-__device__ __forceinline__ int find_segment_by_index(const SegPlan* plan, int S, uint32_t idx) {
+// Last segment whose first emit group is <= g.
+__device__ __forceinline__ int find_segment_by_group(const SegPlan* plan, int S, uint32_t g) {
     int lo = 0, hi = S;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (__ldg(&plan[mid].off) <= idx) lo = mid; else hi = mid;
+        if (__ldg(&plan[mid].grp_off) <= g) lo = mid; else hi = mid;
     }
     return lo;
 }
 
-// One thread per pool entry: the entry's index gives its segment and tile,
-// and its distance from the tile's pool base gives its rank inside the tile,
-// so its output slot is (entries of the learner's earlier segments) + (the
-// tile's first slot in its segment) + rank.  It writes (index,
-// sign(G)*scale) there and fixes the residue R = G - sign(G)*scale.  A
+// One warp per group of kGroup consecutive tiles of a segment: lanes
+// 0..kGroup-1 read the tiles' (pool slot, count) and first output slots, a
+// shuffle scan joins their entries into one run, and the lanes walk that run
+// 32 entries at a time.  Each entry goes to (entries of the learner's earlier
+// segments) + (its tile's first slot in the segment) + (rank in the tile) as
+// (index, sign(G)*scale), and its residue becomes R = G - sign(G)*scale.  A
 // learner whose total exceeds cap sends nothing; its residue keeps G = R + dW
-// (already stored by ada_bins).  seg_out: K*S words of shared memory.
-__global__ void __launch_bounds__(NT) ada_emit(const SegPlan* __restrict__ plan, int S, uint64_t N,
-                                               uint32_t tiles_per_learner, const uint2* __restrict__ tile_tab,
-                                               const uint32_t* __restrict__ tile_rel, const uint2* __restrict__ pool,
-                                               const uint32_t* __restrict__ pool_cnt, uint64_t pool_cap,
-                                               const int64_t* __restrict__ counts, const float* __restrict__ scales,
-                                               float* __restrict__ R, gcsgd_pair* __restrict__ out, uint64_t cap,
-                                               int K, int64_t* __restrict__ totals) {
+// (already stored by the bin pass).  seg_out: K*S words of shared memory.
+__global__ void __launch_bounds__(NT, 6) ada_emit(const SegPlan* __restrict__ plan, int S, uint64_t N,
+                                               uint32_t tiles_per_learner, uint32_t groups_per_learner,
+                                               const uint2* __restrict__ tile_tab, const uint32_t* __restrict__ grp_rel,
+                                               const uint2* __restrict__ pool, const int64_t* __restrict__ counts,
+                                               const float* __restrict__ scales, float* __restrict__ R,
+                                               gcsgd_pair* __restrict__ out, uint64_t cap, int K,
+                                               int64_t* __restrict__ totals) {
     extern __shared__ __align__(8) unsigned char emit_smem[];
     uint64_t* s_total = reinterpret_cast<uint64_t*>(emit_smem);            // [K] entries of each learner
     uint32_t* seg_out = reinterpret_cast<uint32_t*>(emit_smem + 8 * K);  // [K][S] first slot of each segment
@@ -734,31 +749,66 @@ __global__ void __launch_bounds__(NT) ada_emit(const SegPlan* __restrict__ plan,
         }
     }
     __syncthreads();
-    const uint64_t stride = (uint64_t)gridDim.x * NT;
+    const int lane = threadIdx.x & 31;
+    const uint32_t gw = blockIdx.x * (NT / 32) + (threadIdx.x >> 5), nw = gridDim.x * (NT / 32);
     for (int k = 0; k < K; ++k) {
         if (s_total[k] > cap) continue;  // nothing sent
-        const uint32_t pc = pool_cnt[k];
-        const uint2* src = pool + (uint64_t)k * pool_cap;
+        const uint2* src = pool + (uint64_t)k * N;
         const uint2* tt = tile_tab + (uint64_t)k * tiles_per_learner;
-        const uint32_t* tr = tile_rel + (uint64_t)k * tiles_per_learner;
+        const uint32_t* gr = grp_rel + (uint64_t)k * groups_per_learner;
         float* Rk = R + (uint64_t)k * N;
         gcsgd_pair* ok = out + (uint64_t)k * cap;
-        for (uint64_t q = (uint64_t)blockIdx.x * NT + threadIdx.x; q < pc; q += stride) {
-            const uint2 it = src[q];
-            const int s = find_segment_by_index(plan, S, it.x);
-            const SegPlan p = plan[s];
-            const uint32_t t = p.tile_off + (it.x - p.off) / p.tile_len;
-            const uint2 ent = tt[t];
-            const uint64_t slot = (uint64_t)seg_out[k * S + s] + tr[t] + ((uint32_t)q - ent.x);
-            const float g = __uint_as_float(it.y);
-            const float scale = scales[(uint64_t)k * S + s];
-            const float val = g > 0.0f ? scale : -scale;
-            Rk[it.x] = __fsub_rn(g, val);
-            if (slot < cap) {
-                gcsgd_pair pr;
-                pr.idx = it.x;
-                pr.val = val;
-                ok[slot] = pr;
+        // the current segment's group range, tiles and output base, kept while the walk stays inside it
+        int s = -1;
+        uint32_t g_lo = 1, g_hi = 0, s_tiles = 0, s_tile_off = 0;
+        float scale = 0.0f;
+        uint64_t ob = 0;
+        for (uint32_t g = gw; g < groups_per_learner; g += nw) {
+            if (g < g_lo || g >= g_hi) {
+                s = find_segment_by_group(plan, S, g);
+                g_lo = __ldg(&plan[s].grp_off);
+                s_tiles = __ldg(&plan[s].ntiles);
+                g_hi = g_lo + (s_tiles + kGroup - 1) / kGroup;
+                s_tile_off = __ldg(&plan[s].tile_off);
+                scale = scales[(uint64_t)k * S + s];
+                ob = seg_out[k * S + s];
+            }
+            const uint32_t j0 = (g - g_lo) * kGroup;
+            const uint32_t nt = s_tiles - j0 < kGroup ? s_tiles - j0 : kGroup;
+            const uint2 ent = (uint32_t)lane < nt ? tt[s_tile_off + j0 + lane] : make_uint2(0u, 0u);
+            uint32_t inc = ent.y;
+#pragma unroll
+            for (int d = 1; d < (int)kGroup; d <<= 1) {
+                const uint32_t y = __shfl_up_sync(kFull, inc, d);
+                if (lane >= d) inc += y;
+            }
+            const uint32_t T = __shfl_sync(kFull, inc, kGroup - 1);
+            if (T == 0) continue;
+            uint32_t incq[kGroup];
+#pragma unroll
+            for (int q = 0; q < (int)kGroup; ++q) incq[q] = __shfl_sync(kFull, inc, q);
+            const uint32_t exc = inc - ent.y;  // rank of the tile's first entry in the group
+            const uint64_t gob = ob + gr[g];
+            for (uint32_t ib = 0; ib < T; ib += 32) {
+                const uint32_t i = ib + lane;
+                uint32_t c = 0;  // the tile holding entry i
+#pragma unroll
+                for (int q = 0; q < (int)kGroup; ++q) c += i >= incq[q];
+                const uint32_t cx = __shfl_sync(kFull, ent.x, c & 31);
+                const uint32_t ce = __shfl_sync(kFull, exc, c & 31);
+                if (i < T) {
+                    const uint2 it = src[(uint64_t)cx + (i - ce)];
+                    const float gv = __uint_as_float(it.y);
+                    const float val = gv > 0.0f ? scale : -scale;
+                    Rk[it.x] = __fsub_rn(gv, val);
+                    const uint64_t slot = gob + i;
+                    if (slot < cap) {
+                        gcsgd_pair pr;
+                        pr.idx = it.x;
+                        pr.val = val;
+                        ok[slot] = pr;
+                    }
+                }
             }
         }
     }
@@ -769,7 +819,8 @@ __global__ void __launch_bounds__(NT) ada_emit(const SegPlan* __restrict__ plan,
 size_t adacomp_workspace_bytes(const int64_t* off, const int32_t* lt, int S, int K, int64_t cap) {
     ada::HostPlan hp;
     ada::host_plan(off, lt, S, &hp);
-    return ada::layout(S, K, cap, hp, nullptr, nullptr);
+    (void)cap;  // the pool has a slot per element, whatever the capacity
+    return ada::layout(S, K, off[S], hp, nullptr, nullptr);
 }
 
 int adacomp_launch(const int64_t* off, int S, const int32_t* lt, int K, const float* dW, float* R, gcsgd_pair* out,
@@ -779,7 +830,7 @@ int adacomp_launch(const int64_t* off, int S, const int32_t* lt, int K, const fl
     HostPlan hp;
     host_plan(off, lt, S, &hp);
     Workspace w;
-    const size_t need = layout(S, K, cap, hp, ws, &w);
+    const size_t need = layout(S, K, off[S], hp, ws, &w);
     if (ws_bytes < need)
         return set_error(GCSGD_ERR_WORKSPACE, "adacomp_compress: workspace of %zu bytes, %zu needed", ws_bytes, need);
     const uint64_t N = (uint64_t)off[S];
@@ -793,13 +844,12 @@ int adacomp_launch(const int64_t* off, int S, const int32_t* lt, int K, const fl
             SegTable<256> st;
             for (int s = 0; s <= S; ++s) st.off[s] = (uint32_t)off[s];
             for (int s = 0; s < S; ++s) st.L[s] = (uint32_t)lt[s];
-            ada_plan<256><<<1, 1024, 0, stream>>>(st, S, K, hp.big_per_learner, w.plan, w.pool_cnt, w.big);
+            ada_plan<256><<<1, 1024, 0, stream>>>(st, S, K, hp.big_per_learner, w.plan, w.big);
         } else {
             SegTable<GCSGD_MAX_SEGMENTS> st;
             for (int s = 0; s <= S; ++s) st.off[s] = (uint32_t)off[s];
             for (int s = 0; s < S; ++s) st.L[s] = (uint32_t)lt[s];
-            ada_plan<GCSGD_MAX_SEGMENTS><<<1, 1024, 0, stream>>>(st, S, K, hp.big_per_learner, w.plan, w.pool_cnt,
-                                                                w.big);
+            ada_plan<GCSGD_MAX_SEGMENTS><<<1, 1024, 0, stream>>>(st, S, K, hp.big_per_learner, w.plan, w.big);
         }
         if ((rc = check_launch("ada_plan"))) return rc;
     }
@@ -820,24 +870,23 @@ int adacomp_launch(const int64_t* off, int S, const int32_t* lt, int K, const fl
     }
     if (T > 0 && any_warp) {
         LaunchScope ls("ada_bins_warp", stream);
-        const uint64_t wgrid = (uint64_t)sm_count() * 4;
-        ada_bins_warp<<<(unsigned)(T < wgrid ? T : wgrid), NT, 0, stream>>>(
-            w.plan, S, N, (uint32_t)hp.tiles_per_learner, T, dW, R, w.big, hp.big_per_learner, w.pool_cnt,
-            w.tile_tab, w.pool, (uint64_t)cap);
+        const uint64_t wgrid = (uint64_t)sm_count() * 4, need_ctas = (T + NT / 32 - 1) / (NT / 32);
+        ada_bins_warp<<<(unsigned)(need_ctas < wgrid ? need_ctas : wgrid), NT, 0, stream>>>(
+            w.plan, S, N, (uint32_t)hp.tiles_per_learner, T, dW, R, w.big, hp.big_per_learner, w.tile_tab, w.pool);
         if ((rc = check_launch("ada_bins_warp"))) return rc;
     }
     if (T > 0 && any_other) {
         LaunchScope ls("ada_bins", stream);
         ada_bins<<<(unsigned)(T < grid_cap ? T : grid_cap), NT, 0, stream>>>(
-            w.plan, S, N, (uint32_t)hp.tiles_per_learner, T, dW, R, w.big, hp.big_per_learner, w.pool_cnt,
-            w.tile_tab, w.tile_sum, w.pool, (uint64_t)cap);
+            w.plan, S, N, (uint32_t)hp.tiles_per_learner, T, dW, R, w.big, hp.big_per_learner, w.tile_tab,
+            w.tile_sum, w.pool);
         if ((rc = check_launch("ada_bins"))) return rc;
     }
     {
         LaunchScope ls("ada_scan", stream);
         ada_scan<<<(unsigned)(K * S), NT, 0, stream>>>(w.plan, S, (uint32_t)hp.tiles_per_learner, w.tile_tab,
-                                                        w.tile_sum, w.big, hp.big_per_learner, w.tile_rel, counts,
-                                                        scales);
+                                                        w.tile_sum, w.big, hp.big_per_learner,
+                                                        (uint32_t)hp.groups_per_learner, w.grp_rel, counts, scales);
         if ((rc = check_launch("ada_scan"))) return rc;
     }
     {
@@ -857,10 +906,9 @@ int adacomp_launch(const int64_t* off, int S, const int32_t* lt, int K, const fl
                 done[dev] = true;
             }
         }
-        ada_emit<<<(unsigned)sm_count() * 4, NT, smem, stream>>>(w.plan, S, N, (uint32_t)hp.tiles_per_learner,
-                                                                 w.tile_tab, w.tile_rel, w.pool, w.pool_cnt,
-                                                                 (uint64_t)cap, counts, scales, R, out,
-                                                                 (uint64_t)cap, K, totals);
+        ada_emit<<<(unsigned)sm_count() * 6, NT, smem, stream>>>(
+            w.plan, S, N, (uint32_t)hp.tiles_per_learner, (uint32_t)hp.groups_per_learner, w.tile_tab, w.grp_rel,
+            w.pool, counts, scales, R, out, (uint64_t)cap, K, totals);
         if ((rc = check_launch("ada_emit"))) return rc;
     }
     return GCSGD_OK;

@@ -4,7 +4,9 @@
 // average them before the weight update; "Deep Gradient Compression",
 // Appendix A: the nodes' gradients are summed.
 //
-// One kernel.  Each CTA owns a contiguous run of 4096-element output tiles.
+// Two kernels for the dense average (the choice is made on the capacity:
+// K * cap >= n / 4 counts as dense lists) and the tile kernel for the update.
+// Tile kernel: each CTA owns a contiguous run of 4096-element output tiles.
 // A tile lives in shared memory: zeroed, then every list's entries that fall
 // in it are added in list order k = 0..K-1 (entries inside one list have
 // distinct indices, so the adds of one k never collide; a barrier between
@@ -438,12 +440,189 @@ __global__ void __launch_bounds__(NT) spavg_kernel(const gcsgd_pair* __restrict_
     }
 }
 
+
+// ---------------------------------------------------------------- warp spans
+// The dense average for dense lists, without CTA barriers: every warp owns a
+// contiguous run of 512-index output spans and keeps, per list, a cursor at
+// the first entry it has not consumed (found once, at the run's start, by a
+// 32-ary search of eight lists at a time).  For each span the warp loads the
+// next 64 entries of eight lists at once (sixteen loads in flight per lane),
+// then adds them in learner order into its 2 KB accumulator (a list's
+// indices are distinct, so one list's adds never collide; __syncwarp orders
+// the lists), loads more of a list only when all 64 fell inside the span,
+// and writes the span once with 128-bit stores.  Lists sorted ascending make
+// every entry read once (plus the look-ahead) and every output written once.
+// A span costs one load latency, so sparse lists (a few entries per span)
+// go to the tile kernel instead, which pays its latencies per 4096-index
+// tile and stages whole ranges of entries.
+constexpr uint32_t kWSpan = 512;  // output indices per warp span
+constexpr int kBatch = 8;         // lists loaded together
+
+__device__ __forceinline__ gcsgd_pair load_entry(const gcsgd_pair* L, uint32_t i, uint32_t cnt) {
+    gcsgd_pair it;
+    it.idx = 0u;
+    it.val = 0.0f;
+    if (i < cnt) it = L[i];
+    return it;
+}
+
+// First position p in [0, cnt_k] with list_k[p].idx >= target, for the lists
+// k0 .. k0+nb-1 at once (nb <= kBatch); results to cur[k].  Called by a warp.
+__device__ void batch_lower_bound(const gcsgd_pair* lists, uint64_t cap, const uint32_t* cnt, int k0, int nb,
+                                  uint64_t target, uint32_t* cur) {
+    const int lane = threadIdx.x & 31;
+    uint32_t lo[kBatch], hi[kBatch];
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+        lo[q] = 0;
+        hi[q] = q < nb ? cnt[k0 + q] : 0u;
+    }
+    for (;;) {
+        bool wide = false;
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) wide |= hi[q] - lo[q] > 32;
+        if (!wide) break;
+        bool pr[kBatch];
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) {  // every probe of the round in flight together
+            pr[q] = true;
+            if (hi[q] - lo[q] > 32) {
+                const uint32_t step = (hi[q] - lo[q] + 31) / 32;
+                const uint64_t p = (uint64_t)lo[q] + (uint64_t)(lane + 1) * step - 1;
+                if (p < hi[q]) pr[q] = (uint64_t)__ldg(&lists[(uint64_t)(k0 + q) * cap + p].idx) >= target;
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) {
+            if (hi[q] - lo[q] <= 32) continue;  // uniform across the warp
+            const uint32_t step = (hi[q] - lo[q] + 31) / 32;
+            const unsigned b = __ballot_sync(kFull, pr[q]);
+            const int f = b ? __ffs(b) - 1 : 32;
+            const uint64_t nlo = (uint64_t)lo[q] + (uint64_t)f * step;
+            const uint64_t qf = (uint64_t)lo[q] + (uint64_t)(f + 1) * step - 1;
+            hi[q] = (f < 32 && qf < hi[q]) ? (uint32_t)qf : hi[q];
+            lo[q] = (uint32_t)(nlo < hi[q] ? nlo : hi[q]);
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+        if (q >= nb) break;
+        const uint32_t p = lo[q] + lane;
+        const bool pred = p >= hi[q] || (uint64_t)__ldg(&lists[(uint64_t)(k0 + q) * cap + p].idx) >= target;
+        const unsigned b = __ballot_sync(kFull, pred);
+        const uint32_t r = lo[q] + (b ? __ffs(b) - 1 : 32);
+        if (lane == 0) cur[k0 + q] = r < hi[q] ? r : hi[q];
+    }
+}
+
+// Shared memory: acc[NW][kWSpan] floats | cnt[K] | cur[NW][K] (u32)
+__global__ void __launch_bounds__(NT, 4) spavg_warp(const gcsgd_pair* __restrict__ lists, uint64_t cap,
+                                                    const int64_t* __restrict__ counts, int K, uint64_t n,
+                                                    float* __restrict__ out, uint64_t spans, uint64_t per_warp) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float* acc = reinterpret_cast<float*>(smem) + (size_t)warp * kWSpan;
+    uint32_t* cnt = reinterpret_cast<uint32_t*>(smem + sizeof(float) * NW * kWSpan);
+    uint32_t* cur = cnt + K + (size_t)warp * K;
+    for (int k = threadIdx.x; k < K; k += NT) {
+        const int64_t c = counts[k];
+        const uint64_t cc = c < 0 ? 0 : ((uint64_t)c > cap ? cap : (uint64_t)c);
+        cnt[k] = (uint32_t)(cc < 0xffffffffu ? cc : 0xffffffffu);
+    }
+    for (uint32_t j = lane * 4; j < kWSpan; j += 128) *reinterpret_cast<float4*>(acc + j) = make_float4(0.f, 0.f, 0.f, 0.f);
+    __syncthreads();
+    const uint64_t sp0 = ((uint64_t)blockIdx.x * NW + warp) * per_warp;
+    if (sp0 >= spans) return;
+    const uint64_t sp1 = sp0 + per_warp < spans ? sp0 + per_warp : spans;
+    for (int kb = 0; kb < K; kb += kBatch)
+        batch_lower_bound(lists, cap, cnt, kb, K - kb < kBatch ? K - kb : kBatch, sp0 * kWSpan, cur);
+    __syncwarp();
+    const float fk = (float)K, inv_k = 1.0f / fk;
+    const bool pow2 = (K & (K - 1)) == 0;
+    for (uint64_t sp = sp0; sp < sp1; ++sp) {
+        const uint64_t s0 = sp * kWSpan, s1 = s0 + kWSpan < n ? s0 + kWSpan : n;
+        for (int kb = 0; kb < K; kb += kBatch) {
+            const int nb = K - kb < kBatch ? K - kb : kBatch;
+            gcsgd_pair e[kBatch], f[kBatch];  // the next 64 entries of each list (two per lane)
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+                e[q].idx = f[q].idx = 0u;
+                e[q].val = f[q].val = 0.0f;
+                if (q < nb) {
+                    const gcsgd_pair* L = lists + (uint64_t)(kb + q) * cap;
+                    e[q] = load_entry(L, cur[kb + q] + lane, cnt[kb + q]);
+                    f[q] = load_entry(L, cur[kb + q] + 32 + lane, cnt[kb + q]);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+                if (q >= nb) break;
+                const int k = kb + q;
+                uint32_t c0 = cur[k];
+                gcsgd_pair it = e[q];
+                for (int round = 0;; ++round) {
+                    const bool in = c0 + lane < cnt[k] && (uint64_t)it.idx < s1;  // past the end: never
+                    const unsigned b = __ballot_sync(kFull, !in);
+                    const uint32_t c = b ? (uint32_t)__ffs(b) - 1 : 32u;  // entries of this span (a prefix)
+                    if ((uint32_t)lane < c && (uint64_t)it.idx >= s0) {
+                        float* a = acc + (it.idx - s0);
+                        *a = __fadd_rn(*a, it.val);
+                    }
+                    c0 += c;
+                    if (c < 32) break;
+                    it = round == 0 ? f[q] : load_entry(lists + (uint64_t)k * cap, c0 + lane, cnt[k]);
+                }
+                __syncwarp();  // list k's adds land before list k+1's, and every lane has read cur[k]
+                if (lane == 0) cur[k] = c0;
+                __syncwarp();
+            }
+        }
+        // the span's average, written once; acc re-zeroed for the next span
+        const uint64_t len = s1 - s0;
+        const bool al = ((uintptr_t)(out + s0) & 15) == 0;
+#pragma unroll
+        for (int r = 0; r < (int)(kWSpan / 128); ++r) {
+            const uint32_t j = 4u * (lane + 32 * r);
+            float4 q = *reinterpret_cast<const float4*>(acc + j);
+            *reinterpret_cast<float4*>(acc + j) = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (j >= len) continue;
+            q.x = div_k(q.x, fk, inv_k, pow2);
+            q.y = div_k(q.y, fk, inv_k, pow2);
+            q.z = div_k(q.z, fk, inv_k, pow2);
+            q.w = div_k(q.w, fk, inv_k, pow2);
+            if (al && j + 4 <= len) {
+                *reinterpret_cast<float4*>(out + s0 + j) = q;
+            } else {
+                const float* qq = &q.x;
+                for (uint32_t i = 0; i < 4 && j + i < len; ++i) out[s0 + j + i] = qq[i];
+            }
+        }
+        __syncwarp();
+    }
+}
+
+
 }  // namespace spavg
 
 int spavg_launch(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int K, int64_t n, float* out,
                  cudaStream_t stream, bool update, float lr) {
     using namespace spavg;
     if (n == 0) return GCSGD_OK;
+    // dense lists (by capacity: K * cap >= n / 4, a quarter entry per output
+    // or more) take the warp spans, sparse ones the tile kernel
+    if (!update && (uint64_t)K * (uint64_t)cap >= (uint64_t)n / 4) {  // at most 34 KB of shared memory (K = 512)
+        const uint64_t spans = ((uint64_t)n + kWSpan - 1) / kWSpan;
+        uint64_t ctas = (uint64_t)sm_count() * 4;  // resident CTAs per SM
+        const uint64_t need = (spans + NW - 1) / NW;
+        if (ctas > need) ctas = need;
+        const uint64_t per_warp = (spans + ctas * NW - 1) / (ctas * NW);
+        ctas = (spans + per_warp * NW - 1) / (per_warp * NW);
+        const size_t wsmem = sizeof(float) * NW * kWSpan + sizeof(uint32_t) * (size_t)K * (NW + 1);
+        LaunchScope ls("spavg", stream);
+        spavg_warp<<<(unsigned)ctas, NT, wsmem, stream>>>(lists, (uint64_t)cap, counts, K, (uint64_t)n, out, spans,
+                                                          per_warp);
+        return check_launch("spavg");
+    }
     const uint64_t tiles = ((uint64_t)n + kTile - 1) / kTile;
     uint64_t grid = (uint64_t)sm_count() * 4;
     if (grid > tiles) grid = tiles;
@@ -454,7 +633,8 @@ int spavg_launch(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, in
     const size_t stage_items = (size_t)K * C > kStage ? (size_t)K * C : kStage;
     const size_t smem = kTile * sizeof(float) + stage_items * sizeof(gcsgd_pair) + 3 * sizeof(uint64_t) * (size_t)K +
                         sizeof(uint32_t) * (3 * (size_t)K + 1 + (size_t)K * (NW + 1));
-    if (smem > 200 * 1024) return set_error(GCSGD_ERR_INVALID_ARG, "sparse_average: K = %d too large", K);
+    const char* fn = update ? "sparse_average_update" : "sparse_average";
+    if (smem > 200 * 1024) return set_error(GCSGD_ERR_INVALID_ARG, "%s: K = %d too large", fn, K);
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -463,7 +643,7 @@ int spavg_launch(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, in
                 cudaSuccess ||
             cudaFuncSetAttribute(spavg_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
                 cudaSuccess)
-            return set_error(GCSGD_ERR_CUDA, "sparse_average: cannot raise the shared-memory limit");
+            return set_error(GCSGD_ERR_CUDA, "%s: cannot raise the shared-memory limit", fn);
         attr_set[dev] = true;
     }
     LaunchScope ls(update ? "spavg_update" : "spavg", stream);

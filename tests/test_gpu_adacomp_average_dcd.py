@@ -161,6 +161,18 @@ def test_capacity_overflow_sends_nothing_and_keeps_the_residue(cuda_lib):
 
 # ------------------------------------------------------------ sparse average
 
+def padded(idx, val, cap):
+    """The same lists in a wider buffer (the sparse average picks its kernel
+    from K * cap against n: a quarter entry per output or more is dense)."""
+    K, c = idx.shape
+    if cap <= c:
+        return idx, val
+    i2 = np.zeros((K, cap), np.uint32)
+    v2 = np.zeros((K, cap), np.float32)
+    i2[:, :c], v2[:, :c] = idx, val
+    return i2, v2
+
+
 def run_average(gc, idx, val, counts, n, out_offset=0):
     import torch
     K, cap = idx.shape
@@ -182,11 +194,14 @@ def run_average(gc, idx, val, counts, n, out_offset=0):
     return got, want
 
 
+@pytest.mark.parametrize("kernel", ["tiles", "warp_spans"])
 @pytest.mark.parametrize("K", [1, 2, 4, 8, 33])
 @pytest.mark.parametrize("n", [1, 4095, 4096, 100003])
-def test_sparse_average_random_lists(cuda_lib, K, n):
+def test_sparse_average_random_lists(cuda_lib, K, n, kernel):
     rng = np.random.default_rng(K * 7 + n)
-    cap = max(1, min(n, 3000))
+    cap = max(1, min(n, 3000, n // (4 * K) - 1 if kernel == "tiles" else n))
+    if kernel == "tiles" and K * cap >= n // 4:
+        pytest.skip("no list capacity this small is sparse")
     idx = np.zeros((K, cap), np.uint32)
     val = np.zeros((K, cap), np.float32)
     counts = np.zeros(K, np.int64)
@@ -195,6 +210,8 @@ def test_sparse_average_random_lists(cuda_lib, K, n):
         idx[k, :c] = np.sort(rng.choice(n, size=c, replace=False))
         val[k, :c] = rng.standard_normal(c).astype(np.float32)
         counts[k] = c
+    if kernel == "warp_spans":
+        idx, val = padded(idx, val, max(cap, -(-n // (4 * K))))
     got, want = run_average(cuda_lib, idx, val, counts, n)
     np.testing.assert_array_equal(got, want)  # learner order kept: exact
 
@@ -214,6 +231,9 @@ def test_sparse_average_unaligned_output(cuda_lib, offset, K):
         idx[k, :c] = np.sort(pick)
         val[k, :c] = rng.standard_normal(c).astype(np.float32)
         counts[k] = c
+    got, want = run_average(cuda_lib, idx, val, counts, n, out_offset=offset)
+    np.testing.assert_array_equal(got, want)
+    idx, val = padded(idx, val, -(-n // (4 * K)))  # the same lists through the warp-span kernel
     got, want = run_average(cuda_lib, idx, val, counts, n, out_offset=offset)
     np.testing.assert_array_equal(got, want)
 
@@ -242,6 +262,43 @@ def test_sparse_average_dense_lists(cuda_lib):
     val = rng.standard_normal((K, n)).astype(np.float32)
     got, want = run_average(cuda_lib, idx, val, np.full(K, n, np.int64), n)
     np.testing.assert_array_equal(got, want)
+
+
+def test_sparse_average_512_lists(cuda_lib):
+    """The largest K the call takes: 64 batches of eight lists per span."""
+    rng = np.random.default_rng(512)
+    K, n, cap = 512, 20011, 60
+    idx = np.zeros((K, cap), np.uint32)
+    val = np.zeros((K, cap), np.float32)
+    counts = rng.integers(0, cap + 1, size=K).astype(np.int64)
+    for k in range(K):
+        idx[k, :counts[k]] = np.sort(rng.choice(n, size=int(counts[k]), replace=False))
+        val[k, :counts[k]] = rng.standard_normal(int(counts[k])).astype(np.float32)
+    got, want = run_average(cuda_lib, idx, val, counts, n)
+    np.testing.assert_array_equal(got, want)
+
+
+def test_sparse_average_malformed_lists_stay_in_range(cuda_lib):
+    """Unsorted lists, repeated and out-of-range indices: the result is not
+    defined, but the call ends, writes every output and nothing else."""
+    import torch
+    gc = cuda_lib
+    rng = np.random.default_rng(3)
+    K, n, cap = 3, 5000, 700
+    pairs = torch.zeros((K, cap, 2), dtype=torch.int32)
+    idx = rng.integers(0, n, size=(K, cap)).astype(np.int64)
+    idx[0, ::7] = n + 5           # past the end
+    idx[1, :50] = 4999            # one index repeated
+    idx[2] = np.sort(idx[2])[::-1]  # descending
+    pairs[..., 0] = torch.from_numpy(idx).to(torch.int32)
+    pairs[..., 1] = torch.from_numpy(rng.standard_normal((K, cap)).astype(np.float32)).view(torch.int32)
+    buf = torch.full((n + 8,), float("nan"), device="cuda")
+    out = buf[4:4 + n]
+    gc.sparse_average(pairs.cuda(), torch.full((K,), cap, dtype=torch.int64, device="cuda"), n, out)
+    torch.cuda.synchronize()
+    b = buf.cpu().numpy()
+    assert np.isnan(b[:4]).all() and np.isnan(b[4 + n:]).all()
+    assert not np.isnan(b[4:4 + n]).any()
 
 
 # --------------------------------------------- averaged sparse weight update
