@@ -307,31 +307,65 @@ __device__ __forceinline__ void select_tile(const float4 (&Gv)[4], const float4 
 }
 
 // Warp-chunk tiles (4 <= L_T <= 512): a tile is one warp's chunk of bpw
-// whole bins, at most 512 values, four float4 per lane.  Warps run
-// independently, with no block barrier and no shared counter: a warp finds
-// its bins' maxima from its registers (one bin: a warp reduction; several:
-// shared-memory atomicMax per float4 part), writes them to the bins array
-// (ada_scan averages them in fp64), selects, stores R <- G and writes its
-// candidates in index order into the pool slots of its own index range.
-// Lanes past the chunk's end hold 0: G = 0 never raises a maximum and is
-// never sent, so only the loads and stores test bounds.  A warp walks the
-// tiles with a stride of all warps, keeping its segment's plan in registers.
-__global__ void __launch_bounds__(NT, 4) ada_bins_warp(const SegPlan* __restrict__ plan, int S, uint64_t N,
-                                                       uint32_t tiles_per_learner, uint64_t total_tiles,
-                                                       const float* __restrict__ dW, float* __restrict__ R,
-                                                       uint32_t* __restrict__ bins, uint64_t bins_per_learner,
-                                                       uint2* __restrict__ tile_tab, uint2* __restrict__ pool) {
-    __shared__ uint32_t wbins[NT / 32][kWarpChunk / 4];
+// whole bins, at most 512 values.  Warps run independently, with no block
+// barrier and no shared counter.  Each warp streams its chunks through a
+// ring of kRing shared-memory stages filled by cp.async (R and dW, 4 KB a
+// chunk; the copies of the next kRing - 1 chunks are in flight while one is
+// computed, and they hold no registers).  A lane copies and later reads the
+// same 16-byte pieces, so only its own cp.async groups are waited on.  Past a
+// chunk's end the copies zero-fill: G = 0 never raises a maximum and is never
+// sent, so the arithmetic needs no bounds test.  Per chunk the warp finds its
+// bins' maxima (one bin: a warp reduction; several: shared-memory atomicMax
+// per float4 part), writes them to the bins array (ada_scan averages them in
+// fp64), selects, stores R <- G and writes its candidates in index order
+// into the pool slots of its own index range.
+constexpr int NTW = 128;   // threads of an ada_bins_warp CTA
+constexpr int kRing = 3;   // stages per warp
+struct ChunkMeta {         // what the computing side needs of an issued chunk
+    uint32_t rel, clen, k, lt, tj, L, bpw, big_off;
+    float invL;
+};
+constexpr size_t kBinsWarpSmem =
+    sizeof(float) * (NTW / 32) * kRing * 2 * kWarpChunk + sizeof(ChunkMeta) * (NTW / 32) * kRing +
+    sizeof(uint32_t) * (NTW / 32) * (kWarpChunk / 4);
+
+__device__ __forceinline__ void cp_async16(void* sdst, const void* gsrc, uint32_t bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"((uint32_t)__cvta_generic_to_shared(sdst)),
+                 "l"(gsrc), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* sdst, const void* gsrc, uint32_t bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"((uint32_t)__cvta_generic_to_shared(sdst)),
+                 "l"(gsrc), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+__global__ void __launch_bounds__(NTW, 4) ada_bins_warp(const SegPlan* __restrict__ plan, int S, uint64_t N,
+                                                        uint32_t tiles_per_learner, uint64_t total_tiles,
+                                                        const float* __restrict__ dW, float* __restrict__ R,
+                                                        uint32_t* __restrict__ bins, uint64_t bins_per_learner,
+                                                        uint2* __restrict__ tile_tab, uint2* __restrict__ pool) {
+    extern __shared__ __align__(16) unsigned char bw_smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint32_t nw = gridDim.x * (NT / 32), T = (uint32_t)total_tiles;  // T < 2^32 (checked by the host)
-    uint32_t t = blockIdx.x * (NT / 32) + warp;
-    if (t >= T) return;
-    uint32_t k = t / tiles_per_learner, lt = t - k * tiles_per_learner;
-    // the fields of the current segment that a chunk needs (bpw = 0: not a warp-chunk segment)
+    float* ring = reinterpret_cast<float*>(bw_smem) + (size_t)warp * kRing * 2 * kWarpChunk;  // [kRing][dW | R]
+    ChunkMeta* meta = reinterpret_cast<ChunkMeta*>(bw_smem + sizeof(float) * (NTW / 32) * kRing * 2 * kWarpChunk) +
+                      warp * kRing;
+    uint32_t* wb = reinterpret_cast<uint32_t*>(bw_smem + sizeof(float) * (NTW / 32) * kRing * 2 * kWarpChunk +
+                                               sizeof(ChunkMeta) * (NTW / 32) * kRing) +
+                   warp * (kWarpChunk / 4);  // this warp's bin maxima (bpw <= 128)
+    const uint32_t nw = gridDim.x * (NTW / 32), T = (uint32_t)total_tiles;  // T < 2^32 (checked by the host)
+
+    // issuing side: the warp's tiles t = its id + i * nw, keeping the segment's fields
+    uint32_t t = blockIdx.x * (NTW / 32) + warp;
+    bool done = t >= T;
+    uint32_t k = 0, lt = 0;
     struct {
         uint32_t off, n, L, bpw, tile_len, tile_off, big_off, next_off;
         float invL;
-    } p;
+    } p = {};
     auto load_seg = [&](uint32_t at) {
         const int s = find_segment_by_tile(plan, S, at);
         const SegPlan q = plan[s];
@@ -339,139 +373,11 @@ __global__ void __launch_bounds__(NT, 4) ada_bins_warp(const SegPlan* __restrict
         p.tile_len = q.tile_len, p.tile_off = q.tile_off, p.big_off = q.big_off, p.invL = q.invL;
         p.next_off = s + 1 < S ? __ldg(&plan[s + 1].tile_off) : tiles_per_learner;
     };
-    load_seg(lt);
-    uint32_t* wb = wbins[warp];  // this warp's bin maxima (bpw <= 128)
-    for (;;) {
-        if (p.bpw) {  // other tiles: ada_bins
-            const uint32_t tj = lt - p.tile_off;
-            const uint32_t start = tj * p.tile_len;
-            const uint32_t clen = p.n - start < p.tile_len ? p.n - start : p.tile_len;
-            const uint32_t rel = p.off + start;  // the chunk's first index within the learner
-            const uint64_t base = (uint64_t)k * N + rel;
-            const float* dWc = dW + base;
-            float* Rc = R + base;
-            const bool cal = (((uintptr_t)dWc | (uintptr_t)Rc) & 15) == 0;
-            float4 Gv[4], Dv[4];
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const uint32_t e = 4u * (lane + 32 * r);
-                if (cal && e + 4 <= clen) {
-                    Dv[r] = __ldg(reinterpret_cast<const float4*>(dWc + e));
-                    Gv[r] = *reinterpret_cast<const float4*>(Rc + e);
-                } else {
-                    float* d4 = &Dv[r].x;
-                    float* g4 = &Gv[r].x;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const bool in = e + j < clen;
-                        d4[j] = in ? __ldg(dWc + e + j) : 0.0f;
-                        g4[j] = in ? Rc[e + j] : 0.0f;
-                    }
-                }
-                Gv[r].x = __fadd_rn(Gv[r].x, Dv[r].x);
-                Gv[r].y = __fadd_rn(Gv[r].y, Dv[r].y);
-                Gv[r].z = __fadd_rn(Gv[r].z, Dv[r].z);
-                Gv[r].w = __fadd_rn(Gv[r].w, Dv[r].w);
-            }
-            // bin maxima of |G| (fmaxf skips a NaN, so NaN reads as 0)
-            const uint32_t bpw = p.bpw, L = p.L;
-            uint32_t* gb = bins + (uint64_t)k * bins_per_learner + p.big_off + tj * bpw;
-            float m_one = 0.0f;
-            if (bpw == 1) {
-                float m = 0.0f;
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    m = fmaxf(m, fmaxf(fmaxf(fabsf(Gv[r].x), fabsf(Gv[r].y)), fmaxf(fabsf(Gv[r].z), fabsf(Gv[r].w))));
-                }
-                m_one = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(m)));
-                if (lane == 0) gb[0] = __float_as_uint(m_one);
-            } else {
-                for (uint32_t b = lane; b < bpw; b += 32) wb[b] = 0u;
-                __syncwarp();
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const uint32_t e = 4u * (lane + 32 * r);
-                    if (e >= clen) continue;
-                    const uint32_t b0 = bin_of(e, p.invL), cut = (b0 + 1) * L - e;
-                    const float* g4 = &Gv[r].x;
-                    float m0 = 0.0f, m1 = 0.0f;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float a = fabsf(g4[j]);
-                        if ((uint32_t)j < cut) m0 = fmaxf(m0, a); else m1 = fmaxf(m1, a);
-                    }
-                    if (m0 > 0.0f) atomicMax(&wb[b0], __float_as_uint(m0));
-                    if (m1 > 0.0f) atomicMax(&wb[b0 + 1], __float_as_uint(m1));  // only past a bin edge
-                }
-                __syncwarp();
-                const uint32_t nbw = bin_of(clen - 1, p.invL) + 1;
-                for (uint32_t b = lane; b < nbw; b += 32) gb[b] = wb[b];
-            }
-            // selection (float compares, as the definition: |G + dW| >= bin max
-            // and G != 0; a bin max of 0 leaves only G = 0 or NaN, never
-            // sent), R <- G, candidate counts per round
-            uint32_t flags = 0, packed = 0;
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const uint32_t e = 4u * (lane + 32 * r);
-                const float* g4 = &Gv[r].x;
-                const float* d4 = &Dv[r].x;
-                float gm0 = m_one, gm1 = m_one;
-                uint32_t cut = 4;
-                if (bpw != 1 && e < clen) {
-                    const uint32_t b0 = bin_of(e, p.invL);
-                    cut = (b0 + 1) * L - e;
-                    gm0 = __uint_as_float(wb[b0]);
-                    gm1 = cut < 4 && b0 + 1 < bpw ? __uint_as_float(wb[b0 + 1]) : gm0;
-                }
-                uint32_t f = 0;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float gm = (uint32_t)j < cut ? gm0 : gm1;
-                    const bool sel = fabsf(__fadd_rn(g4[j], d4[j])) >= gm && g4[j] != 0.0f;
-                    f |= (uint32_t)sel << j;
-                }
-                flags |= f << (4 * r);
-                packed |= (uint32_t)__popc(f) << (8 * r);
-                if (cal && e + 4 <= clen) {
-                    *reinterpret_cast<float4*>(Rc + e) = Gv[r];
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        if (e + j < clen) Rc[e + j] = g4[j];
-                }
-            }
-            // rank inside the chunk: rounds in order, lanes in order (8 bits per round)
-            uint32_t incl = packed;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const uint32_t y = __shfl_up_sync(kFull, incl, d);
-                if (lane >= d) incl += y;
-            }
-            const uint32_t wtot = __shfl_sync(kFull, incl, 31), excl = incl - packed;
-            if (lane == 0) {
-                const uint32_t W = (wtot & 0xFFu) + ((wtot >> 8) & 0xFFu) + ((wtot >> 16) & 0xFFu) + (wtot >> 24);
-                tile_tab[(uint64_t)k * tiles_per_learner + lt] = make_uint2(rel, W);
-            }
-            if (flags) {
-                uint2* dst = pool + base;
-                uint32_t rb = 0;
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const uint32_t fr = (flags >> (4 * r)) & 0xFu;
-                    uint32_t pos = rb + ((excl >> (8 * r)) & 0xFFu);
-                    rb += (wtot >> (8 * r)) & 0xFFu;
-                    if (!fr) continue;
-                    const uint32_t e = 4u * (lane + 32 * r);
-                    const float* g4 = &Gv[r].x;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        if ((fr >> j) & 1u) dst[pos++] = make_uint2(rel + e + j, __float_as_uint(g4[j]));
-                }
-            }
-            __syncwarp();  // wb is rewritten by the next chunk
+    auto step = [&]() {
+        if (T - t <= nw) {
+            done = true;
+            return;
         }
-        if (T - t <= nw) break;
         t += nw;
         lt += nw;
         while (lt >= tiles_per_learner) {
@@ -479,7 +385,175 @@ __global__ void __launch_bounds__(NT, 4) ada_bins_warp(const SegPlan* __restrict
             ++k;
         }
         if (lt < p.tile_off || lt >= p.next_off) load_seg(lt);
+    };
+    if (!done) {
+        k = t / tiles_per_learner;
+        lt = t - k * tiles_per_learner;
+        load_seg(lt);
+        while (!done && !p.bpw) step();  // other tiles: ada_bins
     }
+    auto issue = [&](int st) {
+        ChunkMeta m = {};
+        if (!done) {
+            const uint32_t tj = lt - p.tile_off, start = tj * p.tile_len;
+            m.rel = p.off + start;
+            m.clen = p.n - start < p.tile_len ? p.n - start : p.tile_len;
+            m.k = k, m.lt = lt, m.tj = tj, m.L = p.L, m.bpw = p.bpw, m.big_off = p.big_off, m.invL = p.invL;
+            const uint64_t base = (uint64_t)k * N + m.rel;
+            const float* dWc = dW + base;
+            const float* Rc = R + base;
+            float* sD = ring + st * 2 * kWarpChunk;
+            float* sR = sD + kWarpChunk;
+            if ((((uintptr_t)dWc | (uintptr_t)Rc) & 15) == 0) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const uint32_t e = 4u * (lane + 32 * r);
+                    const uint32_t by = e < m.clen ? (m.clen - e < 4 ? 4 * (m.clen - e) : 16u) : 0u;
+                    cp_async16(sD + e, by ? dWc + e : dWc, by);
+                    cp_async16(sR + e, by ? Rc + e : Rc, by);
+                }
+            } else {  // 4-byte copies where the chunk is not 16-byte aligned
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const uint32_t e = 4u * (lane + 32 * r);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t by = e + j < m.clen ? 4u : 0u;
+                        cp_async4(sD + e + j, by ? dWc + e + j : dWc, by);
+                        cp_async4(sR + e + j, by ? Rc + e + j : Rc, by);
+                    }
+                }
+            }
+            step();
+            while (!done && !p.bpw) step();
+        }
+        if (lane == 0) meta[st] = m;  // clen = 0: no chunk (every later stage is empty too)
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int st = 0; st < kRing - 1; ++st) issue(st);
+
+    for (int i = 0;; ++i) {
+        const int cs = i % kRing;
+        issue((i + kRing - 1) % kRing);  // that stage's chunk was computed in the previous round
+        cp_async_wait<kRing - 1>();       // this lane's copies of chunk i have landed
+        __syncwarp();                     // and lane 0's meta of it is visible
+        const ChunkMeta m = meta[cs];
+        if (m.clen == 0) break;
+        const float* sD = ring + cs * 2 * kWarpChunk;
+        const float* sR = sD + kWarpChunk;
+        const uint64_t base = (uint64_t)m.k * N + m.rel;
+        float* Rc = R + base;
+        const bool cal = ((uintptr_t)Rc & 15) == 0;
+        const uint32_t clen = m.clen, bpw = m.bpw, L = m.L;
+        float4 Gv[4], Dv[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const uint32_t e = 4u * (lane + 32 * r);
+            Dv[r] = *reinterpret_cast<const float4*>(sD + e);
+            Gv[r] = *reinterpret_cast<const float4*>(sR + e);
+            Gv[r].x = __fadd_rn(Gv[r].x, Dv[r].x);
+            Gv[r].y = __fadd_rn(Gv[r].y, Dv[r].y);
+            Gv[r].z = __fadd_rn(Gv[r].z, Dv[r].z);
+            Gv[r].w = __fadd_rn(Gv[r].w, Dv[r].w);
+        }
+        // bin maxima of |G| (fmaxf skips a NaN, so NaN reads as 0)
+        uint32_t* gb = bins + (uint64_t)m.k * bins_per_learner + m.big_off + m.tj * bpw;
+        float m_one = 0.0f;
+        if (bpw == 1) {
+            float mx = 0.0f;
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                mx = fmaxf(mx, fmaxf(fmaxf(fabsf(Gv[r].x), fabsf(Gv[r].y)), fmaxf(fabsf(Gv[r].z), fabsf(Gv[r].w))));
+            m_one = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(mx)));
+            if (lane == 0) gb[0] = __float_as_uint(m_one);
+        } else {
+            for (uint32_t b = lane; b < bpw; b += 32) wb[b] = 0u;
+            __syncwarp();
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const uint32_t e = 4u * (lane + 32 * r);
+                if (e >= clen) continue;
+                const uint32_t b0 = bin_of(e, m.invL), cut = (b0 + 1) * L - e;
+                const float* g4 = &Gv[r].x;
+                float m0 = 0.0f, m1 = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float a = fabsf(g4[j]);
+                    if ((uint32_t)j < cut) m0 = fmaxf(m0, a); else m1 = fmaxf(m1, a);
+                }
+                if (m0 > 0.0f) atomicMax(&wb[b0], __float_as_uint(m0));
+                if (m1 > 0.0f) atomicMax(&wb[b0 + 1], __float_as_uint(m1));  // only past a bin edge
+            }
+            __syncwarp();
+            const uint32_t nbw = bin_of(clen - 1, m.invL) + 1;
+            for (uint32_t b = lane; b < nbw; b += 32) gb[b] = wb[b];
+        }
+        // selection (float compares, as the definition: |G + dW| >= bin max
+        // and G != 0; a bin max of 0 leaves only G = 0 or NaN, never sent),
+        // R <- G, candidate counts per round
+        uint32_t flags = 0, packed = 0;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const uint32_t e = 4u * (lane + 32 * r);
+            const float* g4 = &Gv[r].x;
+            const float* d4 = &Dv[r].x;
+            float gm0 = m_one, gm1 = m_one;
+            uint32_t cut = 4;
+            if (bpw != 1 && e < clen) {
+                const uint32_t b0 = bin_of(e, m.invL);
+                cut = (b0 + 1) * L - e;
+                gm0 = __uint_as_float(wb[b0]);
+                gm1 = cut < 4 && b0 + 1 < bpw ? __uint_as_float(wb[b0 + 1]) : gm0;
+            }
+            uint32_t f = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float gm = (uint32_t)j < cut ? gm0 : gm1;
+                const bool sel = fabsf(__fadd_rn(g4[j], d4[j])) >= gm && g4[j] != 0.0f;
+                f |= (uint32_t)sel << j;
+            }
+            flags |= f << (4 * r);
+            packed |= (uint32_t)__popc(f) << (8 * r);
+            if (cal && e + 4 <= clen) {
+                *reinterpret_cast<float4*>(Rc + e) = Gv[r];
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (e + j < clen) Rc[e + j] = g4[j];
+            }
+        }
+        // rank inside the chunk: rounds in order, lanes in order (8 bits per round)
+        uint32_t incl = packed;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, incl, d);
+            if (lane >= d) incl += y;
+        }
+        const uint32_t wtot = __shfl_sync(kFull, incl, 31), excl = incl - packed;
+        if (lane == 0) {
+            const uint32_t W = (wtot & 0xFFu) + ((wtot >> 8) & 0xFFu) + ((wtot >> 16) & 0xFFu) + (wtot >> 24);
+            tile_tab[(uint64_t)m.k * tiles_per_learner + m.lt] = make_uint2(m.rel, W);
+        }
+        if (flags) {
+            uint2* dst = pool + base;
+            uint32_t rb = 0;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const uint32_t fr = (flags >> (4 * r)) & 0xFu;
+                uint32_t pos = rb + ((excl >> (8 * r)) & 0xFFu);
+                rb += (wtot >> (8 * r)) & 0xFFu;
+                if (!fr) continue;
+                const uint32_t e = 4u * (lane + 32 * r);
+                const float* g4 = &Gv[r].x;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if ((fr >> j) & 1u) dst[pos++] = make_uint2(m.rel + e + j, __float_as_uint(g4[j]));
+            }
+        }
+        __syncwarp();  // wb and the stage are rewritten later
+    }
+    cp_async_wait<0>();
 }
 
 __global__ void __launch_bounds__(NT, 3) ada_bins(const SegPlan* __restrict__ plan, int S, uint64_t N,
@@ -651,8 +725,10 @@ __global__ void __launch_bounds__(NT) ada_scan(const SegPlan* __restrict__ plan,
         for (int q = 0; q < 2; ++q) {
             c[q] = 0;
             if (g0 + q < ng) {
-                const uint32_t j0 = (g0 + q) * kGroup, j1 = j0 + kGroup < p.ntiles ? j0 + kGroup : p.ntiles;
-                for (uint32_t j = j0; j < j1; ++j) c[q] += tile_tab[t0 + j].y;
+                const uint32_t j0 = (g0 + q) * kGroup;
+#pragma unroll
+                for (uint32_t j = 0; j < kGroup; ++j)  // the group's counts, all loads in flight
+                    c[q] += j0 + j < p.ntiles ? tile_tab[t0 + j0 + j].y : 0u;
             }
         }
         uint64_t tot;
@@ -669,8 +745,15 @@ __global__ void __launch_bounds__(NT) ada_scan(const SegPlan* __restrict__ plan,
     const bool in_bins = p.mode == kModeBig || p.bpw;
     if (in_bins) {
         const uint32_t* bm = big + (uint64_t)k * big_per_learner + p.big_off;
-        double su = 0.0;
-        for (uint32_t b = threadIdx.x; b < p.nbins; b += NT) su = __dadd_rn(su, (double)__uint_as_float(bm[b]));
+        double sq[4] = {0.0, 0.0, 0.0, 0.0};  // four chains, so four loads and adds are in flight
+        uint32_t b = threadIdx.x;
+        for (; b + 3 * NT < p.nbins; b += 4 * NT)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) sq[q] = __dadd_rn(sq[q], (double)__uint_as_float(bm[b + q * NT]));
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (b + q * NT < p.nbins) sq[q] = __dadd_rn(sq[q], (double)__uint_as_float(bm[b + q * NT]));
+        double su = __dadd_rn(__dadd_rn(sq[0], sq[1]), __dadd_rn(sq[2], sq[3]));
 #pragma unroll
         for (int d = 16; d > 0; d >>= 1) su = __dadd_rn(su, __shfl_down_sync(kFull, su, d));
         if (lane == 0) s_wsum[warp] = su;
@@ -870,8 +953,17 @@ int adacomp_launch(const int64_t* off, int S, const int32_t* lt, int K, const fl
     }
     if (T > 0 && any_warp) {
         LaunchScope ls("ada_bins_warp", stream);
-        const uint64_t wgrid = (uint64_t)sm_count() * 4, need_ctas = (T + NT / 32 - 1) / (NT / 32);
-        ada_bins_warp<<<(unsigned)(need_ctas < wgrid ? need_ctas : wgrid), NT, 0, stream>>>(
+        static bool attr_set[64] = {};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (dev < 64 && !attr_set[dev]) {
+            if (cudaFuncSetAttribute(ada_bins_warp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBinsWarpSmem) !=
+                cudaSuccess)
+                return set_error(GCSGD_ERR_CUDA, "adacomp_compress: cannot raise the shared-memory limit");
+            attr_set[dev] = true;
+        }
+        const uint64_t wgrid = (uint64_t)sm_count() * 4, need_ctas = (T + NTW / 32 - 1) / (NTW / 32);
+        ada_bins_warp<<<(unsigned)(need_ctas < wgrid ? need_ctas : wgrid), NTW, kBinsWarpSmem, stream>>>(
             w.plan, S, N, (uint32_t)hp.tiles_per_learner, T, dW, R, w.big, hp.big_per_learner, w.tile_tab, w.pool);
         if ((rc = check_launch("ada_bins_warp"))) return rc;
     }

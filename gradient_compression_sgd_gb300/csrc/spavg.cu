@@ -515,7 +515,9 @@ __device__ void batch_lower_bound(const gcsgd_pair* lists, uint64_t cap, const u
     }
 }
 
-// Shared memory: acc[NW][kWSpan] floats | cnt[K] | cur[NW][K] (u32)
+// Shared memory: acc[NW][kWSpan] floats | cnt[K] | cur[NW][K] (u32).
+// REG (K <= kBatch): counts and cursors live in registers instead.
+template <bool REG>
 __global__ void __launch_bounds__(NT, 4) spavg_warp(const gcsgd_pair* __restrict__ lists, uint64_t cap,
                                                     const int64_t* __restrict__ counts, int K, uint64_t n,
                                                     float* __restrict__ out, uint64_t spans, uint64_t per_warp) {
@@ -527,7 +529,7 @@ __global__ void __launch_bounds__(NT, 4) spavg_warp(const gcsgd_pair* __restrict
     for (int k = threadIdx.x; k < K; k += NT) {
         const int64_t c = counts[k];
         const uint64_t cc = c < 0 ? 0 : ((uint64_t)c > cap ? cap : (uint64_t)c);
-        cnt[k] = (uint32_t)(cc < 0xffffffffu ? cc : 0xffffffffu);
+        cnt[k] = (uint32_t)(cc < 0xffffffffu - 64 ? cc : 0xffffffffu - 64);
     }
     for (uint32_t j = lane * 4; j < kWSpan; j += 128) *reinterpret_cast<float4*>(acc + j) = make_float4(0.f, 0.f, 0.f, 0.f);
     __syncthreads();
@@ -537,11 +539,19 @@ __global__ void __launch_bounds__(NT, 4) spavg_warp(const gcsgd_pair* __restrict
     for (int kb = 0; kb < K; kb += kBatch)
         batch_lower_bound(lists, cap, cnt, kb, K - kb < kBatch ? K - kb : kBatch, sp0 * kWSpan, cur);
     __syncwarp();
+    uint32_t rcur[kBatch], rcnt[kBatch];  // REG: list q's cursor and count (the same in every lane)
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+        rcur[q] = REG && q < K ? cur[q] : 0u;
+        rcnt[q] = REG && q < K ? cnt[q] : 0u;
+    }
     const float fk = (float)K, inv_k = 1.0f / fk;
     const bool pow2 = (K & (K - 1)) == 0;
     for (uint64_t sp = sp0; sp < sp1; ++sp) {
-        const uint64_t s0 = sp * kWSpan, s1 = s0 + kWSpan < n ? s0 + kWSpan : n;
-        for (int kb = 0; kb < K; kb += kBatch) {
+        // span [s0, s0 + len): an entry is inside iff idx - s0 < len in 32 bits (s0 < 2^32)
+        const uint32_t s0 = (uint32_t)(sp * kWSpan);
+        const uint32_t len = (uint32_t)((sp + 1) * kWSpan < n ? kWSpan : n - sp * kWSpan);
+        for (int kb = 0; kb < (REG ? 1 : K); kb += kBatch) {
             const int nb = K - kb < kBatch ? K - kb : kBatch;
             gcsgd_pair e[kBatch], f[kBatch];  // the next 64 entries of each list (two per lane)
 #pragma unroll
@@ -550,35 +560,40 @@ __global__ void __launch_bounds__(NT, 4) spavg_warp(const gcsgd_pair* __restrict
                 e[q].val = f[q].val = 0.0f;
                 if (q < nb) {
                     const gcsgd_pair* L = lists + (uint64_t)(kb + q) * cap;
-                    e[q] = load_entry(L, cur[kb + q] + lane, cnt[kb + q]);
-                    f[q] = load_entry(L, cur[kb + q] + 32 + lane, cnt[kb + q]);
+                    const uint32_t c0 = REG ? rcur[q] : cur[kb + q], c = REG ? rcnt[q] : cnt[kb + q];
+                    e[q] = load_entry(L, c0 + lane, c);
+                    f[q] = load_entry(L, c0 + 32 + lane, c);
                 }
             }
 #pragma unroll
             for (int q = 0; q < kBatch; ++q) {
                 if (q >= nb) break;
                 const int k = kb + q;
-                uint32_t c0 = cur[k];
+                const uint32_t ck = REG ? rcnt[q] : cnt[k];
+                uint32_t c0 = REG ? rcur[q] : cur[k];
                 gcsgd_pair it = e[q];
                 for (int round = 0;; ++round) {
-                    const bool in = c0 + lane < cnt[k] && (uint64_t)it.idx < s1;  // past the end: never
+                    // entries of this span form a prefix of the 32 (lists sorted ascending); an
+                    // entry below the span (an unsorted list) ends the prefix and stays unread
+                    const uint32_t d = it.idx - s0;
+                    const bool in = c0 + lane < ck && d < len;
                     const unsigned b = __ballot_sync(kFull, !in);
-                    const uint32_t c = b ? (uint32_t)__ffs(b) - 1 : 32u;  // entries of this span (a prefix)
-                    if ((uint32_t)lane < c && (uint64_t)it.idx >= s0) {
-                        float* a = acc + (it.idx - s0);
-                        *a = __fadd_rn(*a, it.val);
-                    }
+                    const uint32_t c = b ? (uint32_t)__ffs(b) - 1 : 32u;
+                    if ((uint32_t)lane < c) acc[d] = __fadd_rn(acc[d], it.val);
                     c0 += c;
                     if (c < 32) break;
-                    it = round == 0 ? f[q] : load_entry(lists + (uint64_t)k * cap, c0 + lane, cnt[k]);
+                    it = round == 0 ? f[q] : load_entry(lists + (uint64_t)k * cap, c0 + lane, ck);
                 }
                 __syncwarp();  // list k's adds land before list k+1's, and every lane has read cur[k]
-                if (lane == 0) cur[k] = c0;
-                __syncwarp();
+                if (REG) {
+                    rcur[q] = c0;
+                } else {
+                    if (lane == 0) cur[k] = c0;
+                    __syncwarp();
+                }
             }
         }
         // the span's average, written once; acc re-zeroed for the next span
-        const uint64_t len = s1 - s0;
         const bool al = ((uintptr_t)(out + s0) & 15) == 0;
 #pragma unroll
         for (int r = 0; r < (int)(kWSpan / 128); ++r) {
@@ -586,10 +601,17 @@ __global__ void __launch_bounds__(NT, 4) spavg_warp(const gcsgd_pair* __restrict
             float4 q = *reinterpret_cast<const float4*>(acc + j);
             *reinterpret_cast<float4*>(acc + j) = make_float4(0.f, 0.f, 0.f, 0.f);
             if (j >= len) continue;
-            q.x = div_k(q.x, fk, inv_k, pow2);
-            q.y = div_k(q.y, fk, inv_k, pow2);
-            q.z = div_k(q.z, fk, inv_k, pow2);
-            q.w = div_k(q.w, fk, inv_k, pow2);
+            if (pow2) {  // x * 2^-j is x / 2^j rounded once
+                q.x = __fmul_rn(q.x, inv_k);
+                q.y = __fmul_rn(q.y, inv_k);
+                q.z = __fmul_rn(q.z, inv_k);
+                q.w = __fmul_rn(q.w, inv_k);
+            } else {
+                q.x = div_k(q.x, fk, inv_k, false);
+                q.y = div_k(q.y, fk, inv_k, false);
+                q.z = div_k(q.z, fk, inv_k, false);
+                q.w = div_k(q.w, fk, inv_k, false);
+            }
             if (al && j + 4 <= len) {
                 *reinterpret_cast<float4*>(out + s0 + j) = q;
             } else {
@@ -600,7 +622,6 @@ __global__ void __launch_bounds__(NT, 4) spavg_warp(const gcsgd_pair* __restrict
         __syncwarp();
     }
 }
-
 
 }  // namespace spavg
 
@@ -619,8 +640,12 @@ int spavg_launch(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, in
         ctas = (spans + per_warp * NW - 1) / (per_warp * NW);
         const size_t wsmem = sizeof(float) * NW * kWSpan + sizeof(uint32_t) * (size_t)K * (NW + 1);
         LaunchScope ls("spavg", stream);
-        spavg_warp<<<(unsigned)ctas, NT, wsmem, stream>>>(lists, (uint64_t)cap, counts, K, (uint64_t)n, out, spans,
-                                                          per_warp);
+        if (K <= kBatch)
+            spavg_warp<true><<<(unsigned)ctas, NT, wsmem, stream>>>(lists, (uint64_t)cap, counts, K, (uint64_t)n, out,
+                                                                    spans, per_warp);
+        else
+            spavg_warp<false><<<(unsigned)ctas, NT, wsmem, stream>>>(lists, (uint64_t)cap, counts, K, (uint64_t)n,
+                                                                     out, spans, per_warp);
         return check_launch("spavg");
     }
     const uint64_t tiles = ((uint64_t)n + kTile - 1) / kTile;
