@@ -153,6 +153,22 @@ size_t layout(int S, int K, int64_t off_total, const HostPlan& hp, void* base, W
     return o;
 }
 
+// Double-float accumulation: (hi, lo) += (x, xl) with the rounding error of
+// hi + x kept exactly (TwoSum, Knuth), and renormalisation (FastTwoSum,
+// valid since |hi| >= |lo| after it).  fp32 only.
+__device__ __forceinline__ void df_add(float& hi, float& lo, float x, float xl) {
+    const float s = __fadd_rn(hi, x);
+    const float bp = __fsub_rn(s, hi);
+    const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(x, bp));
+    hi = s;
+    lo = __fadd_rn(lo, __fadd_rn(err, xl));
+}
+__device__ __forceinline__ void df_norm(float& hi, float& lo) {
+    const float s = __fadd_rn(hi, lo);
+    lo = __fsub_rn(lo, __fsub_rn(s, hi));
+    hi = s;
+}
+
 // Neumaier step: (s, c) += x.
 __device__ __forceinline__ void csum_add(double& s, double& c, double x) {
     const double t = __dadd_rn(s, x);
@@ -409,8 +425,9 @@ __global__ void __launch_bounds__(NTW, 4) ada_bins_warp(const SegPlan* __restric
                 for (int r = 0; r < 4; ++r) {
                     const uint32_t e = 4u * (lane + 32 * r);
                     const uint32_t by = e < m.clen ? (m.clen - e < 4 ? 4 * (m.clen - e) : 16u) : 0u;
-                    cp_async16(sD + e, by ? dWc + e : dWc, by);
-                    cp_async16(sR + e, by ? Rc + e : Rc, by);
+                    const uint32_t o = by ? e : 0u;  // a valid address also where nothing is read
+                    cp_async16(sD + e, dWc + o, by);
+                    cp_async16(sR + e, Rc + o, by);
                 }
             } else {  // 4-byte copies where the chunk is not 16-byte aligned
 #pragma unroll
@@ -433,9 +450,8 @@ __global__ void __launch_bounds__(NTW, 4) ada_bins_warp(const SegPlan* __restric
 #pragma unroll
     for (int st = 0; st < kRing - 1; ++st) issue(st);
 
-    for (int i = 0;; ++i) {
-        const int cs = i % kRing;
-        issue((i + kRing - 1) % kRing);  // that stage's chunk was computed in the previous round
+    for (int cs = 0;; cs = cs == kRing - 1 ? 0 : cs + 1) {
+        issue(cs == 0 ? kRing - 1 : cs - 1);  // that stage's chunk was computed in the previous round
         cp_async_wait<kRing - 1>();       // this lane's copies of chunk i have landed
         __syncwarp();                     // and lane 0's meta of it is visible
         const ChunkMeta m = meta[cs];
@@ -492,29 +508,39 @@ __global__ void __launch_bounds__(NTW, 4) ada_bins_warp(const SegPlan* __restric
         // selection (float compares, as the definition: |G + dW| >= bin max
         // and G != 0; a bin max of 0 leaves only G = 0 or NaN, never sent),
         // R <- G, candidate counts per round
-        uint32_t flags = 0, packed = 0;
+        uint32_t flags = 0;
+        if (bpw == 1) {  // one bin: one maximum for the whole chunk
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const float* g4 = &Gv[r].x;
+                const float* d4 = &Dv[r].x;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    flags |= (uint32_t)(fabsf(__fadd_rn(g4[j], d4[j])) >= m_one && g4[j] != 0.0f) << (4 * r + j);
+            }
+        } else {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const uint32_t e = 4u * (lane + 32 * r);
+                if (e >= clen) continue;  // zero-filled: nothing to send
+                const float* g4 = &Gv[r].x;
+                const float* d4 = &Dv[r].x;
+                const uint32_t b0 = bin_of(e, m.invL), cut = (b0 + 1) * L - e;
+                const float gm0 = __uint_as_float(wb[b0]);
+                const float gm1 = cut < 4 && b0 + 1 < bpw ? __uint_as_float(wb[b0 + 1]) : gm0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float gm = (uint32_t)j < cut ? gm0 : gm1;
+                    flags |= (uint32_t)(fabsf(__fadd_rn(g4[j], d4[j])) >= gm && g4[j] != 0.0f) << (4 * r + j);
+                }
+            }
+        }
+        uint32_t packed = 0;  // candidates per round, 8 bits each
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const uint32_t e = 4u * (lane + 32 * r);
             const float* g4 = &Gv[r].x;
-            const float* d4 = &Dv[r].x;
-            float gm0 = m_one, gm1 = m_one;
-            uint32_t cut = 4;
-            if (bpw != 1 && e < clen) {
-                const uint32_t b0 = bin_of(e, m.invL);
-                cut = (b0 + 1) * L - e;
-                gm0 = __uint_as_float(wb[b0]);
-                gm1 = cut < 4 && b0 + 1 < bpw ? __uint_as_float(wb[b0 + 1]) : gm0;
-            }
-            uint32_t f = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float gm = (uint32_t)j < cut ? gm0 : gm1;
-                const bool sel = fabsf(__fadd_rn(g4[j], d4[j])) >= gm && g4[j] != 0.0f;
-                f |= (uint32_t)sel << j;
-            }
-            flags |= f << (4 * r);
-            packed |= (uint32_t)__popc(f) << (8 * r);
+            packed |= (uint32_t)__popc((flags >> (4 * r)) & 0xFu) << (8 * r);
             if (cal && e + 4 <= clen) {
                 *reinterpret_cast<float4*>(Rc + e) = Gv[r];
             } else {
@@ -535,21 +561,18 @@ __global__ void __launch_bounds__(NTW, 4) ada_bins_warp(const SegPlan* __restric
             const uint32_t W = (wtot & 0xFFu) + ((wtot >> 8) & 0xFFu) + ((wtot >> 16) & 0xFFu) + (wtot >> 24);
             tile_tab[(uint64_t)m.k * tiles_per_learner + m.lt] = make_uint2(m.rel, W);
         }
-        if (flags) {
-            uint2* dst = pool + base;
-            uint32_t rb = 0;
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const uint32_t fr = (flags >> (4 * r)) & 0xFu;
-                uint32_t pos = rb + ((excl >> (8 * r)) & 0xFFu);
-                rb += (wtot >> (8 * r)) & 0xFFu;
-                if (!fr) continue;
-                const uint32_t e = 4u * (lane + 32 * r);
-                const float* g4 = &Gv[r].x;
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if ((fr >> j) & 1u) dst[pos++] = make_uint2(m.rel + e + j, __float_as_uint(g4[j]));
-            }
+        // each lane walks its set bits; the rank of bit 4r+j is (entries of the
+        // rounds before r) + (this round's entries of the lanes before) + (its
+        // earlier bits in the round); G is recomputed from the stage, which
+        // is rewritten only by the next round's copies
+        const uint32_t rb1 = wtot & 0xFFu, rb2 = rb1 + ((wtot >> 8) & 0xFFu), rb3 = rb2 + ((wtot >> 16) & 0xFFu);
+        uint2* dst = pool + base;
+        for (uint32_t fb = flags; fb; fb &= fb - 1u) {
+            const uint32_t bit = (uint32_t)__ffs(fb) - 1u, r = bit >> 2;
+            const uint32_t e = 4u * (lane + 32u * r) + (bit & 3u);
+            const uint32_t rb = r == 0 ? 0u : (r == 1 ? rb1 : (r == 2 ? rb2 : rb3));
+            const uint32_t rank = rb + ((excl >> (8 * r)) & 0xFFu) + __popc(flags & ((1u << bit) - 1u) & ~((1u << (4 * r)) - 1u));
+            dst[rank] = make_uint2(m.rel + e, __float_as_uint(__fadd_rn(sR[e], sD[e])));
         }
         __syncwarp();  // wb and the stage are rewritten later
     }
@@ -700,14 +723,18 @@ __global__ void __launch_bounds__(NT, 3) ada_bins(const SegPlan* __restrict__ pl
 }
 
 // One CTA per (learner, segment): output slots of the emit groups in index
-// order, the segment's count, and its scale = mean of the bin maxima.
-__global__ void __launch_bounds__(NT) ada_scan(const SegPlan* __restrict__ plan, int S,
+// order, the segment's count, and its scale = mean of the bin maxima.  The
+// work is a few loads per thread, so the CTA is wide (1024 threads) and every
+// round issues all of its loads before using any: the largest segments
+// (tens of thousands of tiles and bins) take a handful of memory latencies.
+constexpr int NTS = 1024;
+__global__ void __launch_bounds__(NTS) ada_scan(const SegPlan* __restrict__ plan, int S,
                                                uint32_t tiles_per_learner, const uint2* __restrict__ tile_tab,
                                                const double2* __restrict__ tile_sum, const uint32_t* __restrict__ big,
                                                uint64_t big_per_learner, uint32_t groups_per_learner,
                                                uint32_t* __restrict__ grp_rel,
                                                int64_t* __restrict__ counts, float* __restrict__ scales) {
-    __shared__ uint64_t scan[NT / 32 + 1];
+    __shared__ uint64_t scan[NTS / 32 + 1];
     const int unit = blockIdx.x;
     const int k = unit / S, s = unit - k * S;
     const SegPlan p = plan[s];
@@ -718,7 +745,7 @@ __global__ void __launch_bounds__(NT) ada_scan(const SegPlan* __restrict__ plan,
     uint64_t run = 0;
     const uint32_t ng = (p.ntiles + kGroup - 1) / kGroup;
     uint32_t* gr = grp_rel + (uint64_t)k * groups_per_learner + p.grp_off;
-    for (uint32_t gb = 0; gb < ng; gb += 2 * NT) {
+    for (uint32_t gb = 0; gb < ng; gb += 2 * NTS) {
         const uint32_t g0 = gb + 2 * threadIdx.x;
         uint32_t c[2];
 #pragma unroll
@@ -732,46 +759,64 @@ __global__ void __launch_bounds__(NT) ada_scan(const SegPlan* __restrict__ plan,
             }
         }
         uint64_t tot;
-        const uint64_t at = run + block_exclusive_scan<NT>(c[0] + c[1], scan, &tot);
+        const uint64_t at = run + block_exclusive_scan<NTS>(c[0] + c[1], scan, &tot);
         if (g0 < ng) gr[g0] = (uint32_t)at;
         if (g0 + 1 < ng) gr[g0 + 1] = (uint32_t)(at + c[0]);
         run += tot;
     }
-    // bins kept in the bins array (big bins, warp chunks): every thread adds
-    // a strided share in fp64 (plain adds: at most nbins / 256 per thread),
-    // then a fixed tree; the error stays far below the fp32 scale's rounding
-    __shared__ double s_wsum[NT / 32];
-    double bins_sum = 0.0;
+    // Bins kept in the bins array (big bins, warp chunks): a double-float
+    // sum (an fp32 pair hi + lo kept exact by TwoSum, renormalised after
+    // every 16 terms; about 2^-40 relative, far below the fp32 scale's
+    // rounding) in a fixed order: strided shares per thread, a shuffle tree,
+    // then the warps in order.  GB300's fp64 rate is a small fraction of its
+    // fp32 rate, so fp64 is kept to the final division.
+    __shared__ float s_hi[NTS / 32], s_lo[NTS / 32];
     const bool in_bins = p.mode == kModeBig || p.bpw;
     if (in_bins) {
         const uint32_t* bm = big + (uint64_t)k * big_per_learner + p.big_off;
-        double sq[4] = {0.0, 0.0, 0.0, 0.0};  // four chains, so four loads and adds are in flight
-        uint32_t b = threadIdx.x;
-        for (; b + 3 * NT < p.nbins; b += 4 * NT)
+        float hi = 0.0f, lo = 0.0f;
+        for (uint32_t b0 = 0; b0 < p.nbins; b0 += 16 * NTS) {  // sixteen loads in flight, then the adds
+            float v[16];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) sq[q] = __dadd_rn(sq[q], (double)__uint_as_float(bm[b + q * NT]));
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (b + q * NT < p.nbins) sq[q] = __dadd_rn(sq[q], (double)__uint_as_float(bm[b + q * NT]));
-        double su = __dadd_rn(__dadd_rn(sq[0], sq[1]), __dadd_rn(sq[2], sq[3]));
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) su = __dadd_rn(su, __shfl_down_sync(kFull, su, d));
-        if (lane == 0) s_wsum[warp] = su;
-        __syncthreads();
-        for (int q = 0; q < NT / 32; ++q) bins_sum = __dadd_rn(bins_sum, s_wsum[q]);
-    }
-    if (warp == 0) {
-        // compensated sum of the tiles' sums of bin maxima in bin order, 32 contiguous runs
-        double sm = 0.0, cm = 0.0;
-        if (p.mode == kModeSmall && !p.bpw) {
-            const uint32_t per = (p.ntiles + 31) / 32;
-            for (uint32_t j = lane * per; j < p.ntiles && j < (lane + 1) * per; ++j) {
-                const double2 ts = tile_sum[t0 + j];
-                csum_add(sm, cm, ts.x);
-                cm = __dadd_rn(cm, ts.y);
+            for (int q = 0; q < 16; ++q) {
+                const uint32_t b = b0 + q * NTS + threadIdx.x;
+                v[q] = b < p.nbins ? __uint_as_float(bm[b]) : 0.0f;  // + 0 is exact (maxima are >= 0)
             }
-        } else if (in_bins && lane == 0) {
-            sm = bins_sum;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) df_add(hi, lo, v[q], 0.0f);
+            df_norm(hi, lo);
+        }
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) {
+            const float oh = __shfl_down_sync(kFull, hi, d), ol = __shfl_down_sync(kFull, lo, d);
+            df_add(hi, lo, oh, ol);
+            df_norm(hi, lo);
+        }
+        if (lane == 0) {
+            s_hi[warp] = hi;
+            s_lo[warp] = lo;
+        }
+        __syncthreads();
+    }
+    if (in_bins) {
+        if (threadIdx.x == 0) {
+            float hi = 0.0f, lo = 0.0f;
+            for (int q = 0; q < NTS / 32; ++q) {
+                df_add(hi, lo, s_hi[q], s_lo[q]);
+                df_norm(hi, lo);
+            }
+            counts[unit] = (int64_t)run;
+            scales[unit] = p.nbins ? (float)(__dadd_rn((double)hi, (double)lo) / (double)p.nbins) : 0.0f;
+        }
+    } else if (warp == 0) {
+        // small bins in tiles: a compensated sum of the tiles' fp64 sums in
+        // tile order, 32 contiguous runs combined in lane order
+        double sm = 0.0, cm = 0.0;
+        const uint32_t per = (p.ntiles + 31) / 32;
+        for (uint32_t j = lane * per; j < p.ntiles && j < (lane + 1) * per; ++j) {
+            const double2 ts = tile_sum[t0 + j];
+            csum_add(sm, cm, ts.x);
+            cm = __dadd_rn(cm, ts.y);
         }
         double S0 = 0.0, C0 = 0.0;
         for (int l = 0; l < 32; ++l) {
@@ -976,7 +1021,7 @@ int adacomp_launch(const int64_t* off, int S, const int32_t* lt, int K, const fl
     }
     {
         LaunchScope ls("ada_scan", stream);
-        ada_scan<<<(unsigned)(K * S), NT, 0, stream>>>(w.plan, S, (uint32_t)hp.tiles_per_learner, w.tile_tab,
+        ada_scan<<<(unsigned)(K * S), NTS, 0, stream>>>(w.plan, S, (uint32_t)hp.tiles_per_learner, w.tile_tab,
                                                         w.tile_sum, w.big, hp.big_per_learner,
                                                         (uint32_t)hp.groups_per_learner, w.grp_rel, counts, scales);
         if ((rc = check_launch("ada_scan"))) return rc;
