@@ -75,6 +75,7 @@ def lib():
         L.gcsgd_launch_count_reset.restype = None
         L.gcsgd_trace_enable.argtypes = [i32]
         L.gcsgd_trace_read.argtypes = [vp, i32, vp]
+        L.gcsgd_trace_only.argtypes = [ctypes.c_char_p]
         L.gcsgd_dgc_k.restype = i64
         L.gcsgd_dgc_k.argtypes = [f64, i64]
         L.gcsgd_dgc_workspace_size.argtypes = [vp, i32, i32, f64, vp]
@@ -422,6 +423,11 @@ def launch_count_reset():
 
 def trace_enable(on: bool = True):
     lib().gcsgd_trace_enable(1 if on else 0)
+
+
+def trace_only(name=None):
+    """Trace only the launches of kernel `name` (None: every kernel)."""
+    _check("gcsgd_trace_only", lib().gcsgd_trace_only(name.encode() if name else None))
 
 
 def trace_read() -> dict:

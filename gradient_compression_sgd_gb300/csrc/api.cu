@@ -71,6 +71,7 @@ int sm_count() {
 static std::atomic<int64_t> g_launches{0};
 static std::atomic<bool> g_trace{false};
 static std::mutex g_trace_mu;
+static std::string g_trace_name;  // only this kernel is traced when non-empty (guarded by g_trace_mu)
 struct PendingEvent {
     std::string name;
     cudaEvent_t a, b;
@@ -93,6 +94,7 @@ LaunchScope::LaunchScope(const char* n, cudaStream_t s) : name(n), stream(s), sl
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (!g_trace.load(std::memory_order_relaxed)) return;
     std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (!g_trace_name.empty() && g_trace_name != n) return;
     cudaEvent_t a = take_event(), b = take_event();
     if (!a || !b) return;
     cudaEventRecord(a, s);
@@ -151,6 +153,14 @@ void gcsgd_launch_count_reset(void) { g_launches.store(0); }
 
 int gcsgd_trace_enable(int32_t on) {
     g_trace.store(on != 0);
+    return GCSGD_OK;
+}
+
+int gcsgd_trace_only(const char* name) {
+    if (name && strlen(name) >= sizeof(((gcsgd_trace_entry*)nullptr)->name))
+        return set_error(GCSGD_ERR_INVALID_ARG, "gcsgd_trace_only: name longer than 47 bytes");
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    g_trace_name = name ? name : "";
     return GCSGD_OK;
 }
 

@@ -355,6 +355,12 @@ typedef struct {
 } gcsgd_trace_entry;
 int gcsgd_trace_enable(int32_t on);
 int gcsgd_trace_read(gcsgd_trace_entry* entries, int32_t max, int32_t* n_out);
+/* Restricts tracing to the launches of one kernel name (as reported by
+ * gcsgd_trace_read), so that the events of the others do not sit between
+ * kernels of a timed region; NULL or "" traces every kernel again.  The name
+ * is copied.  Returns GCSGD_ERR_INVALID_ARG for a name of 48 bytes or more.
+ * Host. */
+int gcsgd_trace_only(const char* name);
 
 #ifdef __cplusplus
 }

@@ -115,3 +115,13 @@ def test_binding_refuses_cpu_tensors(L):
     with pytest.raises(TypeError):
         gc.dgc_compress(off, g, g, g, torch.zeros((1, 1, 2), dtype=torch.int32), torch.zeros((1, 1), dtype=torch.int64),
                         torch.zeros(1024, dtype=torch.uint8), 0.5, 0.9)
+
+
+def test_trace_filter_takes_and_clears_a_name(L):
+    """Selective tracing is host state: a name is accepted, an over-long one is
+    refused, and None goes back to tracing every kernel."""
+    gc.trace_only("dgc_update")
+    with pytest.raises(gc.GcsgdError):
+        gc.trace_only("x" * 48)
+    gc.trace_only(None)
+    assert L.gcsgd_trace_only(None) == 0
