@@ -87,30 +87,45 @@ struct RadixSmem {
 // First digit of a key: bits [30:20] (exponent and three mantissa bits).
 __device__ __forceinline__ void radix_hist_add(RadixSmem& rs, uint32_t key) { atomicAdd(&rs.hist[key >> 20], 1u); }
 
+// hist[bin] += 1 for every lane with `hit`, lanes with the same bin summed
+// first, so a warp issues one shared atomic per distinct bin (keys near a
+// selection threshold crowd into a few bins).  Called by the whole warp.
+__device__ __forceinline__ void hist_add_warp(uint32_t* hist, uint32_t bin, bool hit) {
+    const unsigned m = __match_any_sync(0xffffffffu, hit ? bin : 0xffffffffu);
+    if (hit && (threadIdx.x & 31) == (unsigned)__ffs(m) - 1u) atomicAdd(&hist[bin], (uint32_t)__popc(m));
+}
+
 template <int NT>
 __device__ __forceinline__ void radix_hist_clear(RadixSmem& rs) {
     for (int b = threadIdx.x; b < 2048; b += NT) rs.hist[b] = 0;
 }
 
 // Histogram of digit (key >> shift) & (nb - 1) over the keys whose bits under
-// pmask equal prefix.  Ends synchronised.
-template <int NT, class Load>
+// pmask equal prefix.  GLOBAL (keys loaded from global memory, many of them
+// near the threshold): eight loads in flight per thread and warp-aggregated
+// adds; else four and plain shared atomics.  Ends synchronised.
+template <int NT, bool GLOBAL, class Load>
 __device__ void radix_count(RadixSmem& rs, Load load, uint64_t count, uint32_t pmask, uint32_t prefix, int shift,
                             int nb) {
+    constexpr int LPT = GLOBAL ? 8 : 4;
     for (int b = threadIdx.x; b < nb; b += NT) rs.hist[b] = 0;
     __syncthreads();
-    for (uint64_t base = 0; base < count; base += 4 * (uint64_t)NT) {
-        uint32_t key[4];
-        bool ok[4];
+    for (uint64_t base = 0; base < count; base += LPT * (uint64_t)NT) {
+        uint32_t key[LPT];
+        bool ok[LPT];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {  // four independent loads in flight
+        for (int j = 0; j < LPT; ++j) {  // independent loads in flight
             const uint64_t i = base + (uint64_t)j * NT + threadIdx.x;
             key[j] = 0;
             ok[j] = (i < count) && load(i, &key[j]);
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (ok[j] && ((key[j] & pmask) == prefix)) atomicAdd(&rs.hist[(key[j] >> shift) & (uint32_t)(nb - 1)], 1u);
+        for (int j = 0; j < LPT; ++j) {
+            const bool hit = ok[j] && (key[j] & pmask) == prefix;
+            const uint32_t bin = (key[j] >> shift) & (uint32_t)(nb - 1);
+            if (GLOBAL) hist_add_warp(rs.hist, bin, hit);
+            else if (hit) atomicAdd(&rs.hist[bin], 1u);
+        }
     }
     __syncthreads();
 }
@@ -152,12 +167,14 @@ __device__ void radix_pick(RadixSmem& rs, int nb, uint32_t need, uint32_t* bucke
 // added every key's first digit into rs.hist (radix_hist_clear, then
 // radix_hist_add per key, then a barrier).  PASSES = 3 is exact; PASSES = 2
 // returns the rank-th largest key with its low 9 bits cleared (greater and
-// ties then refer to the truncated keys).  Every thread must call it.
-template <int NT, int PASSES, class Load>
+// ties then refer to the truncated keys).  GLOBAL: `load` reads global
+// memory (see radix_count).  Every thread must call it.
+template <int NT, int PASSES, bool GLOBAL = false, class Load>
 __device__ SelectResult radix_select_desc(Load load, uint64_t count, uint32_t rank, RadixSmem& rs, bool hist_ready) {
     static_assert(PASSES == 2 || PASSES == 3, "two or three digits");
+    constexpr int LPT = GLOBAL ? 8 : 4;
     const int lane = threadIdx.x & 31;
-    if (!hist_ready) radix_count<NT>(rs, load, count, 0u, 0u, 20, 2048);
+    if (!hist_ready) radix_count<NT, GLOBAL>(rs, load, count, 0u, 0u, 20, 2048);
     uint32_t b, ab, c1;
     radix_pick<NT>(rs, 2048, rank, &b, &ab, &c1);
     uint32_t prefix = b << 20, pmask = 0x7ffu << 20, need = rank - ab, greater = ab;
@@ -165,17 +182,17 @@ __device__ SelectResult radix_select_desc(Load load, uint64_t count, uint32_t ra
     if (compact) {
         if (threadIdx.x == 0) rs.sel[3] = 0;
         __syncthreads();
-        for (uint64_t base = 0; base < count; base += 4 * (uint64_t)NT) {
-            uint32_t key[4];
-            bool ok[4];
+        for (uint64_t base = 0; base < count; base += LPT * (uint64_t)NT) {
+            uint32_t key[LPT];
+            bool ok[LPT];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < LPT; ++j) {
                 const uint64_t i = base + (uint64_t)j * NT + threadIdx.x;
                 key[j] = 0;
                 ok[j] = (i < count) && load(i, &key[j]);
             }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < LPT; ++j) {
                 const bool hit = ok[j] && (key[j] & pmask) == prefix;
                 const unsigned m = __ballot_sync(kFull, hit);
                 if (m) {
@@ -193,8 +210,8 @@ __device__ SelectResult radix_select_desc(Load load, uint64_t count, uint32_t ra
     for (int pass = 1; pass < PASSES; ++pass) {
         const int shift = pass == 1 ? 9 : 0;
         const int nb = pass == 1 ? 2048 : 512;
-        if (compact) radix_count<NT>(rs, cand, c1, pmask, prefix, shift, nb);
-        else radix_count<NT>(rs, load, count, pmask, prefix, shift, nb);
+        if (compact) radix_count<NT, false>(rs, cand, c1, pmask, prefix, shift, nb);
+        else radix_count<NT, GLOBAL>(rs, load, count, pmask, prefix, shift, nb);
         uint32_t cb;
         radix_pick<NT>(rs, nb, need, &b, &ab, &cb);
         prefix |= b << shift;

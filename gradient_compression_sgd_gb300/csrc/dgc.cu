@@ -671,6 +671,7 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
                     const uint32_t q = q0 + jj * NTS + threadIdx.x;
+                    it[jj] = make_uint2(0u, 0u);
                     if (q < total) {
                         int lo = 0, hi = kChunkTiles;  // last tile with toff <= q
                         while (hi - lo > 1) {
@@ -763,7 +764,7 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
     }
     if (!pool_ok) {
         // the hint failed: select among all of the segment's v' in global memory
-        const SelectResult r = radix_select_desc<NTS, 3>(
+        const SelectResult r = radix_select_desc<NTS, 3, true>(
             [&](uint64_t i, uint32_t* key) { *key = mag_key(vseg[i]); return true; }, p.n, p.k, rs, false);
         emit_in_order(
             [&](uint32_t i, uint32_t* loc, uint32_t* bits) {
@@ -776,7 +777,7 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
     // a valid pool too large to stage: select from global memory, emit through the tile table
     uint32_t T = 0, ties = pc;  // take_all: every candidate goes
     if (!take_all) {
-        const SelectResult r = radix_select_desc<NTS, 3>(
+        const SelectResult r = radix_select_desc<NTS, 3, true>(
             [&](uint64_t i, uint32_t* key) { *key = __ldg(&items[i].y) & 0x7fffffffu; return true; }, pc, p.k, rs,
             false);
         T = r.thresh;
@@ -791,32 +792,56 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
         tbase[threadIdx.x] = ent.x;
         __syncthreads();
         const uint32_t chunk_items = (uint32_t)tot;
-        for (uint32_t ib = 0; ib < chunk_items; ib += NTS) {
-            const uint32_t q = ib + threadIdx.x;
-            uint32_t local = 0xffffffffu, bits = 0;
-            const bool live = q < chunk_items;
-            if (live) {
-                int lo = 0, hi = NTS;
+        constexpr int IPT = 8;  // consecutive items per thread per round: eight loads in flight
+        for (uint32_t ib = 0; ib < chunk_items; ib += IPT * NTS) {
+            const uint32_t q0 = ib + IPT * threadIdx.x;
+            uint32_t local[IPT], bits[IPT];
+            uint32_t ngt = 0, neq = 0;
+            int lo = 0;  // last tile with toff <= q0, then walked forward item by item
+            if (q0 < chunk_items) {
+                int hi = NTS;
                 while (hi - lo > 1) {
                     const int mid = (lo + hi) >> 1;
-                    if (toff[mid] <= q) lo = mid; else hi = mid;
+                    if (toff[mid] <= q0) lo = mid; else hi = mid;
                 }
-                const uint2 it = items[tbase[lo] + (q - toff[lo])];
-                local = it.x;
-                bits = it.y;
             }
-            const uint32_t key = bits & 0x7fffffffu;
-            const bool gt = live && key > T, eq = live && key == T;
-            const uint64_t ex2 = block_exclusive_scan<NTS>((uint64_t)gt | ((uint64_t)eq << 32), rs.scan, &tot);
-            const uint32_t gb = run_gt + (uint32_t)ex2, eb = run_eq + (uint32_t)(ex2 >> 32);
-            const uint32_t slot = gb + (eb < ties ? eb : ties);
-            if ((gt || (eq && eb < ties)) && slot < p.k && local < p.n) {
-                gcsgd_pair pr;
-                pr.idx = p.off + local;
-                pr.val = __uint_as_float(bits);
-                dst[slot] = pr;
-                u[ebase + local] = 0.0f;
-                v[ebase + local] = 0.0f;
+#pragma unroll
+            for (int j = 0; j < IPT; ++j) {
+                const uint32_t q = q0 + j;
+                local[j] = 0xffffffffu;
+                bits[j] = 0u;
+                if (q < chunk_items) {
+                    while (lo + 1 < NTS && toff[lo + 1] <= q) ++lo;
+                    const uint2 it = items[tbase[lo] + (q - toff[lo])];
+                    local[j] = it.x;
+                    bits[j] = it.y;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < IPT; ++j) {
+                const uint32_t key = bits[j] & 0x7fffffffu;
+                const bool live = q0 + j < chunk_items;
+                ngt += live && key > T;
+                neq += live && key == T;
+            }
+            const uint64_t ex2 = block_exclusive_scan<NTS>((uint64_t)ngt | ((uint64_t)neq << 32), rs.scan, &tot);
+            uint32_t gb = run_gt + (uint32_t)ex2, eb = run_eq + (uint32_t)(ex2 >> 32);
+#pragma unroll
+            for (int j = 0; j < IPT; ++j) {
+                const uint32_t key = bits[j] & 0x7fffffffu;
+                const bool live = q0 + j < chunk_items;
+                const bool gt = live && key > T, eq = live && key == T;
+                const uint32_t slot = gb + (eb < ties ? eb : ties);
+                if ((gt || (eq && eb < ties)) && slot < p.k && local[j] < p.n) {
+                    gcsgd_pair pr;
+                    pr.idx = p.off + local[j];
+                    pr.val = __uint_as_float(bits[j]);
+                    dst[slot] = pr;
+                    u[ebase + local[j]] = 0.0f;
+                    v[ebase + local[j]] = 0.0f;
+                }
+                gb += gt;
+                eb += eq;
             }
             run_gt += (uint32_t)tot;
             run_eq += (uint32_t)(tot >> 32);
