@@ -117,29 +117,72 @@ int host_plan(const int64_t* off, int S, double density, double sample_frac, Hos
 
 // ---------------------------------------------------------------- kernels
 
-// Sum of squares of learner blockIdx.y's gradient over a fixed slice, fp64
-// with exact products (fma), reduced in a fixed tree: deterministic.
+// Sum of squares of learner blockIdx.y's gradient over a fixed slice.  Each
+// square is split exactly into x*x = p + e (p rounded, e = fma(x, x, -p));
+// the terms are summed as double-float (an fp32 pair kept exact by TwoSum,
+// renormalised every 8 elements; ~2^-40 relative), reduced in a fixed tree
+// and stored as fp64: deterministic, and no per-element fp64 arithmetic,
+// whose rate on GB300 is a small fraction of fp32's.
+__device__ __forceinline__ void dsq_add(float& hi, float& lo, float x) {
+    const float p = __fmul_rn(x, x);
+    const float e = __fmaf_rn(x, x, -p);
+    const float s = __fadd_rn(hi, p);
+    const float bp = __fsub_rn(s, hi);
+    const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(p, bp));
+    hi = s;
+    lo = __fadd_rn(lo, __fadd_rn(err, e));
+}
+__device__ __forceinline__ void dsq_merge(float& hi, float& lo, float oh, float ol) {
+    const float s = __fadd_rn(hi, oh);
+    const float bp = __fsub_rn(s, hi);
+    const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(oh, bp));
+    lo = __fadd_rn(lo, __fadd_rn(err, ol));
+    hi = s;
+}
+__device__ __forceinline__ void dsq_norm(float& hi, float& lo) {
+    const float s = __fadd_rn(hi, lo);
+    lo = __fsub_rn(lo, __fsub_rn(s, hi));
+    hi = s;
+}
+
 __global__ void __launch_bounds__(NT) dgc_sumsq(const float* __restrict__ grad, uint64_t N,
                                                  double* __restrict__ part) {
-    __shared__ double red[NT / 32];
+    __shared__ float red_hi[NT / 32], red_lo[NT / 32];
     const uint64_t k = blockIdx.y;
     const uint64_t chunk = (N + gridDim.x - 1) / gridDim.x;
-    const uint64_t lo = (uint64_t)blockIdx.x * chunk;
-    const uint64_t hi = lo + chunk < N ? lo + chunk : N;
+    const uint64_t lo_i = (uint64_t)blockIdx.x * chunk;
+    const uint64_t hi_i = lo_i + chunk < N ? lo_i + chunk : N;
     const float* g = grad + k * N;
-    double acc = 0.0;
-    for (uint64_t i = lo + threadIdx.x; i < hi; i += NT) {
-        const double x = (double)__ldg(g + i);
-        acc = __fma_rn(x, x, acc);
+    float hi = 0.0f, lo = 0.0f;
+    for (uint64_t i0 = lo_i; i0 < hi_i; i0 += 8 * (uint64_t)NT) {
+        float x[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {  // eight loads in flight
+            const uint64_t i = i0 + (uint64_t)j * NT + threadIdx.x;
+            x[j] = i < hi_i ? __ldg(g + i) : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) dsq_add(hi, lo, x[j]);
+        dsq_norm(hi, lo);
     }
 #pragma unroll
-    for (int d = 16; d > 0; d >>= 1) acc = __dadd_rn(acc, __shfl_down_sync(kFull, acc, d));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+    for (int d = 16; d > 0; d >>= 1) {
+        const float oh = __shfl_down_sync(kFull, hi, d), ol = __shfl_down_sync(kFull, lo, d);
+        dsq_merge(hi, lo, oh, ol);
+        dsq_norm(hi, lo);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        red_hi[threadIdx.x >> 5] = hi;
+        red_lo[threadIdx.x >> 5] = lo;
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
-        double s = 0.0;
-        for (int w = 0; w < NT / 32; ++w) s = __dadd_rn(s, red[w]);
-        part[k * gridDim.x + blockIdx.x] = s;
+        float h = 0.0f, l = 0.0f;
+        for (int w = 0; w < NT / 32; ++w) {
+            dsq_merge(h, l, red_hi[w], red_lo[w]);
+            dsq_norm(h, l);
+        }
+        part[k * gridDim.x + blockIdx.x] = __dadd_rn((double)h, (double)l);
     }
 }
 
