@@ -101,6 +101,40 @@ def test_dgc_full_size(cuda_lib, config):
     np.testing.assert_array_equal(avg.cpu().numpy(), want)
 
 
+def check_adacomp_bins(gc, a, off, lt, dW, R_prev, R, out, totals, seed, bins_per_learner=64):
+    """Every learner, sampled bins: the sent indices of a bin are exactly those
+    with |G + dW| >= the bin's max |G| and G != 0 (G = R_prev + dW in fp32),
+    each sent as sign(G) * the segment's scale, and the residue is G minus
+    what was sent.  Holds at any size; uses only the GPU's inputs."""
+    K = dW.shape[0]
+    counts = a.counts.cpu().numpy()
+    scales = a.scales.cpu().numpy()
+    tot = totals.cpu().numpy()
+    rng = np.random.default_rng(seed)
+    segs = [s for s in range(len(off) - 1) if off[s + 1] > off[s]]
+    for k in range(K):
+        n_k = int(tot[k])
+        idx = gc.pair_indices(out)[k, :n_k].cpu().numpy()
+        val = gc.pair_values(out)[k, :n_k].cpu().numpy()
+        assert n_k == int(counts[k].sum()) and np.all(np.diff(idx) > 0)
+        for _ in range(bins_per_learner):
+            s = int(rng.choice(segs))
+            L, n = int(lt[s]), int(off[s + 1] - off[s])
+            b = int(rng.integers(0, (n + L - 1) // L))
+            lo, hi = int(off[s]) + b * L, int(off[s]) + min((b + 1) * L, n)
+            G = (R_prev[k, lo:hi] + dW[k, lo:hi]).cpu().numpy()
+            d = dW[k, lo:hi].cpu().numpy()
+            gmax = np.float32(np.nanmax(np.abs(np.where(np.isnan(G), 0, G)))) if hi > lo else np.float32(0)
+            with np.errstate(invalid="ignore"):
+                sel = (np.abs(G + d) >= gmax) & (gmax > 0) & (G != 0)
+            a0, a1 = np.searchsorted(idx, [lo, hi])
+            np.testing.assert_array_equal(idx[a0:a1], lo + np.nonzero(sel)[0], err_msg=f"k={k} s={s} bin={b}")
+            q = np.where(G > 0, scales[k, s], -scales[k, s]).astype(np.float32)
+            np.testing.assert_array_equal(val[a0:a1], q[sel])
+            r_want = np.where(sel, G - q, G).astype(np.float32)
+            np.testing.assert_array_equal(R[k, lo:hi].cpu().numpy(), r_want)
+
+
 def test_adacomp_full_size(cuda_lib):
     """LSTM (66,034,000 values, L_T = 500) + VGG-16 convs (14,714,688, L_T = 50),
     K = 8, two steps; learner 0 against the oracle; selection rule checked for
@@ -115,8 +149,10 @@ def test_adacomp_full_size(cuda_lib):
     R0 = np.zeros((1, N), np.float32)
     for t in range(2):
         dW = wl.gradients(w, t, device="cuda")
+        R_prev = R.clone()
         out, totals = a(dW, R)
         torch.cuda.synchronize()
+        check_adacomp_bins(gc, a, off, w.lt, dW, R_prev, R, out, totals, seed=t)
         idx_o, val_o, counts_o, scales_o, totals_o = oracle.adacomp_step(off, w.lt, dW[0:1].cpu().numpy(), R0,
                                                                          cap=cap)
         np.testing.assert_array_equal(a.counts[0].cpu().numpy(), counts_o[0])
