@@ -254,8 +254,16 @@ def config_dict(w, **extra):
 
 
 def kernel_source_sha(name: str = "dgc.cu") -> str:
-    with open(os.path.join(ROOT, "gradient_compression_sgd_gb300", "csrc", name), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """First 16 hex digits of the sha256 of a kernel source file with its
+    comments and blank space removed: a comment edit keeps a profile's DRAM
+    counters valid, any code change voids them."""
+    import re
+    with open(os.path.join(ROOT, "gradient_compression_sgd_gb300", "csrc", name)) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    src = "\n".join(line.strip() for line in src.splitlines() if line.strip())
+    return hashlib.sha256(src.encode()).hexdigest()[:16]
 
 
 KERNEL_SOURCE = {"dgc_update": "dgc.cu", "ada_bins": "adacomp.cu", "ada_bins_warp": "adacomp.cu", "dcd_step": "dcd.cu", "spavg": "spavg.cu"}

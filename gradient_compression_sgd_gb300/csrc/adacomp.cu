@@ -332,9 +332,9 @@ __device__ __forceinline__ void select_tile(const float4 (&Gv)[4], const float4 
 // chunk's end the copies zero-fill: G = 0 never raises a maximum and is never
 // sent, so the arithmetic needs no bounds test.  Per chunk the warp finds its
 // bins' maxima (one bin: a warp reduction; several: shared-memory atomicMax
-// per float4 part), writes them to the bins array (ada_scan averages them in
-// fp64), selects, stores R <- G and writes its candidates in index order
-// into the pool slots of its own index range.
+// per float4 part), writes them to the bins array (ada_scan averages them),
+// selects, stores R <- G and writes its candidates in index order into the
+// pool slots of its own index range.
 constexpr int NTW = 128;   // threads of an ada_bins_warp CTA
 constexpr int kRing = 3;   // stages per warp
 struct ChunkMeta {         // what the computing side needs of an issued chunk

@@ -178,7 +178,9 @@ int dgc_compress_noalloc(const int64_t* seg_offsets, int32_t n_seg, int32_t K,
 /* -------------------------------------------------------------- AdaComp */
 
 /* Bytes of device workspace adacomp_compress needs.  lt: host [n_seg] bin
- * lengths L_T >= 1. Host function. */
+ * lengths L_T >= 1.  Dominated by the candidate pool, 8 B per element per
+ * learner (every tile writes its candidates into the slots of its own index
+ * range, so no counter is shared); cap does not change it.  Host function. */
 int gcsgd_adacomp_workspace_size(const int64_t* seg_offsets, int32_t n_seg, const int32_t* lt,
                                  int32_t K, int64_t cap, size_t* bytes);
 
@@ -188,7 +190,8 @@ int gcsgd_adacomp_workspace_size(const int64_t* seg_offsets, int32_t n_seg, cons
  *   G = R + dW; per bin of L_T values (a last partial bin is a bin of its
  *   own) gmax = max |G|; an entry is selected when |G + dW| >= gmax of its
  *   bin, gmax > 0 and G != 0; scale_s = mean of gmax over every bin of the
- *   segment (fp64 sum, rounded to fp32 once); a selected entry is sent as
+ *   segment (the sum accurate to 2^-40 relative or better, divided in fp64
+ *   and rounded to fp32 once); a selected entry is sent as
  *   sign(G)*scale_s and the residue keeps R = G - sign(G)*scale_s; an
  *   unselected entry keeps R = G.
  *
