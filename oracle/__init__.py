@@ -51,6 +51,8 @@ def lib():
             L.oracle_dgc_step.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, ctypes.c_double,
                                           ctypes.c_float, ctypes.c_float, ctypes.c_int, vp, vp,
                                           ctypes.c_int64, vp, vp]
+            L.oracle_dgc_step_nesterov.restype = ctypes.c_int
+            L.oracle_dgc_step_nesterov.argtypes = L.oracle_dgc_step.argtypes
             L.oracle_dgc_step_sampled.restype = ctypes.c_int
             L.oracle_dgc_step_sampled.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, ctypes.c_double,
                                                   ctypes.c_double, ctypes.c_float, ctypes.c_float, ctypes.c_int, vp,
@@ -112,8 +114,9 @@ def dgc_k(density: float, n: int) -> int:
     return int(lib().oracle_dgc_k(float(density), int(n)))
 
 
-def dgc_step(offsets, grad, u, v, density, momentum, clip_thr=0.0, clip_nodes=1, cap=None):
+def dgc_step(offsets, grad, u, v, density, momentum, clip_thr=0.0, clip_nodes=1, cap=None, nesterov=False):
     """One DGC step of K learners. ``u``/``v`` ([K, N] float32) are updated in place.
+    ``nesterov``: the accumulated state takes the look-ahead step m*u + g.
 
     Returns (idx [K, cap] uint32, val [K, cap] float32, counts [K, S] int64,
     clip_scale [K] float32).
@@ -129,8 +132,9 @@ def dgc_step(offsets, grad, u, v, density, momentum, clip_thr=0.0, clip_nodes=1,
     val = np.zeros((K, cap), dtype=np.float32)
     counts = np.zeros((K, S), dtype=np.int64)
     cs = np.zeros(K, dtype=np.float32)
-    rc = lib().oracle_dgc_step(K, S, _p(off), _p(grad), _p(u), _p(v), float(density), float(momentum),
-                               float(clip_thr), int(clip_nodes), _p(idx), _p(val), int(cap), _p(counts), _p(cs))
+    fn = lib().oracle_dgc_step_nesterov if nesterov else lib().oracle_dgc_step
+    rc = fn(K, S, _p(off), _p(grad), _p(u), _p(v), float(density), float(momentum),
+            float(clip_thr), int(clip_nodes), _p(idx), _p(val), int(cap), _p(counts), _p(cs))
     _check(rc, "oracle_dgc_step")
     return idx, val, counts, cs
 

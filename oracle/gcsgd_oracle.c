@@ -127,8 +127,8 @@ static int dgc_sampled(int64_t n, int64_t ks, double sample_frac) {
 
 static int dgc_step_impl(int K, int S, const int64_t* seg_off,
                          const float* grad, float* u, float* v,
-                         double density, double sample_frac, float momentum, float clip_thr, int clip_nodes,
-                         uint32_t* out_idx, float* out_val, int64_t cap,
+                         double density, double sample_frac, float momentum, int nesterov, float clip_thr,
+                         int clip_nodes, uint32_t* out_idx, float* out_val, int64_t cap,
                          int64_t* counts, float* clip_scale) {
     if (K < 1 || S < 1 || !(density > 0.0 && density <= 1.0) || clip_nodes < 1) return ORACLE_EINVAL;
     if (!(sample_frac >= 0.0 && sample_frac <= 1.0)) return ORACLE_EINVAL;
@@ -161,12 +161,19 @@ static int dgc_step_impl(int K, int S, const int64_t* seg_off,
         }
         if (clip_scale) clip_scale[k] = c;
 
-        /* 2. momentum correction: accumulate the momentum-adjusted gradient */
+        /* 2. momentum correction: accumulate the momentum-adjusted gradient
+         * (Nesterov: the accumulated state takes the look-ahead step m*u + g) */
         for (int64_t i = 0; i < N; ++i) {
             float g = clipped ? G[i] * c : G[i];
             float mu = momentum * uk[i];
             uk[i] = mu + g;
-            vk[i] = vk[i] + uk[i];
+            if (nesterov) {
+                float step = momentum * uk[i];
+                step = step + g;
+                vk[i] = vk[i] + step;
+            } else {
+                vk[i] = vk[i] + uk[i];
+            }
         }
 
         /* 3 + 4. per-tensor top-k of |v|, send, then mask u and v */
@@ -228,8 +235,31 @@ int oracle_dgc_step(int K, int S, const int64_t* seg_off,
                     double density, float momentum, float clip_thr, int clip_nodes,
                     uint32_t* out_idx, float* out_val, int64_t cap,
                     int64_t* counts, float* clip_scale) {
-    return dgc_step_impl(K, S, seg_off, grad, u, v, density, 0.0, momentum, clip_thr, clip_nodes, out_idx, out_val,
-                         cap, counts, clip_scale);
+    return dgc_step_impl(K, S, seg_off, grad, u, v, density, 0.0, momentum, 0, clip_thr, clip_nodes, out_idx,
+                         out_val, cap, counts, clip_scale);
+}
+
+/*
+ * The DGC step with Nesterov momentum ("Deep Gradient Compression",
+ * Appendix B, gradient sparsification with Nesterov momentum correction).
+ * The page states the shape of the update, not its equations: after the
+ * correction the update keeps the local momentum and an accumulated state,
+ * and conventional Nesterov momentum steps by the look-ahead m*u + g.
+ * Reading (parity unpinned by the page): per element, in fp32 with one
+ * rounding per operation,
+ *   u <- m*u + g        (local momentum, as in the vanilla step)
+ *   v <- v + (m*u + g)  (the accumulated state takes the Nesterov step,
+ *                        with the u just updated)
+ * then the same clipping, per-tensor top-k of |v|, sending and masking of u
+ * and v as oracle_dgc_step.  With m = 0 it is the vanilla step.
+ */
+int oracle_dgc_step_nesterov(int K, int S, const int64_t* seg_off,
+                             const float* grad, float* u, float* v,
+                             double density, float momentum, float clip_thr, int clip_nodes,
+                             uint32_t* out_idx, float* out_val, int64_t cap,
+                             int64_t* counts, float* clip_scale) {
+    return dgc_step_impl(K, S, seg_off, grad, u, v, density, 0.0, momentum, 1, clip_thr, clip_nodes, out_idx,
+                         out_val, cap, counts, clip_scale);
 }
 
 /* The DGC step with the sampled threshold (see dgc_sampled above). */
@@ -239,8 +269,8 @@ int oracle_dgc_step_sampled(int K, int S, const int64_t* seg_off,
                             uint32_t* out_idx, float* out_val, int64_t cap,
                             int64_t* counts, float* clip_scale) {
     if (!(sample_frac > 0.0)) return ORACLE_EINVAL;
-    return dgc_step_impl(K, S, seg_off, grad, u, v, density, sample_frac, momentum, clip_thr, clip_nodes, out_idx,
-                         out_val, cap, counts, clip_scale);
+    return dgc_step_impl(K, S, seg_off, grad, u, v, density, sample_frac, momentum, 0, clip_thr, clip_nodes,
+                         out_idx, out_val, cap, counts, clip_scale);
 }
 
 /* --------------------------------------------------------- AdaComp (step) */

@@ -296,3 +296,61 @@ def test_sampled_hand_example_rank_above_one():
     assert counts.tolist() == [[12]]
     assert idx[0, :12].tolist() == want
     assert v[0, 65] == np.float32(100.5) and v[0, 0] == np.float32(100.0)
+
+
+# ------------------------------------------------ Nesterov momentum (reading)
+
+def test_nesterov_worked_example(golden):
+    """The hand-worked two-step example of the Nesterov reading (v takes m*u + G)."""
+    ex = golden("dgc_nesterov_worked_example.txt")
+    sizes = [int(x) for x in ex["sizes"]]
+    off = np.array([0, sizes[0], sizes[0] + sizes[1]], dtype=np.int64)
+    N = off[-1]
+    u = np.zeros((1, N), np.float32)
+    v = np.zeros((1, N), np.float32)
+    for t in (1, 2):
+        idx, val, counts, _ = oracle.dgc_step(off, f32(ex[f"grad{t}"])[None], u, v, float(ex["density"][0]),
+                                              float(ex["momentum"][0]), nesterov=True)
+        tot = counts.sum()
+        assert list(idx[0, :tot]) == [int(x) for x in ex[f"sent{t}_idx"]]
+        np.testing.assert_array_equal(val[0, :tot], f32(ex[f"sent{t}_val"]))
+        np.testing.assert_array_equal(u[0], f32(ex[f"u{t}"]))
+        np.testing.assert_array_equal(v[0], f32(ex[f"v{t}"]))
+
+
+def test_nesterov_closed_form():
+    """Exact rationals: an entry never sent follows u_T = sum_j m^(T-1-j) G_j and
+    v_T = sum_j G_j (1 + m (1 - m^(T-j)) / (1 - m)); the entry sent every step
+    restarts from zero, so it sends (1 + m) G_t."""
+    rng = np.random.default_rng(11)
+    n, T, m = 16, 6, Fraction(1, 2)
+    Gs = rng.integers(-8, 9, size=(T, n)).astype(np.float32)
+    Gs[:, 0] = 1e6 * np.array([1, -1, 1, -1, 1, -1])[:T]
+    u = np.zeros((1, n), np.float32)
+    v = np.zeros((1, n), np.float32)
+    off = np.array([0, n], np.int64)
+    for t in range(T):
+        idx, val, counts, _ = oracle.dgc_step(off, Gs[t][None], u, v, 1.0 / n, 0.5, nesterov=True)
+        assert counts[0, 0] == 1 and idx[0, 0] == 0 and val[0, 0] == np.float32(1.5) * Gs[t, 0]
+    for i in range(1, n):
+        uT = sum(m ** (T - 1 - j) * Fraction(float(Gs[j, i])) for j in range(T))
+        vT = sum(Fraction(float(Gs[j, i])) * (1 + m * (1 - m ** (T - j)) / (1 - m)) for j in range(T))
+        assert Fraction(float(u[0, i])) == uT
+        assert Fraction(float(v[0, i])) == vT
+
+
+def test_nesterov_with_zero_momentum_is_the_vanilla_step():
+    """m = 0: u = G and v += G either way, so the two steps agree bit for bit."""
+    rng = np.random.default_rng(12)
+    off = np.array([0, 300, 1000, 1001], np.int64)
+    G = rng.standard_normal((2, 1001)).astype(np.float32)
+    runs = []
+    for nest in (False, True):
+        u = np.zeros((2, 1001), np.float32)
+        v = np.full((2, 1001), 0.25, np.float32)
+        out = oracle.dgc_step(off, G, u, v, 0.05, 0.0, nesterov=nest)
+        runs.append((out, u, v))
+    for a, b in zip(runs[0][0], runs[1][0]):
+        np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(runs[0][1], runs[1][1])
+    np.testing.assert_array_equal(runs[0][2], runs[1][2])

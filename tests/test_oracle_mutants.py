@@ -30,6 +30,9 @@ MUTANTS = {
     "clip_ignores_nodes": ("/ sqrt((double)clip_nodes)", "/ 1.0"),
     "clip_scale_inverted": ("if (norm > thr_k) { c = (float)(thr_k / norm)", "if (norm > thr_k) { c = (float)(norm / thr_k)"),
     "k_floor": ("double kd = ceil(density * (double)n);", "double kd = floor(density * (double)n);"),
+    # DGC with Nesterov momentum (the reading)
+    "nesterov_step_without_momentum": ("float step = momentum * uk[i];", "float step = uk[i];"),
+    "nesterov_ignored": ("            if (nesterov) {", "            if (0) {"),
     # DGC with the sampled threshold
     "sampled_strict_gt": ("c += order[i].key >= tau;", "c += order[i].key > tau;"),
     "sampled_rank_floor": ("int64_t a = (ks * m + n / 2) / n;", "int64_t a = (ks * m) / n;"),
