@@ -539,6 +539,31 @@ def run_gpu(args):
                    "sent_vs_exact_k": float(cnt.sum()) / float(K * k_s.sum()),
                    "tensors_short_of_k": float((cnt < k_s[None, :]).mean())}
 
+    # DGC with Nesterov momentum (dgc_compress_nesterov) on the same inputs
+    nesterov = None
+    if w.method == "dgc":
+        d_n = gc.DGC(w.offsets, K, w.density, w.momentum, w.clip_thr, w.clip_nodes, device=dev, nesterov=True)
+        u_n, v_n = torch.zeros((K, N), device=dev), torch.zeros((K, N), device=dev)
+        avg_n = torch.empty(N, device=dev)
+
+        def nesterov_step(i):
+            out_n, tot_n = d_n(grads[i % N_SETS], u_n, v_n)
+            gc.sparse_average(out_n, tot_n, N, avg_n)
+
+        for i in range(args.warmup):
+            nesterov_step(i)
+        torch.cuda.synchronize()
+        n0 = torch.cuda.Event(enable_timing=True)
+        n1 = torch.cuda.Event(enable_timing=True)
+        n0.record(stream)
+        for i in range(args.steps):
+            nesterov_step(i)
+        n1.record(stream)
+        torch.cuda.synchronize()
+        ms_n = max_over_ranks(n0.elapsed_time(n1) / args.steps, dev)
+        nesterov = {"step": "dgc_compress_nesterov + sparse_average", "value": job_gbs(world, 4.0 * K * N, ms_n),
+                    "unit": "GB/s", "ms_per_step": ms_n}
+
     # the ECD-PSGD iteration on the same ring (extrapolated estimates,
     # equations (3)-(4)): 24 algorithmic bytes per node-element (read x_t,
     # x_{t-1}, the estimate and g; write x_{t+1} and the estimate)
@@ -672,6 +697,7 @@ def run_gpu(args):
         "wire": wire,
         "fused_update": fused,
         "sampled_threshold": sampled,
+        "nesterov_variant": nesterov,
         "ecd_variant": ecd,
         "gpu_launches": launches,
         "clocks": clk,

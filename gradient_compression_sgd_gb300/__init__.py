@@ -80,6 +80,7 @@ def lib():
         L.gcsgd_dgc_k.argtypes = [f64, i64]
         L.gcsgd_dgc_workspace_size.argtypes = [vp, i32, i32, f64, vp]
         L.dgc_compress.argtypes = [vp, i32, i32, vp, vp, vp, f64, f32, f32, i32, vp, i64, vp, vp, vp, sz, vp]
+        L.dgc_compress_nesterov.argtypes = L.dgc_compress.argtypes
         L.dgc_compress_noalloc.argtypes = [vp, i32, i32, vp, vp, vp, f64, f32, f32, i32, vp, i64, vp, vp, vp]
         L.gcsgd_dgc_sampled_workspace_size.argtypes = [vp, i32, i32, f64, f64, vp]
         L.dgc_compress_sampled.argtypes = [vp, i32, i32, vp, vp, vp, f64, f64, f32, f32, i32, vp, i64, vp, vp, vp,
@@ -229,13 +230,15 @@ def dgc_workspace_size(offsets, K: int, density: float) -> int:
 
 
 def dgc_compress(offsets, grad, u, v, out, counts, workspace, density, momentum, clip_thr=0.0, clip_nodes=1,
-                 totals=None, stream=None):
-    """One DGC step of K learners (see dgc_compress in include/gcsgd.h)."""
+                 totals=None, stream=None, nesterov=False):
+    """One DGC step of K learners (see dgc_compress and, with nesterov,
+    dgc_compress_nesterov in include/gcsgd.h)."""
     import torch
     off = _offsets(offsets)
     K = grad.shape[0]
     cap = out.shape[1]
-    _check("dgc_compress", lib().dgc_compress(
+    fn = "dgc_compress_nesterov" if nesterov else "dgc_compress"
+    _check(fn, getattr(lib(), fn)(
         _ptr(off), len(off) - 1, int(K), _dev(grad, "grad", torch.float32), _dev(u, "u", torch.float32),
         _dev(v, "v", torch.float32), float(density), float(momentum), float(clip_thr), int(clip_nodes),
         _dev(out, "out", torch.int32), int(cap), _dev(counts, "counts", torch.int64),
@@ -291,13 +294,16 @@ class DGC:
     """Buffers of DGC on one layout: workspace, [K, cap] messages and counters."""
 
     def __init__(self, offsets, K: int, density: float, momentum: float, clip_thr: float = 0.0,
-                 clip_nodes: int = 1, device="cuda", sample_frac: float = 0.0):
+                 clip_nodes: int = 1, device="cuda", sample_frac: float = 0.0, nesterov: bool = False):
         import torch
         self.offsets = _offsets(offsets)
         self.S = len(self.offsets) - 1
         self.K, self.density, self.momentum = int(K), float(density), float(momentum)
         self.clip_thr, self.clip_nodes = float(clip_thr), int(clip_nodes)
         self.sample_frac = float(sample_frac)  # > 0: the sampled threshold (dgc_compress_sampled)
+        self.nesterov = bool(nesterov)  # Nesterov momentum (dgc_compress_nesterov)
+        if self.nesterov and self.sample_frac > 0:
+            raise ValueError("Nesterov momentum is available with the exact top-k only")
         self.cap = sum(dgc_k(density, int(self.offsets[s + 1] - self.offsets[s])) for s in range(self.S))
         ws = (dgc_sampled_workspace_size(self.offsets, K, density, self.sample_frac) if self.sample_frac > 0
               else dgc_workspace_size(self.offsets, K, density))
@@ -321,7 +327,8 @@ class DGC:
                                  stream=stream)
         else:
             dgc_compress(self.offsets, grad, u, v, self.out, self.counts, self.workspace, self.density,
-                         self.momentum, self.clip_thr, self.clip_nodes, totals=self.totals, stream=stream)
+                         self.momentum, self.clip_thr, self.clip_nodes, totals=self.totals, stream=stream,
+                         nesterov=self.nesterov)
         return self.out, self.totals
 
 

@@ -224,9 +224,9 @@ int gcsgd_dgc_sampled_workspace_size(const int64_t* seg_offsets, int32_t n_seg, 
 }
 
 static int dgc_common(const char* fn, const int64_t* seg_offsets, int32_t n_seg, int32_t K, const float* grad,
-                      float* u, float* v, double density, double sample_frac, float momentum, float clip_thr,
-                      int32_t clip_nodes, gcsgd_pair* out, int64_t cap, int64_t* counts, int64_t* totals,
-                      void* workspace, size_t workspace_bytes, void* stream) {
+                      float* u, float* v, double density, double sample_frac, float momentum, bool nesterov,
+                      float clip_thr, int32_t clip_nodes, gcsgd_pair* out, int64_t cap, int64_t* counts,
+                      int64_t* totals, void* workspace, size_t workspace_bytes, void* stream) {
     int rc;
     if ((rc = check_layout(fn, seg_offsets, n_seg))) return rc;
     if (K < 1) return set_error(GCSGD_ERR_INVALID_ARG, "%s: K = %d < 1", fn, K);
@@ -242,15 +242,23 @@ static int dgc_common(const char* fn, const int64_t* seg_offsets, int32_t n_seg,
     if (cap > 0 && !out) return set_error(GCSGD_ERR_INVALID_ARG, "%s: out is NULL", fn);
     if ((rc = check_ws(fn, workspace, workspace_bytes, dgc_ws_bytes(seg_offsets, n_seg, K, density, sample_frac))))
         return rc;
-    return dgc_launch(seg_offsets, n_seg, K, grad, u, v, density, sample_frac, momentum, clip_thr, clip_nodes, out,
-                      cap, counts, totals, workspace, workspace_bytes, (cudaStream_t)stream);
+    return dgc_launch(seg_offsets, n_seg, K, grad, u, v, density, sample_frac, momentum, nesterov, clip_thr,
+                      clip_nodes, out, cap, counts, totals, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
 int dgc_compress(const int64_t* seg_offsets, int32_t n_seg, int32_t K, const float* grad, float* u, float* v,
                  double density, float momentum, float clip_thr, int32_t clip_nodes, gcsgd_pair* out, int64_t cap,
                  int64_t* counts, int64_t* totals, void* workspace, size_t workspace_bytes, void* stream) {
-    return dgc_common("dgc_compress", seg_offsets, n_seg, K, grad, u, v, density, 0.0, momentum, clip_thr, clip_nodes,
-                      out, cap, counts, totals, workspace, workspace_bytes, stream);
+    return dgc_common("dgc_compress", seg_offsets, n_seg, K, grad, u, v, density, 0.0, momentum, false, clip_thr,
+                      clip_nodes, out, cap, counts, totals, workspace, workspace_bytes, stream);
+}
+
+int dgc_compress_nesterov(const int64_t* seg_offsets, int32_t n_seg, int32_t K, const float* grad, float* u,
+                          float* v, double density, float momentum, float clip_thr, int32_t clip_nodes,
+                          gcsgd_pair* out, int64_t cap, int64_t* counts, int64_t* totals, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+    return dgc_common("dgc_compress_nesterov", seg_offsets, n_seg, K, grad, u, v, density, 0.0, momentum, true,
+                      clip_thr, clip_nodes, out, cap, counts, totals, workspace, workspace_bytes, stream);
 }
 
 int dgc_compress_sampled(const int64_t* seg_offsets, int32_t n_seg, int32_t K, const float* grad, float* u, float* v,
@@ -260,7 +268,7 @@ int dgc_compress_sampled(const int64_t* seg_offsets, int32_t n_seg, int32_t K, c
     if (!(sample_frac > 0.0 && sample_frac <= 1.0))
         return set_error(GCSGD_ERR_INVALID_ARG, "dgc_compress_sampled: sample_frac %g outside (0, 1]", sample_frac);
     return dgc_common("dgc_compress_sampled", seg_offsets, n_seg, K, grad, u, v, density, sample_frac, momentum,
-                      clip_thr, clip_nodes, out, cap, counts, totals, workspace, workspace_bytes, stream);
+                      false, clip_thr, clip_nodes, out, cap, counts, totals, workspace, workspace_bytes, stream);
 }
 
 int gcsgd_dgc_stats(const int64_t* seg_offsets, int32_t n_seg, int32_t K, double density, const void* workspace,

@@ -204,10 +204,14 @@ __device__ float clip_scale(const double* __restrict__ part, int k, float clip_t
     return norm > thr_k ? (float)(thr_k / norm) : 1.0f;
 }
 
-// The update of one element: u' = m*u + c*g, v' = v + u'.
+// The update of one element: u' = m*u + c*g, v' = v + u' (vanilla momentum,
+// Appendix D), or with NEST (Nesterov momentum, Appendix B, as read: the
+// accumulated state takes the look-ahead step) v' = v + (m*u' + c*g).
+template <bool NEST>
 __device__ __forceinline__ void dgc_elem(float g, float& u, float& v, float m, float c) {
-    u = __fadd_rn(__fmul_rn(m, u), __fmul_rn(g, c));
-    v = __fadd_rn(v, u);
+    const float gc = __fmul_rn(g, c);
+    u = __fadd_rn(__fmul_rn(m, u), gc);
+    v = __fadd_rn(v, NEST ? __fadd_rn(__fmul_rn(m, u), gc) : u);
 }
 
 // The last CTA writes the per-segment plan, the clip scales and the order in
@@ -224,7 +228,7 @@ __device__ __forceinline__ void dgc_elem(float g, float& u, float& v, float m, f
 // |v| -- including the pile-up of entries just below the send threshold that
 // accumulation builds.  The hint only steers speed: dgc_select checks that
 // the pool holds the top k.
-template <int MAXS>
+template <int MAXS, bool NEST>
 __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, PoolList<MAXS> pl, int S, int K,
                                                      double density, double sample_frac,
                                                      float clip_thr, int clip_nodes, const double* __restrict__ part,
@@ -329,7 +333,7 @@ __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, PoolL
                 if (b < nblk) {
 #pragma unroll
                     for (int h = 0; h < kH; ++h) {
-                        dgc_elem(gg[j][h], uu[j][h], vv[j][h], momentum, c);
+                        dgc_elem<NEST>(gg[j][h], uu[j][h], vv[j][h], momentum, c);
                         const uint32_t key = mag_key(vv[j][h]);
                         keys[b * kSampleBlock + 32 * h + lane] = key;
                         radix_hist_add(rs, key);
@@ -369,6 +373,7 @@ __device__ __forceinline__ int find_segment_by_tile(const SegPlan* plan, int S, 
 // all issued before use), fused momentum-corrected update, 128-bit stores of
 // u', v', then an ordered block compaction of the candidates |v'| >= hint
 // into the segment's pool; the tile's (pool offset, count) goes to tile_tab.
+template <bool NEST>
 __global__ void __launch_bounds__(NT, 3) dgc_update(const SegPlan* __restrict__ plan, int S, uint64_t N,
                                                     uint32_t tiles_per_learner, uint64_t total_tiles,
                                                     const float* __restrict__ grad, float* __restrict__ u,
@@ -424,7 +429,7 @@ __global__ void __launch_bounds__(NT, 3) dgc_update(const SegPlan* __restrict__ 
             float* v4 = &V[r].x;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                dgc_elem(g4[j], u4[j], v4[j], momentum, c);
+                dgc_elem<NEST>(g4[j], u4[j], v4[j], momentum, c);
                 const bool cand = (e + j < len) && mag_key(v4[j]) >= h;
                 flags |= (uint32_t)cand << (4 * r + j);
             }
@@ -943,10 +948,13 @@ static int dgc_set_smem_limits() {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return set_error(GCSGD_ERR_CUDA, "dgc_compress: no current device");
     if (done[dev]) return GCSGD_OK;
-    if (cudaFuncSetAttribute(dgc_prepare<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(kSampleMax * sizeof(uint32_t))) != cudaSuccess ||
-        cudaFuncSetAttribute(dgc_prepare<GCSGD_MAX_SEGMENTS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(kSampleMax * sizeof(uint32_t))) != cudaSuccess ||
+    const int ks = (int)(kSampleMax * sizeof(uint32_t));
+    if (cudaFuncSetAttribute(dgc_prepare<256, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, ks) != cudaSuccess ||
+        cudaFuncSetAttribute(dgc_prepare<GCSGD_MAX_SEGMENTS, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, ks) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(dgc_prepare<256, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, ks) != cudaSuccess ||
+        cudaFuncSetAttribute(dgc_prepare<GCSGD_MAX_SEGMENTS, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, ks) !=
+            cudaSuccess ||
         cudaFuncSetAttribute(dgc_select, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStageBytes) !=
             cudaSuccess)
         return set_error(GCSGD_ERR_CUDA, "dgc_compress: cannot raise the shared-memory limit");
@@ -955,8 +963,8 @@ static int dgc_set_smem_limits() {
 }
 
 int dgc_launch(const int64_t* off, int S, int K, const float* grad, float* u, float* v, double density,
-               double sample_frac, float momentum, float clip_thr, int clip_nodes, gcsgd_pair* out, int64_t cap,
-               int64_t* counts, int64_t* totals, void* ws, size_t ws_bytes, cudaStream_t stream) {
+               double sample_frac, float momentum, bool nesterov, float clip_thr, int clip_nodes, gcsgd_pair* out,
+               int64_t cap, int64_t* counts, int64_t* totals, void* ws, size_t ws_bytes, cudaStream_t stream) {
     using namespace dgc;
     HostPlan hp;
     host_plan(off, S, density, sample_frac, &hp);
@@ -1001,17 +1009,17 @@ int dgc_launch(const int64_t* off, int S, int K, const float* grad, float* u, fl
             SegOffsets<256> so;
             PoolList<256> pl;
             fill(so, pl);
-            dgc_prepare<256><<<prep_grid, NTP, smem, stream>>>(so, pl, S, K, density, sample_frac, clip_thr, clip_nodes,
-                                                               w.clip_part, w.plan, w.clip_c, w.order, N, grad, u, v,
-                                                               momentum, w.hint, w.pool_cnt);
+            (nesterov ? dgc_prepare<256, true> : dgc_prepare<256, false>)<<<prep_grid, NTP, smem, stream>>>(
+                so, pl, S, K, density, sample_frac, clip_thr, clip_nodes, w.clip_part, w.plan, w.clip_c, w.order, N,
+                grad, u, v, momentum, w.hint, w.pool_cnt);
         } else {
             SegOffsets<GCSGD_MAX_SEGMENTS> so;
             PoolList<GCSGD_MAX_SEGMENTS> pl;
             fill(so, pl);
-            dgc_prepare<GCSGD_MAX_SEGMENTS><<<prep_grid, NTP, smem, stream>>>(
-                so, pl, S, K, density, sample_frac, clip_thr, clip_nodes, w.clip_part, w.plan, w.clip_c, w.order, N,
-                grad, u, v,
-                momentum, w.hint, w.pool_cnt);
+            (nesterov ? dgc_prepare<GCSGD_MAX_SEGMENTS, true> : dgc_prepare<GCSGD_MAX_SEGMENTS, false>)
+                <<<prep_grid, NTP, smem, stream>>>(so, pl, S, K, density, sample_frac, clip_thr, clip_nodes,
+                                                   w.clip_part, w.plan, w.clip_c, w.order, N, grad, u, v, momentum,
+                                                   w.hint, w.pool_cnt);
         }
         if ((rc = check_launch("dgc_prepare"))) return rc;
     }
@@ -1023,9 +1031,9 @@ int dgc_launch(const int64_t* off, int S, int K, const float* grad, float* u, fl
         LaunchScope ls("dgc_update", stream);
         uint64_t grid = (uint64_t)sm_count() * 3;
         if (grid > total_tiles) grid = total_tiles;
-        dgc_update<<<(unsigned)grid, NT, 0, stream>>>(w.plan, S, N, (uint32_t)hp.tiles_per_learner, total_tiles,
-                                                      grad, u, v, momentum, w.clip_c, w.hint, w.pool_cnt,
-                                                      w.tile_tab, w.pool, hp.pool_per_learner);
+        (nesterov ? dgc_update<true> : dgc_update<false>)<<<(unsigned)grid, NT, 0, stream>>>(
+            w.plan, S, N, (uint32_t)hp.tiles_per_learner, total_tiles, grad, u, v, momentum, w.clip_c, w.hint,
+            w.pool_cnt, w.tile_tab, w.pool, hp.pool_per_learner);
         if ((rc = check_launch("dgc_update"))) return rc;
     }
     {

@@ -72,7 +72,7 @@ int dgc_collect_stats(const int64_t* off, int S, int K, double density, const vo
                       gcsgd_dgc_stats_t* st);
 
 int dgc_launch(const int64_t* off, int S, int K, const float* grad, float* u, float* v, double density,
-               double sample_frac, float momentum, float clip_thr, int clip_nodes, gcsgd_pair* out, int64_t cap,
-               int64_t* counts, int64_t* totals, void* ws, size_t ws_bytes, cudaStream_t stream);
+               double sample_frac, float momentum, bool nesterov, float clip_thr, int clip_nodes, gcsgd_pair* out,
+               int64_t cap, int64_t* counts, int64_t* totals, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 }  // namespace gcsgd

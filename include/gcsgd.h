@@ -103,6 +103,23 @@ int dgc_compress(const int64_t* seg_offsets, int32_t n_seg, int32_t K,
                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The same step with Nesterov momentum ("Deep Gradient Compression",
+ * Appendix B, gradient sparsification with Nesterov momentum correction).
+ * The page gives the shape of the corrected update (local momentum plus an
+ * accumulated state) but not its equations; read as
+ *   u <- m*u + c*G,  then  v <- v + (m*u + c*G)   (fp32, one rounding per
+ *   operation, no FMA; the u just updated),
+ * i.e. the accumulated state takes the look-ahead step of conventional
+ * Nesterov momentum.  Everything else, arguments, workspace and errors, as
+ * dgc_compress.  With momentum 0 it equals dgc_compress.
+ */
+int dgc_compress_nesterov(const int64_t* seg_offsets, int32_t n_seg, int32_t K,
+                          const float* grad, float* u, float* v,
+                          double density, float momentum, float clip_thr, int32_t clip_nodes,
+                          gcsgd_pair* out, int64_t cap, int64_t* counts, int64_t* totals,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * The DGC step with the sampled threshold ("Deep Gradient Compression",
  * section 5: a 0.1 % to 1 % sample of the gradients estimates the population
  * threshold; section 6: hierarchical threshold selection).  Steps 1, 2 and 4

@@ -28,7 +28,8 @@ def shifted(a, offset):
     return view
 
 
-def run_dgc(gc, offsets, grads, density, momentum, clip_thr=0.0, clip_nodes=1, u0=None, v0=None, offset=0):
+def run_dgc(gc, offsets, grads, density, momentum, clip_thr=0.0, clip_nodes=1, u0=None, v0=None, offset=0,
+            nesterov=False):
     """Step both sides through the gradient list and compare after every step."""
     import torch
     offsets = np.asarray(offsets, np.int64)
@@ -37,10 +38,10 @@ def run_dgc(gc, offsets, grads, density, momentum, clip_thr=0.0, clip_nodes=1, u
     v_o = np.zeros((K, N), np.float32) if v0 is None else v0.copy()
     u_g = shifted(u_o, offset)
     v_g = shifted(v_o, offset)
-    d = gc.DGC(offsets, K, density, momentum, clip_thr, clip_nodes)
+    d = gc.DGC(offsets, K, density, momentum, clip_thr, clip_nodes, nesterov=nesterov)
     for t, G in enumerate(grads):
         idx_o, val_o, counts_o, _ = oracle.dgc_step(offsets, G, u_o, v_o, density, momentum, clip_thr, clip_nodes,
-                                                    cap=d.cap)
+                                                    cap=d.cap, nesterov=nesterov)
         out, totals = d(shifted(G, offset), u_g, v_g)
         torch.cuda.synchronize()
         counts_g = d.counts.cpu().numpy()
@@ -279,3 +280,43 @@ def test_sampled_hand_examples_on_the_gpu(cuda_lib):
         G[0, 128 * b] = 100.0 + b
     G[0, 64], G[0, 65] = 150.0, 100.5
     run_dgc_sampled(cuda_lib, [0, n], [G], 0.001, 0.5, 0.9)
+
+
+# ------------------------------------------------ Nesterov momentum (reading)
+
+@pytest.mark.parametrize("config", [2, 4])
+def test_nesterov_small_configs(cuda_lib, config):
+    """dgc_compress_nesterov on the small ResNet-50 and GRU layouts, every step
+    against the oracle's Nesterov step."""
+    w = wl.workload(config, small=True)
+    grads = [wl.gradients(w, t).numpy() for t in range(w.steps)]
+    d = run_dgc(cuda_lib, w.offsets, grads, w.density, w.momentum, nesterov=True)
+    assert d.stats()["hint_failed"] == 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "empty_segments", "misaligned", "two_pool_segments_ragged"])
+def test_nesterov_edge_layouts_with_clipping(cuda_lib, name):
+    sizes = EDGE_LAYOUTS[name]
+    off = wl.layout_offsets(sizes)
+    rng = np.random.default_rng(zlib.crc32(name.encode()))
+    grads = [rng.standard_normal((3, off[-1])).astype(np.float32) * 1e-2 for _ in range(3)]
+    run_dgc(cuda_lib, off, grads, 0.01, 0.9, clip_thr=0.5, clip_nodes=2, nesterov=True)
+
+
+def test_nesterov_with_zero_momentum_matches_dgc_compress(cuda_lib):
+    """m = 0: the Nesterov entry point and dgc_compress give identical bits."""
+    import torch
+    gc = cuda_lib
+    off = wl.layout_offsets([50001, 300, 70001])
+    rng = np.random.default_rng(3)
+    G = torch.from_numpy(rng.standard_normal((2, off[-1])).astype(np.float32)).cuda()
+    res = []
+    for nest in (False, True):
+        u = torch.zeros((2, off[-1]), device="cuda")
+        v = torch.full((2, off[-1]), 0.25, device="cuda")
+        d = gc.DGC(off, 2, 0.01, 0.0, nesterov=nest)
+        out, totals = d(G, u, v)
+        torch.cuda.synchronize()
+        res.append((out.cpu().clone(), totals.cpu().clone(), u.cpu(), v.cpu()))
+    for a, b in zip(res[0], res[1]):
+        assert torch.equal(a, b)
