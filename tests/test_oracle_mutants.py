@@ -21,8 +21,8 @@ PIN_FILES = ["test_oracle_dgc.py", "test_oracle_adacomp.py", "test_oracle_averag
 # name -> (text in the oracle, planted replacement)
 MUTANTS = {
     # DGC (momentum correction, selection, masking, clipping, k)
-    "v_before_u": ("uk[i] = mu + g;\n            vk[i] = vk[i] + uk[i];",
-                   "vk[i] = vk[i] + uk[i];\n            uk[i] = mu + g;"),
+    "v_before_u": ("            } else {\n                vk[i] = vk[i] + uk[i];\n            }",
+                   "            } else {\n                vk[i] = vk[i] + (uk[i] - g) / momentum;\n            }"),
     "no_momentum": ("float mu = momentum * uk[i];", "float mu = 0.0f * uk[i];"),
     "ties_to_higher_index": ("return x->idx < y->idx ? -1 : 1;", "return x->idx > y->idx ? -1 : 1;"),
     "u_not_masked": ("uk[off + i] = 0.0f;\n            }", "}"),
