@@ -327,7 +327,10 @@ __device__ __forceinline__ void select_tile(const float4 (&Gv)[4], const float4 
 // barrier and no shared counter.  Each warp streams its chunks through a
 // ring of kRing shared-memory stages filled by cp.async (R and dW, 4 KB a
 // chunk; the copies of the next kRing - 1 chunks are in flight while one is
-// computed, and they hold no registers).  A lane copies and later reads the
+// computed, and they hold no registers).  Two stages at six CTAs of four
+// warps per SM (24 warps) measured faster than three stages at four CTAs:
+// the pass is bound by its instruction latencies more than by the bytes in
+// flight.  A lane copies and later reads the
 // same 16-byte pieces, so only its own cp.async groups are waited on.  Past a
 // chunk's end the copies zero-fill: G = 0 never raises a maximum and is never
 // sent, so the arithmetic needs no bounds test.  Per chunk the warp finds its
@@ -336,7 +339,7 @@ __device__ __forceinline__ void select_tile(const float4 (&Gv)[4], const float4 
 // selects, stores R <- G and writes its candidates in index order into the
 // pool slots of its own index range.
 constexpr int NTW = 128;   // threads of an ada_bins_warp CTA
-constexpr int kRing = 3;   // stages per warp
+constexpr int kRing = 2;   // stages per warp
 struct ChunkMeta {         // what the computing side needs of an issued chunk
     uint32_t rel, clen, k, lt, tj, L, bpw, big_off;
     float invL;
@@ -359,7 +362,7 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
-__global__ void __launch_bounds__(NTW, 4) ada_bins_warp(const SegPlan* __restrict__ plan, int S, uint64_t N,
+__global__ void __launch_bounds__(NTW, 6) ada_bins_warp(const SegPlan* __restrict__ plan, int S, uint64_t N,
                                                         uint32_t tiles_per_learner, uint64_t total_tiles,
                                                         const float* __restrict__ dW, float* __restrict__ R,
                                                         uint32_t* __restrict__ bins, uint64_t bins_per_learner,
@@ -1007,7 +1010,7 @@ int adacomp_launch(const int64_t* off, int S, const int32_t* lt, int K, const fl
                 return set_error(GCSGD_ERR_CUDA, "adacomp_compress: cannot raise the shared-memory limit");
             attr_set[dev] = true;
         }
-        const uint64_t wgrid = (uint64_t)sm_count() * 4, need_ctas = (T + NTW / 32 - 1) / (NTW / 32);
+        const uint64_t wgrid = (uint64_t)sm_count() * 6, need_ctas = (T + NTW / 32 - 1) / (NTW / 32);
         ada_bins_warp<<<(unsigned)(need_ctas < wgrid ? need_ctas : wgrid), NTW, kBinsWarpSmem, stream>>>(
             w.plan, S, N, (uint32_t)hp.tiles_per_learner, T, dW, R, w.big, hp.big_per_learner, w.tile_tab, w.pool);
         if ((rc = check_launch("ada_bins_warp"))) return rc;
