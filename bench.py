@@ -64,6 +64,30 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+class nvtx_range:
+    """An NVTX range around a phase of the run (seen by Nsight tools); a no-op
+    where torch's NVTX binding is unavailable."""
+
+    def __init__(self, name: str):
+        self.name = name
+        self.pushed = False
+
+    def __enter__(self):
+        try:
+            import torch
+            torch.cuda.nvtx.range_push(self.name)
+            self.pushed = True
+        except Exception:
+            pass
+        return self
+
+    def __exit__(self, *exc):
+        if self.pushed:
+            import torch
+            torch.cuda.nvtx.range_pop()
+        return False
+
+
 def max_over_ranks(x: float, device) -> float:
     """The largest `x` over all ranks of the default process group (x itself
     when there is none): the job's time is its slowest rank's."""
@@ -427,10 +451,11 @@ def run_gpu(args):
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(args.steps):
-        path.step(grads[i % N_SETS], t=args.warmup + i)
-    e1.record(stream)
+    with nvtx_range("timed steps"):
+        e0.record(stream)
+        for i in range(args.steps):
+            path.step(grads[i % N_SETS], t=args.warmup + i)
+        e1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -442,9 +467,10 @@ def run_gpu(args):
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
     # every kernel's time, from a separate traced pass of the same steps (after the timed region)
     gc.trace_enable(True)
-    for i in range(args.steps):
-        path.step(grads[i % N_SETS], t=args.warmup + args.steps + i)
-    torch.cuda.synchronize()
+    with nvtx_range("traced steps"):
+        for i in range(args.steps):
+            path.step(grads[i % N_SETS], t=args.warmup + args.steps + i)
+        torch.cuda.synchronize()
     gc.trace_enable(False)
     trace_all = gc.trace_read()
     grad_bytes = 4.0 * K * N
@@ -641,13 +667,14 @@ def run_gpu(args):
         f0 = torch.cuda.Event(enable_timing=True)
         f1 = torch.cuda.Event(enable_timing=True)
         e2e_steps = max(3, min(args.steps, 20))
-        f0.record(stream)
-        copy_s.wait_event(f0)
-        for i in range(e2e_steps):
-            e2e_step(i)
-        stream.wait_stream(copy_s)
-        stream.wait_stream(d2h_s)
-        f1.record(stream)
+        with nvtx_range("end-to-end steps"):
+            f0.record(stream)
+            copy_s.wait_event(f0)
+            for i in range(e2e_steps):
+                e2e_step(i)
+            stream.wait_stream(copy_s)
+            stream.wait_stream(d2h_s)
+            f1.record(stream)
         torch.cuda.synchronize()
         ms_e2e = max_over_ranks(f0.elapsed_time(f1) / e2e_steps, dev)
         e2e = job_gbs(world, grad_bytes, ms_e2e)
