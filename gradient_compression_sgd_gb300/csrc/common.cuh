@@ -161,16 +161,23 @@ __device__ void radix_pick(RadixSmem& rs, int nb, uint32_t need, uint32_t* bucke
 
 // The rank-th largest of `count` 31-bit keys (1 <= rank <= count), by radix
 // digits [30:20], [19:9] and [8:0] with shared-memory histograms.  After the
-// first digit the keys of the chosen bucket are copied to rs.cand when they
+// first digit the keys of the chosen bucket are copied to cbuf when they
 // fit, so the later digits look at those few keys only.  `load(i, &key)`
 // returns false for items to skip.  With hist_ready the caller has already
 // added every key's first digit into rs.hist (radix_hist_clear, then
 // radix_hist_add per key, then a barrier).  PASSES = 3 is exact; PASSES = 2
 // returns the rank-th largest key with its low 9 bits cleared (greater and
 // ties then refer to the truncated keys).  GLOBAL: `load` reads global
-// memory (see radix_count).  Every thread must call it.
+// memory (see radix_count).  cbuf/ccap: where the chosen bucket's keys are
+// compacted (shared memory; default rs.cand, kCandMax keys).  Every thread
+// must call it.
 template <int NT, int PASSES, bool GLOBAL = false, class Load>
-__device__ SelectResult radix_select_desc(Load load, uint64_t count, uint32_t rank, RadixSmem& rs, bool hist_ready) {
+__device__ SelectResult radix_select_desc(Load load, uint64_t count, uint32_t rank, RadixSmem& rs, bool hist_ready,
+                                          uint32_t* cbuf = nullptr, uint32_t ccap = 0) {
+    if (!cbuf) {
+        cbuf = rs.cand;
+        ccap = kCandMax;
+    }
     static_assert(PASSES == 2 || PASSES == 3, "two or three digits");
     constexpr int LPT = GLOBAL ? 8 : 4;
     const int lane = threadIdx.x & 31;
@@ -178,7 +185,7 @@ __device__ SelectResult radix_select_desc(Load load, uint64_t count, uint32_t ra
     uint32_t b, ab, c1;
     radix_pick<NT>(rs, 2048, rank, &b, &ab, &c1);
     uint32_t prefix = b << 20, pmask = 0x7ffu << 20, need = rank - ab, greater = ab;
-    const bool compact = c1 <= (uint32_t)kCandMax;
+    const bool compact = c1 <= ccap;
     if (compact) {
         if (threadIdx.x == 0) rs.sel[3] = 0;
         __syncthreads();
@@ -199,13 +206,13 @@ __device__ SelectResult radix_select_desc(Load load, uint64_t count, uint32_t ra
                     uint32_t at = 0;
                     if (lane == 0) at = atomicAdd(&rs.sel[3], (uint32_t)__popc(m));
                     at = __shfl_sync(kFull, at, 0);
-                    if (hit) rs.cand[at + __popc(m & ((1u << lane) - 1u))] = key[j];
+                    if (hit) cbuf[at + __popc(m & ((1u << lane) - 1u))] = key[j];
                 }
             }
         }
         __syncthreads();
     }
-    auto cand = [&](uint64_t i, uint32_t* key) { *key = rs.cand[i]; return true; };
+    auto cand = [&](uint64_t i, uint32_t* key) { *key = cbuf[i]; return true; };
 #pragma unroll 1
     for (int pass = 1; pass < PASSES; ++pass) {
         const int shift = pass == 1 ? 9 : 0;

@@ -813,7 +813,8 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
     if (!pool_ok) {
         // the hint failed: select among all of the segment's v' in global memory
         const SelectResult r = radix_select_desc<NTS, 3, true>(
-            [&](uint64_t i, uint32_t* key) { *key = mag_key(vseg[i]); return true; }, p.n, p.k, rs, false);
+            [&](uint64_t i, uint32_t* key) { *key = mag_key(vseg[i]); return true; }, p.n, p.k, rs, false,
+            reinterpret_cast<uint32_t*>(stage_raw), (uint32_t)(kStageBytes / sizeof(uint32_t)));
         emit_in_order(
             [&](uint32_t i, uint32_t* loc, uint32_t* bits) {
                 *loc = i;
@@ -825,19 +826,32 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
     // a valid pool too large to stage: select from global memory, emit through the tile table
     uint32_t T = 0, ties = pc;  // take_all: every candidate goes
     if (!take_all) {
+        // the stage is free on this path: it takes the threshold bucket's keys
         const SelectResult r = radix_select_desc<NTS, 3, true>(
             [&](uint64_t i, uint32_t* key) { *key = __ldg(&items[i].y) & 0x7fffffffu; return true; }, pc, p.k, rs,
-            false);
+            false, reinterpret_cast<uint32_t*>(stage_raw), (uint32_t)(kStageBytes / sizeof(uint32_t)));
         T = r.thresh;
         ties = r.ties;
     }
     uint32_t run_gt = 0, run_eq = 0;
-    for (uint32_t tb = 0; tb < p.ntiles; tb += NTS) {
-        const uint32_t j = tb + threadIdx.x;
-        const uint2 ent = j < p.ntiles ? tt[j] : make_uint2(0u, 0u);
+    for (uint32_t tb = 0; tb < p.ntiles; tb += kChunkTiles) {  // kChunkTiles tiles a round, TPT per thread
+        constexpr int TPT = kChunkTiles / NTS;
+        uint2 ent[TPT];
+        uint32_t c = 0;
+#pragma unroll
+        for (int jj = 0; jj < TPT; ++jj) {
+            const uint32_t j = tb + TPT * threadIdx.x + jj;
+            ent[jj] = j < p.ntiles ? tt[j] : make_uint2(0u, 0u);
+            c += ent[jj].y;
+        }
         uint64_t tot;
-        toff[threadIdx.x] = (uint32_t)block_exclusive_scan<NTS>(ent.y, rs.scan, &tot);
-        tbase[threadIdx.x] = ent.x;
+        uint32_t ex = (uint32_t)block_exclusive_scan<NTS>(c, rs.scan, &tot);
+#pragma unroll
+        for (int jj = 0; jj < TPT; ++jj) {
+            toff[TPT * threadIdx.x + jj] = ex;
+            tbase[TPT * threadIdx.x + jj] = ent[jj].x;
+            ex += ent[jj].y;
+        }
         __syncthreads();
         const uint32_t chunk_items = (uint32_t)tot;
         constexpr int IPT = 8;  // consecutive items per thread per round: eight loads in flight
@@ -847,7 +861,7 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
             uint32_t ngt = 0, neq = 0;
             int lo = 0;  // last tile with toff <= q0, then walked forward item by item
             if (q0 < chunk_items) {
-                int hi = NTS;
+                int hi = kChunkTiles;
                 while (hi - lo > 1) {
                     const int mid = (lo + hi) >> 1;
                     if (toff[mid] <= q0) lo = mid; else hi = mid;
@@ -859,7 +873,7 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
                 local[j] = 0xffffffffu;
                 bits[j] = 0u;
                 if (q < chunk_items) {
-                    while (lo + 1 < NTS && toff[lo + 1] <= q) ++lo;
+                    while (lo + 1 < kChunkTiles && toff[lo + 1] <= q) ++lo;
                     const uint2 it = items[tbase[lo] + (q - toff[lo])];
                     local[j] = it.x;
                     bits[j] = it.y;
