@@ -564,19 +564,31 @@ __global__ void __launch_bounds__(NTW, 6) ada_bins_warp(const SegPlan* __restric
             const uint32_t W = (wtot & 0xFFu) + ((wtot >> 8) & 0xFFu) + ((wtot >> 16) & 0xFFu) + (wtot >> 24);
             tile_tab[(uint64_t)m.k * tiles_per_learner + m.lt] = make_uint2(m.rel, W);
         }
-        // each lane walks its set bits; the rank of bit 4r+j is (entries of the
-        // rounds before r) + (this round's entries of the lanes before) + (its
-        // earlier bits in the round); G is recomputed from the stage, which
-        // is rewritten only by the next round's copies
-        const uint32_t rb1 = wtot & 0xFFu, rb2 = rb1 + ((wtot >> 8) & 0xFFu), rb3 = rb2 + ((wtot >> 16) & 0xFFu);
-        uint2* dst = pool + base;
-        for (uint32_t fb = flags; fb; fb &= fb - 1u) {
-            const uint32_t bit = (uint32_t)__ffs(fb) - 1u, r = bit >> 2;
-            const uint32_t e = 4u * (lane + 32u * r) + (bit & 3u);
-            const uint32_t rb = r == 0 ? 0u : (r == 1 ? rb1 : (r == 2 ? rb2 : rb3));
-            const uint32_t rank = rb + ((excl >> (8 * r)) & 0xFFu) + __popc(flags & ((1u << bit) - 1u) & ~((1u << (4 * r)) - 1u));
-            dst[rank] = make_uint2(m.rel + e, __float_as_uint(__fadd_rn(sR[e], sD[e])));
+        // the candidates in rank order (rounds in order, lanes in order, bits in
+        // order) into this chunk's stage, which every lane has read into its
+        // registers; then one coalesced copy to the pool.  The stage is next
+        // written by the copies issued two rounds on, after the __syncwarp below.
+        __syncwarp();  // every lane's reads of the stage are done
+        uint2* cst = reinterpret_cast<uint2*>(const_cast<float*>(sD));  // kWarpChunk pairs (dW and R halves)
+        {
+            uint32_t rbase = 0;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                uint32_t pos = rbase + ((excl >> (8 * r)) & 0xFFu);
+                rbase += (wtot >> (8 * r)) & 0xFFu;
+                const uint32_t e = 4u * (lane + 32 * r);
+                const float* g4 = &Gv[r].x;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if ((flags >> (4 * r + j)) & 1u) cst[pos] = make_uint2(m.rel + e + j, __float_as_uint(g4[j]));
+                    pos += (flags >> (4 * r + j)) & 1u;
+                }
+            }
         }
+        __syncwarp();
+        const uint32_t W = (wtot & 0xFFu) + ((wtot >> 8) & 0xFFu) + ((wtot >> 16) & 0xFFu) + (wtot >> 24);
+        uint2* dst = pool + base;
+        for (uint32_t i = lane; i < W; i += 32) dst[i] = cst[i];
         __syncwarp();  // wb and the stage are rewritten later
     }
     cp_async_wait<0>();
