@@ -519,6 +519,7 @@ def run_gpu(args):
         for i in range(args.warmup):
             path.step_update(grads[i % N_SETS], weights, 0.01, state_u)
         torch.cuda.synchronize()
+        gc.trace_only("spavg_update")  # events around the update kernel only, as in the timed region
         gc.trace_enable(True)
         h0 = torch.cuda.Event(enable_timing=True)
         h1 = torch.cuda.Event(enable_timing=True)
@@ -528,6 +529,7 @@ def run_gpu(args):
         h1.record(stream)
         torch.cuda.synchronize()
         gc.trace_enable(False)
+        gc.trace_only(None)
         tr_u = gc.trace_read()
         ms_u = max_over_ranks(h0.elapsed_time(h1) / args.steps, dev)
         nu, tu = tr_u.get("spavg_update", (0, 0.0))
