@@ -22,9 +22,14 @@
 //                 and when the hint failed, the segment's v' in shared memory,
 //                 finds the k-th largest |v'| exactly by radix select, then
 //                 emits (index, v') in index order with ties to the lower
-//                 index and masks u = v = 0 at the sent indices.
+//                 index and masks u = v = 0 at the sent indices; a pool too
+//                 large to stage is selected and emitted from global memory
+//   [dgc_pack]    sampled threshold only: packs each learner's per-tensor
+//                 regions into one list
 // The answer never depends on the hint: a pool is used only when it provably
 // contains every entry of the top k (at least k candidates, no overflow).
+// Nesterov momentum (Appendix B, as read) is the same sequence with the
+// update of dgc_prepare's samples and of dgc_update templated on it.
 #include <math.h>
 #include <string.h>
 
