@@ -7,7 +7,9 @@ Compression of all four learners' gradients (density 0.001 per tensor,
 momentum 0.9, exact top-k, masking) followed by the sparse average of their
 four messages into a dense gradient.  Inputs are seeded synthetic gradients
 already resident in HBM; three distinct gradient sets rotate, 409 MB each,
-so every step streams inputs far larger than the 129 MB L2.
+so every step streams inputs far larger than the 129 MB L2.  The timed
+steps are plain calls; the same steps replayed from CUDA graphs are timed
+afterwards and reported beside them.
 
 One JSON line on rank 0: whole-job gradient GB/s (value), the same metric end
 to end with host buffers (e2e), the roofline of the dominant kernel, the CPU
@@ -448,43 +450,46 @@ def run_gpu(args):
     # a gradient set that L2 could hold is not "larger than L2": flush between steps instead
     flush_l2 = 4 * K * N < 2 * L2_BYTES
     flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev) if flush_l2 else None
-    # timed region: events bracket only the dominant kernel's launches (events
-    # around every kernel would sit between the kernels and stretch the step)
-    clocks = ClockSampler(local)
-    gc.launch_count_reset()
-    gc.trace_only(path.dominant)
-    gc.trace_enable(True)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    if flush_l2:  # each step timed alone, with L2 flushed before it (the flush is outside the events)
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-        with nvtx_range("timed steps"):
+    def run_timed(step_fn):
+        """Times args.steps calls of step_fn(i), with a barrier and a synchronize on both sides; returns
+        this rank's ms per step (L2 flushed before each step, outside the events, when flush_l2)."""
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        if flush_l2:
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
             for i in range(args.steps):
                 flush_buf.fill_(i)
                 ev[i][0].record(stream)
-                path.step(grads[i % N_SETS], t=args.warmup + i)
+                step_fn(i)
                 ev[i][1].record(stream)
-    else:
-        with nvtx_range("timed steps"):
+        else:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             for i in range(args.steps):
-                path.step(grads[i % N_SETS], t=args.warmup + i)
+                step_fn(i)
             e1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    clk = clocks.stop()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        if flush_l2:
+            return sum(x.elapsed_time(y) for x, y in ev) / args.steps
+        return e0.elapsed_time(e1) / args.steps
+
+    clocks = ClockSampler(local)
+    gc.launch_count_reset()
+    gc.trace_only(path.dominant)  # events around the dominant kernel only
+    gc.trace_enable(True)
+    with nvtx_range("timed steps"):
+        ms_local = run_timed(lambda i: path.step(grads[i % N_SETS], t=args.warmup + i))
     gc.trace_enable(False)
     gc.trace_only(None)
     launches = gc.launch_count()
     trace = gc.trace_read()
-    if flush_l2:
-        ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev) / args.steps, dev)
-    else:
-        ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
+    clk = clocks.stop()
+    ms = max_over_ranks(ms_local, dev)
     # every kernel's time, from a separate traced pass of the same steps (after the timed region)
     gc.trace_enable(True)
     with nvtx_range("traced steps"):
@@ -495,6 +500,25 @@ def run_gpu(args):
     trace_all = gc.trace_read()
     grad_bytes = 4.0 * K * N
     value = job_gbs(world, grad_bytes, ms)
+
+    # For comparison, the same steps replayed from CUDA graphs (one captured per gradient set, no
+    # trace events in them): what launching from the host costs the step.  DCD's graphs replay the
+    # step counters they were captured with.
+    timing = {"mode": "plain calls"}
+    try:
+        graphs = []
+        for i in range(N_SETS):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                path.step(grads[i], t=args.warmup + i)
+            graphs.append(g)
+        with nvtx_range("graph replays"):
+            ms_graph = max_over_ranks(run_timed(lambda i: graphs[i % N_SETS].replay()), dev)
+        timing.update(graph_ms_per_step=ms_graph, graph_value=job_gbs(world, grad_bytes, ms_graph))
+        del graphs
+    except Exception as exc:  # reported, not fatal: the timed figure above stands
+        torch.cuda.synchronize()
+        timing["graph_error"] = f"{type(exc).__name__}: {exc}"[:200]
 
     # the messages as byte streams (DGC: 16-bit zero runs + 32-bit values;
     # AdaComp: per-layer count and scale, then index|sign words), from the
@@ -737,6 +761,7 @@ def run_gpu(args):
                      "peak_kind": f"{peak_kind} (copy)", "unit": "GB/s",
                      "frac": (achieved / hbm) if achieved else None,
                      "algorithmic_bytes_per_launch": dom_bytes, "traffic": traffic,
+                     "launches_timed": n_dom,
                      "frac_of_nominal_8tbs": (achieved / 8000.0) if achieved else None},
         "kernels": kernels,  # from the traced pass after the timed region
         "kernels_pass": "separate traced pass of the same steps",
@@ -747,6 +772,7 @@ def run_gpu(args):
         "fused_update": fused,
         "sampled_threshold": sampled,
         "nesterov_variant": nesterov,
+        "timing": timing,
         "ecd_variant": ecd,
         "gpu_launches": launches,
         "clocks": clk,

@@ -90,14 +90,29 @@ static cudaEvent_t take_event() {
     return e;
 }
 
+// A trace event is recorded as an external event node when the stream is
+// being captured into a CUDA graph (so each replay records it again and the
+// replays can be timed from outside the graph), as a plain record otherwise;
+// the external flag is refused on a stream that is not capturing.
+static void record_trace_event(cudaEvent_t e, cudaStream_t s) {
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &st) == cudaSuccess && st == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+    else
+        cudaEventRecord(e, s);
+}
+
+// Any error left over from an earlier runtime call is cleared before the
+// launch, so check_launch reports this launch's own.
 LaunchScope::LaunchScope(const char* n, cudaStream_t s) : name(n), stream(s), slot(-1) {
+    (void)cudaGetLastError();
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (!g_trace.load(std::memory_order_relaxed)) return;
     std::lock_guard<std::mutex> lk(g_trace_mu);
     if (!g_trace_name.empty() && g_trace_name != n) return;
     cudaEvent_t a = take_event(), b = take_event();
     if (!a || !b) return;
-    cudaEventRecord(a, s);
+    record_trace_event(a, s);
     g_pending.push_back({std::string(n), a, b});
     slot = (int)g_pending.size() - 1;
 }
@@ -105,7 +120,7 @@ LaunchScope::LaunchScope(const char* n, cudaStream_t s) : name(n), stream(s), sl
 LaunchScope::~LaunchScope() {
     if (slot < 0) return;
     std::lock_guard<std::mutex> lk(g_trace_mu);
-    if (slot < (int)g_pending.size()) cudaEventRecord(g_pending[slot].b, stream);
+    if (slot < (int)g_pending.size()) record_trace_event(g_pending[slot].b, stream);
 }
 
 // ------------------------------------------------------------ validation
@@ -171,8 +186,10 @@ int gcsgd_trace_read(gcsgd_trace_entry* entries, int32_t max, int32_t* n_out) {
     int rc = GCSGD_OK;
     for (auto& p : g_pending) {
         float ms = 0.0f;
-        if (cudaEventSynchronize(p.b) != cudaSuccess || cudaEventElapsedTime(&ms, p.a, p.b) != cudaSuccess)
+        if (cudaEventSynchronize(p.b) != cudaSuccess || cudaEventElapsedTime(&ms, p.a, p.b) != cudaSuccess) {
             rc = set_error(GCSGD_ERR_CUDA, "gcsgd_trace_read: event timing failed");
+            (void)cudaGetLastError();  // not left pending for the next launch check
+        }
         if (!agg.count(p.name)) order.push_back(p.name);
         agg[p.name].first += 1;
         agg[p.name].second += ms;

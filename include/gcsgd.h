@@ -364,7 +364,10 @@ int64_t gcsgd_launch_count(void);
 void gcsgd_launch_count_reset(void);
 
 /* Per-kernel timing.  While enabled, every kernel launch is bracketed by
- * two CUDA events recorded on its own stream (a small extra cost).
+ * two CUDA events recorded on its own stream (a small extra cost).  Under
+ * stream capture the events become external event nodes of the graph: each
+ * replay records them again, and a read after the replays returns the last
+ * replay's times.
  * gcsgd_trace_read waits for the recorded events, then writes up to `max`
  * entries (kernel name, launches, summed milliseconds) and the entry count
  * to *n_out; it clears the record.  Host functions. */

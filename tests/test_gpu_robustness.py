@@ -1,8 +1,9 @@
 """Robustness of the CUDA path: nothing is written past a buffer the caller
 passed (canary words after every output and state buffer), a learner that
 drops out of a step leaves an average of the others equal to the oracle's,
-and AdaComp's state is the caller's residue (save, restore, resume bit for
-bit).  No test here faults or hangs a GPU: a failure is made on the host.
+AdaComp's state is the caller's residue (save, restore, resume bit for
+bit), and a whole step replays from a CUDA graph.  No test here faults or
+hangs a GPU: a failure is made on the host.
 """
 import numpy as np
 import pytest
@@ -176,3 +177,92 @@ def test_adacomp_checkpoint_resume_is_bit_identical(cuda_lib):
             n = int(tot[k])
             assert torch.equal(o[k, :n], outs[t][0][k, :n])
     assert torch.equal(R3, R)
+
+
+@pytest.mark.parametrize("method", ["dgc", "adacomp"])
+def test_step_replays_from_a_cuda_graph(cuda_lib, method):
+    """A whole step (compress + average) captured once into a CUDA graph and
+    replayed: the library allocates nothing and never synchronises, so the
+    replays give the same bits as eager calls from the same state."""
+    import torch
+    gc = cuda_lib
+    w = wl.workload(2 if method == "dgc" else 3, small=True)
+    K, N = w.learners, w.n
+    grads = [wl.gradients(w, t).cuda() for t in range(3)]
+    g_in = grads[0].clone()
+
+    def make():
+        if method == "dgc":
+            obj = gc.DGC(w.offsets, K, w.density, w.momentum)
+            state = [torch.zeros((K, N), device="cuda"), torch.zeros((K, N), device="cuda")]
+        else:
+            obj = gc.AdaComp(w.offsets, w.lt, K, N // 4)
+            state = [torch.zeros((K, N), device="cuda")]
+        return obj, state, torch.empty(N, device="cuda")
+
+    def step(obj, state, g, avg):
+        out, tot = obj(g, *state)
+        gc.sparse_average(out, tot, N, avg)
+
+    # eager reference
+    obj_e, st_e, avg_e = make()
+    ref = []
+    for t in range(3):
+        step(obj_e, st_e, grads[t], avg_e)
+        ref.append((avg_e.clone(), [x.clone() for x in st_e]))
+    torch.cuda.synchronize()
+    # captured: warm up the library (first-call attributes) on a side stream, then capture
+    obj_g, st_g, avg_g = make()
+    scratch = [torch.zeros_like(x) for x in st_g]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        step(obj_g, scratch, g_in, avg_g)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(obj_g, st_g, g_in, avg_g)
+    for x in st_g:
+        x.zero_()
+    for t in range(3):
+        g_in.copy_(grads[t])
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(avg_g, ref[t][0])
+        for a, b in zip(st_g, ref[t][1]):
+            assert torch.equal(a, b)
+
+
+def test_trace_events_captured_into_a_graph_time_its_replay(cuda_lib):
+    """Tracing on while a step is captured: the traced kernel's two events
+    become event nodes of the graph, and a read after a replay returns one
+    launch of that kernel with a positive duration (the replay's)."""
+    import torch
+    gc = cuda_lib
+    w = wl.workload(2, small=True)
+    K, N = w.learners, w.n
+    d = gc.DGC(w.offsets, K, w.density, w.momentum)
+    u = torch.zeros((K, N), device="cuda")
+    v = torch.zeros((K, N), device="cuda")
+    g_in = wl.gradients(w, 0).cuda()
+    s = torch.cuda.Stream()
+    gc.trace_only("dgc_update")
+    gc.trace_enable(True)
+    try:
+        with torch.cuda.stream(s):  # eager traced call: first-call attributes, events in the pool
+            d(g_in, u, v)
+        torch.cuda.synchronize()
+        gc.trace_read()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            d(g_in, u, v)
+        gc.trace_enable(False)
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize()
+        tr = gc.trace_read()
+    finally:
+        gc.trace_enable(False)
+        gc.trace_only(None)
+    assert set(tr) == {"dgc_update"}
+    n, ms = tr["dgc_update"]
+    assert n == 1 and 0.0 < ms < 1000.0
