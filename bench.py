@@ -271,7 +271,7 @@ def config_dict(w, **extra):
              "dcd": "dcd_step(n ring nodes)"}
     d = {"workload": w.name, "learners": w.learners, "elements_per_learner": w.n, "segments": len(w.sizes),
          "step": steps[w.method],
-         "l2": ("L2 flushed between steps (a 256 MB write outside the timed events), each step timed alone"
+         "l2": ("L2 flushed between steps (a 256 MB write, then a read of it, outside the timed events), each step timed alone"
                 if 4 * w.learners * w.n < 2 * L2_BYTES else
                 "inputs larger than L2: 3 rotating gradient sets of K*N*4 bytes each")}
     if w.method == "dgc":
@@ -460,7 +460,8 @@ def run_gpu(args):
             ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                   for _ in range(args.steps)]
             for i in range(args.steps):
-                flush_buf.fill_(i)
+                flush_buf.fill_(i)  # evicts the step's inputs from L2 ...
+                flush_buf.sum()  # ... and reading it back writes its dirty lines out before the events
                 ev[i][0].record(stream)
                 step_fn(i)
                 ev[i][1].record(stream)

@@ -56,7 +56,7 @@ constexpr uint32_t kStageItems = 8192;   // candidates dgc_select stages in shar
 constexpr int kChunkTiles = 4 * NTS;     // tile-table entries dgc_select scans per round
 constexpr size_t kStageBytes = kStageItems * sizeof(uint2);  // also holds kRawMax floats
 static_assert(kStageBytes >= kRawMax * sizeof(float), "the stage must hold a raw segment");
-constexpr int kSumsqBlocks = 128;        // CTAs per learner in dgc_sumsq
+constexpr int kSumsqBlocks = 512;        // CTAs per learner in dgc_sumsq
 
 // Plan of one segment.  sample_frac = 0: the exact step (the hint only
 // steers the candidate pool).  sample_frac > 0: the sampled threshold (the
@@ -192,19 +192,27 @@ __global__ void __launch_bounds__(NT) dgc_sumsq(const float* __restrict__ grad, 
 }
 
 // Local gradient clipping scale (Appendix C): thr_k = thr / sqrt(N_nodes),
-// c = thr_k / ||G|| when ||G|| > thr_k.  The per-CTA partial sums of squares
-// are combined in a fixed order with compensated summation, so every CTA that
-// evaluates this gets the same c.
-__device__ float clip_scale(const double* __restrict__ part, int k, float clip_thr, int clip_nodes) {
+// c = thr_k / ||G|| when ||G|| > thr_k.  Called by a whole warp: lane l adds
+// partial sums 16l .. 16l+15 as a pairwise tree, then a butterfly over the
+// lanes adds the lane sums in a fixed tree (a + b and b + a are the same
+// bits), so every lane of every CTA that evaluates this gets the same c.
+// The partials are non-negative, so the tree sum needs no compensation
+// (relative error below 9 * 2^-53).
+__device__ float clip_scale_warp(const double* __restrict__ part, int k, float clip_thr, int clip_nodes) {
+    static_assert(kSumsqBlocks == 16 * 32, "16 partial sums per lane");
     if (!(clip_thr > 0.0f)) return 1.0f;
-    double s = 0.0, comp = 0.0;
-    for (int i = 0; i < kSumsqBlocks; ++i) {
-        const double x = part[(uint64_t)k * kSumsqBlocks + i];
-        const double t = s + x;
-        comp += fabs(s) >= fabs(x) ? (s - t) + x : (x - t) + s;
-        s = t;
-    }
-    const double norm = sqrt(s + comp);
+    const double* pk = part + (uint64_t)k * kSumsqBlocks + 16 * (threadIdx.x & 31);
+    double x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = pk[i];
+#pragma unroll
+    for (int w = 1; w < 16; w <<= 1)
+#pragma unroll
+        for (int i = 0; i < 16; i += 2 * w) x[i] = x[i] + x[i + w];
+    double s = x[0];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) s = s + __shfl_xor_sync(kFull, s, d);
+    const double norm = sqrt(s);
     const double thr_k = (double)clip_thr / sqrt((double)clip_nodes);
     return norm > thr_k ? (float)(thr_k / norm) : 1.0f;
 }
@@ -284,7 +292,10 @@ __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, PoolL
             }
             __syncthreads();
         }
-        for (int k = threadIdx.x; k < K; k += NTP) clip_c[k] = clip_scale(part, k, clip_thr, clip_nodes);
+        for (int k = (int)threadIdx.x >> 5; k < K; k += NTP / 32) {  // one warp per learner
+            const float c = clip_scale_warp(part, k, clip_thr, clip_nodes);
+            if ((threadIdx.x & 31) == 0) clip_c[k] = c;
+        }
         return;
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -294,9 +305,12 @@ __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, PoolL
         const int k = pj / P, q = pj - k * P;
         const int s = pl.seg[q];
         const int unit = k * S + s;
-        if (threadIdx.x == 0) {
-            s_c = clip_scale(part, k, clip_thr, clip_nodes);
-            pool_cnt[unit] = 0;
+        if (warp == 0) {
+            const float c = clip_scale_warp(part, k, clip_thr, clip_nodes);
+            if (lane == 0) {
+                s_c = c;
+                pool_cnt[unit] = 0;
+            }
         }
         __syncthreads();
         SegPlan p;
