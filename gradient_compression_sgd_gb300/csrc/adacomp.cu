@@ -53,6 +53,11 @@ struct SegPlan {
 };
 
 constexpr uint32_t kGroup = 8;  // tiles per ada_emit work item
+constexpr size_t kEmitSmemMax = 200 * 1024;  // ada_emit's per-learner and per-segment tables
+
+// Shared memory of ada_emit: each learner's total and each (learner,
+// segment)'s first output slot.
+inline size_t emit_smem_bytes(int K, int S) { return sizeof(uint32_t) * (size_t)K * S + sizeof(uint64_t) * (size_t)K; }
 
 template <int MAXS>
 struct SegTable {
@@ -980,6 +985,10 @@ int adacomp_launch(const int64_t* off, int S, const int32_t* lt, int K, const fl
     const uint64_t T = (uint64_t)K * hp.tiles_per_learner;
     if (T >= ((uint64_t)1 << 32))
         return set_error(GCSGD_ERR_INVALID_ARG, "adacomp_compress: K * tiles = %llu exceeds 2^32", (unsigned long long)T);
+    if (emit_smem_bytes(K, S) > kEmitSmemMax)  // checked before anything is enqueued
+        return set_error(GCSGD_ERR_INVALID_ARG,
+                         "adacomp_compress: K * (4 n_seg + 8) = %lld bytes of emit tables exceed %d",
+                         (long long)emit_smem_bytes(K, S), (int)kEmitSmemMax);
     int rc;
     {
         LaunchScope ls("ada_plan", stream);
@@ -1043,16 +1052,13 @@ int adacomp_launch(const int64_t* off, int S, const int32_t* lt, int K, const fl
     }
     {
         LaunchScope ls("ada_emit", stream);
-        const size_t smem = sizeof(uint32_t) * (size_t)K * S + sizeof(uint64_t) * (size_t)K;
-        if (smem > 200 * 1024)
-            return set_error(GCSGD_ERR_INVALID_ARG, "adacomp_compress: K * n_seg = %d too large (at most ~51000)",
-                             K * S);
+        const size_t smem = emit_smem_bytes(K, S);
         if (smem > 48 * 1024) {
             static bool done[64] = {};
             int dev = 0;
             cudaGetDevice(&dev);
             if (dev < 64 && !done[dev]) {
-                if (cudaFuncSetAttribute(ada_emit, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
+                if (cudaFuncSetAttribute(ada_emit, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kEmitSmemMax) !=
                     cudaSuccess)
                     return set_error(GCSGD_ERR_CUDA, "adacomp_compress: cannot raise the shared-memory limit");
                 done[dev] = true;

@@ -1010,6 +1010,10 @@ int dgc_launch(const int64_t* off, int S, int K, const float* grad, float* u, fl
     if ((uint64_t)cap < hp.out_per_learner)
         return set_error(GCSGD_ERR_CAPACITY, "dgc_compress: cap %lld below the %llu entries per learner",
                          (long long)cap, (unsigned long long)hp.out_per_learner);
+    const uint64_t total_tiles = (uint64_t)K * hp.tiles_per_learner;
+    if (total_tiles >= ((uint64_t)1 << 32))
+        return set_error(GCSGD_ERR_INVALID_ARG, "dgc_compress: K * tiles = %llu exceeds 2^32",
+                         (unsigned long long)total_tiles);
     const bool clip = clip_thr > 0.0f;
     int rc;
     if (clip) {
@@ -1056,10 +1060,6 @@ int dgc_launch(const int64_t* off, int S, int K, const float* grad, float* u, fl
         }
         if ((rc = check_launch("dgc_prepare"))) return rc;
     }
-    const uint64_t total_tiles = (uint64_t)K * hp.tiles_per_learner;
-    if (total_tiles >= ((uint64_t)1 << 32))
-        return set_error(GCSGD_ERR_INVALID_ARG, "dgc_compress: K * tiles = %llu exceeds 2^32",
-                         (unsigned long long)total_tiles);
     if (total_tiles > 0) {
         LaunchScope ls("dgc_update", stream);
         uint64_t grid = (uint64_t)sm_count() * 3;

@@ -223,6 +223,9 @@ int gcsgd_adacomp_workspace_size(const int64_t* seg_offsets, int32_t n_seg, cons
  *             cap the list and residue of learner k are unspecified and the
  *             caller must retry with a larger cap.
  * workspace   at least gcsgd_adacomp_workspace_size bytes, 256-byte aligned.
+ * Limit: K * (4 * n_seg + 8) <= 204800 (K <= 24 at 2048 tensors, K <= 198 at
+ * 256); a larger call returns GCSGD_ERR_INVALID_ARG before anything is
+ * enqueued.
  */
 int adacomp_compress(const int64_t* seg_offsets, int32_t n_seg, const int32_t* lt, int32_t K,
                      const float* dW, float* residue,

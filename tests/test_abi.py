@@ -125,3 +125,17 @@ def test_trace_filter_takes_and_clears_a_name(L):
         gc.trace_only("x" * 48)
     gc.trace_only(None)
     assert L.gcsgd_trace_only(None) == 0
+
+
+def test_adacomp_emit_table_limit_checked_before_launch(L):
+    """K * (4 n_seg + 8) bytes of emit tables above 200 KiB: refused before
+    anything is enqueued (no GPU is touched here)."""
+    S = gc.MAX_SEGMENTS
+    off = np.arange(S + 1, dtype=np.int64)
+    lt = np.full(S, 50, np.int32)
+    x = ctypes.c_void_p(0x1000)
+    ws = ctypes.c_void_p(0x1000 * 256)
+    K = 25  # 25 * (4 * 2048 + 8) = 205,000 > 204,800
+    rc, msg = _call(L, "adacomp_compress", off.ctypes.data_as(ctypes.c_void_p), S, lt.ctypes.data_as(ctypes.c_void_p),
+                    K, x, x, x, S, x, x, x, ws, 1 << 40, None)
+    assert rc == -1 and "emit tables" in msg

@@ -91,3 +91,25 @@ def test_adacomp_average_and_wire_at_the_maximum_tensor_count(cuda_lib):
         n = int(tot[k])
         np.testing.assert_array_equal(li[k, :n, 0].view(np.uint32), idx[k, :n])
         np.testing.assert_array_equal(li[k, :n, 1].view(np.float32), val[k, :n])
+
+
+def test_adacomp_learner_limit_at_the_maximum_tensor_count(cuda_lib):
+    """At 2048 tensors 24 learners fit ada_emit's tables and match the
+    oracle; 25 are refused before anything runs, leaving the residue as it
+    was."""
+    import torch
+    gc = cuda_lib
+    S = gc.MAX_SEGMENTS
+    sizes = [3] * S
+    off = wl.layout_offsets(sizes)
+    lt = [2] * S
+    rng = np.random.default_rng(37)
+    dWs = [rng.laplace(0, 1e-2, size=(24, 3 * S)).astype(np.float32)]
+    run_adacomp(gc, off, lt, dWs)
+    R = torch.from_numpy(rng.standard_normal((25, 3 * S)).astype(np.float32)).cuda()
+    R0 = R.clone()
+    a = gc.AdaComp(off, lt, 25, 3 * S)
+    with pytest.raises(gc.GcsgdError, match="emit tables"):
+        a(torch.from_numpy(rng.laplace(0, 1e-2, size=(25, 3 * S)).astype(np.float32)).cuda(), R)
+    torch.cuda.synchronize()
+    assert torch.equal(R, R0)
