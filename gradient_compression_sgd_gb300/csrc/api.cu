@@ -111,7 +111,11 @@ LaunchScope::LaunchScope(const char* n, cudaStream_t s) : name(n), stream(s), sl
     std::lock_guard<std::mutex> lk(g_trace_mu);
     if (!g_trace_name.empty() && g_trace_name != n) return;
     cudaEvent_t a = take_event(), b = take_event();
-    if (!a || !b) return;
+    if (!a || !b) {  // untraced launch; keep whichever event was made
+        if (a) g_free_events.push_back(a);
+        if (b) g_free_events.push_back(b);
+        return;
+    }
     record_trace_event(a, s);
     g_pending.push_back({std::string(n), a, b});
     slot = (int)g_pending.size() - 1;

@@ -370,7 +370,9 @@ void gcsgd_launch_count_reset(void);
  * two CUDA events recorded on its own stream (a small extra cost).  Under
  * stream capture the events become external event nodes of the graph: each
  * replay records them again, and a read after the replays returns the last
- * replay's times.
+ * replay's times.  The read hands the events back to the library, so a
+ * graph replayed after it records into events that later launches may
+ * reuse: read once, after the last replay.
  * gcsgd_trace_read waits for the recorded events, then writes up to `max`
  * entries (kernel name, launches, summed milliseconds) and the entry count
  * to *n_out; it clears the record.  Host functions. */
