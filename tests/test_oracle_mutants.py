@@ -46,6 +46,9 @@ MUTANTS = {
     "ada_mean_over_nb_minus_1": ("/ (double)nb);", "/ (double)(nb > 1 ? nb - 1 : 1));"),
     "ada_partial_bin_dropped": ("const int64_t nb = (n + L - 1) / L;", "const int64_t nb = n / L > 0 ? n / L : 1;"),
     # sparse average
+    "average_reverse_learner_order": ("    for (int k = 0; k < K; ++k) {\n        if (counts[k] < 0 || counts[k] > cap)",
+                                      "    for (int k = K - 1; k >= 0; --k) {\n        if (counts[k] < 0 || counts[k] > cap)"),
+    "ada_bin_max_of_dw": ("float a = fabsf(G[off + i]);", "float a = fabsf(dWk[off + i]);"),
     "average_not_divided": ("out[j] = out[j] / fk;", "out[j] = out[j];"),
     "update_adds_the_step": ("w[j] = w[j] - step;", "w[j] = w[j] + step;"),
     "update_skips_last_list": ("for (int k = 0; k < K; ++k)\n            for (int64_t p = 0; p < counts[k]; ++p) carried",
