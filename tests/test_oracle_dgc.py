@@ -142,6 +142,31 @@ def test_zero_momentum_is_plain_residual_accumulation():
     np.testing.assert_array_equal(total_sent + v[0], total_grad)
 
 
+def test_clipping_norm_spans_every_tensor_of_a_learner():
+    """The clipping norm is the learner's whole gradient, across tensors (DGC,
+    Appendix C: the local gradient's L2 norm), and each learner has its own:
+    the scale is thr / ||G_k|| over all of learner k's values (numpy's fp64
+    norm), not over one tensor, and at density 1 what is sent has norm thr."""
+    rng = np.random.default_rng(7)
+    sizes = [1000, 3000, 96]
+    off = np.array([0, 1000, 4000, 4096], np.int64)
+    K, N = 2, 4096
+    G = np.concatenate([rng.standard_normal((K, n)) * s for n, s in zip(sizes, (0.2, 0.01, 0.5))], axis=1)
+    G = G.astype(np.float32)
+    thr = 1.0
+    u = np.zeros((K, N), np.float32)
+    v = np.zeros((K, N), np.float32)
+    _, val, _, cs = _step(off, G, u, v, 1.0, 0.0, clip=thr, nodes=1)
+    for k in range(K):
+        whole = np.linalg.norm(G[k].astype(np.float64))
+        first = np.linalg.norm(G[k, :1000].astype(np.float64))
+        assert whole > thr and abs(whole - first) > 0.1 * whole
+        assert cs[k] == np.float32(thr / whole)
+        sent = val[k].astype(np.float64)
+        assert abs(np.linalg.norm(sent) - thr) <= 1e-6 * thr
+    assert cs[0] != cs[1]
+
+
 @pytest.mark.parametrize("nodes", [1, 4])
 def test_local_gradient_clipping(nodes):
     """The scale is thr_k / ||G|| with thr_k = thr / sqrt(N) (Appendix C), from

@@ -27,6 +27,9 @@ MUTANTS = {
     "ties_to_higher_index": ("return x->idx < y->idx ? -1 : 1;", "return x->idx > y->idx ? -1 : 1;"),
     "u_not_masked": ("uk[off + i] = 0.0f;\n            }", "}"),
     "v_not_masked": ("vk[off + i] = 0.0f;\n                uk", "uk"),
+    "clip_norm_of_first_tensor": ("for (int64_t i = 0; i < N; ++i) csum_add(&acc, (double)G[i] * (double)G[i]);",
+                                  "for (int64_t i = 0; i < seg_off[1]; ++i) csum_add(&acc, (double)G[i] * (double)G[i]);"),
+    "topk_key_keeps_sign": ("return bits_of(f) & 0x7fffffffu;", "return bits_of(f);"),
     "clip_ignores_nodes": ("/ sqrt((double)clip_nodes)", "/ 1.0"),
     "clip_scale_inverted": ("if (norm > thr_k) { c = (float)(thr_k / norm)", "if (norm > thr_k) { c = (float)(norm / thr_k)"),
     "k_floor": ("double kd = ceil(density * (double)n);", "double kd = floor(density * (double)n);"),
