@@ -52,6 +52,12 @@ MUTANTS = {
     "average_reverse_learner_order": ("    for (int k = 0; k < K; ++k) {\n        if (counts[k] < 0 || counts[k] > cap)",
                                       "    for (int k = K - 1; k >= 0; --k) {\n        if (counts[k] < 0 || counts[k] > cap)"),
     "ada_bin_max_of_dw": ("float a = fabsf(G[off + i]);", "float a = fabsf(dWk[off + i]);"),
+    "dgc_sends_u": ("out_val[pos] = vk[off + i];", "out_val[pos] = uk[off + i];"),
+    "ada_unselected_residue_dw": ("                Rk[i] = G[i];\n            }", "                Rk[i] = G[i] - Rk[i];\n            }"),
+    "ada_scale_of_last_bin": ("const float scale = (float)(csum_value(&acc) / (double)nb);",
+                              "const float scale = (float)bmax[nb - 1];"),
+    "dcd_reads_updated_left_neighbour": ("const float* xl = xhat + (int64_t)l * d;",
+                                         "const float* xl = (l < i ? xn : xhat) + (int64_t)l * d;"),
     "average_not_divided": ("out[j] = out[j] / fk;", "out[j] = out[j];"),
     "update_adds_the_step": ("w[j] = w[j] - step;", "w[j] = w[j] + step;"),
     "update_skips_last_list": ("for (int k = 0; k < K; ++k)\n            for (int64_t p = 0; p < counts[k]; ++p) carried",
