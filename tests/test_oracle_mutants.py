@@ -30,6 +30,7 @@ MUTANTS = {
     "clip_norm_of_first_tensor": ("for (int64_t i = 0; i < N; ++i) csum_add(&acc, (double)G[i] * (double)G[i]);",
                                   "for (int64_t i = 0; i < seg_off[1]; ++i) csum_add(&acc, (double)G[i] * (double)G[i]);"),
     "topk_key_keeps_sign": ("return bits_of(f) & 0x7fffffffu;", "return bits_of(f);"),
+    "clip_not_applied": ("float g = clipped ? G[i] * c : G[i];", "float g = G[i];"),
     "clip_ignores_nodes": ("/ sqrt((double)clip_nodes)", "/ 1.0"),
     "clip_scale_inverted": ("if (norm > thr_k) { c = (float)(thr_k / norm)", "if (norm > thr_k) { c = (float)(norm / thr_k)"),
     "k_floor": ("double kd = ceil(density * (double)n);", "double kd = floor(density * (double)n);"),
