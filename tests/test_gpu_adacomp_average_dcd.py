@@ -408,6 +408,20 @@ def test_dcd_keep_all_and_weights(cuda_lib):
     run_dcd(cuda_lib, 1, 5000, 2, 1.0, w=(0.0, 1.0, 0.0))
 
 
+@pytest.mark.parametrize("n", [5, 13])
+def test_dcd_asymmetric_ring_weights(cuda_lib, n):
+    """w_ring = (left, self, right) with unequal weights, p = 1 and p = 0.3:
+    the fixed-size (n = 5) and rolling (n = 13) kernels take node i - 1 as
+    the left neighbour, as the oracle does (3 steps, so the models differ)."""
+    run_dcd(cuda_lib, n, 5003, 3, 1.0, w=(0.6, 0.3, 0.1))
+    run_dcd(cuda_lib, n, 5003, 3, 0.3, w=(0.1, 0.25, 0.65))
+
+
+@pytest.mark.parametrize("n", [3, 9])
+def test_ecd_asymmetric_ring_weights(cuda_lib, n):
+    run_ecd(cuda_lib, n, 4099, 3, 0.5, w=(0.6, 0.3, 0.1))
+
+
 def test_philox_matches_curand_device_api(cuda_lib, tmp_path):
     """The oracle's Philox4x32-10 word block at counter (q, node, t, q >> 32)
     under key (seed) equals cuRAND's curand4 after curand_init(seed,

@@ -143,6 +143,20 @@ def test_keep_all_is_dpsgd():
     assert np.abs(got - x_half).max() <= 8 * np.spacing(np.float32(scale))
 
 
+def test_left_weight_takes_the_previous_node():
+    """w_ring is (left, self, right) with node i's left neighbour i - 1 (mod n):
+    with W = (1, 0, 0), p = 1 and g = 0 every node's model becomes its left
+    neighbour's, exactly (small integers: every sum and difference is exact);
+    with W = (0, 0, 1) its right neighbour's."""
+    n, d = 5, 37
+    x = np.arange(n * d, dtype=np.float32).reshape(n, d) % 97
+    g = np.zeros((n, d), np.float32)
+    left = oracle.dcd_step(x.copy(), g, (1.0, 0.0, 0.0), 0.1, 1.0, 9, 0)
+    np.testing.assert_array_equal(left, np.roll(x, 1, axis=0))
+    right = oracle.dcd_step(x.copy(), g, (0.0, 0.0, 1.0), 0.1, 1.0, 9, 0)
+    np.testing.assert_array_equal(right, np.roll(x, -1, axis=0))
+
+
 def test_single_node_is_sgd():
     rng = np.random.default_rng(5)
     d = 777

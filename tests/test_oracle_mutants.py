@@ -70,6 +70,8 @@ MUTANTS = {
     "philox_key_word_swapped": ("uint32_t n0 = hi1 ^ c1 ^ k0;", "uint32_t n0 = hi1 ^ c1 ^ k1;"),
     "dcd_wrong_neighbour": ("const int l = (i + n - 1) % n, r = (i + 1) % n;\n        const float* xl",
                             "const int l = (i + n - 1) % n, r = (i + 2) % n;\n        const float* xl"),
+    "dcd_ring_weights_mirrored": ("float acc = w[0] * xl[e];\n            acc = acc + w[1] * xi[e];\n            acc = acc + w[2] * xr[e];",
+                                  "float acc = w[2] * xl[e];\n            acc = acc + w[1] * xi[e];\n            acc = acc + w[0] * xr[e];"),
     "dcd_gradient_sign": ("const float xh = acc - gamma * gi[e];", "const float xh = acc + gamma * gi[e];"),
     "dcd_no_unbiasing_scale": ("return ((uint64_t)word < thr) ? z * inv_p : 0.0f;",
                                "return ((uint64_t)word < thr) ? z : 0.0f;"),
