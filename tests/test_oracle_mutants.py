@@ -72,6 +72,8 @@ MUTANTS = {
                             "const int l = (i + n - 1) % n, r = (i + 2) % n;\n        const float* xl"),
     "dcd_ring_weights_mirrored": ("float acc = w[0] * xl[e];\n            acc = acc + w[1] * xi[e];\n            acc = acc + w[2] * xr[e];",
                                   "float acc = w[2] * xl[e];\n            acc = acc + w[1] * xi[e];\n            acc = acc + w[0] * xr[e];"),
+    "dcd_compresses_the_model": ("            const float z = xh - xi[e];\n            const uint32_t word = dcd_word(",
+                                 "            const float z = xh;\n            const uint32_t word = dcd_word("),
     "dcd_gradient_sign": ("const float xh = acc - gamma * gi[e];", "const float xh = acc + gamma * gi[e];"),
     "dcd_no_unbiasing_scale": ("return ((uint64_t)word < thr) ? z * inv_p : 0.0f;",
                                "return ((uint64_t)word < thr) ? z : 0.0f;"),
