@@ -77,6 +77,9 @@ MUTANTS = {
     "dcd_gradient_sign": ("const float xh = acc - gamma * gi[e];", "const float xh = acc + gamma * gi[e];"),
     "dcd_no_unbiasing_scale": ("return ((uint64_t)word < thr) ? z * inv_p : 0.0f;",
                                "return ((uint64_t)word < thr) ? z : 0.0f;"),
+    "ecd_estimate_from_uncompressed_z": ("xt[q] = c * xt[q] + e2 * cz;", "xt[q] = c * xt[q] + e2 * z;"),
+    "ecd_gradient_sign": ("x_prev[(int64_t)i * d + e] = acc - gamma * g[(int64_t)i * d + e];",
+                          "x_prev[(int64_t)i * d + e] = acc + gamma * g[(int64_t)i * d + e];"),
     "ecd_extrapolation_swapped": ("const float z = a * x_prev[q] + b * x[q];", "const float z = b * x_prev[q] + a * x[q];"),
     "ecd_estimate_weight": ("const float c = (float)(1.0 - 2.0 / (double)t)", "const float c = (float)(1.0 - 1.0 / (double)t)"),
     "ecd_self_from_estimate": ("acc = acc + w[1] * x[(int64_t)i * d + e];", "acc = acc + w[1] * xt[(int64_t)i * d + e];"),
