@@ -65,6 +65,10 @@ MUTANTS = {
                                "for (int k = 0; k < K - 1; ++k)\n            for (int64_t p = 0; p < counts[k]; ++p) carried"),
     # wire encodings
     "wire_escape_width": ("            gap -= 65536;", "            gap -= 65535;"),
+    "wire_ada_global_index": ("const uint32_t local = (uint32_t)((int64_t)idx[j] - seg_off[s]);",
+                              "const uint32_t local = (uint32_t)((int64_t)idx[j]);"),
+    "wire_dgc_decode_gap_off_by_one": ("        memcpy(&dense[pos], &b, 4);\n        ++pos;\n",
+                                       "        memcpy(&dense[pos], &b, 4);\n"),
     "wire_sign_bit": ("const uint32_t sign = val[j] < 0.0f ? 1u : 0u;", "const uint32_t sign = val[j] > 0.0f ? 1u : 0u;"),
     # Philox and DCD-PSGD
     "philox_key_word_swapped": ("uint32_t n0 = hi1 ^ c1 ^ k0;", "uint32_t n0 = hi1 ^ c1 ^ k1;"),
