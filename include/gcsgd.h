@@ -220,8 +220,10 @@ int gcsgd_adacomp_workspace_size(const int64_t* seg_offsets, int32_t n_seg, cons
  * scales      [K][n_seg] fp32 scale of each segment.
  * totals      [K] int64 entries per learner (required).  The number of
  *             selected entries is only known on the GPU: when totals[k] >
- *             cap the list and residue of learner k are unspecified and the
- *             caller must retry with a larger cap.
+ *             cap, learner k sends nothing this step (its list is not
+ *             written; counts and totals hold the would-be numbers) and its
+ *             residue becomes G = R + dW, so no gradient mass is lost; a
+ *             larger cap lets the next step send.
  * workspace   at least gcsgd_adacomp_workspace_size bytes, 256-byte aligned.
  * Limit: K * (4 * n_seg + 8) <= 204800 (K <= 24 at 2048 tensors, K <= 198 at
  * 256); a larger call returns GCSGD_ERR_INVALID_ARG before anything is

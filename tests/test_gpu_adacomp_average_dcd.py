@@ -159,6 +159,35 @@ def test_capacity_overflow_sends_nothing_and_keeps_the_residue(cuda_lib):
     assert res[0][0] == "overflow"
 
 
+def test_capacity_overflow_leaves_the_list_and_reports_would_be_counts(cuda_lib):
+    """A learner over cap: its list is not written (sentinel words stay), its
+    counts add up to its would-be total, and its residue is G = R + dW; the
+    learner that fits sends as usual."""
+    import torch
+    gc = cuda_lib
+    rng = np.random.default_rng(61)
+    off = wl.layout_offsets([20000])
+    dW = rng.laplace(0, 1.0, size=(2, 20000)).astype(np.float32)
+    R0 = rng.laplace(0, 0.1, size=(2, 20000)).astype(np.float32)
+    dW[1, 100:] = 0.0  # learner 1: G = 0 past its first 100 values, so it sends at most 100
+    R0[1] = 0.0
+    a = gc.AdaComp(off, [1], 2, 5000)
+    a.out.fill_(0x7A7A7A7A)
+    R = torch.from_numpy(R0.copy()).cuda()
+    out, totals = a(torch.from_numpy(dW).cuda(), R)
+    torch.cuda.synchronize()
+    tot = totals.cpu().numpy()
+    assert tot[0] > 5000 >= tot[1]
+    assert int(a.counts[0].sum().item()) == tot[0]
+    assert bool(torch.all(out[0] == 0x7A7A7A7A).item())
+    np.testing.assert_array_equal(R[0].cpu().numpy(), R0[0] + dW[0])
+    Ro = R0.copy()
+    idx_o, val_o, counts_o, scales_o, totals_o = oracle.adacomp_step(off, [1], dW[1:], Ro[1:], cap=5000)
+    n1 = int(totals_o[0])
+    assert tot[1] == n1
+    np.testing.assert_array_equal(gc.pair_indices(out)[1, :n1].cpu().numpy(), idx_o[0, :n1].astype(np.int64))
+
+
 # ------------------------------------------------------------ sparse average
 
 def padded(idx, val, cap):
