@@ -1,7 +1,7 @@
 // wire.cu -- the messages as byte streams, and back.
 //
-// "Deep Gradient Compression", section 3.1: the encoder packs 32-bit
-// non-zero gradient values and 16-bit zero run lengths.  Reading: one 6-byte
+// "Deep Gradient Compression", section 3.1: a sent value travels as 32 bits
+// and the unsent positions before it as a 16-bit count.  Reading: one 6-byte
 // record per sent entry, little-endian [uint16 unsent positions since the
 // previous entry][fp32 value]; a gap of 65536 or more is split by escape
 // records (65535, +0.0f), each covering 65535 zeros and one explicit zero.

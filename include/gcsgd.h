@@ -318,8 +318,8 @@ int ecd_step(int32_t n_nodes, int64_t d, const float* w_ring, const float* x, fl
 
 /*
  * DGC's messages as byte streams ("Deep Gradient Compression", section 3.1:
- * the encoder packs 32-bit non-zero gradient values and 16-bit zero run
- * lengths).  Learner k's list (lists[k*cap ..], totals[k] entries, indices
+ * a sent value travels as 32 bits and the unsent positions before it as a
+ * 16-bit count).  Learner k's list (lists[k*cap ..], totals[k] entries, indices
  * strictly ascending) becomes streams[k*stream_cap ..]: one 6-byte record
  * per entry, little-endian [uint16 unsent positions since the previous
  * entry (or index 0)][fp32 value]; a gap of 65536 or more is split by escape

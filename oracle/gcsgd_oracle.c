@@ -7,8 +7,8 @@
  * may load it; the product path never calls it and shares no code with it.
  *
  * Precision.  The DGC page fixes 32-bit gradient values on the wire
- * ("Deep Gradient Compression", section 3.1: the encoder packs 32-bit
- * non-zero gradient values), and the workloads are fp32 tensors, so every
+ * ("Deep Gradient Compression", section 3.1, its description of the
+ * message encoding), and the workloads are fp32 tensors, so every
  * element-wise update here is fp32 with one IEEE round-to-nearest per
  * operation and no fused multiply-add (compile with -ffp-contract=off).
  * Reductions that feed a single scalar (the clipping norm, the AdaComp scale)
@@ -655,8 +655,8 @@ static uint32_t get_u32(const unsigned char* b) {
 
 /*
  * DGC's message as a byte stream ("Deep Gradient Compression", section 3.1:
- * the encoder packs 32-bit non-zero gradient values and 16-bit zero run
- * lengths).  Reading: one 6-byte record per sent entry, little-endian
+ * each sent value travels as 32 bits, and the unsent positions before it as
+ * a 16-bit count).  Reading: one 6-byte record per sent entry, little-endian
  * [uint16 number of unsent positions since the previous entry (or the
  * start)][fp32 value]; a gap of 65536 or more is split by escape records
  * (65535, +0.0f), each standing for 65535 zeros and one explicit zero.
