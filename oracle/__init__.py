@@ -140,7 +140,8 @@ def dgc_step(offsets, grad, u, v, density, momentum, clip_thr=0.0, clip_nodes=1,
 
 
 def dgc_step_sampled(offsets, grad, u, v, density, sample_frac, momentum, clip_thr=0.0, clip_nodes=1, cap=None):
-    """The DGC step with the sampled threshold (tensors above 16384 values).
+    """The DGC step with the sampled threshold (every tensor whose sample of
+    floor(sample_frac * n) values holds a whole 64-value block; the others exact).
 
     Same returns as ``dgc_step``; learner k's list has ``counts[k].sum()`` entries."""
     off = np.ascontiguousarray(offsets, dtype=np.int64)

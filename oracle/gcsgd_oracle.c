@@ -101,28 +101,32 @@ static int keyed_cmp(const void* a, const void* b) {
  */
 /*
  * The sampled threshold ("Deep Gradient Compression", section 5, system
- * analysis: a 0.1 % to 1 % sample of the gradients estimates the population
- * threshold; section 6: hierarchical threshold selection).  The pages give
- * the idea, not the procedure; reading, per tensor of n values with k_s to
- * send, when n > 16384 and k_s <= n / 5 (smaller tensors are selected
- * exactly, their sample would be most of the tensor):
- *   - the sample is m = floor(sample_frac * n) rounded down to a multiple of
- *     64 (at least 64, at most 16384) values of the updated |v|, taken as
- *     m / 64 blocks of 64 consecutive values starting at b * (n / (m / 64));
+ * analysis: a sample of 0.1 % to 1 % of the gradients is enough to estimate
+ * the threshold of the whole population; section 6: hierarchical threshold
+ * selection).  The pages give the idea, not the procedure.  Reading, per
+ * tensor of n values with k_s to send and the caller's sample fraction f:
+ *   - the sample is m = floor(f * n) values rounded down to whole blocks of
+ *     64 consecutive values (how the sample is drawn is not on the page:
+ *     evenly spaced blocks keep it deterministic), block b starting at
+ *     b * floor(n / (m / 64));
+ *   - a tensor whose sample holds no whole block (f * n < 64) has nothing to
+ *     estimate from and is selected exactly (the second, exact step alone);
  *   - the threshold tau is the a-th largest sampled |v| (bit pattern order),
- *     a = round(k_s * m / n) clamped to [1, m];
+ *     a = round(k_s * m / n) clamped to [1, m]: the sample's share of k_s;
  *   - every entry with |v| >= tau is selected; when that is more than k_s
  *     (the hierarchical second step) the k_s largest of them are kept, which
  *     is the exact top-k, otherwise all of them are sent (fewer than k_s).
- * Learner k's list holds its tensors' selections one after another, so its
- * length is the sum of the per-tensor counts.
+ * Nothing else limits the sample: every tensor size and every density is
+ * sampled the same way.  Learner k's list holds its tensors' selections one
+ * after another, so its length is the sum of the per-tensor counts.
  */
-#define ORACLE_SAMPLED_MIN_N 16384
 #define ORACLE_SAMPLE_BLOCK 64
-#define ORACLE_SAMPLE_MAX 16384
 
-static int dgc_sampled(int64_t n, int64_t ks, double sample_frac) {
-    return sample_frac > 0.0 && n > ORACLE_SAMPLED_MIN_N && 5 * ks <= n;
+/* Values sampled from a tensor of n values at fraction f (0: not sampled). */
+static int64_t dgc_sample_size(int64_t n, double sample_frac) {
+    if (!(sample_frac > 0.0)) return 0;
+    int64_t m = (int64_t)(sample_frac * (double)n);
+    return m - m % ORACLE_SAMPLE_BLOCK;
 }
 
 static int dgc_step_impl(int K, int S, const int64_t* seg_off,
@@ -188,12 +192,9 @@ static int dgc_step_impl(int K, int S, const int64_t* seg_off,
                 sent[i] = 0;
             }
             int64_t take = ks;
-            if (dgc_sampled(n, ks, sample_frac)) {
+            const int64_t m = dgc_sample_size(n, sample_frac);
+            if (m > 0) {
                 /* the sample and its a-th largest |v| */
-                int64_t m = (int64_t)(sample_frac * (double)n);
-                m -= m % ORACLE_SAMPLE_BLOCK;
-                if (m < ORACLE_SAMPLE_BLOCK) m = ORACLE_SAMPLE_BLOCK;
-                if (m > ORACLE_SAMPLE_MAX) m = ORACLE_SAMPLE_MAX;
                 const int64_t nblk = m / ORACLE_SAMPLE_BLOCK, stride = n / nblk;
                 keyed_t* smp = (keyed_t*)malloc(sizeof(keyed_t) * (size_t)m);
                 if (!smp) { free(order); free(sent); return ORACLE_ENOMEM; }
@@ -262,7 +263,7 @@ int oracle_dgc_step_nesterov(int K, int S, const int64_t* seg_off,
                          out_val, cap, counts, clip_scale);
 }
 
-/* The DGC step with the sampled threshold (see dgc_sampled above). */
+/* The DGC step with the sampled threshold (see dgc_sample_size above). */
 int oracle_dgc_step_sampled(int K, int S, const int64_t* seg_off,
                             const float* grad, float* u, float* v,
                             double density, double sample_frac, float momentum, float clip_thr, int clip_nodes,

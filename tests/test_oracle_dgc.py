@@ -263,13 +263,53 @@ def test_sampled_hand_example():
     assert v[0, 300] == np.float32(4.9) and u[0, 300] == np.float32(4.9)
 
 
-@pytest.mark.parametrize("frac", [0.001, 0.003, 0.01])
+def sampled_example(ex, name):
+    n = int(ex[f"{name}_n"][0])
+    G = np.full((1, n), float(ex[f"{name}_base"][0]), np.float32)
+    if f"{name}_ramp" in ex:
+        r = int(ex[f"{name}_ramp"][0])
+        G[0, :r] = np.arange(1, r + 1, dtype=np.float32)
+    G[0, [int(x) for x in ex[f"{name}_at"]]] = f32(ex[f"{name}_val"])
+    return n, G
+
+
+@pytest.mark.parametrize("name", ["A", "B", "C", "D"])
+def test_sampled_small_tensor_examples(golden, name):
+    """Hand-worked examples (tests/golden/dgc_sampled_small_examples.txt): a
+    tensor of 6400 values sampled by one block, a density of 0.5 sampled, a
+    sample of 20480 values, and a tensor whose 1 % sample is under one block
+    selected exactly."""
+    ex = golden("dgc_sampled_small_examples.txt")
+    n, G = sampled_example(ex, name)
+    u = np.zeros((1, n), np.float32)
+    v = np.zeros((1, n), np.float32)
+    idx, val, counts, _ = oracle.dgc_step_sampled([0, n], G, u, v, float(ex[f"{name}_density"][0]),
+                                                  float(ex[f"{name}_frac"][0]), 0.9)
+    want_idx = [int(x) for x in ex[f"{name}_sent_idx"]]
+    c = len(want_idx)
+    assert counts.tolist() == [[c]]
+    assert idx[0, :c].tolist() == want_idx
+    np.testing.assert_array_equal(val[0, :c], f32(ex[f"{name}_sent_val"]))
+    assert not v[0, want_idx].any() and not u[0, want_idx].any()
+    keep = np.ones(n, bool)
+    keep[want_idx] = False
+    np.testing.assert_array_equal(v[0, keep], G[0, keep])
+
+
+def sample_blocks(n, frac):
+    """Whole 64-value blocks in floor(frac * n) values (0: the tensor is exact)."""
+    m = int(frac * n)
+    return (m - m % 64) // 64
+
+
+@pytest.mark.parametrize("frac", [0.001, 0.003, 0.01, 0.2])
 def test_sampled_is_a_top_set_and_exact_when_full(frac):
     """Whatever the sample, the sent set is the top of |v| (everything sent is
     at least as large as everything kept); when it reaches k it is exactly
-    the exact step's top-k; tensors of at most 16384 values are exact."""
+    the exact step's top-k; a tensor whose sample holds no whole 64-value
+    block is exact."""
     rng = np.random.default_rng(int(frac * 1e4))
-    sizes = [16384, 50000, 200000, 33333]
+    sizes = [16384, 50000, 200000, 33333, 6400, 700]
     off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
     K, N = 2, int(off[-1])
     for step in range(3):
@@ -289,7 +329,7 @@ def test_sampled_is_a_top_set_and_exact_when_full(frac):
                 cs, ce = int(cnt_s[k, s]), int(cnt_e[k, s])
                 assert cs <= ce
                 sent = idx_s[k, ps:ps + cs].astype(np.int64)
-                if s == 0 or cs == ce:
+                if sample_blocks(sizes[s], frac) == 0 or cs == ce:
                     np.testing.assert_array_equal(sent, idx_e[k, pe:pe + ce])
                 mag = np.abs(vacc[k, off[s]:off[s + 1]])
                 mask = np.zeros(sizes[s], bool)
@@ -300,6 +340,29 @@ def test_sampled_is_a_top_set_and_exact_when_full(frac):
                 ps, pe = ps + cs, pe + ce
         G_sent = vs.copy()
         assert not any(G_sent[k, idx_s[k, :cnt_s[k].sum()]].any() for k in range(K))
+
+
+@pytest.mark.parametrize("density,frac", [(0.01, 0.01), (0.1, 0.001), (0.05, 0.01), (0.3, 0.003)])
+def test_sampled_count_near_k(density, frac):
+    """On i.i.d. normal values the sample's a-th largest sits near the
+    population's k-th largest, so the sent count is close to k, never above
+    it, and what was sent plus what stays in v is the accumulated v, bit for
+    bit.  a = round(k m / n) is at least 20 in every case here, so the
+    relative spread of the count is about 1 / sqrt(a) < 0.25."""
+    rng = np.random.default_rng(int(density * 1000 + frac * 1e5))
+    n = 1 << 20
+    G = rng.standard_normal((1, n)).astype(np.float32)
+    u = np.zeros((1, n), np.float32)
+    v = np.zeros((1, n), np.float32)
+    idx, val, counts, _ = oracle.dgc_step_sampled([0, n], G, u, v, density, frac, 0.0)
+    k = oracle.dgc_k(density, n)
+    m = sample_blocks(n, frac) * 64
+    assert round(k * m / n) >= 20
+    c = int(counts[0, 0])
+    assert 0.5 * k <= c <= k
+    recon = v[0].copy()
+    recon[idx[0, :c].astype(np.int64)] += val[0, :c]
+    np.testing.assert_array_equal(recon, G[0])
 
 
 def test_sampled_hand_example_rank_above_one():

@@ -40,6 +40,13 @@ MUTANTS = {
     # DGC with the sampled threshold
     "sampled_strict_gt": ("c += order[i].key >= tau;", "c += order[i].key > tau;"),
     "sampled_rank_floor": ("int64_t a = (ks * m + n / 2) / n;", "int64_t a = (ks * m) / n;"),
+    # the sampled threshold limited by the earlier plan's sizes, which the page does not give
+    "sampled_only_above_16384": ("if (m > 0) {", "if (m > 0 && n > 16384) {"),
+    "sampled_only_at_low_density": ("if (m > 0) {", "if (m > 0 && 5 * ks <= n) {"),
+    "sampled_capped_at_16384": ("return m - m % ORACLE_SAMPLE_BLOCK;",
+                                "m -= m % ORACLE_SAMPLE_BLOCK;\n    return m > 16384 ? 16384 : m;"),
+    "sampled_at_least_one_block": ("return m - m % ORACLE_SAMPLE_BLOCK;",
+                                   "m -= m % ORACLE_SAMPLE_BLOCK;\n    return m < ORACLE_SAMPLE_BLOCK ? ORACLE_SAMPLE_BLOCK : m;"),
     "sampled_stride": ("const int64_t nblk = m / ORACLE_SAMPLE_BLOCK, stride = n / nblk;",
                        "const int64_t nblk = m / ORACLE_SAMPLE_BLOCK, stride = n / (nblk + 1);"),
     # AdaComp
