@@ -60,9 +60,11 @@ constexpr int kSumsqBlocks = 512;        // CTAs per learner in dgc_sumsq
 
 // Plan of one segment.  sample_frac = 0: the exact step (the hint only
 // steers the candidate pool).  sample_frac > 0: the sampled threshold (the
-// system-analysis reading: m = floor(sample_frac n) rounded down to 64-value
-// blocks, at most kSampleMax, and the hint is the round(k m / n)-th largest
-// sampled |v|, which is then the selection threshold itself).
+// system-analysis reading: m = floor(sample_frac n) rounded down to whole
+// 64-value blocks; a tensor with no whole block is selected exactly; tau is
+// the round(k m / n)-th largest sampled |v| and is the selection threshold
+// itself).  Sampled tensors of at most kRawMax values take tau from the
+// staged v' in dgc_select; larger ones get it from dgc_prepare as the hint.
 __host__ __device__ __forceinline__ void seg_fields(uint32_t n, double density, double sample_frac, SegPlan* p) {
     p->n = n;
     p->k = dgc_k_of(density, n);
@@ -71,23 +73,28 @@ __host__ __device__ __forceinline__ void seg_fields(uint32_t n, double density, 
     p->m = 0;
     p->a = 0;
     p->sampled = 0;
+    uint64_t ms = 0;  // sampled threshold: whole blocks in floor(sample_frac n) values
+    if (sample_frac > 0.0) {
+        ms = (uint64_t)(sample_frac * (double)n);
+        ms -= ms % kSampleBlock;
+    }
     if (n == 0) {
         p->kind = kKindEmpty;
+    } else if (ms > 0) {
+        p->sampled = 1;
+        p->m = (uint32_t)ms;
+        const uint64_t a = ((uint64_t)p->k * ms + n / 2) / n;
+        p->a = (uint32_t)(a < 1 ? 1 : (a > ms ? ms : a));
+        if (n <= kRawMax) {
+            p->kind = kKindRaw;
+        } else {
+            p->kind = kKindPool;
+            const uint64_t R = p->k > kPoolFloor ? p->k : kPoolFloor;  // expected candidates ~ k
+            const uint64_t cap = 4 * R + 256;
+            p->cap = (uint32_t)(cap < n ? cap : n);
+        }
     } else if (n <= kRawMax || 5ull * p->k > n) {
         p->kind = kKindRaw;
-    } else if (sample_frac > 0.0) {
-        p->kind = kKindPool;
-        p->sampled = 1;
-        const uint64_t R = p->k > kPoolFloor ? p->k : kPoolFloor;  // expected candidates ~ k
-        const uint64_t cap = 4 * R + 256;
-        p->cap = (uint32_t)(cap < n ? cap : n);
-        uint64_t m = (uint64_t)(sample_frac * (double)n);
-        m -= m % kSampleBlock;
-        if (m < kSampleBlock) m = kSampleBlock;
-        if (m > kSampleMax) m = kSampleMax;
-        p->m = (uint32_t)m;
-        uint64_t a = ((uint64_t)p->k * m + n / 2) / n;
-        p->a = (uint32_t)(a < 1 ? 1 : (a > m ? m : a));
     } else {
         p->kind = kKindPool;
         const uint64_t R = 5ull * p->k / 2 > kPoolFloor ? 5ull * p->k / 2 : kPoolFloor;  // expected candidates
@@ -103,12 +110,19 @@ __host__ __device__ __forceinline__ void seg_fields(uint32_t n, double density, 
     }
 }
 
+// Sample keys of a pool segment that do not fit dgc_prepare's shared memory
+// go to the workspace (sampled threshold only).
+__host__ __device__ __forceinline__ bool sample_spills(const SegPlan& p) {
+    return p.kind == kKindPool && p.sampled && p.m > kSampleMax;
+}
+
 // Host mirror of the plan's totals (workspace sizing and argument checks).
 int host_plan(const int64_t* off, int S, double density, double sample_frac, HostPlan* hp) {
     hp->tiles_per_learner = 0;
     hp->pool_per_learner = 0;
     hp->out_per_learner = 0;
     hp->pool_segments = 0;
+    hp->skeys_per_learner = 0;
     for (int s = 0; s < S; ++s) {
         SegPlan p;
         seg_fields((uint32_t)(off[s + 1] - off[s]), density, sample_frac, &p);
@@ -116,6 +130,7 @@ int host_plan(const int64_t* off, int S, double density, double sample_frac, Hos
         hp->pool_per_learner += p.cap;
         hp->out_per_learner += p.k;
         hp->pool_segments += p.kind == kKindPool;
+        if (sample_spills(p)) hp->skeys_per_learner += p.m;
     }
     return 0;
 }
@@ -249,7 +264,8 @@ __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, PoolL
                                                      uint16_t* __restrict__ order, uint64_t N,
                                                      const float* __restrict__ grad, const float* __restrict__ u,
                                                      const float* __restrict__ v, float momentum,
-                                                     uint32_t* __restrict__ hint, uint32_t* __restrict__ pool_cnt) {
+                                                     uint32_t* __restrict__ hint, uint32_t* __restrict__ pool_cnt,
+                                                     uint32_t* __restrict__ skeys, uint64_t skeys_per_learner) {
     extern __shared__ __align__(16) uint32_t keys[];  // kSampleMax
     __shared__ RadixSmem rs;
     __shared__ uint64_t carry[3];
@@ -314,13 +330,14 @@ __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, PoolL
         }
         __syncthreads();
         SegPlan p;
+        seg_fields(so.off[s + 1] - so.off[s], density, sample_frac, &p);
         p.off = so.off[s];
-        p.n = so.off[s + 1] - so.off[s];
-        p.m = pl.m[q];
-        p.a = pl.a[q];
         const float c = s_c;
         const uint32_t nblk = p.m / kSampleBlock;
-        const uint32_t stride = p.n / nblk;  // >= 64 * 512 / 48 (m <= 48 n / 512): blocks never overlap
+        const uint32_t stride = p.n / nblk;  // >= 64 since m <= n: blocks never overlap
+        // keys of a sample larger than the shared array go to the learner's spill region
+        const bool spill = sample_spills(p);
+        uint32_t* kdst = spill ? skeys + (uint64_t)k * skeys_per_learner + pl.koff[q] : keys;
         const uint64_t base = (uint64_t)k * N + p.off;
         const float* gs = grad + base;
         const float* us = u + base;
@@ -354,14 +371,22 @@ __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, PoolL
                     for (int h = 0; h < kH; ++h) {
                         dgc_elem<NEST>(gg[j][h], uu[j][h], vv[j][h], momentum, c);
                         const uint32_t key = mag_key(vv[j][h]);
-                        keys[b * kSampleBlock + 32 * h + lane] = key;
+                        kdst[b * kSampleBlock + 32 * h + lane] = key;
                         radix_hist_add(rs, key);
                     }
                 }
             }
         }
         __syncthreads();
-        if (sample_frac > 0.0) {
+        if (spill) {
+            // the sampled threshold over spilled keys (written by this CTA before
+            // the barrier above; plain loads, not the read-only path): the shared
+            // array is free and takes the first digit's bucket
+            const SelectResult sr = radix_select_desc<NTP, 3, true>(
+                [&](uint64_t i, uint32_t* key) { *key = kdst[i]; return true; }, p.m, p.a, rs, true, keys,
+                kSampleMax);
+            if (threadIdx.x == 0) hint[unit] = sr.thresh;
+        } else if (p.sampled) {
             // the sampled threshold: the a-th largest sampled key, exactly
             const SelectResult sr = radix_select_desc<NTP, 3>(
                 [&](uint64_t i, uint32_t* key) { *key = keys[i]; return true; }, p.m, p.a, rs, true);
@@ -696,8 +721,9 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
     const uint32_t pc = p.kind == kKindPool ? pool_cnt[unit] : 0;
     // sampled threshold, fewer than k above it: every candidate is sent
     const bool take_all = p.kind == kKindPool && p.sampled && pc < p.k;
+    const bool raw_sampled = p.kind == kKindRaw && p.sampled;  // counted once tau is known
     if (threadIdx.x == 0) {
-        counts[unit] = take_all ? pc : p.k;
+        if (!raw_sampled) counts[unit] = take_all ? pc : p.k;
         if (s == 0 && totals && !sampled) totals[k] = out_per_learner;
     }
     if (p.k == 0) return;
@@ -776,9 +802,44 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
             pc, T, ties, p, dst, u, v, ebase, wsum);
         return;
     }
-    if (!pool_ok && p.n <= kSmallN && p.k <= kSmallK) {
+    if (!pool_ok && p.n <= kSmallN && p.k <= kSmallK && !raw_sampled) {
         small_topk(p, vseg, u, v, ebase, dst, reinterpret_cast<uint64_t*>(stage_raw),
                    reinterpret_cast<uint64_t*>(stage_raw) + (NTS / 32) * kSmallK);
+        return;
+    }
+    if (raw_sampled) {
+        // the sampled threshold on a segment of at most kRawMax values: v' is
+        // staged, tau = the a-th largest |v'| of the sample blocks (block b at
+        // b * stride), and either every |v'| >= tau is sent (fewer than k) or,
+        // the hierarchical second step, the exact top k
+        for (uint32_t i = threadIdx.x; i < p.n; i += NTS) stagef[i] = vseg[i];
+        __syncthreads();
+        const uint32_t stride = p.n / (p.m / kSampleBlock);
+        const SelectResult st = radix_select_desc<NTS, 3>(
+            [&](uint64_t i, uint32_t* key) {
+                *key = mag_key(stagef[(uint32_t)i / kSampleBlock * stride + ((uint32_t)i & (kSampleBlock - 1))]);
+                return true;
+            },
+            p.m, p.a, rs, false);
+        const uint32_t tau = st.thresh;
+        uint32_t above = 0;
+        for (uint32_t i = threadIdx.x; i < p.n; i += NTS) above += mag_key(stagef[i]) >= tau;
+        uint64_t tot;
+        block_exclusive_scan<NTS>(above, rs.scan, &tot);
+        uint32_t T = tau, ties = p.n;  // fewer than k at or above tau: all of them
+        if (tot >= p.k) {
+            const SelectResult r = radix_select_desc<NTS, 3>(
+                [&](uint64_t i, uint32_t* key) { *key = mag_key(stagef[i]); return true; }, p.n, p.k, rs, false);
+            T = r.thresh;
+            ties = r.ties;
+        }
+        if (threadIdx.x == 0) counts[unit] = tot >= p.k ? (int64_t)p.k : (int64_t)tot;
+        emit_in_order(
+            [&](uint32_t i, uint32_t* loc, uint32_t* bits) {
+                *loc = i;
+                *bits = __float_as_uint(stagef[i]);
+            },
+            p.n, T, ties, p, dst, u, v, ebase, wsum);
         return;
     }
     if (!pool_ok && p.n <= kRawMax) {
@@ -1028,14 +1089,15 @@ int dgc_launch(const int64_t* off, int S, int K, const float* grad, float* u, fl
         const size_t smem = kSampleMax * sizeof(uint32_t);
         auto fill = [&](auto& so, auto& pl) {
             pl.n_pool = 0;
+            uint32_t koff = 0;
             for (int s = 0; s <= S; ++s) so.off[s] = (uint32_t)off[s];
             for (int s = 0; s < S; ++s) {
                 SegPlan sp;
                 seg_fields((uint32_t)(off[s + 1] - off[s]), density, sample_frac, &sp);
                 if (sp.kind != kKindPool) continue;
                 pl.seg[pl.n_pool] = (uint16_t)s;
-                pl.m[pl.n_pool] = sp.m;
-                pl.a[pl.n_pool] = sp.a;
+                pl.koff[pl.n_pool] = koff;
+                if (sample_spills(sp)) koff += sp.m;
                 ++pl.n_pool;
             }
         };
@@ -1048,7 +1110,7 @@ int dgc_launch(const int64_t* off, int S, int K, const float* grad, float* u, fl
             fill(so, pl);
             (nesterov ? dgc_prepare<256, true> : dgc_prepare<256, false>)<<<prep_grid, NTP, smem, stream>>>(
                 so, pl, S, K, density, sample_frac, clip_thr, clip_nodes, w.clip_part, w.plan, w.clip_c, w.order, N,
-                grad, u, v, momentum, w.hint, w.pool_cnt);
+                grad, u, v, momentum, w.hint, w.pool_cnt, w.skeys, hp.skeys_per_learner);
         } else {
             SegOffsets<GCSGD_MAX_SEGMENTS> so;
             PoolList<GCSGD_MAX_SEGMENTS> pl;
@@ -1056,7 +1118,7 @@ int dgc_launch(const int64_t* off, int S, int K, const float* grad, float* u, fl
             (nesterov ? dgc_prepare<GCSGD_MAX_SEGMENTS, true> : dgc_prepare<GCSGD_MAX_SEGMENTS, false>)
                 <<<prep_grid, NTP, smem, stream>>>(so, pl, S, K, density, sample_frac, clip_thr, clip_nodes,
                                                    w.clip_part, w.plan, w.clip_c, w.order, N, grad, u, v, momentum,
-                                                   w.hint, w.pool_cnt);
+                                                   w.hint, w.pool_cnt, w.skeys, hp.skeys_per_learner);
         }
         if ((rc = check_launch("dgc_prepare"))) return rc;
     }
@@ -1135,6 +1197,7 @@ size_t dgc_workspace_layout(int S, int K, const dgc::HostPlan& hp, bool sampled,
     const size_t o_tt = take(sizeof(uint2) * (size_t)K * hp.tiles_per_learner);
     const size_t o_pool = take(sizeof(uint2) * (size_t)K * hp.pool_per_learner);
     const size_t o_msg = take(sampled ? sizeof(gcsgd_pair) * (size_t)K * hp.out_per_learner : 0);
+    const size_t o_skeys = take(sampled ? sizeof(uint32_t) * (size_t)K * hp.skeys_per_learner : 0);
     if (w) {
         char* b = (char*)base;
         w->plan = (SegPlan*)(b + o_plan);
@@ -1146,6 +1209,7 @@ size_t dgc_workspace_layout(int S, int K, const dgc::HostPlan& hp, bool sampled,
         w->tile_tab = (uint2*)(b + o_tt);
         w->pool = (uint2*)(b + o_pool);
         w->msg = sampled ? (gcsgd_pair*)(b + o_msg) : nullptr;
+        w->skeys = sampled ? (uint32_t*)(b + o_skeys) : nullptr;
     }
     return o;
 }

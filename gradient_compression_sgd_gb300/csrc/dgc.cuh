@@ -18,8 +18,8 @@ struct SegPlan {
     uint32_t k;         // entries sent
     uint32_t kind;      // kKindEmpty / kKindRaw (select from v') / kKindPool (candidates)
     uint32_t cap;       // candidate pool capacity
-    uint32_t m;         // hint sample size (multiple of 32)
-    uint32_t a;         // rank of the hint within the sample
+    uint32_t m;         // sample size (whole 64-value blocks)
+    uint32_t a;         // rank of the hint (or of tau, sampled) within the sample
     uint32_t pool_off;  // first pool slot within a learner's pool
     uint32_t tile_off;  // first tile within a learner's tiles
     uint32_t ntiles;    // tiles of 4096 elements
@@ -33,14 +33,13 @@ struct SegOffsets {
     uint32_t off[MAXS + 1];
 };
 
-// Segments with a candidate pool and their sample sizes, from the host plan
-// (passed by value so the sampling CTAs need no fp64 or 64-bit division).
+// Segments with a candidate pool, from the host plan (passed by value; the
+// sampling CTAs recompute each segment's sample size and rank).
 template <int MAXS>
 struct PoolList {
     uint32_t n_pool;
     uint16_t seg[MAXS];
-    uint32_t m[MAXS];  // sample size (multiple of 32)
-    uint32_t a[MAXS];  // rank of the hint within the sample
+    uint32_t koff[MAXS];  // sampled threshold, samples above kSampleMax: first key in the learner's spill region
 };
 
 struct HostPlan {
@@ -48,6 +47,7 @@ struct HostPlan {
     uint64_t pool_per_learner;
     uint64_t out_per_learner;
     uint64_t pool_segments;
+    uint64_t skeys_per_learner;  // sampled threshold: spilled sample keys per learner
 };
 
 struct DgcWorkspace {
@@ -60,6 +60,7 @@ struct DgcWorkspace {
     uint2* tile_tab;
     uint2* pool;
     gcsgd_pair* msg;  // sampled threshold: per-tensor regions before packing
+    uint32_t* skeys;  // sampled threshold: sample keys of pool segments above kSampleMax
 };
 
 int host_plan(const int64_t* off, int S, double density, double sample_frac, HostPlan* hp);

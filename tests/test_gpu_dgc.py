@@ -255,10 +255,34 @@ def run_dgc_sampled(gc, offsets, grads, density, frac, momentum, offset=0):
 
 @pytest.mark.parametrize("frac", [0.001, 0.003, 0.01, 0.2])
 def test_sampled_threshold(cuda_lib, frac):
+    """Tensors of every kind: small ones sampled from the select kernel's
+    stage (6400 .. 16384 values), pool tensors, samples above 16384 keys
+    (700000 and 2.4M values at 0.2 and 0.01), ones under one block."""
     rng = np.random.default_rng(int(frac * 1000) + 7)
-    off = wl.layout_offsets([16384, 50000, 200000, 33333, 0, 700000])
+    off = wl.layout_offsets([16384, 50000, 200000, 33333, 0, 700000, 6400, 9000, 700, 2359296])
     grads = [(rng.standard_normal((2, off[-1])) * 1e-3).astype(np.float32) for _ in range(3)]
     run_dgc_sampled(cuda_lib, off, grads, 0.002, frac, 0.9)
+
+
+@pytest.mark.parametrize("density", [0.05, 0.3, 0.9])
+def test_sampled_threshold_high_density(cuda_lib, density):
+    """Densities with 5 k > n: every tensor with a whole sample block is
+    sampled, small (staged) and large (pool) alike."""
+    rng = np.random.default_rng(int(density * 100) + 3)
+    off = wl.layout_offsets([640, 6400, 16384, 40000, 300000])
+    grads = [(rng.standard_normal((2, off[-1])) * 1e-2).astype(np.float32) for _ in range(3)]
+    run_dgc_sampled(cuda_lib, off, grads, density, 0.1, 0.9)
+
+
+def test_sampled_small_tensor_examples_on_the_gpu(cuda_lib):
+    """The hand-worked examples of tests/golden/dgc_sampled_small_examples.txt."""
+    from conftest import load_golden
+    from test_oracle_dgc import sampled_example
+
+    ex = load_golden("dgc_sampled_small_examples.txt")
+    for name in "ABCD":
+        n, G = sampled_example(ex, name)
+        run_dgc_sampled(cuda_lib, [0, n], [G], float(ex[f"{name}_density"][0]), float(ex[f"{name}_frac"][0]), 0.9)
 
 
 def test_sampled_threshold_resnet50_small_layout(cuda_lib):
