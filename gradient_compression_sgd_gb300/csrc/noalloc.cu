@@ -12,7 +12,16 @@
 //
 // The array's name is only a host-side stand-in for the device array, so the
 // host looks up its device address once per device (with that device
-// current) and passes that address to the kernels.  Every call shares the
+// current) and passes that address to the kernels.  With CUDA's lazy module
+// loading (the default) the array is not placed on a device when the library
+// loads but when that lookup first runs there: the first call on each device
+// is where the driver commits the GCSGD_NOALLOC_SCRATCH_BYTES, and it fails
+// with GCSGD_ERR_CUDA ("cannot place ...") if the device has no room left.
+// Callers make one warm-up call per device before their own allocator
+// reserves the device's memory and before any stream capture.  The cached
+// address belongs to the device's primary context: after cudaDeviceReset, or
+// from another driver context on the same device, it is stale and the entry
+// point must not be called.  Every call shares the
 // one array; the DGC kernels rewrite everything they read from it (the plan
 // and the candidate counters are set at the start of each call), so nothing
 // has to be cleared between calls, but calls whose work overlaps on the GPU
@@ -44,6 +53,13 @@ int noalloc_scratch(void** out) {
     if (!g_noalloc_ptr[dev]) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e == cudaErrorMemoryAllocation) {
+            (void)cudaGetLastError();  // not sticky: clear it for the caller
+            return set_error(GCSGD_ERR_CUDA,
+                             "dgc_compress_noalloc: cannot place the library's %zu-byte scratch array on device %d "
+                             "(out of memory); make the first call on a device before reserving its memory",
+                             (size_t)GCSGD_NOALLOC_SCRATCH_BYTES, dev);
+        }
         if (e != cudaSuccess || !p)
             return set_error(GCSGD_ERR_CUDA, "dgc_compress_noalloc: cudaGetSymbolAddress failed: %s",
                              cudaGetErrorString(e));

@@ -123,11 +123,12 @@ int dgc_compress_nesterov(const int64_t* seg_offsets, int32_t n_seg, int32_t K,
  * The DGC step with the sampled threshold ("Deep Gradient Compression",
  * section 5: a 0.1 % to 1 % sample of the gradients estimates the population
  * threshold; section 6: hierarchical threshold selection).  Steps 1, 2 and 4
- * as dgc_compress; step 3, for every tensor of n > 16384 values with
- * 5 k_s <= n (smaller ones are selected exactly):
- *   m   = floor(sample_frac * n) rounded down to a multiple of 64, clamped to
- *         [64, 16384]; the sample is m / 64 blocks of 64 consecutive updated
- *         |v| starting at b * floor(n / (m / 64));
+ * as dgc_compress; step 3, per tensor of n values:
+ *   m   = floor(sample_frac * n) rounded down to a multiple of 64; the
+ *         sample is m / 64 blocks of 64 consecutive updated |v| starting at
+ *         b * floor(n / (m / 64)).  A tensor with m = 0 (fewer than 64
+ *         values in its sample) is selected exactly, as dgc_compress does;
+ *         no other size or density is exempt and the sample is not capped;
  *   tau = the a-th largest sampled |v| (bit-pattern order),
  *         a = round(k_s * m / n) clamped to [1, m];
  *   every entry with |v| >= tau is selected; past k_s the k_s largest of
@@ -174,13 +175,19 @@ int gcsgd_dgc_stats(const int64_t* seg_offsets, int32_t n_seg, int32_t K, double
  * same DGC step, with the same arguments and results as dgc_compress.
  *
  * Its scratch is a fixed array of GCSGD_NOALLOC_SCRATCH_BYTES built into the
- * library; every GPU that loads the library holds it until the process
+ * library, held on a device from the first call there until the process
  * exits.  A layout and K that need more scratch than that
  * (gcsgd_dgc_workspace_size) are rejected with GCSGD_ERR_WORKSPACE before any
  * GPU work.  The first call on a device looks up the array's device address
- * (once per device, with that device current); make that first call before
- * any stream capture.  The call allocates nothing (no cudaMalloc, no
- * cudaFree).  All calls share the one array and leave their contents in it;
+ * (once per device, with that device current).  Under CUDA's default lazy
+ * module loading that first lookup is also when the driver places the array
+ * on the device, committing its bytes: if the device is already full it fails
+ * with GCSGD_ERR_CUDA and a message saying so.  Make one warm-up call per
+ * device before the caller's allocator reserves the device's memory, and
+ * before any stream capture.  Later calls allocate nothing (no cudaMalloc, no
+ * cudaFree, no driver allocation).  The address is looked up in the device's
+ * primary context: do not call this after cudaDeviceReset or from another
+ * driver context on the same device.  All calls share the one array and leave their contents in it;
  * nothing in it needs clearing between calls, but calls that overlap on the
  * GPU (unordered streams, several host threads) race on it and must not be
  * made.
