@@ -13,9 +13,13 @@ afterwards and reported beside them.
 
 One JSON line on rank 0: whole-job gradient GB/s (value), the same metric end
 to end with host buffers (e2e), the roofline of the dominant kernel, the CPU
-oracle's figure on a bounded sample (cpu_baseline), clocks and launches.
-``--impl reference`` times the CPU oracle itself (the only other
-implementation of this path) on the same workload.
+oracle's figure on a bounded sample pinned to one host core (cpu_baseline),
+clocks and launches; then, under ``other_workloads``, the other four
+workloads (one 1M tensor with clipping, LSTM+VGG AdaComp K=8, the GRU layout
+DGC K=8, the DCD ring of 8 nodes), each timed the same way over a shorter
+run with its dominant kernel's roofline.  ``--impl reference`` times the CPU
+oracle itself (the only other implementation of this path) on the same
+workload.
 
 Multi-GPU (torchrun): every rank runs its own K learners (independent
 problems, no collective in the data path); value = all ranks' gradient bytes
@@ -61,6 +65,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement (ncu captures)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="time only the chosen workload (skip the other four; for ncu captures)")
     return ap.parse_args()
 
 
@@ -171,29 +177,45 @@ class ClockSampler:
 
 # --------------------------------------------------------- CPU oracle sample
 
-def oracle_inputs(w):
+# Values of learner 0 one oracle step may cover.  The CPU-baseline leg takes
+# the whole ResNet-50 layout (25,557,032 values: one learner's full step,
+# ~4 s on one core); the reference arm, which runs --warmup + --steps such
+# steps, takes every 2nd tensor so that the default run ends in about two
+# minutes.  Larger layouts take every j-th tensor within the budget.
+BASELINE_STEP_VALUES = 26_000_000
+REFERENCE_STEP_VALUES = 13_000_000
+DCD_WINDOW = 1 << 22  # columns of every ring node per oracle DCD iteration
+
+
+def oracle_inputs(w, max_values: int):
     """Learner 0's (or, for DCD, every node's) seeded step-0 input on the host,
-    cut to the bounded sample the oracle is timed on."""
+    cut to the bounded sample the oracle is timed on: every j-th tensor of the
+    layout, j the smallest stride that keeps the sample within max_values
+    (then trailing picks dropped while it is still larger)."""
     from gradient_compression_sgd_gb300 import workloads as wl
     if w.method == "dcd":
-        win = min(w.n, 1 << 20)
+        win = min(w.n, DCD_WINDOW)
         g = np.stack([wl.gradient(w, k, 0)[:win].numpy() for k in range(w.learners)])
         x = np.ascontiguousarray(wl.dcd_initial_model(w)[:, :win].numpy())
         return {"g": g, "x": x, "win": win}
     grad = wl.gradient(w, 0, 0).numpy()
-    sizes = np.asarray(w.sizes)
-    pick = np.arange(0, len(sizes), 4)
+    sizes = np.asarray(w.sizes, np.int64)
+    j = max(1, -(-int(sizes.sum()) // max_values))
+    pick = list(range(0, len(sizes), j))
+    while len(pick) > 1 and int(sizes[pick].sum()) > max_values:
+        pick.pop()
+    pick = np.asarray(pick)
     off = w.offsets
     g = np.concatenate([grad[off[s]:off[s + 1]] for s in pick])[None, :]
     sub = np.concatenate([[0], np.cumsum(sizes[pick])]).astype(np.int64)
     lt = [w.lt[s] for s in pick] if w.method == "adacomp" else None
-    return {"g": g, "sub": sub, "pick": pick, "lt": lt}
+    return {"g": g, "sub": sub, "pick": pick, "lt": lt, "stride": j}
 
 
 def oracle_sample(w, inputs, target_s: float, min_steps: int = 1):
-    """Time the oracle on a bounded sample of the workload: the DGC or AdaComp
-    step + sparse average of learner 0 on every 4th tensor of the layout, or
-    one DCD ring iteration of all nodes on the first 2^20 columns.
+    """Time the oracle on a bounded sample of the workload: learner 0's DGC or
+    AdaComp step + sparse average over the tensors oracle_inputs picked, or
+    one DCD ring iteration of all nodes on the first DCD_WINDOW columns.
 
     Returns (gradient bytes processed, seconds, description)."""
     import oracle
@@ -207,7 +229,7 @@ def oracle_sample(w, inputs, target_s: float, min_steps: int = 1):
             oracle.dcd_step_window(x, g, w.ring_w, w.gamma, w.keep_p, seed, t, 0)
         n = g.size
         what = (f"oracle DCD ring iteration of all {w.learners} nodes on columns [0, {inputs['win']}) "
-                f"({n} values)")
+                f"({n} values; the kernel's work per column is the same everywhere)")
     else:
         sub = inputs["sub"]
         n = int(sub[-1])
@@ -222,8 +244,10 @@ def oracle_sample(w, inputs, target_s: float, min_steps: int = 1):
             def one(t):
                 idx, val, counts, _, _ = oracle.adacomp_step(sub, inputs["lt"], g, state)
                 oracle.sparse_average(idx, val, counts.sum(axis=1), n)
-        what = (f"oracle {w.method.upper()} step + sparse average of learner 0 on every 4th tensor of the "
-                f"layout ({len(inputs['pick'])} tensors, {n} values)")
+        span = (f"all {len(w.sizes)} tensors" if len(inputs["pick"]) == len(w.sizes) else
+                f"{len(inputs['pick'])} of its {len(w.sizes)} tensors (every {inputs['stride']}"
+                f"{'nd' if inputs['stride'] == 2 else 'th'} from the first)")
+        what = f"oracle {w.method.upper()} step + sparse average of learner 0, {span}, {n} values"
     t0 = time.perf_counter()
     steps = 0
     while steps < min_steps or time.perf_counter() - t0 < target_s:
@@ -231,6 +255,25 @@ def oracle_sample(w, inputs, target_s: float, min_steps: int = 1):
         steps += 1
     dt = time.perf_counter() - t0
     return 4.0 * n * steps, dt, f"{what}, {steps} step(s), single thread"
+
+
+class one_core:
+    """Pins this process to one host core for the oracle's timing (the
+    sched_setaffinity call taskset makes) and restores the previous set."""
+
+    def __enter__(self):
+        self.prev = os.sched_getaffinity(0)
+        self.core = max(self.prev)
+        os.sched_setaffinity(0, {self.core})
+        return self
+
+    def __exit__(self, *exc):
+        os.sched_setaffinity(0, self.prev)
+        return False
+
+    def describe(self) -> dict:
+        return {"cores": 1, "core": self.core, "box_cores": os.cpu_count(), "nproc": len(self.prev),
+                "pinned": f"sched_setaffinity to core {self.core} (as taskset -c {self.core})"}
 
 
 # ------------------------------------------------------------ reference arm
@@ -242,15 +285,16 @@ def run_reference(args):
     import torch  # noqa: F401  (seeded generator)
     from gradient_compression_sgd_gb300 import workloads as wl
     w = wl.workload(args.config)
-    inputs = oracle_inputs(w)
-    for _ in range(args.warmup):
-        oracle_sample(w, inputs, 0.0)
+    inputs = oracle_inputs(w, REFERENCE_STEP_VALUES)
     times, nbytes = [], 0.0
     desc = ""
-    for _ in range(args.steps):
-        b, dt, desc = oracle_sample(w, inputs, 0.0)
-        times.append(dt)
-        nbytes = b
+    with one_core() as pin:
+        for _ in range(args.warmup):
+            oracle_sample(w, inputs, 0.0)
+        for _ in range(args.steps):
+            b, dt, desc = oracle_sample(w, inputs, 0.0)
+            times.append(dt)
+            nbytes = b
     total = sum(times)
     value = nbytes * len(times) / total / 1e9
     line = {
@@ -258,8 +302,8 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded N(0, sigma^2) per tensor, sigma log-uniform in [1e-5, 1e-2])",
-        "config": config_dict(w, sample=desc),
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
+        "config": config_dict(w),
+        "cpu_baseline": {"value": value, "unit": "GB/s", **pin.describe(), "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -413,6 +457,101 @@ class DcdPath:
         return {}
 
 
+def timed_ms(step_fn, steps, stream, world, flush_buf=None) -> float:
+    """Times `steps` calls of step_fn(i) with a barrier and a synchronize on
+    both sides; returns this rank's ms per step.  With flush_buf (a workload
+    whose gradient set L2 could hold), L2 is flushed before each step outside
+    the events and each step is timed alone."""
+    import torch
+    import torch.distributed as dist
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    if flush_buf is not None:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(steps):
+            flush_buf.fill_(i)  # evicts the step's inputs from L2 ...
+            flush_buf.sum()  # ... and reading it back writes its dirty lines out before the events
+            ev[i][0].record(stream)
+            step_fn(i)
+            ev[i][1].record(stream)
+    else:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            step_fn(i)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    if flush_buf is not None:
+        return sum(x.elapsed_time(y) for x, y in ev) / steps
+    return e0.elapsed_time(e1) / steps
+
+
+def step_bytes_of(path, w, K, N) -> float:
+    """Algorithmic HBM bytes of one step: the dominant pass, 16 B per sent
+    entry (written by the compressor, read by the average) and the dense
+    average's 4 B per output."""
+    return path.bytes_per_elem * K * N + 16.0 * path.sent() + (4.0 * N if w.method != "dcd" else 0.0)
+
+
+OTHER_STEPS = 20  # timed steps of each workload besides the headline one
+
+
+def measure_other(gc, config, args, world, local, dev, stream) -> dict:
+    """One more workload's compress (+ average) step, timed like the headline
+    (warm-up, barrier + synchronize around the timed steps, L2 flushed between
+    steps when a gradient set fits L2, max over ranks, clocks sampled) with
+    events around its dominant kernel."""
+    import torch
+
+    from gradient_compression_sgd_gb300 import workloads as wl
+    w = wl.workload(config)
+    K, N = w.learners, w.n
+    grads = [wl.gradients(w, t, device=dev) for t in range(N_SETS)]
+    path = PATHS[w.method](gc, w, dev)
+    warm = max(3, min(args.warmup, 5))
+    for i in range(warm):
+        path.step(grads[i % N_SETS], t=i)
+    flush_buf = (torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+                 if 4 * K * N < 2 * L2_BYTES else None)
+    steps = max(3, min(args.steps, OTHER_STEPS))
+    clocks = ClockSampler(local)
+    gc.trace_only(path.dominant)
+    gc.trace_enable(True)
+    with nvtx_range(f"timed steps, {w.name}"):
+        ms_local = timed_ms(lambda i: path.step(grads[i % N_SETS], t=warm + i), steps, stream, world, flush_buf)
+    gc.trace_enable(False)
+    gc.trace_only(None)
+    trace = gc.trace_read()
+    clk = clocks.stop()
+    ms = max_over_ranks(ms_local, dev)
+    hbm, peak_kind = peaks()
+    n_dom, t_dom = trace.get(path.dominant, (0, 0.0))
+    dom_ms = t_dom / max(n_dom, 1)
+    dom_bytes = float(path.bytes_per_elem) * K * N
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9 if dom_ms > 0 else None
+    traffic = profiled_traffic(path.dominant, w.name)
+    out = {"config": config_dict(w), "steps": steps, "warmup": warm, "ms_per_step": ms,
+           "value": job_gbs(world, 4.0 * K * N, ms), "unit": "GB/s",
+           "elements_per_s": world * K * N / (ms * 1e-3),
+           "step_roofline_frac": step_bytes_of(path, w, K, N) / (ms * 1e-3) / 1e9 / hbm,
+           "dominant": {"kernel": path.dominant, "ms_per_launch": dom_ms, "achieved": achieved, "peak": hbm,
+                        "peak_kind": f"{peak_kind} (copy)", "unit": "GB/s",
+                        "frac": (achieved / hbm) if achieved else None,
+                        "algorithmic_bytes_per_launch": dom_bytes, "traffic": traffic,
+                        "traffic_over_algorithmic": (traffic / dom_bytes) if traffic else None},
+           "clocks": clk}
+    del path, grads, flush_buf
+    torch.cuda.empty_cache()
+    return out
+
+
+PATHS = {"dgc": DgcPath, "adacomp": AdaCompPath, "dcd": DcdPath}
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -438,7 +577,7 @@ def run_gpu(args):
     K, N = w.learners, w.n
     dev = torch.device("cuda", local)
     grads = [wl.gradients(w, t, device=dev) for t in range(N_SETS)]
-    path = {"dgc": DgcPath, "adacomp": AdaCompPath, "dcd": DcdPath}[w.method](gc, w, dev)
+    path = PATHS[w.method](gc, w, dev)
     stream = torch.cuda.current_stream()
 
     for i in range(args.warmup):
@@ -450,34 +589,9 @@ def run_gpu(args):
     # a gradient set that L2 could hold is not "larger than L2": flush between steps instead
     flush_l2 = 4 * K * N < 2 * L2_BYTES
     flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev) if flush_l2 else None
+
     def run_timed(step_fn):
-        """Times args.steps calls of step_fn(i), with a barrier and a synchronize on both sides; returns
-        this rank's ms per step (L2 flushed before each step, outside the events, when flush_l2)."""
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        if flush_l2:
-            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(args.steps)]
-            for i in range(args.steps):
-                flush_buf.fill_(i)  # evicts the step's inputs from L2 ...
-                flush_buf.sum()  # ... and reading it back writes its dirty lines out before the events
-                ev[i][0].record(stream)
-                step_fn(i)
-                ev[i][1].record(stream)
-        else:
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for i in range(args.steps):
-                step_fn(i)
-            e1.record(stream)
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        if flush_l2:
-            return sum(x.elapsed_time(y) for x, y in ev) / args.steps
-        return e0.elapsed_time(e1) / args.steps
+        return timed_ms(step_fn, args.steps, stream, world, flush_buf)
 
     clocks = ClockSampler(local)
     gc.launch_count_reset()
@@ -582,7 +696,7 @@ def run_gpu(args):
                  "value": job_gbs(world, 4.0 * K * N, ms_u), "unit": "GB/s", "ms_per_step": ms_u,
                  "update_ms_per_launch": tu / max(nu, 1)}
 
-    # the sampled threshold (1 % samples, at most 16384 values per tensor):
+    # the sampled threshold (a 1 % sample of every tensor that holds a whole 64-value block):
     # the same step with the selection threshold taken from the sample
     sampled = None
     if w.method == "dgc":
@@ -607,7 +721,7 @@ def run_gpu(args):
         ms_s = max_over_ranks(g0.elapsed_time(g1) / args.steps, dev)
         k_s = np.array([gc.dgc_k(w.density, n) for n in w.sizes], np.int64)
         cnt = d_s.counts.cpu().numpy()
-        sampled = {"step": "dgc_compress_sampled (1 % sample per tensor, at most 16384) + sparse_average",
+        sampled = {"step": "dgc_compress_sampled (1 % sample of every tensor with a whole 64-value block) + sparse_average",
                    "value": job_gbs(world, 4.0 * K * N, ms_s), "unit": "GB/s", "ms_per_step": ms_s,
                    "sent_vs_exact_k": float(cnt.sum()) / float(K * k_s.sum()),
                    "tensors_short_of_k": float((cnt < k_s[None, :]).mean())}
@@ -726,6 +840,16 @@ def run_gpu(args):
         ms_e2e = max_over_ranks(f0.elapsed_time(f1) / e2e_steps, dev)
         e2e = job_gbs(world, grad_bytes, ms_e2e)
 
+    # every other workload of the method's five, timed the same way (a
+    # shorter run each), for the record; the headline stays the one above
+    others = None
+    if not args.no_other_configs:
+        others = {}
+        for c in (1, 2, 3, 4, 5):
+            if c != args.config:
+                m = measure_other(gc, c, args, world, local, dev, stream)
+                others[m["config"]["workload"]] = m
+
     if rank != 0:
         if world > 1:
             dist.barrier()
@@ -738,16 +862,17 @@ def run_gpu(args):
     dom_bytes = float(path.bytes_per_elem) * K * N
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9 if dom_ms > 0 else None
     traffic = profiled_traffic(path.dominant, w.name)
-    sent = path.sent()
-    step_bytes = path.bytes_per_elem * K * N + 16.0 * sent + (4.0 * N if w.method != "dcd" else 0.0)
+    step_bytes = step_bytes_of(path, w, K, N)
     total_ms = max(sum(x[1] for x in trace_all.values()), 1e-9)
     kernels = {name: {"launches": c, "ms_per_launch": t / max(c, 1), "share": t / total_ms}
                for name, (c, t) in trace_all.items()}
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        b, dt, desc = oracle_sample(w, oracle_inputs(w), args.cpu_seconds)
-        cpu = {"value": b / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc}
+        inputs = oracle_inputs(w, BASELINE_STEP_VALUES)
+        with one_core() as pin:
+            b, dt, desc = oracle_sample(w, inputs, args.cpu_seconds)
+        cpu = {"value": b / dt / 1e9, "unit": "GB/s", **pin.describe(), "kind": "oracle", "sample": desc}
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -778,6 +903,7 @@ def run_gpu(args):
         "gpu_launches": launches,
         "clocks": clk,
         "cpu_baseline": cpu,
+        "other_workloads": others,
     }
     print(json.dumps(line))
     if world > 1:
