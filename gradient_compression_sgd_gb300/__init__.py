@@ -92,6 +92,8 @@ def lib():
         L.sparse_average_update.argtypes = [vp, i64, vp, i32, i64, f32, vp, vp]
         L.dcd_step.argtypes = [i32, i64, vp, vp, vp, f32, f64, u64, u32, vp]
         L.ecd_step.argtypes = [i32, i64, vp, vp, vp, vp, vp, f32, f64, u64, u32, vp]
+        L.dcd_step_rows.argtypes = [i32, i64, i64, vp, vp, vp, f32, f64, u64, u32, vp, vp, i64, vp, vp]
+        L.dcd_copy_add.argtypes = [vp, i64, vp, vp, i64, i32, vp]
         L.dgc_encode.argtypes = [vp, i64, vp, i32, vp, i64, vp, vp]
         L.dgc_decode.argtypes = [vp, i64, vp, i32, vp, i64, vp, vp]
         L.adacomp_encode.argtypes = [vp, i32, vp, i64, vp, vp, i32, vp, i64, vp, vp]
@@ -416,6 +418,38 @@ def dcd_step(xhat, grad, w_ring, gamma: float, keep_p: float, seed: int, t: int,
     _check("dcd_step", lib().dcd_step(int(n), int(d), _ptr(w), _dev(xhat, "xhat", torch.float32),
                                       _dev(grad, "grad", torch.float32), float(gamma), float(keep_p),
                                       int(seed) & 0xFFFFFFFFFFFFFFFF, int(t) & 0xFFFFFFFF, _stream(stream)))
+
+
+def dcd_step_rows(xrows, grad, w_ring, gamma: float, keep_p: float, seed: int, t: int, first_node: int,
+                  c_first, c_last, counts, stream=None):
+    """DCD-PSGD on the own rows 1..R-2 of xrows [R, d] beside the neighbours'
+    copies in rows 0 and R-1 (see dcd_step_rows in include/gcsgd.h).  c_first,
+    c_last: [cap, 2] int32 pair buffers; counts: [2] int64, set on the device."""
+    import torch
+    R, d = xrows.shape
+    if grad.shape != (R - 2, d):
+        raise ValueError(f"grad must be [{R - 2}, {d}]")
+    if c_first.shape != c_last.shape or c_first.dim() != 2 or c_first.shape[1] != 2 or counts.numel() != 2:
+        raise ValueError("c_first, c_last: [cap, 2] int32 pair buffers; counts: 2 int64")
+    w = np.ascontiguousarray(np.asarray(w_ring, dtype=np.float32))
+    if w.shape != (3,):
+        raise ValueError("w_ring must hold 3 weights (left, self, right)")
+    _check("dcd_step_rows", lib().dcd_step_rows(
+        int(R), int(d), int(first_node), _ptr(w), _dev(xrows, "xrows", torch.float32), _dev(grad, "grad", torch.float32),
+        float(gamma), float(keep_p), int(seed) & 0xFFFFFFFFFFFFFFFF, int(t) & 0xFFFFFFFF,
+        _dev(c_first, "c_first", torch.int32), _dev(c_last, "c_last", torch.int32), int(c_first.shape[0]),
+        _dev(counts, "counts", torch.int64), _stream(stream)))
+
+
+def dcd_copy_add(x_row, pairs, count, zero_pass: bool = False, stream=None):
+    """x_row [d] += the C(z) a neighbour sent as pairs [cap, 2] int32, count a
+    device int64 (see dcd_copy_add in include/gcsgd.h)."""
+    import torch
+    if pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError("pairs: [cap, 2] int32")
+    _check("dcd_copy_add", lib().dcd_copy_add(
+        _dev(x_row, "x_row", torch.float32), int(x_row.numel()), _dev(pairs, "pairs", torch.int32) if pairs.numel() else None,
+        _dev(count, "count", torch.int64), int(pairs.shape[0]), 1 if zero_pass else 0, _stream(stream)))
 
 
 # ------------------------------------------------------- counting, tracing

@@ -25,6 +25,11 @@ int spavg_launch(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, in
                  cudaStream_t stream, bool update, float lr);
 int dcd_launch(int n, int64_t d, const float* w, float* xhat, const float* grad, float gamma, double p, uint64_t seed,
                uint32_t t, cudaStream_t stream);
+int dcd_rows_launch(int rows, int64_t d, int64_t first_node, const float* w, float* xhat, const float* grad,
+                    float gamma, double p, uint64_t seed, uint32_t t, gcsgd_pair* c_first, gcsgd_pair* c_last,
+                    int64_t cap, int64_t* counts, cudaStream_t stream);
+int dcd_copy_add_launch(float* x, int64_t d, const gcsgd_pair* pairs, const int64_t* count, int64_t cap,
+                        bool zero_pass, cudaStream_t stream);
 int ecd_launch(int n, int64_t d, const float* w, const float* x, float* x_prev, float* xt, const float* grad,
                float gamma, double p, uint64_t seed, uint32_t t, cudaStream_t stream);
 int wire_dgc_encode(const gcsgd_pair* lists, int64_t cap, const int64_t* totals, int K, uint8_t* streams,
@@ -372,6 +377,37 @@ int dcd_step(int32_t n_nodes, int64_t d, const float* w_ring, float* xhat, const
     if (!isfinite(gamma) || !isfinite(w_ring[0]) || !isfinite(w_ring[1]) || !isfinite(w_ring[2]))
         return set_error(GCSGD_ERR_INVALID_ARG, "%s: gamma and weights must be finite", fn);
     return dcd_launch(n_nodes, d, w_ring, xhat, grad, gamma, keep_p, seed, t, (cudaStream_t)stream);
+}
+
+int dcd_step_rows(int32_t rows, int64_t d, int64_t first_node, const float* w_ring, float* xhat, const float* grad,
+                  float gamma, double keep_p, uint64_t seed, uint32_t t, gcsgd_pair* c_first, gcsgd_pair* c_last,
+                  int64_t cap, int64_t* counts, void* stream) {
+    const char* fn = "dcd_step_rows";
+    if (rows < 3) return set_error(GCSGD_ERR_INVALID_ARG, "%s: rows = %d < 3 (two copies and an own node)", fn, rows);
+    if (d < 0 || d > ((int64_t)1 << 32)) return set_error(GCSGD_ERR_INVALID_ARG, "%s: d outside [0, 2^32]", fn);
+    if (first_node < 0 || first_node + rows - 2 > ((int64_t)1 << 32))
+        return set_error(GCSGD_ERR_INVALID_ARG, "%s: node indices outside [0, 2^32)", fn);
+    if (!w_ring) return set_error(GCSGD_ERR_INVALID_ARG, "%s: w_ring is NULL", fn);
+    if (!counts) return set_error(GCSGD_ERR_INVALID_ARG, "%s: counts is NULL", fn);
+    if (d > 0 && (!xhat || !grad)) return set_error(GCSGD_ERR_INVALID_ARG, "%s: xhat and grad must be non-NULL", fn);
+    if (cap < 0 || (cap > 0 && (!c_first || !c_last)))
+        return set_error(GCSGD_ERR_INVALID_ARG, "%s: cap < 0 or NULL lists", fn);
+    if (!(keep_p > 0.0 && keep_p <= 1.0))
+        return set_error(GCSGD_ERR_INVALID_ARG, "%s: keep_p %g outside (0, 1]", fn, keep_p);
+    if (!isfinite(gamma) || !isfinite(w_ring[0]) || !isfinite(w_ring[1]) || !isfinite(w_ring[2]))
+        return set_error(GCSGD_ERR_INVALID_ARG, "%s: gamma and weights must be finite", fn);
+    return dcd_rows_launch(rows, d, first_node, w_ring, xhat, grad, gamma, keep_p, seed, t, c_first, c_last, cap,
+                           counts, (cudaStream_t)stream);
+}
+
+int dcd_copy_add(float* x_row, int64_t d, const gcsgd_pair* pairs, const int64_t* count, int64_t cap,
+                 int32_t zero_pass, void* stream) {
+    const char* fn = "dcd_copy_add";
+    if (d < 0 || d > ((int64_t)1 << 32)) return set_error(GCSGD_ERR_INVALID_ARG, "%s: d outside [0, 2^32]", fn);
+    if (cap < 0) return set_error(GCSGD_ERR_INVALID_ARG, "%s: cap < 0", fn);
+    if (d > 0 && !x_row) return set_error(GCSGD_ERR_INVALID_ARG, "%s: x_row is NULL", fn);
+    if (cap > 0 && (!pairs || !count)) return set_error(GCSGD_ERR_INVALID_ARG, "%s: NULL list", fn);
+    return dcd_copy_add_launch(x_row, d, pairs, count, cap, zero_pass != 0, (cudaStream_t)stream);
 }
 
 int ecd_step(int32_t n_nodes, int64_t d, const float* w_ring, const float* x, float* x_prev, float* xtilde,

@@ -233,6 +233,120 @@ __device__ SelectResult radix_select_desc(Load load, uint64_t count, uint32_t ra
     return r;
 }
 
+// The rank-th largest of `count` keys that all lie in [base, base + 2^bits)
+// (1 <= rank <= count, bits <= 31): the selection of radix_select_desc on
+// d = key - base, with digits cut from the top of d's own bit range (11
+// bits, then 11, then the rest).  Keys crowded into a narrow range -- the
+// candidates above a threshold hint all share their leading bits -- then
+// spread over the first histogram's bins instead of piling into a few,
+// which would serialise the shared-memory atomics.  After the first digit
+// the chosen bucket's keys are copied to cbuf (ccap keys) when they fit.
+// `load(i, &key)` reads key i (every item counts).  Every thread must call
+// it; ends synchronised.
+template <int NT, class Load>
+__device__ SelectResult radix_select_span(Load load, uint32_t count, uint32_t rank, uint32_t base, int bits,
+                                          RadixSmem& rs, uint32_t* cbuf, uint32_t ccap) {
+    static_assert(NT == 512, "radix_pick needs at least NT buckets: digits are padded to 512 bins");
+    const int lane = threadIdx.x & 31;
+    uint32_t prefix = 0, pmask = 0, need = rank, greater = 0;
+    bool compact = false;
+    uint32_t ncand = 0;
+    int shift = bits;
+#pragma unroll 1
+    for (int pass = 0; shift > 0 || pass == 0; ++pass) {
+        const int nshift = shift > 11 ? shift - 11 : 0;
+        const uint32_t dmask = (1u << (shift - nshift)) - 1u;  // this digit's width
+        const int nb = (int)(dmask + 1) > NT ? (int)(dmask + 1) : NT;
+        for (int b = threadIdx.x; b < nb; b += NT) rs.hist[b] = 0;
+        __syncthreads();
+        const uint32_t n_it = compact ? ncand : count;
+        for (uint32_t i0 = 0; i0 < n_it; i0 += 4u * NT) {
+            uint32_t d[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t i = i0 + j * NT + threadIdx.x;
+                d[j] = 0xffffffffu;
+                if (i < n_it) {
+                    if (compact) {
+                        d[j] = cbuf[i];
+                    } else {
+                        uint32_t key;
+                        load(i, &key);
+                        d[j] = key - base;
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (i0 + j * NT + threadIdx.x < n_it && (d[j] & pmask) == prefix)
+                    atomicAdd(&rs.hist[(d[j] >> nshift) & dmask], 1u);
+        }
+        __syncthreads();
+        uint32_t b, ab, cb;
+        radix_pick<NT>(rs, nb, need, &b, &ab, &cb);
+        prefix |= b << nshift;
+        pmask |= dmask << nshift;
+        greater += ab;
+        need -= ab;
+        if (pass == 0 && nshift > 0 && cb <= ccap) {  // keep the chosen bucket's keys for the later digits
+            if (threadIdx.x == 0) rs.sel[3] = 0;
+            __syncthreads();
+            for (uint32_t i0 = 0; i0 < count; i0 += NT) {
+                const uint32_t i = i0 + threadIdx.x;
+                uint32_t dv = 0;
+                bool hit = false;
+                if (i < count) {
+                    uint32_t key;
+                    load(i, &key);
+                    dv = key - base;
+                    hit = (dv & pmask) == prefix;
+                }
+                const unsigned m = __ballot_sync(kFull, hit);
+                if (m) {
+                    uint32_t at = 0;
+                    if (lane == 0) at = atomicAdd(&rs.sel[3], (uint32_t)__popc(m));
+                    at = __shfl_sync(kFull, at, 0);
+                    if (hit) cbuf[at + __popc(m & ((1u << lane) - 1u))] = dv;
+                }
+            }
+            __syncthreads();
+            ncand = rs.sel[3];
+            compact = true;
+            __syncthreads();
+            if (ncand <= (uint32_t)NT) {
+                // few keys left: rank them exactly instead of more digits.
+                // Key j's rank: keys above it, plus equal keys before it.
+                if (threadIdx.x < ncand) {
+                    const uint32_t mine = cbuf[threadIdx.x];
+                    uint32_t above = 0, rank = 0;
+                    for (uint32_t i = 0; i < ncand; ++i) {
+                        const uint32_t o = cbuf[i];
+                        above += o > mine;
+                        rank += o > mine || (o == mine && i < threadIdx.x);
+                    }
+                    if (rank == need - 1) {
+                        rs.sel[0] = mine;
+                        rs.sel[1] = above;
+                    }
+                }
+                __syncthreads();
+                SelectResult r;
+                r.thresh = base + rs.sel[0];
+                r.greater = greater + rs.sel[1];
+                r.ties = need - rs.sel[1];
+                __syncthreads();
+                return r;
+            }
+        }
+        shift = nshift;
+    }
+    SelectResult r;
+    r.thresh = base + prefix;
+    r.greater = greater;
+    r.ties = need;
+    return r;
+}
+
 // ---------------------------------------------------------------- host side
 
 // Records the last error of the calling thread; returns `code`.

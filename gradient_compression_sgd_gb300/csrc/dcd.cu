@@ -128,6 +128,139 @@ __global__ void __launch_bounds__(NT) dcd_rolling(Params P, int n, uint64_t d, f
     }
 }
 
+// ------------------------------------------------ DCD-PSGD across ranks
+//
+// The nodes one rank of several holds, with copies of its two ring
+// neighbours beside them: rows 0 and R-1 of xhat are the copies (read only),
+// rows 1..R-2 the own nodes first_node.. .  Each own row mixes its row
+// neighbours as dcd_fixed mixes its ring neighbours; the C(z) the first and
+// the last own node add to themselves is what the neighbouring ranks add to
+// their copies (DCD-PSGD step 3), so every kept entry of those two rows goes
+// out as an (index, value) pair: per CTA and round, a block scan of the
+// threads' kept counts and one atomic per list reserve the slots (the lists
+// are not in index order; their indices are unique).
+
+// mix_step, also returning C(z) and whether the entry was kept.
+__device__ __forceinline__ float mix_step_c(const Params& P, float xl, float xi, float xr, float g, uint32_t word,
+                                            float* cz, bool* kept) {
+    float acc = __fmul_rn(P.w0, xl);
+    acc = __fadd_rn(acc, __fmul_rn(P.w1, xi));
+    acc = __fadd_rn(acc, __fmul_rn(P.w2, xr));
+    const float xh = __fsub_rn(acc, __fmul_rn(P.gamma, g));
+    const float z = __fsub_rn(xh, xi);
+    *kept = (uint64_t)word < P.thr;
+    *cz = *kept ? __fmul_rn(z, P.inv_p) : 0.0f;
+    return __fadd_rn(xi, *cz);
+}
+
+__global__ void __launch_bounds__(NT) dcd_rows(Params P, int R, uint64_t d, uint32_t first_node,
+                                               float* __restrict__ xhat, const float* __restrict__ grad,
+                                               bool rows_aligned, gcsgd_pair* __restrict__ c_first,
+                                               gcsgd_pair* __restrict__ c_last, uint64_t cap,
+                                               unsigned long long* __restrict__ counts) {
+    __shared__ uint64_t scan[NT / 32 + 1];
+    __shared__ unsigned long long s_base[2];
+    const uint64_t nq = (d + 3) / 4;
+    const int own = R - 2;
+    for (uint64_t q0 = (uint64_t)blockIdx.x * NT; q0 < nq; q0 += (uint64_t)gridDim.x * NT) {  // CTA-uniform
+        const uint64_t q = q0 + threadIdx.x;
+        const bool live = q < nq;
+        const uint64_t e = 4 * q;
+        const bool vec = rows_aligned && e + 4 <= d;
+        float cf[4] = {0.f, 0.f, 0.f, 0.f}, cl[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t kf = 0, kl = 0;  // kept masks of the first and last own row's four entries
+        if (live) {
+            float4 left = ld4(xhat, e, d, vec);
+            float4 cur = ld4(xhat + d, e, d, vec);
+            for (int r = 1; r <= own; ++r) {
+                const float4 right = ld4(xhat + (uint64_t)(r + 1) * d, e, d, vec);
+                const float4 g = ld4(grad + (uint64_t)(r - 1) * d, e, d, vec);
+                const uint4 w = philox4x32_10(make_uint4((uint32_t)q, first_node + (uint32_t)(r - 1), P.t,
+                                                         (uint32_t)(q >> 32)), P.key0, P.key1);
+                const float* L = &left.x;
+                const float* X = &cur.x;
+                const float* Rr = &right.x;
+                const float* G = &g.x;
+                const uint32_t* W = &w.x;
+                float4 o;
+                float* oo = &o.x;
+                float cz[4];
+                uint32_t km = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    bool kept;
+                    oo[j] = mix_step_c(P, L[j], X[j], Rr[j], G[j], W[j], &cz[j], &kept);
+                    km |= (uint32_t)(kept && e + j < d) << j;
+                }
+                st4(xhat + (uint64_t)r * d, e, d, vec, o);
+                if (r == 1) {
+                    kf = km;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) cf[j] = cz[j];
+                }
+                if (r == own) {
+                    kl = km;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) cl[j] = cz[j];
+                }
+                left = cur;
+                cur = right;
+            }
+        }
+        uint64_t tot;
+        const uint64_t ex = block_exclusive_scan<NT>((uint64_t)__popc(kf) | ((uint64_t)__popc(kl) << 32), scan, &tot);
+        if (threadIdx.x == 0) {
+            s_base[0] = atomicAdd(&counts[0], (unsigned long long)(tot & 0xffffffffu));
+            s_base[1] = atomicAdd(&counts[1], (unsigned long long)(tot >> 32));
+        }
+        __syncthreads();
+        uint64_t at_f = s_base[0] + (ex & 0xffffffffu), at_l = s_base[1] + (ex >> 32);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if ((kf >> j) & 1u) {
+                if (at_f < cap) {
+                    gcsgd_pair pr;
+                    pr.idx = (uint32_t)(e + j);
+                    pr.val = cf[j];
+                    c_first[at_f] = pr;
+                }
+                ++at_f;
+            }
+            if ((kl >> j) & 1u) {
+                if (at_l < cap) {
+                    gcsgd_pair pr;
+                    pr.idx = (uint32_t)(e + j);
+                    pr.val = cl[j];
+                    c_last[at_l] = pr;
+                }
+                ++at_l;
+            }
+        }
+        __syncthreads();  // s_base and scan are reused by the next round
+    }
+}
+
+// A neighbour's copy takes the C(z) its owner added: x[idx] += val at every
+// pair (the indices of a list are unique, so the adds do not race).
+__global__ void __launch_bounds__(NT) dcd_copy_scatter(float* __restrict__ x, uint64_t d,
+                                                       const gcsgd_pair* __restrict__ pairs,
+                                                       const int64_t* __restrict__ count, uint64_t cap) {
+    const int64_t c = *count;
+    const uint64_t n = c < 0 ? 0 : ((uint64_t)c < cap ? (uint64_t)c : cap);
+    for (uint64_t i = (uint64_t)blockIdx.x * NT + threadIdx.x; i < n; i += (uint64_t)gridDim.x * NT) {
+        const gcsgd_pair pr = pairs[i];
+        if (pr.idx < d) x[pr.idx] = __fadd_rn(x[pr.idx], pr.val);
+    }
+}
+
+// x <- x + 0 everywhere: the owner adds C(z) = +0 to every entry it did not
+// keep, which turns a -0 into +0; a copy that starts with -0 entries takes
+// this once so that its later adds stay bit-equal to the owner's.
+__global__ void __launch_bounds__(NT) dcd_copy_zero_pass(float* __restrict__ x, uint64_t d) {
+    for (uint64_t i = (uint64_t)blockIdx.x * NT + threadIdx.x; i < d; i += (uint64_t)gridDim.x * NT)
+        x[i] = __fadd_rn(x[i], 0.0f);
+}
+
 // ---------------------------------------------------------------- ECD-PSGD
 //
 // "Communication Compression for Decentralized Training", ECD-PSGD,
@@ -277,6 +410,55 @@ int dcd_launch(int n, int64_t d, const float* w, float* xhat, const float* grad,
             dcd_rolling<<<(unsigned)grid, NT, 0, stream>>>(P, n, (uint64_t)d, xhat, grad, rows_aligned);
     }
     return check_launch("dcd_step");
+}
+
+int dcd_rows_launch(int rows, int64_t d, int64_t first_node, const float* w, float* xhat, const float* grad,
+                    float gamma, double p, uint64_t seed, uint32_t t, gcsgd_pair* c_first, gcsgd_pair* c_last,
+                    int64_t cap, int64_t* counts, cudaStream_t stream) {
+    using namespace dcd;
+    if (cudaMemsetAsync(counts, 0, 2 * sizeof(int64_t), stream) != cudaSuccess)
+        return set_error(GCSGD_ERR_CUDA, "dcd_step_rows: clearing counts failed");
+    if (d == 0) return GCSGD_OK;
+    Params P;
+    P.w0 = w[0];
+    P.w1 = w[1];
+    P.w2 = w[2];
+    P.gamma = gamma;
+    P.inv_p = (float)(1.0 / p);
+    P.thr = p >= 1.0 ? (1ull << 32) : (uint64_t)llround(p * 4294967296.0);
+    P.key0 = (uint32_t)seed;
+    P.key1 = (uint32_t)(seed >> 32);
+    P.t = t;
+    const bool rows_aligned = ((d & 3) == 0) && (((uintptr_t)xhat & 15) == 0) && (((uintptr_t)grad & 15) == 0);
+    const uint64_t nq = ((uint64_t)d + 3) / 4;
+    uint64_t grid = (uint64_t)sm_count() * 4;
+    const uint64_t need = (nq + NT - 1) / NT;
+    if (grid > need) grid = need;
+    LaunchScope ls("dcd_step_rows", stream);
+    dcd_rows<<<(unsigned)grid, NT, 0, stream>>>(P, rows, (uint64_t)d, (uint32_t)first_node, xhat, grad, rows_aligned,
+                                                c_first, c_last, (uint64_t)cap,
+                                                reinterpret_cast<unsigned long long*>(counts));
+    return check_launch("dcd_step_rows");
+}
+
+int dcd_copy_add_launch(float* x, int64_t d, const gcsgd_pair* pairs, const int64_t* count, int64_t cap,
+                        bool zero_pass, cudaStream_t stream) {
+    using namespace dcd;
+    if (d == 0) return GCSGD_OK;
+    int rc;
+    if (zero_pass) {
+        uint64_t grid = (uint64_t)sm_count() * 4, need = ((uint64_t)d + NT - 1) / NT;
+        if (grid > need) grid = need;
+        LaunchScope ls("dcd_copy_zero_pass", stream);
+        dcd_copy_zero_pass<<<(unsigned)grid, NT, 0, stream>>>(x, (uint64_t)d);
+        if ((rc = check_launch("dcd_copy_zero_pass"))) return rc;
+    }
+    if (cap == 0) return GCSGD_OK;
+    uint64_t grid = (uint64_t)sm_count() * 2, need = ((uint64_t)cap + NT - 1) / NT;
+    if (grid > need) grid = need;
+    LaunchScope ls("dcd_copy_add", stream);
+    dcd_copy_scatter<<<(unsigned)grid, NT, 0, stream>>>(x, (uint64_t)d, pairs, count, (uint64_t)cap);
+    return check_launch("dcd_copy_add");
 }
 
 int ecd_launch(int n, int64_t d, const float* w, const float* x, float* x_prev, float* xt, const float* grad,

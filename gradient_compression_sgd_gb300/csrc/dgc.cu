@@ -33,6 +33,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
 #include <vector>
 
 #include "common.cuh"
@@ -97,7 +98,7 @@ __host__ __device__ __forceinline__ void seg_fields(uint32_t n, double density, 
         p->kind = kKindRaw;
     } else {
         p->kind = kKindPool;
-        const uint64_t R = 5ull * p->k / 2 > kPoolFloor ? 5ull * p->k / 2 : kPoolFloor;  // expected candidates
+        const uint64_t R = 2ull * p->k > kPoolFloor ? 2ull * p->k : kPoolFloor;  // expected candidates
         const uint64_t cap = 4 * R + 256;
         p->cap = (uint32_t)(cap < n ? cap : n);
         uint64_t m = (uint64_t)kSampleAbove * n / R;
@@ -212,10 +213,13 @@ __global__ void __launch_bounds__(NT) dgc_sumsq(const float* __restrict__ grad, 
 // lanes adds the lane sums in a fixed tree (a + b and b + a are the same
 // bits), so every lane of every CTA that evaluates this gets the same c.
 // The partials are non-negative, so the tree sum needs no compensation
-// (relative error below 9 * 2^-53).
-__device__ float clip_scale_warp(const double* __restrict__ part, int k, float clip_thr, int clip_nodes) {
+// (relative error below 9 * 2^-53).  Callers test clip_thr > 0 first and
+// call it only then: kept out of line so that its fp64 square root and
+// division, slow on GB300's few FP64 units, never run when clipping is off
+// (inlined, the unclipped path paid ~4 us per CTA for them).
+__device__ __noinline__ float clip_scale_warp(const double* __restrict__ part, int k, float clip_thr,
+                                              int clip_nodes) {
     static_assert(kSumsqBlocks == 16 * 32, "16 partial sums per lane");
-    if (!(clip_thr > 0.0f)) return 1.0f;
     const double* pk = part + (uint64_t)k * kSumsqBlocks + 16 * (threadIdx.x & 31);
     double x[16];
 #pragma unroll
@@ -270,6 +274,7 @@ __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, PoolL
     __shared__ RadixSmem rs;
     __shared__ uint64_t carry[3];
     __shared__ float s_c;
+    __shared__ SegPlan s_plan;
     if (blockIdx.x == gridDim.x - 1) {  // the extra CTA: plan, order, clip scales
         if (threadIdx.x < 3) carry[threadIdx.x] = 0;
         __syncthreads();
@@ -297,20 +302,17 @@ __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, PoolL
                 p.tile_off = (uint32_t)(c1 + ex_tile);
                 p.out_off = (uint32_t)(c2 + ex_out);
                 plan[s] = p;
-                // rank by size, largest first (ties: lower index first)
-                const uint32_t ns = so.off[s + 1] - so.off[s];
-                uint32_t rank = 0;
-                for (int q = 0; q < S; ++q) {
-                    const uint32_t nq = so.off[q + 1] - so.off[q];
-                    rank += nq > ns || (nq == ns && q < s);
-                }
-                order[rank] = (uint16_t)s;
+                order[s] = pl.order[s];  // segments by size, largest first (from the host)
             }
             __syncthreads();
         }
-        for (int k = (int)threadIdx.x >> 5; k < K; k += NTP / 32) {  // one warp per learner
-            const float c = clip_scale_warp(part, k, clip_thr, clip_nodes);
-            if ((threadIdx.x & 31) == 0) clip_c[k] = c;
+        if (clip_thr > 0.0f) {
+            for (int k = (int)threadIdx.x >> 5; k < K; k += NTP / 32) {  // one warp per learner
+                const float c = clip_scale_warp(part, k, clip_thr, clip_nodes);
+                if ((threadIdx.x & 31) == 0) clip_c[k] = c;
+            }
+        } else {
+            for (int k = (int)threadIdx.x; k < K; k += NTP) clip_c[k] = 1.0f;
         }
         return;
     }
@@ -322,16 +324,20 @@ __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, PoolL
         const int s = pl.seg[q];
         const int unit = k * S + s;
         if (warp == 0) {
-            const float c = clip_scale_warp(part, k, clip_thr, clip_nodes);
+            const float c = clip_thr > 0.0f ? clip_scale_warp(part, k, clip_thr, clip_nodes) : 1.0f;
             if (lane == 0) {
                 s_c = c;
                 pool_cnt[unit] = 0;
             }
         }
+        if (threadIdx.x == 32) {  // one thread evaluates the plan (fp64; GB300 has few FP64 units)
+            SegPlan sp;
+            seg_fields(so.off[s + 1] - so.off[s], density, sample_frac, &sp);
+            sp.off = so.off[s];
+            s_plan = sp;
+        }
         __syncthreads();
-        SegPlan p;
-        seg_fields(so.off[s + 1] - so.off[s], density, sample_frac, &p);
-        p.off = so.off[s];
+        const SegPlan p = s_plan;
         const float c = s_c;
         const uint32_t nblk = p.m / kSampleBlock;
         const uint32_t stride = p.n / nblk;  // >= 64 since m <= n: blocks never overlap
@@ -342,6 +348,8 @@ __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, PoolL
         const float* gs = grad + base;
         const float* us = u + base;
         const float* vs = v + base;
+        const bool hint_mode = !p.sampled;  // the hint: a <= 48 (see below), no histogram while sampling
+        uint32_t t1 = 0, t2 = 0, t3 = 0;     // hint mode: the lane's three largest keys (a multiset)
         radix_hist_clear<NTP>(rs);
         __syncthreads();
         // sample element j of block b sits at b * stride + j; a warp issues
@@ -372,7 +380,23 @@ __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, PoolL
                         dgc_elem<NEST>(gg[j][h], uu[j][h], vv[j][h], momentum, c);
                         const uint32_t key = mag_key(vv[j][h]);
                         kdst[b * kSampleBlock + 32 * h + lane] = key;
-                        radix_hist_add(rs, key);
+                        if (hint_mode) {
+                            if (key > t3) {
+                                if (key > t2) {
+                                    t3 = t2;
+                                    if (key > t1) {
+                                        t2 = t1;
+                                        t1 = key;
+                                    } else {
+                                        t2 = key;
+                                    }
+                                } else {
+                                    t3 = key;
+                                }
+                            }
+                        } else {
+                            radix_hist_add(rs, key);
+                        }
                     }
                 }
             }
@@ -392,11 +416,79 @@ __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, PoolL
                 [&](uint64_t i, uint32_t* key) { *key = keys[i]; return true; }, p.m, p.a, rs, true);
             if (threadIdx.x == 0) hint[unit] = sr.thresh;
         } else {
-            // two digits suffice: the hint only needs to sit at or below the
-            // a-th largest sampled key
-            const SelectResult sr = radix_select_desc<NTP, 2>(
-                [&](uint64_t i, uint32_t* key) { *key = keys[i]; return true; }, p.m, p.a, rs, true);
-            const uint32_t h = sr.thresh;
+            // The hint: the a-th largest sampled key, a <= 48.  Every warp's
+            // third largest key is found by three rounds of warp max over the
+            // lanes' top-3 lists; L = the smallest of the 16 is exceeded or
+            // matched by at least 3 keys of every warp, 48 >= a keys in all,
+            // so the a-th largest key is among the keys >= L, usually a few
+            // dozen: they are compacted and ranked exactly, with no
+            // histogram (sampled keys crowd into a few radix bins, which
+            // serialises shared-memory atomics).
+            uint32_t w3 = 0;
+#pragma unroll
+            for (int r = 0; r < 3; ++r) {
+                w3 = __reduce_max_sync(kFull, t1);
+                const unsigned own = __ballot_sync(kFull, t1 == w3);
+                if (lane == __ffs(own) - 1) {
+                    t1 = t2;
+                    t2 = t3;
+                    t3 = 0;
+                }
+            }
+            if (lane == 0) rs.hist[warp] = w3;
+            if (threadIdx.x == 0) {
+                rs.sel[0] = 0;
+                rs.sel[3] = 0;
+            }
+            __syncthreads();
+            uint32_t L = 0xffffffffu;
+#pragma unroll
+            for (int w = 0; w < NTP / 32; ++w) L = min(L, rs.hist[w]);
+            // warp-uniform trip count (the ballots need every lane); a lane's
+            // four keys are all in range or all out (m is a multiple of 64)
+            for (uint32_t w0 = 128u * warp; w0 < p.m; w0 += 128u * (NTP / 32)) {
+                const uint32_t i0 = w0 + 4u * lane;
+                const bool in = i0 < p.m;
+                const uint4 q4 = in ? *reinterpret_cast<const uint4*>(keys + i0) : make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t kk[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const bool hit = in && kk[j] >= L;
+                    const unsigned mk = __ballot_sync(kFull, hit);
+                    if (mk) {
+                        uint32_t at = 0;
+                        if (lane == 0) at = atomicAdd(&rs.sel[3], (uint32_t)__popc(mk));
+                        at = __shfl_sync(kFull, at, 0);
+                        const uint32_t slot = at + __popc(mk & ((1u << lane) - 1u));
+                        if (hit && slot < (uint32_t)kCandMax) rs.cand[slot] = kk[j];
+                    }
+                }
+            }
+            __syncthreads();
+            const uint32_t c = rs.sel[3];
+            uint32_t h = 0;
+            if (c <= (uint32_t)NTP) {
+                // rank of candidate j: keys above it, plus equal keys before it
+                if (threadIdx.x < c) {
+                    const uint32_t mine = rs.cand[threadIdx.x];
+                    uint32_t rank = 0;
+                    for (uint32_t i = 0; i < c; ++i) {
+                        const uint32_t o = rs.cand[i];
+                        rank += o > mine || (o == mine && i < threadIdx.x);
+                    }
+                    if (rank == p.a - 1) rs.sel[0] = mine;
+                }
+                __syncthreads();
+                h = rs.sel[0];
+            } else if (c <= (uint32_t)kCandMax) {
+                h = radix_select_desc<NTP, 3>([&](uint64_t i, uint32_t* key) { *key = rs.cand[i]; return true; },
+                                              c, p.a, rs, false, keys + p.m, kSampleMax - p.m)
+                        .thresh;
+            } else {
+                h = radix_select_desc<NTP, 3>([&](uint64_t i, uint32_t* key) { *key = keys[i]; return true; },
+                                              p.m, p.a, rs, false)
+                        .thresh;
+            }
             if (threadIdx.x == 0) hint[unit] = h > 1u ? h : 1u;
         }
         __syncthreads();
@@ -735,9 +827,13 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
     gcsgd_pair* dst = out + (uint64_t)k * cap + p.out_off;
 
     if (pool_ok && pc <= kStageItems) {
-        // stage the candidates in index order (tiles in order, items of a tile
-        // in order) and count their first radix digit on the way
-        radix_hist_clear<NTS>(rs);
+        // Stage the candidates in index order (tiles in order, items of a
+        // tile in order), noting the range of their keys on the way.  Per
+        // chunk of tiles: a block scan of the tile counts gives each tile's
+        // stage offset; every tile writes its own (chunk-local) index into
+        // the stage slots it owns; then every thread gathers its slots'
+        // items, eight loads in flight, reading the tile from the slot.
+        uint32_t kmin = 0xffffffffu, kmax = 0;
         uint32_t run = 0;
         for (uint32_t tb = 0; tb < p.ntiles; tb += kChunkTiles) {
             constexpr int TPT = kChunkTiles / NTS;  // tiles per thread
@@ -753,33 +849,34 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
             uint32_t ex = (uint32_t)block_exclusive_scan<NTS>(c, rs.scan, &tot);
 #pragma unroll
             for (int j = 0; j < TPT; ++j) {
-                toff[TPT * threadIdx.x + j] = ex;
-                tbase[TPT * threadIdx.x + j] = ent[j].x;
+                const uint32_t lt = TPT * threadIdx.x + j;
+                toff[lt] = ex;
+                tbase[lt] = ent[j].x;
+                for (uint32_t i = 0; i < ent[j].y && run + ex + i < kStageItems; ++i) stage[run + ex + i].x = lt;
                 ex += ent[j].y;
             }
             __syncthreads();
             const uint32_t total = (uint32_t)tot;
-            for (uint32_t q0 = 0; q0 < total; q0 += 4 * NTS) {
-                uint2 it[4];
+            constexpr int IPT = 8;
+            for (uint32_t q0 = 0; q0 < total; q0 += IPT * NTS) {
+                uint2 it[IPT];
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
+                for (int jj = 0; jj < IPT; ++jj) {
                     const uint32_t q = q0 + jj * NTS + threadIdx.x;
                     it[jj] = make_uint2(0u, 0u);
-                    if (q < total) {
-                        int lo = 0, hi = kChunkTiles;  // last tile with toff <= q
-                        while (hi - lo > 1) {
-                            const int mid = (lo + hi) >> 1;
-                            if (toff[mid] <= q) lo = mid; else hi = mid;
-                        }
-                        it[jj] = items[tbase[lo] + (q - toff[lo])];
+                    if (q < total && run + q < kStageItems) {
+                        const uint32_t lt = stage[run + q].x;
+                        it[jj] = items[tbase[lt] + (q - toff[lt])];
                     }
                 }
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
+                for (int jj = 0; jj < IPT; ++jj) {
                     const uint32_t q = q0 + jj * NTS + threadIdx.x;
                     if (q < total && run + q < kStageItems) {
                         stage[run + q] = it[jj];
-                        radix_hist_add(rs, it[jj].y & 0x7fffffffu);
+                        const uint32_t key = it[jj].y & 0x7fffffffu;
+                        kmin = min(kmin, key);
+                        kmax = max(kmax, key);
                     }
                 }
             }
@@ -788,8 +885,22 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
         }
         uint32_t T = 0, ties = pc;  // take_all: every key >= 0 goes, in index order
         if (!take_all) {
-            const SelectResult r = radix_select_desc<NTS, 3>(
-                [&](uint64_t i, uint32_t* key) { *key = stage[i].y & 0x7fffffffu; return true; }, pc, p.k, rs, true);
+            // the candidates share their leading bits (all sit just above the
+            // hint): select over their own key range [kmin, kmax]
+            kmin = __reduce_min_sync(kFull, kmin);
+            kmax = __reduce_max_sync(kFull, kmax);
+            if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = make_uint2(kmin, kmax);
+            __syncthreads();
+#pragma unroll
+            for (int w = 0; w < NTS / 32; ++w) {
+                kmin = min(kmin, wsum[w].x);
+                kmax = max(kmax, wsum[w].y);
+            }
+            __syncthreads();  // wsum is reused by the emission
+            const int bits = kmax > kmin ? 32 - __clz(kmax - kmin) : 0;
+            const SelectResult r = radix_select_span<NTS>(
+                [&](uint32_t i, uint32_t* key) { *key = stage[i].y & 0x7fffffffu; }, pc, p.k, kmin, bits, rs,
+                rs.cand, (uint32_t)kCandMax);
             T = r.thresh;
             ties = r.ties;
         }
@@ -1091,6 +1202,10 @@ int dgc_launch(const int64_t* off, int S, int K, const float* grad, float* u, fl
             pl.n_pool = 0;
             uint32_t koff = 0;
             for (int s = 0; s <= S; ++s) so.off[s] = (uint32_t)off[s];
+            // segments by size, largest first, ties to the lower index (a stable sort)
+            for (int s = 0; s < S; ++s) pl.order[s] = (uint16_t)s;
+            std::stable_sort(pl.order, pl.order + S,
+                             [&](uint16_t a, uint16_t b) { return off[a + 1] - off[a] > off[b + 1] - off[b]; });
             for (int s = 0; s < S; ++s) {
                 SegPlan sp;
                 seg_fields((uint32_t)(off[s + 1] - off[s]), density, sample_frac, &sp);

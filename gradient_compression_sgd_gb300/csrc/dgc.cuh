@@ -40,6 +40,7 @@ struct PoolList {
     uint32_t n_pool;
     uint16_t seg[MAXS];
     uint32_t koff[MAXS];  // sampled threshold, samples above kSampleMax: first key in the learner's spill region
+    uint16_t order[MAXS];  // all segments by size, largest first (dgc_select's order)
 };
 
 struct HostPlan {

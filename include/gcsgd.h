@@ -302,6 +302,42 @@ int dcd_step(int32_t n_nodes, int64_t d, const float* w_ring, float* xhat, const
              float gamma, double keep_p, uint64_t seed, uint32_t t, void* stream);
 
 /*
+ * dcd_step for the nodes one process of several holds ("Communication
+ * Compression for Decentralized Training", DCD-PSGD steps 1-3, with step 3's
+ * message to the neighbours made explicit).  xhat is [rows][d]: row 0 is this
+ * process's copy of node first_node - 1, rows 1 .. rows-2 its own nodes
+ * first_node .. first_node + rows - 3, row rows-1 its copy of the node after
+ * them (ring indices mod n are the caller's).  Every own row takes dcd_step's
+ * update with its row neighbours (the copies are read, not written) and the
+ * keep draw of its own node index; the result equals the own rows of a
+ * dcd_step over the whole ring, bit for bit.
+ * c_first / c_last  [cap] gcsgd_pair: every kept entry (C(z) bits and
+ *         column index) of the first and of the last own row -- what the
+ *         holders of copies of those nodes must add (dcd_copy_add).  The
+ *         pairs of a list are not in index order; their indices are unique.
+ * counts  device [2] int64: set by the call to the number of kept entries of
+ *         each list; entries past cap are counted, not written (size cap to d
+ *         to never drop one).
+ * rows >= 3; d <= 2^32 (32-bit pair indices); other arguments as dcd_step.
+ */
+int dcd_step_rows(int32_t rows, int64_t d, int64_t first_node, const float* w_ring, float* xhat, const float* grad,
+                  float gamma, double keep_p, uint64_t seed, uint32_t t, gcsgd_pair* c_first, gcsgd_pair* c_last,
+                  int64_t cap, int64_t* counts, void* stream);
+
+/*
+ * A neighbour's copy of node j takes the C(z_j) the node added to itself
+ * (DCD-PSGD step 3): x_row[idx] += val (fp32) for the first min(*count, cap)
+ * pairs, whose indices are unique.  The owner adds +0 to every entry it did
+ * not keep, which only changes a -0 into +0: with zero_pass != 0 the call
+ * first adds +0 to every entry of x_row, which a copy needs once, before its
+ * first update, if its starting model may hold -0 (after one iteration no
+ * own row holds -0).  x_row [d] fp32, updated in place; count is a device
+ * pointer (for example dcd_step_rows's counts, after the transfer).
+ */
+int dcd_copy_add(float* x_row, int64_t d, const gcsgd_pair* pairs, const int64_t* count, int64_t cap,
+                 int32_t zero_pass, void* stream);
+
+/*
  * One ECD-PSGD iteration t >= 1 of n_nodes nodes on a ring ("Communication
  * Compression for Decentralized Training", ECD-PSGD, equations (3)-(4)):
  *   z_j   = (1 - t/2) x_{t-1}^(j) + (t/2) x_t^(j)          (extrapolation)

@@ -83,6 +83,10 @@ def lib():
             L.oracle_dcd_step_window.restype = ctypes.c_int
             L.oracle_dcd_step_window.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, vp, vp, vp,
                                                  ctypes.c_float, ctypes.c_double, ctypes.c_uint64, ctypes.c_uint32]
+            L.oracle_dcd_step_rows.restype = ctypes.c_int
+            L.oracle_dcd_step_rows.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, vp, vp, vp,
+                                               ctypes.c_float, ctypes.c_double, ctypes.c_uint64, ctypes.c_uint32,
+                                               vp, vp]
             for f in (L.oracle_dcd_step, L.oracle_dcd_step_replicas):
                 f.restype = ctypes.c_int
                 f.argtypes = [ctypes.c_int, ctypes.c_int64, vp, vp, vp, ctypes.c_float, ctypes.c_double,
@@ -243,6 +247,23 @@ def dcd_step_window(xhat, g, w, gamma, p, seed, t, e_base):
                                       int(t))
     _check(rc, "oracle_dcd_step_window")
     return xhat
+
+
+def dcd_step_rows(xrows, g, w, gamma, p, seed, t, first_node):
+    """One DCD iteration of the own rows 1..R-2 of ``xrows`` ([R, d] float32,
+    updated in place; rows 0 and R-1 are the neighbours' copies, read only),
+    own nodes first_node.. ; g: [R-2, d].  Returns (C of row 1, C of row R-2)."""
+    assert xrows.dtype == np.float32 and xrows.flags["C_CONTIGUOUS"]
+    R, d = xrows.shape
+    g = _f32(g)
+    assert g.shape == (R - 2, d)
+    wr = np.ascontiguousarray(w, dtype=np.float32)
+    c_first = np.zeros(d, np.float32)
+    c_last = np.zeros(d, np.float32)
+    rc = lib().oracle_dcd_step_rows(int(R), int(d), int(first_node), _p(wr), _p(xrows), _p(g), float(gamma),
+                                    float(p), int(seed), int(t), _p(c_first), _p(c_last))
+    _check(rc, "oracle_dcd_step_rows")
+    return c_first, c_last
 
 
 def dcd_step_replicas(rep, g, w, gamma, p, seed, t):

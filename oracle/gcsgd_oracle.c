@@ -555,6 +555,50 @@ int oracle_dcd_step(int n, int64_t d, const float w[3], float* xhat, const float
 }
 
 /*
+ * The same iteration for the nodes one rank of several holds, with copies of
+ * its two ring neighbours beside them (DCD-PSGD step 3 across processes: the
+ * neighbours' C(z) reach the copies by a message).  xhat is [rows][d]: row 0
+ * is the copy of node first_node - 1, rows 1 .. rows-2 the own nodes
+ * first_node .. first_node + rows - 3, row rows-1 the copy of the node after
+ * them (ring indices taken by the caller).  Own row r mixes rows r-1, r and
+ * r+1 exactly as oracle_dcd_step mixes its ring neighbours, with the keep
+ * draw of node first_node + r - 1; the copies are read, not updated.
+ * g is [rows-2][d].  c_first and c_last ([d] each) receive the C(z) the first
+ * and the last own node added to themselves, which their neighbours' holders
+ * add to their copies.
+ */
+int oracle_dcd_step_rows(int rows, int64_t d, int64_t first_node, const float w[3], float* xhat, const float* g,
+                         float gamma, double p, uint64_t seed, uint32_t t, float* c_first, float* c_last) {
+    if (rows < 3 || d < 0 || first_node < 0 || !(p > 0.0 && p <= 1.0)) return ORACLE_EINVAL;
+    const int own = rows - 2;
+    float* xn = (float*)malloc(sizeof(float) * (size_t)(own * d > 0 ? own * d : 1));
+    if (!xn) return ORACLE_ENOMEM;
+    const uint64_t thr = oracle_keep_threshold(p);
+    const float inv_p = (float)(1.0 / p);
+    for (int r = 1; r <= own; ++r) {
+        const float* xl = xhat + (int64_t)(r - 1) * d;
+        const float* xi = xhat + (int64_t)r * d;
+        const float* xr = xhat + (int64_t)(r + 1) * d;
+        const float* gi = g + (int64_t)(r - 1) * d;
+        const uint32_t node = (uint32_t)(first_node + r - 1);
+        for (int64_t e = 0; e < d; ++e) {
+            float acc = w[0] * xl[e];
+            acc = acc + w[1] * xi[e];
+            acc = acc + w[2] * xr[e];
+            const float xh = acc - gamma * gi[e];
+            const float z = xh - xi[e];
+            const float cz = dcd_compress(z, dcd_word(seed, node, t, (uint64_t)e), thr, inv_p);
+            xn[(int64_t)(r - 1) * d + e] = xi[e] + cz;
+            if (r == 1) c_first[e] = cz;
+            if (r == own) c_last[e] = cz;
+        }
+    }
+    memcpy(xhat + d, xn, sizeof(float) * (size_t)(own * d));
+    free(xn);
+    return ORACLE_OK;
+}
+
+/*
  * The same iteration with every replica stored explicitly, for the replica
  * identity check: rep[i][j] is node i's copy of node j's model ([n][n][d];
  * rep[i][i] is node i's own model).  Node i mixes its own copies of its ring
