@@ -233,6 +233,102 @@ __device__ SelectResult radix_select_desc(Load load, uint64_t count, uint32_t ra
     return r;
 }
 
+// ------------------------------------------------ selection of a small top
+//
+// For a small rank (at most 48) among keys spread over the threads of a
+// block: every lane keeps its three largest keys (top3_insert); three rounds
+// of warp max give every warp's third-largest key; the smallest of those, L,
+// is matched or exceeded by at least three keys of every warp that holds
+// three keys, so at least 48 keys are >= L (or L = 0 and every key is).  The
+// keys >= L, usually a few dozen, are appended to rs.cand (cand_append) and
+// ranked exactly (rank_select).  No histogram is built: keys of similar
+// magnitude crowd into a few radix bins, which serialises shared atomics.
+
+// Inserts key into the lane's three largest (a multiset; 0 = empty).
+__device__ __forceinline__ void top3_insert(uint32_t key, uint32_t& t1, uint32_t& t2, uint32_t& t3) {
+    if (key > t3) {
+        if (key > t2) {
+            t3 = t2;
+            if (key > t1) {
+                t2 = t1;
+                t1 = key;
+            } else {
+                t2 = key;
+            }
+        } else {
+            t3 = key;
+        }
+    }
+}
+
+// L = the smallest of the warps' third-largest keys, on every thread; also
+// empties rs.cand (rs.sel[3] = 0).  Every thread must call it.
+template <int NT>
+__device__ uint32_t top3_bound(uint32_t t1, uint32_t t2, uint32_t t3, RadixSmem& rs) {
+    static_assert(NT / 32 <= 2048, "one word per warp");
+    uint32_t w3 = 0;
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {
+        w3 = __reduce_max_sync(kFull, t1);
+        const unsigned own = __ballot_sync(kFull, t1 == w3);
+        if ((threadIdx.x & 31) == (unsigned)__ffs(own) - 1u) {
+            t1 = t2;
+            t2 = t3;
+            t3 = 0;
+        }
+    }
+    if ((threadIdx.x & 31) == 0) rs.hist[threadIdx.x >> 5] = w3;
+    if (threadIdx.x == 0) rs.sel[3] = 0;
+    __syncthreads();
+    uint32_t L = 0xffffffffu;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) L = min(L, rs.hist[w]);
+    __syncthreads();  // rs.hist is free again
+    return L;
+}
+
+// Appends `key` to rs.cand where `hit` (slots past kCandMax are counted in
+// rs.sel[3], not written).  The whole warp calls it.
+__device__ __forceinline__ void cand_append(RadixSmem& rs, uint32_t key, bool hit) {
+    const unsigned m = __ballot_sync(kFull, hit);
+    if (m) {
+        const int lane = threadIdx.x & 31;
+        uint32_t at = 0;
+        if (lane == 0) at = atomicAdd(&rs.sel[3], (uint32_t)__popc(m));
+        at = __shfl_sync(kFull, at, 0);
+        const uint32_t slot = at + __popc(m & ((1u << lane) - 1u));
+        if (hit && slot < (uint32_t)kCandMax) rs.cand[slot] = key;
+    }
+}
+
+// The rank-th largest (1 <= rank <= c) of the c <= NT keys in rs.cand,
+// exactly: key j's rank is the keys above it plus the equal keys before it.
+// Returns the key, how many keys are above it, and rank - that (the equal
+// keys to take).  Every thread must call it.
+template <int NT>
+__device__ SelectResult rank_select(RadixSmem& rs, uint32_t c, uint32_t rank) {
+    if (threadIdx.x < c) {
+        const uint32_t mine = rs.cand[threadIdx.x];
+        uint32_t above = 0, r = 0;
+        for (uint32_t i = 0; i < c; ++i) {
+            const uint32_t o = rs.cand[i];
+            above += o > mine;
+            r += o > mine || (o == mine && i < threadIdx.x);
+        }
+        if (r == rank - 1) {
+            rs.sel[0] = mine;
+            rs.sel[1] = above;
+        }
+    }
+    __syncthreads();
+    SelectResult res;
+    res.thresh = rs.sel[0];
+    res.greater = rs.sel[1];
+    res.ties = rank - rs.sel[1];
+    __syncthreads();
+    return res;
+}
+
 // The rank-th largest of `count` keys that all lie in [base, base + 2^bits)
 // (1 <= rank <= count, bits <= 31): the selection of radix_select_desc on
 // d = key - base, with digits cut from the top of d's own bit range (11

@@ -48,13 +48,13 @@ constexpr int NTP = 512;                 // threads per CTA of dgc_prepare
 constexpr uint32_t kSmallK = 32;         // raw segments with k <= 32 ...
 constexpr uint32_t kSmallN = 8192;       // ... and at most 8192 values use the register top-k
 constexpr int kTile = 4096;              // elements per dgc_update tile (NT x 4 float4)
-constexpr uint32_t kRawMax = 16384;      // segments up to this size select from v' directly
+constexpr uint32_t kRawMax = 8192;       // segments up to this size select from v' directly
 constexpr uint32_t kSampleMax = 16384;   // largest hint sample (keys held in shared memory)
 constexpr uint32_t kSampleAbove = 48;    // sampled entries expected above the hint
 constexpr uint32_t kSampleBlock = 64;    // consecutive values per sample block
 constexpr uint32_t kPoolFloor = 512;     // smallest expected candidate count
-constexpr uint32_t kStageItems = 8192;   // candidates dgc_select stages in shared memory
-constexpr int kChunkTiles = 4 * NTS;     // tile-table entries dgc_select scans per round
+constexpr uint32_t kStageItems = 10240;  // candidates dgc_select stages in shared memory (80 KB)
+constexpr int kChunkTiles = 2 * NTS;     // tile-table entries dgc_select scans per round
 constexpr size_t kStageBytes = kStageItems * sizeof(uint2);  // also holds kRawMax floats
 static_assert(kStageBytes >= kRawMax * sizeof(float), "the stage must hold a raw segment");
 constexpr int kSumsqBlocks = 512;        // CTAs per learner in dgc_sumsq
@@ -98,7 +98,7 @@ __host__ __device__ __forceinline__ void seg_fields(uint32_t n, double density, 
         p->kind = kKindRaw;
     } else {
         p->kind = kKindPool;
-        const uint64_t R = 2ull * p->k > kPoolFloor ? 2ull * p->k : kPoolFloor;  // expected candidates
+        const uint64_t R = 5ull * p->k / 2 > kPoolFloor ? 5ull * p->k / 2 : kPoolFloor;  // expected candidates
         const uint64_t cap = 4 * R + 256;
         p->cap = (uint32_t)(cap < n ? cap : n);
         uint64_t m = (uint64_t)kSampleAbove * n / R;
@@ -381,19 +381,7 @@ __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, PoolL
                         const uint32_t key = mag_key(vv[j][h]);
                         kdst[b * kSampleBlock + 32 * h + lane] = key;
                         if (hint_mode) {
-                            if (key > t3) {
-                                if (key > t2) {
-                                    t3 = t2;
-                                    if (key > t1) {
-                                        t2 = t1;
-                                        t1 = key;
-                                    } else {
-                                        t2 = key;
-                                    }
-                                } else {
-                                    t3 = key;
-                                }
-                            }
+                            top3_insert(key, t1, t2, t3);
                         } else {
                             radix_hist_add(rs, key);
                         }
@@ -416,70 +404,25 @@ __global__ void __launch_bounds__(NTP, 2) dgc_prepare(SegOffsets<MAXS> so, PoolL
                 [&](uint64_t i, uint32_t* key) { *key = keys[i]; return true; }, p.m, p.a, rs, true);
             if (threadIdx.x == 0) hint[unit] = sr.thresh;
         } else {
-            // The hint: the a-th largest sampled key, a <= 48.  Every warp's
-            // third largest key is found by three rounds of warp max over the
-            // lanes' top-3 lists; L = the smallest of the 16 is exceeded or
-            // matched by at least 3 keys of every warp, 48 >= a keys in all,
-            // so the a-th largest key is among the keys >= L, usually a few
-            // dozen: they are compacted and ranked exactly, with no
-            // histogram (sampled keys crowd into a few radix bins, which
-            // serialises shared-memory atomics).
-            uint32_t w3 = 0;
-#pragma unroll
-            for (int r = 0; r < 3; ++r) {
-                w3 = __reduce_max_sync(kFull, t1);
-                const unsigned own = __ballot_sync(kFull, t1 == w3);
-                if (lane == __ffs(own) - 1) {
-                    t1 = t2;
-                    t2 = t3;
-                    t3 = 0;
-                }
-            }
-            if (lane == 0) rs.hist[warp] = w3;
-            if (threadIdx.x == 0) {
-                rs.sel[0] = 0;
-                rs.sel[3] = 0;
-            }
-            __syncthreads();
-            uint32_t L = 0xffffffffu;
-#pragma unroll
-            for (int w = 0; w < NTP / 32; ++w) L = min(L, rs.hist[w]);
+            // The hint: the a-th largest sampled key, a <= 48, among the
+            // keys at or above the per-warp top-3 bound (top3_bound).
+            const uint32_t L = top3_bound<NTP>(t1, t2, t3, rs);
             // warp-uniform trip count (the ballots need every lane); a lane's
             // four keys are all in range or all out (m is a multiple of 64)
             for (uint32_t w0 = 128u * warp; w0 < p.m; w0 += 128u * (NTP / 32)) {
                 const uint32_t i0 = w0 + 4u * lane;
                 const bool in = i0 < p.m;
                 const uint4 q4 = in ? *reinterpret_cast<const uint4*>(keys + i0) : make_uint4(0u, 0u, 0u, 0u);
-                const uint32_t kk[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const bool hit = in && kk[j] >= L;
-                    const unsigned mk = __ballot_sync(kFull, hit);
-                    if (mk) {
-                        uint32_t at = 0;
-                        if (lane == 0) at = atomicAdd(&rs.sel[3], (uint32_t)__popc(mk));
-                        at = __shfl_sync(kFull, at, 0);
-                        const uint32_t slot = at + __popc(mk & ((1u << lane) - 1u));
-                        if (hit && slot < (uint32_t)kCandMax) rs.cand[slot] = kk[j];
-                    }
-                }
+                cand_append(rs, q4.x, in && q4.x >= L);
+                cand_append(rs, q4.y, in && q4.y >= L);
+                cand_append(rs, q4.z, in && q4.z >= L);
+                cand_append(rs, q4.w, in && q4.w >= L);
             }
             __syncthreads();
             const uint32_t c = rs.sel[3];
             uint32_t h = 0;
             if (c <= (uint32_t)NTP) {
-                // rank of candidate j: keys above it, plus equal keys before it
-                if (threadIdx.x < c) {
-                    const uint32_t mine = rs.cand[threadIdx.x];
-                    uint32_t rank = 0;
-                    for (uint32_t i = 0; i < c; ++i) {
-                        const uint32_t o = rs.cand[i];
-                        rank += o > mine || (o == mine && i < threadIdx.x);
-                    }
-                    if (rank == p.a - 1) rs.sel[0] = mine;
-                }
-                __syncthreads();
-                h = rs.sel[0];
+                h = rank_select<NTP>(rs, c, p.a).thresh;
             } else if (c <= (uint32_t)kCandMax) {
                 h = radix_select_desc<NTP, 3>([&](uint64_t i, uint32_t* key) { *key = rs.cand[i]; return true; },
                                               c, p.a, rs, false, keys + p.m, kSampleMax - p.m)
@@ -954,8 +897,7 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
         return;
     }
     if (!pool_ok && p.n <= kRawMax) {
-        // kRawMax = 8 float4 per thread: issue every load before the first store
-        radix_hist_clear<NTS>(rs);
+        // kRawMax = 4 float4 per thread: issue every load before the first store
         const bool aligned = ((uintptr_t)vseg & 15) == 0;
         float4 q[kRawMax / (4 * NTS)];
 #pragma unroll
@@ -981,6 +923,37 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
                 if (e0 + 2 < p.n) stagef[e0 + 2] = q[r].z;
             }
         }
+        __syncthreads();
+        auto emit_stage = [&](uint32_t T, uint32_t ties) {
+            emit_in_order(
+                [&](uint32_t i, uint32_t* loc, uint32_t* bits) {
+                    *loc = i;
+                    *bits = __float_as_uint(stagef[i]);
+                },
+                p.n, T, ties, p, dst, u, v, ebase, wsum);
+        };
+        if (p.k <= 48) {  // a small top: the top-3 bound and an exact rank, no histogram
+            // rolled loops over the staged keys: a CTA runs each phase once, and
+            // unrolled it would be long straight-line code fetched line by line
+            uint32_t t1 = 0, t2 = 0, t3 = 0;
+#pragma unroll 1
+            for (uint32_t i = threadIdx.x; i < p.n; i += NTS) top3_insert(mag_key(stagef[i]), t1, t2, t3);
+            const uint32_t L = top3_bound<NTS>(t1, t2, t3, rs);
+#pragma unroll 1
+            for (uint32_t i0 = 0; i0 < p.n; i0 += NTS) {  // CTA-uniform trip count (cand_append is warp-wide)
+                const uint32_t i = i0 + threadIdx.x;
+                const uint32_t key = i < p.n ? mag_key(stagef[i]) : 0u;
+                cand_append(rs, key, i < p.n && key >= L);
+            }
+            __syncthreads();
+            const uint32_t c = rs.sel[3];
+            if (c <= (uint32_t)NTS) {
+                const SelectResult r = rank_select<NTS>(rs, c, p.k);
+                emit_stage(r.thresh, r.ties);
+                return;
+            }
+        }
+        radix_hist_clear<NTS>(rs);
         __syncthreads();  // the histogram is clear everywhere before any count
 #pragma unroll
         for (int r = 0; r < (int)(kRawMax / (4 * NTS)); ++r) {
@@ -993,12 +966,7 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
         __syncthreads();
         const SelectResult r = radix_select_desc<NTS, 3>(
             [&](uint64_t i, uint32_t* key) { *key = mag_key(stagef[i]); return true; }, p.n, p.k, rs, true);
-        emit_in_order(
-            [&](uint32_t i, uint32_t* loc, uint32_t* bits) {
-                *loc = i;
-                *bits = __float_as_uint(stagef[i]);
-            },
-            p.n, r.thresh, r.ties, p, dst, u, v, ebase, wsum);
+        emit_stage(r.thresh, r.ties);
         return;
     }
     if (!pool_ok) {

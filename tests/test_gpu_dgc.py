@@ -126,11 +126,11 @@ def test_hint_above_the_kth_value_falls_back(cuda_lib):
     hint is 3.0 and only a < k entries qualify), the other sampled values 1.0
     (ties), some unsampled ones 0.5, the rest tiny.  The select must fall
     back to the whole segment and still be exact.  (The sample layout mirrors
-    the kernel's plan: R = max(2 k, 512), m = min(48 n / R, 16384) rounded
+    the kernel's plan: R = max(2.5 k, 512), m = min(48 n / R, 16384) rounded
     down to 64, blocks of 64 at stride n / (m / 64), a = round(R m / n).)"""
     n, density = 40000, 0.003
     k = oracle.dgc_k(density, n)
-    R = max(2 * k, 512)
+    R = max(5 * k // 2, 512)
     m = min(48 * n // R, 16384) & ~63
     nblk, stride = m // 64, n // (m // 64)
     a = (R * m + n // 2) // n
