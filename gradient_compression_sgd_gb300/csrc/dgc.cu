@@ -55,6 +55,7 @@ constexpr uint32_t kSampleBlock = 64;    // consecutive values per sample block
 constexpr uint32_t kPoolFloor = 512;     // smallest expected candidate count
 constexpr uint32_t kStageItems = 10240;  // candidates dgc_select stages in shared memory (80 KB)
 constexpr int kChunkTiles = 2 * NTS;     // tile-table entries dgc_select scans per round
+static_assert(kChunkTiles <= kCandMax, "the crowded-tile list lives in the radix scratch");
 constexpr size_t kStageBytes = kStageItems * sizeof(uint2);  // also holds kRawMax floats
 static_assert(kStageBytes >= kRawMax * sizeof(float), "the stage must hold a raw segment");
 constexpr int kSumsqBlocks = 512;        // CTAs per learner in dgc_sumsq
@@ -788,6 +789,7 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
                 ent[j] = jt < p.ntiles ? tt[jt] : make_uint2(0u, 0u);
                 c += ent[j].y;
             }
+            if (threadIdx.x == 0) rs.sel[3] = 0;  // tiles with many candidates, tagged by warps below
             uint64_t tot;
             uint32_t ex = (uint32_t)block_exclusive_scan<NTS>(c, rs.scan, &tot);
 #pragma unroll
@@ -795,8 +797,21 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
                 const uint32_t lt = TPT * threadIdx.x + j;
                 toff[lt] = ex;
                 tbase[lt] = ent[j].x;
-                for (uint32_t i = 0; i < ent[j].y && run + ex + i < kStageItems; ++i) stage[run + ex + i].x = lt;
+                if (ent[j].y <= 16) {
+                    for (uint32_t i = 0; i < ent[j].y && run + ex + i < kStageItems; ++i) stage[run + ex + i].x = lt;
+                } else {
+                    rs.cand[atomicAdd(&rs.sel[3], 1u)] = lt;  // kChunkTiles <= kCandMax slots
+                }
                 ex += ent[j].y;
+            }
+            __syncthreads();
+            {  // a warp per crowded tile tags its slots
+                const uint32_t nbig = rs.sel[3], lane = threadIdx.x & 31;
+                for (uint32_t b = threadIdx.x >> 5; b < nbig; b += NTS / 32) {
+                    const uint32_t lt = rs.cand[b], o = toff[lt];
+                    const uint32_t cnt = (lt + 1 < (uint32_t)kChunkTiles ? toff[lt + 1] : (uint32_t)tot) - o;
+                    for (uint32_t i = lane; i < cnt && run + o + i < kStageItems; i += 32) stage[run + o + i].x = lt;
+                }
             }
             __syncthreads();
             const uint32_t total = (uint32_t)tot;
