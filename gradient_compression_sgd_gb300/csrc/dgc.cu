@@ -36,6 +36,8 @@
 #include <algorithm>
 #include <vector>
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "dgc.cuh"
 
@@ -563,7 +565,8 @@ __global__ void __launch_bounds__(NT, 3) dgc_update(const SegPlan* __restrict__ 
 
 // Ordered emission over `count` items given in ascending index order: an
 // item is sent if its key > T, or == T and fewer than `ties` equal keys
-// precede it; its slot is (#greater before it) + min(#equal before it, ties).
+// precede it; its slot is slot0 + (#greater before it) + min(#equal before
+// it, ties).
 // Sent items are written to dst and u = v = 0 at their indices (momentum
 // factor masking).  Warp w owns one contiguous run of the items: a first
 // sweep counts its greater and equal keys (warp ballots), one barrier shares
@@ -572,7 +575,7 @@ __global__ void __launch_bounds__(NT, 3) dgc_update(const SegPlan* __restrict__ 
 template <class Get>
 __device__ void emit_in_order(Get get, uint32_t count, uint32_t T, uint32_t ties, const SegPlan& p,
                               gcsgd_pair* __restrict__ dst, float* __restrict__ u, float* __restrict__ v,
-                              uint64_t ebase, uint2* wsum) {
+                              uint64_t ebase, uint2* wsum, uint32_t slot0 = 0) {
     constexpr uint32_t NW = NTS / 32;
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t per = (count + NW * 32 - 1) / (NW * 32) * 32;  // items per warp, a multiple of 32
@@ -605,7 +608,7 @@ __device__ void emit_in_order(Get get, uint32_t count, uint32_t T, uint32_t ties
             const bool gt = i < hi && key > T, eq = i < hi && key == T;
             const unsigned mg = __ballot_sync(kFull, gt), me = __ballot_sync(kFull, eq);
             const uint32_t g_before = gb + __popc(mg & below), e_before = eb + __popc(me & below);
-            const uint32_t slot = g_before + (e_before < ties ? e_before : ties);
+            const uint32_t slot = slot0 + g_before + (e_before < ties ? e_before : ties);
             if ((gt || (eq && e_before < ties)) && slot < p.k && loc < p.n) {
                 gcsgd_pair pr;
                 pr.idx = p.off + loc;
@@ -723,8 +726,124 @@ __device__ void small_topk(const SegPlan& p, const float* __restrict__ vseg, flo
     }
 }
 
-// One CTA per (learner, segment): exact top-k and ordered emission.
-// Sources, fastest first:
+// Stages the candidates of tiles [t_begin, t_end) of a pool in index order
+// (tiles in order, items of a tile in order) at stage[0 ..), noting the range
+// of their keys in kmin/kmax (this thread's share).  Per chunk of tiles: a
+// block scan of the tile counts gives each tile's stage offset; every tile
+// writes its own (chunk-local) index into the stage slots it owns (a warp
+// per tile holding more than 16); then every thread gathers its slots'
+// items, eight loads in flight, reading the tile from the slot.  The caller
+// guarantees at most kStageItems items.  Returns the items staged.  Every
+// thread must call it; ends synchronised.
+__device__ uint32_t stage_tiles(const uint2* __restrict__ tt, uint32_t t_begin, uint32_t t_end,
+                                const uint2* __restrict__ items, uint2* stage, uint32_t* toff, uint32_t* tbase,
+                                RadixSmem& rs, uint32_t& kmin, uint32_t& kmax) {
+    uint32_t run = 0;
+    for (uint32_t tb = t_begin; tb < t_end; tb += kChunkTiles) {
+        constexpr int TPT = kChunkTiles / NTS;  // tiles per thread
+        uint2 ent[TPT];
+        uint32_t c = 0;
+#pragma unroll
+        for (int j = 0; j < TPT; ++j) {
+            const uint32_t jt = tb + TPT * threadIdx.x + j;
+            ent[j] = jt < t_end ? tt[jt] : make_uint2(0u, 0u);
+            c += ent[j].y;
+        }
+        if (threadIdx.x == 0) rs.sel[3] = 0;  // tiles with many candidates, tagged by warps below
+        uint64_t tot;
+        uint32_t ex = (uint32_t)block_exclusive_scan<NTS>(c, rs.scan, &tot);
+#pragma unroll
+        for (int j = 0; j < TPT; ++j) {
+            const uint32_t lt = TPT * threadIdx.x + j;
+            toff[lt] = ex;
+            tbase[lt] = ent[j].x;
+            if (ent[j].y <= 16) {
+                for (uint32_t i = 0; i < ent[j].y && run + ex + i < kStageItems; ++i) stage[run + ex + i].x = lt;
+            } else {
+                rs.cand[atomicAdd(&rs.sel[3], 1u)] = lt;  // kChunkTiles <= kCandMax slots
+            }
+            ex += ent[j].y;
+        }
+        __syncthreads();
+        {  // a warp per crowded tile tags its slots
+            const uint32_t nbig = rs.sel[3], lane = threadIdx.x & 31;
+            for (uint32_t b = threadIdx.x >> 5; b < nbig; b += NTS / 32) {
+                const uint32_t lt = rs.cand[b], o = toff[lt];
+                const uint32_t cnt = (lt + 1 < (uint32_t)kChunkTiles ? toff[lt + 1] : (uint32_t)tot) - o;
+                for (uint32_t i = lane; i < cnt && run + o + i < kStageItems; i += 32) stage[run + o + i].x = lt;
+            }
+        }
+        __syncthreads();
+        const uint32_t total = (uint32_t)tot;
+        constexpr int IPT = 8;
+        for (uint32_t q0 = 0; q0 < total; q0 += IPT * NTS) {
+            uint2 it[IPT];
+#pragma unroll
+            for (int jj = 0; jj < IPT; ++jj) {
+                const uint32_t q = q0 + jj * NTS + threadIdx.x;
+                it[jj] = make_uint2(0u, 0u);
+                if (q < total && run + q < kStageItems) {
+                    const uint32_t lt = stage[run + q].x;
+                    it[jj] = items[tbase[lt] + (q - toff[lt])];
+                }
+            }
+#pragma unroll
+            for (int jj = 0; jj < IPT; ++jj) {
+                const uint32_t q = q0 + jj * NTS + threadIdx.x;
+                if (q < total && run + q < kStageItems) {
+                    stage[run + q] = it[jj];
+                    const uint32_t key = it[jj].y & 0x7fffffffu;
+                    kmin = min(kmin, key);
+                    kmax = max(kmax, key);
+                }
+            }
+        }
+        run += total;
+        __syncthreads();
+    }
+    return run;
+}
+
+// Arguments of dgc_select and dgc_select_big.
+struct SelectArgs {
+    const SegPlan* plan;
+    int S;
+    uint64_t N;
+    uint32_t tiles_per_learner;
+    float* u;
+    float* v;
+    const uint32_t* pool_cnt;
+    const uint2* tile_tab;
+    const uint2* pool;
+    uint64_t pool_per_learner;
+    gcsgd_pair* out;
+    uint64_t cap;
+    int64_t* counts;
+    int64_t* totals;
+    uint32_t out_per_learner;
+    const uint16_t* order;
+    int K;
+    int sampled;
+};
+
+// Shared memory of one selecting CTA.
+struct SelectSmem {
+    unsigned char* stage_raw;  // kStageBytes, dynamic
+    RadixSmem* rs;
+    uint32_t* toff;  // [kChunkTiles]
+    uint32_t* tbase;  // [kChunkTiles]
+    uint2* wsum;  // [NTS / 32]
+};
+
+// Pools whose expected candidate count (about cap / 4) is too large for one
+// CTA's stage go to dgc_select_big; a smaller pool that happens to outgrow
+// the stage is read from global memory by select_unit.
+__host__ __device__ __forceinline__ bool big_pool(const SegPlan& p) {
+    return p.kind == kKindPool && p.cap > 4 * kStageItems;
+}
+
+// The exact top-k and ordered emission of unit (learner k, segment s) by
+// one CTA.  Sources, fastest first:
 //   pool, staged  -- the candidates (k <= count <= pool capacity, so they hold
 //                    the whole top k), copied tile by tile in index order into
 //                    shared memory when they fit (kStageItems);
@@ -734,34 +853,34 @@ __device__ void small_topk(const SegPlan& p, const float* __restrict__ vseg, flo
 //                    shared memory;
 //   global        -- anything else (a failed hint, or more candidates than
 //                    fit): the same selection read from global memory.
-__global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__ plan, int S, uint64_t N,
-                                                  uint32_t tiles_per_learner, float* __restrict__ u,
-                                                  float* __restrict__ v, const uint32_t* __restrict__ pool_cnt,
-                                                  const uint2* __restrict__ tile_tab, const uint2* __restrict__ pool,
-                                                  uint64_t pool_per_learner, gcsgd_pair* __restrict__ out,
-                                                  uint64_t cap, int64_t* __restrict__ counts,
-                                                  int64_t* __restrict__ totals, uint32_t out_per_learner,
-                                                  const uint16_t* __restrict__ order, int K, int sampled) {
-    extern __shared__ __align__(16) unsigned char stage_raw[];  // kStageBytes
+__device__ void select_unit(const SelectArgs& A, const SelectSmem& M, int k, int s) {
+    const SegPlan* __restrict__ plan = A.plan;
+    const int S = A.S;
+    const uint64_t N = A.N;
+    const uint32_t tiles_per_learner = A.tiles_per_learner;
+    float* __restrict__ u = A.u;
+    float* __restrict__ v = A.v;
+    const uint32_t* __restrict__ pool_cnt = A.pool_cnt;
+    const uint2* __restrict__ tile_tab = A.tile_tab;
+    const uint2* __restrict__ pool = A.pool;
+    const uint64_t pool_per_learner = A.pool_per_learner;
+    gcsgd_pair* __restrict__ out = A.out;
+    const uint64_t cap = A.cap;
+    int64_t* __restrict__ counts = A.counts;
+    unsigned char* stage_raw = M.stage_raw;
     uint2* stage = reinterpret_cast<uint2*>(stage_raw);
     float* stagef = reinterpret_cast<float*>(stage_raw);
-    __shared__ RadixSmem rs;
-    __shared__ uint32_t toff[kChunkTiles];
-    __shared__ uint32_t tbase[kChunkTiles];
-    __shared__ uint2 wsum[NTS / 32];
-    // largest segments first, every learner's copy of a segment together
-    const int k = (int)blockIdx.x % K;
-    const int s = order[(int)blockIdx.x / K];
+    RadixSmem& rs = *M.rs;
+    uint32_t* toff = M.toff;
+    uint32_t* tbase = M.tbase;
+    uint2* wsum = M.wsum;
     const int unit = k * S + s;
     const SegPlan p = plan[s];
     const uint32_t pc = p.kind == kKindPool ? pool_cnt[unit] : 0;
     // sampled threshold, fewer than k above it: every candidate is sent
     const bool take_all = p.kind == kKindPool && p.sampled && pc < p.k;
     const bool raw_sampled = p.kind == kKindRaw && p.sampled;  // counted once tau is known
-    if (threadIdx.x == 0) {
-        if (!raw_sampled) counts[unit] = take_all ? pc : p.k;
-        if (s == 0 && totals && !sampled) totals[k] = out_per_learner;
-    }
+    if (threadIdx.x == 0 && !raw_sampled) counts[unit] = take_all ? pc : p.k;
     if (p.k == 0) return;
     const uint64_t ebase = (uint64_t)k * N + p.off;
     const bool pool_ok = p.kind == kKindPool && (pc >= p.k || take_all) && pc <= p.cap;
@@ -771,76 +890,8 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
     gcsgd_pair* dst = out + (uint64_t)k * cap + p.out_off;
 
     if (pool_ok && pc <= kStageItems) {
-        // Stage the candidates in index order (tiles in order, items of a
-        // tile in order), noting the range of their keys on the way.  Per
-        // chunk of tiles: a block scan of the tile counts gives each tile's
-        // stage offset; every tile writes its own (chunk-local) index into
-        // the stage slots it owns; then every thread gathers its slots'
-        // items, eight loads in flight, reading the tile from the slot.
         uint32_t kmin = 0xffffffffu, kmax = 0;
-        uint32_t run = 0;
-        for (uint32_t tb = 0; tb < p.ntiles; tb += kChunkTiles) {
-            constexpr int TPT = kChunkTiles / NTS;  // tiles per thread
-            uint2 ent[TPT];
-            uint32_t c = 0;
-#pragma unroll
-            for (int j = 0; j < TPT; ++j) {
-                const uint32_t jt = tb + TPT * threadIdx.x + j;
-                ent[j] = jt < p.ntiles ? tt[jt] : make_uint2(0u, 0u);
-                c += ent[j].y;
-            }
-            if (threadIdx.x == 0) rs.sel[3] = 0;  // tiles with many candidates, tagged by warps below
-            uint64_t tot;
-            uint32_t ex = (uint32_t)block_exclusive_scan<NTS>(c, rs.scan, &tot);
-#pragma unroll
-            for (int j = 0; j < TPT; ++j) {
-                const uint32_t lt = TPT * threadIdx.x + j;
-                toff[lt] = ex;
-                tbase[lt] = ent[j].x;
-                if (ent[j].y <= 16) {
-                    for (uint32_t i = 0; i < ent[j].y && run + ex + i < kStageItems; ++i) stage[run + ex + i].x = lt;
-                } else {
-                    rs.cand[atomicAdd(&rs.sel[3], 1u)] = lt;  // kChunkTiles <= kCandMax slots
-                }
-                ex += ent[j].y;
-            }
-            __syncthreads();
-            {  // a warp per crowded tile tags its slots
-                const uint32_t nbig = rs.sel[3], lane = threadIdx.x & 31;
-                for (uint32_t b = threadIdx.x >> 5; b < nbig; b += NTS / 32) {
-                    const uint32_t lt = rs.cand[b], o = toff[lt];
-                    const uint32_t cnt = (lt + 1 < (uint32_t)kChunkTiles ? toff[lt + 1] : (uint32_t)tot) - o;
-                    for (uint32_t i = lane; i < cnt && run + o + i < kStageItems; i += 32) stage[run + o + i].x = lt;
-                }
-            }
-            __syncthreads();
-            const uint32_t total = (uint32_t)tot;
-            constexpr int IPT = 8;
-            for (uint32_t q0 = 0; q0 < total; q0 += IPT * NTS) {
-                uint2 it[IPT];
-#pragma unroll
-                for (int jj = 0; jj < IPT; ++jj) {
-                    const uint32_t q = q0 + jj * NTS + threadIdx.x;
-                    it[jj] = make_uint2(0u, 0u);
-                    if (q < total && run + q < kStageItems) {
-                        const uint32_t lt = stage[run + q].x;
-                        it[jj] = items[tbase[lt] + (q - toff[lt])];
-                    }
-                }
-#pragma unroll
-                for (int jj = 0; jj < IPT; ++jj) {
-                    const uint32_t q = q0 + jj * NTS + threadIdx.x;
-                    if (q < total && run + q < kStageItems) {
-                        stage[run + q] = it[jj];
-                        const uint32_t key = it[jj].y & 0x7fffffffu;
-                        kmin = min(kmin, key);
-                        kmax = max(kmax, key);
-                    }
-                }
-            }
-            run += total;
-            __syncthreads();
-        }
+        stage_tiles(tt, 0, p.ntiles, items, stage, toff, tbase, rs, kmin, kmax);
         uint32_t T = 0, ties = pc;  // take_all: every key >= 0 goes, in index order
         if (!take_all) {
             // the candidates share their leading bits (all sit just above the
@@ -1086,6 +1137,284 @@ __global__ void __launch_bounds__(NTS, 2) dgc_select(const SegPlan* __restrict__
     }
 }
 
+// One CTA per (learner, segment), largest segments first, every learner's
+// copy of a segment together; pools too large for the stage are left to
+// dgc_select_big.
+__global__ void __launch_bounds__(NTS, 2) dgc_select(SelectArgs A) {
+    extern __shared__ __align__(16) unsigned char stage_raw[];  // kStageBytes
+    __shared__ RadixSmem rs;
+    __shared__ uint32_t toff[kChunkTiles];
+    __shared__ uint32_t tbase[kChunkTiles];
+    __shared__ uint2 wsum[NTS / 32];
+    const int k = (int)blockIdx.x % A.K;
+    const int s = A.order[(int)blockIdx.x / A.K];
+    if (threadIdx.x == 0 && s == 0 && A.totals && !A.sampled) A.totals[k] = A.out_per_learner;
+    if (big_pool(A.plan[s])) return;
+    const SelectSmem M = {stage_raw, &rs, toff, tbase, wsum};
+    select_unit(A, M, k, s);
+}
+
+// ------------------------------------------------------- large pools
+//
+// Pools whose capacity exceeds one CTA's stage (more than kStageItems
+// candidates possible) are selected by a thread-block cluster of
+// kClusterCTAs CTAs, one cluster per (learner, segment).  CTA r stages the
+// candidates of its share of the tiles (index order, so the cluster holds
+// the pool in index order across its ranks), and the cluster then runs the
+// range-adaptive radix select of select_unit with distributed shared memory:
+// every rank histograms its own keys, rank 0 adds the kClusterCTAs
+// histograms and picks the bucket, every rank appends that bucket's keys to
+// rank 0's candidate buffer, and rank 0 finishes the selection (exact rank or
+// more digits).  Each rank then emits its own items at slots offset by the
+// greater and tied items of the ranks before it.  A pool the cluster cannot
+// stage (a rank's share above kStageItems, a failed hint, an overflow) is
+// selected by rank 0 alone through select_unit's global paths.
+namespace cg = cooperative_groups;
+constexpr int kClusterCTAs = 8;
+
+template <int MAXS>
+struct BigList {
+    uint32_t n;
+    uint16_t seg[MAXS];  // segments whose pools go to dgc_select_big
+};
+
+// Per-rank words of the cluster exchange (each rank's own shared memory,
+// read by the others through distributed shared memory).
+struct ClusterXch {
+    uint32_t cnt, kmin, kmax, ngt, neq;  // this rank's items, key range, emission counts
+    uint32_t bucket, above, bcnt;        // rank 0: the pass's pick
+    uint32_t T, ties;                    // rank 0: the selection's result
+};
+
+template <int MAXS>
+__global__ void __cluster_dims__(kClusterCTAs, 1, 1) __launch_bounds__(NTS, 2)
+    dgc_select_big(SelectArgs A, BigList<MAXS> big) {
+    extern __shared__ __align__(16) unsigned char stage_raw[];  // kStageBytes
+    __shared__ RadixSmem rs;
+    __shared__ uint32_t toff[kChunkTiles];
+    __shared__ uint32_t tbase[kChunkTiles];
+    __shared__ uint2 wsum[NTS / 32];
+    __shared__ ClusterXch xch;
+    __shared__ uint32_t red[NTS / 32][2];
+    cg::cluster_group cl = cg::this_cluster();
+    const uint32_t r = cl.block_rank();
+    const int c = (int)(blockIdx.x / kClusterCTAs);
+    const int k = c % A.K;
+    const int s = big.seg[c / A.K];
+    const SegPlan p = A.plan[s];
+    const SelectSmem M = {stage_raw, &rs, toff, tbase, wsum};
+    uint2* stage = reinterpret_cast<uint2*>(stage_raw);
+    const int unit = k * A.S + s;
+    const uint32_t pc = A.pool_cnt[unit];
+    const bool take_all = p.sampled && pc < p.k;
+    const bool pool_ok = (pc >= p.k || take_all) && pc <= p.cap;
+    const uint2* tt = A.tile_tab + (uint64_t)k * A.tiles_per_learner + p.tile_off;
+    const uint2* items = A.pool + (uint64_t)k * A.pool_per_learner + p.pool_off;
+    const uint32_t t0 = (uint32_t)((uint64_t)r * p.ntiles / kClusterCTAs);
+    const uint32_t t1 = (uint32_t)((uint64_t)(r + 1) * p.ntiles / kClusterCTAs);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+    // block sums of two words (warp shuffles, then one word per warp)
+    auto block_sum2 = [&](uint32_t a, uint32_t b, uint32_t* ta, uint32_t* tb) {
+        a = __reduce_add_sync(kFull, a);
+        b = __reduce_add_sync(kFull, b);
+        if (lane == 0) {
+            red[warp][0] = a;
+            red[warp][1] = b;
+        }
+        __syncthreads();
+        uint32_t sa = 0, sb = 0;
+#pragma unroll
+        for (int w = 0; w < NTS / 32; ++w) {
+            sa += red[w][0];
+            sb += red[w][1];
+        }
+        *ta = sa;
+        *tb = sb;
+        __syncthreads();
+    };
+
+    // this rank's share of the candidates
+    uint32_t mine = 0;
+    if (pool_ok)
+        for (uint32_t t = t0 + threadIdx.x; t < t1; t += NTS) mine += tt[t].y;
+    uint32_t my_cnt, unused;
+    block_sum2(mine, 0u, &my_cnt, &unused);
+    if (threadIdx.x == 0) xch.cnt = my_cnt;
+    cl.sync();
+    bool fits = pool_ok;
+    for (int q = 0; q < kClusterCTAs; ++q) fits = fits && cl.map_shared_rank(&xch, q)->cnt <= kStageItems;
+    cl.sync();  // every rank has read the counts before any rank leaves
+    if (!fits) {
+        if (r == 0) select_unit(A, M, k, s);
+        return;
+    }
+    if (r == 0 && threadIdx.x == 0) A.counts[unit] = take_all ? pc : p.k;
+    if (p.k == 0) return;  // uniform: every rank leaves (no later cluster barrier)
+
+    // stage this rank's items; the cluster's key range
+    uint32_t kmin = 0xffffffffu, kmax = 0;
+    const uint32_t cnt = stage_tiles(tt, t0, t1, items, stage, toff, tbase, rs, kmin, kmax);
+    kmin = __reduce_min_sync(kFull, kmin);
+    kmax = __reduce_max_sync(kFull, kmax);
+    if (lane == 0) {
+        red[warp][0] = kmin;
+        red[warp][1] = kmax;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t a = 0xffffffffu, b = 0;
+        for (int w = 0; w < NTS / 32; ++w) {
+            a = min(a, red[w][0]);
+            b = max(b, red[w][1]);
+        }
+        xch.kmin = a;
+        xch.kmax = b;
+    }
+    cl.sync();
+    kmin = 0xffffffffu;
+    kmax = 0;
+    for (int q = 0; q < kClusterCTAs; ++q) {
+        const ClusterXch* o = cl.map_shared_rank(&xch, q);
+        kmin = min(kmin, o->kmin);
+        kmax = max(kmax, o->kmax);
+    }
+
+    uint32_t T = 0, ties = pc;  // take_all: every candidate goes
+    if (!take_all) {
+        // the range-adaptive radix select, distributed over the ranks
+        const uint32_t base = kmin;
+        int shift = kmax > kmin ? 32 - __clz(kmax - kmin) : 0;
+        uint32_t prefix = 0, pmask = 0, need = p.k, greater = 0;
+        bool done = false;
+#pragma unroll 1
+        for (int pass = 0; !done; ++pass) {
+            const int nshift = shift > 11 ? shift - 11 : 0;
+            const uint32_t dmask = (1u << (shift - nshift)) - 1u;
+            const int nb = (int)(dmask + 1) > NTS ? (int)(dmask + 1) : NTS;
+            for (int b = threadIdx.x; b < nb; b += NTS) rs.hist[b] = 0;
+            __syncthreads();
+#pragma unroll 1
+            for (uint32_t i = threadIdx.x; i < cnt; i += NTS) {
+                const uint32_t d = (stage[i].y & 0x7fffffffu) - base;
+                if ((d & pmask) == prefix) atomicAdd(&rs.hist[(d >> nshift) & dmask], 1u);
+            }
+            cl.sync();  // every rank's histogram is complete
+            if (r == 0) {
+                // totals into rs.cand (free until the compaction), then back into rs.hist
+                for (int b = threadIdx.x; b < nb; b += NTS) {
+                    uint32_t t = 0;
+                    for (int q = 0; q < kClusterCTAs; ++q) t += cl.map_shared_rank(rs.hist, q)[b];
+                    rs.cand[b] = t;
+                }
+            }
+            cl.sync();  // the other ranks' histograms have been read
+            if (r == 0) {
+                for (int b = threadIdx.x; b < nb; b += NTS) rs.hist[b] = rs.cand[b];
+                __syncthreads();
+                uint32_t b, ab, cb;
+                radix_pick<NTS>(rs, nb, need, &b, &ab, &cb);
+                if (threadIdx.x == 0) {
+                    xch.bucket = b;
+                    xch.above = ab;
+                    xch.bcnt = cb;
+                    rs.sel[3] = 0;  // the candidate buffer, empty
+                }
+            }
+            cl.sync();
+            {
+                const ClusterXch* o = cl.map_shared_rank(&xch, 0);
+                prefix |= o->bucket << nshift;
+                pmask |= dmask << nshift;
+                greater += o->above;
+                need -= o->above;
+                const uint32_t cb = o->bcnt;
+                shift = nshift;
+                if (shift == 0) {  // every digit taken: the bucket is the threshold
+                    T = base + prefix;
+                    ties = need;
+                    done = true;
+                } else if (cb <= (uint32_t)kCandMax) {
+                    // the bucket's keys (offsets from base) to rank 0, which finishes
+                    RadixSmem* rs0 = cl.map_shared_rank(&rs, 0);
+#pragma unroll 1
+                    for (uint32_t i0 = 0; i0 < cnt; i0 += NTS) {  // CTA-uniform trip count
+                        const uint32_t i = i0 + threadIdx.x;
+                        const uint32_t d = i < cnt ? (stage[i].y & 0x7fffffffu) - base : 0u;
+                        const bool hit = i < cnt && (d & pmask) == prefix;
+                        const unsigned m = __ballot_sync(kFull, hit);
+                        if (m) {
+                            uint32_t at = 0;
+                            if (lane == 0) at = atomicAdd(&rs0->sel[3], (uint32_t)__popc(m));
+                            at = __shfl_sync(kFull, at, 0);
+                            const uint32_t slot = at + __popc(m & ((1u << lane) - 1u));
+                            if (hit && slot < (uint32_t)kCandMax) rs0->cand[slot] = d;
+                        }
+                    }
+                    cl.sync();  // rank 0 holds the bucket's cb keys
+                    if (r == 0) {
+                        SelectResult sr;
+                        if (cb <= (uint32_t)NTS) {
+                            sr = rank_select<NTS>(rs, cb, need);  // offsets rank like keys
+                        } else {
+                            // keys in [base + prefix, base + prefix + 2^shift)
+                            sr = radix_select_span<NTS>(
+                                [&](uint32_t i, uint32_t* key) { *key = rs.cand[i] - prefix; }, cb, need, 0u, shift,
+                                rs, toff, (uint32_t)kChunkTiles);
+                            sr.thresh += prefix;
+                        }
+                        if (threadIdx.x == 0) {
+                            xch.T = base + sr.thresh;
+                            xch.ties = sr.ties;
+                        }
+                    }
+                    cl.sync();
+                    const ClusterXch* o0 = cl.map_shared_rank(&xch, 0);
+                    T = o0->T;
+                    ties = o0->ties;
+                    done = true;
+                }
+                // else another digit over the staged keys
+            }
+            cl.sync();  // rank 0's words have been read before the next pass rewrites them
+        }
+    }
+
+    // emission: this rank's items at slots after the ranks before it
+    uint32_t ngt = 0, neq = 0;
+#pragma unroll 1
+    for (uint32_t i = threadIdx.x; i < cnt; i += NTS) {
+        const uint32_t key = stage[i].y & 0x7fffffffu;
+        ngt += key > T;
+        neq += key == T;
+    }
+    uint32_t tg, te;
+    block_sum2(ngt, neq, &tg, &te);
+    if (threadIdx.x == 0) {
+        xch.ngt = tg;
+        xch.neq = te;
+    }
+    cl.sync();
+    uint32_t gb = 0, eb = 0;
+    for (uint32_t q = 0; q < r; ++q) {
+        const ClusterXch* o = cl.map_shared_rank(&xch, q);
+        gb += o->ngt;
+        eb += o->neq;
+    }
+    const uint32_t mine_ties = eb >= ties ? 0u : (ties - eb < te ? ties - eb : te);
+    const uint32_t slot0 = gb + (eb < ties ? eb : ties);
+    const uint64_t ebase = (uint64_t)k * A.N + p.off;
+    gcsgd_pair* dst = A.out + (uint64_t)k * A.cap + p.out_off;
+    emit_in_order(
+        [&](uint32_t i, uint32_t* loc, uint32_t* bits) {
+            const uint2 it = stage[i];
+            *loc = it.x;
+            *bits = it.y;
+        },
+        cnt, T, mine_ties, p, dst, A.u, A.v, ebase, wsum, slot0);
+    cl.sync();  // no rank leaves while another may still read its words
+}
+
 // Sampled threshold: the selection wrote tensor s's entries at its k_s-slot
 // region of the scratch list; each learner's list is packed to be contiguous
 // (tensors in order, a warp per tensor) and its total written.
@@ -1144,7 +1473,11 @@ static int dgc_set_smem_limits() {
         cudaFuncSetAttribute(dgc_prepare<GCSGD_MAX_SEGMENTS, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, ks) !=
             cudaSuccess ||
         cudaFuncSetAttribute(dgc_select, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStageBytes) !=
-            cudaSuccess)
+            cudaSuccess ||
+        cudaFuncSetAttribute(dgc_select_big<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStageBytes) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(dgc_select_big<GCSGD_MAX_SEGMENTS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kStageBytes) != cudaSuccess)
         return set_error(GCSGD_ERR_CUDA, "dgc_compress: cannot raise the shared-memory limit");
     done[dev] = true;
     return GCSGD_OK;
@@ -1234,10 +1567,38 @@ int dgc_launch(const int64_t* off, int S, int K, const float* grad, float* u, fl
         // the sampled threshold writes each tensor's entries into its k_s-slot region of the scratch list
         gcsgd_pair* dst = sampled ? w.msg : out;
         const uint64_t dst_stride = sampled ? hp.out_per_learner : (uint64_t)cap;
-        dgc_select<<<units, NTS, kStageBytes, stream>>>(w.plan, S, N, (uint32_t)hp.tiles_per_learner, u, v, w.pool_cnt,
-                                             w.tile_tab, w.pool, hp.pool_per_learner, dst, dst_stride, counts,
-                                             totals, (uint32_t)hp.out_per_learner, w.order, K, sampled ? 1 : 0);
+        SelectArgs A = {w.plan, S, N, (uint32_t)hp.tiles_per_learner, u, v, w.pool_cnt, w.tile_tab, w.pool,
+                        hp.pool_per_learner, dst, dst_stride, counts, totals, (uint32_t)hp.out_per_learner,
+                        w.order, K, sampled ? 1 : 0};
+        dgc_select<<<units, NTS, kStageBytes, stream>>>(A);
         if ((rc = check_launch("dgc_select"))) return rc;
+    }
+    {
+        // pools too large for one CTA's stage: a cluster per (learner, segment)
+        gcsgd_pair* dst = sampled ? w.msg : out;
+        const uint64_t dst_stride = sampled ? hp.out_per_learner : (uint64_t)cap;
+        SelectArgs A = {w.plan, S, N, (uint32_t)hp.tiles_per_learner, u, v, w.pool_cnt, w.tile_tab, w.pool,
+                        hp.pool_per_learner, dst, dst_stride, counts, totals, (uint32_t)hp.out_per_learner,
+                        w.order, K, sampled ? 1 : 0};
+        auto launch_big = [&](auto& bl, auto kernel) {
+            bl.n = 0;
+            for (int s = 0; s < S; ++s) {
+                SegPlan sp;
+                seg_fields((uint32_t)(off[s + 1] - off[s]), density, sample_frac, &sp);
+                if (big_pool(sp)) bl.seg[bl.n++] = (uint16_t)s;
+            }
+            if (bl.n == 0) return GCSGD_OK;
+            LaunchScope lb("dgc_select_big", stream);
+            kernel<<<(unsigned)K * bl.n * kClusterCTAs, NTS, kStageBytes, stream>>>(A, bl);
+            return check_launch("dgc_select_big");
+        };
+        if (S <= 256) {
+            BigList<256> bl;
+            if ((rc = launch_big(bl, dgc_select_big<256>))) return rc;
+        } else {
+            BigList<GCSGD_MAX_SEGMENTS> bl;
+            if ((rc = launch_big(bl, dgc_select_big<GCSGD_MAX_SEGMENTS>))) return rc;
+        }
     }
     if (sampled) {
         LaunchScope ls("dgc_pack", stream);
@@ -1272,7 +1633,8 @@ int dgc_collect_stats(const int64_t* off, int S, int K, double density, const vo
             if (p.kind == kKindEmpty) ++st->empty;
             else if (p.kind == kKindRaw) (p.n <= kRawMax ? st->raw : st->raw_global)++;
             else if (c < p.k || c > p.cap) ++st->hint_failed;
-            else (c <= kStageItems ? st->pool : st->pool_global)++;
+            else (c <= kStageItems || (big_pool(p) && c <= (uint32_t)kClusterCTAs * kStageItems) ? st->pool
+                                                                                                  : st->pool_global)++;
         }
     return GCSGD_OK;
 }

@@ -220,6 +220,55 @@ def test_async_on_side_stream(cuda_lib):
     assert int(totals[0]) == sum(gc.dgc_k(0.01, int(off[i + 1] - off[i])) for i in range(2))
 
 
+# ------------------------------------------- pools larger than one CTA's stage
+
+def test_big_pool_ties_across_cluster_ranks(cuda_lib):
+    """Pools of up to ~52K candidates are selected by a thread-block cluster,
+    each CTA holding an eighth of the tiles.  Values from a small discrete set
+    put thousands of exact ties at the k-th value, spread over every rank;
+    the ties must go to the lowest indices across ranks."""
+    rng = np.random.default_rng(21)
+    n, density = 1 << 21, 0.01  # k = 20972, expected candidates 52430: more than one stage
+    off = wl.layout_offsets([n, 5000])
+    grads = [(rng.integers(0, 200, size=(2, off[-1])) * 1e-3).astype(np.float32) for _ in range(2)]
+    run_dgc(cuda_lib, off, grads, density, 0.0)
+
+
+def test_big_pool_heavy_duplicates(cuda_lib):
+    """Most candidates share one value and one candidate is huge, so the key
+    range is wide and a single radix bucket holds far more keys than the
+    candidate buffer: every digit runs across the cluster until the last one
+    names the threshold, and the ties at 0.5 go to the lowest indices."""
+    rng = np.random.default_rng(22)
+    n, density = 3 << 20, 0.004  # k = 12583
+    G = np.full((1, n), 1e-4, np.float32)
+    G[0, rng.choice(n, 40000, replace=False)] = 0.5
+    G[0, rng.choice(n, 3000, replace=False)] = np.float32(0.5) * np.float32(1.0000001)
+    G[0, 12345] = 1e6
+    run_dgc(cuda_lib, [0, n], [G, G], density, 0.9)
+
+
+def test_big_pool_skewed_to_one_rank_falls_back(cuda_lib):
+    """Every candidate in the first eighth of the tiles: one rank's share is
+    above its stage, so the cluster's first CTA selects the pool alone."""
+    rng = np.random.default_rng(23)
+    n, density = 1 << 21, 0.01
+    G = (rng.standard_normal((1, n)) * 1e-6).astype(np.float32)
+    G[0, : n // 8] = (rng.standard_normal(n // 8) * 1.0).astype(np.float32)
+    d = run_dgc(cuda_lib, [0, n], [G], density, 0.9)
+    assert d.stats()["hint_failed"] == 0
+
+
+@pytest.mark.parametrize("frac", [0.01, 0.3])
+def test_big_pool_sampled_threshold(cuda_lib, frac):
+    """The sampled threshold on pools larger than one stage (the cluster also
+    sends every candidate when there are fewer than k)."""
+    rng = np.random.default_rng(int(frac * 100))
+    off = wl.layout_offsets([1 << 21, 3 << 19])
+    grads = [(rng.standard_normal((2, off[-1])) * 1e-3).astype(np.float32) for _ in range(2)]
+    run_dgc_sampled(cuda_lib, off, grads, 0.01, frac, 0.9)
+
+
 # ------------------------------------------------------- sampled threshold
 
 def run_dgc_sampled(gc, offsets, grads, density, frac, momentum, offset=0):
