@@ -311,7 +311,8 @@ def run_reference(args):
 
 
 def config_dict(w, **extra):
-    steps = {"dgc": "dgc_compress(K learners) + sparse_average", "adacomp": "adacomp_compress(K learners) + sparse_average",
+    steps = {"dgc": "dgc_compress(K learners) + sparse_average",
+             "adacomp": "adacomp_compress(K learners) + sparse_average_ws (cursor table + TMA-staged regions)",
              "dcd": "dcd_step(n ring nodes)"}
     d = {"workload": w.name, "learners": w.learners, "elements_per_learner": w.n, "segments": len(w.sizes),
          "step": steps[w.method],
@@ -411,12 +412,13 @@ class AdaCompPath(DgcPath):
         self.obj = gc.AdaComp(w.offsets, w.lt, self.K, self.N // 8, device=dev)
         self.state = [torch.zeros((self.K, self.N), device=dev)]
         self.avg = torch.empty(self.N, device=dev)
+        self.ws = torch.empty(gc.sparse_average_workspace_size(self.K, self.N), dtype=torch.uint8, device=dev)
 
     def step(self, g, state=None, t=0, res=None):
         (R,) = state or self.state
         out, totals = self.obj(g, R)
         res = self.avg if res is None else res
-        self.gc.sparse_average(out, totals, self.N, res)
+        self.gc.sparse_average_ws(out, totals, self.N, res, self.ws)
         return res
 
     def step_update(self, g, w, lr, state=None):

@@ -90,6 +90,9 @@ def lib():
         L.adacomp_compress.argtypes = [vp, i32, vp, i32, vp, vp, vp, i64, vp, vp, vp, vp, sz, vp]
         L.sparse_average.argtypes = [vp, i64, vp, i32, i64, vp, vp]
         L.sparse_average_update.argtypes = [vp, i64, vp, i32, i64, f32, vp, vp]
+        L.gcsgd_sparse_average_workspace_size.argtypes = [i32, i64, vp]
+        L.sparse_average_ws.argtypes = [vp, i64, vp, i32, i64, vp, vp, sz, vp]
+        L.gcsgd_sparse_average_status.argtypes = [vp, i32, i64, vp, vp]
         L.dcd_step.argtypes = [i32, i64, vp, vp, vp, f32, f64, u64, u32, vp]
         L.ecd_step.argtypes = [i32, i64, vp, vp, vp, vp, vp, f32, f64, u64, u32, vp]
         L.dcd_step_rows.argtypes = [i32, i64, i64, vp, vp, vp, f32, f64, u64, u32, vp, vp, i64, vp, vp]
@@ -393,6 +396,37 @@ def sparse_average(lists, counts, n: int, out, stream=None):
     _check("sparse_average", lib().sparse_average(
         _dev(lists, "lists", torch.int32), int(cap), _dev(counts, "counts", torch.int64), int(K), int(n),
         _dev(out, "out", torch.float32), _stream(stream)))
+
+
+def sparse_average_workspace_size(K: int, n: int) -> int:
+    """Bytes of workspace sparse_average_ws needs (see gcsgd_sparse_average_workspace_size in include/gcsgd.h)."""
+    b = ctypes.c_size_t(0)
+    _check("gcsgd_sparse_average_workspace_size",
+           lib().gcsgd_sparse_average_workspace_size(int(K), int(n), ctypes.byref(b)))
+    return int(b.value)
+
+
+def sparse_average_ws(lists, counts, n: int, out, workspace, stream=None):
+    """sparse_average through the cursor-table kernels; workspace: a uint8 device
+    tensor of at least sparse_average_workspace_size(K, n) bytes (see
+    sparse_average_ws in include/gcsgd.h)."""
+    import torch
+    K, cap = lists.shape[0], lists.shape[1]
+    if counts.numel() != K:
+        raise ValueError("counts must have K entries")
+    _check("sparse_average_ws", lib().sparse_average_ws(
+        _dev(lists, "lists", torch.int32), int(cap), _dev(counts, "counts", torch.int64), int(K), int(n),
+        _dev(out, "out", torch.float32), _dev(workspace, "workspace", torch.uint8), int(workspace.numel()),
+        _stream(stream)))
+
+
+def sparse_average_status(workspace, K: int, n: int, stream=None) -> int:
+    """Status word of the last sparse_average_ws call with this workspace, K and n
+    (0: every bulk copy completed); waits for the stream."""
+    st = ctypes.c_int32(-1)
+    _check("gcsgd_sparse_average_status", lib().gcsgd_sparse_average_status(
+        ctypes.c_void_p(workspace.data_ptr()), int(K), int(n), _stream(stream), ctypes.byref(st)))
+    return int(st.value)
 
 
 def sparse_average_update(lists, counts, n: int, lr: float, w, stream=None):

@@ -23,6 +23,10 @@ int adacomp_launch(const int64_t* off, int S, const int32_t* lt, int K, const fl
                    cudaStream_t stream);
 int spavg_launch(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int K, int64_t n, float* out,
                  cudaStream_t stream, bool update, float lr);
+size_t spavg_ws_bytes(int K, int64_t n);
+int spavg_ws_launch(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int K, int64_t n, float* out,
+                    void* ws, cudaStream_t stream);
+int spavg_ws_status(const void* ws, int K, int64_t n, cudaStream_t stream, int32_t* status);
 int dcd_launch(int n, int64_t d, const float* w, float* xhat, const float* grad, float gamma, double p, uint64_t seed,
                uint32_t t, cudaStream_t stream);
 int dcd_rows_launch(int rows, int64_t d, int64_t first_node, const float* w, float* xhat, const float* grad,
@@ -355,6 +359,37 @@ int sparse_average(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, 
     int rc = check_average("sparse_average", lists, cap, counts, K, n, out);
     if (rc) return rc;
     return spavg_launch(lists, cap, counts, K, n, out, (cudaStream_t)stream, false, 0.0f);
+}
+
+int gcsgd_sparse_average_workspace_size(int32_t K, int64_t n, size_t* bytes) {
+    if (K < 1 || K > 512) return set_error(GCSGD_ERR_INVALID_ARG, "gcsgd_sparse_average_workspace_size: K = %d outside [1, 512]", K);
+    if (n < 0 || n > ((int64_t)1 << 32))
+        return set_error(GCSGD_ERR_INVALID_ARG, "gcsgd_sparse_average_workspace_size: n outside [0, 2^32]");
+    if (!bytes) return set_error(GCSGD_ERR_INVALID_ARG, "gcsgd_sparse_average_workspace_size: bytes is NULL");
+    *bytes = spavg_ws_bytes(K, n);
+    return GCSGD_OK;
+}
+
+int sparse_average_ws(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int32_t K, int64_t n, float* out,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+    const char* fn = "sparse_average_ws";
+    int rc = check_average(fn, lists, cap, counts, K, n, out);
+    if (rc) return rc;
+    if (n == 0) return GCSGD_OK;
+    if (!workspace) return set_error(GCSGD_ERR_INVALID_ARG, "%s: workspace is NULL", fn);
+    if (((uintptr_t)workspace & 255) != 0) return set_error(GCSGD_ERR_INVALID_ARG, "%s: workspace not 256-byte aligned", fn);
+    if (workspace_bytes < spavg_ws_bytes(K, n))
+        return set_error(GCSGD_ERR_WORKSPACE, "%s: workspace of %zu bytes, %zu needed", fn, workspace_bytes,
+                         spavg_ws_bytes(K, n));
+    return spavg_ws_launch(lists, cap, counts, K, n, out, workspace, (cudaStream_t)stream);
+}
+
+int gcsgd_sparse_average_status(const void* workspace, int32_t K, int64_t n, void* stream, int32_t* status) {
+    const char* fn = "gcsgd_sparse_average_status";
+    if (K < 1 || K > 512) return set_error(GCSGD_ERR_INVALID_ARG, "%s: K = %d outside [1, 512]", fn, K);
+    if (n < 1 || n > ((int64_t)1 << 32)) return set_error(GCSGD_ERR_INVALID_ARG, "%s: n outside [1, 2^32]", fn);
+    if (!workspace || !status) return set_error(GCSGD_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+    return spavg_ws_status(workspace, K, n, (cudaStream_t)stream, status);
 }
 
 int sparse_average_update(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int32_t K, int64_t n,

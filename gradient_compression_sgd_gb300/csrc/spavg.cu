@@ -623,6 +623,466 @@ __global__ void __launch_bounds__(NT, 4) spavg_warp(const gcsgd_pair* __restrict
     }
 }
 
+
+// ---------------------------------------------------------------- regions
+// The dense average with a workspace (sparse_average_ws), in two kernels.
+//
+// spavg_checkpoints reads every 128th entry of every list and writes a
+// cursor table: lo[k][g] = 128 j for the last checkpoint j of list k whose
+// index is below g * kRegion (0 if none).  The first entry of list k at or
+// after region g then lies in [lo[k][g], lo[k][g] + 128], and every entry of
+// region g in [lo[k][g], lo[k][g+1] + 128).  (A 32-byte read brings in the
+// whole 128-byte line, so a denser table would cost far more list bytes.)
+//
+// spavg_region: CTA c takes the 4096-output regions c, c + grid, ... (every
+// CTA gets dense and sparse parts of the output alike).  One producer warp
+// plans each region (the list ranges from the table, their stage slots)
+// and copies the ranges into shared memory with TMA bulk copies (one per
+// list, 16-byte aligned; a first or last pair off that boundary by
+// cp.async), completing on an mbarrier, into one of two stage buffers: the
+// copies for the next region fly while the consumers add the current one.
+// Eight consumer warps add each list's staged entries into a shared
+// accumulator in learner order (a named barrier among them between lists;
+// a list's indices are distinct, so its adds never collide; entries outside
+// the region are skipped), release the buffer and write the region once.
+// A region whose ranges exceed a stage buffer is added straight from global
+// memory instead.
+constexpr uint32_t kRegion = 4096;        // outputs per region
+constexpr uint32_t kRStage = 6048;        // list entries per stage buffer
+constexpr uint32_t kCheck = 128;          // checkpoint stride of the cursor table
+constexpr uint32_t kSlow = 0xffffffffu;   // stage total of a region added from global memory
+constexpr uint32_t kSuspendNs = 20000;    // longest sleep of one barrier try
+constexpr uint64_t kWaitNs = 1000000000;  // a barrier phase not complete after 1 s counts as lost
+constexpr uint32_t kWaitLimit = 1u << 26; // tries, should the global timer not advance
+
+__device__ __forceinline__ uint32_t clamp_count(int64_t c, uint64_t cap) {
+    const uint64_t cc = c < 0 ? 0 : ((uint64_t)c > cap ? cap : (uint64_t)c);
+    return (uint32_t)(cc < 0xffffffffu ? cc : 0xffffffffu);
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// True once the phase with `parity` has completed; the warp sleeps (up to
+// kSuspendNs) while it has not, instead of spinning.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "n"(kSuspendNs)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
+
+// Waits until the phase with `parity` completes; false once kWaitNs have
+// passed (or kWaitLimit tries, should the clock not advance).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 0; it < kWaitLimit; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitNs) return false;
+    }
+    return false;
+}
+
+// Global -> shared bulk copy of `bytes` (multiple of 16, both addresses
+// 16-byte aligned), counted on `bar`.
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+
+// Cursor table lo[K][G+1] (G regions; lo[k][G] closes the last one).  Block
+// row y = list; blocks along x stride over the list's checkpoints.  For a
+// sorted list every lo[k][g] is written exactly once: checkpoint j (index a)
+// owns the regions g with a < g * kRegion <= the next checkpoint's index
+// (all regions up to G for the last checkpoint, from 0 for the first).
+// Block (0, 0) also clears the status word.
+__global__ void __launch_bounds__(NT) spavg_checkpoints(const gcsgd_pair* __restrict__ lists, uint64_t cap,
+                                                        const int64_t* __restrict__ counts, uint64_t G,
+                                                        uint32_t* __restrict__ lo, uint32_t* __restrict__ status) {
+    const int k = blockIdx.y;
+    const int lane = threadIdx.x & 31;
+    const uint32_t cnt = clamp_count(counts[k], cap);
+    const uint64_t J = (cnt + kCheck - 1) / kCheck;
+    uint32_t* row = lo + (uint64_t)k * (G + 1);
+    if (k == 0 && blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;
+    if (J == 0) {  // an empty list: every region starts at position 0
+        for (uint64_t g = (uint64_t)blockIdx.x * NT + threadIdx.x; g <= G; g += (uint64_t)gridDim.x * NT) row[g] = 0u;
+        return;
+    }
+    const gcsgd_pair* L = lists + (uint64_t)k * cap;
+    for (uint64_t j0 = (uint64_t)blockIdx.x * NT; j0 < J; j0 += (uint64_t)gridDim.x * NT) {  // uniform per block
+        const uint64_t j = j0 + threadIdx.x;
+        uint64_t g0 = 0, g1 = 0;  // this checkpoint's regions [g0, g1)
+        if (j < J) {
+            const uint64_t a = __ldg(&L[j * kCheck].idx);
+            g0 = j == 0 ? 0 : a / kRegion + 1;
+            g1 = j + 1 < J ? (uint64_t)__ldg(&L[(j + 1) * kCheck].idx) / kRegion + 1 : G + 1;
+            g0 = g0 < G + 1 ? g0 : G + 1;
+            g1 = g1 < G + 1 ? g1 : G + 1;
+            g1 = g1 > g0 ? g1 : g0;  // a checkpoint out of order (a malformed list) owns none
+        }
+        const uint32_t val = (uint32_t)(j * kCheck);
+        const bool many = g1 - g0 > 4;
+        if (!many)
+            for (uint64_t g = g0; g < g1; ++g) row[g] = val;
+        for (unsigned pend = __ballot_sync(kFull, many); pend; pend &= pend - 1u) {  // long runs: the warp writes them
+            const int src = __ffs(pend) - 1;
+            const uint64_t s0 = __shfl_sync(kFull, g0, src), s1 = __shfl_sync(kFull, g1, src);
+            const uint32_t v = __shfl_sync(kFull, val, src);
+            for (uint64_t g = s0 + lane; g < s1; g += 32) row[g] = v;
+        }
+    }
+}
+
+// Shared memory (dynamic): acc[kRegion] floats | stage[kNBuf][kRStage] pairs |
+// per buffer b: pa[K] (first list position of the range), pl[K] (its
+// length), pm[K] (staged slots, even, | 1 when the first pair is copied
+// alone), st[K] (stage slot of the first entry) | cnt[K].  Lists must be
+// 8-byte aligned.
+//
+// Warp kCW is the producer: for its CTA's regions in turn it waits until
+// the consumers have released the stage buffer (empty[b]), plans the
+// region's ranges and stage slots, and issues the copies, which complete
+// on full[b] (kFullArrivals arrivals: its expect-tx arrive plus one
+// cp.async arrive per lane, and the bulk-copied bytes).  Warps 0..kCW-1 are
+// the consumers: wait for full[b], add list by list (a named barrier among
+// them between lists), release the buffer, and store the region.  Every
+// wait is bounded; a wait that runs out sets the status word, and the
+// consumers leave together (their decision is reduced over all of them).
+constexpr int kCW = 8;                      // consumer warps
+constexpr int kProducer = kCW;
+constexpr int NTR = (kCW + 1) * 32;         // threads per CTA: consumers and one producer warp
+constexpr int kNBuf = 2;                    // stage buffers
+constexpr int kPer = 2;                     // entries per consumer thread and list read ahead
+constexpr uint32_t kFullArrivals = 33;      // producer lane 0's expect-tx arrive + 32 cp.async arrives
+
+__device__ __forceinline__ void mbar_init_n(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// One arrive on `bar` once every cp.async this thread issued so far has landed.
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;\n" ::"n"(kCW * 32) : "memory"); }
+
+// True iff p holds in every consumer thread (a named barrier among them).
+__device__ __forceinline__ bool consumers_all(bool p) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred q, a;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred a, 1, %2, q;\n selp.u32 %0, 1, 0, a;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)p), "n"(kCW * 32)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
+    for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(kFull, v, d);
+    return v;
+}
+
+// A list's range for a region from its table entries t_a = lo[k][g] and
+// t_b = lo[k][g+1]: the first position a, the length, whether the first
+// pair is copied alone (it sits 8 bytes off the 16-byte boundary), the
+// bulk-copied pairs and the staged slots (even; the first and last pairs
+// copied alone take slots of their own beside the bulk part).
+struct Range {
+    uint32_t a, len, head, body, slots;
+};
+
+__device__ __forceinline__ Range range_of(const gcsgd_pair* lists, uint64_t cap, uint32_t c, int k, uint32_t t_a,
+                                          uint32_t t_b) {
+    Range R;
+    R.a = t_a < c ? t_a : c;
+    const uint64_t e64 = (uint64_t)t_b + kCheck;
+    const uint32_t e0 = e64 < c ? (uint32_t)e64 : c;
+    R.len = e0 > R.a ? e0 - R.a : 0u;
+    const uintptr_t s = (uintptr_t)(lists + (uint64_t)k * cap + R.a);
+    R.head = R.len > 0 && (s & 8) ? 1u : 0u;
+    const uintptr_t bs = s + 8 * R.head, be = (s + 8 * (uintptr_t)R.len) & ~(uintptr_t)15;
+    R.body = be > bs ? (uint32_t)((be - bs) / 8) : 0u;
+    R.slots = (2 * R.head + R.body + (R.len - R.head - R.body) + 1) & ~1u;
+    return R;
+}
+
+__global__ void __launch_bounds__(NTR, 2) spavg_region(const gcsgd_pair* __restrict__ lists, uint64_t cap,
+                                                    const int64_t* __restrict__ counts, int K, uint64_t n,
+                                                    float* __restrict__ out, const uint32_t* __restrict__ lo,
+                                                    uint64_t G, uint32_t* __restrict__ status) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    float* acc = reinterpret_cast<float*>(smem);
+    gcsgd_pair* stage = reinterpret_cast<gcsgd_pair*>(smem + kRegion * sizeof(float));
+    uint32_t* arr = reinterpret_cast<uint32_t*>(stage + kNBuf * kRStage);
+    uint32_t* cnt = arr + 4 * kNBuf * K;
+    __shared__ __align__(8) uint64_t full[kNBuf], empty[kNBuf];
+    __shared__ uint32_t s_total[kNBuf];
+    auto PA = [&](int b) { return arr + (4 * b + 0) * K; };
+    auto PL = [&](int b) { return arr + (4 * b + 1) * K; };
+    auto PM = [&](int b) { return arr + (4 * b + 2) * K; };
+    auto ST = [&](int b) { return arr + (4 * b + 3) * K; };
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint64_t g0 = blockIdx.x, grid = gridDim.x;
+    if (g0 >= G) return;
+    for (int k = threadIdx.x; k < K; k += NTR) cnt[k] = clamp_count(counts[k], cap);
+    for (uint32_t j = threadIdx.x * 4; j < kRegion; j += NTR * 4)
+        *reinterpret_cast<float4*>(acc + j) = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < kNBuf; ++b) {
+            mbar_init_n(&full[b], kFullArrivals);
+            mbar_init_n(&empty[b], kCW);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        fence_proxy_async();
+    }
+    __syncthreads();
+
+    if (warp == kProducer) {
+        // ------------------------------------------------------ producer
+        uint32_t pre_a = 0, pre_b = 0;  // K <= 32: list `lane`'s table entries for the next region
+        auto prefetch = [&](uint64_t gr) {
+            if (K <= 32 && gr < G && lane < K) {
+                pre_a = __ldg(&lo[(uint64_t)lane * (G + 1) + gr]);
+                pre_b = __ldg(&lo[(uint64_t)lane * (G + 1) + gr + 1]);
+            }
+        };
+        prefetch(g0);
+        int i = 0;
+        bool aborted = false;
+        for (uint64_t g = g0; g < G; g += grid, ++i) {
+            const int b = i % kNBuf;
+            if (i >= kNBuf && !mbar_wait_bounded(&empty[b], (uint32_t)((i / kNBuf - 1) & 1))) {
+                aborted = true;
+                break;
+            }
+            uint32_t* pa = PA(b);
+            uint32_t* pl = PL(b);
+            uint32_t* pm = PM(b);
+            uint32_t* st = ST(b);
+            gcsgd_pair* buf = stage + (size_t)b * kRStage;
+            // ranges (chunks of 32 lists), the stage total and the bulk bytes
+            uint32_t total = 0, bytes = 0;
+            for (int c0 = 0; c0 < K; c0 += 32) {
+                const int k = c0 + lane;
+                uint32_t slots = 0, body = 0;
+                if (k < K) {
+                    const uint32_t ta_ = K <= 32 ? pre_a : __ldg(&lo[(uint64_t)k * (G + 1) + g]);
+                    const uint32_t tb_ = K <= 32 ? pre_b : __ldg(&lo[(uint64_t)k * (G + 1) + g + 1]);
+                    const Range R = range_of(lists, cap, cnt[k], k, ta_, tb_);
+                    pa[k] = R.a;
+                    pl[k] = R.len;
+                    pm[k] = R.slots | R.head;
+                    slots = R.slots;
+                    body = R.body;
+                }
+                total += warp_sum(slots);
+                bytes += warp_sum(body * 8u);
+            }
+            prefetch(g + grid);
+            const bool fits = total <= kRStage;
+            // stage slots; the single first and last pairs by cp.async
+            uint32_t carry = 0;
+            for (int c0 = 0; c0 < K; c0 += 32) {
+                const int k = c0 + lane;
+                const uint32_t m = k < K ? pm[k] : 0u, slots = m & ~1u, head = m & 1u;
+                uint32_t incl = slots;
+                for (int d = 1; d < 32; d <<= 1) {
+                    const uint32_t v = __shfl_up_sync(kFull, incl, d);
+                    if (lane >= d) incl += v;
+                }
+                if (k < K) {
+                    const uint32_t slot = carry + incl - slots + head;
+                    st[k] = slot;
+                    const uint32_t len = pl[k];
+                    if (fits && len > 0) {
+                        const gcsgd_pair* L = lists + (uint64_t)k * cap + pa[k];
+                        const uintptr_t s = (uintptr_t)L;
+                        const uintptr_t bs = s + 8 * head, be = (s + 8 * (uintptr_t)len) & ~(uintptr_t)15;
+                        const uint32_t body = be > bs ? (uint32_t)((be - bs) / 8) : 0u;
+                        if (head) cp_async8(&buf[slot], &L[0]);
+                        if (head + body < len) cp_async8(&buf[slot + len - 1], &L[len - 1]);
+                    }
+                }
+                carry += __shfl_sync(kFull, incl, 31);
+            }
+            __syncwarp();  // every lane's plan written before lane 0 publishes it
+            if (lane == 0) {
+                s_total[b] = fits ? total : kSlow;
+                mbar_arrive_expect(&full[b], fits ? bytes : 0u);
+            }
+            __syncwarp();
+            if (fits)
+                for (int k = lane; k < K; k += 32) {
+                    const uint32_t len = pl[k], head = pm[k] & 1u;
+                    if (len == 0) continue;
+                    const gcsgd_pair* L = lists + (uint64_t)k * cap + pa[k];
+                    const uintptr_t s = (uintptr_t)L;
+                    const uintptr_t bs = s + 8 * head, be = (s + 8 * (uintptr_t)len) & ~(uintptr_t)15;
+                    const uint32_t body = be > bs ? (uint32_t)((be - bs) / 8) : 0u;
+                    if (body) bulk_copy(&buf[st[k] + head], L + head, body * 8u, &full[b]);
+                }
+            cp_async_arrive(&full[b]);
+        }
+        if (aborted) {
+            atomicOr(status, 1u);
+            // the copies of the buffers still armed land before the CTA may end
+            for (int q = 1; q <= kNBuf && i - q >= 0; ++q)
+                (void)mbar_wait_bounded(&full[(i - q) % kNBuf], (uint32_t)(((i - q) / kNBuf) & 1));
+        }
+        cp_async_wait<0>();
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    // Every consumer thread takes entries ct, ct + 256, ... of each list's
+    // staged range, list after list in learner order (a named barrier among
+    // the consumers between lists; a list's indices are distinct, so its adds
+    // never collide; entries outside the region are skipped), then the
+    // consumers release the buffer and store the region.  The first two
+    // entries per thread of list k+1 are read while list k is added.
+    const int ct = threadIdx.x;
+    constexpr int NC = kCW * 32;
+    const float fk = (float)K, inv_k = 1.0f / fk;
+    const bool pow2 = (K & (K - 1)) == 0;
+    const bool al = ((uintptr_t)out & 15) == 0;
+    int i = 0;
+    for (uint64_t g = g0; g < G; g += grid, ++i) {
+        const int b = i % kNBuf;
+        const bool ok = mbar_wait_bounded(&full[b], (uint32_t)((i / kNBuf) & 1));
+        if (!consumers_all(ok)) {
+            if (ct == 0) atomicOr(status, 1u);
+            return;
+        }
+        const uint32_t R0 = (uint32_t)(g * kRegion);
+        const uint32_t rlen = (uint32_t)((uint64_t)R0 + kRegion < n ? kRegion : n - R0);
+        const uint32_t* pl = PL(b);
+        if (s_total[b] != kSlow) {
+            const gcsgd_pair* buf = stage + (size_t)b * kRStage;
+            const uint32_t* st = ST(b);
+            const gcsgd_pair none = {0xffffffffu, 0.0f};
+            uint32_t lenN = pl[0];
+            const gcsgd_pair* SN = buf + st[0];
+            gcsgd_pair nx[kPer];
+#pragma unroll
+            for (int r = 0; r < kPer; ++r) nx[r] = (uint32_t)(ct + r * NC) < lenN ? SN[ct + r * NC] : none;
+            for (int k = 0; k < K; ++k) {
+                const uint32_t len = lenN;
+                const gcsgd_pair* S = SN;
+                gcsgd_pair e[kPer];
+#pragma unroll
+                for (int r = 0; r < kPer; ++r) e[r] = nx[r];
+                if (k + 1 < K) {
+                    lenN = pl[k + 1];
+                    SN = buf + st[k + 1];
+#pragma unroll
+                    for (int r = 0; r < kPer; ++r) nx[r] = (uint32_t)(ct + r * NC) < lenN ? SN[ct + r * NC] : none;
+                }
+                if (len == 0) continue;  // uniform: an empty range needs no barrier
+                {
+                    // a list's indices are distinct, so these adds touch different outputs:
+                    // every read of acc before any write
+                    uint32_t d[kPer];
+                    bool in[kPer];
+                    float a[kPer];
+#pragma unroll
+                    for (int r = 0; r < kPer; ++r) {
+                        d[r] = e[r].idx - R0;  // inside iff d < rlen (R0 + rlen <= 2^32)
+                        in[r] = (uint32_t)(ct + r * NC) < len && d[r] < rlen;
+                        a[r] = in[r] ? acc[d[r]] : 0.0f;
+                    }
+#pragma unroll
+                    for (int r = 0; r < kPer; ++r)
+                        if (in[r]) acc[d[r]] = __fadd_rn(a[r], e[r].val);
+                }
+                for (uint32_t q = ct + kPer * NC; q < len; q += NC) {  // longer ranges
+                    const gcsgd_pair e = S[q];
+                    const uint32_t d = e.idx - R0;
+                    if (d < rlen) acc[d] = __fadd_rn(acc[d], e.val);
+                }
+                consumer_sync();  // list k's adds land before list k+1's
+            }
+        } else {
+            const uint32_t* pa = PA(b);
+            for (int k = 0; k < K; ++k) {
+                const uint32_t len = pl[k];
+                if (len == 0) continue;
+                const gcsgd_pair* S = lists + (uint64_t)k * cap + pa[k];
+                for (uint32_t q = ct; q < len; q += NC) {
+                    const gcsgd_pair e = S[q];
+                    const uint32_t d = e.idx - R0;
+                    if (d < rlen) acc[d] = __fadd_rn(acc[d], e.val);
+                }
+                consumer_sync();
+            }
+        }
+        // the buffer is free: its reads done before the bulk copies that refill it
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[b]);
+        // the region's average, written once; acc re-zeroed for the next region
+        float* o = out + R0;
+#pragma unroll
+        for (int r = 0; r < (int)(kRegion / (4 * NC)); ++r) {
+            const uint32_t j = 4u * (ct + r * NC);
+            float4 q = *reinterpret_cast<const float4*>(acc + j);
+            *reinterpret_cast<float4*>(acc + j) = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (j >= rlen) continue;
+            if (pow2) {  // x * 2^-j is x / 2^j rounded once
+                q.x = __fmul_rn(q.x, inv_k);
+                q.y = __fmul_rn(q.y, inv_k);
+                q.z = __fmul_rn(q.z, inv_k);
+                q.w = __fmul_rn(q.w, inv_k);
+            } else {
+                q.x = div_k(q.x, fk, inv_k, false);
+                q.y = div_k(q.y, fk, inv_k, false);
+                q.z = div_k(q.z, fk, inv_k, false);
+                q.w = div_k(q.w, fk, inv_k, false);
+            }
+            if (al && j + 4 <= rlen) {
+                *reinterpret_cast<float4*>(o + j) = q;
+            } else {
+                const float* qq = &q.x;
+                for (uint32_t t = 0; t < 4 && j + t < rlen; ++t) o[j + t] = qq[t];
+            }
+        }
+        consumer_sync();  // acc zeroed before the next region's adds
+    }
+}
+
 }  // namespace spavg
 
 int spavg_launch(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int K, int64_t n, float* out,
@@ -679,6 +1139,83 @@ int spavg_launch(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, in
         spavg_kernel<false><<<(unsigned)grid, NT, smem, stream>>>(lists, (uint64_t)cap, counts, K, (uint64_t)n, out,
                                                                   tiles, per, C, 0.0f);
     return check_launch(update ? "spavg_update" : "spavg");
+}
+
+}  // namespace gcsgd
+
+namespace gcsgd {
+
+static size_t spavg_table_bytes(int K, int64_t n) {
+    const uint64_t G = ((uint64_t)(n > 0 ? n : 0) + spavg::kRegion - 1) / spavg::kRegion;
+    return ((size_t)K * (size_t)(G + 1) * sizeof(uint32_t) + 255) / 256 * 256;
+}
+
+size_t spavg_ws_bytes(int K, int64_t n) { return spavg_table_bytes(K, n) + 256; }  // the table, then the status word
+
+int spavg_ws_launch(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int K, int64_t n, float* out,
+                    void* ws, cudaStream_t stream) {
+    using namespace spavg;
+    if (n == 0) return GCSGD_OK;
+    // sparse lists (K * cap < n / 4) stay on the tile kernel, and lists off
+    // the 8-byte boundary (which bulk copies cannot fetch) on sparse_average's
+    // kernels; the status word still reads 0
+    if ((uint64_t)K * (uint64_t)cap < (uint64_t)n / 4 || ((uintptr_t)lists & 7) != 0) {
+        const cudaError_t e =
+            cudaMemsetAsync(static_cast<unsigned char*>(ws) + spavg_table_bytes(K, n), 0, sizeof(uint32_t), stream);
+        if (e != cudaSuccess)
+            return set_error(GCSGD_ERR_CUDA, "sparse_average_ws: status clear failed: %s", cudaGetErrorString(e));
+        return spavg_launch(lists, cap, counts, K, n, out, stream, false, 0.0f);
+    }
+    const uint64_t G = ((uint64_t)n + kRegion - 1) / kRegion;
+    uint32_t* lo = static_cast<uint32_t*>(ws);
+    uint32_t* status = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(ws) + spavg_table_bytes(K, n));
+    const int sms = sm_count();
+    const uint64_t checks = ((uint64_t)cap + kCheck - 1) / kCheck;
+    uint64_t bx = (checks + NT - 1) / NT;
+    const uint64_t bx_max = ((uint64_t)sms * 8 + K - 1) / K;
+    if (bx > bx_max) bx = bx_max;
+    if (bx < 1) bx = 1;
+    const size_t smem =
+        kRegion * sizeof(float) + kNBuf * kRStage * sizeof(gcsgd_pair) + sizeof(uint32_t) * (4 * kNBuf + 1) * (size_t)K;
+    constexpr size_t kMaxSmem =
+        kRegion * sizeof(float) + kNBuf * kRStage * sizeof(gcsgd_pair) + sizeof(uint32_t) * (4 * kNBuf + 1) * 512;
+    static int occ_of[64][2] = {};  // per device: resident CTAs for K <= 64 and for larger K
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int kc = K <= 64 ? 0 : 1;
+    if (dev >= 64) return set_error(GCSGD_ERR_CUDA, "sparse_average_ws: device ordinal %d >= 64", dev);
+    if (!occ_of[dev][kc]) {
+        int occ = 0;
+        if (cudaFuncSetAttribute(spavg_region, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem) !=
+                cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, spavg_region, NTR, kc ? kMaxSmem : smem) != cudaSuccess)
+            return set_error(GCSGD_ERR_CUDA, "sparse_average_ws: cannot set up the region kernel");
+        occ_of[dev][kc] = occ > 0 ? occ : 1;
+    }
+    uint64_t grid = (uint64_t)sms * (uint64_t)occ_of[dev][kc];
+    if (grid > G) grid = G;
+    {
+        LaunchScope ls("spavg_checkpoints", stream);
+        spavg_checkpoints<<<dim3((unsigned)bx, (unsigned)K), NT, 0, stream>>>(lists, (uint64_t)cap, counts, G, lo,
+                                                                             status);
+        const int rc = check_launch("spavg_checkpoints");
+        if (rc) return rc;
+    }
+    LaunchScope ls("spavg", stream);
+    spavg_region<<<(unsigned)grid, NTR, smem, stream>>>(lists, (uint64_t)cap, counts, K, (uint64_t)n, out, lo, G,
+                                                       status);
+    return check_launch("spavg_region");
+}
+
+int spavg_ws_status(const void* ws, int K, int64_t n, cudaStream_t stream, int32_t* status) {
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, static_cast<const unsigned char*>(ws) + spavg_table_bytes(K, n), sizeof(v),
+                                    cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess)
+        return set_error(GCSGD_ERR_CUDA, "gcsgd_sparse_average_status: %s", cudaGetErrorString(e));
+    *status = (int32_t)v;
+    return GCSGD_OK;
 }
 
 }  // namespace gcsgd

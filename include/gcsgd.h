@@ -260,6 +260,45 @@ int adacomp_compress(const int64_t* seg_offsets, int32_t n_seg, const int32_t* l
 int sparse_average(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int32_t K,
                    int64_t n, float* out, void* stream);
 
+/* Bytes of device workspace sparse_average_ws needs for K lists over n
+ * outputs: 4 K (ceil(n / 4096) + 1) rounded up to a multiple of 256, plus
+ * 256 for a status word.  Host call; GCSGD_ERR_INVALID_ARG for K outside
+ * [1, 512], n outside [0, 2^32] or bytes NULL. */
+int gcsgd_sparse_average_workspace_size(int32_t K, int64_t n, size_t* bytes);
+
+/*
+ * sparse_average with device scratch: the same out, bit for bit (learner
+ * order, one fp32 divide by K).  For dense lists (K * cap >= n / 4) with
+ * 8-byte aligned records it runs two kernels: the first reads every 128th
+ * entry of every list and writes a cursor table into the workspace (per
+ * list and 4096-output region, a position at most 128 entries before the
+ * region's first entry); the second copies each region's list ranges into
+ * shared memory with TMA bulk copies, the next region's copies in flight
+ * while the current one is added, and writes every region's average once.
+ * Other lists take sparse_average's kernels (the workspace then only holds
+ * the status word).
+ * lists, cap, counts, K, n, out: as for sparse_average.
+ * workspace   device scratch of at least gcsgd_sparse_average_workspace_size
+ *             bytes, 256-byte aligned, contents ignored and overwritten; one
+ *             call at a time per workspace (calls that share one must be
+ *             ordered, e.g. on one stream).
+ * Errors: as for sparse_average; GCSGD_ERR_WORKSPACE when workspace_bytes is
+ * too small, GCSGD_ERR_INVALID_ARG when workspace is NULL or misaligned
+ * (n = 0 writes nothing and needs no workspace).  Every wait in the kernel
+ * is bounded: a copy that has not completed after 1 s ends the kernel early
+ * with part of out unwritten and sets the status word, which
+ * gcsgd_sparse_average_status reads.
+ */
+int sparse_average_ws(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int32_t K,
+                      int64_t n, float* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* The status word of the last sparse_average_ws call made with `workspace`
+ * for this K and n (0: every copy completed; 1: a copy timed out).  Waits for
+ * `stream`, then reads 4 bytes.  Errors: GCSGD_ERR_INVALID_ARG for K outside
+ * [1, 512], n outside [1, 2^32] or a NULL pointer; GCSGD_ERR_CUDA when the
+ * copy or the wait fails. */
+int gcsgd_sparse_average_status(const void* workspace, int32_t K, int64_t n, void* stream, int32_t* status);
+
 /*
  * The averaged sparse weight update: the K messages are averaged exactly as
  * sparse_average does (learner order, one fp32 divide by K) and the weights
