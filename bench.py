@@ -312,7 +312,8 @@ def run_reference(args):
 
 def config_dict(w, **extra):
     steps = {"dgc": "dgc_compress(K learners) + sparse_average",
-             "adacomp": "adacomp_compress(K learners) + sparse_average_ws (cursor table + TMA-staged regions)",
+             "adacomp": "adacomp_compress_deferred(K learners; each step's residue fix-up runs in the next step's "
+                        "bin pass) + sparse_average_ws (cursor table + TMA-staged regions)",
              "dcd": "dcd_step(n ring nodes)"}
     d = {"workload": w.name, "learners": w.learners, "elements_per_learner": w.n, "segments": len(w.sizes),
          "step": steps[w.method],
@@ -409,7 +410,7 @@ class AdaCompPath(DgcPath):
     def __init__(self, gc, w, dev):
         import torch
         self.gc, self.w, self.K, self.N = gc, w, w.learners, w.n
-        self.obj = gc.AdaComp(w.offsets, w.lt, self.K, self.N // 8, device=dev)
+        self.obj = gc.AdaComp(w.offsets, w.lt, self.K, self.N // 8, device=dev, deferred=True)
         self.state = [torch.zeros((self.K, self.N), device=dev)]
         self.avg = torch.empty(self.N, device=dev)
         self.ws = torch.empty(gc.sparse_average_workspace_size(self.K, self.N), dtype=torch.uint8, device=dev)

@@ -88,6 +88,8 @@ def lib():
         L.gcsgd_dgc_stats.argtypes = [vp, i32, i32, f64, vp, vp, vp]
         L.gcsgd_adacomp_workspace_size.argtypes = [vp, i32, vp, i32, i64, vp]
         L.adacomp_compress.argtypes = [vp, i32, vp, i32, vp, vp, vp, i64, vp, vp, vp, vp, sz, vp]
+        L.adacomp_compress_deferred.argtypes = [vp, i32, vp, i32, vp, vp, vp, i64, vp, vp, vp, i32, vp, sz, vp]
+        L.adacomp_settle.argtypes = [vp, i32, vp, i32, vp, vp, i64, vp, vp, vp, sz, vp]
         L.sparse_average.argtypes = [vp, i64, vp, i32, i64, vp, vp]
         L.sparse_average_update.argtypes = [vp, i64, vp, i32, i64, f32, vp, vp]
         L.gcsgd_sparse_average_workspace_size.argtypes = [i32, i64, vp]
@@ -363,10 +365,45 @@ def adacomp_compress(offsets, lt, dW, residue, out, counts, scales, totals, work
         _stream(stream)))
 
 
-class AdaComp:
-    """Buffers of AdaComp on one layout; ``cap`` bounds the entries per learner."""
+def adacomp_compress_deferred(offsets, lt, dW, residue, out, counts, scales, totals, workspace, pending: bool,
+                              stream=None):
+    """One AdaComp step with the residue fix-up deferred to the next call (see
+    adacomp_compress_deferred in include/gcsgd.h)."""
+    import torch
+    off = _offsets(offsets)
+    lt = np.ascontiguousarray(np.asarray(lt, dtype=np.int32))
+    K = dW.shape[0]
+    cap = out.shape[1]
+    _check("adacomp_compress_deferred", lib().adacomp_compress_deferred(
+        _ptr(off), len(off) - 1, _ptr(lt), int(K), _dev(dW, "dW", torch.float32),
+        _dev(residue, "residue", torch.float32), _dev(out, "out", torch.int32), int(cap),
+        _dev(counts, "counts", torch.int64), _dev(scales, "scales", torch.float32),
+        _dev(totals, "totals", torch.int64), 1 if pending else 0, _dev(workspace, "workspace", torch.uint8),
+        int(workspace.numel()), _stream(stream)))
 
-    def __init__(self, offsets, lt, K: int, cap: int, device="cuda"):
+
+def adacomp_settle(offsets, lt, residue, out, counts, totals, workspace, stream=None):
+    """Applies a deferred call's pending residue fix-up (see adacomp_settle in include/gcsgd.h)."""
+    import torch
+    off = _offsets(offsets)
+    lt = np.ascontiguousarray(np.asarray(lt, dtype=np.int32))
+    K = out.shape[0]
+    _check("adacomp_settle", lib().adacomp_settle(
+        _ptr(off), len(off) - 1, _ptr(lt), int(K), _dev(residue, "residue", torch.float32),
+        _dev(out, "out", torch.int32), int(out.shape[1]), _dev(counts, "counts", torch.int64),
+        _dev(totals, "totals", torch.int64), _dev(workspace, "workspace", torch.uint8), int(workspace.numel()),
+        _stream(stream)))
+
+
+class AdaComp:
+    """Buffers of AdaComp on one layout; ``cap`` bounds the entries per learner.
+
+    With ``deferred=True`` each call leaves the residue fix-up of its sent
+    entries to the next call on the same residue tensor (adacomp_compress_deferred);
+    ``settle(residue)`` applies a pending one, and a call on another residue
+    tensor settles the previous tensor first."""
+
+    def __init__(self, offsets, lt, K: int, cap: int, device="cuda", deferred: bool = False):
         import torch
         self.offsets = _offsets(offsets)
         self.lt = np.ascontiguousarray(np.asarray(lt, dtype=np.int32))
@@ -378,11 +415,29 @@ class AdaComp:
         self.counts = torch.zeros((K, self.S), dtype=torch.int64, device=device)
         self.scales = torch.zeros((K, self.S), dtype=torch.float32, device=device)
         self.totals = torch.zeros(K, dtype=torch.int64, device=device)
+        self.deferred = bool(deferred)
+        self._pending = None  # the residue tensor whose fix-up is pending
 
     def __call__(self, dW, residue, stream=None):
-        adacomp_compress(self.offsets, self.lt, dW, residue, self.out, self.counts, self.scales, self.totals,
-                         self.workspace, stream=stream)
+        if not self.deferred:
+            adacomp_compress(self.offsets, self.lt, dW, residue, self.out, self.counts, self.scales, self.totals,
+                             self.workspace, stream=stream)
+            return self.out, self.totals
+        if self._pending is not None and self._pending.data_ptr() != residue.data_ptr():
+            self.settle(self._pending, stream=stream)
+        pending = self._pending is not None
+        adacomp_compress_deferred(self.offsets, self.lt, dW, residue, self.out, self.counts, self.scales,
+                                  self.totals, self.workspace, pending, stream=stream)
+        self._pending = residue
         return self.out, self.totals
+
+    def settle(self, residue=None, stream=None):
+        """Applies the pending fix-up to `residue` (default: the pending tensor), if any."""
+        r = self._pending if residue is None else residue
+        if self._pending is None or r is None or r.data_ptr() != self._pending.data_ptr():
+            return
+        adacomp_settle(self.offsets, self.lt, r, self.out, self.counts, self.totals, self.workspace, stream=stream)
+        self._pending = None
 
 
 # ---------------------------------------------------------- sparse average

@@ -26,6 +26,16 @@
 // bin's maximum is final inside one warp or CTA and the first pass is
 // single-read.  Every tile owns the pool slots of its index range, so no
 // counter is shared between CTAs and the result is deterministic.
+//
+// Deferred residue (adacomp_compress_deferred), for the warp-chunk segments:
+// ada_emit does not rewrite R at the sent indices (a scattered read-modify-
+// write of a 32-byte sector per entry); ada_bins_warp keeps the chunk's
+// selection bits instead (16 bits per lane, 64 bytes a chunk), and the next
+// call's ada_bins_warp, which streams R anyway, subtracts the sent value
+// sign(R) * scale at those bits before forming G = R + dW: the same fp32
+// subtraction, of the same operands, as the eager fix-up, so every message
+// and every residue is bit-identical.  Until then R holds G at the sent
+// indices; ada_settle applies the pending subtraction.
 #include <math.h>
 
 #include "common.cuh"
@@ -127,6 +137,7 @@ struct Workspace {
     uint32_t* grp_rel;   // first output slot of the emit group within its segment
     uint32_t* big;       // bin maxima (|G| bits) of big-mode segments
     uint2* pool;         // (index within the learner, G bits); a tile's entries sit at its own index range
+    uint16_t* sent;      // deferred residue: per tile and lane, the chunk's selection bits (warp-chunk tiles)
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -146,6 +157,7 @@ size_t layout(int S, int K, int64_t off_total, const HostPlan& hp, void* base, W
     const size_t o_tr = take(sizeof(uint32_t) * (size_t)K * hp.groups_per_learner);
     const size_t o_big = take(sizeof(uint32_t) * (size_t)K * hp.big_per_learner);
     const size_t o_pool = take(sizeof(uint2) * (size_t)K * (size_t)N);  // one slot per element: no shared counter
+    const size_t o_sent = take(sizeof(uint16_t) * 32 * T);
     if (w) {
         char* b = (char*)base;
         w->plan = (SegPlan*)(b + o_plan);
@@ -154,6 +166,7 @@ size_t layout(int S, int K, int64_t off_total, const HostPlan& hp, void* base, W
         w->grp_rel = (uint32_t*)(b + o_tr);
         w->big = (uint32_t*)(b + o_big);
         w->pool = (uint2*)(b + o_pool);
+        w->sent = (uint16_t*)(b + o_sent);
     }
     return o;
 }
@@ -348,10 +361,14 @@ constexpr int kRing = 2;   // stages per warp
 struct ChunkMeta {         // what the computing side needs of an issued chunk
     uint32_t rel, clen, k, lt, tj, L, bpw, big_off;
     float invL;
+    float pscale;          // deferred residue: the previous call's scale of the segment
+    uint32_t pfix;         // the previous call's selection bits apply (its learner sent)
 };
+// the previous call's selection bits of a chunk: 32 lanes x 16 bits
+constexpr size_t kSentBytes = 32 * sizeof(uint16_t);
 constexpr size_t kBinsWarpSmem =
     sizeof(float) * (NTW / 32) * kRing * 2 * kWarpChunk + sizeof(ChunkMeta) * (NTW / 32) * kRing +
-    sizeof(uint32_t) * (NTW / 32) * (kWarpChunk / 4);
+    sizeof(uint32_t) * (NTW / 32) * (kWarpChunk / 4) + kSentBytes * (NTW / 32) * kRing;
 
 __device__ __forceinline__ void cp_async16(void* sdst, const void* gsrc, uint32_t bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"((uint32_t)__cvta_generic_to_shared(sdst)),
@@ -367,11 +384,17 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
+// defer: keep the selection bits in `sent` instead of having ada_emit fix R;
+// pending: R holds the previous deferred call's G at its sent indices, whose
+// bits are in `sent` and whose scales and totals are prev_scales, prev_totals.
 __global__ void __launch_bounds__(NTW, 6) ada_bins_warp(const SegPlan* __restrict__ plan, int S, uint64_t N,
                                                         uint32_t tiles_per_learner, uint64_t total_tiles,
                                                         const float* __restrict__ dW, float* __restrict__ R,
                                                         uint32_t* __restrict__ bins, uint64_t bins_per_learner,
-                                                        uint2* __restrict__ tile_tab, uint2* __restrict__ pool) {
+                                                        uint2* __restrict__ tile_tab, uint2* __restrict__ pool,
+                                                        int defer, int pending, uint16_t* __restrict__ sent,
+                                                        const float* __restrict__ prev_scales,
+                                                        const int64_t* __restrict__ prev_totals, uint64_t cap) {
     extern __shared__ __align__(16) unsigned char bw_smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     float* ring = reinterpret_cast<float*>(bw_smem) + (size_t)warp * kRing * 2 * kWarpChunk;  // [kRing][dW | R]
@@ -380,6 +403,10 @@ __global__ void __launch_bounds__(NTW, 6) ada_bins_warp(const SegPlan* __restric
     uint32_t* wb = reinterpret_cast<uint32_t*>(bw_smem + sizeof(float) * (NTW / 32) * kRing * 2 * kWarpChunk +
                                                sizeof(ChunkMeta) * (NTW / 32) * kRing) +
                    warp * (kWarpChunk / 4);  // this warp's bin maxima (bpw <= 128)
+    uint16_t* sbits = reinterpret_cast<uint16_t*>(bw_smem + sizeof(float) * (NTW / 32) * kRing * 2 * kWarpChunk +
+                                                  sizeof(ChunkMeta) * (NTW / 32) * kRing +
+                                                  sizeof(uint32_t) * (NTW / 32) * (kWarpChunk / 4)) +
+                      warp * kRing * 32;  // [kRing][32] the previous selection bits of the staged chunks
     const uint32_t nw = gridDim.x * (NTW / 32), T = (uint32_t)total_tiles;  // T < 2^32 (checked by the host)
 
     // issuing side: the warp's tiles t = its id + i * nw, keeping the segment's fields
@@ -387,8 +414,8 @@ __global__ void __launch_bounds__(NTW, 6) ada_bins_warp(const SegPlan* __restric
     bool done = t >= T;
     uint32_t k = 0, lt = 0;
     struct {
-        uint32_t off, n, L, bpw, tile_len, tile_off, big_off, next_off;
-        float invL;
+        uint32_t off, n, L, bpw, tile_len, tile_off, big_off, next_off, k, pfix;
+        float invL, pscale;
     } p = {};
     auto load_seg = [&](uint32_t at) {
         const int s = find_segment_by_tile(plan, S, at);
@@ -396,6 +423,13 @@ __global__ void __launch_bounds__(NTW, 6) ada_bins_warp(const SegPlan* __restric
         p.off = q.off, p.n = q.n, p.L = q.L, p.bpw = q.mode == kModeSmall ? q.bpw : 0u;
         p.tile_len = q.tile_len, p.tile_off = q.tile_off, p.big_off = q.big_off, p.invL = q.invL;
         p.next_off = s + 1 < S ? __ldg(&plan[s + 1].tile_off) : tiles_per_learner;
+        p.k = k;
+        p.pfix = 0u;
+        p.pscale = 0.0f;
+        if (pending && p.bpw) {  // the learner's previous message was sent (not over cap)
+            p.pfix = (uint64_t)prev_totals[k] <= cap ? 1u : 0u;
+            p.pscale = prev_scales[(uint64_t)k * S + s];
+        }
     };
     auto step = [&]() {
         if (T - t <= nw) {
@@ -408,7 +442,7 @@ __global__ void __launch_bounds__(NTW, 6) ada_bins_warp(const SegPlan* __restric
             lt -= tiles_per_learner;
             ++k;
         }
-        if (lt < p.tile_off || lt >= p.next_off) load_seg(lt);
+        if (lt < p.tile_off || lt >= p.next_off || k != p.k) load_seg(lt);
     };
     if (!done) {
         k = t / tiles_per_learner;
@@ -423,6 +457,11 @@ __global__ void __launch_bounds__(NTW, 6) ada_bins_warp(const SegPlan* __restric
             m.rel = p.off + start;
             m.clen = p.n - start < p.tile_len ? p.n - start : p.tile_len;
             m.k = k, m.lt = lt, m.tj = tj, m.L = p.L, m.bpw = p.bpw, m.big_off = p.big_off, m.invL = p.invL;
+            m.pscale = p.pscale, m.pfix = p.pfix;
+            if (lane < 16) {  // the previous selection bits (zeros where none apply)
+                const uint16_t* src = sent + ((uint64_t)k * tiles_per_learner + lt) * 32 + 2 * lane;
+                cp_async4(sbits + st * 32 + 2 * lane, src, p.pfix ? 4u : 0u);
+            }
             const uint64_t base = (uint64_t)k * N + m.rel;
             const float* dWc = dW + base;
             const float* Rc = R + base;
@@ -471,11 +510,18 @@ __global__ void __launch_bounds__(NTW, 6) ada_bins_warp(const SegPlan* __restric
         const bool cal = ((uintptr_t)Rc & 15) == 0;
         const uint32_t clen = m.clen, bpw = m.bpw, L = m.L;
         float4 Gv[4], Dv[4];
+        const uint32_t pbits = m.pfix ? (uint32_t)sbits[cs * 32 + lane] : 0u;  // bit 4r+j: element j of round r
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const uint32_t e = 4u * (lane + 32 * r);
             Dv[r] = *reinterpret_cast<const float4*>(sD + e);
             Gv[r] = *reinterpret_cast<const float4*>(sR + e);
+            if (pbits & (0xFu << (4 * r))) {  // the previous call's deferred fix-up: R -= sign(R) * scale
+                float* g4 = &Gv[r].x;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if ((pbits >> (4 * r + j)) & 1u) g4[j] = __fsub_rn(g4[j], g4[j] > 0.0f ? m.pscale : -m.pscale);
+            }
             Gv[r].x = __fadd_rn(Gv[r].x, Dv[r].x);
             Gv[r].y = __fadd_rn(Gv[r].y, Dv[r].y);
             Gv[r].z = __fadd_rn(Gv[r].z, Dv[r].z);
@@ -543,6 +589,7 @@ __global__ void __launch_bounds__(NTW, 6) ada_bins_warp(const SegPlan* __restric
                 }
             }
         }
+        if (defer) sent[((uint64_t)m.k * tiles_per_learner + m.lt) * 32 + lane] = (uint16_t)flags;
         uint32_t packed = 0;  // candidates per round, 8 bits each
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
@@ -867,16 +914,18 @@ __device__ __forceinline__ int find_segment_by_group(const SegPlan* plan, int S,
 // shuffle scan joins their entries into one run, and the lanes walk that run
 // 32 entries at a time.  Each entry goes to (entries of the learner's earlier
 // segments) + (its tile's first slot in the segment) + (rank in the tile) as
-// (index, sign(G)*scale), and its residue becomes R = G - sign(G)*scale.  A
-// learner whose total exceeds cap sends nothing; its residue keeps G = R + dW
-// (already stored by the bin pass).  seg_out: K*S words of shared memory.
+// (index, sign(G)*scale), and its residue becomes R = G - sign(G)*scale
+// (with defer, only outside the warp-chunk segments: there the next call's
+// bin pass subtracts it).  A learner whose total exceeds cap sends nothing;
+// its residue keeps G = R + dW (already stored by the bin pass).  seg_out:
+// K*S words of shared memory.
 __global__ void __launch_bounds__(NT, 6) ada_emit(const SegPlan* __restrict__ plan, int S, uint64_t N,
                                                uint32_t tiles_per_learner, uint32_t groups_per_learner,
                                                const uint2* __restrict__ tile_tab, const uint32_t* __restrict__ grp_rel,
                                                const uint2* __restrict__ pool, const int64_t* __restrict__ counts,
                                                const float* __restrict__ scales, float* __restrict__ R,
                                                gcsgd_pair* __restrict__ out, uint64_t cap, int K,
-                                               int64_t* __restrict__ totals) {
+                                               int64_t* __restrict__ totals, int defer) {
     extern __shared__ __align__(8) unsigned char emit_smem[];
     uint64_t* s_total = reinterpret_cast<uint64_t*>(emit_smem);            // [K] entries of each learner
     uint32_t* seg_out = reinterpret_cast<uint32_t*>(emit_smem + 8 * K);  // [K][S] first slot of each segment
@@ -911,6 +960,7 @@ __global__ void __launch_bounds__(NT, 6) ada_emit(const SegPlan* __restrict__ pl
         uint32_t g_lo = 1, g_hi = 0, s_tiles = 0, s_tile_off = 0;
         float scale = 0.0f;
         uint64_t ob = 0;
+        bool fix_r = true;
         for (uint32_t g = gw; g < groups_per_learner; g += nw) {
             if (g < g_lo || g >= g_hi) {
                 s = find_segment_by_group(plan, S, g);
@@ -920,6 +970,7 @@ __global__ void __launch_bounds__(NT, 6) ada_emit(const SegPlan* __restrict__ pl
                 s_tile_off = __ldg(&plan[s].tile_off);
                 scale = scales[(uint64_t)k * S + s];
                 ob = seg_out[k * S + s];
+                fix_r = !(defer && __ldg(&plan[s].mode) == kModeSmall && __ldg(&plan[s].bpw) != 0u);
             }
             const uint32_t j0 = (g - g_lo) * kGroup;
             const uint32_t nt = s_tiles - j0 < kGroup ? s_tiles - j0 : kGroup;
@@ -948,7 +999,7 @@ __global__ void __launch_bounds__(NT, 6) ada_emit(const SegPlan* __restrict__ pl
                     const uint2 it = src[(uint64_t)cx + (i - ce)];
                     const float gv = __uint_as_float(it.y);
                     const float val = gv > 0.0f ? scale : -scale;
-                    Rk[it.x] = __fsub_rn(gv, val);
+                    if (fix_r) Rk[it.x] = __fsub_rn(gv, val);
                     const uint64_t slot = gob + i;
                     if (slot < cap) {
                         gcsgd_pair pr;
@@ -962,6 +1013,39 @@ __global__ void __launch_bounds__(NT, 6) ada_emit(const SegPlan* __restrict__ pl
     }
 }
 
+// The pending fix-up of a deferred call, applied to R: for every warp-chunk
+// segment of every learner that sent, R[i] -= v for each (i, v) of its part
+// of the message (the same fp32 subtraction the eager ada_emit makes).  One
+// CTA per (learner, segment); the segment's first slot is the sum of the
+// learner's earlier counts.
+__global__ void __launch_bounds__(NT) ada_settle(const SegPlan* __restrict__ plan, int S, uint64_t N,
+                                                 const int64_t* __restrict__ counts,
+                                                 const int64_t* __restrict__ totals, uint64_t cap,
+                                                 const gcsgd_pair* __restrict__ out, float* __restrict__ R) {
+    __shared__ uint64_t red[NT / 32];
+    const int unit = blockIdx.x;
+    const int k = unit / S, s = unit - k * S;
+    const SegPlan p = plan[s];
+    if (!(p.mode == kModeSmall && p.bpw != 0u)) return;
+    if ((uint64_t)totals[k] > cap) return;  // the learner sent nothing
+    uint64_t part = 0;
+    for (int q = threadIdx.x; q < s; q += NT) part += (uint64_t)counts[(uint64_t)k * S + q];
+    for (int d = 16; d > 0; d >>= 1) part += __shfl_xor_sync(kFull, part, d);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = part;
+    __syncthreads();
+    uint64_t first = 0;
+    for (int w = 0; w < NT / 32; ++w) first += red[w];
+    const uint64_t c = (uint64_t)counts[(uint64_t)k * S + s];
+    const gcsgd_pair* L = out + (uint64_t)k * cap;
+    float* Rk = R + (uint64_t)k * N;
+    for (uint64_t i = threadIdx.x; i < c; i += NT) {
+        const uint64_t slot = first + i;
+        if (slot >= cap) break;
+        const gcsgd_pair e = L[slot];
+        if ((uint64_t)e.idx < N) Rk[e.idx] = __fsub_rn(Rk[e.idx], e.val);
+    }
+}
+
 }  // namespace ada
 
 size_t adacomp_workspace_bytes(const int64_t* off, const int32_t* lt, int S, int K, int64_t cap) {
@@ -971,9 +1055,27 @@ size_t adacomp_workspace_bytes(const int64_t* off, const int32_t* lt, int S, int
     return ada::layout(S, K, off[S], hp, nullptr, nullptr);
 }
 
+static int launch_plan(const int64_t* off, int S, const int32_t* lt, int K, const ada::HostPlan& hp,
+                       const ada::Workspace& w, cudaStream_t stream) {
+    using namespace ada;
+    LaunchScope ls("ada_plan", stream);
+    if (S <= 256) {
+        SegTable<256> st;
+        for (int s = 0; s <= S; ++s) st.off[s] = (uint32_t)off[s];
+        for (int s = 0; s < S; ++s) st.L[s] = (uint32_t)lt[s];
+        ada_plan<256><<<1, 1024, 0, stream>>>(st, S, K, hp.big_per_learner, w.plan, w.big);
+    } else {
+        SegTable<GCSGD_MAX_SEGMENTS> st;
+        for (int s = 0; s <= S; ++s) st.off[s] = (uint32_t)off[s];
+        for (int s = 0; s < S; ++s) st.L[s] = (uint32_t)lt[s];
+        ada_plan<GCSGD_MAX_SEGMENTS><<<1, 1024, 0, stream>>>(st, S, K, hp.big_per_learner, w.plan, w.big);
+    }
+    return check_launch("ada_plan");
+}
+
 int adacomp_launch(const int64_t* off, int S, const int32_t* lt, int K, const float* dW, float* R, gcsgd_pair* out,
                    int64_t cap, int64_t* counts, float* scales, int64_t* totals, void* ws, size_t ws_bytes,
-                   cudaStream_t stream) {
+                   cudaStream_t stream, int defer, int pending) {
     using namespace ada;
     HostPlan hp;
     host_plan(off, lt, S, &hp);
@@ -990,21 +1092,7 @@ int adacomp_launch(const int64_t* off, int S, const int32_t* lt, int K, const fl
                          "adacomp_compress: K * (4 n_seg + 8) = %lld bytes of emit tables exceed %d",
                          (long long)emit_smem_bytes(K, S), (int)kEmitSmemMax);
     int rc;
-    {
-        LaunchScope ls("ada_plan", stream);
-        if (S <= 256) {
-            SegTable<256> st;
-            for (int s = 0; s <= S; ++s) st.off[s] = (uint32_t)off[s];
-            for (int s = 0; s < S; ++s) st.L[s] = (uint32_t)lt[s];
-            ada_plan<256><<<1, 1024, 0, stream>>>(st, S, K, hp.big_per_learner, w.plan, w.big);
-        } else {
-            SegTable<GCSGD_MAX_SEGMENTS> st;
-            for (int s = 0; s <= S; ++s) st.off[s] = (uint32_t)off[s];
-            for (int s = 0; s < S; ++s) st.L[s] = (uint32_t)lt[s];
-            ada_plan<GCSGD_MAX_SEGMENTS><<<1, 1024, 0, stream>>>(st, S, K, hp.big_per_learner, w.plan, w.big);
-        }
-        if ((rc = check_launch("ada_plan"))) return rc;
-    }
+    if ((rc = launch_plan(off, S, lt, K, hp, w, stream))) return rc;
     const uint64_t grid_cap = (uint64_t)sm_count() * 3;
     bool any_warp = false, any_other = false, any_big = false;
     for (int s = 0; s < S; ++s) {
@@ -1033,7 +1121,8 @@ int adacomp_launch(const int64_t* off, int S, const int32_t* lt, int K, const fl
         }
         const uint64_t wgrid = (uint64_t)sm_count() * 6, need_ctas = (T + NTW / 32 - 1) / (NTW / 32);
         ada_bins_warp<<<(unsigned)(need_ctas < wgrid ? need_ctas : wgrid), NTW, kBinsWarpSmem, stream>>>(
-            w.plan, S, N, (uint32_t)hp.tiles_per_learner, T, dW, R, w.big, hp.big_per_learner, w.tile_tab, w.pool);
+            w.plan, S, N, (uint32_t)hp.tiles_per_learner, T, dW, R, w.big, hp.big_per_learner, w.tile_tab, w.pool,
+            defer, pending, w.sent, scales, totals, (uint64_t)cap);
         if ((rc = check_launch("ada_bins_warp"))) return rc;
     }
     if (T > 0 && any_other) {
@@ -1066,10 +1155,28 @@ int adacomp_launch(const int64_t* off, int S, const int32_t* lt, int K, const fl
         }
         ada_emit<<<(unsigned)sm_count() * 6, NT, smem, stream>>>(
             w.plan, S, N, (uint32_t)hp.tiles_per_learner, (uint32_t)hp.groups_per_learner, w.tile_tab, w.grp_rel,
-            w.pool, counts, scales, R, out, (uint64_t)cap, K, totals);
+            w.pool, counts, scales, R, out, (uint64_t)cap, K, totals, defer);
         if ((rc = check_launch("ada_emit"))) return rc;
     }
     return GCSGD_OK;
+}
+
+int adacomp_settle_launch(const int64_t* off, int S, const int32_t* lt, int K, float* R, const gcsgd_pair* out,
+                          int64_t cap, const int64_t* counts, const int64_t* totals, void* ws, size_t ws_bytes,
+                          cudaStream_t stream) {
+    using namespace ada;
+    HostPlan hp;
+    host_plan(off, lt, S, &hp);
+    Workspace w;
+    const size_t need = layout(S, K, off[S], hp, ws, &w);
+    if (ws_bytes < need)
+        return set_error(GCSGD_ERR_WORKSPACE, "adacomp_settle: workspace of %zu bytes, %zu needed", ws_bytes, need);
+    if (K * S == 0 || off[S] == 0) return GCSGD_OK;
+    int rc;
+    if ((rc = launch_plan(off, S, lt, K, hp, w, stream))) return rc;  // the plan, whatever the workspace holds
+    LaunchScope ls("ada_settle", stream);
+    ada_settle<<<(unsigned)(K * S), NT, 0, stream>>>(w.plan, S, (uint64_t)off[S], counts, totals, (uint64_t)cap, out, R);
+    return check_launch("ada_settle");
 }
 
 }  // namespace gcsgd

@@ -20,7 +20,10 @@ namespace gcsgd {
 size_t adacomp_workspace_bytes(const int64_t* off, const int32_t* lt, int S, int K, int64_t cap);
 int adacomp_launch(const int64_t* off, int S, const int32_t* lt, int K, const float* dW, float* R, gcsgd_pair* out,
                    int64_t cap, int64_t* counts, float* scales, int64_t* totals, void* ws, size_t ws_bytes,
-                   cudaStream_t stream);
+                   cudaStream_t stream, int defer, int pending);
+int adacomp_settle_launch(const int64_t* off, int S, const int32_t* lt, int K, float* R, const gcsgd_pair* out,
+                          int64_t cap, const int64_t* counts, const int64_t* totals, void* ws, size_t ws_bytes,
+                          cudaStream_t stream);
 int spavg_launch(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int K, int64_t n, float* out,
                  cudaStream_t stream, bool update, float lr);
 size_t spavg_ws_bytes(int K, int64_t n);
@@ -322,10 +325,9 @@ int gcsgd_adacomp_workspace_size(const int64_t* seg_offsets, int32_t n_seg, cons
     return GCSGD_OK;
 }
 
-int adacomp_compress(const int64_t* seg_offsets, int32_t n_seg, const int32_t* lt, int32_t K, const float* dW,
-                     float* residue, gcsgd_pair* out, int64_t cap, int64_t* counts, float* scales, int64_t* totals,
-                     void* workspace, size_t workspace_bytes, void* stream) {
-    const char* fn = "adacomp_compress";
+static int adacomp_check(const char* fn, const int64_t* seg_offsets, int32_t n_seg, const int32_t* lt, int32_t K,
+                         const float* dW, float* residue, gcsgd_pair* out, int64_t cap, int64_t* counts,
+                         float* scales, int64_t* totals, void* workspace, size_t workspace_bytes) {
     int rc;
     if ((rc = check_layout(fn, seg_offsets, n_seg))) return rc;
     if (!lt) return set_error(GCSGD_ERR_INVALID_ARG, "%s: lt is NULL", fn);
@@ -338,10 +340,50 @@ int adacomp_compress(const int64_t* seg_offsets, int32_t n_seg, const int32_t* l
     if (!counts || !scales || !totals)
         return set_error(GCSGD_ERR_INVALID_ARG, "%s: counts, scales and totals must be non-NULL", fn);
     if (cap > 0 && !out) return set_error(GCSGD_ERR_INVALID_ARG, "%s: out is NULL", fn);
+    return check_ws(fn, workspace, workspace_bytes, adacomp_workspace_bytes(seg_offsets, lt, n_seg, K, cap));
+}
+
+int adacomp_compress(const int64_t* seg_offsets, int32_t n_seg, const int32_t* lt, int32_t K, const float* dW,
+                     float* residue, gcsgd_pair* out, int64_t cap, int64_t* counts, float* scales, int64_t* totals,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = adacomp_check("adacomp_compress", seg_offsets, n_seg, lt, K, dW, residue, out, cap, counts, scales,
+                           totals, workspace, workspace_bytes);
+    if (rc) return rc;
+    return adacomp_launch(seg_offsets, n_seg, lt, K, dW, residue, out, cap, counts, scales, totals, workspace,
+                          workspace_bytes, (cudaStream_t)stream, 0, 0);
+}
+
+int adacomp_compress_deferred(const int64_t* seg_offsets, int32_t n_seg, const int32_t* lt, int32_t K,
+                              const float* dW, float* residue, gcsgd_pair* out, int64_t cap, int64_t* counts,
+                              float* scales, int64_t* totals, int32_t pending, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+    const char* fn = "adacomp_compress_deferred";
+    int rc = adacomp_check(fn, seg_offsets, n_seg, lt, K, dW, residue, out, cap, counts, scales, totals, workspace,
+                           workspace_bytes);
+    if (rc) return rc;
+    if (pending != 0 && pending != 1) return set_error(GCSGD_ERR_INVALID_ARG, "%s: pending = %d, not 0 or 1", fn, pending);
+    return adacomp_launch(seg_offsets, n_seg, lt, K, dW, residue, out, cap, counts, scales, totals, workspace,
+                          workspace_bytes, (cudaStream_t)stream, 1, pending);
+}
+
+int adacomp_settle(const int64_t* seg_offsets, int32_t n_seg, const int32_t* lt, int32_t K, float* residue,
+                   const gcsgd_pair* out, int64_t cap, const int64_t* counts, const int64_t* totals, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+    const char* fn = "adacomp_settle";
+    int rc;
+    if ((rc = check_layout(fn, seg_offsets, n_seg))) return rc;
+    if (!lt) return set_error(GCSGD_ERR_INVALID_ARG, "%s: lt is NULL", fn);
+    for (int s = 0; s < n_seg; ++s)
+        if (lt[s] < 1) return set_error(GCSGD_ERR_INVALID_ARG, "%s: lt[%d] = %d < 1", fn, s, lt[s]);
+    if (K < 1) return set_error(GCSGD_ERR_INVALID_ARG, "%s: K = %d < 1", fn, K);
+    if (cap < 0 || cap >= (int64_t)1 << 32) return set_error(GCSGD_ERR_INVALID_ARG, "%s: cap outside [0, 2^32)", fn);
+    if (seg_offsets[n_seg] > 0 && !residue) return set_error(GCSGD_ERR_INVALID_ARG, "%s: residue is NULL", fn);
+    if (!counts || !totals) return set_error(GCSGD_ERR_INVALID_ARG, "%s: counts and totals must be non-NULL", fn);
+    if (cap > 0 && !out) return set_error(GCSGD_ERR_INVALID_ARG, "%s: out is NULL", fn);
     if ((rc = check_ws(fn, workspace, workspace_bytes, adacomp_workspace_bytes(seg_offsets, lt, n_seg, K, cap))))
         return rc;
-    return adacomp_launch(seg_offsets, n_seg, lt, K, dW, residue, out, cap, counts, scales, totals, workspace,
-                          workspace_bytes, (cudaStream_t)stream);
+    return adacomp_settle_launch(seg_offsets, n_seg, lt, K, residue, out, cap, counts, totals, workspace,
+                                 workspace_bytes, (cudaStream_t)stream);
 }
 
 static int check_average(const char* fn, const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int32_t K,

@@ -241,6 +241,40 @@ int adacomp_compress(const int64_t* seg_offsets, int32_t n_seg, const int32_t* l
                      gcsgd_pair* out, int64_t cap, int64_t* counts, float* scales, int64_t* totals,
                      void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * The same step with the residue fix-up deferred to the next call
+ * ("AdaComp ...", Proposed method: the residue keeps what was not sent; the
+ * order of the fp32 operations is unchanged, so every list, count, scale and
+ * residue is bit-identical to adacomp_compress over the same calls).  In the
+ * segments with 4 <= L_T <= 512 the sent entries' R = G - sign(G)*scale is
+ * not written at the end of the call: R keeps G there, the workspace keeps
+ * the call's selection bits, and the next deferred call subtracts sign(R) *
+ * scale at those bits while it reads R to form G = R + dW, which saves the
+ * scattered read-modify-write of R per sent entry.  Other segments are fixed
+ * at once, as in adacomp_compress.
+ * pending     0: R is a settled residue (the first call, or after
+ *             adacomp_settle); 1: the previous call on this R was deferred,
+ *             and out, counts, scales, totals and the workspace still hold
+ *             what it wrote.
+ * Everything else as for adacomp_compress.  Before R is read as a residue,
+ * call adacomp_settle.
+ */
+int adacomp_compress_deferred(const int64_t* seg_offsets, int32_t n_seg, const int32_t* lt, int32_t K,
+                              const float* dW, float* residue, gcsgd_pair* out, int64_t cap, int64_t* counts,
+                              float* scales, int64_t* totals, int32_t pending, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
+ * Applies the fix-up a deferred call left pending: R[i] -= v for every
+ * (i, v) of the message in out, in the 4 <= L_T <= 512 segments of every
+ * learner that sent (totals[k] <= cap), one fp32 subtraction each.  out,
+ * counts and totals: the deferred call's; workspace: any workspace of the
+ * layout's size (the plan is rebuilt).  Errors as for adacomp_compress.
+ */
+int adacomp_settle(const int64_t* seg_offsets, int32_t n_seg, const int32_t* lt, int32_t K, float* residue,
+                   const gcsgd_pair* out, int64_t cap, const int64_t* counts, const int64_t* totals,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
 /* ------------------------------------------------------- sparse average */
 
 /*
