@@ -510,18 +510,20 @@ __global__ void __launch_bounds__(NTW, 6) ada_bins_warp(const SegPlan* __restric
         const bool cal = ((uintptr_t)Rc & 15) == 0;
         const uint32_t clen = m.clen, bpw = m.bpw, L = m.L;
         float4 Gv[4], Dv[4];
-        const uint32_t pbits = m.pfix ? (uint32_t)sbits[cs * 32 + lane] : 0u;  // bit 4r+j: element j of round r
+        if (m.pfix) {  // the previous call's deferred fix-up, R -= sign(R) * scale, on this lane's staged values
+            float* sRw = const_cast<float*>(sR);
+            for (uint32_t pb = sbits[cs * 32 + lane]; pb; pb &= pb - 1u) {  // bit 4r+j: element j of round r
+                const uint32_t b = (uint32_t)__ffs(pb) - 1u;
+                const uint32_t e = 4u * (lane + 32u * (b >> 2)) + (b & 3u);
+                const float g = sRw[e];
+                sRw[e] = __fsub_rn(g, g > 0.0f ? m.pscale : -m.pscale);
+            }
+        }
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const uint32_t e = 4u * (lane + 32 * r);
             Dv[r] = *reinterpret_cast<const float4*>(sD + e);
             Gv[r] = *reinterpret_cast<const float4*>(sR + e);
-            if (pbits & (0xFu << (4 * r))) {  // the previous call's deferred fix-up: R -= sign(R) * scale
-                float* g4 = &Gv[r].x;
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if ((pbits >> (4 * r + j)) & 1u) g4[j] = __fsub_rn(g4[j], g4[j] > 0.0f ? m.pscale : -m.pscale);
-            }
             Gv[r].x = __fadd_rn(Gv[r].x, Dv[r].x);
             Gv[r].y = __fadd_rn(Gv[r].y, Dv[r].y);
             Gv[r].z = __fadd_rn(Gv[r].z, Dv[r].z);
