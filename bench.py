@@ -425,7 +425,7 @@ class AdaCompPath(DgcPath):
     def step_update(self, g, w, lr, state=None):
         (R,) = state or self.state
         out, totals = self.obj(g, R)
-        self.gc.sparse_average_update(out, totals, self.N, lr, w)
+        self.gc.sparse_average_update_ws(out, totals, self.N, lr, w, self.ws)
 
     def extra(self):
         tot = self.obj.totals.cpu()
@@ -695,7 +695,8 @@ def run_gpu(args):
         tr_u = gc.trace_read()
         ms_u = max_over_ranks(h0.elapsed_time(h1) / args.steps, dev)
         nu, tu = tr_u.get("spavg_update", (0, 0.0))
-        fused = {"step": "compress + sparse_average_update (weights stepped on the carried indices)",
+        fused = {"step": "compress + " + ("sparse_average_update_ws" if isinstance(path, AdaCompPath) else
+                                          "sparse_average_update") + " (weights stepped on the carried indices)",
                  "value": job_gbs(world, 4.0 * K * N, ms_u), "unit": "GB/s", "ms_per_step": ms_u,
                  "update_ms_per_launch": tu / max(nu, 1)}
 

@@ -95,6 +95,7 @@ def lib():
         L.gcsgd_sparse_average_workspace_size.argtypes = [i32, i64, vp]
         L.sparse_average_ws.argtypes = [vp, i64, vp, i32, i64, vp, vp, sz, vp]
         L.gcsgd_sparse_average_status.argtypes = [vp, i32, i64, vp, vp]
+        L.sparse_average_update_ws.argtypes = [vp, i64, vp, i32, i64, f32, vp, vp, sz, vp]
         L.dcd_step.argtypes = [i32, i64, vp, vp, vp, f32, f64, u64, u32, vp]
         L.ecd_step.argtypes = [i32, i64, vp, vp, vp, vp, vp, f32, f64, u64, u32, vp]
         L.dcd_step_rows.argtypes = [i32, i64, i64, vp, vp, vp, f32, f64, u64, u32, vp, vp, i64, vp, vp]
@@ -472,6 +473,19 @@ def sparse_average_ws(lists, counts, n: int, out, workspace, stream=None):
     _check("sparse_average_ws", lib().sparse_average_ws(
         _dev(lists, "lists", torch.int32), int(cap), _dev(counts, "counts", torch.int64), int(K), int(n),
         _dev(out, "out", torch.float32), _dev(workspace, "workspace", torch.uint8), int(workspace.numel()),
+        _stream(stream)))
+
+
+def sparse_average_update_ws(lists, counts, n: int, lr: float, w, workspace, stream=None):
+    """w[j] -= lr * (K-way average)[j] at every carried index, through the
+    cursor-table kernels (see sparse_average_update_ws in include/gcsgd.h)."""
+    import torch
+    K, cap = lists.shape[0], lists.shape[1]
+    if counts.numel() != K:
+        raise ValueError("counts must have K entries")
+    _check("sparse_average_update_ws", lib().sparse_average_update_ws(
+        _dev(lists, "lists", torch.int32), int(cap), _dev(counts, "counts", torch.int64), int(K), int(n),
+        float(lr), _dev(w, "w", torch.float32), _dev(workspace, "workspace", torch.uint8), int(workspace.numel()),
         _stream(stream)))
 
 

@@ -28,7 +28,7 @@ int spavg_launch(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, in
                  cudaStream_t stream, bool update, float lr);
 size_t spavg_ws_bytes(int K, int64_t n);
 int spavg_ws_launch(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int K, int64_t n, float* out,
-                    void* ws, cudaStream_t stream);
+                    void* ws, cudaStream_t stream, bool update, float lr);
 int spavg_ws_status(const void* ws, int K, int64_t n, cudaStream_t stream, int32_t* status);
 int dcd_launch(int n, int64_t d, const float* w, float* xhat, const float* grad, float gamma, double p, uint64_t seed,
                uint32_t t, cudaStream_t stream);
@@ -423,7 +423,22 @@ int sparse_average_ws(const gcsgd_pair* lists, int64_t cap, const int64_t* count
     if (workspace_bytes < spavg_ws_bytes(K, n))
         return set_error(GCSGD_ERR_WORKSPACE, "%s: workspace of %zu bytes, %zu needed", fn, workspace_bytes,
                          spavg_ws_bytes(K, n));
-    return spavg_ws_launch(lists, cap, counts, K, n, out, workspace, (cudaStream_t)stream);
+    return spavg_ws_launch(lists, cap, counts, K, n, out, workspace, (cudaStream_t)stream, false, 0.0f);
+}
+
+int sparse_average_update_ws(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int32_t K, int64_t n,
+                             float lr, float* w, void* workspace, size_t workspace_bytes, void* stream) {
+    const char* fn = "sparse_average_update_ws";
+    int rc = check_average(fn, lists, cap, counts, K, n, w);
+    if (rc) return rc;
+    if (!isfinite(lr)) return set_error(GCSGD_ERR_INVALID_ARG, "%s: lr is not finite", fn);
+    if (n == 0) return GCSGD_OK;
+    if (!workspace) return set_error(GCSGD_ERR_INVALID_ARG, "%s: workspace is NULL", fn);
+    if (((uintptr_t)workspace & 255) != 0) return set_error(GCSGD_ERR_INVALID_ARG, "%s: workspace not 256-byte aligned", fn);
+    if (workspace_bytes < spavg_ws_bytes(K, n))
+        return set_error(GCSGD_ERR_WORKSPACE, "%s: workspace of %zu bytes, %zu needed", fn, workspace_bytes,
+                         spavg_ws_bytes(K, n));
+    return spavg_ws_launch(lists, cap, counts, K, n, w, workspace, (cudaStream_t)stream, true, lr);
 }
 
 int gcsgd_sparse_average_status(const void* workspace, int32_t K, int64_t n, void* stream, int32_t* status) {

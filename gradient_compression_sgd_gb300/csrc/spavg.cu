@@ -840,10 +840,16 @@ __device__ __forceinline__ Range range_of(const gcsgd_pair* lists, uint64_t cap,
     return R;
 }
 
+// UPDATE: instead of writing the average, step the weights in `out` at the
+// carried indices, w <- w - lr * avg (one rounding each; every other weight
+// keeps its bits): the consumers mark the carried positions in a bitmap (two,
+// by region parity, so the next region's is cleared while this one is read)
+// and read the region's weights while the lists are added.
+template <bool UPDATE>
 __global__ void __launch_bounds__(NTR, 2) spavg_region(const gcsgd_pair* __restrict__ lists, uint64_t cap,
                                                     const int64_t* __restrict__ counts, int K, uint64_t n,
                                                     float* __restrict__ out, const uint32_t* __restrict__ lo,
-                                                    uint64_t G, uint32_t* __restrict__ status) {
+                                                    uint64_t G, uint32_t* __restrict__ status, float lr) {
     extern __shared__ __align__(16) unsigned char smem[];
     float* acc = reinterpret_cast<float*>(smem);
     gcsgd_pair* stage = reinterpret_cast<gcsgd_pair*>(smem + kRegion * sizeof(float));
@@ -851,6 +857,7 @@ __global__ void __launch_bounds__(NTR, 2) spavg_region(const gcsgd_pair* __restr
     uint32_t* cnt = arr + 4 * kNBuf * K;
     __shared__ __align__(8) uint64_t full[kNBuf], empty[kNBuf];
     __shared__ uint32_t s_total[kNBuf];
+    __shared__ uint32_t touched[UPDATE ? 2 : 1][UPDATE ? kRegion / 32 : 1];
     auto PA = [&](int b) { return arr + (4 * b + 0) * K; };
     auto PL = [&](int b) { return arr + (4 * b + 1) * K; };
     auto PM = [&](int b) { return arr + (4 * b + 2) * K; };
@@ -861,6 +868,8 @@ __global__ void __launch_bounds__(NTR, 2) spavg_region(const gcsgd_pair* __restr
     for (int k = threadIdx.x; k < K; k += NTR) cnt[k] = clamp_count(counts[k], cap);
     for (uint32_t j = threadIdx.x * 4; j < kRegion; j += NTR * 4)
         *reinterpret_cast<float4*>(acc + j) = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (UPDATE)
+        for (uint32_t q = threadIdx.x; q < 2 * (kRegion / 32); q += NTR) (&touched[0][0])[q] = 0u;
     if (threadIdx.x == 0) {
         for (int b = 0; b < kNBuf; ++b) {
             mbar_init_n(&full[b], kFullArrivals);
@@ -990,6 +999,23 @@ __global__ void __launch_bounds__(NTR, 2) spavg_region(const gcsgd_pair* __restr
         const uint32_t R0 = (uint32_t)(g * kRegion);
         const uint32_t rlen = (uint32_t)((uint64_t)R0 + kRegion < n ? kRegion : n - R0);
         const uint32_t* pl = PL(b);
+        uint32_t* tb = touched[UPDATE ? (i & 1) : 0];
+        constexpr int kW = UPDATE ? (int)(kRegion / (4 * NC)) : 1;
+        float4 wv[kW];  // UPDATE: the region's weights of this thread, read while the lists are added
+        if (UPDATE) {
+#pragma unroll
+            for (int r = 0; r < kW; ++r) {
+                const uint32_t j = 4u * (ct + r * NC);
+                const float* wj = out + R0 + j;
+                wv[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (al && j + 4 <= rlen) {
+                    wv[r] = *reinterpret_cast<const float4*>(wj);
+                } else {
+                    float* ww = &wv[r].x;
+                    for (uint32_t t = 0; t < 4 && j + t < rlen; ++t) ww[t] = wj[t];
+                }
+            }
+        }
         if (s_total[b] != kSlow) {
             const gcsgd_pair* buf = stage + (size_t)b * kRStage;
             const uint32_t* st = ST(b);
@@ -1026,12 +1052,18 @@ __global__ void __launch_bounds__(NTR, 2) spavg_region(const gcsgd_pair* __restr
                     }
 #pragma unroll
                     for (int r = 0; r < kPer; ++r)
-                        if (in[r]) acc[d[r]] = __fadd_rn(a[r], e[r].val);
+                        if (in[r]) {
+                            acc[d[r]] = __fadd_rn(a[r], e[r].val);
+                            if (UPDATE) atomicOr(&tb[d[r] >> 5], 1u << (d[r] & 31));
+                        }
                 }
                 for (uint32_t q = ct + kPer * NC; q < len; q += NC) {  // longer ranges
                     const gcsgd_pair e = S[q];
                     const uint32_t d = e.idx - R0;
-                    if (d < rlen) acc[d] = __fadd_rn(acc[d], e.val);
+                    if (d < rlen) {
+                        acc[d] = __fadd_rn(acc[d], e.val);
+                        if (UPDATE) atomicOr(&tb[d >> 5], 1u << (d & 31));
+                    }
                 }
                 consumer_sync();  // list k's adds land before list k+1's
             }
@@ -1044,7 +1076,10 @@ __global__ void __launch_bounds__(NTR, 2) spavg_region(const gcsgd_pair* __restr
                 for (uint32_t q = ct; q < len; q += NC) {
                     const gcsgd_pair e = S[q];
                     const uint32_t d = e.idx - R0;
-                    if (d < rlen) acc[d] = __fadd_rn(acc[d], e.val);
+                    if (d < rlen) {
+                        acc[d] = __fadd_rn(acc[d], e.val);
+                        if (UPDATE) atomicOr(&tb[d >> 5], 1u << (d & 31));
+                    }
                 }
                 consumer_sync();
             }
@@ -1053,8 +1088,33 @@ __global__ void __launch_bounds__(NTR, 2) spavg_region(const gcsgd_pair* __restr
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[b]);
-        // the region's average, written once; acc re-zeroed for the next region
         float* o = out + R0;
+        if (UPDATE) {  // the carried weights stepped, each float4 written only where one of its values is carried
+            uint32_t* tn = touched[(i + 1) & 1];  // the next region's bitmap, last read a region ago
+            for (int q = ct; q < (int)(kRegion / 32); q += NC) tn[q] = 0u;
+#pragma unroll
+            for (int r = 0; r < kW; ++r) {
+                const uint32_t j = 4u * (ct + r * NC);
+                const float4 q = *reinterpret_cast<const float4*>(acc + j);
+                *reinterpret_cast<float4*>(acc + j) = make_float4(0.f, 0.f, 0.f, 0.f);
+                const uint32_t bits = j < rlen ? (tb[j >> 5] >> (j & 31)) & 0xFu : 0u;
+                if (!bits) continue;
+                const float* qq = &q.x;
+                float* xx = &wv[r].x;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    if ((bits >> c) & 1u) xx[c] = __fsub_rn(xx[c], __fmul_rn(lr, div_k(qq[c], fk, inv_k, pow2)));
+                if (al && j + 4 <= rlen) {
+                    *reinterpret_cast<float4*>(o + j) = wv[r];
+                } else {
+                    for (uint32_t t = 0; t < 4 && j + t < rlen; ++t)
+                        if ((bits >> t) & 1u) o[j + t] = xx[t];
+                }
+            }
+            consumer_sync();  // acc zeroed and the bitmaps read before the next region's adds
+            continue;
+        }
+        // the region's average, written once; acc re-zeroed for the next region
 #pragma unroll
         for (int r = 0; r < (int)(kRegion / (4 * NC)); ++r) {
             const uint32_t j = 4u * (ct + r * NC);
@@ -1152,8 +1212,11 @@ static size_t spavg_table_bytes(int K, int64_t n) {
 
 size_t spavg_ws_bytes(int K, int64_t n) { return spavg_table_bytes(K, n) + 256; }  // the table, then the status word
 
+// update: step the weights in `out` (w -= lr * avg at the carried indices)
+// instead of writing the dense average.
 int spavg_ws_launch(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int K, int64_t n, float* out,
-                    void* ws, cudaStream_t stream) {
+                    void* ws, cudaStream_t stream, bool update, float lr) {
+    const char* fn = update ? "sparse_average_update_ws" : "sparse_average_ws";
     using namespace spavg;
     if (n == 0) return GCSGD_OK;
     // sparse lists (K * cap < n / 4) stay on the tile kernel, and lists off
@@ -1163,8 +1226,8 @@ int spavg_ws_launch(const gcsgd_pair* lists, int64_t cap, const int64_t* counts,
         const cudaError_t e =
             cudaMemsetAsync(static_cast<unsigned char*>(ws) + spavg_table_bytes(K, n), 0, sizeof(uint32_t), stream);
         if (e != cudaSuccess)
-            return set_error(GCSGD_ERR_CUDA, "sparse_average_ws: status clear failed: %s", cudaGetErrorString(e));
-        return spavg_launch(lists, cap, counts, K, n, out, stream, false, 0.0f);
+            return set_error(GCSGD_ERR_CUDA, "%s: status clear failed: %s", fn, cudaGetErrorString(e));
+        return spavg_launch(lists, cap, counts, K, n, out, stream, update, lr);
     }
     const uint64_t G = ((uint64_t)n + kRegion - 1) / kRegion;
     uint32_t* lo = static_cast<uint32_t*>(ws);
@@ -1179,20 +1242,20 @@ int spavg_ws_launch(const gcsgd_pair* lists, int64_t cap, const int64_t* counts,
         kRegion * sizeof(float) + kNBuf * kRStage * sizeof(gcsgd_pair) + sizeof(uint32_t) * (4 * kNBuf + 1) * (size_t)K;
     constexpr size_t kMaxSmem =
         kRegion * sizeof(float) + kNBuf * kRStage * sizeof(gcsgd_pair) + sizeof(uint32_t) * (4 * kNBuf + 1) * 512;
-    static int occ_of[64][2] = {};  // per device: resident CTAs for K <= 64 and for larger K
+    static int occ_of[64][2][2] = {};  // per device and mode: resident CTAs for K <= 64 and for larger K
     int dev = 0;
     cudaGetDevice(&dev);
-    const int kc = K <= 64 ? 0 : 1;
-    if (dev >= 64) return set_error(GCSGD_ERR_CUDA, "sparse_average_ws: device ordinal %d >= 64", dev);
-    if (!occ_of[dev][kc]) {
+    const int kc = K <= 64 ? 0 : 1, um = update ? 1 : 0;
+    if (dev >= 64) return set_error(GCSGD_ERR_CUDA, "%s: device ordinal %d >= 64", fn, dev);
+    if (!occ_of[dev][um][kc]) {
         int occ = 0;
-        if (cudaFuncSetAttribute(spavg_region, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem) !=
-                cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, spavg_region, NTR, kc ? kMaxSmem : smem) != cudaSuccess)
-            return set_error(GCSGD_ERR_CUDA, "sparse_average_ws: cannot set up the region kernel");
-        occ_of[dev][kc] = occ > 0 ? occ : 1;
+        const void* kern = update ? (const void*)spavg_region<true> : (const void*)spavg_region<false>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, NTR, kc ? kMaxSmem : smem) != cudaSuccess)
+            return set_error(GCSGD_ERR_CUDA, "%s: cannot set up the region kernel", fn);
+        occ_of[dev][um][kc] = occ > 0 ? occ : 1;
     }
-    uint64_t grid = (uint64_t)sms * (uint64_t)occ_of[dev][kc];
+    uint64_t grid = (uint64_t)sms * (uint64_t)occ_of[dev][um][kc];
     if (grid > G) grid = G;
     {
         LaunchScope ls("spavg_checkpoints", stream);
@@ -1201,9 +1264,13 @@ int spavg_ws_launch(const gcsgd_pair* lists, int64_t cap, const int64_t* counts,
         const int rc = check_launch("spavg_checkpoints");
         if (rc) return rc;
     }
-    LaunchScope ls("spavg", stream);
-    spavg_region<<<(unsigned)grid, NTR, smem, stream>>>(lists, (uint64_t)cap, counts, K, (uint64_t)n, out, lo, G,
-                                                       status);
+    LaunchScope ls(update ? "spavg_update" : "spavg", stream);
+    if (update)
+        spavg_region<true><<<(unsigned)grid, NTR, smem, stream>>>(lists, (uint64_t)cap, counts, K, (uint64_t)n, out,
+                                                                  lo, G, status, lr);
+    else
+        spavg_region<false><<<(unsigned)grid, NTR, smem, stream>>>(lists, (uint64_t)cap, counts, K, (uint64_t)n, out,
+                                                                   lo, G, status, 0.0f);
     return check_launch("spavg_region");
 }
 

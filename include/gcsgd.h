@@ -326,8 +326,25 @@ int gcsgd_sparse_average_workspace_size(int32_t K, int64_t n, size_t* bytes);
 int sparse_average_ws(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int32_t K,
                       int64_t n, float* out, void* workspace, size_t workspace_bytes, void* stream);
 
-/* The status word of the last sparse_average_ws call made with `workspace`
- * for this K and n (0: every copy completed; 1: a copy timed out).  Waits for
+/*
+ * sparse_average_update with device scratch: the same weights, bit for bit
+ * (the learner-order average, one fp32 divide by K, then w <- w - lr * avg
+ * with one rounding for the product and one for the difference, at every
+ * index some list carries; every other weight keeps its bits).  Dense,
+ * 8-byte aligned lists take the cursor table and region kernel of
+ * sparse_average_ws, in update mode: the carried positions are marked in a
+ * bitmap while the lists are added, the region's weights are read
+ * meanwhile, and only the 16-byte groups holding a carried weight are
+ * written back.  Other lists take sparse_average_update's kernels.
+ * lists, cap, counts, K, n, lr, w: as for sparse_average_update;
+ * workspace, workspace_bytes, errors, the status word: as for
+ * sparse_average_ws.
+ */
+int sparse_average_update_ws(const gcsgd_pair* lists, int64_t cap, const int64_t* counts, int32_t K,
+                             int64_t n, float lr, float* w, void* workspace, size_t workspace_bytes, void* stream);
+
+/* The status word of the last sparse_average_ws or sparse_average_update_ws
+ * call made with `workspace` for this K and n (0: every copy completed; 1: a copy timed out).  Waits for
  * `stream`, then reads 4 bytes.  Errors: GCSGD_ERR_INVALID_ARG for K outside
  * [1, 512], n outside [1, 2^32] or a NULL pointer; GCSGD_ERR_CUDA when the
  * copy or the wait fails. */

@@ -256,3 +256,112 @@ def test_ws_adacomp_full_size(cuda_lib):
     want = oracle.sparse_average(gc.pair_indices(out[:, :m]).cpu().numpy().astype(np.uint32),
                                  gc.pair_values(out[:, :m]).cpu().numpy(), tot, N)
     np.testing.assert_array_equal(avg.cpu().numpy().view(np.uint32), want.view(np.uint32))
+
+
+# ---------------------------------------- averaged weight update, workspace
+
+def run_update_ws(gc, idx, val, counts, n, lr, seed=0, w_offset=0, list_offset_words=0, ws=None):
+    """Weights after sparse_average_update_ws against the oracle's update, bit
+    for bit (untouched weights included: -0.0 and a NaN payload among them;
+    a carried NaN weight is NaN on both sides)."""
+    import torch
+    K, cap = idx.shape
+    rng = np.random.default_rng(seed)
+    w0 = rng.standard_normal(max(n, 1)).astype(np.float32)
+    if n > 2:
+        w0[n // 2] = -0.0
+        w0[n - 1] = np.frombuffer(np.uint32(0x7FC00321).tobytes(), np.float32)[0]
+    flat = torch.zeros(max(n, 1) + w_offset + 3, dtype=torch.float32)
+    flat[:] = float("nan")
+    flat[w_offset:w_offset + max(n, 1)] = torch.from_numpy(w0)
+    buf = flat.cuda()
+    w_g = buf[w_offset:w_offset + max(n, 1)]
+    if ws is None:
+        ws = torch.empty(gc.sparse_average_workspace_size(K, n), dtype=torch.uint8, device="cuda")
+    gc.sparse_average_update_ws(pairs_of(idx, val, list_offset_words),
+                                torch.from_numpy(np.asarray(counts, np.int64)).cuda(), n, lr, w_g, ws)
+    torch.cuda.synchronize()
+    if n > 0:
+        assert gc.sparse_average_status(ws, K, n) == 0
+    rest = buf.cpu().numpy()
+    assert np.isnan(rest[:w_offset]).all() and np.isnan(rest[w_offset + max(n, 1):]).all()
+    want = oracle.sparse_average_update(idx, val, np.asarray(counts, np.int64), n, lr, w0.copy())
+    got = w_g.cpu().numpy()[:n]
+    both_nan = np.isnan(got) & np.isnan(want[:n])
+    carried = np.zeros(n, bool)
+    for k in range(K):
+        carried[idx[k, :counts[k]]] = True
+    keep = ~(both_nan & carried)
+    np.testing.assert_array_equal(got.view(np.uint32)[keep], want[:n].view(np.uint32)[keep])
+    np.testing.assert_array_equal(np.isnan(got), np.isnan(want[:n]))
+
+
+@pytest.mark.parametrize("K", [1, 2, 4, 8, 33])
+@pytest.mark.parametrize("n", [1, 4095, 8193, 100003])
+@pytest.mark.parametrize("cap_frac", [0.01, 0.3])
+def test_update_ws_random_lists(cuda_lib, K, n, cap_frac):
+    rng = np.random.default_rng(K * 17 + n + int(cap_frac * 100))
+    cap = max(1, int(cap_frac * n))
+    idx, val, counts = random_lists(rng, K, n, cap)
+    run_update_ws(cuda_lib, idx, val, counts, n, 0.05, seed=K + n)
+
+
+@pytest.mark.parametrize("K,n,fill", [(8, 3 * 4096 + 77, 1.0), (3, 200000, 0.6), (5, 77777, 0.12)])
+def test_update_ws_staged_and_overflowing_regions(cuda_lib, K, n, fill):
+    """Regions that fit the stage (AdaComp-like density) and regions added
+    from global memory (full lists), with a negative learning rate."""
+    rng = np.random.default_rng(K + n)
+    idx, val, counts = random_lists(rng, K, n, n, fill=fill)
+    run_update_ws(cuda_lib, idx, val, counts, n, -0.01, seed=K)
+
+
+@pytest.mark.parametrize("w_offset,list_offset_words", [(1, 0), (3, 0), (2, 1)])
+def test_update_ws_unaligned(cuda_lib, w_offset, list_offset_words):
+    """Weights off the 16-byte boundary (scalar writes of the carried values
+    only); lists 4 bytes off the 8-byte boundary (sparse_average_update)."""
+    rng = np.random.default_rng(w_offset * 5 + list_offset_words)
+    K, n = 4, 70001
+    idx, val, counts = random_lists(rng, K, n, 20000)
+    run_update_ws(cuda_lib, idx, val, counts, n, 0.1, seed=w_offset, w_offset=w_offset,
+                  list_offset_words=list_offset_words)
+
+
+def test_update_ws_512_lists_and_reuse(cuda_lib):
+    import torch
+    gc = cuda_lib
+    ws = torch.empty(gc.sparse_average_workspace_size(512, 300000), dtype=torch.uint8, device="cuda")
+    ws.fill_(0x5A)
+    rng = np.random.default_rng(7)
+    for K, n, cap in [(512, 20011, 60), (4, 300000, 30000), (8, 8193, 8193)]:
+        idx, val, counts = random_lists(rng, K, n, cap)
+        run_update_ws(gc, idx, val, counts, n, 0.02, seed=K, ws=ws)
+
+
+def test_update_ws_adacomp_full_size(cuda_lib):
+    """The K = 8 AdaComp messages of the LSTM + VGG-16 layout: the weights
+    after sparse_average_update_ws equal sparse_average_update's bit for bit,
+    and on a sample of 20,000 indices the oracle's update of those indices."""
+    import torch
+    gc = cuda_lib
+    w = wl.workload(3)
+    K, N = w.learners, w.n
+    a = gc.AdaComp(w.offsets, w.lt, K, N // 8)
+    R = torch.zeros((K, N), device="cuda")
+    out, totals = a(wl.gradients(w, 0, device="cuda"), R)
+    del R
+    g = torch.Generator(device="cpu").manual_seed(5)
+    w0 = torch.randn(N, generator=g).cuda()
+    w1, w2 = w0.clone(), w0.clone()
+    gc.sparse_average_update(out, totals, N, 0.03, w1)
+    ws = torch.empty(gc.sparse_average_workspace_size(K, N), dtype=torch.uint8, device="cuda")
+    gc.sparse_average_update_ws(out, totals, N, 0.03, w2, ws)
+    torch.cuda.synchronize()
+    assert gc.sparse_average_status(ws, K, N) == 0
+    assert torch.equal(w1.view(torch.int32), w2.view(torch.int32))
+    tot = totals.cpu().numpy()
+    m = int(tot.max())
+    idx = gc.pair_indices(out[:, :m]).cpu().numpy().astype(np.uint32)
+    val = gc.pair_values(out[:, :m]).cpu().numpy()
+    want = oracle.sparse_average_update(idx, val, tot, N, 0.03, w0.cpu().numpy().copy())
+    sample = np.random.default_rng(1).choice(N, size=20000, replace=False)
+    np.testing.assert_array_equal(w2.cpu().numpy()[sample].view(np.uint32), want[sample].view(np.uint32))
