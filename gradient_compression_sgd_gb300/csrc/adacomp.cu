@@ -614,10 +614,13 @@ __global__ void __launch_bounds__(NTW, 6) ada_bins_warp(const SegPlan* __restric
             if (lane >= d) incl += y;
         }
         const uint32_t wtot = __shfl_sync(kFull, incl, 31), excl = incl - packed;
-        if (lane == 0) {
-            const uint32_t W = (wtot & 0xFFu) + ((wtot >> 8) & 0xFFu) + ((wtot >> 16) & 0xFFu) + (wtot >> 24);
-            tile_tab[(uint64_t)m.k * tiles_per_learner + m.lt] = make_uint2(m.rel, W);
-        }
+        const uint32_t W = (wtot & 0xFFu) + ((wtot >> 8) & 0xFFu) + ((wtot >> 16) & 0xFFu) + (wtot >> 24);
+        // the chunk's records start at the first 128-byte boundary of its own
+        // pool slots [rel, rel + clen) when they fit after it (ada_emit then
+        // reads whole lines), else at rel
+        const uint32_t up = (uint32_t)(((16u - (uint32_t)(base & 15u)) & 15u));
+        const uint32_t at = W + up <= clen ? m.rel + up : m.rel;
+        if (lane == 0) tile_tab[(uint64_t)m.k * tiles_per_learner + m.lt] = make_uint2(at, W);
         // the candidates in rank order (rounds in order, lanes in order, bits in
         // order) into this chunk's stage, which every lane has read into its
         // registers; then one coalesced copy to the pool.  The stage is next
@@ -640,8 +643,7 @@ __global__ void __launch_bounds__(NTW, 6) ada_bins_warp(const SegPlan* __restric
             }
         }
         __syncwarp();
-        const uint32_t W = (wtot & 0xFFu) + ((wtot >> 8) & 0xFFu) + ((wtot >> 16) & 0xFFu) + (wtot >> 24);
-        uint2* dst = pool + base;
+        uint2* dst = pool + (uint64_t)m.k * N + at;
         for (uint32_t i = lane; i < W; i += 32) dst[i] = cst[i];
         __syncwarp();  // wb and the stage are rewritten later
     }
