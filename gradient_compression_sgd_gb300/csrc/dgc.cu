@@ -571,8 +571,9 @@ __global__ void __launch_bounds__(NT, 3) dgc_update(const SegPlan* __restrict__ 
 // factor masking).  Warp w owns one contiguous run of the items: a first
 // sweep counts its greater and equal keys (warp ballots), one barrier shares
 // the 16 warp counts, and a second sweep writes, ranking each item by ballots
-// inside its warp.  wsum: NTS / 32 words of shared memory.
-template <class Get>
+// inside its warp.  wsum: NTS / 32 words of shared memory.  R: rounds of 32
+// items whose loads are issued together (items read from global memory).
+template <int R = 1, class Get>
 __device__ void emit_in_order(Get get, uint32_t count, uint32_t T, uint32_t ties, const SegPlan& p,
                               gcsgd_pair* __restrict__ dst, float* __restrict__ u, float* __restrict__ v,
                               uint64_t ebase, uint2* wsum, uint32_t slot0 = 0) {
@@ -583,13 +584,22 @@ __device__ void emit_in_order(Get get, uint32_t count, uint32_t T, uint32_t ties
     const uint32_t hi = lo + per < count ? lo + per : count;
     const unsigned below = (1u << lane) - 1u;
     uint32_t ngt = 0, neq = 0;
-    for (uint32_t b = lo; b < hi; b += 32) {
-        const uint32_t i = b + lane;
-        uint32_t loc = 0, bits = 0;
-        if (i < hi) get(i, &loc, &bits);
-        const uint32_t key = bits & 0x7fffffffu;
-        ngt += __popc(__ballot_sync(kFull, i < hi && key > T));
-        neq += __popc(__ballot_sync(kFull, i < hi && key == T));
+    for (uint32_t b = lo; b < hi; b += 32 * R) {
+        uint32_t bits[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {  // every load of the R rounds in flight before the first ballot
+            const uint32_t i = b + 32 * r + lane;
+            uint32_t loc = 0;
+            bits[r] = 0;
+            if (i < hi) get(i, &loc, &bits[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint32_t i = b + 32 * r + lane;
+            const uint32_t key = bits[r] & 0x7fffffffu;
+            ngt += __popc(__ballot_sync(kFull, i < hi && key > T));
+            neq += __popc(__ballot_sync(kFull, i < hi && key == T));
+        }
     }
     if (lane == 0) wsum[warp] = make_uint2(ngt, neq);
     __syncthreads();
@@ -600,25 +610,34 @@ __device__ void emit_in_order(Get get, uint32_t count, uint32_t T, uint32_t ties
         eb += c.y;
     }
     if (ngt > 0 || (neq > 0 && eb < ties)) {
-        for (uint32_t b = lo; b < hi; b += 32) {
-            const uint32_t i = b + lane;
-            uint32_t loc = 0, bits = 0;
-            if (i < hi) get(i, &loc, &bits);
-            const uint32_t key = bits & 0x7fffffffu;
-            const bool gt = i < hi && key > T, eq = i < hi && key == T;
-            const unsigned mg = __ballot_sync(kFull, gt), me = __ballot_sync(kFull, eq);
-            const uint32_t g_before = gb + __popc(mg & below), e_before = eb + __popc(me & below);
-            const uint32_t slot = slot0 + g_before + (e_before < ties ? e_before : ties);
-            if ((gt || (eq && e_before < ties)) && slot < p.k && loc < p.n) {
-                gcsgd_pair pr;
-                pr.idx = p.off + loc;
-                pr.val = __uint_as_float(bits);
-                dst[slot] = pr;
-                u[ebase + loc] = 0.0f;
-                v[ebase + loc] = 0.0f;
+        for (uint32_t b = lo; b < hi; b += 32 * R) {
+            uint32_t locs[R], bits[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const uint32_t i = b + 32 * r + lane;
+                locs[r] = 0;
+                bits[r] = 0;
+                if (i < hi) get(i, &locs[r], &bits[r]);
             }
-            gb += __popc(mg);
-            eb += __popc(me);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const uint32_t i = b + 32 * r + lane;
+                const uint32_t key = bits[r] & 0x7fffffffu;
+                const bool gt = i < hi && key > T, eq = i < hi && key == T;
+                const unsigned mg = __ballot_sync(kFull, gt), me = __ballot_sync(kFull, eq);
+                const uint32_t g_before = gb + __popc(mg & below), e_before = eb + __popc(me & below);
+                const uint32_t slot = slot0 + g_before + (e_before < ties ? e_before : ties);
+                if ((gt || (eq && e_before < ties)) && slot < p.k && locs[r] < p.n) {
+                    gcsgd_pair pr;
+                    pr.idx = p.off + locs[r];
+                    pr.val = __uint_as_float(bits[r]);
+                    dst[slot] = pr;
+                    u[ebase + locs[r]] = 0.0f;
+                    v[ebase + locs[r]] = 0.0f;
+                }
+                gb += __popc(mg);
+                eb += __popc(me);
+            }
         }
     }
     __syncthreads();  // wsum is reused
@@ -1040,7 +1059,7 @@ __device__ void select_unit(const SelectArgs& A, const SelectSmem& M, int k, int
         const SelectResult r = radix_select_desc<NTS, 3, true>(
             [&](uint64_t i, uint32_t* key) { *key = mag_key(vseg[i]); return true; }, p.n, p.k, rs, false,
             reinterpret_cast<uint32_t*>(stage_raw), (uint32_t)(kStageBytes / sizeof(uint32_t)));
-        emit_in_order(
+        emit_in_order<8>(
             [&](uint32_t i, uint32_t* loc, uint32_t* bits) {
                 *loc = i;
                 *bits = __float_as_uint(vseg[i]);

@@ -120,15 +120,17 @@ def test_ties_and_zeros(cuda_lib, levels):
     run_dgc(cuda_lib, off, grads, 0.003, 0.5)
 
 
-def test_hint_above_the_kth_value_falls_back(cuda_lib):
+@pytest.mark.parametrize("n,density", [(40000, 0.003), (2359296, 0.001)])
+def test_hint_above_the_kth_value_falls_back(cuda_lib, n, density):
     """Values planted where the threshold sample reads push the candidate
     threshold above the k-th value: exactly a sampled values are 3.0 (so the
     hint is 3.0 and only a < k entries qualify), the other sampled values 1.0
     (ties), some unsampled ones 0.5, the rest tiny.  The select must fall
-    back to the whole segment and still be exact.  (The sample layout mirrors
-    the kernel's plan: R = max(2.5 k, 512), m = min(48 n / R, 16384) rounded
-    down to 64, blocks of 64 at stride n / (m / 64), a = round(R m / n).)"""
-    n, density = 40000, 0.003
+    back to the whole segment and still be exact, also for a tensor of
+    ResNet-50's largest size (2,359,296 values, the emission sweeping it from
+    global memory).  (The sample layout mirrors the kernel's plan: R = max(2.5
+    k, 512), m = min(48 n / R, 16384) rounded down to 64, blocks of 64 at
+    stride n / (m / 64), a = round(R m / n).)"""
     k = oracle.dgc_k(density, n)
     R = max(5 * k // 2, 512)
     m = min(48 * n // R, 16384) & ~63
