@@ -812,27 +812,31 @@ __global__ void __launch_bounds__(NTS) ada_scan(const SegPlan* __restrict__ plan
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint64_t t0 = (uint64_t)k * tiles_per_learner + p.tile_off;
     // output slots of the emit groups (kGroup consecutive tiles; ada_emit
-    // ranks the tiles inside a group), two groups per thread per round
+    // ranks the tiles inside a group): chunks of kGroup * NTS tiles whose
+    // counts are read coalesced into shared memory (thread t, tiles t + r NTS),
+    // then one group per thread and one block scan per chunk
+    static_assert(kGroup == 8, "a group is two 16-byte reads of the staged counts");
+    __shared__ __align__(16) uint32_t s_cnt[kGroup * NTS];
     uint64_t run = 0;
     const uint32_t ng = (p.ntiles + kGroup - 1) / kGroup;
     uint32_t* gr = grp_rel + (uint64_t)k * groups_per_learner + p.grp_off;
-    for (uint32_t gb = 0; gb < ng; gb += 2 * NTS) {
-        const uint32_t g0 = gb + 2 * threadIdx.x;
-        uint32_t c[2];
+    for (uint32_t tb = 0; tb < p.ntiles; tb += kGroup * NTS) {
+        uint32_t cv[kGroup];
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            c[q] = 0;
-            if (g0 + q < ng) {
-                const uint32_t j0 = (g0 + q) * kGroup;
-#pragma unroll
-                for (uint32_t j = 0; j < kGroup; ++j)  // the group's counts, all loads in flight
-                    c[q] += j0 + j < p.ntiles ? tile_tab[t0 + j0 + j].y : 0u;
-            }
+        for (int r = 0; r < (int)kGroup; ++r) {  // every load of the chunk in flight
+            const uint32_t j = tb + (uint32_t)r * NTS + threadIdx.x;
+            cv[r] = j < p.ntiles ? tile_tab[t0 + j].y : 0u;
         }
+#pragma unroll
+        for (int r = 0; r < (int)kGroup; ++r) s_cnt[r * NTS + threadIdx.x] = cv[r];
+        __syncthreads();
+        const uint4 a = reinterpret_cast<const uint4*>(s_cnt)[2 * threadIdx.x];
+        const uint4 b = reinterpret_cast<const uint4*>(s_cnt)[2 * threadIdx.x + 1];
+        const uint32_t c = a.x + a.y + a.z + a.w + b.x + b.y + b.z + b.w;  // group tb / kGroup + t
         uint64_t tot;
-        const uint64_t at = run + block_exclusive_scan<NTS>(c[0] + c[1], scan, &tot);
-        if (g0 < ng) gr[g0] = (uint32_t)at;
-        if (g0 + 1 < ng) gr[g0 + 1] = (uint32_t)(at + c[0]);
+        const uint64_t at = run + block_exclusive_scan<NTS>(c, scan, &tot);  // ends synchronised: s_cnt is free
+        const uint32_t g = tb / kGroup + threadIdx.x;
+        if (g < ng) gr[g] = (uint32_t)at;
         run += tot;
     }
     // Bins kept in the bins array (big bins, warp chunks): a double-float
