@@ -118,6 +118,44 @@ def test_ws_staged_regions(cuda_lib, K, n, density):
     run_ws(cuda_lib, idx, val, counts, n)
 
 
+def shared_lists(rng, K, n, cap, density, shared):
+    """K lists of density * n sorted indices (the same indices in every list
+    when `shared`), normal values with -0.0 among them."""
+    c = int(density * n)
+    idx = np.zeros((K, cap), np.uint32)
+    val = np.zeros((K, cap), np.float32)
+    common = np.sort(rng.choice(n, size=c, replace=False))
+    for k in range(K):
+        idx[k, :c] = common if shared else np.sort(rng.choice(n, size=c, replace=False))
+        v = rng.standard_normal(c).astype(np.float32)
+        v[rng.choice(c, size=max(1, c // 50), replace=False)] = -0.0
+        val[k, :c] = v
+    return idx, val, np.full(K, c, np.int64)
+
+
+@pytest.mark.parametrize("K,density,shared", [(8, 0.05, False), (8, 0.09, False), (8, 0.04, True), (3, 0.1, True),
+                                              (1, 0.1, False), (7, 0.06, False), (2, 0.08, True)])
+def test_ws_shared_indices(cuda_lib, K, density, shared):
+    """Up to 8 lists whose ranges in a region fit the consumers' read-ahead
+    (at most 512 staged entries per list), some carrying the same outputs:
+    the learner-order sum bit for bit.  `shared`: every list carries the
+    same indices, so each carried output is a sum of K values; -0.0 values
+    check that the first add is 0 + value."""
+    rng = np.random.default_rng(K * 31 + int(density * 1000) + shared)
+    n = 12 * 4096 + 1234
+    idx, val, counts = shared_lists(rng, K, n, n // 2, density, shared)  # K * cap >= n / 4: the region kernel
+    run_ws(cuda_lib, idx, val, counts, n)
+
+
+@pytest.mark.parametrize("K,shared", [(8, True), (8, False), (5, True)])
+def test_update_ws_shared_indices(cuda_lib, K, shared):
+    """The update mode on the same kind of lists."""
+    rng = np.random.default_rng(K + 7 * shared)
+    n = 9 * 4096 + 77
+    idx, val, counts = shared_lists(rng, K, n, n // 2, 0.05, shared)
+    run_update_ws(cuda_lib, idx, val, counts, n, 0.03, seed=K)
+
+
 def test_ws_empty_regions_and_ragged_tail(cuda_lib):
     """Entries only near the ends of a long output (capacities large enough
     for the region kernel): most regions have none, a checkpoint owns a long
