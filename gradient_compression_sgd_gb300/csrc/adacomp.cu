@@ -348,9 +348,10 @@ __device__ __forceinline__ void select_tile(const float4 (&Gv)[4], const float4 
 // computed, and they hold no registers).  Two stages at six CTAs of four
 // warps per SM (24 warps) measured faster than three stages at four CTAs:
 // the pass is bound by its instruction latencies more than by the bytes in
-// flight.  When a warp issues a chunk's copies, lane 0 also asks L2 for the
-// warp's next chunk (a bulk prefetch), which puts more bytes in flight than
-// the ring holds; asking for the chunk after that instead measured slower.
+// flight.  When a warp issues a chunk's copies, lanes 0 and 1 also ask L2
+// for the warp's next chunk of dW and R (bulk prefetches; every lane forms
+// the address, no branch), which puts more bytes in flight than the ring
+// holds; asking for the chunk after that instead measured slower.
 // A lane copies and later reads the
 // same 16-byte pieces, so only its own cp.async groups are waited on.  Past a
 // chunk's end the copies zero-fill: G = 0 never raises a maximum and is never
@@ -499,15 +500,12 @@ __global__ void __launch_bounds__(NTW, 6) ada_bins_warp(const SegPlan* __restric
             while (!done && !p.bpw) step();
             // the warp's next chunk into L2 now (its copies are issued a round
             // later): more bytes in flight than the shared-memory ring holds
-            if (!done && lane == 0) {
+            {
                 const uint32_t s2 = (lt - p.tile_off) * p.tile_len;
                 const uint32_t c2 = p.n - s2 < p.tile_len ? p.n - s2 : p.tile_len;
-                const uint64_t b2 = (uint64_t)k * N + p.off + s2;
+                const float* src = (lane ? (const float*)R : dW) + ((uint64_t)k * N + p.off + s2);
                 const uint32_t by = (c2 * 4u) & ~15u;  // whole 16-byte pieces inside the chunk
-                if (by && ((((uintptr_t)(dW + b2)) | ((uintptr_t)(R + b2))) & 15) == 0) {
-                    l2_prefetch(dW + b2, by);
-                    l2_prefetch(R + b2, by);
-                }
+                if (!done && lane < 2 && by && ((uintptr_t)src & 15) == 0) l2_prefetch(src, by);  // lane 0: dW, 1: R
             }
         }
         if (lane == 0) meta[st] = m;  // clen = 0: no chunk (every later stage is empty too)
