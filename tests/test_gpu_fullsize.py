@@ -1,12 +1,18 @@
 """Full-size workloads, in the launch configuration the benchmark times.
 
-At these sizes the oracle runs on one learner (learners share nothing, so
-learner 0 of a K-learner call must equal the oracle run on learner 0 alone),
-on sampled windows (DCD), and properties that hold at any size are checked
-for every learner: exact counts, ascending in-segment indices, every sent
-magnitude at least every unsent one in its segment (ties to the lower
-index), and the masked state.
+Every learner is compared with the oracle element by element: learners
+share nothing, so learner k of a K-learner call must equal the oracle run
+on learner k alone, and the K oracle runs go to a thread pool (the oracle's
+C calls release the GIL).  DCD columns are independent, so the ring is
+checked over every column in windows.  Properties that hold at any size
+are checked beside the oracle: exact counts, ascending in-segment indices,
+every sent magnitude at least every unsent one in its segment (ties to the
+lower index), and the masked state (DGC); the selection rule on sampled
+bins (AdaComp).
 """
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import pytest
 
@@ -15,6 +21,12 @@ from conftest import rel_err
 from gradient_compression_sgd_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
+
+
+def oracle_map(fn, items):
+    """fn over items in threads (the oracle's C calls run in parallel)."""
+    with ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1))) as ex:
+        return list(ex.map(fn, items))
 
 
 def check_topk_properties(gc, off, idx, val, counts, v_before_mask, v_after, u_after, density):
@@ -45,8 +57,9 @@ def check_topk_properties(gc, off, idx, val, counts, v_before_mask, v_after, u_a
 def test_dgc_full_size(cuda_lib, config):
     """ResNet-50 (25,557,032 values, 161 tensors, K = 4) and the GRU layout
     (98,378,240 values, K = 8) at density 0.001, momentum 0.9: two steps;
-    learner 0 against the oracle, every learner against the properties; then
-    the sparse average of the K messages against the oracle."""
+    every learner's message, u and v against the oracle, learners 0 and K-1
+    also against the properties; then the sparse average of the K messages
+    against the oracle."""
     import torch
     gc = cuda_lib
     w = wl.workload(config)
@@ -54,8 +67,8 @@ def test_dgc_full_size(cuda_lib, config):
     d = gc.DGC(off, K, w.density, w.momentum)
     u = torch.zeros((K, N), device="cuda")
     v = torch.zeros((K, N), device="cuda")
-    u0 = np.zeros((1, N), np.float32)
-    v0 = np.zeros((1, N), np.float32)
+    u_o = np.zeros((K, N), np.float32)  # the oracle's state, learner by learner
+    v_o = np.zeros((K, N), np.float32)
     for t in range(2):
         G = wl.gradients(w, t, device="cuda")
         u_prev, v_prev = u.clone(), v.clone()
@@ -63,21 +76,28 @@ def test_dgc_full_size(cuda_lib, config):
         torch.cuda.synchronize()
         st = d.stats()
         assert st["hint_failed"] == 0 and st["raw_global"] == 0, st  # the fast paths served every segment
-        # learner 0 against the oracle
-        idx_o, val_o, counts_o, _ = oracle.dgc_step(off, G[0:1].cpu().numpy(), u0, v0, w.density, w.momentum,
-                                                    cap=d.cap)
+        Gh = G.cpu().numpy()
         idx_g = gc.pair_indices(out).cpu().numpy()
         val_g = gc.pair_values(out).cpu().numpy()
-        n0 = int(counts_o[0].sum())
-        np.testing.assert_array_equal(idx_g[0, :n0], idx_o[0, :n0].astype(np.int64))
-        assert rel_err(val_g[0, :n0], val_o[0, :n0]) <= 1e-6
-        assert rel_err(u[0].cpu().numpy(), u0[0]) <= 1e-6
-        assert rel_err(v[0].cpu().numpy(), v0[0]) <= 1e-6
-        # every learner: properties; the pre-mask velocity is v_after plus the sent values
         counts = d.counts.cpu().numpy()
-        for k in range(K):
-            va = v[k].cpu().numpy()
-            ua = u[k].cpu().numpy()
+        ug, vg = u.cpu().numpy(), v.cpu().numpy()
+
+        def learner(k):
+            idx_o, val_o, counts_o, _ = oracle.dgc_step(off, Gh[k:k + 1], u_o[k:k + 1], v_o[k:k + 1], w.density,
+                                                        w.momentum, cap=d.cap)
+            return idx_o[0], val_o[0], counts_o[0]
+
+        for k, (idx_o, val_o, counts_o) in enumerate(oracle_map(learner, range(K))):
+            n_k = int(counts_o.sum())
+            np.testing.assert_array_equal(counts[k], counts_o, err_msg=f"t={t} k={k}")
+            np.testing.assert_array_equal(idx_g[k, :n_k], idx_o[:n_k].astype(np.int64), err_msg=f"t={t} k={k}")
+            assert rel_err(val_g[k, :n_k], val_o[:n_k]) <= 1e-6, (t, k)
+            assert rel_err(ug[k], u_o[k]) <= 1e-6, (t, k)
+            assert rel_err(vg[k], v_o[k]) <= 1e-6, (t, k)
+        # learners 0 and K-1: properties; the pre-mask velocity is v_after plus the sent values
+        for k in sorted({0, K - 1}):
+            va = vg[k]
+            ua = ug[k]
             n = int(counts[k].sum())
             vb = va.copy()
             vb[idx_g[k, :n]] = val_g[k, :n]
@@ -88,7 +108,7 @@ def test_dgc_full_size(cuda_lib, config):
             sample = sample[va[sample] != 0]
             up = u_prev[k].cpu().numpy()[sample]
             vp = v_prev[k].cpu().numpy()[sample]
-            g = G[k].cpu().numpy()[sample]
+            g = Gh[k][sample]
             un = np.float32(w.momentum) * up + g
             np.testing.assert_array_equal(ua[sample], un)
             np.testing.assert_array_equal(va[sample], vp + un)
@@ -137,8 +157,9 @@ def check_adacomp_bins(gc, a, off, lt, dW, R_prev, R, out, totals, seed, bins_pe
 
 def test_adacomp_full_size(cuda_lib):
     """LSTM (66,034,000 values, L_T = 500) + VGG-16 convs (14,714,688, L_T = 50),
-    K = 8, two steps; learner 0 against the oracle; selection rule checked for
-    every learner on sampled bins."""
+    K = 8, two steps; every learner's message, scales and residue against the
+    oracle (the residue relative to max(|G|, |R|), G = R_prev + dW in fp32);
+    the selection rule checked for every learner on sampled bins."""
     import torch
     gc = cuda_lib
     w = wl.workload(3)
@@ -146,21 +167,34 @@ def test_adacomp_full_size(cuda_lib):
     cap = N // 8
     a = gc.AdaComp(off, w.lt, K, cap)
     R = torch.zeros((K, N), device="cuda")
-    R0 = np.zeros((1, N), np.float32)
+    R_o = np.zeros((K, N), np.float32)  # the oracle's residue, learner by learner
     for t in range(2):
         dW = wl.gradients(w, t, device="cuda")
         R_prev = R.clone()
         out, totals = a(dW, R)
         torch.cuda.synchronize()
         check_adacomp_bins(gc, a, off, w.lt, dW, R_prev, R, out, totals, seed=t)
-        idx_o, val_o, counts_o, scales_o, totals_o = oracle.adacomp_step(off, w.lt, dW[0:1].cpu().numpy(), R0,
-                                                                         cap=cap)
-        np.testing.assert_array_equal(a.counts[0].cpu().numpy(), counts_o[0])
-        assert rel_err(a.scales[0].cpu().numpy(), scales_o[0]) <= 1e-6
-        n0 = int(totals_o[0])
-        np.testing.assert_array_equal(gc.pair_indices(out)[0, :n0].cpu().numpy(), idx_o[0, :n0].astype(np.int64))
-        assert rel_err(gc.pair_values(out)[0, :n0].cpu().numpy(), val_o[0, :n0]) <= 1e-6
         assert np.all(totals.cpu().numpy() <= cap)
+        dWh = dW.cpu().numpy()
+        Rp = R_prev.cpu().numpy()
+        Rg = R.cpu().numpy()
+        counts_g, scales_g = a.counts.cpu().numpy(), a.scales.cpu().numpy()
+        idx_g = gc.pair_indices(out).cpu().numpy()
+        val_g = gc.pair_values(out).cpu().numpy()
+
+        def learner(k):
+            idx_o, val_o, counts_o, scales_o, totals_o = oracle.adacomp_step(off, w.lt, dWh[k:k + 1],
+                                                                             R_o[k:k + 1], cap=cap)
+            return idx_o[0], val_o[0], counts_o[0], scales_o[0], int(totals_o[0])
+
+        for k, (idx_o, val_o, counts_o, scales_o, n_k) in enumerate(oracle_map(learner, range(K))):
+            np.testing.assert_array_equal(counts_g[k], counts_o, err_msg=f"t={t} k={k}")
+            assert rel_err(scales_g[k], scales_o) <= 1e-6, (t, k)
+            np.testing.assert_array_equal(idx_g[k, :n_k], idx_o[:n_k].astype(np.int64), err_msg=f"t={t} k={k}")
+            assert rel_err(val_g[k, :n_k], val_o[:n_k]) <= 1e-6, (t, k)
+            G = Rp[k] + dWh[k]
+            denom = np.maximum(np.maximum(np.abs(G), np.abs(R_o[k])), np.finfo(np.float32).tiny)
+            assert float((np.abs(Rg[k].astype(np.float64) - R_o[k]) / denom).max(initial=0.0)) <= 1e-6, (t, k)
     avg = torch.empty(N, device="cuda")
     gc.sparse_average(out, totals, N, avg)
     torch.cuda.synchronize()
@@ -170,22 +204,29 @@ def test_adacomp_full_size(cuda_lib):
 
 
 def test_dcd_full_size(cuda_lib):
-    """Ring of 8 nodes, 25.6M values each, 3 iterations; four 4096-column
-    windows (including the last) against the oracle's windowed step."""
+    """Ring of 8 nodes, 25.6M values each, 3 iterations; every column against
+    the oracle's step, run on 64 column windows (columns are independent;
+    the keep draws take the absolute column, so the windows' boundaries do
+    not matter), bit for bit after every iteration."""
     import torch
     gc = cuda_lib
     w = wl.workload(5)
     n, D = w.learners, w.n
     x = wl.dcd_initial_model(w, device="cuda")
     seed = wl.dcd_seed(w)
-    windows = [(0, 4096), (12_345_678, 12_349_774), (D - 4096, D), (777, 4873)]
-    x_win = [x[:, a:b].cpu().numpy().copy() for a, b in windows]
+    cuts = [D * j // 64 for j in range(65)]
+    windows = list(zip(cuts[:-1], cuts[1:]))
+    xh = x.cpu().numpy()
+    x_win = [np.ascontiguousarray(xh[:, a:b]) for a, b in windows]
+    del xh
     for t in range(3):
         g = torch.stack([wl.gradient(w, i, t, device="cuda") for i in range(n)])
         gc.dcd_step(x, g, w.ring_w, w.gamma, w.keep_p, seed, t)
+        gh = g.cpu().numpy()
+        oracle_map(lambda j: oracle.dcd_step_window(x_win[j], np.ascontiguousarray(gh[:, windows[j][0]:windows[j][1]]),
+                                                    w.ring_w, w.gamma, w.keep_p, seed, t, windows[j][0]),
+                   range(len(windows)))
+        torch.cuda.synchronize()
+        xg = x.cpu().numpy()
         for j, (a, b) in enumerate(windows):
-            oracle.dcd_step_window(x_win[j], np.ascontiguousarray(g[:, a:b].cpu().numpy()), w.ring_w, w.gamma,
-                                   w.keep_p, seed, t, a)
-    torch.cuda.synchronize()
-    for j, (a, b) in enumerate(windows):
-        np.testing.assert_array_equal(x[:, a:b].cpu().numpy(), x_win[j])
+            np.testing.assert_array_equal(xg[:, a:b], x_win[j], err_msg=f"t={t} columns [{a}, {b})")
