@@ -547,12 +547,51 @@ def measure_other(gc, config, args, world, local, dev, stream) -> dict:
                         "algorithmic_bytes_per_launch": dom_bytes, "traffic": traffic,
                         "traffic_over_algorithmic": (traffic / dom_bytes) if traffic else None},
            "clocks": clk}
+    if w.method == "dcd":  # the extrapolation variant on the same ring, for the record
+        out["ecd_variant"] = measure_ecd(gc, w, grads, warm, steps, world, dev, stream)
     del path, grads, flush_buf
     torch.cuda.empty_cache()
     return out
 
 
 PATHS = {"dgc": DgcPath, "adacomp": AdaCompPath, "dcd": DcdPath}
+
+
+def measure_ecd(gc, w, grads, warm, steps, world, dev, stream) -> dict:
+    """The ECD-PSGD iteration on the DCD workload's ring (extrapolated
+    estimates, equations (3)-(4)): 24 algorithmic bytes per node-element
+    (read x_t, x_{t-1}, the estimate and g; write x_{t+1} and the estimate),
+    timed over `steps` iterations after `warm`, with its kernel's events."""
+    import torch
+
+    from gradient_compression_sgd_gb300 import workloads as wl
+    K, N = w.learners, w.n
+    x_a = wl.dcd_initial_model(w, device=dev)
+    x_b, x_t = x_a.clone(), x_a.clone()
+    seed = wl.dcd_seed(w)
+    for i in range(warm):
+        gc.ecd_step(x_a, x_b, x_t, grads[i % N_SETS], w.ring_w, w.gamma, w.keep_p, seed, i + 1)
+        x_a, x_b = x_b, x_a
+    torch.cuda.synchronize()
+    gc.trace_enable(True)
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    for i in range(steps):
+        gc.ecd_step(x_a, x_b, x_t, grads[i % N_SETS], w.ring_w, w.gamma, w.keep_p, seed, warm + i + 1)
+        x_a, x_b = x_b, x_a
+    c1.record(stream)
+    torch.cuda.synchronize()
+    gc.trace_enable(False)
+    tr_e = gc.trace_read()
+    ms_e = max_over_ranks(c0.elapsed_time(c1) / steps, dev)
+    ne, te = tr_e.get("ecd_step", (0, 0.0))
+    kms = te / max(ne, 1)
+    hbm_e, _ = peaks()
+    ach = 24.0 * K * N / (kms * 1e-3) / 1e9 if kms > 0 else None
+    del x_a, x_b, x_t
+    return {"step": "ecd_step (ring of the same nodes)", "value": job_gbs(world, 4.0 * K * N, ms_e), "unit": "GB/s",
+            "ms_per_step": ms_e, "kernel_achieved_gbs": ach, "frac_of_measured_copy": (ach / hbm_e) if ach else None}
 
 
 def run_gpu(args):
@@ -755,37 +794,7 @@ def run_gpu(args):
         nesterov = {"step": "dgc_compress_nesterov + sparse_average", "value": job_gbs(world, 4.0 * K * N, ms_n),
                     "unit": "GB/s", "ms_per_step": ms_n}
 
-    # the ECD-PSGD iteration on the same ring (extrapolated estimates,
-    # equations (3)-(4)): 24 algorithmic bytes per node-element (read x_t,
-    # x_{t-1}, the estimate and g; write x_{t+1} and the estimate)
-    ecd = None
-    if w.method == "dcd":
-        from gradient_compression_sgd_gb300 import workloads as wl2
-        x_a = wl2.dcd_initial_model(w, device=dev)
-        x_b, x_t = x_a.clone(), x_a.clone()
-        seed = wl2.dcd_seed(w)
-        for i in range(args.warmup):
-            gc.ecd_step(x_a, x_b, x_t, grads[i % N_SETS], w.ring_w, w.gamma, w.keep_p, seed, i + 1)
-            x_a, x_b = x_b, x_a
-        torch.cuda.synchronize()
-        gc.trace_enable(True)
-        c0 = torch.cuda.Event(enable_timing=True)
-        c1 = torch.cuda.Event(enable_timing=True)
-        c0.record(stream)
-        for i in range(args.steps):
-            gc.ecd_step(x_a, x_b, x_t, grads[i % N_SETS], w.ring_w, w.gamma, w.keep_p, seed, args.warmup + i + 1)
-            x_a, x_b = x_b, x_a
-        c1.record(stream)
-        torch.cuda.synchronize()
-        gc.trace_enable(False)
-        tr_e = gc.trace_read()
-        ms_e = max_over_ranks(c0.elapsed_time(c1) / args.steps, dev)
-        ne, te = tr_e.get("ecd_step", (0, 0.0))
-        kms = te / max(ne, 1)
-        hbm_e, _ = peaks()
-        ach = 24.0 * K * N / (kms * 1e-3) / 1e9 if kms > 0 else None
-        ecd = {"step": "ecd_step (ring of the same nodes)", "value": job_gbs(world, 4.0 * K * N, ms_e), "unit": "GB/s",
-               "ms_per_step": ms_e, "kernel_achieved_gbs": ach, "frac_of_measured_copy": (ach / hbm_e) if ach else None}
+    ecd = measure_ecd(gc, w, grads, args.warmup, args.steps, world, dev, stream) if w.method == "dcd" else None
 
     # end to end through the public API: every step copies its gradients in
     # from pinned host memory and its dense result out to pinned host memory.
