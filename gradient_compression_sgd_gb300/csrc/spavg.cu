@@ -783,6 +783,7 @@ constexpr int kProducer = kCW;
 constexpr int NTR = (kCW + 1) * 32;         // threads per CTA: consumers and one producer warp
 constexpr int kNBuf = 2;                    // stage buffers
 constexpr int kPer = 2;                     // entries per consumer thread and list read ahead
+constexpr int kRegK = 8;                    // lists whose staged ranges the consumers keep in registers
 constexpr uint32_t kFullArrivals = 33;      // producer lane 0's expect-tx arrive + 32 cp.async arrives
 
 __device__ __forceinline__ void mbar_init_n(uint64_t* bar, uint32_t count) {
@@ -982,7 +983,11 @@ __global__ void __launch_bounds__(NTR, 2) spavg_region(const gcsgd_pair* __restr
     // the consumers between lists; a list's indices are distinct, so its adds
     // never collide; entries outside the region are skipped), then the
     // consumers release the buffer and store the region.  The first two
-    // entries per thread of list k+1 are read while list k is added.
+    // entries per thread of list k+1 are read while list k is added.  A list
+    // step is a dependent chain (accumulator read, add, write, barrier), so
+    // for K <= 8 the ranges sit in registers and the next list's entries are
+    // read after this list's accumulator reads are issued: nothing of the
+    // read-ahead waits in front of the chain.
     const int ct = threadIdx.x;
     constexpr int NC = kCW * 32;
     const float fk = (float)K, inv_k = 1.0f / fk;
@@ -1016,7 +1021,62 @@ __global__ void __launch_bounds__(NTR, 2) spavg_region(const gcsgd_pair* __restr
                 }
             }
         }
-        if (s_total[b] != kSlow) {
+        if (s_total[b] != kSlow && K <= kRegK) {
+            // every list's staged range (length, first slot) in registers
+            const gcsgd_pair* buf = stage + (size_t)b * kRStage;
+            const uint32_t* st = ST(b);
+            uint32_t rl[kRegK], rs[kRegK];
+#pragma unroll
+            for (int k = 0; k < kRegK; ++k) {
+                rl[k] = k < K ? pl[k] : 0u;
+                rs[k] = k < K ? st[k] : 0u;
+            }
+            const gcsgd_pair none = {0xffffffffu, 0.0f};
+            gcsgd_pair nx[kPer];
+            auto read_ahead = [&](int k) {  // this thread's first kPer entries of list k
+#pragma unroll
+                for (int r = 0; r < kPer; ++r)
+                    nx[r] = (uint32_t)(ct + r * NC) < rl[k] ? buf[rs[k] + ct + r * NC] : none;
+            };
+            read_ahead(0);
+#pragma unroll
+            for (int k = 0; k < kRegK; ++k) {
+                if (k >= K) break;
+                const uint32_t len = rl[k];
+                gcsgd_pair e[kPer];
+#pragma unroll
+                for (int r = 0; r < kPer; ++r) e[r] = nx[r];
+                if (len != 0) {  // uniform: an empty range needs no barrier
+                    uint32_t d[kPer];
+                    bool in[kPer];
+                    float a[kPer];
+#pragma unroll
+                    for (int r = 0; r < kPer; ++r) {
+                        d[r] = e[r].idx - R0;
+                        in[r] = (uint32_t)(ct + r * NC) < len && d[r] < rlen;
+                        a[r] = in[r] ? acc[d[r]] : 0.0f;
+                    }
+                    if (k + 1 < kRegK && k + 1 < K) read_ahead(k + 1);  // after this list's reads
+#pragma unroll
+                    for (int r = 0; r < kPer; ++r)
+                        if (in[r]) {
+                            acc[d[r]] = __fadd_rn(a[r], e[r].val);
+                            if (UPDATE) atomicOr(&tb[d[r] >> 5], 1u << (d[r] & 31));
+                        }
+                    for (uint32_t q = ct + kPer * NC; q < len; q += NC) {  // longer ranges
+                        const gcsgd_pair ee = buf[rs[k] + q];
+                        const uint32_t dd = ee.idx - R0;
+                        if (dd < rlen) {
+                            acc[dd] = __fadd_rn(acc[dd], ee.val);
+                            if (UPDATE) atomicOr(&tb[dd >> 5], 1u << (dd & 31));
+                        }
+                    }
+                    consumer_sync();  // list k's adds land before list k+1's
+                } else if (k + 1 < kRegK && k + 1 < K) {
+                    read_ahead(k + 1);
+                }
+            }
+        } else if (s_total[b] != kSlow) {
             const gcsgd_pair* buf = stage + (size_t)b * kRStage;
             const uint32_t* st = ST(b);
             const gcsgd_pair none = {0xffffffffu, 0.0f};
